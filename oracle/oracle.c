@@ -1,0 +1,307 @@
+/*
+ * oracle.c -- plain, slow, obviously-correct CPU oracle of the CSA2 attention step.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Only the tests, the smoke check and the benchmark's
+ * CPU-baseline leg may load this library.  It shares no code with the CUDA path.
+ *
+ * Arithmetic is IEEE double throughout; bf16 inputs are widened exactly, and the
+ * only rounding to bf16 is the compressor's final store (one rounding, ties to
+ * even).  Each function names the passage of the source pages it restates.
+ * Pages:
+ *   [A] "DeepSeek-V4.1-Flash 架构解剖" (perryzhang01.github.io, v41_flash_anatomy)
+ *   [B] "DeepSeek-V4.1-Flash 结构说明" (treert.github.io, ds-v4-1-flash-structure)
+ *   [C] "万字长文解析DeekSeekV4.1flash" (yuyanqi.com)
+ *   [E] "DeepSeek-V4-Pro 架构解剖" (perryzhang01.github.io, v4_pro_anatomy)
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define D_LAT 512
+#define D_IDX 128
+#define N_HEADS 64
+#define ROPE_DIM0 448
+#define RING 128
+
+/* ---- number formats ----------------------------------------------------------- */
+
+static double bf16_val(uint16_t b) {
+  uint32_t u = (uint32_t)b << 16;
+  float f;
+  memcpy(&f, &u, 4);
+  return (double)f;
+}
+
+/* Round a double to the nearest bf16, ties to even, in one rounding. */
+uint16_t orc_f64_to_bf16(double x) {
+  if (isnan(x)) return 0x7FC0;
+  uint16_t sign = signbit(x) ? 0x8000 : 0;
+  double a = fabs(x);
+  if (a == 0.0) return sign;
+  if (isinf(a)) return sign | 0x7F80;
+  int e;
+  double m = frexp(a, &e); /* a = m * 2^e, 0.5 <= m < 1 */
+  if (e - 1 < -126) {      /* subnormal: quantum 2^-133 */
+    double qv = nearbyint(ldexp(a, 133));
+    return sign | (uint16_t)qv; /* 128 is the smallest normal, encoded 0x0080 */
+  }
+  double s = nearbyint(ldexp(m, 8)); /* 8 significant bits: 128..256 */
+  if (s == 256.0) { s = 128.0; e += 1; }
+  int E = e - 1;
+  if (E > 127) return sign | 0x7F80;
+  return sign | (uint16_t)(((E + 127) << 7) | ((int)s - 128));
+}
+
+/* OCP FP8 E4M3 decode from the format's definition: bias 7, 3 mantissa bits,
+ * exponent field 0 is subnormal (m/8 * 2^-6), S.1111.111 is NaN. */
+double orc_e4m3_val(uint8_t c) {
+  int sgn = c >> 7, ex = (c >> 3) & 15, mn = c & 7;
+  double v;
+  if (ex == 15 && mn == 7) return NAN;
+  if (ex == 0) v = ldexp((double)mn / 8.0, -6);
+  else v = ldexp(1.0 + (double)mn / 8.0, ex - 7);
+  return sgn ? -v : v;
+}
+
+/* ---- visibility [A] "visible 是每行自己的前缀长度"; [B] §4.1 -------------------- */
+
+/* Compressed row j covers positions j*m .. j*m+m-1 and becomes visible to the
+ * query at position p once p has passed its last token.  Written as the count
+ * of such rows, by enumeration. */
+int64_t orc_n_visible(int64_t p, int m) {
+  int64_t n = 0;
+  while ((n + 1) * m - 1 <= p) n++;
+  return n;
+}
+
+/* ---- compressor [A] "特殊模块 · compressor", "CSA2 的池化比 V4 简单一截";
+ *      [C] §6.2, §6.4, A.15.1; [B] §4.1 (tail), §6.1-6.2 (RoPE) ---------------------
+ *
+ * Every new token at position t is appended to the tail slot t % m.  When the slot
+ * is the last of its group (t % m == m-1) the group j = t / m is complete:
+ *   r[d]  = sum_i softmax_i(score[i][d]) * kv[i][d]     (softmax over the m slots)
+ *   y     = r / sqrt(mean(r^2) + eps) * norm_w          (RMSNorm over all 512 dims)
+ *   y[448+2i], y[449+2i] rotated by angle (j*m) * inv_freq[i], i < 32
+ * and y is stored to plane row row_base[b] + j as bf16.
+ * State arrays are [B][m][512]; slot s holds the last token with t % m == s.
+ * Returns the number of rows emitted in total. */
+int64_t orc_compress(const uint16_t* kv, const uint16_t* score, const int32_t* cu_seqlens, int B,
+                     const int64_t* start_pos, int m, double* kv_state, double* score_state,
+                     uint16_t* plane, double* plane_f64, const int64_t* row_base,
+                     const float* norm_w, double eps, const float* inv_freq) {
+  int64_t emitted = 0;
+  for (int b = 0; b < B; b++) {
+    double* ks = kv_state + (int64_t)b * m * D_LAT;
+    double* ss = score_state + (int64_t)b * m * D_LAT;
+    for (int64_t t = cu_seqlens[b]; t < cu_seqlens[b + 1]; t++) {
+      int64_t pos = start_pos[b] + (t - cu_seqlens[b]);
+      int slot = (int)(pos % m);
+      for (int d = 0; d < D_LAT; d++) {
+        ks[slot * D_LAT + d] = bf16_val(kv[t * D_LAT + d]);
+        ss[slot * D_LAT + d] = score ? bf16_val(score[t * D_LAT + d]) : 0.0;
+      }
+      if (slot != m - 1) continue;
+      int64_t j = pos / m;
+      double y[D_LAT];
+      for (int d = 0; d < D_LAT; d++) {
+        double mx = -INFINITY;
+        for (int i = 0; i < m; i++) mx = fmax(mx, ss[i * D_LAT + d]);
+        double z = 0.0, acc = 0.0;
+        for (int i = 0; i < m; i++) {
+          double e = exp(ss[i * D_LAT + d] - mx);
+          z += e;
+          acc += e * ks[i * D_LAT + d];
+        }
+        y[d] = acc / z;
+      }
+      double ms = 0.0;
+      for (int d = 0; d < D_LAT; d++) ms += y[d] * y[d];
+      double inv = 1.0 / sqrt(ms / D_LAT + eps);
+      for (int d = 0; d < D_LAT; d++) y[d] = y[d] * inv * (norm_w ? (double)norm_w[d] : 1.0);
+      double p0 = (double)(j * m); /* group-head position */
+      for (int i = 0; i < 32; i++) {
+        double ang = p0 * (double)inv_freq[i];
+        double c = cos(ang), s = sin(ang);
+        double a0 = y[ROPE_DIM0 + 2 * i], a1 = y[ROPE_DIM0 + 2 * i + 1];
+        y[ROPE_DIM0 + 2 * i] = a0 * c - a1 * s;
+        y[ROPE_DIM0 + 2 * i + 1] = a0 * s + a1 * c;
+      }
+      int64_t row = row_base[b] + j;
+      for (int d = 0; d < D_LAT; d++) {
+        plane[row * D_LAT + d] = orc_f64_to_bf16(y[d]);
+        if (plane_f64) plane_f64[row * D_LAT + d] = y[d];
+      }
+      emitted++;
+    }
+  }
+  return emitted;
+}
+
+/* ---- lightning indexer [A] "特殊模块 · indexer" Fig. 3b (score formula and
+ *      weights_scale); [C] A.15.2 (ReLU per head, gather candidates first);
+ *      [A] Fig. 2c (candidate blocks x 8 rows) -------------------------------------
+ *
+ * score[c] = alpha * sum_h w[h] * act(<iq[h], K[c]>),  alpha = 128^-1/2 * H^-1/2,
+ * act = ReLU when relu != 0, identity otherwise.
+ * FULL (cand == NULL): positions c < n_visible(p) are rows c.
+ * REINDEX: position i*8 + r is row 8*cand[i] + r; it is scored only when
+ * cand[i] >= 0 and that row is visible.
+ * Outputs per query q: scores[q*ld + pos] and rows[q*ld + pos] (-1 = not scored). */
+void orc_index_scores(const uint16_t* iq, const float* w, int Q, int H, const uint16_t* index_k,
+                      const int64_t* row_base, const int32_t* q_seq, const int64_t* q_pos, int m,
+                      const int32_t* cand, int ncb, int relu, double* scores, int64_t* rows,
+                      int64_t ld) {
+  double alpha = 1.0 / sqrt((double)D_IDX) / sqrt((double)H);
+  for (int q = 0; q < Q; q++) {
+    int64_t nvis = orc_n_visible(q_pos[q], m);
+    const uint16_t* kb = index_k + row_base[q_seq[q]] * D_IDX;
+    double qv[64 * D_IDX];
+    for (int i = 0; i < H * D_IDX; i++) qv[i] = bf16_val(iq[(int64_t)q * H * D_IDX + i]);
+    int64_t npos = cand ? (int64_t)ncb * 8 : nvis;
+#pragma omp parallel for schedule(static)
+    for (int64_t pos = 0; pos < ld; pos++) {
+      int64_t row = -1;
+      if (pos < npos) {
+        if (!cand) row = pos;
+        else {
+          int32_t blk = cand[(int64_t)q * ncb + pos / 8];
+          if (blk >= 0 && (int64_t)blk * 8 + pos % 8 < nvis) row = (int64_t)blk * 8 + pos % 8;
+        }
+      }
+      rows[(int64_t)q * ld + pos] = row;
+      if (row < 0) { scores[(int64_t)q * ld + pos] = 0.0; continue; }
+      double kr[D_IDX];
+      for (int d = 0; d < D_IDX; d++) kr[d] = bf16_val(kb[row * D_IDX + d]);
+      double s = 0.0;
+      for (int h = 0; h < H; h++) {
+        double dot = 0.0;
+        for (int d = 0; d < D_IDX; d++) dot += qv[h * D_IDX + d] * kr[d];
+        if (relu && dot < 0.0) dot = 0.0;
+        s += (double)w[(int64_t)q * H + h] * dot;
+      }
+      scores[(int64_t)q * ld + pos] = alpha * s;
+    }
+  }
+}
+
+/* ---- top-k [A] Fig. 3b ("selected [rows, 512] 升序，-1 填充"), "visible 是每行
+ *      自己的前缀长度" (-1 means the history is shorter than 512) ----------------------
+ *
+ * Keep k_eff = min(k, #scored) entries of highest score, ties to the lower row id,
+ * NaN ranked as -inf; emit their row ids in ascending order, -1 padded to k. */
+typedef struct { double s; int64_t row; } orc_pair;
+
+static int cmp_rank(const void* a, const void* b) {
+  const orc_pair* x = (const orc_pair*)a;
+  const orc_pair* y = (const orc_pair*)b;
+  if (x->s > y->s) return -1;
+  if (x->s < y->s) return 1;
+  return (x->row < y->row) ? -1 : (x->row > y->row);
+}
+
+static int cmp_i64(const void* a, const void* b) {
+  int64_t x = *(const int64_t*)a, y = *(const int64_t*)b;
+  return (x < y) ? -1 : (x > y);
+}
+
+int orc_topk(const double* scores, const int64_t* rows, int64_t n, int k, int32_t* sel) {
+  orc_pair* v = (orc_pair*)malloc(sizeof(orc_pair) * (n > 0 ? n : 1));
+  int64_t nv = 0;
+  for (int64_t i = 0; i < n; i++) {
+    if (rows[i] < 0) continue;
+    v[nv].s = isnan(scores[i]) ? -INFINITY : scores[i];
+    v[nv].row = rows[i];
+    nv++;
+  }
+  qsort(v, nv, sizeof(orc_pair), cmp_rank);
+  int64_t keff = nv < k ? nv : k;
+  int64_t* r = (int64_t*)malloc(sizeof(int64_t) * (keff > 0 ? keff : 1));
+  for (int64_t i = 0; i < keff; i++) r[i] = v[i].row;
+  qsort(r, keff, sizeof(int64_t), cmp_i64);
+  for (int i = 0; i < k; i++) sel[i] = (i < keff) ? (int32_t)r[i] : -1;
+  free(v);
+  free(r);
+  return (int)keff;
+}
+
+/* ---- sparse MQA attention with sink [A] "四种层合并出来的是什么形状", Fig. 2a-2d;
+ *      [E] Fig. 2d (out_h formula with exp(sink_h) in the denominator);
+ *      [B] §4.1 (640 positions, no de-duplication), §4.4 step 4 (window slots);
+ *      [C] §5.5 (one softmax over the concatenated entries) ---------------------------
+ *
+ * For query q at position p in sequence b the entry set is the window positions
+ * max(0, p-127) .. p (ring slot pos % 128, or the linear row for pos) followed by
+ * the plane rows sel[q][i] != -1.  One KV vector per entry serves as key and value.
+ *   s_j   = scale * <q_h, x_j>
+ *   out_h = sum_j e^{s_j} x_j / (e^{sink_h} + sum_j e^{s_j})
+ *   lse_h = log(e^{sink_h} + sum_j e^{s_j})
+ * sink == NULL drops the sink term.  swa_mode 0 = ring [B][128][512],
+ * 1 = linear rows lin_base[b] + (pos - lin_pos0[b]).  swa_dtype 0 = bf16,
+ * 1 = 528-byte FP8 rows (512 E4M3 codes then 4 fp32 scales, one per 128 codes). */
+void orc_sparse_attn(const uint16_t* q, int Q, const int32_t* q_seq, const int64_t* q_pos,
+                     int swa_mode, int swa_dtype, const void* swa, const int64_t* lin_base,
+                     const int64_t* lin_pos0, const uint16_t* plane, const int64_t* row_base,
+                     const int32_t* sel, int nsel, const float* sink, double scale, double* out,
+                     double* lse) {
+#pragma omp parallel for schedule(dynamic)
+  for (int qi = 0; qi < Q; qi++) {
+    int b = q_seq[qi];
+    int64_t p = q_pos[qi];
+    int64_t lo = p - (RING - 1) < 0 ? 0 : p - (RING - 1);
+    int nwin = (int)(p - lo + 1);
+    int nent = nwin;
+    for (int i = 0; i < nsel; i++) nent += sel[(int64_t)qi * nsel + i] >= 0;
+    double* x = (double*)malloc(sizeof(double) * (size_t)nent * D_LAT);
+    int e = 0;
+    for (int64_t pos = lo; pos <= p; pos++, e++) {
+      if (swa_dtype == 0) {
+        const uint16_t* src;
+        if (swa_mode == 0) src = (const uint16_t*)swa + ((int64_t)b * RING + pos % RING) * D_LAT;
+        else src = (const uint16_t*)swa + (lin_base[b] + (pos - lin_pos0[b])) * D_LAT;
+        for (int d = 0; d < D_LAT; d++) x[(int64_t)e * D_LAT + d] = bf16_val(src[d]);
+      } else {
+        const uint8_t* src;
+        if (swa_mode == 0) src = (const uint8_t*)swa + ((int64_t)b * RING + pos % RING) * 528;
+        else src = (const uint8_t*)swa + (lin_base[b] + (pos - lin_pos0[b])) * 528;
+        for (int d = 0; d < D_LAT; d++) {
+          float sc;
+          memcpy(&sc, src + 512 + 4 * (d / 128), 4);
+          x[(int64_t)e * D_LAT + d] = orc_e4m3_val(src[d]) * (double)sc;
+        }
+      }
+    }
+    for (int i = 0; i < nsel; i++) {
+      int32_t r = sel[(int64_t)qi * nsel + i];
+      if (r < 0) continue;
+      const uint16_t* src = plane + (row_base[b] + r) * D_LAT;
+      for (int d = 0; d < D_LAT; d++) x[(int64_t)e * D_LAT + d] = bf16_val(src[d]);
+      e++;
+    }
+    double* s = (double*)malloc(sizeof(double) * (size_t)nent);
+    for (int h = 0; h < N_HEADS; h++) {
+      const uint16_t* qh = q + ((int64_t)qi * N_HEADS + h) * D_LAT;
+      double qd[D_LAT];
+      for (int d = 0; d < D_LAT; d++) qd[d] = bf16_val(qh[d]);
+      double mx = sink ? (double)sink[h] : -INFINITY;
+      for (int j = 0; j < nent; j++) {
+        double dot = 0.0;
+        for (int d = 0; d < D_LAT; d++) dot += qd[d] * x[(int64_t)j * D_LAT + d];
+        s[j] = scale * dot;
+        if (s[j] > mx) mx = s[j];
+      }
+      double z = sink ? exp((double)sink[h] - mx) : 0.0;
+      double o[D_LAT];
+      for (int d = 0; d < D_LAT; d++) o[d] = 0.0;
+      for (int j = 0; j < nent; j++) {
+        double pj = exp(s[j] - mx);
+        z += pj;
+        for (int d = 0; d < D_LAT; d++) o[d] += pj * x[(int64_t)j * D_LAT + d];
+      }
+      for (int d = 0; d < D_LAT; d++) out[((int64_t)qi * N_HEADS + h) * D_LAT + d] = o[d] / z;
+      if (lse) lse[(int64_t)qi * N_HEADS + h] = mx + log(z);
+    }
+    free(s);
+    free(x);
+  }
+}

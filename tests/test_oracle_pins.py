@@ -1,0 +1,465 @@
+"""Pins of the CPU oracle against facts that do not come from the oracle itself.
+
+Each pin is an independent route to the same number: a library routine (numpy
+matmul, scipy expit, torch's bf16 / float8 conversions), a closed form, an
+invariant, brute force on tiny inputs, or a count printed on the pages
+(tests/golden).  A plausible slip in the oracle -- a dropped term, a wrong sign,
+a transposed operand, an off-by-one in visibility -- fails at least one of them.
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+from scipy.special import expit
+
+import oracle
+from synth import workloads
+
+GOLD = os.path.join(os.path.dirname(__file__), "golden", "tail_and_visibility.json")
+RNG = np.random.default_rng(1234)
+
+
+def bf16(x):
+    return torch.as_tensor(np.asarray(x, dtype=np.float32)).bfloat16()
+
+
+def bf16_np(t):
+    return t.float().numpy().astype(np.float64)
+
+
+# ---- number formats ---------------------------------------------------------------
+
+def test_bf16_rounding_matches_torch_on_floats():
+    x = (RNG.standard_normal(20000) * np.exp(RNG.uniform(-20, 20, 20000))).astype(np.float32)
+    ref = torch.from_numpy(x).bfloat16().view(torch.int16).numpy().view(np.uint16)
+    got = np.array([oracle.f64_to_bf16(float(v)) for v in x], dtype=np.uint16)
+    assert np.array_equal(got, ref)
+
+
+def test_bf16_rounding_single_rounding_from_double():
+    # 1 + 2^-8 is a tie between 1 and 1 + 2^-7: ties to even -> 1.0
+    assert oracle.f64_to_bf16(1.0 + 2.0 ** -8) == 0x3F80
+    # just above the tie rounds up; a detour through float would round to the tie
+    # and then to even, giving 0x3F80.
+    assert oracle.f64_to_bf16(1.0 + 2.0 ** -8 + 2.0 ** -40) == 0x3F81
+    assert oracle.f64_to_bf16(-2.0) == 0xC000
+
+
+def test_e4m3_decode_matches_torch_float8():
+    codes = np.arange(256, dtype=np.uint8)
+    ref = torch.from_numpy(codes).view(torch.float8_e4m3fn).float().numpy().astype(np.float64)
+    got = np.array([oracle.e4m3_value(c) for c in codes])
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], ref[~nan])
+    assert oracle.e4m3_value(0x7E) == 448.0 and oracle.e4m3_value(0x01) == 2.0 ** -9
+
+
+# ---- visibility ---------------------------------------------------------------------
+
+def test_visibility_closed_form():
+    for m in (1, 2, 3, 4):
+        for p in list(range(0, 40)) + [1023, 1024, 1025, 4095, 262143, 1048575]:
+            assert oracle.n_visible(p, m) == (p + 1) // m
+
+
+def test_golden_selected_and_window_widths():
+    g = json.load(open(GOLD))
+    for e in g["selected_width"]:
+        assert min(oracle.n_visible(e["pos"], e["ratio"]), 512) == e["width"]
+    for e in g["window_width"]:
+        assert min(e["pos"] + 1, 128) == e["width"]
+    c = g["candidate_rows"]
+    assert c["blocks"] * c["block_rows"] == c["rows"] and c["rows"] >= c["topk"]
+    assert 128 + 512 == g["max_entries"]
+
+
+# ---- compressor ---------------------------------------------------------------------
+
+INV_FREQ = workloads.rope_inv_freq()
+
+
+def run_compress(kv, score, ratio, chunks, start=0, norm_w=None, eps=1e-6):
+    """Compress one sequence given as [S,512] float arrays, fed in the given chunk sizes."""
+    S = kv.shape[0]
+    assert sum(chunks) == S
+    nrows = (start + S) // ratio
+    plane = np.zeros((max(nrows, 1), 512), dtype=np.uint16)
+    pf = np.zeros((max(nrows, 1), 512))
+    ks = np.zeros((1, ratio, 512))
+    ss = np.zeros((1, ratio, 512))
+    total = 0
+    off = 0
+    for c in chunks:
+        kvb = oracle.bf16_bits(bf16(kv[off:off + c]))
+        scb = oracle.bf16_bits(bf16(score[off:off + c]))
+        n, f = oracle.compress(kvb, scb, [0, c], [start + off], ratio, ks, ss, plane, [0],
+                               INV_FREQ, norm_w=norm_w, eps=eps)
+        rows_now = (start + off + c) // ratio
+        first = (start + off) // ratio
+        pf[first:rows_now] = f[first:rows_now]
+        total += n
+        off += c
+    return total, plane, pf, ks, ss
+
+
+def rope_angles(pos):
+    return pos * INV_FREQ.astype(np.float64)
+
+
+def test_golden_tail_counts():
+    g = json.load(open(GOLD))
+    for ratio, key in ((2, "tail_ratio2"), (1, "tail_ratio1")):
+        for e in g[key]:
+            S = e["processed"]
+            kv = RNG.standard_normal((S, 512))
+            n, *_ = run_compress(kv, kv, ratio, [S - 2, 1, 1] if S > 2 else [S])
+            assert n == e["complete_rows"]
+            assert S - n * ratio == e["pending_tokens"]
+
+
+def test_ratio1_norm_and_rotation_invariants():
+    S = 40
+    kv = bf16_np(bf16(RNG.standard_normal((S, 512)) * 3.0))
+    n, plane, pf, *_ = run_compress(kv, kv, 1, [S], eps=1e-6)
+    assert n == S
+    for t in range(S):
+        x = kv[t]
+        ms = np.mean(x * x)
+        rstd = 1.0 / math.sqrt(ms + 1e-6)
+        y = pf[t]
+        # NoPE dims are the input scaled by one factor (normalised over all 512 dims)
+        np.testing.assert_allclose(y[:448], x[:448] * rstd, rtol=1e-12, atol=1e-12)
+        # the rotation preserves each pair's norm
+        n_in = x[448::2] ** 2 + x[449::2] ** 2
+        n_out = y[448::2] ** 2 + y[449::2] ** 2
+        np.testing.assert_allclose(n_out, n_in * rstd * rstd, rtol=1e-12)
+        # rotating back by the conjugate phase e^{-i t theta_i} recovers the input
+        z = (y[448::2] + 1j * y[449::2]) * np.exp(-1j * rope_angles(t))
+        np.testing.assert_allclose(z.real, x[448::2] * rstd, atol=1e-12)
+        np.testing.assert_allclose(z.imag, x[449::2] * rstd, atol=1e-12)
+        # stored row is the double value rounded to bf16 once
+        assert all(plane[t, d] == oracle.f64_to_bf16(y[d]) for d in range(0, 512, 37))
+
+
+def test_rope_unit_vector_phase_and_sign():
+    # (1, 0) at pair i maps to (cos, sin) and (0, 1) to (-sin, cos): multiplication of
+    # x_{2i} + i x_{2i+1} by e^{i p theta_i}.
+    S = 12
+    kv = np.zeros((S, 512))
+    kv[:, :448] = 1.0
+    kv[::2, 448] = 5.0   # even tokens: unit vector in the first dim of pair 0
+    kv[1::2, 449] = 5.0  # odd tokens: second dim of pair 0
+    n, _, pf, *_ = run_compress(kv, kv, 1, [S])
+    for t in range(S):
+        y = pf[t]
+        ms = np.mean(kv[t] ** 2)
+        r = 5.0 / math.sqrt(ms + 1e-6)
+        a = t * float(INV_FREQ[0])
+        if t % 2 == 0:
+            np.testing.assert_allclose(y[448:450], [r * math.cos(a), r * math.sin(a)], atol=1e-12)
+        else:
+            np.testing.assert_allclose(y[448:450], [-r * math.sin(a), r * math.cos(a)], atol=1e-12)
+
+
+def test_ratio2_group_head_position_and_equal_scores_mean():
+    # Two identical tokens with equal gates pool to that token; the row must then equal
+    # the ratio-1 row at the group's FIRST position j*m (not j*m+1).
+    S = 16
+    base = RNG.standard_normal((S // 2, 512))
+    kv = np.repeat(base, 2, axis=0)
+    sc = np.zeros((S, 512))
+    _, _, pf2, *_ = run_compress(kv, sc, 2, [S])
+    _, _, pf1, *_ = run_compress(kv, sc, 1, [S])
+    for j in range(S // 2):
+        np.testing.assert_allclose(pf2[j], pf1[2 * j], atol=1e-12)
+        assert np.max(np.abs(pf2[j] - pf1[2 * j + 1])) > 1e-3
+    # equal gates with different tokens: the mean of the pair, before RMSNorm
+    kv = bf16_np(bf16(RNG.standard_normal((S, 512))))
+    _, _, pf, *_ = run_compress(kv, np.full((S, 512), 0.25), 2, [S])
+    for j in range(S // 2):
+        r = 0.5 * (kv[2 * j] + kv[2 * j + 1])
+        rstd = 1.0 / math.sqrt(np.mean(r * r) + 1e-6)
+        np.testing.assert_allclose(pf[j][:448], r[:448] * rstd, rtol=1e-11, atol=1e-12)
+
+
+def test_ratio2_gate_is_per_channel_sigmoid():
+    # softmax over two slots = logistic function of the difference, channel by channel.
+    S = 8
+    kv = bf16_np(bf16(RNG.standard_normal((S, 512))))
+    sc = bf16_np(bf16(RNG.standard_normal((S, 512)) * 2.0))
+    _, _, pf, *_ = run_compress(kv, sc, 2, [S])
+    for j in range(S // 2):
+        g = expit(sc[2 * j] - sc[2 * j + 1])
+        r = kv[2 * j + 1] + g * (kv[2 * j] - kv[2 * j + 1])
+        rstd = 1.0 / math.sqrt(np.mean(r * r) + 1e-6)
+        np.testing.assert_allclose(pf[j][:448], r[:448] * rstd, rtol=1e-10, atol=1e-12)
+
+
+@pytest.mark.parametrize("ratio", [1, 2])
+def test_chunked_equals_one_shot(ratio):
+    S = 37
+    kv = RNG.standard_normal((S, 512))
+    sc = RNG.standard_normal((S, 512))
+    for start in (0, 5):
+        n1, p1, *_ = run_compress(kv, sc, ratio, [S], start=start)
+        for chunks in ([1] * S, [3, 4, 1, 29], [2, 2, 33], [36, 1]):
+            n2, p2, *_ = run_compress(kv, sc, ratio, chunks, start=start)
+            assert n2 == n1
+            first = start // ratio
+            assert np.array_equal(p1[first:], p2[first:])
+
+
+def test_norm_weight_applies_per_channel():
+    S = 4
+    kv = RNG.standard_normal((S, 512))
+    nw = RNG.uniform(0.5, 1.5, 512).astype(np.float32)
+    _, _, pa, *_ = run_compress(kv, kv, 1, [S])
+    _, _, pb, *_ = run_compress(kv, kv, 1, [S], norm_w=nw)
+    np.testing.assert_allclose(pb[:, :448], pa[:, :448] * nw[:448].astype(np.float64), rtol=1e-12)
+
+
+# ---- indexer ------------------------------------------------------------------------
+
+def make_index_case(Q=3, H=64, rows=300, seq=2):
+    iq = bf16(RNG.standard_normal((Q, H, 128)))
+    K = bf16(RNG.standard_normal((rows * seq, 128)))
+    w = RNG.standard_normal((Q, H)).astype(np.float32)
+    row_base = np.array([0, rows][:seq], dtype=np.int64)
+    return iq, K, w, row_base
+
+
+def test_index_single_head_is_relu_gemv():
+    iq, K, w, rb = make_index_case(Q=2, H=1, rows=200, seq=1)
+    w = np.ones((2, 1), dtype=np.float32)
+    pos = np.array([399, 250])  # ratio 2 -> 200, 125 visible
+    sc, rows = oracle.index_scores(iq, w, K, rb, [0, 0], pos, 2)
+    Kd, qd = bf16_np(K), bf16_np(iq)
+    for q in range(2):
+        nv = (pos[q] + 1) // 2
+        ref = np.maximum(Kd[:nv] @ qd[q, 0], 0.0) / math.sqrt(128)
+        np.testing.assert_allclose(sc[q, :nv], ref, rtol=1e-12, atol=1e-12)
+        assert np.all(rows[q, :nv] == np.arange(nv)) and np.all(rows[q, nv:] == -1)
+
+
+@pytest.mark.parametrize("H", [32, 64])
+def test_index_one_hot_weights_and_linearity(H):
+    iq, K, w, rb = make_index_case(Q=1, H=H, rows=150, seq=2)
+    Kd, qd = bf16_np(K), bf16_np(iq)
+    pos = [299]
+    alpha = 1.0 / math.sqrt(128 * H)
+    for h in (0, 7, H - 1):
+        oh = np.zeros((1, H), dtype=np.float32)
+        oh[0, h] = 1.0
+        sc, _ = oracle.index_scores(iq, oh, K, rb, [1], pos, 2)
+        ref = alpha * np.maximum(Kd[150:300] @ qd[0, h], 0.0)
+        np.testing.assert_allclose(sc[0, :150], ref, rtol=1e-12, atol=1e-13)
+    # dyadic weights: w1 + w2 is exact in fp32, so the score is exactly linear in w
+    w1 = (RNG.integers(-64, 64, (1, H)) / 8.0).astype(np.float32)
+    w2 = (RNG.integers(-64, 64, (1, H)) / 8.0).astype(np.float32)
+    s1, _ = oracle.index_scores(iq, w1, K, rb, [1], pos, 2)
+    s2, _ = oracle.index_scores(iq, w2, K, rb, [1], pos, 2)
+    s12, _ = oracle.index_scores(iq, w1 + w2, K, rb, [1], pos, 2)
+    np.testing.assert_allclose(s12, s1 + s2, rtol=1e-9, atol=1e-12)
+
+
+def test_index_without_relu_is_one_gemv():
+    iq, K, w, rb = make_index_case(Q=1, H=64, rows=120, seq=1)
+    Kd, qd = bf16_np(K), bf16_np(iq)
+    sc, _ = oracle.index_scores(iq, w, K, rb, [0], [119], 1, relu=False)
+    qc = (w[0].astype(np.float64)[:, None] * qd[0]).sum(0)
+    ref = (Kd @ qc) / math.sqrt(128 * 64)
+    np.testing.assert_allclose(sc[0, :120], ref, rtol=1e-9, atol=1e-12)
+
+
+def test_index_reindex_rows_and_masks():
+    iq, K, w, rb = make_index_case(Q=1, H=64, rows=200, seq=1)
+    cand = np.array([[0, 3, 24, -1]], dtype=np.int32)  # block 24 -> rows 192..199
+    pos = [196]  # ratio 1 -> 197 visible: rows 192..196 visible, 197..199 not
+    sc, rows = oracle.index_scores(iq, w, K, rb, [0], pos, 1, cand=cand)
+    full, frows = oracle.index_scores(iq, w, K, rb, [0], pos, 1)
+    expect_rows = list(range(0, 8)) + list(range(24, 32)) + list(range(192, 197)) + [-1] * 11
+    assert rows[0].tolist() == expect_rows
+    for i, r in enumerate(expect_rows):
+        if r >= 0:
+            assert sc[0, i] == full[0, r]
+
+
+# ---- top-k --------------------------------------------------------------------------
+
+def brute_topk(scores, rows, k):
+    valid = [(s if not math.isnan(s) else -math.inf, r) for s, r in zip(scores, rows) if r >= 0]
+    best = []
+    for _ in range(min(k, len(valid))):  # O(n k): repeatedly take the best remaining
+        i = max(range(len(valid)), key=lambda t: (valid[t][0], -valid[t][1]))
+        best.append(valid.pop(i)[1])
+    best.sort()
+    return best + [-1] * (k - len(best))
+
+
+def test_topk_brute_force_with_ties_and_nan():
+    for trial in range(300):
+        n = int(RNG.integers(1, 64))
+        k = int(RNG.integers(1, 70))
+        scores = RNG.integers(-3, 4, n).astype(np.float64)  # many ties
+        if trial % 3 == 0:
+            scores[RNG.integers(0, n, 3)] = np.nan
+        if trial % 5 == 0:
+            scores[RNG.integers(0, n, 2)] = -np.inf
+        rows = RNG.permutation(1000)[:n].astype(np.int64)
+        rows[RNG.random(n) < 0.1] = -1
+        got = oracle.topk(scores, rows, k)
+        assert got.tolist() == brute_topk(scores, rows, k)
+
+
+def test_topk_float32_ties_exact_and_negative_zero():
+    s = np.array([0.0, -0.0, 1.5, 1.5, -1.0, 1.5], dtype=np.float32).astype(np.float64)
+    got = oracle.topk(s, np.arange(6), 4)
+    assert got.tolist() == [0, 2, 3, 5]  # -0.0 == 0.0, lower row wins the tie
+
+
+# ---- sparse attention ---------------------------------------------------------------
+
+def dense_attention(qd, X, scale, sink=None):
+    """Textbook softmax attention for one query: qd [64,512], X [n,512]."""
+    S = (qd @ X.T) * scale
+    if sink is None:
+        P = np.exp(S - S.max(1, keepdims=True))
+        return (P / P.sum(1, keepdims=True)) @ X
+    mx = np.maximum(S.max(1), sink)
+    P = np.exp(S - mx[:, None])
+    Z = P.sum(1) + np.exp(sink - mx)
+    return (P @ X) / Z[:, None]
+
+
+def attn_case(p, nsel_valid, B=1, nrows=700, seed=0):
+    g = np.random.default_rng(seed)
+    q = bf16(g.standard_normal((1, 64, 512)))
+    ring = bf16(g.standard_normal((B, 128, 512)))
+    plane = bf16(g.standard_normal((nrows, 512)))
+    sel = np.full((1, 512), -1, dtype=np.int32)
+    sel[0, :nsel_valid] = np.sort(g.permutation(nrows)[:nsel_valid])
+    sink = g.standard_normal(64).astype(np.float32)
+    return q, ring, plane, sel, sink
+
+
+def window_rows(ring, p, b=0):
+    lo = max(0, p - 127)
+    return np.stack([bf16_np(ring[b, pos % 128]) for pos in range(lo, p + 1)])
+
+
+def test_attention_no_sink_all_rows_is_dense_softmax():
+    for p, ns in ((4095, 512), (5, 40), (130, 0)):
+        q, ring, plane, sel, _ = attn_case(p, ns)
+        out, _ = oracle.sparse_attn(q, [0], [p], ring, plane, [0], sel, None)
+        X = window_rows(ring, p)
+        if ns:
+            X = np.concatenate([X, bf16_np(plane)[sel[0, :ns]]])
+        ref = dense_attention(bf16_np(q)[0], X, 512 ** -0.5)
+        np.testing.assert_allclose(out[0], ref, rtol=1e-10, atol=1e-12)
+
+
+def test_attention_sink_closed_form_and_lse():
+    p, ns = 1000, 300
+    q, ring, plane, sel, sink = attn_case(p, ns, seed=3)
+    out0, lse0 = oracle.sparse_attn(q, [0], [p], ring, plane, [0], sel, None)
+    out1, lse1 = oracle.sparse_attn(q, [0], [p], ring, plane, [0], sel, sink)
+    Z = np.exp(lse0[0])  # sum_j e^{s_j}
+    factor = Z / (Z + np.exp(sink.astype(np.float64)))
+    np.testing.assert_allclose(out1[0], out0[0] * factor[:, None], rtol=1e-10, atol=1e-13)
+    np.testing.assert_allclose(np.exp(lse1[0]), Z + np.exp(sink.astype(np.float64)), rtol=1e-10)
+    # a very negative sink is the no-sink case
+    out2, _ = oracle.sparse_attn(q, [0], [p], ring, plane, [0], sel, np.full(64, -1e4, np.float32))
+    np.testing.assert_allclose(out2, out0, rtol=1e-12, atol=1e-14)
+
+
+def test_attention_duplicate_entry_counts_twice():
+    # A plane row equal to a window row is a second entry, not merged: the pair acts
+    # as one entry whose logit is larger by ln 2.
+    p = 300
+    q, ring, plane, sel, sink = attn_case(p, 10, seed=5)
+    plane = plane.clone()
+    plane[sel[0, 0]] = ring[0, p % 128]  # duplicate of the current position's window row
+    out, _ = oracle.sparse_attn(q, [0], [p], ring, plane, [0], sel, sink)
+    X = window_rows(ring, p)
+    Y = bf16_np(plane)[sel[0, 1:10]]
+    qd = bf16_np(q)[0]
+    S = np.concatenate([X, Y]) @ qd.T * 512 ** -0.5  # [n, 64]
+    dup = X.shape[0] - 1  # the window row of position p is the last window entry
+    S[dup] += math.log(2.0)
+    mx = np.maximum(S.max(0), sink)
+    P = np.exp(S - mx)
+    Z = P.sum(0) + np.exp(sink - mx)
+    ref = (P.T @ np.concatenate([X, Y])) / Z[:, None]
+    np.testing.assert_allclose(out[0], ref, rtol=1e-10, atol=1e-13)
+
+
+def test_attention_entry_cap_and_ragged_window():
+    # 128 window + 512 selected = 640 entries at most; an early position sees p+1 slots.
+    q, ring, plane, sel, _ = attn_case(4095, 512, seed=7)
+    X = np.concatenate([window_rows(ring, 4095), bf16_np(plane)[sel[0]]])
+    assert X.shape[0] == 640
+    q, ring, plane, sel, _ = attn_case(9, 3, seed=8)
+    # slots beyond position 9 hold junk that must not be read
+    ring2 = ring.clone()
+    ring2[0, 10:] = bf16(np.full((118, 512), 1e3))
+    a, _ = oracle.sparse_attn(q, [0], [9], ring, plane, [0], sel, None)
+    b, _ = oracle.sparse_attn(q, [0], [9], ring2, plane, [0], sel, None)
+    assert np.array_equal(a, b)
+
+
+def test_attention_linear_window_equals_ring():
+    p = 500
+    q, ring, plane, sel, sink = attn_case(p, 64, seed=9)
+    lo = p - 127
+    lin = torch.stack([ring[0, pos % 128] for pos in range(lo, p + 1)])
+    a, la = oracle.sparse_attn(q, [0], [p], ring, plane, [0], sel, sink)
+    b, lb = oracle.sparse_attn(q, [0], [p], lin, plane, [0], sel, sink, swa_mode="linear",
+                               lin_base=[0], lin_pos0=[lo])
+    np.testing.assert_allclose(a, b, rtol=1e-12, atol=1e-14)
+
+
+def test_attention_fp8_ring_dequant_matches_torch_float8():
+    p = 200
+    g = np.random.default_rng(11)
+    q = bf16(g.standard_normal((1, 64, 512)))
+    codes = g.integers(0, 256, (1, 128, 512)).astype(np.uint8)
+    codes[(codes & 0x7F) == 0x7F] = 0x3C  # no NaN codes
+    scales = g.uniform(0.01, 0.02, (1, 128, 4)).astype(np.float32)
+    ring8 = np.concatenate([codes, scales.view(np.uint8).reshape(1, 128, 16)], axis=2)
+    plane = bf16(g.standard_normal((10, 512)))
+    sel = np.full((1, 512), -1, dtype=np.int32)
+    sel[0, :4] = [1, 3, 5, 7]
+    out, _ = oracle.sparse_attn(q, [0], [p], torch.from_numpy(ring8), plane, [0], sel, None)
+    deq = torch.from_numpy(codes).view(torch.float8_e4m3fn).double().numpy()
+    deq = deq * np.repeat(scales.astype(np.float64), 128, axis=2)
+    X = np.stack([deq[0, pos % 128] for pos in range(p - 127, p + 1)])
+    X = np.concatenate([X, bf16_np(plane)[[1, 3, 5, 7]]])
+    ref = dense_attention(bf16_np(q)[0], X, 512 ** -0.5)
+    np.testing.assert_allclose(out[0], ref, rtol=1e-10, atol=1e-13)
+
+
+# ---- generator ----------------------------------------------------------------------
+
+def test_synth_normal_moments_and_determinism():
+    import synth
+    x = synth.normal_f32(1 << 20, 7, 3).numpy().astype(np.float64)
+    assert abs(x.mean()) < 5e-3 and abs(x.std() - 1.0) < 5e-3
+    y = synth.normal_f32(1 << 20, 7, 3).numpy().astype(np.float64)
+    assert np.array_equal(x, y)
+    z = synth.normal_f32(16, 7, 3, offset=100).numpy()
+    assert np.array_equal(z, x[100:116].astype(np.float32))
+
+
+def test_synth_e4m3_encode_matches_torch():
+    import synth
+    r = synth.rows_fp8s128(0, 0, 64, 5, 9)
+    codes = r[:, :512].contiguous()
+    vals = synth.rows_f32(0, 0, 64, 512, 5, 9) * 64.0
+    ref = vals.to(torch.float8_e4m3fn).view(torch.uint8)
+    assert torch.equal(codes, ref)
+    sc = r[:, 512:].contiguous().view(torch.float32)
+    assert float(sc.min()) >= 0.75 / 64 and float(sc.max()) < 1.25 / 64
