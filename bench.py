@@ -1,0 +1,428 @@
+"""Benchmark of the CSA2 attention step on GB300.
+
+Default workload: FULL-layer decode batch -- 64 sequences with context lengths
+uniform in [16384, 65536], ratio 2 (compressor with odd-tail state), 64-head x
+128-d indexer over the visible rows, top-512, 64 x 512 queries over the 128-slot
+bf16 window plus the selected rows with a per-head sink.  One step = compress the
+64 new tokens + index + top-512 + sparse attention, all through the C ABI.
+
+Prints one JSON line (rank 0).  `--impl reference` times the CPU oracle instead.
+Under torchrun every rank runs its own batch (weak scaling, no collective on the
+data path); the step time is the maximum over ranks.
+"""
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "CSA2 decode queries/sec & achieved HBM GB/s (index+top-512+sparse_attn), 1 GB300"
+PEAKS = os.path.join(ROOT, "MEASURED_PEAKS.json")
+FALLBACK_HBM = 6800.0
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=3000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--config", default="decode",
+                    choices=["tiny", "decode", "reindex", "prefill", "long"])
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--cpu-queries", type=int, default=64)
+    return ap.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def hbm_peak():
+    try:
+        with open(PEAKS) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM, "fallback"
+
+
+def make_workload(name, rank):
+    from synth import workloads as W
+    seed_off = 1000 * rank
+    if name == "decode":
+        return W.decode_batch(seed=1 + seed_off)
+    if name == "tiny":
+        return W.tiny_decode(seed=0 + seed_off)
+    if name == "reindex":
+        return W.reindex_decode(seed=2 + seed_off)
+    if name == "prefill":
+        return W.prefill_reuse(seed=3 + seed_off)
+    return W.long_decode(seed=4 + seed_off)
+
+
+def spec_for(wl):
+    from csa2_compressed_sparse_gb300 import SWA_LINEAR, SWA_RING
+    from csa2_compressed_sparse_gb300.step import StepSpec
+    ms = wl.ncb * 8 if wl.reindex else int(max((int(p) + 1) // wl.ratio for p in wl.q_pos))
+    return StepSpec(ratio=wl.ratio, H=wl.H, k=wl.k, max_scored=ms,
+                    swa_mode=SWA_LINEAR if wl.swa == "linear" else SWA_RING)
+
+
+def algorithmic_bytes(wl):
+    """Bytes a step must move at least (the scores spill is excluded).
+    Returns (total, index-stage bytes, attention bytes per layer)."""
+    nvis = np.array([(int(p) + 1) // wl.ratio for p in wl.q_pos], dtype=np.int64)
+    scored = np.full_like(nvis, wl.ncb * 8) if wl.reindex else nvis
+    keff = np.minimum(scored, wl.k)
+    index = int((scored * 128 * 2).sum()) + wl.Q * (wl.H * 128 * 2 + wl.H * 4 + wl.k * 4)
+    if wl.reindex:
+        index += wl.Q * wl.ncb * 4
+    win_row = 528 if wl.swa_dtype == "fp8" else 1024
+    win = np.minimum(wl.q_pos + 1, 128)
+    if wl.swa == "linear":  # windows of neighbouring queries overlap: count the distinct rows
+        win_bytes = int(wl.lin_len.sum()) * 1024
+    else:
+        win_bytes = int(win.sum()) * win_row
+    attn = int(keff.sum()) * 1024 + win_bytes + wl.Q * (64 * 512 * 2 * 2 + wl.k * 4 + 64)
+    comp = wl.T * 512 * 2 * 2 + int((wl.n_rows - wl.n_hist).sum()) * 1024 + wl.B * 2 * 512 * 4 * 2
+    return comp + index + attn * wl.layers, index, attn
+
+
+class Clocks:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            return None
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def traffic_from_profile(config):
+    """DRAM bytes per launch of the index score kernel from the committed ncu summary."""
+    p = os.path.join(ROOT, "profiles", f"index_score_kernel.{config}.md")
+    try:
+        for line in open(p):
+            if line.startswith("dram_bytes_per_launch:"):
+                v = line.split(":", 1)[1].strip()
+                return None if v == "null" else float(v)
+    except OSError:
+        pass
+    return None
+
+
+def run_ours(args):
+    import torch.distributed as dist
+    rank, world, local = dist_env()
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device(f"cuda:{local}"))
+    torch.cuda.set_device(local)
+    import csa2_compressed_sparse_gb300 as csa2
+    from csa2_compressed_sparse_gb300.step import allocate, kernel_launches, run_step
+
+    wl = make_workload(args.config, rank)
+    spec = spec_for(wl)
+    t = wl.materialize("cuda")
+    buf = allocate(spec, t)
+    stream = torch.cuda.current_stream()
+    for _ in range(max(args.warmup, 3)):
+        run_step(spec, t, buf)
+    csa2.csa2_device_status()
+
+    # ---- device-resident timing of K steps ----
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ix0 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ix1 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    clocks = Clocks(local)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    ev0.record(stream)
+    for i in range(args.steps):
+        if spec and t["kv"].shape[0]:
+            csa2.csa2_compress(t["kv"], t["score"], t["cu_seqlens"], t["start_pos"], spec.ratio,
+                               t["kv_state"], t["score_state"], t["plane"], t["row_base"],
+                               t["inv_freq"], eps=spec.eps)
+        ix0[i].record(stream)
+        csa2.csa2_index_topk(t["iq"], t["w"], t["index_k"], t["row_base"], t["q_seq"], t["q_pos"],
+                             spec.ratio, spec.k, spec.max_scored, buf.sel, buf.ws,
+                             sel_scores=buf.sel_scores, cand=t.get("cand"), relu=spec.relu)
+        ix1[i].record(stream)
+        from csa2_compressed_sparse_gb300.step import swa_of
+        for layer in range(len(t["q"])):
+            fn = csa2.csa2_sparse_attn if layer == 0 else csa2.csa2_reuse_attn
+            fn(t["q"][layer], t["q_seq"], t["q_pos"], swa_of(spec, t, layer), t["plane"],
+               t["row_base"], buf.sel, t["sink"], buf.out[layer], scale=spec.scale)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    if world > 1:
+        dist.barrier()
+    ms = ev0.elapsed_time(ev1)
+    idx_ms = sum(a.elapsed_time(b) for a, b in zip(ix0, ix1)) / args.steps
+    csa2.csa2_device_status()
+    tmax = torch.tensor([ms], dtype=torch.float64, device="cuda")
+    if world > 1:
+        dist.all_reduce(tmax, op=dist.ReduceOp.MAX)
+    ms = float(tmax.item())
+    ms_step = ms / args.steps
+    q_total = wl.Q * world * args.steps
+    value = q_total / (ms / 1e3)
+    total_bytes, index_bytes, attn_bytes = algorithmic_bytes(wl)
+    peak, peak_kind = hbm_peak()
+    achieved_index = index_bytes / (idx_ms / 1e3) / 1e9
+
+    # ---- end to end through the public API with host buffers ----
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e(args, wl, spec, t, buf, world)
+
+    line = {
+        "metric": METRIC,
+        "value": value,
+        "unit": "queries/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms_step,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded SplitMix64 generator, N(0,1)-like values)",
+        "config": {
+            "workload": wl.name,
+            "description": wl.description,
+            "queries_per_step_per_gpu": wl.Q,
+            "sequences": wl.B,
+            "ratio": wl.ratio,
+            "indexer_heads": wl.H,
+            "topk": wl.k,
+            "max_visible_rows": spec.max_scored,
+            "mean_visible_rows": float(np.mean([(int(p) + 1) // wl.ratio for p in wl.q_pos])),
+            "attention_layers": wl.layers,
+            "l2": "inputs larger than L2: the index plane read per step is "
+                  f"{index_bytes / 1e6:.0f} MB",
+            "parallelism": f"dp{world} (independent sequence batches per GPU)",
+        },
+        "achieved_hbm_gbs": total_bytes / (ms_step / 1e3) / 1e9,
+        "algorithmic_bytes_per_step": total_bytes,
+        "roofline": {
+            "kernel": "csa2_index_topk stage (index prep + tcgen05 score kernel + top-k)",
+            "bound": "hbm",
+            "achieved": achieved_index,
+            "peak": peak,
+            "peak_kind": f"{peak_kind} hbm_gbs",
+            "unit": "GB/s",
+            "frac": achieved_index / peak,
+            "traffic": traffic_from_profile(args.config),
+            "stage_ms": idx_ms,
+            "algorithmic_bytes_per_launch": index_bytes,
+        },
+        "gpu_launches": kernel_launches(spec, t) * args.steps,
+        "clocks": clk,
+        "e2e": e2e,
+    }
+    if rank == 0 and not args.no_cpu:
+        line["cpu_baseline"] = cpu_baseline(wl, args.cpu_queries)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def run_e2e(args, wl, spec, t, buf, world):
+    """Each step copies its inputs from pinned host memory, runs the step through the
+    C ABI and reads the outputs back; timed on the host and on the stream."""
+    import csa2_compressed_sparse_gb300 as csa2
+    from csa2_compressed_sparse_gb300.step import run_step
+    names = ["kv", "score", "iq", "w", "q_pos", "q_seq", "cu_seqlens", "start_pos"]
+    host = {n: t[n].cpu().pin_memory() for n in names}
+    hq = [x.cpu().pin_memory() for x in t["q"]]
+    out_h = [torch.empty(x.shape, dtype=x.dtype).pin_memory() for x in buf.out]
+    sel_h = torch.empty(buf.sel.shape, dtype=buf.sel.dtype).pin_memory()
+    h2d = sum(x.numel() * x.element_size() for x in host.values()) + \
+        sum(x.numel() * x.element_size() for x in hq)
+    d2h = sum(x.numel() * x.element_size() for x in out_h) + sel_h.numel() * 4
+    steps = max(20, args.steps // 10)
+    stream = torch.cuda.current_stream()
+
+    def one():
+        for n in names:
+            t[n].copy_(host[n], non_blocking=True)
+        for d, h in zip(t["q"], hq):
+            d.copy_(h, non_blocking=True)
+        run_step(spec, t, buf)
+        for h, d in zip(out_h, buf.out):
+            h.copy_(d, non_blocking=True)
+        sel_h.copy_(buf.sel, non_blocking=True)
+
+    for _ in range(3):
+        one()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    w0 = time.perf_counter()
+    e0.record(stream)
+    for _ in range(steps):
+        one()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - w0
+    csa2.csa2_device_status()
+    return {"value": wl.Q * world * steps / wall, "unit": "queries/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "device_ms_per_step": e0.elapsed_time(e1) / steps, "steps": steps}
+
+
+# ---- CPU oracle legs ------------------------------------------------------------------------
+
+def oracle_step(wl, queries):
+    """The oracle on a subset of queries: compress their sequences' new tokens, index,
+    top-k, and every attention layer.  Returns seconds of oracle work."""
+    import oracle
+    import synth
+    from oracle.harness import HostSeq, query_inputs, window_rows
+    prep = []
+    for q in queries:
+        b = int(wl.q_seq[q])
+        iq, w = query_inputs(wl, q)
+        k_rows = synth.rows_bf16(b, 0, int(wl.n_rows[b]), 128, wl.seed, synth.INDEX_K)
+        prep.append((q, b, iq, w, k_rows))
+    t0 = time.perf_counter()
+    sels = {}
+    seqs = {}
+    for q, b, iq, w, k_rows in prep:
+        if b not in seqs:
+            seqs[b] = HostSeq(wl, b)   # the oracle compressor over the step's tokens
+        cand = None if wl.cand is None else wl.cand[q:q + 1]
+        sc, rows = oracle.index_scores(iq, w, k_rows, [0], [0], [int(wl.q_pos[q])], wl.ratio,
+                                       cand=cand)
+        sels[q] = oracle.topk(sc[0], rows[0], wl.k)
+    t_index = time.perf_counter() - t0
+    # attention: one batched oracle call per layer over the sampled queries
+    t_attn = 0.0
+    for layer in range(wl.layers):
+        qs, planes, sel_c, wins = [], [], [], []
+        base = 0
+        for q, b, *_ in prep:
+            s = sels[q]
+            v = s >= 0
+            planes.append(seqs[b].plane_rows(s[v]))
+            sc = np.full(len(s), -1, dtype=np.int32)
+            sc[v] = base + np.arange(int(v.sum()))
+            base += int(v.sum())
+            sel_c.append(sc)
+            qs.append(wl.host_q(q, layer))
+            wins.append(window_rows(wl, q, layer))
+        plane = oracle.bf16_from_bits(np.concatenate(planes)) if base else torch.zeros((1, 512), dtype=torch.bfloat16)
+        sink = synth.normal_f32(64, wl.seed, synth.SINK)
+        t1 = time.perf_counter()
+        for i, (q, b, *_) in enumerate(prep):
+            w = wins[i]
+            oracle.sparse_attn(qs[i].view(1, 64, 512), [0], [int(wl.q_pos[q])], w["swa"], plane,
+                               [0], sel_c[i].reshape(1, -1), sink, swa_mode=w["swa_mode"],
+                               lin_base=w["lin_base"], lin_pos0=w["lin_pos0"])
+        t_attn += time.perf_counter() - t1
+    return t_index + t_attn
+
+
+def cpu_baseline(wl, nq):
+    import oracle  # noqa: F401  (built on first use)
+    qs = list(range(min(nq, wl.Q)))
+    secs = oracle_step(wl, qs)
+    cores = int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1))
+    return {"value": len(qs) / secs, "unit": "queries/s", "cores": cores, "kind": "oracle",
+            "sample": f"{len(qs)} of {wl.Q} queries of one step ({wl.name}): oracle compressor, "
+                      f"indexer, top-k and {wl.layers} attention layer(s); {secs:.1f} s"}
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    wl = make_workload(args.config, 0)
+    nq = min(8, wl.Q)
+    qs = list(range(nq))
+    for _ in range(args.warmup):
+        oracle_step(wl, qs[:1])
+    tot = 0.0
+    for i in range(args.steps):
+        tot += oracle_step(wl, qs)
+    value = nq * args.steps / tot
+    cores = int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1))
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "queries/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": tot / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": wl.name, "description": wl.description,
+                   "sample_queries_per_step": nq},
+        "cpu_baseline": {"value": value, "unit": "queries/s", "cores": cores, "kind": "oracle",
+                         "sample": f"{nq} queries of {wl.name} per step"},
+        "e2e": {"value": value, "unit": "queries/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,148 @@
+// common.cuh -- argument blocks shared by the C-ABI layer and the kernels, plus the
+// per-translation-unit fault flag helpers.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <string.h>
+
+#include "ptx.cuh"
+
+namespace csa2 {
+
+constexpr int kDLat = 512;   // latent width (K = V)
+constexpr int kDIdx = 128;   // indexer head width
+constexpr int kHeads = 64;   // attention query heads
+constexpr int kRing = 128;   // sliding-window slots
+constexpr int kRopeDim0 = 448;
+constexpr int kMaxK = 512;   // largest top-k
+
+struct CompressArgs {
+  const uint16_t* kv;
+  const uint16_t* score;
+  int T;
+  const int32_t* cu_seqlens;
+  int B;
+  const int64_t* start_pos;
+  int ratio;
+  float* kv_state;
+  float* score_state;
+  uint16_t* plane;
+  int64_t plane_rows;
+  const int64_t* row_base;
+  const float* norm_w;
+  float eps;
+  const float* inv_freq;
+};
+
+struct IndexArgs {
+  const uint16_t* iq;   // [Q][H][128]
+  const float* w;       // [Q][H]
+  int Q, H;
+  const uint16_t* index_k;
+  int64_t index_rows;
+  const int64_t* row_base;
+  const int32_t* q_seq;
+  const int64_t* q_pos;
+  int ratio;
+  const int32_t* cand;  // [Q][ncb] or null
+  int ncb;
+  int relu;
+  int64_t ld;           // max_scored: row stride of the key / score arrays
+  float* scores_out;    // optional [Q][ld]
+  // workspace views
+  uint32_t* keys;       // [Q][ld]
+  int32_t* n_scored;    // [Q]
+  int32_t* grp_q0;      // [Q]  first query of group g
+  int32_t* grp_nq;      // [Q]  queries in group g
+  int64_t* grp_tile0;   // [Q+1] first work tile of group g (prefix)
+  int32_t* n_groups;    // [1]
+  int32_t* tmp;         // [Q]  scratch of the grouping pass
+  int group_max;        // queries per group (FULL: 256 / H; REINDEX: 1)
+};
+
+struct TopkArgs {
+  const uint32_t* keys;   // [Q][ld] order-preserving keys (0 = not scored), or
+  const float* scores;    // [Q][ld] raw fp32 scores (converted on load)
+  const int32_t* n;       // [Q] positions per row
+  int Q;
+  int64_t ld;
+  int k;
+  const int32_t* cand;    // [Q][ncb] position -> row map for REINDEX, else null
+  int ncb;
+  int32_t* sel;           // [Q][k]
+  float* sel_scores;      // [Q][k] or null
+  uint64_t* part;         // [Q][nchunk][k] (key << 32 | position) partial results
+  int nchunk;             // chunks per row (1 = single pass)
+};
+
+struct AttnArgs {
+  const uint16_t* q;
+  int Q;
+  const int32_t* q_seq;
+  const int64_t* q_pos;
+  int swa_mode, swa_dtype;
+  const uint8_t* swa;
+  int64_t swa_rows;
+  const int64_t* lin_base;
+  const int64_t* lin_pos0;
+  const uint16_t* plane;
+  int64_t plane_rows;
+  const int64_t* row_base;
+  const int32_t* sel;
+  int nsel;
+  const float* sink;
+  float scale;
+  uint16_t* out;
+  float* lse;
+};
+
+cudaError_t launch_compress(const CompressArgs& a, cudaStream_t s);
+cudaError_t launch_index(const IndexArgs& a, int num_sms, cudaStream_t s);
+cudaError_t launch_topk(const TopkArgs& a, cudaStream_t s);
+cudaError_t launch_attn(const AttnArgs& a, cudaStream_t s);
+
+// Fault flags of each translation unit (read and cleared, host side).
+int take_fault_compress();
+int take_fault_index();
+int take_fault_topk();
+int take_fault_attn();
+
+// Order-preserving map of fp32 scores to uint32 keys: NaN ranks as -inf, -0 as +0,
+// and every key of a real score is >= 1 so that 0 can mark "not scored".
+__host__ __device__ __forceinline__ uint32_t score_key(float f) {
+  uint32_t u;
+#ifdef __CUDA_ARCH__
+  u = __float_as_uint(f);
+#else
+  memcpy(&u, &f, 4);
+#endif
+  if ((u & 0x7FFFFFFFu) > 0x7F800000u) u = 0xFF800000u;  // NaN -> -inf
+  if (u == 0x80000000u) u = 0u;                           // -0 -> +0
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+__host__ __device__ __forceinline__ float key_score(uint32_t k) {
+  uint32_t u = (k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k;
+#ifdef __CUDA_ARCH__
+  return __uint_as_float(u);
+#else
+  float f;
+  memcpy(&f, &u, 4);
+  return f;
+#endif
+}
+
+}  // namespace csa2
+
+// Host reader of this translation unit's fault flag.
+#define CSA2_DEFINE_FAULT_FLAG(NAME)                                     \
+  namespace csa2 {                                                       \
+  int take_fault_##NAME() {                                              \
+    int v = 0, z = 0;                                                    \
+    if (cudaMemcpyFromSymbol(&v, g_fault, sizeof(int)) != cudaSuccess)   \
+      return 0;                                                          \
+    if (v) cudaMemcpyToSymbol(g_fault, &z, sizeof(int));                 \
+    return v;                                                            \
+  }                                                                      \
+  }

@@ -1,0 +1,267 @@
+// csa2_api.cu -- the extern "C" entry points declared in include/csa2.h: argument
+// validation on the host, workspace layout, kernel dispatch and error reporting.
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <string>
+
+#include "../../include/csa2.h"
+#include "common.cuh"
+
+namespace csa2 {
+int topk_num_chunks(int64_t ld);
+int topk_max_chunks();
+}  // namespace csa2
+
+namespace {
+
+thread_local std::string g_last_error;
+
+csa2_status fail(csa2_status st, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return st;
+}
+
+csa2_status cuda_fail(cudaError_t e, const char* where) {
+  return fail(CSA2_ECUDA, "%s: %s", where, cudaGetErrorString(e));
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+#define REQUIRE(cond, ...)                         \
+  do {                                             \
+    if (!(cond)) return fail(CSA2_EINVAL, __VA_ARGS__); \
+  } while (0)
+
+int num_sms() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  return n;
+}
+
+size_t up256(size_t x) { return (x + 255) & ~size_t(255); }
+
+// Workspace of csa2_index_topk.
+struct IndexWs {
+  size_t keys, n_scored, grp_q0, grp_nq, tmp, grp_tile0, n_groups, part, total;
+  int nchunk;
+};
+
+IndexWs index_ws_layout(int Q, int64_t ld, int k) {
+  IndexWs w{};
+  size_t o = 0;
+  w.keys = o; o = up256(o + (size_t)Q * (size_t)ld * 4);
+  w.n_scored = o; o = up256(o + (size_t)Q * 4);
+  w.grp_q0 = o; o = up256(o + (size_t)Q * 4);
+  w.grp_nq = o; o = up256(o + (size_t)Q * 4);
+  w.tmp = o; o = up256(o + (size_t)Q * 4);
+  w.grp_tile0 = o; o = up256(o + (size_t)(Q + 1) * 8);
+  w.n_groups = o; o = up256(o + 4);
+  w.nchunk = csa2::topk_num_chunks(ld);
+  w.part = o;
+  if (w.nchunk > 1) o = up256(o + (size_t)Q * w.nchunk * k * 8);
+  w.total = o;
+  return w;
+}
+
+size_t topk_ws_bytes(int Q, int64_t ld, int k) {
+  const int nchunk = csa2::topk_num_chunks(ld);
+  return nchunk > 1 ? up256((size_t)Q * nchunk * k * 8) : 0;
+}
+
+csa2_status attn_common(const char* name, const csa2_bf16* q, int Q, const int32_t* q_seq,
+                        const int64_t* q_pos, const csa2_swa* swa, const csa2_bf16* plane,
+                        int64_t plane_rows, const int64_t* row_base, const int32_t* sel, int nsel,
+                        const float* sink, float scale, csa2_bf16* out, float* lse,
+                        csa2_stream stream) {
+  REQUIRE(Q >= 0, "%s: Q must be >= 0 (got %d)", name, Q);
+  if (Q == 0) return CSA2_OK;
+  REQUIRE(q && q_seq && q_pos && swa && out, "%s: q, q_seq, q_pos, swa and out are required", name);
+  REQUIRE(aligned16(q) && aligned16(out), "%s: q and out must be 16-byte aligned", name);
+  REQUIRE(nsel >= 0 && nsel <= 512, "%s: nsel must be in [0, 512] (got %d)", name, nsel);
+  REQUIRE(nsel == 0 || (sel && plane && row_base), "%s: sel, plane and row_base are required when nsel > 0", name);
+  REQUIRE(plane == nullptr || aligned16(plane), "%s: plane must be 16-byte aligned", name);
+  REQUIRE(swa->mode == CSA2_SWA_RING || swa->mode == CSA2_SWA_LINEAR, "%s: bad swa.mode %d", name, swa->mode);
+  REQUIRE(swa->dtype == CSA2_SWA_BF16 || swa->dtype == CSA2_SWA_FP8_S128, "%s: bad swa.dtype %d", name, swa->dtype);
+  REQUIRE(swa->data && aligned16(swa->data), "%s: swa.data must be a 16-byte aligned pointer", name);
+  REQUIRE(swa->n_rows >= 0, "%s: swa.n_rows must be >= 0", name);
+  REQUIRE(swa->mode == CSA2_SWA_RING || (swa->lin_base && swa->lin_pos0),
+          "%s: LINEAR windows need lin_base and lin_pos0", name);
+  REQUIRE(std::isfinite(scale), "%s: scale must be finite", name);
+  REQUIRE(plane_rows >= 0, "%s: plane_rows must be >= 0", name);
+  csa2::AttnArgs a{};
+  a.q = q; a.Q = Q; a.q_seq = q_seq; a.q_pos = q_pos;
+  a.swa_mode = swa->mode; a.swa_dtype = swa->dtype;
+  a.swa = static_cast<const uint8_t*>(swa->data); a.swa_rows = swa->n_rows;
+  a.lin_base = swa->lin_base; a.lin_pos0 = swa->lin_pos0;
+  a.plane = plane; a.plane_rows = plane_rows; a.row_base = row_base;
+  a.sel = sel; a.nsel = nsel; a.sink = sink; a.scale = scale; a.out = out; a.lse = lse;
+  cudaError_t e = csa2::launch_attn(a, stream);
+  if (e != cudaSuccess) return cuda_fail(e, name);
+  return CSA2_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* csa2_last_error(void) { return g_last_error.c_str(); }
+
+const char* csa2_version(void) { return "csa2 0.1 sm_103a"; }
+
+csa2_status csa2_device_status(csa2_stream stream) {
+  cudaError_t e = cudaStreamSynchronize(stream);
+  if (e != cudaSuccess) return cuda_fail(e, "csa2_device_status");
+  int f = 0;
+  for (int v : {csa2::take_fault_compress(), csa2::take_fault_index(), csa2::take_fault_topk(),
+                csa2::take_fault_attn()})
+    if (!f) f = v;
+  if (f == csa2::kFaultTimeout) return fail(CSA2_ETIMEOUT, "a kernel gave up a bounded wait");
+  if (f == csa2::kFaultBounds) return fail(CSA2_EBOUNDS, "a kernel met an index outside its buffer");
+  return CSA2_OK;
+}
+
+csa2_status csa2_compress(const csa2_bf16* kv, const csa2_bf16* score, int T,
+                          const int32_t* cu_seqlens, int B, const int64_t* start_pos, int ratio,
+                          float* kv_state, float* score_state, csa2_bf16* plane,
+                          int64_t plane_rows, const int64_t* row_base, const float* norm_w,
+                          float eps, const float* inv_freq, csa2_stream stream) {
+  REQUIRE(ratio == 1 || ratio == 2, "csa2_compress: ratio must be 1 or 2 (got %d)", ratio);
+  REQUIRE(B >= 1 && B <= 8192, "csa2_compress: B must be in [1, 8192] (got %d)", B);
+  REQUIRE(T >= 0, "csa2_compress: T must be >= 0 (got %d)", T);
+  if (T == 0) return CSA2_OK;
+  REQUIRE(kv && cu_seqlens && start_pos && plane && row_base && inv_freq,
+          "csa2_compress: kv, cu_seqlens, start_pos, plane, row_base and inv_freq are required");
+  REQUIRE(ratio == 1 || (score && kv_state && score_state),
+          "csa2_compress: ratio 2 needs score, kv_state and score_state");
+  REQUIRE(aligned16(kv) && aligned16(plane) && (!score || aligned16(score)) &&
+              (!kv_state || aligned16(kv_state)) && (!score_state || aligned16(score_state)) &&
+              (!norm_w || aligned16(norm_w)),
+          "csa2_compress: kv, score, plane, states and norm_w must be 16-byte aligned");
+  REQUIRE(eps >= 0.f && std::isfinite(eps), "csa2_compress: eps must be finite and >= 0");
+  REQUIRE(plane_rows >= 0, "csa2_compress: plane_rows must be >= 0");
+  csa2::CompressArgs a{kv, score, T, cu_seqlens, B, start_pos, ratio, kv_state, score_state,
+                       plane, plane_rows, row_base, norm_w, eps, inv_freq};
+  cudaError_t e = csa2::launch_compress(a, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "csa2_compress");
+  return CSA2_OK;
+}
+
+size_t csa2_index_topk_workspace_size(int Q, int H, int64_t max_scored, int k) {
+  (void)H;
+  if (Q < 0 || max_scored < 1 || k < 1 || k > 512) return 0;
+  return index_ws_layout(Q, max_scored, k).total;
+}
+
+csa2_status csa2_index_topk(const csa2_bf16* iq, const float* w, int Q, int H,
+                            const csa2_bf16* index_k, int64_t index_rows,
+                            const int64_t* row_base, const int32_t* q_seq, const int64_t* q_pos,
+                            int ratio, const int32_t* cand, int ncb, int k, int relu,
+                            int64_t max_scored, int32_t* sel, float* sel_scores,
+                            float* scores_out, void* ws, size_t ws_bytes, csa2_stream stream) {
+  REQUIRE(Q >= 0, "csa2_index_topk: Q must be >= 0 (got %d)", Q);
+  REQUIRE(H == 32 || H == 64, "csa2_index_topk: H must be 32 or 64 (got %d)", H);
+  REQUIRE(ratio == 1 || ratio == 2, "csa2_index_topk: ratio must be 1 or 2 (got %d)", ratio);
+  REQUIRE(k >= 1 && k <= 512, "csa2_index_topk: k must be in [1, 512] (got %d)", k);
+  REQUIRE(max_scored >= 1, "csa2_index_topk: max_scored must be >= 1");
+  if (cand) {
+    REQUIRE(ncb >= 1, "csa2_index_topk: ncb must be >= 1 with a candidate pool");
+    REQUIRE((int64_t)ncb * 8 >= k,
+            "csa2_index_topk: candidate pool of %d blocks x 8 rows cannot hold top-%d", ncb, k);
+    REQUIRE(max_scored == (int64_t)ncb * 8, "csa2_index_topk: REINDEX needs max_scored == ncb * 8");
+  }
+  REQUIRE(csa2::topk_num_chunks(max_scored) <= csa2::topk_max_chunks(),
+          "csa2_index_topk: max_scored %lld exceeds the supported %lld positions",
+          (long long)max_scored, (long long)csa2::topk_max_chunks() * 16384);
+  if (Q == 0) return CSA2_OK;
+  REQUIRE(iq && w && index_k && row_base && q_seq && q_pos && sel && ws,
+          "csa2_index_topk: iq, w, index_k, row_base, q_seq, q_pos, sel and ws are required");
+  REQUIRE(aligned16(iq) && aligned16(index_k), "csa2_index_topk: iq and index_k must be 16-byte aligned");
+  REQUIRE(index_rows >= 1 && index_rows < (int64_t)1 << 31, "csa2_index_topk: index_rows out of range");
+  REQUIRE((int64_t)Q * H < (int64_t)1 << 31, "csa2_index_topk: Q * H out of range");
+  REQUIRE((reinterpret_cast<uintptr_t>(ws) & 255u) == 0, "csa2_index_topk: ws must be 256-byte aligned");
+  const IndexWs L = index_ws_layout(Q, max_scored, k);
+  if (ws_bytes < L.total)
+    return fail(CSA2_ENOSPACE, "csa2_index_topk: workspace %zu bytes < required %zu", ws_bytes, L.total);
+  uint8_t* base = static_cast<uint8_t*>(ws);
+  csa2::IndexArgs a{};
+  a.iq = iq; a.w = w; a.Q = Q; a.H = H; a.index_k = index_k; a.index_rows = index_rows;
+  a.row_base = row_base; a.q_seq = q_seq; a.q_pos = q_pos; a.ratio = ratio; a.cand = cand;
+  a.ncb = cand ? ncb : 0; a.relu = relu ? 1 : 0; a.ld = max_scored; a.scores_out = scores_out;
+  a.keys = reinterpret_cast<uint32_t*>(base + L.keys);
+  a.n_scored = reinterpret_cast<int32_t*>(base + L.n_scored);
+  a.grp_q0 = reinterpret_cast<int32_t*>(base + L.grp_q0);
+  a.grp_nq = reinterpret_cast<int32_t*>(base + L.grp_nq);
+  a.tmp = reinterpret_cast<int32_t*>(base + L.tmp);
+  a.grp_tile0 = reinterpret_cast<int64_t*>(base + L.grp_tile0);
+  a.n_groups = reinterpret_cast<int32_t*>(base + L.n_groups);
+  a.group_max = cand ? 1 : 256 / H;
+  const int sms = num_sms();
+  if (sms <= 0) return fail(CSA2_ECUDA, "csa2_index_topk: no CUDA device");
+  cudaError_t e = csa2::launch_index(a, sms, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "csa2_index_topk (scores)");
+  csa2::TopkArgs t{};
+  t.keys = a.keys; t.scores = nullptr; t.n = a.n_scored; t.Q = Q; t.ld = max_scored; t.k = k;
+  t.cand = cand; t.ncb = a.ncb; t.sel = sel; t.sel_scores = sel_scores;
+  t.part = reinterpret_cast<uint64_t*>(base + L.part); t.nchunk = L.nchunk;
+  e = csa2::launch_topk(t, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "csa2_index_topk (top-k)");
+  return CSA2_OK;
+}
+
+size_t csa2_topk_workspace_size(int Q, int64_t ld, int k) {
+  if (Q < 0 || ld < 1 || k < 1 || k > 512) return 0;
+  return topk_ws_bytes(Q, ld, k);
+}
+
+csa2_status csa2_topk_scores(const float* scores, const int32_t* n, int Q, int64_t ld, int k,
+                             int32_t* sel, float* sel_scores, void* ws, size_t ws_bytes,
+                             csa2_stream stream) {
+  REQUIRE(Q >= 0, "csa2_topk_scores: Q must be >= 0");
+  REQUIRE(k >= 1 && k <= 512, "csa2_topk_scores: k must be in [1, 512] (got %d)", k);
+  REQUIRE(ld >= 1, "csa2_topk_scores: ld must be >= 1");
+  REQUIRE(csa2::topk_num_chunks(ld) <= csa2::topk_max_chunks(),
+          "csa2_topk_scores: ld %lld exceeds the supported length", (long long)ld);
+  if (Q == 0) return CSA2_OK;
+  REQUIRE(scores && n && sel, "csa2_topk_scores: scores, n and sel are required");
+  const size_t need = topk_ws_bytes(Q, ld, k);
+  if (need) {
+    REQUIRE(ws && (reinterpret_cast<uintptr_t>(ws) & 255u) == 0,
+            "csa2_topk_scores: ws must be a 256-byte aligned pointer");
+    if (ws_bytes < need)
+      return fail(CSA2_ENOSPACE, "csa2_topk_scores: workspace %zu bytes < required %zu", ws_bytes, need);
+  }
+  csa2::TopkArgs t{};
+  t.keys = nullptr; t.scores = scores; t.n = n; t.Q = Q; t.ld = ld; t.k = k; t.cand = nullptr;
+  t.ncb = 0; t.sel = sel; t.sel_scores = sel_scores; t.part = static_cast<uint64_t*>(ws);
+  t.nchunk = csa2::topk_num_chunks(ld);
+  cudaError_t e = csa2::launch_topk(t, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "csa2_topk_scores");
+  return CSA2_OK;
+}
+
+csa2_status csa2_sparse_attn(const csa2_bf16* q, int Q, const int32_t* q_seq,
+                             const int64_t* q_pos, const csa2_swa* swa, const csa2_bf16* plane,
+                             int64_t plane_rows, const int64_t* row_base, const int32_t* sel,
+                             int nsel, const float* sink, float scale, csa2_bf16* out, float* lse,
+                             csa2_stream stream) {
+  return attn_common("csa2_sparse_attn", q, Q, q_seq, q_pos, swa, plane, plane_rows, row_base,
+                     sel, nsel, sink, scale, out, lse, stream);
+}
+
+csa2_status csa2_reuse_attn(const csa2_bf16* q, int Q, const int32_t* q_seq,
+                            const int64_t* q_pos, const csa2_swa* swa, const csa2_bf16* plane,
+                            int64_t plane_rows, const int64_t* row_base, const int32_t* sel,
+                            int nsel, const float* sink, float scale, csa2_bf16* out, float* lse,
+                            csa2_stream stream) {
+  return attn_common("csa2_reuse_attn", q, Q, q_seq, q_pos, swa, plane, plane_rows, row_base,
+                     sel, nsel, sink, scale, out, lse, stream);
+}
+
+}  // extern "C"

@@ -1,0 +1,189 @@
+// k_compress.cu -- the CSA2 compressor: softmax-gated pooling of m (1 or 2) tokens
+// per row, RMSNorm over the 512 dims, partial RoPE on dims 448..511 at the group's
+// first position, bf16 store; the odd tail is kept in the per-sequence fp32 state.
+// [A] "特殊模块 · compressor" and "CSA2 的池化比 V4 简单一截"; [B] §4.1, §6.1-6.2;
+// [C] §6.2 (tail state), §6.4 (ratio 1 degenerates to projection + norm).
+//
+// One warp per new token.  The warp of a token that closes a group (pos % m == m-1)
+// emits that group's row; the group's earlier tokens come from this call's input
+// or, for the first group of a sequence, from the state.  The warp of the first
+// token of each sequence additionally stores the tokens of a group left incomplete
+// at the end of the call into the state.  With m <= 2 that warp is also the only
+// reader of the state, so state reads precede state writes within one warp.
+//
+// Lane layout: lane l owns channels [8l, 8l+8) and [256+8l, 256+8l+8), i.e. two
+// 16-byte vectors per row (coalesced 1 KiB row accesses).  Lanes 24..31 hold the
+// RoPE dims 448..511 in their second vector, four adjacent pairs each.
+#include "common.cuh"
+
+CSA2_DEFINE_FAULT_FLAG(compress)
+
+namespace csa2 {
+namespace {
+
+constexpr int kWarps = 8;
+
+__device__ __forceinline__ void load8_bf16(const uint16_t* p, float (&v)[8]) {
+  uint4 u = *reinterpret_cast<const uint4*>(p);
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    v[2 * i] = __uint_as_float(w[i] << 16);
+    v[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+  }
+}
+
+__device__ __forceinline__ void load8_f32(const float* p, float (&v)[8]) {
+  float4 a = *reinterpret_cast<const float4*>(p);
+  float4 b = *reinterpret_cast<const float4*>(p + 4);
+  v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+  v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+}
+
+__device__ __forceinline__ void store8_f32(float* p, const float (&v)[8]) {
+  *reinterpret_cast<float4*>(p) = make_float4(v[0], v[1], v[2], v[3]);
+  *reinterpret_cast<float4*>(p + 4) = make_float4(v[4], v[5], v[6], v[7]);
+}
+
+__device__ __forceinline__ void store8_bf16(uint16_t* p, const float (&v)[8]) {
+  uint4 u;
+  u.x = pack_bf16x2(v[0], v[1]);
+  u.y = pack_bf16x2(v[2], v[3]);
+  u.z = pack_bf16x2(v[4], v[5]);
+  u.w = pack_bf16x2(v[6], v[7]);
+  *reinterpret_cast<uint4*>(p) = u;
+}
+
+// Fetch channels (c0..c0+7) of the token at position `pos` of sequence b: from the
+// input when it arrived in this call, else from the state slot pos % m.
+__device__ __forceinline__ void fetch(const CompressArgs& a, int b, int64_t pos, int64_t s0,
+                                      int64_t t0, int c0, float (&kv)[8], float (&sc)[8]) {
+  if (pos >= s0) {
+    int64_t t = t0 + (pos - s0);
+    load8_bf16(a.kv + t * kDLat + c0, kv);
+    if (a.score) load8_bf16(a.score + t * kDLat + c0, sc);
+    else
+#pragma unroll
+      for (int i = 0; i < 8; ++i) sc[i] = 0.f;
+  } else {
+    int slot = (int)(pos % a.ratio);
+    load8_f32(a.kv_state + ((int64_t)b * 2 + slot) * kDLat + c0, kv);
+    load8_f32(a.score_state + ((int64_t)b * 2 + slot) * kDLat + c0, sc);
+  }
+}
+
+__global__ void __launch_bounds__(kWarps * 32) compress_kernel(CompressArgs a) {
+  const int lane = threadIdx.x & 31;
+  const int64_t t = (int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5);
+  if (t >= a.T) return;
+  // sequence of token t: last b with cu_seqlens[b] <= t
+  int lo = 0, hi = a.B - 1;
+  while (lo < hi) {
+    int mid = (lo + hi + 1) >> 1;
+    if (a.cu_seqlens[mid] <= t) lo = mid; else hi = mid - 1;
+  }
+  const int b = lo;
+  const int64_t t0 = a.cu_seqlens[b];
+  const int64_t t1 = a.cu_seqlens[b + 1];
+  const int64_t s0 = a.start_pos[b];
+  const int64_t pos = s0 + (t - t0);
+  const int m = a.ratio;
+  const int c[2] = {8 * lane, 256 + 8 * lane};
+
+  // ---- emit the row of a group that this token closes ----
+  if (pos % m == m - 1) {
+    const int64_t j = pos / m;
+    float r[2][8];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      if (m == 1) {
+        float kv[8], sc[8];
+        fetch(a, b, pos, s0, t0, c[h], kv, sc);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) r[h][i] = kv[i];
+      } else {
+        float k0[8], q0[8], k1[8], q1[8];
+        fetch(a, b, pos - 1, s0, t0, c[h], k0, q0);
+        fetch(a, b, pos, s0, t0, c[h], k1, q1);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {  // per-channel softmax over the two slots
+          float mx = fmaxf(q0[i], q1[i]);
+          float e0 = expf(q0[i] - mx), e1 = expf(q1[i] - mx);
+          r[h][i] = (e0 * k0[i] + e1 * k1[i]) / (e0 + e1);
+        }
+      }
+    }
+    float ss = 0.f;
+#pragma unroll
+    for (int h = 0; h < 2; ++h)
+#pragma unroll
+      for (int i = 0; i < 8; ++i) ss += r[h][i] * r[h][i];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xFFFFFFFFu, ss, o);
+    const float rstd = 1.0f / sqrtf(ss / (float)kDLat + a.eps);
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      float wv[8];
+      if (a.norm_w) load8_f32(a.norm_w + c[h], wv);
+      else
+#pragma unroll
+        for (int i = 0; i < 8; ++i) wv[i] = 1.f;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) r[h][i] = r[h][i] * rstd * wv[i];
+    }
+    if (lane >= 24) {  // dims 448 + 8(lane-24) .. +7: four rotation pairs
+      const double p0 = (double)(j * m);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int pair = 4 * (lane - 24) + k;
+        double sn, cs;
+        sincos(p0 * (double)a.inv_freq[pair], &sn, &cs);
+        const float fc = (float)cs, fs = (float)sn;
+        const float x0 = r[1][2 * k], x1 = r[1][2 * k + 1];
+        r[1][2 * k] = x0 * fc - x1 * fs;
+        r[1][2 * k + 1] = x0 * fs + x1 * fc;
+      }
+    }
+    const int64_t row = a.row_base[b] + j;
+    if (row < 0 || row >= a.plane_rows) {
+      if (lane == 0) raise_fault(kFaultBounds);
+    } else {
+      store8_bf16(a.plane + row * kDLat + c[0], r[0]);
+      store8_bf16(a.plane + row * kDLat + c[1], r[1]);
+    }
+  }
+
+  // ---- first token of the sequence: keep an incomplete trailing group ----
+  if (t == t0 && m > 1) {
+    const int64_t last = s0 + (t1 - t0) - 1;
+    if (last % m != m - 1) {
+      for (int64_t p = (last / m) * m; p <= last; ++p) {
+        if (p < s0) continue;  // already in the state from an earlier call
+        const int64_t tp = t0 + (p - s0);
+        const int slot = (int)(p % m);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          float kv[8], sc[8];
+          load8_bf16(a.kv + tp * kDLat + c[h], kv);
+          if (a.score) load8_bf16(a.score + tp * kDLat + c[h], sc);
+          else
+#pragma unroll
+            for (int i = 0; i < 8; ++i) sc[i] = 0.f;
+          store8_f32(a.kv_state + ((int64_t)b * 2 + slot) * kDLat + c[h], kv);
+          store8_f32(a.score_state + ((int64_t)b * 2 + slot) * kDLat + c[h], sc);
+        }
+      }
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_compress(const CompressArgs& a, cudaStream_t s) {
+  if (a.T == 0) return cudaSuccess;
+  const int grid = (a.T + kWarps - 1) / kWarps;
+  compress_kernel<<<grid, kWarps * 32, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace csa2

@@ -1,0 +1,446 @@
+// k_index.cu -- lightning-indexer scores on tcgen05 tensor cores.
+// [A] "特殊模块 · indexer" Fig. 3b: logits[r, c] = sum_h w[r,h] * <q[r,h], k[c]> scaled by
+// head_dim^-1/2 * n_heads^-1/2, each row scored only up to its own visible prefix;
+// [C] A.15.2: ReLU on each head's dot product, candidates gathered before scoring;
+// [A] Fig. 2c: REINDEX scores only the 2048 candidate blocks x 8 rows.
+//
+// Formulation (per work tile of 128 index rows and one query group):
+//     S^T[128 rows x N] = K_tile[128 x 128] . Qg^T[128 x N],   N = nq * H <= 256
+// with the index rows on the M side, so TMEM lane r holds every head score of row
+// r and the ReLU, the head weights and the head sum are thread-local in the
+// epilogue.  A query group is up to 256/H consecutive queries of one sequence
+// (prefill); they share the K tile, which is then read once for all of them.
+//
+// Persistent CTA, one per SM, warp-specialised:
+//   warp 0      TMA producer: K tiles (4-stage ring) and the group's Q block
+//   warp 1      TMEM allocation; lane 0 issues the MMAs (8 x K=16 per tile)
+//   warps 2..5  epilogue: TMEM -> relu * w -> sum -> order-preserving key
+// TMEM holds two 256-column fp32 accumulators so the epilogue of tile i overlaps
+// the MMAs of tile i+1.  The scores are written as uint32 keys for the top-k.
+#include <cudaTypedefs.h>
+
+#include "common.cuh"
+
+CSA2_DEFINE_FAULT_FLAG(index)
+
+namespace csa2 {
+namespace {
+
+constexpr int kStages = 4;
+constexpr int kTileRows = 128;
+constexpr int kThreads = 192;
+constexpr int kStageBytes = kTileRows * kDIdx * 2;  // 32 KiB: two 64-dim blocks
+constexpr int kBBytes = 2 * 256 * 128;              // 64 KiB: two 64-dim blocks x 256 rows
+constexpr int kMaxGroup = 8;
+
+struct __align__(8) Bars {
+  uint64_t full[kStages];
+  uint64_t empty[kStages];
+  uint64_t acc_full[2];
+  uint64_t acc_empty[2];
+  uint64_t b_full;
+  uint64_t b_empty;
+};
+
+struct GroupInfo {
+  int q0, nq, seq;
+  int64_t tile0, tile1;
+};
+
+__device__ __forceinline__ int64_t n_visible(int64_t pos, int ratio) { return (pos + 1) / ratio; }
+
+// ---- prep: scored counts, query groups, tile prefix ---------------------------------
+constexpr int kPrepThreads = 1024;
+
+__device__ int block_excl_sum(int v, int* red, int& total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int incl = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    int t = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+    if (lane >= o) incl += t;
+  }
+  if (lane == 31) red[warp] = incl;
+  __syncthreads();
+  int base = 0, tot = 0;
+  for (int w = 0; w < kPrepThreads / 32; ++w) {
+    if (w < warp) base += red[w];
+    tot += red[w];
+  }
+  __syncthreads();
+  total = tot;
+  return base + incl - v;
+}
+
+__global__ void __launch_bounds__(kPrepThreads) index_prep_kernel(IndexArgs a, int32_t* tmp) {
+  __shared__ int red[kPrepThreads / 32];
+  __shared__ int carry_run;
+  __shared__ int carry_groups;
+  __shared__ long long carry_tiles;
+  const int tid = threadIdx.x;
+  if (tid == 0) { carry_run = 0; carry_groups = 0; carry_tiles = 0; }
+  __syncthreads();
+  // pass 1: scored positions per query and group-start flags
+  for (int base = 0; base < a.Q; base += kPrepThreads) {
+    const int q = base + tid;
+    int start = 0;
+    if (q < a.Q) {
+      int64_t ns;
+      if (a.cand) ns = (int64_t)a.ncb * 8;
+      else {
+        ns = n_visible(a.q_pos[q], a.ratio);
+        if (ns > a.ld) { raise_fault(kFaultBounds); ns = a.ld; }
+      }
+      a.n_scored[q] = (int32_t)ns;
+      start = (q == 0 || a.q_seq[q] != a.q_seq[q - 1]) ? q : -1;
+    } else {
+      start = -1;
+    }
+    // inclusive max-scan of run starts
+    int v = start;
+    const int lane = tid & 31, warp = tid >> 5;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      int t = __shfl_up_sync(0xFFFFFFFFu, v, o);
+      if (lane >= o) v = max(v, t);
+    }
+    if (lane == 31) red[warp] = v;
+    __syncthreads();
+    int pre = carry_run;
+    for (int w = 0; w < warp; ++w) pre = max(pre, red[w]);
+    const int rs = max(pre, v);
+    __syncthreads();
+    if (tid == kPrepThreads - 1) carry_run = rs;
+    if (q < a.Q) tmp[q] = ((q - rs) % a.group_max) == 0 ? 1 : 0;
+    __syncthreads();
+  }
+  // pass 2: group ids, members and tile counts
+  for (int base = 0; base < a.Q; base += kPrepThreads) {
+    const int q = base + tid;
+    const int f = q < a.Q ? tmp[q] : 0;
+    int total;
+    const int g = carry_groups + block_excl_sum(f, red, total);
+    if (f) {
+      int nq = 1;
+      int64_t mx = a.n_scored[q];
+      while (nq < a.group_max && q + nq < a.Q && a.q_seq[q + nq] == a.q_seq[q] &&
+             tmp[q + nq] == 0) {
+        mx = max(mx, (int64_t)a.n_scored[q + nq]);
+        ++nq;
+      }
+      a.grp_q0[g] = q;
+      a.grp_nq[g] = nq;
+      a.grp_tile0[g] = (mx + kTileRows - 1) / kTileRows;  // count for now
+    }
+    __syncthreads();
+    if (tid == 0) carry_groups += total;
+    __syncthreads();
+  }
+  const int ng = carry_groups;
+  // pass 3: exclusive prefix of tile counts (in place), total at [ng]
+  for (int base = 0; base < ng; base += kPrepThreads) {
+    const int g = base + tid;
+    const int64_t c = g < ng ? a.grp_tile0[g] : 0;
+    // 64-bit scan through two 32-bit halves is unnecessary: counts fit in int
+    int total;
+    const int ex = block_excl_sum((int)c, red, total);
+    if (g < ng) a.grp_tile0[g] = carry_tiles + ex;
+    __syncthreads();
+    if (tid == 0) carry_tiles += total;
+    __syncthreads();
+  }
+  if (tid == 0) {
+    a.grp_tile0[ng] = carry_tiles;
+    *a.n_groups = ng;
+  }
+}
+
+// ---- main kernel -----------------------------------------------------------------------
+
+__device__ __forceinline__ void load_group(const IndexArgs& a, int g, GroupInfo& gi) {
+  gi.q0 = a.grp_q0[g];
+  gi.nq = a.grp_nq[g];
+  gi.seq = a.q_seq[gi.q0];
+  gi.tile0 = a.grp_tile0[g];
+  gi.tile1 = a.grp_tile0[g + 1];
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    index_score_kernel(IndexArgs a, const __grid_constant__ CUtensorMap kmap_tile,
+                       const __grid_constant__ CUtensorMap kmap_blk,
+                       const __grid_constant__ CUtensorMap qmap) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  uint8_t* a_smem = smem;                              // kStages x 32 KiB
+  uint8_t* b_smem = smem + kStages * kStageBytes;      // 64 KiB
+  float* w_s = reinterpret_cast<float*>(b_smem + kBBytes);  // [256]
+  Bars* bars = reinterpret_cast<Bars*>(w_s + 256);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  int64_t* gq = reinterpret_cast<int64_t*>(tmem_slot + 4);  // [kMaxGroup] n_visible
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int ng = *a.n_groups;
+  const int64_t total = a.grp_tile0[ng];
+  const int64_t per = (total + gridDim.x - 1) / gridDim.x;
+  const int64_t it_lo = (int64_t)blockIdx.x * per;
+  const int64_t it_hi = min(total, it_lo + per);
+  if (it_lo >= it_hi) return;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(smem_u32(&bars->full[s]), 1);
+      mbar_init(smem_u32(&bars->empty[s]), 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(smem_u32(&bars->acc_full[s]), 1);
+      mbar_init(smem_u32(&bars->acc_empty[s]), 4);
+    }
+    mbar_init(smem_u32(&bars->b_full), 1);
+    mbar_init(smem_u32(&bars->b_empty), 1);
+    *abort_flag = 0;
+    mbar_fence_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  // first group of this CTA's range: last g with grp_tile0[g] <= it_lo
+  int g_first;
+  {
+    int lo = 0, hi = ng - 1;
+    while (lo < hi) {
+      int mid = (lo + hi + 1) >> 1;
+      if (a.grp_tile0[mid] <= it_lo) lo = mid; else hi = mid - 1;
+    }
+    g_first = lo;
+  }
+  const float alpha = rsqrtf((float)kDIdx) * rsqrtf((float)a.H);
+
+  if (warp == 0) {
+    // ===================== TMA producer =====================
+    if (lane == 0) {
+      prefetch_tensormap(&kmap_tile);
+      prefetch_tensormap(&kmap_blk);
+      prefetch_tensormap(&qmap);
+      const uint64_t pol_k = policy_evict_first();
+      const uint64_t pol_q = policy_evict_last();
+      GroupInfo gi;
+      int g = g_first - 1;
+      gi.tile1 = -1;
+      int u = 0;  // groups loaded
+      int64_t issued[kStages];
+      for (int s = 0; s < kStages; ++s) issued[s] = -1;
+      for (int64_t it = it_lo; it < it_hi; ++it) {
+        if (*abort_flag) break;
+        while (it >= gi.tile1) {
+          ++g;
+          load_group(a, g, gi);
+        }
+        if (it == it_lo || it == gi.tile0) {  // new group: load its Q block
+          if (u > 0 && !mbar_wait(smem_u32(&bars->b_empty), (u - 1) & 1)) { *abort_flag = 1; break; }
+          const uint32_t bb = smem_u32(&bars->b_full);
+          mbar_arrive_expect_tx(bb, (uint32_t)(gi.nq * a.H * kDIdx * 2));
+          for (int i = 0; i < gi.nq; ++i)
+            for (int db = 0; db < 2; ++db)
+              tma_load_2d(smem_u32(b_smem + db * 32768 + i * a.H * 128), &qmap, db * 64,
+                          (gi.q0 + i) * a.H, bb, pol_q);
+          ++u;
+        }
+        const int64_t k = it - it_lo;
+        const int s = (int)(k % kStages);
+        const uint32_t round = (uint32_t)(k / kStages);
+        if (!mbar_wait(smem_u32(&bars->empty[s]), (round & 1) ^ 1)) { *abort_flag = 1; break; }
+        const uint32_t fb = smem_u32(&bars->full[s]);
+        mbar_arrive_expect_tx(fb, kStageBytes);
+        issued[s] = round;
+        const int64_t tile = it - gi.tile0;
+        const int64_t rb = a.row_base[gi.seq];
+        uint8_t* dst = a_smem + s * kStageBytes;
+        if (!a.cand) {
+          const int32_t y = (int32_t)(rb + tile * kTileRows);
+          for (int db = 0; db < 2; ++db)
+            tma_load_2d(smem_u32(dst + db * 16384), &kmap_tile, db * 64, y, fb, pol_k);
+        } else {
+          const int32_t* cb = a.cand + (int64_t)gi.q0 * a.ncb + tile * 16;
+          for (int i = 0; i < 16; ++i) {
+            const int32_t blk = cb[i];
+            const int32_t y = (int32_t)(rb + (blk >= 0 ? (int64_t)blk * 8 : 0));
+            for (int db = 0; db < 2; ++db)
+              tma_load_2d(smem_u32(dst + db * 16384 + i * 1024), &kmap_blk, db * 64, y, fb, pol_k);
+          }
+        }
+      }
+      // do not leave the CTA with copies still landing in shared memory
+      for (int s = 0; s < kStages; ++s)
+        if (issued[s] >= 0) mbar_wait(smem_u32(&bars->full[s]), (uint32_t)(issued[s] & 1),
+                                      100000000ull);
+      if (u > 0) mbar_wait(smem_u32(&bars->b_full), (u - 1) & 1, 100000000ull);
+    }
+  } else if (warp == 1) {
+    // ===================== MMA issuer =====================
+    if (lane == 0) {
+      GroupInfo gi;
+      int g = g_first - 1;
+      gi.tile1 = -1;
+      int u = 0;
+      uint32_t idesc = 0;
+      for (int64_t it = it_lo; it < it_hi; ++it) {
+        if (*abort_flag) break;
+        while (it >= gi.tile1) {
+          ++g;
+          load_group(a, g, gi);
+        }
+        if (it == it_lo || it == gi.tile0) {
+          if (!mbar_wait(smem_u32(&bars->b_full), u & 1)) { *abort_flag = 1; break; }
+          ++u;
+          idesc = idesc_bf16(128, gi.nq * a.H, 0, 0);
+        }
+        const int64_t k = it - it_lo;
+        const int s = (int)(k % kStages);
+        const uint32_t round = (uint32_t)(k / kStages);
+        const int ab = (int)(k & 1);
+        const uint32_t use = (uint32_t)(k >> 1);
+        if (!mbar_wait(smem_u32(&bars->full[s]), round & 1)) { *abort_flag = 1; break; }
+        if (!mbar_wait(smem_u32(&bars->acc_empty[ab]), (use & 1) ^ 1)) { *abort_flag = 1; break; }
+        tc_fence_after();
+        const uint32_t a_base = smem_u32(a_smem + s * kStageBytes);
+        const uint32_t b_base = smem_u32(b_smem);
+        const uint32_t d = tmem + (uint32_t)(ab * 256);
+#pragma unroll
+        for (int db = 0; db < 2; ++db)
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            const uint64_t ad = sdesc_sw128(a_base + db * 16384 + kk * 32, 16, 1024);
+            const uint64_t bd = sdesc_sw128(b_base + db * 32768 + kk * 32, 16, 1024);
+            umma_bf16(d, ad, bd, idesc, (db | kk) != 0);
+          }
+        umma_commit(smem_u32(&bars->empty[s]));
+        umma_commit(smem_u32(&bars->acc_full[ab]));
+        if (it + 1 == it_hi || it + 1 == gi.tile1) umma_commit(smem_u32(&bars->b_empty));
+      }
+    }
+  } else {
+    // ===================== epilogue (warps 2..5) =====================
+    const int sub = warp & 3;             // TMEM sub-partition of this warp
+    const int r = sub * 32 + lane;        // tile row = TMEM lane
+    GroupInfo gi;
+    int g = g_first - 1;
+    gi.tile1 = -1;
+    for (int64_t it = it_lo; it < it_hi; ++it) {
+      if (*abort_flag) break;
+      while (it >= gi.tile1) {
+        ++g;
+        load_group(a, g, gi);
+      }
+      if (it == it_lo || it == gi.tile0) {
+        asm volatile("bar.sync 1, 128;" ::: "memory");
+        const int nw = gi.nq * a.H;
+        for (int i = threadIdx.x - 64; i < nw; i += 128)
+          w_s[i] = a.w[(int64_t)gi.q0 * a.H + i] * alpha;
+        if (threadIdx.x - 64 < gi.nq) gq[threadIdx.x - 64] = n_visible(a.q_pos[gi.q0 + threadIdx.x - 64], a.ratio);
+        asm volatile("bar.sync 1, 128;" ::: "memory");
+      }
+      const int64_t k = it - it_lo;
+      const int ab = (int)(k & 1);
+      const uint32_t use = (uint32_t)(k >> 1);
+      if (!mbar_wait(smem_u32(&bars->acc_full[ab]), use & 1)) { *abort_flag = 1; break; }
+      tc_fence_after();
+      const int64_t tile = it - gi.tile0;
+      const int64_t pos = tile * kTileRows + r;
+      const uint32_t tbase = tmem + ((uint32_t)(sub * 32) << 16) + (uint32_t)(ab * 256);
+      for (int i = 0; i < gi.nq; ++i) {
+        float acc = 0.f;
+        for (int c = 0; c < a.H; c += 32) {
+          uint32_t v[32];
+          tmem_ld32(tbase + (uint32_t)(i * a.H + c), v);
+          tmem_ld_wait();
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            float x = __uint_as_float(v[j]);
+            if (a.relu) x = fmaxf(x, 0.f);
+            acc = fmaf(w_s[i * a.H + c + j], x, acc);
+          }
+        }
+        const int q = gi.q0 + i;
+        bool valid;
+        if (!a.cand) {
+          valid = pos < (int64_t)a.n_scored[q];
+        } else {
+          const int32_t blk = a.cand[(int64_t)q * a.ncb + (pos >> 3)];
+          valid = blk >= 0 && (int64_t)blk * 8 + (pos & 7) < gq[i];
+        }
+        if (pos < a.ld) {
+          a.keys[(int64_t)q * a.ld + pos] = valid ? score_key(acc) : 0u;
+          if (valid && a.scores_out) a.scores_out[(int64_t)q * a.ld + pos] = acc;
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&bars->acc_empty[ab]));
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem, 512);
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult qr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &qr) == cudaSuccess &&
+        qr == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint32_t box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)kDIdx, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)kDIdx * 2};
+  cuuint32_t box[2] = {64, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+size_t index_smem_bytes() {
+  return 1024 + kStages * kStageBytes + kBBytes + 256 * 4 + sizeof(Bars) + 16 + 8 * kMaxGroup;
+}
+
+cudaError_t launch_index(const IndexArgs& a, int num_sms, cudaStream_t s) {
+  if (a.Q == 0) return cudaSuccess;
+  index_prep_kernel<<<1, kPrepThreads, 0, s>>>(a, a.tmp);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  CUtensorMap kt, kb, qm;
+  if (!make_map(&kt, a.index_k, (uint64_t)a.index_rows, kTileRows) ||
+      !make_map(&kb, a.index_k, (uint64_t)a.index_rows, 8) ||
+      !make_map(&qm, a.iq, (uint64_t)a.Q * a.H, (uint32_t)a.H))
+    return cudaErrorInvalidValue;
+  const size_t smem = index_smem_bytes();
+  e = cudaFuncSetAttribute(index_score_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)smem);
+  if (e != cudaSuccess) return e;
+  index_score_kernel<<<num_sms, kThreads, smem, s>>>(a, kt, kb, qm);
+  return cudaGetLastError();
+}
+
+}  // namespace csa2

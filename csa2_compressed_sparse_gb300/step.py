@@ -1,0 +1,91 @@
+"""One CSA2 attention step over resident device tensors, through the C ABI.
+
+A step is: compress the new tokens -> index + top-k (FULL or REINDEX) -> sparse
+attention for the scoring layer -> REUSE attention for the following layers of the
+index group (same selection, each layer with its own q and window).
+"""
+from dataclasses import dataclass, field
+from typing import List, Optional
+
+import torch
+
+from . import (Swa, SWA_LINEAR, SWA_RING, csa2_compress, csa2_index_topk,
+               csa2_index_topk_workspace_size, csa2_reuse_attn, csa2_sparse_attn)
+
+
+@dataclass
+class StepSpec:
+    ratio: int
+    H: int = 64
+    k: int = 512
+    max_scored: int = 0          # FULL: >= max visible rows; REINDEX: ncb * 8
+    swa_mode: int = SWA_RING
+    scale: float = 512 ** -0.5
+    eps: float = 1e-6
+    relu: bool = True
+
+
+@dataclass
+class StepBuffers:
+    sel: torch.Tensor
+    sel_scores: Optional[torch.Tensor]
+    out: List[torch.Tensor]
+    lse: List[Optional[torch.Tensor]]
+    ws: torch.Tensor
+    scores_out: Optional[torch.Tensor] = None
+    launches: int = 0
+
+
+def allocate(spec: StepSpec, t, want_scores=False, want_lse=False) -> StepBuffers:
+    dev = t["iq"].device
+    Q = t["iq"].shape[0]
+    layers = len(t["q"])
+    ws_bytes = csa2_index_topk_workspace_size(Q, spec.H, spec.max_scored, spec.k)
+    ws = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=dev)
+    return StepBuffers(
+        sel=torch.empty((Q, spec.k), dtype=torch.int32, device=dev),
+        sel_scores=torch.empty((Q, spec.k), dtype=torch.float32, device=dev),
+        out=[torch.empty((Q, 64, 512), dtype=torch.bfloat16, device=dev) for _ in range(layers)],
+        lse=[torch.empty((Q, 64), dtype=torch.float32, device=dev) if want_lse else None
+             for _ in range(layers)],
+        ws=ws,
+        scores_out=(torch.full((Q, spec.max_scored), float("nan"), dtype=torch.float32,
+                               device=dev) if want_scores else None),
+    )
+
+
+def swa_of(spec: StepSpec, t, layer):
+    if spec.swa_mode == SWA_LINEAR:
+        return Swa(t["swa"][layer], SWA_LINEAR, t["lin_base"], t["lin_pos0"])
+    return Swa(t["swa"][layer], SWA_RING)
+
+
+def kernel_launches(spec: StepSpec, t) -> int:
+    """Kernels one step launches (compress, index prep + scores, top-k, attention)."""
+    from . import lib  # noqa: F401  (library must be loaded)
+    n = 0
+    if t["kv"].shape[0]:
+        n += 1
+    Q = t["iq"].shape[0]
+    if Q:
+        n += 2  # prep + score kernel
+        nchunk = (spec.max_scored + 16383) // 16384
+        n += 1 if nchunk == 1 else 2
+        n += len(t["q"])
+    return n
+
+
+def run_step(spec: StepSpec, t, buf: StepBuffers, stream=None, compress=True):
+    if compress and t["kv"].shape[0]:
+        csa2_compress(t["kv"], t["score"], t["cu_seqlens"], t["start_pos"], spec.ratio,
+                      t["kv_state"], t["score_state"], t["plane"], t["row_base"], t["inv_freq"],
+                      eps=spec.eps, stream=stream)
+    csa2_index_topk(t["iq"], t["w"], t["index_k"], t["row_base"], t["q_seq"], t["q_pos"],
+                    spec.ratio, spec.k, spec.max_scored, buf.sel, buf.ws,
+                    sel_scores=buf.sel_scores, cand=t.get("cand"), relu=spec.relu,
+                    scores_out=buf.scores_out, stream=stream)
+    for layer in range(len(t["q"])):
+        fn = csa2_sparse_attn if layer == 0 else csa2_reuse_attn
+        fn(t["q"][layer], t["q_seq"], t["q_pos"], swa_of(spec, t, layer), t["plane"],
+           t["row_base"], buf.sel, t["sink"], buf.out[layer], lse=buf.lse[layer],
+           scale=spec.scale, stream=stream)

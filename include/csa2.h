@@ -1,0 +1,208 @@
+/*
+ * csa2.h -- C ABI of the CSA2 compressed-sparse attention step on one GB300 (sm_103a).
+ *
+ * The step, as the source pages state it (DeepSeek-V4.1-Flash CSA2 attention):
+ *   compress     -> pool each group of m (1 or 2) new tokens into one 512-d row
+ *   index_topk   -> lightning-indexer scores over the visible rows (or over a
+ *                   candidate pool), then the 512 best rows
+ *   sparse_attn  -> 64-head single-KV-head attention over the 128-position window
+ *                   plus the selected rows, one softmax with a per-head sink
+ *   reuse_attn   -> the same attention with a selection taken from another layer
+ *
+ * Conventions (every entry point):
+ *   - Every pointer argument is a DEVICE pointer unless its comment says HOST.  The
+ *     caller owns every buffer; the library allocates no device memory.  Scratch
+ *     memory is caller-provided through the *_workspace_size queries.
+ *   - Work is enqueued asynchronously on `stream` (a cudaStream_t; NULL = the legacy
+ *     default stream).  No call synchronises except csa2_device_status().
+ *   - Argument errors are detected on the host before anything is launched and
+ *     return CSA2_EINVAL.  CUDA launch failures return CSA2_ECUDA.  The text of the
+ *     last failure on the calling thread is available from csa2_last_error().
+ *   - Data-dependent faults found by the kernels (an index outside its buffer, a
+ *     wait that ran past its time limit) skip the offending access and raise a
+ *     device-side flag; csa2_device_status() reports and clears it.
+ *   - Row ids in `sel`/`cand` are sequence-local; -1 marks an empty entry.  bf16
+ *     tensors are raw 16-bit patterns (csa2_bf16).  Layouts are row-major, dense.
+ *   - Base addresses must be 16-byte aligned; the library checks this.
+ *
+ * Page references ("section" names are the pages' own headings):
+ *   [A] "DeepSeek-V4.1-Flash 架构解剖" (perryzhang01.github.io, v41_flash_anatomy)
+ *   [B] "DeepSeek-V4.1-Flash 结构说明" (treert.github.io, ds-v4-1-flash-structure)
+ *   [C] "万字长文解析DeekSeekV4.1flash" (yuyanqi.com)
+ *   [E] "DeepSeek-V4-Pro 架构解剖" (perryzhang01.github.io, v4_pro_anatomy)
+ */
+#ifndef CSA2_H
+#define CSA2_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  CSA2_OK = 0,
+  CSA2_EINVAL = 1,   /* invalid argument; nothing was enqueued */
+  CSA2_ECUDA = 2,    /* a CUDA runtime call failed */
+  CSA2_ETIMEOUT = 3, /* a kernel gave up a bounded wait (from csa2_device_status) */
+  CSA2_EBOUNDS = 4,  /* a kernel met an index outside its buffer (from csa2_device_status) */
+  CSA2_ENOSPACE = 5  /* the workspace is smaller than the size query returned */
+} csa2_status;
+
+typedef struct CUstream_st* csa2_stream; /* same type as cudaStream_t */
+typedef uint16_t csa2_bf16;              /* bfloat16 bit pattern */
+
+/* Message of the last failing call on this thread ("" if none).  The string is
+ * owned by the library and stays valid until the next call on this thread. */
+const char* csa2_last_error(void);
+
+/* Library version string, e.g. "csa2 0.1 sm_103a". */
+const char* csa2_version(void);
+
+/* Synchronises `stream`, then reports and clears the device-side fault flag raised
+ * by any kernel of this library since the previous call: CSA2_OK, CSA2_ETIMEOUT or
+ * CSA2_EBOUNDS (the first fault wins).  CSA2_ECUDA if the synchronisation failed. */
+csa2_status csa2_device_status(csa2_stream stream);
+
+/* ---------------------------------------------------------------------------------
+ * csa2_compress -- [A] "特殊模块 · compressor", "CSA2 的池化比 V4 简单一截";
+ * [B] §4.1 (odd tail), §6.1-6.2 (partial RoPE at the group head); [C] §6.2, §6.4.
+ *
+ * New tokens of B sequences arrive as a ragged batch: tokens cu_seqlens[b] ..
+ * cu_seqlens[b+1]-1 of kv/score belong to sequence b and sit at absolute positions
+ * start_pos[b], start_pos[b]+1, ...  For every group j whose last token
+ * (j*ratio + ratio - 1) arrives in this call the library writes plane row
+ * row_base[b] + j:
+ *     r[d] = sum_i softmax_i(score_i[d]) * kv_i[d]          (i over the group's tokens)
+ *     y    = r * rsqrt(mean(r^2) + eps) * norm_w             (RMSNorm over 512 dims)
+ *     y[448+2i], y[449+2i] rotated by angle (j*ratio) * inv_freq[i], i = 0..31
+ * in fp32, stored as bf16 (round to nearest even).  Tokens of a group that is still
+ * incomplete at the end of the call are stored in kv_state/score_state slot
+ * (position % ratio) of their sequence; tokens of a group that started in an
+ * earlier call are read from there.  With ratio 1 every token is a group and the
+ * states are not touched (they may be NULL).
+ *   kv, score    [T][512] bf16 (score may be NULL when ratio == 1)
+ *   cu_seqlens   [B+1] int32, non-decreasing, cu_seqlens[0] == 0, cu_seqlens[B] == T
+ *   start_pos    [B] int64 >= 0
+ *   ratio        1 or 2
+ *   kv_state, score_state  [B][2][512] fp32, read and written
+ *   plane        [plane_rows][512] bf16, rows written as above
+ *   row_base     [B] int64; rows past plane_rows raise CSA2_EBOUNDS and are skipped
+ *   norm_w       [512] fp32 RMSNorm weight, NULL = all ones
+ *   inv_freq     [32] fp32 RoPE inverse frequencies (a YaRN table drops in here)
+ * Limits: 1 <= B <= 8192, T >= 0. */
+csa2_status csa2_compress(const csa2_bf16* kv, const csa2_bf16* score, int T,
+                          const int32_t* cu_seqlens, int B, const int64_t* start_pos, int ratio,
+                          float* kv_state, float* score_state, csa2_bf16* plane,
+                          int64_t plane_rows, const int64_t* row_base, const float* norm_w,
+                          float eps, const float* inv_freq, csa2_stream stream);
+
+/* ---------------------------------------------------------------------------------
+ * csa2_index_topk -- [A] "特殊模块 · indexer" Fig. 3b and "visible 是每行自己的前缀长度";
+ * [A] Fig. 2c (candidate blocks); [C] A.15.2.
+ *
+ * For query q (sequence q_seq[q], position q_pos[q]) the visible rows are
+ * c < n_vis = floor((q_pos[q] + 1) / ratio).  Each scored row c gets
+ *     s(c) = alpha * sum_h w[q][h] * relu(<iq[q][h], index_k[row_base[b] + c]>),
+ *     alpha = 128^-1/2 * H^-1/2   (relu dropped when relu == 0)
+ * FULL mode (cand == NULL): every visible row is scored.
+ * REINDEX mode: only rows 8*cand[q][i] + r (r < 8) that are visible; cand[q] holds
+ * ncb block ids in ascending order, -1 padded.
+ * The k_eff = min(k, #scored) highest scores are kept (ties: lower row id;
+ * NaN ranks as -inf) and written as ascending row ids to sel[q][0..k_eff), the rest
+ * of sel[q][0..k) set to -1.  sel_scores (optional) receives the matching scores
+ * (0 for -1 entries).
+ *   iq         [Q][H][128] bf16;  w [Q][H] fp32;  H = 32 or 64
+ *   index_k    [index_rows][128] bf16;  row_base [..] int64;  q_seq [Q] int32;
+ *   q_pos      [Q] int64
+ *   max_scored bound on positions scored per query: FULL >= max n_vis (larger n_vis
+ *              raises CSA2_EBOUNDS and is clipped); REINDEX must equal ncb * 8
+ *   k          1..512;  REINDEX requires ncb * 8 >= k
+ *   scores_out optional [Q][max_scored] fp32: the score of every position (FULL:
+ *              position = row; REINDEX: position = 8 * i + r); unscored positions
+ *              are not written.  For tests.
+ *   ws         workspace of at least csa2_index_topk_workspace_size(Q, H,
+ *              max_scored, k) bytes, 256-byte aligned; contents are scratch. */
+size_t csa2_index_topk_workspace_size(int Q, int H, int64_t max_scored, int k);
+csa2_status csa2_index_topk(const csa2_bf16* iq, const float* w, int Q, int H,
+                            const csa2_bf16* index_k, int64_t index_rows,
+                            const int64_t* row_base, const int32_t* q_seq, const int64_t* q_pos,
+                            int ratio, const int32_t* cand, int ncb, int k, int relu,
+                            int64_t max_scored, int32_t* sel, float* sel_scores,
+                            float* scores_out, void* ws, size_t ws_bytes, csa2_stream stream);
+
+/* ---------------------------------------------------------------------------------
+ * csa2_topk_scores -- the selection step of csa2_index_topk on given scores.
+ * [A] Fig. 3b (top_k_per_row: ascending, -1 padded).
+ *
+ * For row q of scores [Q][ld] fp32, the k_eff = min(k, n[q]) highest of
+ * scores[q][0..n[q]) (ties: lower index; NaN ranks as -inf; -0 equals +0) are
+ * written as ascending indices to sel[q][0..k_eff), -1 after.  sel_scores optional.
+ *   n  [Q] int32, 0 <= n[q] <= ld;  k 1..512
+ *   ws workspace of csa2_topk_workspace_size(Q, ld, k) bytes, 256-byte aligned. */
+size_t csa2_topk_workspace_size(int Q, int64_t ld, int k);
+csa2_status csa2_topk_scores(const float* scores, const int32_t* n, int Q, int64_t ld, int k,
+                             int32_t* sel, float* sel_scores, void* ws, size_t ws_bytes,
+                             csa2_stream stream);
+
+/* ---------------------------------------------------------------------------------
+ * csa2_sparse_attn -- [A] "四种层合并出来的是什么形状" and Fig. 2a-2d; [B] §4.1, §4.4;
+ * [C] §5.5-5.6, A.19.3; [E] Fig. 2d (sink in the denominator).
+ *
+ * Query q (sequence b = q_seq[q], position p = q_pos[q]) attends, with all 64 heads,
+ * to the entry set
+ *     window:   positions max(0, p-127) .. p of the layer's own sliding window
+ *     selected: plane rows row_base[b] + sel[q][i] for sel[q][i] != -1
+ * (the two parts are not de-duplicated, at most 128 + 512 entries).  Each entry's
+ * 512-d vector x_j serves as key and value:
+ *     s_j   = scale * <q[q][h], x_j>
+ *     out_h = sum_j e^{s_j} x_j / (e^{sink[h]} + sum_j e^{s_j})
+ *     lse_h = ln(e^{sink[h]} + sum_j e^{s_j})
+ * computed with fp32 accumulation of bf16 operands; out is bf16 and still carries
+ * the RoPE phase of the keys (the inverse rotation is not part of this call).
+ *   q      [Q][64][512] bf16;  q_seq [Q] int32;  q_pos [Q] int64
+ *   swa    window source (HOST struct, device pointers inside):
+ *          RING:   data holds [B][128] rows, position pos in slot pos % 128
+ *          LINEAR: data holds rows; position pos of sequence b is row
+ *                  lin_base[b] + pos - lin_pos0[b]
+ *          BF16 rows are 512 bf16; FP8_S128 rows are 528 bytes: 512 E4M3 codes then
+ *          four fp32 scales, value = code * scale[d / 128]
+ *          n_rows = rows in data (indices beyond raise CSA2_EBOUNDS and are skipped)
+ *   plane  [plane_rows][512] bf16;  row_base int64;  sel [Q][nsel] int32, nsel <= 512
+ *          (sel may be NULL with nsel == 0: window only)
+ *   sink   [64] fp32 or NULL (no sink term);  scale: softmax temperature (1/sqrt(512))
+ *   out    [Q][64][512] bf16;  lse [Q][64] fp32 or NULL */
+typedef enum { CSA2_SWA_RING = 0, CSA2_SWA_LINEAR = 1 } csa2_swa_mode;
+typedef enum { CSA2_SWA_BF16 = 0, CSA2_SWA_FP8_S128 = 1 } csa2_swa_dtype;
+typedef struct {
+  int32_t mode;            /* csa2_swa_mode */
+  int32_t dtype;           /* csa2_swa_dtype */
+  const void* data;        /* device rows, see above */
+  int64_t n_rows;          /* rows in data */
+  const int64_t* lin_base; /* LINEAR only: device [B] */
+  const int64_t* lin_pos0; /* LINEAR only: device [B] */
+} csa2_swa;
+
+csa2_status csa2_sparse_attn(const csa2_bf16* q, int Q, const int32_t* q_seq,
+                             const int64_t* q_pos, const csa2_swa* swa, const csa2_bf16* plane,
+                             int64_t plane_rows, const int64_t* row_base, const int32_t* sel,
+                             int nsel, const float* sink, float scale, csa2_bf16* out, float* lse,
+                             csa2_stream stream);
+
+/* ---------------------------------------------------------------------------------
+ * csa2_reuse_attn -- [A] Fig. 2d (REUSE: no scoring kernel, the selection of the
+ * group's first layer is replayed); [C] A.8.1.
+ * Identical arguments and result to csa2_sparse_attn; `sel` is the stored selection
+ * of the index-group start layer while q and swa are this layer's own. */
+csa2_status csa2_reuse_attn(const csa2_bf16* q, int Q, const int32_t* q_seq,
+                            const int64_t* q_pos, const csa2_swa* swa, const csa2_bf16* plane,
+                            int64_t plane_rows, const int64_t* row_base, const int32_t* sel,
+                            int nsel, const float* sink, float scale, csa2_bf16* out, float* lse,
+                            csa2_stream stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CSA2_H */
