@@ -17,7 +17,8 @@ from . import build as _build
 
 __all__ = [
     "Csa2Error", "Swa", "lib", "csa2_version", "csa2_device_status", "csa2_compress",
-    "csa2_index_topk_workspace_size", "csa2_index_topk", "csa2_topk_workspace_size",
+    "csa2_index_topk_workspace_size", "csa2_index_topk", "csa2_index_topk_noalloc",
+    "csa2_topk_workspace_size",
     "csa2_topk_scores", "csa2_sparse_attn", "csa2_reuse_attn",
 ]
 
@@ -50,6 +51,8 @@ _SIGS = {
     "csa2_index_topk_workspace_size": ([_i32, _i32, _i64, _i32], _sz),
     "csa2_index_topk": ([_vp, _vp, _i32, _i32, _vp, _i64, _vp, _vp, _vp, _i32, _vp, _i32, _i32,
                          _i32, _i64, _vp, _vp, _vp, _vp, _sz, _vp], _i32),
+    "csa2_index_topk_noalloc": ([_vp, _vp, _i32, _i32, _vp, _i64, _vp, _vp, _vp, _i32, _vp,
+                                 _i32, _i32, _i32, _i64, _vp, _vp, _vp, _vp], _i32),
     "csa2_topk_workspace_size": ([_i32, _i64, _i32], _sz),
     "csa2_topk_scores": ([_vp, _vp, _i32, _i64, _i32, _vp, _vp, _vp, _sz, _vp], _i32),
     "csa2_sparse_attn": ([_vp, _i32, _vp, _vp, ctypes.POINTER(_SwaC), _vp, _i64, _vp, _vp, _i32,
@@ -142,6 +145,18 @@ def csa2_index_topk(iq, w, index_k, row_base, q_seq, q_pos, ratio, k, max_scored
                                  1 if relu else 0, max_scored, _p(sel), _p(sel_scores),
                                  _p(scores_out), _p(ws), ws.numel() * ws.element_size(),
                                  _stream(stream)))
+
+
+def csa2_index_topk_noalloc(iq, w, index_k, row_base, q_seq, q_pos, ratio, k, max_scored, sel,
+                            sel_scores=None, cand=None, relu=True, scores_out=None, stream=None):
+    """csa2_index_topk without a workspace: for callers that cannot allocate device
+    memory; its scratch is a fixed 64 MiB device array inside the library."""
+    Q, H = iq.shape[0], iq.shape[1]
+    ncb = 0 if cand is None else cand.shape[1]
+    _check(lib().csa2_index_topk_noalloc(_p(iq), _p(w), Q, H, _p(index_k), index_k.shape[0],
+                                         _p(row_base), _p(q_seq), _p(q_pos), ratio, _p(cand),
+                                         ncb, k, 1 if relu else 0, max_scored, _p(sel),
+                                         _p(sel_scores), _p(scores_out), _stream(stream)))
 
 
 def csa2_topk_workspace_size(Q, ld, k):

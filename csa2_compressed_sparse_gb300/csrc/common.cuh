@@ -102,6 +102,9 @@ cudaError_t launch_index(const IndexArgs& a, int num_sms, cudaStream_t s);
 cudaError_t launch_topk(const TopkArgs& a, cudaStream_t s);
 cudaError_t launch_attn(const AttnArgs& a, cudaStream_t s);
 
+// Replace the calling thread's csa2_last_error() text.
+void set_last_error(const char* msg);
+
 // Fault flags of each translation unit (read and cleared, host side).
 int take_fault_compress();
 int take_fault_index();

@@ -109,6 +109,10 @@ csa2_status attn_common(const char* name, const csa2_bf16* q, int Q, const int32
 
 }  // namespace
 
+namespace csa2 {
+void set_last_error(const char* msg) { g_last_error = msg; }
+}  // namespace csa2
+
 extern "C" {
 
 const char* csa2_last_error(void) { return g_last_error.c_str(); }

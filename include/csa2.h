@@ -133,6 +133,31 @@ csa2_status csa2_index_topk(const csa2_bf16* iq, const float* w, int Q, int H,
                             float* scores_out, void* ws, size_t ws_bytes, csa2_stream stream);
 
 /* ---------------------------------------------------------------------------------
+ * csa2_index_topk_noalloc -- the paper has no counterpart: this is a library service.
+ *
+ * Same arguments and results as csa2_index_topk, minus the workspace.  It is for
+ * callers that cannot provide device scratch memory: a plugin driven through a fixed
+ * interface that passes only its inputs and outputs, an engine that owns all device
+ * memory through its own pool and forbids other allocations, or a path that cannot
+ * afford the device-wide synchronisation of cudaMalloc/cudaFree.  The scratch lives in
+ * a fixed 64 MiB device array inside the library, present on every GPU that loads the
+ * library until the process exits; the call itself allocates nothing.
+ *   - Sizes needing more than 64 MiB (see csa2_index_topk_workspace_size) are refused
+ *     with CSA2_ENOSPACE before anything is enqueued.
+ *   - The first call on a device looks up the array's device address with a host-side
+ *     runtime call; make that first call before any stream capture.
+ *   - All calls on a device share the array.  Calls whose kernels can overlap on the
+ *     GPU (unordered streams) race and give wrong results: order them.
+ *   - Nothing in the array needs to start at zero: each call writes every entry it
+ *     reads, so stale contents of an earlier call are harmless. */
+csa2_status csa2_index_topk_noalloc(const csa2_bf16* iq, const float* w, int Q, int H,
+                                    const csa2_bf16* index_k, int64_t index_rows,
+                                    const int64_t* row_base, const int32_t* q_seq,
+                                    const int64_t* q_pos, int ratio, const int32_t* cand, int ncb,
+                                    int k, int relu, int64_t max_scored, int32_t* sel,
+                                    float* sel_scores, float* scores_out, csa2_stream stream);
+
+/* ---------------------------------------------------------------------------------
  * csa2_topk_scores -- the selection step of csa2_index_topk on given scores.
  * [A] Fig. 3b (top_k_per_row: ascending, -1 padded).
  *
