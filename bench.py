@@ -32,7 +32,7 @@ FALLBACK_HBM = 6800.0
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=3000)
+    ap.add_argument("--steps", type=int, default=5000)
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--config", default="decode",
@@ -175,11 +175,52 @@ def run_ours(args):
     t = wl.materialize("cuda")
     buf = allocate(spec, t)
     stream = torch.cuda.current_stream()
-    for _ in range(max(args.warmup, 3)):
-        run_step(spec, t, buf)
+    run_step(spec, t, buf)
     csa2.csa2_device_status()
 
     # ---- device-resident timing of K steps ----
+    # Each stage of the step is captured once as a CUDA graph (the C ABI only enqueues
+    # kernels, so it captures as is) and replayed; events between the stage graphs time
+    # the index stage on the launching stream.
+    from csa2_compressed_sparse_gb300.step import swa_of
+
+    def st_compress():
+        if t["kv"].shape[0]:
+            csa2.csa2_compress(t["kv"], t["score"], t["cu_seqlens"], t["start_pos"],
+                               spec.ratio, t["kv_state"], t["score_state"], t["plane"],
+                               t["row_base"], t["inv_freq"], eps=spec.eps)
+
+    def st_index():
+        csa2.csa2_index_topk(t["iq"], t["w"], t["index_k"], t["row_base"], t["q_seq"],
+                             t["q_pos"], spec.ratio, spec.k, spec.max_scored, buf.sel, buf.ws,
+                             sel_scores=buf.sel_scores, cand=t.get("cand"), relu=spec.relu)
+
+    def st_attn():
+        for layer in range(len(t["q"])):
+            fn = csa2.csa2_sparse_attn if layer == 0 else csa2.csa2_reuse_attn
+            fn(t["q"][layer], t["q_seq"], t["q_pos"], swa_of(spec, t, layer), t["plane"],
+               t["row_base"], buf.sel, t["sink"], buf.out[layer], scale=spec.scale,
+               ws=buf.attn_ws)
+
+    graphs = []
+    side = torch.cuda.Stream()
+    side.wait_stream(stream)
+    with torch.cuda.stream(side):
+        for fn in (st_compress, st_index, st_attn):
+            fn()
+    stream.wait_stream(side)
+    torch.cuda.synchronize()
+    for fn in (st_compress, st_index, st_attn):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            fn()
+        graphs.append(g)
+    for _ in range(max(args.warmup, 3)):
+        for g in graphs:
+            g.replay()
+    torch.cuda.synchronize()
+    csa2.csa2_device_status()
+
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     ix0 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     ix1 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
@@ -191,20 +232,11 @@ def run_ours(args):
     time.sleep(0.3)
     ev0.record(stream)
     for i in range(args.steps):
-        if spec and t["kv"].shape[0]:
-            csa2.csa2_compress(t["kv"], t["score"], t["cu_seqlens"], t["start_pos"], spec.ratio,
-                               t["kv_state"], t["score_state"], t["plane"], t["row_base"],
-                               t["inv_freq"], eps=spec.eps)
+        graphs[0].replay()
         ix0[i].record(stream)
-        csa2.csa2_index_topk(t["iq"], t["w"], t["index_k"], t["row_base"], t["q_seq"], t["q_pos"],
-                             spec.ratio, spec.k, spec.max_scored, buf.sel, buf.ws,
-                             sel_scores=buf.sel_scores, cand=t.get("cand"), relu=spec.relu)
+        graphs[1].replay()
         ix1[i].record(stream)
-        from csa2_compressed_sparse_gb300.step import swa_of
-        for layer in range(len(t["q"])):
-            fn = csa2.csa2_sparse_attn if layer == 0 else csa2.csa2_reuse_attn
-            fn(t["q"][layer], t["q_seq"], t["q_pos"], swa_of(spec, t, layer), t["plane"],
-               t["row_base"], buf.sel, t["sink"], buf.out[layer], scale=spec.scale)
+        graphs[2].replay()
     ev1.record(stream)
     torch.cuda.synchronize()
     clk = clocks.stop()

@@ -19,7 +19,7 @@ __all__ = [
     "Csa2Error", "Swa", "lib", "csa2_version", "csa2_device_status", "csa2_compress",
     "csa2_index_topk_workspace_size", "csa2_index_topk", "csa2_index_topk_noalloc",
     "csa2_topk_workspace_size",
-    "csa2_topk_scores", "csa2_sparse_attn", "csa2_reuse_attn",
+    "csa2_topk_scores", "csa2_attn_workspace_size", "csa2_sparse_attn", "csa2_reuse_attn",
 ]
 
 STATUS = {0: "CSA2_OK", 1: "CSA2_EINVAL", 2: "CSA2_ECUDA", 3: "CSA2_ETIMEOUT", 4: "CSA2_EBOUNDS",
@@ -55,10 +55,11 @@ _SIGS = {
                                  _i32, _i32, _i32, _i64, _vp, _vp, _vp, _vp], _i32),
     "csa2_topk_workspace_size": ([_i32, _i64, _i32], _sz),
     "csa2_topk_scores": ([_vp, _vp, _i32, _i64, _i32, _vp, _vp, _vp, _sz, _vp], _i32),
+    "csa2_attn_workspace_size": ([_i32, _i32], _sz),
     "csa2_sparse_attn": ([_vp, _i32, _vp, _vp, ctypes.POINTER(_SwaC), _vp, _i64, _vp, _vp, _i32,
-                          _vp, _f32, _vp, _vp, _vp], _i32),
+                          _vp, _f32, _vp, _vp, _vp, _sz, _vp], _i32),
     "csa2_reuse_attn": ([_vp, _i32, _vp, _vp, ctypes.POINTER(_SwaC), _vp, _i64, _vp, _vp, _i32,
-                         _vp, _f32, _vp, _vp, _vp], _i32),
+                         _vp, _f32, _vp, _vp, _vp, _sz, _vp], _i32),
 }
 
 _LIB = None
@@ -170,22 +171,27 @@ def csa2_topk_scores(scores, n, k, sel, sel_scores=None, ws=None, stream=None):
                                   nbytes, _stream(stream)))
 
 
-def _attn(fn, q, q_seq, q_pos, swa, plane, row_base, sel, sink, out, lse, scale, stream):
+def csa2_attn_workspace_size(Q, nsel):
+    return int(lib().csa2_attn_workspace_size(Q, nsel))
+
+
+def _attn(fn, q, q_seq, q_pos, swa, plane, row_base, sel, sink, out, lse, scale, ws, stream):
     sw = swa.c()
     nsel = 0 if sel is None else sel.shape[1]
     plane_rows = 0 if plane is None else plane.shape[0]
+    nbytes = 0 if ws is None else ws.numel() * ws.element_size()
     _check(fn(_p(q), q.shape[0], _p(q_seq), _p(q_pos), ctypes.byref(sw), _p(plane), plane_rows,
-              _p(row_base), _p(sel), nsel, _p(sink), float(scale), _p(out), _p(lse),
-              _stream(stream)))
+              _p(row_base), _p(sel), nsel, _p(sink), float(scale), _p(out), _p(lse), _p(ws),
+              nbytes, _stream(stream)))
 
 
 def csa2_sparse_attn(q, q_seq, q_pos, swa: Swa, plane, row_base, sel, sink, out, lse=None,
-                     scale=512 ** -0.5, stream=None):
+                     scale=512 ** -0.5, ws=None, stream=None):
     _attn(lib().csa2_sparse_attn, q, q_seq, q_pos, swa, plane, row_base, sel, sink, out, lse,
-          scale, stream)
+          scale, ws, stream)
 
 
 def csa2_reuse_attn(q, q_seq, q_pos, swa: Swa, plane, row_base, sel, sink, out, lse=None,
-                    scale=512 ** -0.5, stream=None):
+                    scale=512 ** -0.5, ws=None, stream=None):
     _attn(lib().csa2_reuse_attn, q, q_seq, q_pos, swa, plane, row_base, sel, sink, out, lse,
-          scale, stream)
+          scale, ws, stream)

@@ -48,16 +48,18 @@ struct IndexArgs {
   const int32_t* cand;  // [Q][ncb] or null
   int ncb;
   int relu;
-  int64_t ld;           // max_scored: row stride of the key / score arrays
+  int64_t ld;           // max_scored: positions per query (row stride of scores_out)
+  int64_t ldk;          // row stride of keys (ld rounded up to a multiple of 4)
   float* scores_out;    // optional [Q][ld]
   // workspace views
-  uint32_t* keys;       // [Q][ld]
+  uint32_t* keys;       // [Q][ldk]
   int32_t* n_scored;    // [Q]
   int32_t* grp_q0;      // [Q]  first query of group g
   int32_t* grp_nq;      // [Q]  queries in group g
   int64_t* grp_tile0;   // [Q+1] first work tile of group g (prefix)
   int32_t* n_groups;    // [1]
   int32_t* tmp;         // [Q]  scratch of the grouping pass
+  int32_t* topk_count;  // [Q]  zeroed by the prep kernel for the top-k merge
   int group_max;        // queries per group (FULL: 256 / H; REINDEX: 1)
 };
 
@@ -73,7 +75,9 @@ struct TopkArgs {
   int32_t* sel;           // [Q][k]
   float* sel_scores;      // [Q][k] or null
   uint64_t* part;         // [Q][nchunk][k] (key << 32 | position) partial results
+  int32_t* count;         // [Q] chunk arrivals (zero before the call; reset by the merge)
   int nchunk;             // chunks per row (1 = single pass)
+  int chunk;              // positions per chunk
 };
 
 struct AttnArgs {
@@ -95,12 +99,19 @@ struct AttnArgs {
   float scale;
   uint16_t* out;
   float* lse;
+  float* part_o;   // [Q][nsplit][64][512] partial outputs (nsplit > 1)
+  float* part_ml;  // [Q][nsplit][2][64] partial running max (log2) and sum
 };
 
 cudaError_t launch_compress(const CompressArgs& a, cudaStream_t s);
 cudaError_t launch_index(const IndexArgs& a, int num_sms, cudaStream_t s);
 cudaError_t launch_topk(const TopkArgs& a, cudaStream_t s);
-cudaError_t launch_attn(const AttnArgs& a, cudaStream_t s);
+int attn_num_splits(int Q, int nsel, int num_sms);
+cudaError_t launch_attn(const AttnArgs& a, int nsplit, cudaStream_t s);
+
+int topk_chunk_len(int64_t ld);
+int topk_num_chunks(int64_t ld);
+int64_t topk_max_len();
 
 // Replace the calling thread's csa2_last_error() text.
 void set_last_error(const char* msg);

@@ -8,11 +8,6 @@
 #include "../../include/csa2.h"
 #include "common.cuh"
 
-namespace csa2 {
-int topk_num_chunks(int64_t ld);
-int topk_max_chunks();
-}  // namespace csa2
-
 namespace {
 
 thread_local std::string g_last_error;
@@ -49,20 +44,21 @@ size_t up256(size_t x) { return (x + 255) & ~size_t(255); }
 
 // Workspace of csa2_index_topk.
 struct IndexWs {
-  size_t keys, n_scored, grp_q0, grp_nq, tmp, grp_tile0, n_groups, part, total;
+  size_t keys, n_scored, grp_q0, grp_nq, tmp, grp_tile0, n_groups, count, part, total;
   int nchunk;
 };
 
 IndexWs index_ws_layout(int Q, int64_t ld, int k) {
   IndexWs w{};
   size_t o = 0;
-  w.keys = o; o = up256(o + (size_t)Q * (size_t)ld * 4);
+  w.keys = o; o = up256(o + (size_t)Q * (size_t)((ld + 3) & ~int64_t(3)) * 4);
   w.n_scored = o; o = up256(o + (size_t)Q * 4);
   w.grp_q0 = o; o = up256(o + (size_t)Q * 4);
   w.grp_nq = o; o = up256(o + (size_t)Q * 4);
   w.tmp = o; o = up256(o + (size_t)Q * 4);
   w.grp_tile0 = o; o = up256(o + (size_t)(Q + 1) * 8);
   w.n_groups = o; o = up256(o + 4);
+  w.count = o; o = up256(o + (size_t)Q * 4);
   w.nchunk = csa2::topk_num_chunks(ld);
   w.part = o;
   if (w.nchunk > 1) o = up256(o + (size_t)Q * w.nchunk * k * 8);
@@ -70,17 +66,25 @@ IndexWs index_ws_layout(int Q, int64_t ld, int k) {
   return w;
 }
 
+// csa2_topk_scores: per-row arrival counters, then the partial lists.
 size_t topk_ws_bytes(int Q, int64_t ld, int k) {
   const int nchunk = csa2::topk_num_chunks(ld);
-  return nchunk > 1 ? up256((size_t)Q * nchunk * k * 8) : 0;
+  return nchunk > 1 ? up256((size_t)Q * 4) + up256((size_t)Q * nchunk * k * 8) : 0;
+}
+
+// Workspace of the split attention: partial O [nsplit][64][512] fp32 and (max, sum)
+// [nsplit][2][64] fp32 per query.
+size_t attn_ws_bytes(int Q, int nsplit) {
+  if (nsplit <= 1) return 0;
+  return up256((size_t)Q * nsplit * 64 * 512 * 4) + up256((size_t)Q * nsplit * 128 * 4);
 }
 
 csa2_status attn_common(const char* name, const csa2_bf16* q, int Q, const int32_t* q_seq,
                         const int64_t* q_pos, const csa2_swa* swa, const csa2_bf16* plane,
                         int64_t plane_rows, const int64_t* row_base, const int32_t* sel, int nsel,
-                        const float* sink, float scale, csa2_bf16* out, float* lse,
-                        csa2_stream stream) {
-  REQUIRE(Q >= 0, "%s: Q must be >= 0 (got %d)", name, Q);
+                        const float* sink, float scale, csa2_bf16* out, float* lse, void* ws,
+                        size_t ws_bytes, csa2_stream stream) {
+  REQUIRE(Q >= 0 && Q <= 65535, "%s: Q must be in [0, 65535] (got %d)", name, Q);
   if (Q == 0) return CSA2_OK;
   REQUIRE(q && q_seq && q_pos && swa && out, "%s: q, q_seq, q_pos, swa and out are required", name);
   REQUIRE(aligned16(q) && aligned16(out), "%s: q and out must be 16-byte aligned", name);
@@ -102,7 +106,18 @@ csa2_status attn_common(const char* name, const csa2_bf16* q, int Q, const int32
   a.lin_base = swa->lin_base; a.lin_pos0 = swa->lin_pos0;
   a.plane = plane; a.plane_rows = plane_rows; a.row_base = row_base;
   a.sel = sel; a.nsel = nsel; a.sink = sink; a.scale = scale; a.out = out; a.lse = lse;
-  cudaError_t e = csa2::launch_attn(a, stream);
+  REQUIRE(ws == nullptr || (reinterpret_cast<uintptr_t>(ws) & 255u) == 0,
+          "%s: ws must be 256-byte aligned", name);
+  const int sms = num_sms();
+  if (sms <= 0) return fail(CSA2_ECUDA, "%s: no CUDA device", name);
+  int nsplit = csa2::attn_num_splits(Q, nsel, sms);
+  while (nsplit > 1 && (ws == nullptr || attn_ws_bytes(Q, nsplit) > ws_bytes)) --nsplit;
+  if (nsplit > 1) {
+    a.part_o = static_cast<float*>(ws);
+    a.part_ml = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) +
+                                         up256((size_t)Q * nsplit * 64 * 512 * 4));
+  }
+  cudaError_t e = csa2::launch_attn(a, nsplit, stream);
   if (e != cudaSuccess) return cuda_fail(e, name);
   return CSA2_OK;
 }
@@ -180,9 +195,9 @@ csa2_status csa2_index_topk(const csa2_bf16* iq, const float* w, int Q, int H,
             "csa2_index_topk: candidate pool of %d blocks x 8 rows cannot hold top-%d", ncb, k);
     REQUIRE(max_scored == (int64_t)ncb * 8, "csa2_index_topk: REINDEX needs max_scored == ncb * 8");
   }
-  REQUIRE(csa2::topk_num_chunks(max_scored) <= csa2::topk_max_chunks(),
+  REQUIRE(max_scored <= csa2::topk_max_len(),
           "csa2_index_topk: max_scored %lld exceeds the supported %lld positions",
-          (long long)max_scored, (long long)csa2::topk_max_chunks() * 16384);
+          (long long)max_scored, (long long)csa2::topk_max_len());
   if (Q == 0) return CSA2_OK;
   REQUIRE(iq && w && index_k && row_base && q_seq && q_pos && sel && ws,
           "csa2_index_topk: iq, w, index_k, row_base, q_seq, q_pos, sel and ws are required");
@@ -198,6 +213,7 @@ csa2_status csa2_index_topk(const csa2_bf16* iq, const float* w, int Q, int H,
   a.iq = iq; a.w = w; a.Q = Q; a.H = H; a.index_k = index_k; a.index_rows = index_rows;
   a.row_base = row_base; a.q_seq = q_seq; a.q_pos = q_pos; a.ratio = ratio; a.cand = cand;
   a.ncb = cand ? ncb : 0; a.relu = relu ? 1 : 0; a.ld = max_scored; a.scores_out = scores_out;
+  a.ldk = (max_scored + 3) & ~int64_t(3);
   a.keys = reinterpret_cast<uint32_t*>(base + L.keys);
   a.n_scored = reinterpret_cast<int32_t*>(base + L.n_scored);
   a.grp_q0 = reinterpret_cast<int32_t*>(base + L.grp_q0);
@@ -205,15 +221,19 @@ csa2_status csa2_index_topk(const csa2_bf16* iq, const float* w, int Q, int H,
   a.tmp = reinterpret_cast<int32_t*>(base + L.tmp);
   a.grp_tile0 = reinterpret_cast<int64_t*>(base + L.grp_tile0);
   a.n_groups = reinterpret_cast<int32_t*>(base + L.n_groups);
+  a.topk_count = reinterpret_cast<int32_t*>(base + L.count);
   a.group_max = cand ? 1 : 256 / H;
   const int sms = num_sms();
   if (sms <= 0) return fail(CSA2_ECUDA, "csa2_index_topk: no CUDA device");
   cudaError_t e = csa2::launch_index(a, sms, stream);
   if (e != cudaSuccess) return cuda_fail(e, "csa2_index_topk (scores)");
   csa2::TopkArgs t{};
-  t.keys = a.keys; t.scores = nullptr; t.n = a.n_scored; t.Q = Q; t.ld = max_scored; t.k = k;
+  t.keys = a.keys; t.scores = nullptr; t.n = a.n_scored; t.Q = Q; t.ld = a.ldk; t.k = k;
   t.cand = cand; t.ncb = a.ncb; t.sel = sel; t.sel_scores = sel_scores;
   t.part = reinterpret_cast<uint64_t*>(base + L.part); t.nchunk = L.nchunk;
+  t.count = a.topk_count;
+  t.chunk = csa2::topk_chunk_len(max_scored);
+  // n_scored <= max_scored <= ldk: the chunking of max_scored covers every row
   e = csa2::launch_topk(t, stream);
   if (e != cudaSuccess) return cuda_fail(e, "csa2_index_topk (top-k)");
   return CSA2_OK;
@@ -230,8 +250,9 @@ csa2_status csa2_topk_scores(const float* scores, const int32_t* n, int Q, int64
   REQUIRE(Q >= 0, "csa2_topk_scores: Q must be >= 0");
   REQUIRE(k >= 1 && k <= 512, "csa2_topk_scores: k must be in [1, 512] (got %d)", k);
   REQUIRE(ld >= 1, "csa2_topk_scores: ld must be >= 1");
-  REQUIRE(csa2::topk_num_chunks(ld) <= csa2::topk_max_chunks(),
-          "csa2_topk_scores: ld %lld exceeds the supported length", (long long)ld);
+  REQUIRE(ld <= csa2::topk_max_len(),
+          "csa2_topk_scores: ld %lld exceeds the supported %lld positions", (long long)ld,
+          (long long)csa2::topk_max_len());
   if (Q == 0) return CSA2_OK;
   REQUIRE(scores && n && sel, "csa2_topk_scores: scores, n and sel are required");
   const size_t need = topk_ws_bytes(Q, ld, k);
@@ -243,29 +264,43 @@ csa2_status csa2_topk_scores(const float* scores, const int32_t* n, int Q, int64
   }
   csa2::TopkArgs t{};
   t.keys = nullptr; t.scores = scores; t.n = n; t.Q = Q; t.ld = ld; t.k = k; t.cand = nullptr;
-  t.ncb = 0; t.sel = sel; t.sel_scores = sel_scores; t.part = static_cast<uint64_t*>(ws);
+  t.ncb = 0; t.sel = sel; t.sel_scores = sel_scores;
   t.nchunk = csa2::topk_num_chunks(ld);
+  t.chunk = csa2::topk_chunk_len(ld);
+  if (t.nchunk > 1) {
+    t.count = static_cast<int32_t*>(ws);
+    t.part = reinterpret_cast<uint64_t*>(static_cast<uint8_t*>(ws) + up256((size_t)Q * 4));
+    cudaError_t z = cudaMemsetAsync(t.count, 0, (size_t)Q * 4, stream);
+    if (z != cudaSuccess) return cuda_fail(z, "csa2_topk_scores");
+  }
   cudaError_t e = csa2::launch_topk(t, stream);
   if (e != cudaSuccess) return cuda_fail(e, "csa2_topk_scores");
   return CSA2_OK;
+}
+
+size_t csa2_attn_workspace_size(int Q, int nsel) {
+  if (Q <= 0 || nsel < 0 || nsel > 512) return 0;
+  const int sms = num_sms();
+  if (sms <= 0) return 0;
+  return attn_ws_bytes(Q, csa2::attn_num_splits(Q, nsel, sms));
 }
 
 csa2_status csa2_sparse_attn(const csa2_bf16* q, int Q, const int32_t* q_seq,
                              const int64_t* q_pos, const csa2_swa* swa, const csa2_bf16* plane,
                              int64_t plane_rows, const int64_t* row_base, const int32_t* sel,
                              int nsel, const float* sink, float scale, csa2_bf16* out, float* lse,
-                             csa2_stream stream) {
+                             void* ws, size_t ws_bytes, csa2_stream stream) {
   return attn_common("csa2_sparse_attn", q, Q, q_seq, q_pos, swa, plane, plane_rows, row_base,
-                     sel, nsel, sink, scale, out, lse, stream);
+                     sel, nsel, sink, scale, out, lse, ws, ws_bytes, stream);
 }
 
 csa2_status csa2_reuse_attn(const csa2_bf16* q, int Q, const int32_t* q_seq,
                             const int64_t* q_pos, const csa2_swa* swa, const csa2_bf16* plane,
                             int64_t plane_rows, const int64_t* row_base, const int32_t* sel,
                             int nsel, const float* sink, float scale, csa2_bf16* out, float* lse,
-                            csa2_stream stream) {
+                            void* ws, size_t ws_bytes, csa2_stream stream) {
   return attn_common("csa2_reuse_attn", q, Q, q_seq, q_pos, swa, plane, plane_rows, row_base,
-                     sel, nsel, sink, scale, out, lse, stream);
+                     sel, nsel, sink, scale, out, lse, ws, ws_bytes, stream);
 }
 
 }  // extern "C"

@@ -73,18 +73,46 @@ __device__ __forceinline__ void fetch(const CompressArgs& a, int b, int64_t pos,
 }
 
 __global__ void __launch_bounds__(kWarps * 32) compress_kernel(CompressArgs a) {
+  // cu_seqlens in shared memory (one coalesced read instead of a chain of dependent
+  // global loads in the binary search below)
+  extern __shared__ int32_t cu_s[];
+  __shared__ uint64_t turn_s[32];
+  griddep_launch_dependents();
+  griddep_wait();
+  for (int i = threadIdx.x; i <= a.B; i += blockDim.x) cu_s[i] = a.cu_seqlens[i];
+  if (threadIdx.x < 32) {
+    // inv_freq[i] / (2 pi) as a 64-bit binary fraction of a turn (fractional part only):
+    // the phase of position p is then (p * turn) mod 2^64, exact in integer arithmetic.
+    double tr = (double)a.inv_freq[threadIdx.x] * 0.15915494309189535;
+    tr -= floor(tr);
+    const double sc = tr * 18446744073709551616.0;  // 2^64
+    turn_s[threadIdx.x] = sc >= 18446744073709551615.0 ? ~0ull : (uint64_t)sc;
+  }
   const int lane = threadIdx.x & 31;
   const int64_t t = (int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5);
+  // this token's own kv / score do not depend on its sequence: start them now
+  float own_kv[2][8], own_sc[2][8];
+  if (t < a.T) {
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      load8_bf16(a.kv + t * kDLat + (h ? 256 : 0) + 8 * lane, own_kv[h]);
+      if (a.score) load8_bf16(a.score + t * kDLat + (h ? 256 : 0) + 8 * lane, own_sc[h]);
+      else
+#pragma unroll
+        for (int i = 0; i < 8; ++i) own_sc[h][i] = 0.f;
+    }
+  }
+  __syncthreads();
   if (t >= a.T) return;
   // sequence of token t: last b with cu_seqlens[b] <= t
   int lo = 0, hi = a.B - 1;
   while (lo < hi) {
     int mid = (lo + hi + 1) >> 1;
-    if (a.cu_seqlens[mid] <= t) lo = mid; else hi = mid - 1;
+    if (cu_s[mid] <= t) lo = mid; else hi = mid - 1;
   }
   const int b = lo;
-  const int64_t t0 = a.cu_seqlens[b];
-  const int64_t t1 = a.cu_seqlens[b + 1];
+  const int64_t t0 = cu_s[b];
+  const int64_t t1 = cu_s[b + 1];
   const int64_t s0 = a.start_pos[b];
   const int64_t pos = s0 + (t - t0);
   const int m = a.ratio;
@@ -97,19 +125,17 @@ __global__ void __launch_bounds__(kWarps * 32) compress_kernel(CompressArgs a) {
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
       if (m == 1) {
-        float kv[8], sc[8];
-        fetch(a, b, pos, s0, t0, c[h], kv, sc);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) r[h][i] = kv[i];
+        for (int i = 0; i < 8; ++i) r[h][i] = own_kv[h][i];
       } else {
-        float k0[8], q0[8], k1[8], q1[8];
+        float k0[8], q0[8];
         fetch(a, b, pos - 1, s0, t0, c[h], k0, q0);
-        fetch(a, b, pos, s0, t0, c[h], k1, q1);
 #pragma unroll
         for (int i = 0; i < 8; ++i) {  // per-channel softmax over the two slots
-          float mx = fmaxf(q0[i], q1[i]);
-          float e0 = expf(q0[i] - mx), e1 = expf(q1[i] - mx);
-          r[h][i] = (e0 * k0[i] + e1 * k1[i]) / (e0 + e1);
+          const float k1 = own_kv[h][i], q1 = own_sc[h][i];
+          float mx = fmaxf(q0[i], q1);
+          float e0 = expf(q0[i] - mx), e1 = expf(q1 - mx);
+          r[h][i] = (e0 * k0[i] + e1 * k1) / (e0 + e1);
         }
       }
     }
@@ -132,13 +158,15 @@ __global__ void __launch_bounds__(kWarps * 32) compress_kernel(CompressArgs a) {
       for (int i = 0; i < 8; ++i) r[h][i] = r[h][i] * rstd * wv[i];
     }
     if (lane >= 24) {  // dims 448 + 8(lane-24) .. +7: four rotation pairs
-      const double p0 = (double)(j * m);
+      const uint64_t p0 = (uint64_t)(j * m);
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
         const int pair = 4 * (lane - 24) + k;
-        double sn, cs;
-        sincos(p0 * (double)a.inv_freq[pair], &sn, &cs);
-        const float fc = (float)cs, fs = (float)sn;
+        // phase in turns as a signed 64-bit fraction, then the angle in [-pi, pi)
+        const int64_t ph = (int64_t)(p0 * turn_s[pair]);
+        const float ang = (float)ph * 3.4061215800865545e-19f;  // 2 pi / 2^64
+        float fs, fc;
+        sincosf(ang, &fs, &fc);
         const float x0 = r[1][2 * k], x1 = r[1][2 * k + 1];
         r[1][2 * k] = x0 * fc - x1 * fs;
         r[1][2 * k + 1] = x0 * fs + x1 * fc;
@@ -182,8 +210,8 @@ __global__ void __launch_bounds__(kWarps * 32) compress_kernel(CompressArgs a) {
 cudaError_t launch_compress(const CompressArgs& a, cudaStream_t s) {
   if (a.T == 0) return cudaSuccess;
   const int grid = (a.T + kWarps - 1) / kWarps;
-  compress_kernel<<<grid, kWarps * 32, 0, s>>>(a);
-  return cudaGetLastError();
+  return launch_pdl(compress_kernel, dim3(grid), dim3(kWarps * 32),
+                    (size_t)(a.B + 1) * sizeof(int32_t), s, a);
 }
 
 }  // namespace csa2

@@ -14,9 +14,10 @@
 // Persistent CTA, one per SM, warp-specialised:
 //   warp 0      TMA producer: K tiles (4-stage ring) and the group's Q block
 //   warp 1      TMEM allocation; lane 0 issues the MMAs (8 x K=16 per tile)
-//   warps 2..5  epilogue: TMEM -> relu * w -> sum -> order-preserving key
-// TMEM holds two 256-column fp32 accumulators so the epilogue of tile i overlaps
-// the MMAs of tile i+1.  The scores are written as uint32 keys for the top-k.
+//   warps 2..9  epilogue in two groups of four warps: group e reads TMEM accumulator e
+//               (tiles of parity e) -> relu * w -> sum -> order-preserving key
+// TMEM holds two 256-column fp32 accumulators, so two tiles are in the epilogue while
+// the MMAs of the next one run.  The scores are written as uint32 keys for the top-k.
 #include <cudaTypedefs.h>
 
 #include "common.cuh"
@@ -28,7 +29,7 @@ namespace {
 
 constexpr int kStages = 4;
 constexpr int kTileRows = 128;
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;
 constexpr int kStageBytes = kTileRows * kDIdx * 2;  // 32 KiB: two 64-dim blocks
 constexpr int kBBytes = 2 * 256 * 128;              // 64 KiB: two 64-dim blocks x 256 rows
 constexpr int kMaxGroup = 8;
@@ -78,6 +79,8 @@ __global__ void __launch_bounds__(kPrepThreads) index_prep_kernel(IndexArgs a, i
   __shared__ int carry_groups;
   __shared__ long long carry_tiles;
   const int tid = threadIdx.x;
+  griddep_launch_dependents();
+  griddep_wait();
   if (tid == 0) { carry_run = 0; carry_groups = 0; carry_tiles = 0; }
   __syncthreads();
   // pass 1: scored positions per query and group-start flags
@@ -92,6 +95,7 @@ __global__ void __launch_bounds__(kPrepThreads) index_prep_kernel(IndexArgs a, i
         if (ns > a.ld) { raise_fault(kFaultBounds); ns = a.ld; }
       }
       a.n_scored[q] = (int32_t)ns;
+      a.topk_count[q] = 0;
       start = (q == 0 || a.q_seq[q] != a.q_seq[q - 1]) ? q : -1;
     } else {
       start = -1;
@@ -174,13 +178,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                                              ~uintptr_t(1023));
   uint8_t* a_smem = smem;                              // kStages x 32 KiB
   uint8_t* b_smem = smem + kStages * kStageBytes;      // 64 KiB
-  float* w_s = reinterpret_cast<float*>(b_smem + kBBytes);  // [256]
-  Bars* bars = reinterpret_cast<Bars*>(w_s + 256);
+  float* w_all = reinterpret_cast<float*>(b_smem + kBBytes);  // [2][256], per epilogue group
+  Bars* bars = reinterpret_cast<Bars*>(w_all + 512);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  int64_t* gq = reinterpret_cast<int64_t*>(tmem_slot + 4);  // [kMaxGroup] n_visible
+  int64_t* gq_all = reinterpret_cast<int64_t*>(tmem_slot + 4);  // [2][kMaxGroup] n_visible
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  griddep_launch_dependents();
+  if (threadIdx.x == 0) {
+    prefetch_tensormap(&kmap_tile);
+    prefetch_tensormap(&kmap_blk);
+    prefetch_tensormap(&qmap);
+  }
+  griddep_wait();
   const int ng = *a.n_groups;
   const int64_t total = a.grp_tile0[ng];
   const int64_t per = (total + gridDim.x - 1) / gridDim.x;
@@ -327,47 +338,81 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   } else {
-    // ===================== epilogue (warps 2..5) =====================
+    // ============ epilogue: warps 2..5 (tiles k even), warps 6..9 (k odd) ============
+    const int eg = (warp - 2) >> 2;       // epilogue group = TMEM accumulator it reads
+    const int et = threadIdx.x - 64 - 128 * eg;  // thread index within the group
     const int sub = warp & 3;             // TMEM sub-partition of this warp
     const int r = sub * 32 + lane;        // tile row = TMEM lane
+    float* w_s = w_all + 256 * eg;
+    int64_t* gq = gq_all + kMaxGroup * eg;
     GroupInfo gi;
     int g = g_first - 1;
     gi.tile1 = -1;
-    for (int64_t it = it_lo; it < it_hi; ++it) {
+    int loaded = -1;  // query group whose weights sit in w_s
+    for (int64_t it = it_lo + eg; it < it_hi; it += 2) {
       if (*abort_flag) break;
       while (it >= gi.tile1) {
         ++g;
         load_group(a, g, gi);
       }
-      if (it == it_lo || it == gi.tile0) {
-        asm volatile("bar.sync 1, 128;" ::: "memory");
+      if (g != loaded) {
+        if (eg == 0) asm volatile("bar.sync 1, 128;" ::: "memory");
+        else asm volatile("bar.sync 2, 128;" ::: "memory");
         const int nw = gi.nq * a.H;
-        for (int i = threadIdx.x - 64; i < nw; i += 128)
-          w_s[i] = a.w[(int64_t)gi.q0 * a.H + i] * alpha;
-        if (threadIdx.x - 64 < gi.nq) gq[threadIdx.x - 64] = n_visible(a.q_pos[gi.q0 + threadIdx.x - 64], a.ratio);
-        asm volatile("bar.sync 1, 128;" ::: "memory");
+        for (int i = et; i < nw; i += 128) w_s[i] = a.w[(int64_t)gi.q0 * a.H + i] * alpha;
+        if (et < gi.nq) gq[et] = n_visible(a.q_pos[gi.q0 + et], a.ratio);
+        if (eg == 0) asm volatile("bar.sync 1, 128;" ::: "memory");
+        else asm volatile("bar.sync 2, 128;" ::: "memory");
+        loaded = g;
       }
       const int64_t k = it - it_lo;
-      const int ab = (int)(k & 1);
       const uint32_t use = (uint32_t)(k >> 1);
-      if (!mbar_wait(smem_u32(&bars->acc_full[ab]), use & 1)) { *abort_flag = 1; break; }
+      if (!mbar_wait(smem_u32(&bars->acc_full[eg]), use & 1)) { *abort_flag = 1; break; }
       tc_fence_after();
       const int64_t tile = it - gi.tile0;
       const int64_t pos = tile * kTileRows + r;
-      const uint32_t tbase = tmem + ((uint32_t)(sub * 32) << 16) + (uint32_t)(ab * 256);
+      const uint32_t tbase = tmem + ((uint32_t)(sub * 32) << 16) + (uint32_t)(eg * 256);
       for (int i = 0; i < gi.nq; ++i) {
-        float acc = 0.f;
-        for (int c = 0; c < a.H; c += 32) {
-          uint32_t v[32];
-          tmem_ld32(tbase + (uint32_t)(i * a.H + c), v);
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        const float4* w4 = reinterpret_cast<const float4*>(w_s + i * a.H);
+        if (a.H == 64) {
+          uint32_t v0[32], v1[32];
+          tmem_ld32(tbase + (uint32_t)(i * 64), v0);
+          tmem_ld32(tbase + (uint32_t)(i * 64 + 32), v1);
           tmem_ld_wait();
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            float x = __uint_as_float(v[j]);
-            if (a.relu) x = fmaxf(x, 0.f);
-            acc = fmaf(w_s[i * a.H + c + j], x, acc);
+          for (int j = 0; j < 32; j += 4) {
+            const float4 wa = w4[j >> 2], wb = w4[8 + (j >> 2)];
+            float x0 = __uint_as_float(v0[j]), x1 = __uint_as_float(v0[j + 1]);
+            float x2 = __uint_as_float(v0[j + 2]), x3 = __uint_as_float(v0[j + 3]);
+            float y0 = __uint_as_float(v1[j]), y1 = __uint_as_float(v1[j + 1]);
+            float y2 = __uint_as_float(v1[j + 2]), y3 = __uint_as_float(v1[j + 3]);
+            if (a.relu) {
+              x0 = fmaxf(x0, 0.f); x1 = fmaxf(x1, 0.f); x2 = fmaxf(x2, 0.f); x3 = fmaxf(x3, 0.f);
+              y0 = fmaxf(y0, 0.f); y1 = fmaxf(y1, 0.f); y2 = fmaxf(y2, 0.f); y3 = fmaxf(y3, 0.f);
+            }
+            acc[0] = fmaf(wa.x, x0, acc[0]); acc[1] = fmaf(wa.y, x1, acc[1]);
+            acc[2] = fmaf(wa.z, x2, acc[2]); acc[3] = fmaf(wa.w, x3, acc[3]);
+            acc[0] = fmaf(wb.x, y0, acc[0]); acc[1] = fmaf(wb.y, y1, acc[1]);
+            acc[2] = fmaf(wb.z, y2, acc[2]); acc[3] = fmaf(wb.w, y3, acc[3]);
+          }
+        } else {
+          uint32_t v0[32];
+          tmem_ld32(tbase + (uint32_t)(i * 32), v0);
+          tmem_ld_wait();
+#pragma unroll
+          for (int j = 0; j < 32; j += 4) {
+            const float4 wa = w4[j >> 2];
+            float x0 = __uint_as_float(v0[j]), x1 = __uint_as_float(v0[j + 1]);
+            float x2 = __uint_as_float(v0[j + 2]), x3 = __uint_as_float(v0[j + 3]);
+            if (a.relu) {
+              x0 = fmaxf(x0, 0.f); x1 = fmaxf(x1, 0.f); x2 = fmaxf(x2, 0.f); x3 = fmaxf(x3, 0.f);
+            }
+            acc[0] = fmaf(wa.x, x0, acc[0]); acc[1] = fmaf(wa.y, x1, acc[1]);
+            acc[2] = fmaf(wa.z, x2, acc[2]); acc[3] = fmaf(wa.w, x3, acc[3]);
           }
         }
+        const float score = (acc[0] + acc[1]) + (acc[2] + acc[3]);
         const int q = gi.q0 + i;
         bool valid;
         if (!a.cand) {
@@ -377,13 +422,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           valid = blk >= 0 && (int64_t)blk * 8 + (pos & 7) < gq[i];
         }
         if (pos < a.ld) {
-          a.keys[(int64_t)q * a.ld + pos] = valid ? score_key(acc) : 0u;
-          if (valid && a.scores_out) a.scores_out[(int64_t)q * a.ld + pos] = acc;
+          a.keys[(int64_t)q * a.ldk + pos] = valid ? score_key(score) : 0u;
+          if (valid && a.scores_out) a.scores_out[(int64_t)q * a.ld + pos] = score;
         }
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&bars->acc_empty[ab]));
+      if (lane == 0) mbar_arrive(smem_u32(&bars->acc_empty[eg]));
     }
   }
 
@@ -422,13 +467,13 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint32_t box_rows
 }  // namespace
 
 size_t index_smem_bytes() {
-  return 1024 + kStages * kStageBytes + kBBytes + 256 * 4 + sizeof(Bars) + 16 + 8 * kMaxGroup;
+  return 1024 + kStages * kStageBytes + kBBytes + 512 * 4 + sizeof(Bars) + 16 +
+         2 * 8 * kMaxGroup;
 }
 
 cudaError_t launch_index(const IndexArgs& a, int num_sms, cudaStream_t s) {
   if (a.Q == 0) return cudaSuccess;
-  index_prep_kernel<<<1, kPrepThreads, 0, s>>>(a, a.tmp);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_pdl(index_prep_kernel, dim3(1), dim3(kPrepThreads), 0, s, a, a.tmp);
   if (e != cudaSuccess) return e;
   CUtensorMap kt, kb, qm;
   if (!make_map(&kt, a.index_k, (uint64_t)a.index_rows, kTileRows) ||
@@ -439,8 +484,7 @@ cudaError_t launch_index(const IndexArgs& a, int num_sms, cudaStream_t s) {
   e = cudaFuncSetAttribute(index_score_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)smem);
   if (e != cudaSuccess) return e;
-  index_score_kernel<<<num_sms, kThreads, smem, s>>>(a, kt, kb, qm);
-  return cudaGetLastError();
+  return launch_pdl(index_score_kernel, dim3(num_sms), dim3(kThreads), smem, s, a, kt, kb, qm);
 }
 
 }  // namespace csa2

@@ -1,49 +1,68 @@
-// k_topk.cu -- exact top-k per row by CTA-level radix select.
+// k_topk.cu -- exact top-k per row.
 // [A] "特殊模块 · indexer" Fig. 3b (top_k_per_row: k = 512, ascending, -1 padded) and
 // "visible 是每行自己的前缀长度" (-1 means fewer than k rows were scored).
 //
 // Scores are handled as order-preserving uint32 keys (score_key); key 0 marks a
-// position that was not scored.  For one row segment of n keys cached in shared
-// memory the CTA finds the threshold key T of the k-th largest entry with three
-// histogram passes (key bits 31..21, 20..10, 9..0), then compacts, in position
-// order, every key > T and the first (k - #greater) keys == T.  Ties therefore go
-// to the lower position, and the output is ascending.
+// position that was not scored.  One CTA selects from a row segment of up to 32768
+// positions:
+//   1. sample: a histogram of the top 11 key bits over an even sample of the segment
+//      gives a threshold bin expected to hold about 2k + 64 of its keys above it;
+//   2. filter: one streaming pass keeps the (key, position) pairs at or above the
+//      threshold (a few times k of them) and counts the scored positions;
+//   3. select: three histogram passes (key bits 31..21, 20..10, 9..0) over the kept
+//      pairs give the k-th largest key T and how many keys equal to T are needed;
+//   4. output: winners are marked in a position bitmap (keys > T; the lowest
+//      positions among keys == T), which is scanned in order, so ties go to the lower
+//      position and the output is ascending.
+// If the sample misleads (fewer than k kept, or more than the buffer holds), steps 3
+// and 4 run over the whole segment instead; the result is the same.
 //
-// Rows longer than one chunk are split: every chunk CTA writes its own exact top-k
-// (key, position) list, and a merge CTA selects the top-k of the concatenated
-// lists.  The true top-k is a subset of the union of the per-chunk top-k sets under
-// the same total order (key desc, position asc), so the merge is exact.
+// Longer rows are split into chunks of 32768: every chunk CTA writes its exact top-k
+// (key, position) list, and the chunk CTA that finishes last (a per-row arrival
+// counter) selects the top-k of the concatenated lists.  The true top-k is a subset of
+// the union of the per-chunk top-k sets under the same total order (key desc,
+// position asc), so the merge is exact.
 #include "common.cuh"
 
 CSA2_DEFINE_FAULT_FLAG(topk)
 
 namespace csa2 {
 
-constexpr int kTopkThreads = 512;
+constexpr int kTopkThreads = 1024;
 constexpr int kTopkWarps = kTopkThreads / 32;
-constexpr int kChunk = 16384;        // keys per chunk CTA (64 KiB of shared memory)
-constexpr int kMaxChunks = 96;       // merge holds kMaxChunks * k keys (<= 192 KiB)
+constexpr int kChunkLen = 32768;   // positions per CTA
+constexpr int kMaxChunks = 48;     // the merge holds kMaxChunks * 512 <= kChunkLen pairs
+constexpr int kCandCap = 8192;     // kept (key, index) pairs
+constexpr int kWarpCap = kCandCap / (kTopkThreads / 32);  // per-warp region
+constexpr int kWords = kChunkLen / 32;
 
 namespace {
 
 struct SelectSmem {
   uint32_t hist[2048];
+  uint32_t ckey[kCandCap];
+  uint32_t cidx[kCandCap];
+  uint32_t selmap[kWords];  // positions with key > T
+  uint32_t eqmap[kWords];   // positions with key == T
+  int out[kMaxK];
+  int wcnt[kTopkThreads / 32];  // kept pairs per warp region
+  int ncand;
+  int nvalid;
   int warp_a[kTopkWarps];
   int warp_b[kTopkWarps];
   int found_bin;
   int found_above;
-  int keff;
+  int last;
 };
 
 // Block-wide: among bins (descending), find the bin where the running count from the
 // top crosses `need`.  Writes found_bin and found_above (= count strictly above).
+// If the total is below `need`, found_bin is 0 and found_above the total.
 __device__ void find_crossing(SelectSmem& S, int nbins, int need) {
   const int tid = threadIdx.x;
-  const int per = nbins / kTopkThreads;  // 4 or 2
-  // thread tid owns bins nbins-1-per*tid-j, j = 0..per-1 (descending)
+  const int per = nbins / kTopkThreads;  // 2 or 1
   int local = 0;
   for (int j = 0; j < per; ++j) local += (int)S.hist[nbins - 1 - per * tid - j];
-  // exclusive scan of `local` over the block in tid order
   const int lane = tid & 31, warp = tid >> 5;
   int incl = local;
 #pragma unroll
@@ -51,10 +70,14 @@ __device__ void find_crossing(SelectSmem& S, int nbins, int need) {
     int v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
     if (lane >= o) incl += v;
   }
+  if (tid == 0) { S.found_bin = 0; S.found_above = 0; }
   if (lane == 31) S.warp_a[warp] = incl;
   __syncthreads();
-  int wbase = 0;
-  for (int w = 0; w < warp; ++w) wbase += S.warp_a[w];
+  int wbase = 0, total = 0;
+  for (int w = 0; w < kTopkWarps; ++w) {
+    if (w < warp) wbase += S.warp_a[w];
+    total += S.warp_a[w];
+  }
   int above = wbase + incl - local;
   for (int j = 0; j < per; ++j) {
     int bin = nbins - 1 - per * tid - j;
@@ -65,92 +88,210 @@ __device__ void find_crossing(SelectSmem& S, int nbins, int need) {
     }
     above += c;
   }
+  if (tid == 0 && total < need) S.found_above = total;
   __syncthreads();
 }
 
-// Exact top-k of keys[0..n) (shared memory).  Writes the selected positions in
-// ascending order to out[0..keff) (shared memory) and returns keff.
-__device__ int select_topk(const uint32_t* keys, int n, int k, int* out, SelectSmem& S) {
+__device__ __forceinline__ void clear_hist(SelectSmem& S, int nbins) {
+  for (int i = threadIdx.x; i < nbins; i += kTopkThreads) S.hist[i] = 0;
+}
+
+// Keys of a row segment: workspace keys, raw fp32 scores, or the merge's (key << 32 |
+// position) pairs.
+enum SrcKind { kSrcKeys = 0, kSrcScores = 1, kSrcPairs = 2 };
+
+template <int kKind>
+struct RowSrc {
+  const void* base;
+  bool aligned;  // 16-byte aligned base
+  __device__ __forceinline__ uint32_t operator()(int i) const {
+    if (kKind == kSrcPairs) return (uint32_t)(__ldcg(static_cast<const uint64_t*>(base) + i) >> 32);
+    if (kKind == kSrcScores) return score_key(__ldcg(static_cast<const float*>(base) + i));
+    return __ldcg(static_cast<const uint32_t*>(base) + i);
+  }
+  // keys 4g .. 4g+3 (0 past n), with 16-byte loads when aligned
+  __device__ __forceinline__ uint4 load4(int g, int n) const {
+    const int i = 4 * g;
+    uint4 r = make_uint4(0u, 0u, 0u, 0u);
+    if (i >= n) return r;
+    if (aligned && i + 4 <= n) {
+      if (kKind == kSrcPairs) {
+        const uint4* p = reinterpret_cast<const uint4*>(static_cast<const uint64_t*>(base) + i);
+        const uint4 a = __ldcg(p), b = __ldcg(p + 1);
+        return make_uint4(a.y, a.w, b.y, b.w);
+      }
+      r = __ldcg(reinterpret_cast<const uint4*>(static_cast<const uint32_t*>(base) + i));
+      if (kKind == kSrcScores)
+        r = make_uint4(score_key(__uint_as_float(r.x)), score_key(__uint_as_float(r.y)),
+                       score_key(__uint_as_float(r.z)), score_key(__uint_as_float(r.w)));
+      return r;
+    }
+    r.x = (*this)(i);
+    if (i + 1 < n) r.y = (*this)(i + 1);
+    if (i + 2 < n) r.z = (*this)(i + 2);
+    if (i + 3 < n) r.w = (*this)(i + 3);
+    return r;
+  }
+};
+
+// Exact top-k of src[0..n) (n <= kChunkLen): selected indices, ascending, in S.out.
+// Returns keff = min(k, #scored).
+template <int kKind>
+__device__ int select_topk(const RowSrc<kKind>& src, int n, int k, SelectSmem& S) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  for (int i = tid; i < 2048; i += kTopkThreads) S.hist[i] = 0;
+  const int nw = (n + 31) >> 5;
+  // ---- 1. threshold from a sample ----
+  const int ns = n < 2 * kTopkThreads ? n : 2 * kTopkThreads;
+  clear_hist(S, 2048);
+  if (tid == 0) { S.ncand = 0; S.nvalid = 0; }
+  if (tid < kTopkWarps) S.wcnt[tid] = 0;
+  for (int w = tid; w < nw; w += kTopkThreads) { S.selmap[w] = 0; S.eqmap[w] = 0; }
   __syncthreads();
-  for (int i = tid; i < n; i += kTopkThreads) atomicAdd(&S.hist[keys[i] >> 21], 1u);
+  for (int s = tid; s < ns; s += kTopkThreads) {
+    const int i = (int)(((int64_t)(2 * s + 1) * n) / (2 * ns));
+    const uint32_t key = src(i);
+    if (key) atomicAdd(&S.hist[key >> 21], 1u);
+  }
   __syncthreads();
-  const int nvalid = n - (int)S.hist[0];  // only key 0 falls in bin 0
-  const int keff = nvalid < k ? nvalid : k;
+  // sample keys wanted above the threshold: about (2k + 64) / n of the sample
+  const int want = (int)(((int64_t)(2 * k + 64) * ns + n - 1) / (n > 0 ? n : 1));
+  find_crossing(S, 2048, want);
+  const uint32_t thr = want >= ns ? 1u : max((uint32_t)S.found_bin << 21, 1u);
+  // ---- 2. filter: keep keys >= thr, count scored positions ----
+  // groups of 4 keys; each thread holds 8 groups in flight per round (warp-uniform).
+  // Warp w appends to its own region [w * kWarpCap, ...) through its shared counter.
+  int nval = 0;
+  uint32_t* wkey = S.ckey + warp * kWarpCap;
+  uint32_t* widx = S.cidx + warp * kWarpCap;
+  const int ng = (n + 3) >> 2;
+  constexpr int kU = 8;
+  for (int r0 = warp * 32; r0 < ng; r0 += kU * kTopkThreads) {
+    uint4 v[kU];
+#pragma unroll
+    for (int u = 0; u < kU; ++u) v[u] = src.load4(r0 + u * kTopkThreads + lane, n);
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      const int g = r0 + u * kTopkThreads + lane;
+      const uint32_t kk[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const uint32_t key = kk[j];
+        nval += key != 0u;
+        if (key >= thr) {  // thr >= 1: unscored keys are never kept
+          const int slot = atomicAdd(&S.wcnt[warp], 1);
+          if (slot < kWarpCap) { wkey[slot] = key; widx[slot] = (uint32_t)(4 * g + j); }
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) nval += __shfl_xor_sync(0xFFFFFFFFu, nval, o);
+  if (lane == 0) atomicAdd(&S.nvalid, nval);
+  __syncwarp();
+  if (lane == 0) {
+    const int wc = S.wcnt[warp];
+    atomicAdd(&S.ncand, wc > kWarpCap ? kCandCap + 1 : wc);  // a full region: no fast path
+  }
+  __syncthreads();
+  const int keff = S.nvalid < k ? S.nvalid : k;
   if (keff <= 0) return 0;
-  // pass 1: bits 31..21
+  const int nc = S.ncand;
+  const bool fast = nc >= keff && nc <= kCandCap;  // the kept pairs hold the top-k
+  // ---- 3. radix select over the kept pairs (or the whole segment) ----
+  const int my_cnt = S.wcnt[warp];
+  auto for_keys = [&](auto&& fn) {
+    if (fast) {  // each warp walks its own region
+      for (int j = lane; j < my_cnt; j += 32) fn(wkey[j]);
+    } else {
+      for (int i = tid; i < n; i += kTopkThreads) fn(src(i));
+    }
+  };
+  clear_hist(S, 2048);
+  __syncthreads();
+  for_keys([&](uint32_t key) { if (key) atomicAdd(&S.hist[key >> 21], 1u); });
+  __syncthreads();
   find_crossing(S, 2048, keff);
   const uint32_t b1 = (uint32_t)S.found_bin;
   int above = S.found_above;
-  // pass 2: bits 20..10 among keys in bin b1
-  for (int i = tid; i < 2048; i += kTopkThreads) S.hist[i] = 0;
+  clear_hist(S, 2048);
   __syncthreads();
-  for (int i = tid; i < n; i += kTopkThreads) {
-    uint32_t kk = keys[i];
-    if ((kk >> 21) == b1) atomicAdd(&S.hist[(kk >> 10) & 2047u], 1u);
-  }
+  for_keys([&](uint32_t key) {
+    if (key && (key >> 21) == b1) atomicAdd(&S.hist[(key >> 10) & 2047u], 1u);
+  });
   __syncthreads();
   find_crossing(S, 2048, keff - above);
-  const uint32_t b2 = (uint32_t)S.found_bin;
+  const uint32_t pre = (b1 << 11) | (uint32_t)S.found_bin;
   above += S.found_above;
-  // pass 3: bits 9..0 among keys with prefix (b1, b2)
-  for (int i = tid; i < 1024; i += kTopkThreads) S.hist[i] = 0;
+  clear_hist(S, 1024);
   __syncthreads();
-  const uint32_t pre = (b1 << 11) | b2;
-  for (int i = tid; i < n; i += kTopkThreads) {
-    uint32_t kk = keys[i];
-    if ((kk >> 10) == pre) atomicAdd(&S.hist[kk & 1023u], 1u);
-  }
+  for_keys([&](uint32_t key) {
+    if (key && (key >> 10) == pre) atomicAdd(&S.hist[key & 1023u], 1u);
+  });
   __syncthreads();
   find_crossing(S, 1024, keff - above);
   const uint32_t T = (pre << 10) | (uint32_t)S.found_bin;
   above += S.found_above;
   const int need_eq = keff - above;  // >= 1
-  // compaction in position order: warp w owns the contiguous segment [w*seg, ...)
-  const int seg = ((n + kTopkWarps * 32 - 1) / (kTopkWarps * 32)) * 32;
-  const int s0 = warp * seg, s1 = min(n, s0 + seg);
-  int n_gt = 0, n_eq = 0;
-  for (int i = s0 + lane; i < s1; i += 32) {
-    uint32_t kk = keys[i];
-    n_gt += kk > T;
-    n_eq += kk == T;
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    n_gt += __shfl_xor_sync(0xFFFFFFFFu, n_gt, o);
-    n_eq += __shfl_xor_sync(0xFFFFFFFFu, n_eq, o);
-  }
-  if (lane == 0) { S.warp_a[warp] = n_gt; S.warp_b[warp] = n_eq; }
-  __syncthreads();
-  int eq_before = 0, sel_before = 0;
-  for (int w = 0; w < warp; ++w) {
-    int take = min(max(need_eq - eq_before, 0), S.warp_b[w]);
-    sel_before += S.warp_a[w] + take;
-    eq_before += S.warp_b[w];
-  }
-  int take_eq = min(max(need_eq - eq_before, 0), n_eq);
-  int off = sel_before;
-  const uint32_t lt = (1u << lane) - 1u;
-  for (int base = s0; base < s1; base += 32) {
-    int i = base + lane;
-    uint32_t kk = i < s1 ? keys[i] : 0u;
-    uint32_t gt = __ballot_sync(0xFFFFFFFFu, i < s1 && kk > T);
-    uint32_t eq = __ballot_sync(0xFFFFFFFFu, i < s1 && kk == T);
-    // keep the first take_eq equal keys of the segment
-    uint32_t eq_keep = 0;
-    if (take_eq > 0) {
-      int cnt = __popc(eq);
-      if (cnt <= take_eq) eq_keep = eq;
-      else {
-        uint32_t m = eq;
-        for (int r = 0; r < take_eq; ++r) { uint32_t low = m & (~m + 1u); eq_keep |= low; m ^= low; }
-      }
-      take_eq -= __popc(eq_keep);
+  // ---- 4. mark winners by position, then scan the bitmaps in order ----
+  if (fast) {
+    for (int j = lane; j < my_cnt; j += 32) {
+      const uint32_t key = wkey[j], idx = widx[j];
+      if (key > T) atomicOr(&S.selmap[idx >> 5], 1u << (idx & 31));
+      else if (key == T) atomicOr(&S.eqmap[idx >> 5], 1u << (idx & 31));
     }
-    uint32_t selm = gt | eq_keep;
-    if (selm & (1u << lane)) out[off + __popc(selm & lt)] = i;
-    off += __popc(selm);
+  } else {
+    for (int i0 = warp * 32; i0 < nw * 32; i0 += kTopkThreads) {  // one word per warp step
+      const int i = i0 + lane;
+      const uint32_t key = i < n ? src(i) : 0u;
+      const uint32_t gt = __ballot_sync(0xFFFFFFFFu, key && key > T);
+      const uint32_t eq = __ballot_sync(0xFFFFFFFFu, key && key == T);
+      if (lane == 0) { S.selmap[i0 >> 5] = gt; S.eqmap[i0 >> 5] = eq; }
+    }
+  }
+  __syncthreads();
+  // thread t owns words [t*wpt, (t+1)*wpt); equal keys are taken in position order
+  const int wpt = (nw + kTopkThreads - 1) / kTopkThreads;
+  const int w0 = tid * wpt, w1 = min(nw, w0 + wpt);
+  int c_eq = 0, c_gt = 0;
+  for (int w = w0; w < w1; ++w) { c_eq += __popc(S.eqmap[w]); c_gt += __popc(S.selmap[w]); }
+  int eq_incl = c_eq;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    int v = __shfl_up_sync(0xFFFFFFFFu, eq_incl, o);
+    if (lane >= o) eq_incl += v;
+  }
+  if (lane == 31) S.warp_a[warp] = eq_incl;
+  __syncthreads();
+  int eq_base = 0;
+  for (int w = 0; w < warp; ++w) eq_base += S.warp_a[w];
+  const int eq_before = eq_base + eq_incl - c_eq;
+  int take_eq = min(max(need_eq - eq_before, 0), c_eq);
+  const int c_sel = c_gt + take_eq;
+  int sel_incl = c_sel;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    int v = __shfl_up_sync(0xFFFFFFFFu, sel_incl, o);
+    if (lane >= o) sel_incl += v;
+  }
+  if (lane == 31) S.warp_b[warp] = sel_incl;
+  __syncthreads();
+  int sel_base = 0;
+  for (int w = 0; w < warp; ++w) sel_base += S.warp_b[w];
+  int o = sel_base + sel_incl - c_sel;
+  for (int w = w0; w < w1; ++w) {
+    uint32_t bits = S.selmap[w];
+    uint32_t eqb = S.eqmap[w];
+    while (take_eq > 0 && eqb) {  // lowest positions first
+      const uint32_t low = eqb & (~eqb + 1u);
+      bits |= low;
+      eqb ^= low;
+      --take_eq;
+    }
+    while (bits) {
+      const int b = __ffs(bits) - 1;
+      S.out[o++] = w * 32 + b;
+      bits &= bits - 1u;
+    }
   }
   __syncthreads();
   return keff;
@@ -179,82 +320,70 @@ __device__ void write_row(const TopkArgs& a, int q, int keff, const int* idx, Po
   }
 }
 
-template <bool kFromFloat>
-__global__ void __launch_bounds__(kTopkThreads) topk_chunk_kernel(TopkArgs a) {
+template <int kKind>
+__global__ void __launch_bounds__(kTopkThreads) topk_kernel(TopkArgs a) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
-  uint32_t* keys = reinterpret_cast<uint32_t*>(smem_raw);
-  int* out = reinterpret_cast<int*>(keys + kChunk);
-  SelectSmem& S = *reinterpret_cast<SelectSmem*>(out + kMaxK);
+  SelectSmem& S = *reinterpret_cast<SelectSmem*>(smem_raw);
   const int q = blockIdx.y, c = blockIdx.x;
+  griddep_launch_dependents();
+  griddep_wait();
   int n = a.n[q];
   if (n > a.ld) { if (threadIdx.x == 0) raise_fault(kFaultBounds); n = (int)a.ld; }
-  const int begin = c * kChunk;
-  const int len = max(0, min(kChunk, n - begin));
+  const int begin = c * a.chunk;
+  const int len = max(0, min(a.chunk, n - begin));
   const int64_t rowoff = (int64_t)q * a.ld + begin;
-  for (int i = threadIdx.x; i < len; i += kTopkThreads)
-    keys[i] = kFromFloat ? score_key(a.scores[rowoff + i]) : a.keys[rowoff + i];
-  __syncthreads();
-  const int keff = select_topk(keys, len, a.k, out, S);
+  const void* base = kKind == kSrcScores ? static_cast<const void*>(a.scores + rowoff)
+                                          : static_cast<const void*>(a.keys + rowoff);
+  RowSrc<kKind> src{base, (reinterpret_cast<uintptr_t>(base) & 15u) == 0};
+  int keff = select_topk(src, len, a.k, S);
   if (a.nchunk == 1) {
-    write_row(a, q, keff, out, [&](int i) { return (uint32_t)(begin + i); },
-              [&](int i) { return keys[i]; });
-  } else {
-    uint64_t* part = a.part + ((int64_t)q * a.nchunk + c) * a.k;
-    for (int i = threadIdx.x; i < a.k; i += kTopkThreads) {
-      uint64_t v = 0;
-      if (i < keff) v = ((uint64_t)keys[out[i]] << 32) | (uint32_t)(begin + out[i]);
-      part[i] = v;
-    }
+    write_row(a, q, keff, S.out, [&](int i) { return (uint32_t)(begin + i); },
+              [&](int i) { return src(i); });
+    return;
   }
-}
-
-__global__ void __launch_bounds__(kTopkThreads) topk_merge_kernel(TopkArgs a) {
-  extern __shared__ __align__(16) uint8_t smem_raw[];
-  const int ncand = a.nchunk * a.k;
-  uint32_t* keys = reinterpret_cast<uint32_t*>(smem_raw);
-  int* out = reinterpret_cast<int*>(keys + ncand);
-  SelectSmem& S = *reinterpret_cast<SelectSmem*>(out + kMaxK);
-  const int q = blockIdx.x;
-  const uint64_t* part = a.part + (int64_t)q * ncand;
-  for (int i = threadIdx.x; i < ncand; i += kTopkThreads) keys[i] = (uint32_t)(part[i] >> 32);
+  // partial list of this chunk, then the last chunk CTA of the row merges
+  uint64_t* part = a.part + ((int64_t)q * a.nchunk + c) * a.k;
+  for (int i = threadIdx.x; i < a.k; i += kTopkThreads) {
+    uint64_t v = 0;
+    if (i < keff) v = ((uint64_t)src(S.out[i]) << 32) | (uint32_t)(begin + S.out[i]);
+    part[i] = v;
+  }
+  __threadfence();
   __syncthreads();
+  if (threadIdx.x == 0) S.last = atomicAdd(&a.count[q], 1) == a.nchunk - 1;
+  __syncthreads();
+  if (!S.last) return;
+  __threadfence();
   // candidates are in chunk order and ascending within a chunk: index order is
   // position order, so the select's tie rule stays "lower position".
-  const int keff = select_topk(keys, ncand, a.k, out, S);
-  write_row(a, q, keff, out, [&](int i) { return (uint32_t)(part[i] & 0xFFFFFFFFu); },
-            [&](int i) { return keys[i]; });
+  const int ncand = a.nchunk * a.k;
+  const uint64_t* row = a.part + (int64_t)q * ncand;
+  RowSrc<kSrcPairs> msrc{row, (reinterpret_cast<uintptr_t>(row) & 15u) == 0};
+  keff = select_topk(msrc, ncand, a.k, S);
+  write_row(a, q, keff, S.out, [&](int i) { return (uint32_t)(__ldcg(row + i) & 0xFFFFFFFFu); },
+            [&](int i) { return msrc(i); });
+  if (threadIdx.x == 0) a.count[q] = 0;  // ready for the next call
 }
 
 }  // namespace
 
-int topk_num_chunks(int64_t ld) { return (int)((ld + kChunk - 1) / kChunk); }
-int topk_max_chunks() { return kMaxChunks; }
+// Positions per chunk CTA: the whole row up to 32768, else chunks of 32768 (rows up to
+// 48 x 32768 = 1,572,864 positions).
+int topk_chunk_len(int64_t ld) { return ld <= kChunkLen ? (int)ld : kChunkLen; }
+int topk_num_chunks(int64_t ld) {
+  const int64_t c = topk_chunk_len(ld);
+  return (int)((ld + c - 1) / c);
+}
+int64_t topk_max_len() { return (int64_t)kChunkLen * kMaxChunks; }
 
 cudaError_t launch_topk(const TopkArgs& a, cudaStream_t s) {
   if (a.Q == 0) return cudaSuccess;
-  const size_t sel_smem = sizeof(SelectSmem) + kMaxK * sizeof(int);
-  const size_t smem1 = (size_t)kChunk * 4 + sel_smem;
-  dim3 grid(a.nchunk, a.Q);
-  cudaError_t e;
-  if (a.scores) {
-    e = cudaFuncSetAttribute(topk_chunk_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)smem1);
-    if (e != cudaSuccess) return e;
-    topk_chunk_kernel<true><<<grid, kTopkThreads, smem1, s>>>(a);
-  } else {
-    e = cudaFuncSetAttribute(topk_chunk_kernel<false>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem1);
-    if (e != cudaSuccess) return e;
-    topk_chunk_kernel<false><<<grid, kTopkThreads, smem1, s>>>(a);
-  }
-  e = cudaGetLastError();
-  if (e != cudaSuccess || a.nchunk == 1) return e;
-  const size_t smem2 = (size_t)a.nchunk * a.k * 4 + sel_smem;
-  e = cudaFuncSetAttribute(topk_merge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)smem2);
+  const size_t smem = sizeof(SelectSmem);
+  auto kern = a.scores ? topk_kernel<kSrcScores> : topk_kernel<kSrcKeys>;
+  cudaError_t e =
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  topk_merge_kernel<<<a.Q, kTopkThreads, smem2, s>>>(a);
-  return cudaGetLastError();
+  return launch_pdl(kern, dim3(a.nchunk, a.Q), dim3(kTopkThreads), smem, s, a);
 }
 
 }  // namespace csa2

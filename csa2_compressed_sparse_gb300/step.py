@@ -9,8 +9,9 @@ from typing import List, Optional
 
 import torch
 
-from . import (Swa, SWA_LINEAR, SWA_RING, csa2_compress, csa2_index_topk,
-               csa2_index_topk_workspace_size, csa2_reuse_attn, csa2_sparse_attn)
+from . import (Swa, SWA_LINEAR, SWA_RING, csa2_attn_workspace_size, csa2_compress,
+               csa2_index_topk, csa2_index_topk_workspace_size, csa2_reuse_attn,
+               csa2_sparse_attn)
 
 
 @dataclass
@@ -32,6 +33,7 @@ class StepBuffers:
     out: List[torch.Tensor]
     lse: List[Optional[torch.Tensor]]
     ws: torch.Tensor
+    attn_ws: Optional[torch.Tensor] = None
     scores_out: Optional[torch.Tensor] = None
     launches: int = 0
 
@@ -42,6 +44,8 @@ def allocate(spec: StepSpec, t, want_scores=False, want_lse=False) -> StepBuffer
     layers = len(t["q"])
     ws_bytes = csa2_index_topk_workspace_size(Q, spec.H, spec.max_scored, spec.k)
     ws = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=dev)
+    aws_bytes = csa2_attn_workspace_size(Q, spec.k)
+    attn_ws = torch.empty(aws_bytes, dtype=torch.uint8, device=dev) if aws_bytes else None
     return StepBuffers(
         sel=torch.empty((Q, spec.k), dtype=torch.int32, device=dev),
         sel_scores=torch.empty((Q, spec.k), dtype=torch.float32, device=dev),
@@ -49,6 +53,7 @@ def allocate(spec: StepSpec, t, want_scores=False, want_lse=False) -> StepBuffer
         lse=[torch.empty((Q, 64), dtype=torch.float32, device=dev) if want_lse else None
              for _ in range(layers)],
         ws=ws,
+        attn_ws=attn_ws,
         scores_out=(torch.full((Q, spec.max_scored), float("nan"), dtype=torch.float32,
                                device=dev) if want_scores else None),
     )
@@ -60,6 +65,12 @@ def swa_of(spec: StepSpec, t, layer):
     return Swa(t["swa"][layer], SWA_RING)
 
 
+def topk_chunks(ld: int) -> int:
+    """Chunk CTAs per row of the top-k (the library's rule: whole rows up to 32768
+    positions, else chunks of 32768)."""
+    return (ld + 32767) // 32768
+
+
 def kernel_launches(spec: StepSpec, t) -> int:
     """Kernels one step launches (compress, index prep + scores, top-k, attention)."""
     from . import lib  # noqa: F401  (library must be loaded)
@@ -68,10 +79,9 @@ def kernel_launches(spec: StepSpec, t) -> int:
         n += 1
     Q = t["iq"].shape[0]
     if Q:
-        n += 2  # prep + score kernel
-        nchunk = (spec.max_scored + 16383) // 16384
-        n += 1 if nchunk == 1 else 2
-        n += len(t["q"])
+        n += 3  # prep, score and top-k kernels (the top-k merges in its last CTA)
+        split = csa2_attn_workspace_size(Q, spec.k) > 0
+        n += len(t["q"]) * (2 if split else 1)
     return n
 
 
@@ -88,4 +98,4 @@ def run_step(spec: StepSpec, t, buf: StepBuffers, stream=None, compress=True):
         fn = csa2_sparse_attn if layer == 0 else csa2_reuse_attn
         fn(t["q"][layer], t["q_seq"], t["q_pos"], swa_of(spec, t, layer), t["plane"],
            t["row_base"], buf.sel, t["sink"], buf.out[layer], lse=buf.lse[layer],
-           scale=spec.scale, stream=stream)
+           scale=spec.scale, ws=buf.attn_ws, stream=stream)

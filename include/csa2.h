@@ -197,7 +197,12 @@ csa2_status csa2_topk_scores(const float* scores, const int32_t* n, int Q, int64
  *   plane  [plane_rows][512] bf16;  row_base int64;  sel [Q][nsel] int32, nsel <= 512
  *          (sel may be NULL with nsel == 0: window only)
  *   sink   [64] fp32 or NULL (no sink term);  scale: softmax temperature (1/sqrt(512))
- *   out    [Q][64][512] bf16;  lse [Q][64] fp32 or NULL */
+ *   out    [Q][64][512] bf16;  lse [Q][64] fp32 or NULL
+ *   ws     optional workspace (256-byte aligned) of csa2_attn_workspace_size(Q, nsel)
+ *          bytes.  With few queries the entries of one query are spread over several
+ *          CTAs whose partial results are merged through it; with ws == NULL (or a
+ *          smaller one) fewer CTAs per query are used.  The result does not depend on
+ *          it beyond rounding. */
 typedef enum { CSA2_SWA_RING = 0, CSA2_SWA_LINEAR = 1 } csa2_swa_mode;
 typedef enum { CSA2_SWA_BF16 = 0, CSA2_SWA_FP8_S128 = 1 } csa2_swa_dtype;
 typedef struct {
@@ -209,11 +214,12 @@ typedef struct {
   const int64_t* lin_pos0; /* LINEAR only: device [B] */
 } csa2_swa;
 
+size_t csa2_attn_workspace_size(int Q, int nsel);
 csa2_status csa2_sparse_attn(const csa2_bf16* q, int Q, const int32_t* q_seq,
                              const int64_t* q_pos, const csa2_swa* swa, const csa2_bf16* plane,
                              int64_t plane_rows, const int64_t* row_base, const int32_t* sel,
                              int nsel, const float* sink, float scale, csa2_bf16* out, float* lse,
-                             csa2_stream stream);
+                             void* ws, size_t ws_bytes, csa2_stream stream);
 
 /* ---------------------------------------------------------------------------------
  * csa2_reuse_attn -- [A] Fig. 2d (REUSE: no scoring kernel, the selection of the
@@ -224,7 +230,7 @@ csa2_status csa2_reuse_attn(const csa2_bf16* q, int Q, const int32_t* q_seq,
                             const int64_t* q_pos, const csa2_swa* swa, const csa2_bf16* plane,
                             int64_t plane_rows, const int64_t* row_base, const int32_t* sel,
                             int nsel, const float* sink, float scale, csa2_bf16* out, float* lse,
-                            csa2_stream stream);
+                            void* ws, size_t ws_bytes, csa2_stream stream);
 
 #ifdef __cplusplus
 }

@@ -92,8 +92,8 @@ def test_workspace_sizes_are_monotone():
     b = csa2.csa2_index_topk_workspace_size(64, 64, 65536, 512)
     assert 0 < a < b
     assert a >= 64 * 32768 * 4
-    assert csa2.csa2_topk_workspace_size(8, 16384, 512) == 0  # one chunk: no scratch
-    assert csa2.csa2_topk_workspace_size(8, 1 << 20, 512) >= 8 * 64 * 512 * 8
+    assert csa2.csa2_topk_workspace_size(8, 32768, 512) == 0  # one chunk: no scratch
+    assert csa2.csa2_topk_workspace_size(8, 1 << 20, 512) >= 8 * 32 * 512 * 8
 
 
 def test_attn_rejects_bad_arguments():
@@ -101,12 +101,12 @@ def test_attn_rejects_bad_arguments():
     p = ctypes.c_void_p(256)
     sw = csa2._SwaC(0, 0, 256, 512, None, None)
     st = L.csa2_sparse_attn(p, 2, p, p, ctypes.byref(sw), p, 100, p, p, 513, None, 0.04, p, None,
-                            None)
+                            None, 0, None)
     assert st == 1 and b"nsel" in L.csa2_last_error()
     bad = csa2._SwaC(1, 0, 256, 512, None, None)  # LINEAR without lin_base/lin_pos0
     st = L.csa2_reuse_attn(p, 2, p, p, ctypes.byref(bad), p, 100, p, p, 512, None, 0.04, p, None,
-                           None)
+                           None, 0, None)
     assert st == 1 and b"LINEAR" in L.csa2_last_error()
     st = L.csa2_sparse_attn(p, 2, p, p, ctypes.byref(sw), p, 100, p, p, 512, None,
-                            float("nan"), p, None, None)
+                            float("nan"), p, None, None, 0, None)
     assert st == 1 and b"scale" in L.csa2_last_error()

@@ -230,6 +230,29 @@ def test_step_h32_and_no_relu():
             check_sel(buf.sel[q].cpu().numpy(), sel_ref, sc, rows, wl.k)
 
 
+def test_attention_split_and_unsplit_agree_with_the_oracle():
+    """The same queries with and without the attention workspace (several CTAs per
+    query merged through it, or one CTA per query)."""
+    from csa2_compressed_sparse_gb300 import (csa2_attn_workspace_size, csa2_device_status,
+                                              csa2_sparse_attn)
+    from csa2_compressed_sparse_gb300.step import swa_of
+    wl = W.decode_batch(B=9, lo=300, hi=7000, seed=26)
+    t, spec, buf = run_workload(wl)
+    key = register(wl)
+    nb = csa2_attn_workspace_size(wl.Q, spec.k)
+    assert nb > 0
+    for ws in (None, torch.empty(nb, dtype=torch.uint8, device="cuda")):
+        out = torch.empty_like(buf.out[0])
+        lse = torch.empty((wl.Q, 64), dtype=torch.float32, device="cuda")
+        csa2_sparse_attn(t["q"][0], t["q_seq"], t["q_pos"], swa_of(spec, t, 0), t["plane"],
+                         t["row_base"], buf.sel, t["sink"], out, lse=lse, ws=ws)
+        csa2_device_status()
+        for q in range(wl.Q):
+            ref, ref_lse = oracle_attn(wl, key, q, buf.sel[q].cpu().numpy())
+            check_attn(out[q].float().cpu().numpy(), ref)
+            assert np.abs(lse[q].cpu().numpy() - ref_lse).max() < 1e-2
+
+
 def test_bounds_fault_is_reported_and_recoverable():
     from csa2_compressed_sparse_gb300 import (Csa2Error, Swa, csa2_device_status,
                                               csa2_sparse_attn)
