@@ -46,6 +46,7 @@ struct __align__(8) Bars {
 struct GroupInfo {
   int q0, nq, seq;
   int64_t tile0, tile1;
+  int64_t rb;  // row_base of the group's sequence
 };
 
 __device__ __forceinline__ int64_t n_visible(int64_t pos, int ratio) { return (pos + 1) / ratio; }
@@ -167,6 +168,7 @@ __device__ __forceinline__ void load_group(const IndexArgs& a, int g, GroupInfo&
   gi.seq = a.q_seq[gi.q0];
   gi.tile0 = a.grp_tile0[g];
   gi.tile1 = a.grp_tile0[g + 1];
+  gi.rb = a.row_base[gi.seq];
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -182,7 +184,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   Bars* bars = reinterpret_cast<Bars*>(w_all + 512);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  int64_t* gq_all = reinterpret_cast<int64_t*>(tmem_slot + 4);  // [2][kMaxGroup] n_visible
+  int64_t* gq_all = reinterpret_cast<int64_t*>(tmem_slot + 4);  // [2][kMaxGroup] row limit
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   griddep_launch_dependents();
@@ -272,17 +274,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive_expect_tx(fb, kStageBytes);
         issued[s] = round;
         const int64_t tile = it - gi.tile0;
-        const int64_t rb = a.row_base[gi.seq];
         uint8_t* dst = a_smem + s * kStageBytes;
         if (!a.cand) {
-          const int32_t y = (int32_t)(rb + tile * kTileRows);
+          const int32_t y = (int32_t)(gi.rb + tile * kTileRows);
           for (int db = 0; db < 2; ++db)
             tma_load_2d(smem_u32(dst + db * 16384), &kmap_tile, db * 64, y, fb, pol_k);
         } else {
+          // all 16 block ids first (one round trip), then the 32 copies
           const int32_t* cb = a.cand + (int64_t)gi.q0 * a.ncb + tile * 16;
+          int32_t blk[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) blk[i] = tile * 16 + i < a.ncb ? __ldg(cb + i) : -1;
+#pragma unroll
           for (int i = 0; i < 16; ++i) {
-            const int32_t blk = cb[i];
-            const int32_t y = (int32_t)(rb + (blk >= 0 ? (int64_t)blk * 8 : 0));
+            const int32_t y = (int32_t)(gi.rb + (blk[i] >= 0 ? (int64_t)blk[i] * 8 : 0));
             for (int db = 0; db < 2; ++db)
               tma_load_2d(smem_u32(dst + db * 16384 + i * 1024), &kmap_blk, db * 64, y, fb, pol_k);
           }
@@ -360,17 +365,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         else asm volatile("bar.sync 2, 128;" ::: "memory");
         const int nw = gi.nq * a.H;
         for (int i = et; i < nw; i += 128) w_s[i] = a.w[(int64_t)gi.q0 * a.H + i] * alpha;
-        if (et < gi.nq) gq[et] = n_visible(a.q_pos[gi.q0 + et], a.ratio);
+        if (et < gi.nq)
+          gq[et] = a.cand ? n_visible(a.q_pos[gi.q0 + et], a.ratio) : (int64_t)a.n_scored[gi.q0 + et];
         if (eg == 0) asm volatile("bar.sync 1, 128;" ::: "memory");
         else asm volatile("bar.sync 2, 128;" ::: "memory");
         loaded = g;
       }
       const int64_t k = it - it_lo;
       const uint32_t use = (uint32_t)(k >> 1);
-      if (!mbar_wait(smem_u32(&bars->acc_full[eg]), use & 1)) { *abort_flag = 1; break; }
-      tc_fence_after();
       const int64_t tile = it - gi.tile0;
       const int64_t pos = tile * kTileRows + r;
+      // REINDEX groups hold one query: fetch its candidate block id before the wait
+      const int32_t cblk = a.cand && (pos >> 3) < a.ncb
+                               ? __ldg(a.cand + (int64_t)gi.q0 * a.ncb + (pos >> 3)) : -1;
+      if (!mbar_wait(smem_u32(&bars->acc_full[eg]), use & 1)) { *abort_flag = 1; break; }
+      tc_fence_after();
       const uint32_t tbase = tmem + ((uint32_t)(sub * 32) << 16) + (uint32_t)(eg * 256);
       for (int i = 0; i < gi.nq; ++i) {
         float acc[4] = {0.f, 0.f, 0.f, 0.f};
@@ -416,10 +425,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int q = gi.q0 + i;
         bool valid;
         if (!a.cand) {
-          valid = pos < (int64_t)a.n_scored[q];
+          valid = pos < gq[i];
         } else {
-          const int32_t blk = a.cand[(int64_t)q * a.ncb + (pos >> 3)];
-          valid = blk >= 0 && (int64_t)blk * 8 + (pos & 7) < gq[i];
+          valid = cblk >= 0 && (int64_t)cblk * 8 + (pos & 7) < gq[i];
         }
         if (pos < a.ld) {
           a.keys[(int64_t)q * a.ldk + pos] = valid ? score_key(score) : 0u;

@@ -198,6 +198,8 @@ SMALL = {
     "tiny": lambda: W.tiny_decode(),
     "decode_small": lambda: W.decode_batch(B=12, lo=300, hi=9000, seed=21),
     "reindex_small": lambda: W.reindex_decode(B=3, ctx=24576, ncb=256, seed=22),
+    # 100 blocks: the candidate list ends inside a 16-block work tile
+    "reindex_ragged": lambda: W.reindex_decode(B=3, ctx=9000, ncb=100, seed=26),
     "prefill_small": lambda: W.prefill_reuse(n_new=128, ctx=4224, layers=3, seed=23),
     "long_small": lambda: W.long_decode(B=2, ctx=40000, seed=24),
 }
