@@ -107,6 +107,11 @@ cudaError_t launch_compress(const CompressArgs& a, cudaStream_t s);
 cudaError_t launch_index(const IndexArgs& a, int num_sms, cudaStream_t s);
 cudaError_t launch_topk(const TopkArgs& a, cudaStream_t s);
 int attn_num_splits(int Q, int nsel, int num_sms);
+
+// 2-D tensor map over `rows` bf16 rows of `cols` elements (row stride cols * 2 bytes),
+// boxes of box_cols x box_rows, 128-byte swizzle, out-of-range elements read as zero.
+bool encode_rows_bf16(CUtensorMap* m, const void* base, uint64_t rows, uint32_t cols,
+                      uint32_t box_cols, uint32_t box_rows);
 cudaError_t launch_attn(const AttnArgs& a, int nsplit, cudaStream_t s);
 
 int topk_chunk_len(int64_t ld);

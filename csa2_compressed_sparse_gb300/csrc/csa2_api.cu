@@ -5,6 +5,8 @@
 #include <cstdio>
 #include <string>
 
+#include <cudaTypedefs.h>
+
 #include "../../include/csa2.h"
 #include "common.cuh"
 
@@ -98,7 +100,9 @@ csa2_status attn_common(const char* name, const csa2_bf16* q, int Q, const int32
   REQUIRE(swa->mode == CSA2_SWA_RING || (swa->lin_base && swa->lin_pos0),
           "%s: LINEAR windows need lin_base and lin_pos0", name);
   REQUIRE(std::isfinite(scale), "%s: scale must be finite", name);
-  REQUIRE(plane_rows >= 0, "%s: plane_rows must be >= 0", name);
+  REQUIRE(plane_rows >= 0 && plane_rows < ((int64_t)1 << 31),
+          "%s: plane_rows must be in [0, 2^31)", name);
+  REQUIRE(swa->n_rows < ((int64_t)1 << 31), "%s: swa.n_rows must be < 2^31", name);
   csa2::AttnArgs a{};
   a.q = q; a.Q = Q; a.q_seq = q_seq; a.q_pos = q_pos;
   a.swa_mode = swa->mode; a.swa_dtype = swa->dtype;
@@ -304,3 +308,34 @@ csa2_status csa2_reuse_attn(const csa2_bf16* q, int Q, const int32_t* q_seq,
 }
 
 }  // extern "C"
+
+namespace csa2 {
+
+static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult qr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &qr) == cudaSuccess &&
+        qr == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+bool encode_rows_bf16(CUtensorMap* m, const void* base, uint64_t rows, uint32_t cols,
+                      uint32_t box_cols, uint32_t box_rows) {
+  auto fn = tensor_map_encoder();
+  if (!fn || !base || rows == 0) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+  cuuint32_t box[2] = {box_cols, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+}  // namespace csa2

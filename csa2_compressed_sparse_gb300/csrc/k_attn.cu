@@ -7,24 +7,33 @@
 // int32 index, online softmax with running max and sum, fused sink);
 // [E] Fig. 2d (out_h = sum e^{s_j} v_j / (e^{sink_h} + sum e^{s_j})).
 //
-// A query's entries form up to five tiles of 128 rows: tile 0 is the window
-// (positions p-127..p), tiles 1..4 hold sel[0..511].  The tiles of one query are
-// spread over nsplit CTAs (grid = nsplit x Q); each CTA keeps an online softmax over
-// its tiles:
-//   gather   rows (bf16, or FP8 dequantised to bf16) into a 128-byte-swizzled shared
-//            tile [8 dim blocks][128 rows][128 B], in four groups of two dim blocks,
-//            each signalled on its own mbarrier so the MMAs start on early groups
-//   S^T      = KV[128 x 512] . Q^T[512 x 64]  -> TMEM (row = lane, head = column)
-//   softmax  per head over the rows (warp butterfly + 4-warp combine); the running
-//            max moves only when it grows by more than 8 (log2 units)
-//   O^T     += V^T[512 x 128] . P^T[128 x 64] -> TMEM, four M = 128 tiles; the same
-//            shared tile is the A operand again, read MN-major
+// A query's entries form up to ten chunks of 64 rows: chunks 0 and 1 are the window
+// (positions p-127..p-64 and p-63..p), chunks 2..9 hold sel[64 (c-2) ..].  The chunks
+// of one query are dealt round-robin to nsplit CTAs (grid = nsplit x Q); each CTA
+// runs an online softmax over its chunks through a two-buffer pipeline:
+//   gather   two teams of 256 threads, team b filling KV buffer b with every other
+//            chunk in the 128-byte-swizzled layout [8 dim blocks][64 rows][128 B]
+//            (bf16 rows by 16-byte cp.async, FP8 rows dequantised to bf16).  Row
+//            gathers reach the HBM rate only with many requests in flight per SM, so
+//            most of the CTA's threads are gatherers
+//   S        = Q[64 x 512] . KV^T[512 x 64] -> TMEM buffer b: lane = head, column =
+//            row.  The MMA is M = 128; its upper 64 rows read the next 8 KiB of shared
+//            memory and land in TMEM lanes 64..127, which nothing reads
+//   softmax  thread h (warps 0, 1) owns head h: its running max m_h and sum l_h stay
+//            in registers and every reduction is over its own 64 columns.  P uses the
+//            running max, which moves only when a score exceeds it by more than 64
+//            (log2 units: P <= 2^64 keeps bf16 P and the fp32 sums finite); then
+//            warps 0..3 rescale O^T in TMEM, decided by one barrier vote
+//   O^T     += V^T[512 x 64] . P^T[64 x 64] -> TMEM, four M = 128 tiles; the KV buffer
+//            is the A operand again, read MN-major, and P [head][row] is the B operand
+// S of the next chunk runs while the softmax of this one does, and the gather of
+// chunk c + 2 starts as soon as the PV of chunk c has released its buffer.
 // With nsplit = 1 the CTA starts from the sink (running max = sink, running sum = 1)
 // and writes the output.  Otherwise every CTA writes its partial (max, sum, O) to the
 // workspace and attn_combine_kernel merges them, adding the sink's e^{sink_h} once.
 //
-// Warps 0..7 gather and write the output, warps 0..3 also run the softmax, warp 8
-// owns the TMEM allocation and its lane 0 issues every tcgen05.mma.
+// Warps 0..3 softmax (0, 1) + O^T rescale + output, warps 4..19 gather (teams of eight
+// warps), warp 20 owns the TMEM allocation and its lane 0 issues every tcgen05.mma.
 #include <cuda_fp8.h>
 
 #include "common.cuh"
@@ -34,57 +43,44 @@ CSA2_DEFINE_FAULT_FLAG(attn)
 namespace csa2 {
 namespace {
 
-constexpr int kThreads = 288;
-constexpr int kWorkers = 256;             // warps 0..7
-constexpr int kMaxTiles = 5;
-constexpr int kQBytes = 8 * 64 * 128;     // 64 KiB
-constexpr int kKVBytes = 8 * 128 * 128;   // 128 KiB (also the fp32 [64][512] partial O)
-constexpr int kPBytes = 128 * 128;        // 16 KiB
-constexpr uint32_t kColS = 0;             // TMEM columns of S^T (64)
-constexpr uint32_t kColO = 64;            // O^T tiles at 64 + 64 * mt
+constexpr int kThreads = 672;             // 21 warps
+constexpr int kGroupThreads = 128;        // warps 0..3
+constexpr int kTeam = 256;                // threads per gather team
+constexpr int kGatherWarp0 = 4;
+constexpr int kMmaWarp = 20;
+constexpr int kChunk = 64;                // rows per chunk
+constexpr int kMaxChunks = 10;            // 2 window + 8 selected chunks
+constexpr int kDimBlock = 64 * 128;       // one 64-dim block of 64 rows (8 KiB)
+constexpr int kQBytes = 8 * kDimBlock;    // Q [8 dim blocks][64 heads][128 B]
+constexpr int kBufBytes = 8 * kDimBlock;  // KV [8 dim blocks][64 rows][128 B]
+constexpr int kPBytes = 64 * 128;         // P [64 heads][64 rows] bf16
+constexpr uint32_t kColS = 0;             // TMEM columns of S buffer b: 64 b
+constexpr uint32_t kColO = 128;           // O^T tiles at 128 + 64 * mt
 constexpr float kLog2e = 1.4426950408889634f;
-constexpr float kLazy = 8.0f;
+constexpr float kLazy = 64.0f;
 
 struct __align__(16) Aux {
-  float red[4][64];
   float m_run[64];
   float l_run[64];
-  float fac[64];
-  int64_t rowsrc[kMaxTiles][128];  // per slot of this CTA (tile t = rank + slot * nsplit)
-  int cnt[kMaxTiles];               // valid rows per slot
-  int tiles[kMaxTiles];             // non-empty slots, in order
-  uint64_t bar_g[4];   // gather group done (256 arrivals)
-  uint64_t bar_s;      // S^T complete (commit)
-  uint64_t bar_p;      // P^T written (128 arrivals)
-  uint64_t bar_pv[4];  // PV M-tile complete (commit)
+  float fac[2][64];  // rescale factor per head, by chunk parity (1 / l in the epilogue)
+  int32_t rowidx[kMaxChunks][kChunk];  // source row per slot (chunk = rank + slot * nsplit)
+  uint32_t rowmask[kMaxChunks][2];     // valid rows of each slot
+  int chunks[kMaxChunks];              // non-empty slots, in order
+  uint64_t q_full;      // Q landed (TMA transaction count)
+  uint64_t kv_full[2];  // KV buffer filled (one arrival of the team)
+  uint64_t s_full[2];   // S buffer written (commit)
+  uint64_t p_full[2];   // P buffer written and O^T rescaled (128 arrivals)
+  uint64_t pv_done[2];  // PV of the buffer's chunk complete (commit)
+  uint64_t fin;         // every MMA of the CTA complete (commit)
   uint32_t tmem_slot;
-  int rescale;
-  int ntile;
+  int nchunk;
+  int abort;
 };
 
 __device__ __forceinline__ float ex2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
-}
-
-// Butterfly reduce-scatter of 64 per-lane values across the warp: afterwards lane l
-// holds the reduction over the 32 lanes of heads 2l and 2l+1 in v[0], v[1].
-template <bool kMax>
-__device__ __forceinline__ void warp_reduce_heads(float (&v)[64], int lane) {
-#pragma unroll
-  for (int step = 0; step < 5; ++step) {
-    const int half = 32 >> step;
-    const int bit = 16 >> step;
-    const bool upper = (lane & bit) != 0;
-#pragma unroll
-    for (int i = 0; i < half; ++i) {
-      const float send = upper ? v[i] : v[i + half];
-      const float keep = upper ? v[i + half] : v[i];
-      const float recv = __shfl_xor_sync(0xFFFFFFFFu, send, bit);
-      v[i] = kMax ? fmaxf(keep, recv) : keep + recv;
-    }
-  }
 }
 
 __device__ __forceinline__ void st_shared_zero16(uint32_t addr) {
@@ -97,19 +93,31 @@ __device__ __forceinline__ void st_shared16(uint32_t addr, uint4 v) {
                : "memory");
 }
 
-// Gather group g (dim blocks 2g, 2g+1) of the current tile.
-__device__ __forceinline__ void gather_group(const AttnArgs& a, const Aux& X, int slot, int g,
-                                             bool fp8, const uint8_t* base, uint32_t kvb,
-                                             int tid) {
-  const int64_t* src_of = X.rowsrc[slot];
+// OR of `pred` over warps 0..3 (a barrier of the group with a reduction)
+__device__ __forceinline__ bool group_any(bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred pi, po;\n\tsetp.ne.u32 pi, %1, 0;\n\t"
+      "bar.red.or.pred po, 1, 128, pi;\n\tselp.u32 %0, 1, 0, po;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)pred)
+      : "memory");
+  return r != 0;
+}
+
+// Rows of one chunk into the KV buffer at `kvb` by the threads of a team (t = 0..255);
+// a row index below zero gives a row of zeros.
+__device__ __forceinline__ void gather_chunk(const int32_t* rows, bool fp8, const uint8_t* base,
+                                             uint32_t kvb, int t) {
   if (fp8) {
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int flat = i * kWorkers + tid;
-      const int r = flat >> 3, c16 = 8 * g + (flat & 7);
-      const int64_t off = src_of[r];
-      const uint32_t d0 = kvb + (c16 >> 2) * 16384 + sw128_off(r, (2 * c16) & 7);
-      const uint32_t d1 = kvb + (c16 >> 2) * 16384 + sw128_off(r, (2 * c16 + 1) & 7);
+    // 64 rows x 32 pieces of 16 codes; each piece becomes two 16-byte bf16 chunks
+#pragma unroll 2
+    for (int i = 0; i < 64 * 32 / kTeam; ++i) {
+      const int flat = i * kTeam + t;
+      const int r = flat >> 5, c16 = flat & 31;
+      const int64_t off = rows[r] < 0 ? -1 : (int64_t)rows[r] * 528;
+      const uint32_t d0 = kvb + (c16 >> 2) * kDimBlock + sw128_off(r, (2 * c16) & 7);
+      const uint32_t d1 = kvb + (c16 >> 2) * kDimBlock + sw128_off(r, (2 * c16 + 1) & 7);
       if (off < 0) { st_shared_zero16(d0); st_shared_zero16(d1); continue; }
       const uint8_t* src = base + off;
       const uint4 codes = *reinterpret_cast<const uint4*>(src + c16 * 16);
@@ -130,26 +138,28 @@ __device__ __forceinline__ void gather_group(const AttnArgs& a, const Aux& X, in
       st_shared16(d1, make_uint4(packed[4], packed[5], packed[6], packed[7]));
     }
   } else {
+    // four 1 KiB rows per iteration of the team
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const int flat = i * kWorkers + tid;
-      const int r = flat >> 4, c = 16 * g + (flat & 15);
-      const int64_t off = src_of[r];
-      const uint32_t dst = kvb + (c >> 3) * 16384 + sw128_off(r, c & 7);
+    for (int i = 0; i < 64 * 64 / kTeam; ++i) {
+      const int flat = i * kTeam + t;
+      const int r = flat >> 6, c = flat & 63;
+      const int64_t off = rows[r] < 0 ? -1 : (int64_t)rows[r] * 1024;
+      const uint32_t dst = kvb + (c >> 3) * kDimBlock + sw128_off(r, c & 7);
       if (off < 0) st_shared_zero16(dst);
       else cp_async16(dst, base + off + c * 16);
     }
   }
 }
 
-__global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(AttnArgs a) {
+__global__ void __launch_bounds__(kThreads, 1)
+    sparse_attn_kernel(AttnArgs a, const __grid_constant__ CUtensorMap qmap) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
   uint8_t* q_s = smem;
-  uint8_t* kv_s = smem + kQBytes;
-  uint8_t* p_s = kv_s + kKVBytes;
-  Aux& X = *reinterpret_cast<Aux*>(p_s + kPBytes);
+  uint8_t* kv_s = smem + kQBytes;            // two buffers
+  uint8_t* p_s = kv_s + 2 * kBufBytes;       // two buffers
+  Aux& X = *reinterpret_cast<Aux*>(p_s + 2 * kPBytes);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int q = blockIdx.y;
@@ -157,257 +167,296 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(AttnArgs a) {
   const int nsplit = gridDim.x;
   griddep_launch_dependents();
   if (tid == 0) {
-    for (int g = 0; g < 4; ++g) {
-      mbar_init(smem_u32(&X.bar_g[g]), kWorkers);
-      mbar_init(smem_u32(&X.bar_pv[g]), 1);
+    prefetch_tensormap(&qmap);
+    mbar_init(smem_u32(&X.q_full), 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(smem_u32(&X.kv_full[b]), 1);
+      mbar_init(smem_u32(&X.s_full[b]), 1);
+      mbar_init(smem_u32(&X.p_full[b]), kGroupThreads);
+      mbar_init(smem_u32(&X.pv_done[b]), 1);
     }
-    mbar_init(smem_u32(&X.bar_s), 1);
-    mbar_init(smem_u32(&X.bar_p), 128);
-    X.rescale = 0;
-    X.ntile = 0;
-    for (int i = 0; i < kMaxTiles; ++i) X.cnt[i] = 0;
+    mbar_init(smem_u32(&X.fin), 1);
+    X.nchunk = 0;
+    X.abort = 0;
     mbar_fence_init();
   }
-  if (warp == 8) {
+  if (warp == kMmaWarp) {
     tmem_alloc(smem_u32(&X.tmem_slot), 512);
     tmem_relinquish();
   }
   griddep_wait();
+  const uint32_t qb = smem_u32(q_s), kv0 = smem_u32(kv_s), p0 = smem_u32(p_s);
+  if (tid == 0) {
+    // Q [64 heads][512] of this query: eight 64 x 64 boxes, one per dim block
+    const uint32_t qf = smem_u32(&X.q_full);
+    mbar_arrive_expect_tx(qf, kQBytes);
+    const uint64_t pol = policy_evict_first();
+#pragma unroll
+    for (int db = 0; db < 8; ++db) tma_load_2d(qb + db * kDimBlock, &qmap, 64 * db, q * kHeads, qf, pol);
+  }
   const int b = a.q_seq[q];
   const int64_t p = a.q_pos[q];
   const float scale2 = a.scale * kLog2e;
-  const int ntiles_total = 1 + (a.nsel + 127) / 128;
+  const int nchunks_total = 2 + (a.nsel + kChunk - 1) / kChunk;
 
-  if (tid < 64) {
-    if (nsplit == 1 && a.sink) { X.m_run[tid] = a.sink[tid] * kLog2e; X.l_run[tid] = 1.f; }
-    else { X.m_run[tid] = -INFINITY; X.l_run[tid] = 0.f; }
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = X.tmem_slot;
-
-  // Q[64 heads][512] -> 8 dim blocks of [64 rows][128 B], swizzled.  These copies join
-  // the first commit group of the first tile, so its group-0 barrier also covers Q.
-  if (warp < 8) {
-    const uint8_t* qg = reinterpret_cast<const uint8_t*>(a.q + (int64_t)q * kHeads * kDLat);
-    const uint32_t qb = smem_u32(q_s);
-#pragma unroll 4
-    for (int i = 0; i < 16; ++i) {
-      const int flat = i * kWorkers + tid;
-      const int h = flat >> 6, c = flat & 63;
-      cp_async16(qb + (c >> 3) * 8192 + sw128_off(h, c & 7), qg + h * 1024 + c * 16);
-    }
-  }
-  // ---- row sources of this CTA's tiles (t = rank + slot * nsplit), one pass ----
+  // ---- row sources of this CTA's chunks (chunk = rank + slot * nsplit), one pass ----
   {
-    const int nslot = (ntiles_total - rank + nsplit - 1) / nsplit;
-    const int64_t win_lo = p - (kRing - 1) < 0 ? 0 : p - (kRing - 1);
-    const int row_bytes_swa = a.swa_dtype == 1 ? 528 : 1024;
+    const int nslot = (nchunks_total - rank + nsplit - 1) / nsplit;
     const int64_t rb = a.row_base[b];
-    for (int e = tid; e < nslot * 128; e += kThreads) {
-      const int slot = e >> 7, r = e & 127;
-      const int t = rank + slot * nsplit;
-      int64_t off = -1;
-      if (t == 0) {
-        const int64_t pos = win_lo + r;
-        if (pos <= p) {
+    for (int e = tid; e < nslot * kChunk; e += kThreads) {
+      const int slot = e >> 6, r = e & 63;
+      const int c = rank + slot * nsplit;
+      int32_t idx32 = -1;
+      if (c < 2) {
+        const int64_t pos = p - (kRing - 1) + kChunk * c + r;
+        if (pos >= 0) {
           int64_t idx;
           if (a.swa_mode == 0) idx = (int64_t)b * kRing + (pos & (kRing - 1));
           else idx = a.lin_base[b] + (pos - a.lin_pos0[b]);
-          if (idx >= 0 && idx < a.swa_rows) off = idx * row_bytes_swa;
+          if (idx >= 0 && idx < a.swa_rows) idx32 = (int32_t)idx;
           else raise_fault(kFaultBounds);
         }
       } else {
-        const int i = (t - 1) * 128 + r;
+        const int i = (c - 2) * kChunk + r;
         if (i < a.nsel) {
           const int32_t rr = a.sel[(int64_t)q * a.nsel + i];
           if (rr >= 0) {
             const int64_t idx = rb + rr;
-            if (idx < a.plane_rows) off = idx * 1024;
+            if (idx >= 0 && idx < a.plane_rows) idx32 = (int32_t)idx;
             else raise_fault(kFaultBounds);
           }
         }
       }
-      X.rowsrc[slot][r] = off;
-      // all 32 lanes of a warp share one slot (128 rows per slot)
-      const uint32_t vm = __ballot_sync(0xFFFFFFFFu, off >= 0);
-      if (lane == 0 && vm) atomicAdd(&X.cnt[slot], __popc(vm));
+      X.rowidx[slot][r] = idx32;
+      // the 32 lanes of a warp cover one half of a slot (672 threads = 21 warps)
+      const uint32_t vm = __ballot_sync(0xFFFFFFFFu, idx32 >= 0);
+      if (lane == 0) X.rowmask[slot][r >> 5] = vm;
     }
+    tc_fence_before();
     __syncthreads();
+    tc_fence_after();
     if (tid == 0) {
       int n = 0;
       for (int slot = 0; slot < nslot; ++slot)
-        if (X.cnt[slot] > 0) X.tiles[n++] = slot;
-      X.ntile = n;
+        if (X.rowmask[slot][0] | X.rowmask[slot][1]) X.chunks[n++] = slot;
+      X.nchunk = n;
     }
     __syncthreads();
   }
-  const int ntile = X.ntile;
+  const int n = X.nchunk;
+  const uint32_t tmem = X.tmem_slot;
 
-  if (warp < 8) {
-    // =================== gather (warps 0..7), softmax (warps 0..3) ===================
-    const uint32_t kvb = smem_u32(kv_s);
-    for (int it = 0; it < ntile; ++it) {
-      const int slot = X.tiles[it];
-      const int t = rank + slot * nsplit;
-      const bool fp8 = (t == 0 && a.swa_dtype == 1);
-      const uint8_t* base = t == 0 ? a.swa : reinterpret_cast<const uint8_t*>(a.plane);
-      for (int g = 0; g < 4; ++g) {
-        if (it > 0) mbar_wait(smem_u32(&X.bar_pv[g]), (it - 1) & 1);
-        gather_group(a, X, slot, g, fp8, base, kvb, tid);
-        cp_async_commit();
-      }
-      cp_async_wait_group<3>();
-      fence_proxy_async_smem();
-      mbar_arrive(smem_u32(&X.bar_g[0]));
-      cp_async_wait_group<2>();
-      fence_proxy_async_smem();
-      mbar_arrive(smem_u32(&X.bar_g[1]));
-      cp_async_wait_group<1>();
-      fence_proxy_async_smem();
-      mbar_arrive(smem_u32(&X.bar_g[2]));
+  if (warp >= kGatherWarp0 && warp < kMmaWarp) {
+    // =================== gather: team 0 = warps 4..11; team 1 = warps 12..19 ===================
+    const int team = (warp - kGatherWarp0) / (kTeam / 32);
+    const int t = tid - kGatherWarp0 * 32 - kTeam * team;
+    const uint32_t kvb = kv0 + team * kBufBytes;
+    const uint32_t full_bar = smem_u32(&X.kv_full[team]);
+    int last = -1;  // last chunk of this team (its kv_full phase ends every copy of the team)
+    for (int it = team; it < n; it += 2) {
+      last = it;
+      if (it >= 2 && !X.abort &&
+          !mbar_wait(smem_u32(&X.pv_done[team]), (uint32_t)((it - 2) >> 1) & 1))
+        X.abort = 1;
+      const int slot = X.chunks[it];
+      const int c = rank + slot * nsplit;
+      const bool fp8 = c < 2 && a.swa_dtype == 1;
+      const uint8_t* base = c < 2 ? a.swa : reinterpret_cast<const uint8_t*>(a.plane);
+      gather_chunk(X.rowidx[slot], fp8, base, kvb, t);
+      cp_async_commit();
       cp_async_wait_group<0>();
       fence_proxy_async_smem();
-      mbar_arrive(smem_u32(&X.bar_g[3]));
-
-      if (warp < 4) {
-        mbar_wait(smem_u32(&X.bar_s), it & 1);
+      // every thread of the team has landed its rows
+      if (team == 0) asm volatile("bar.sync 2, 256;" ::: "memory");
+      else asm volatile("bar.sync 3, 256;" ::: "memory");
+      if (t == 0) mbar_arrive(full_bar);
+    }
+    // no copy may still be landing in shared memory when the CTA exits
+    if (t == 0 && last >= 0) mbar_wait(full_bar, (uint32_t)(last >> 1) & 1, 100000000ull);
+  } else if (warp == kMmaWarp) {
+    // =================== MMA issuer (warp 20, lane 0) ===================
+    if (lane == 0 && n > 0 && mbar_wait(smem_u32(&X.q_full), 0)) {
+      const uint32_t id_s = idesc_bf16(128, 64, 0, 0);
+      const uint32_t id_o = idesc_bf16(128, 64, 1, 0);
+      int sn = 0, pn = 0;  // next chunk to score / to accumulate
+      uint64_t t0 = globaltimer_ns();
+      while (pn < n && !X.abort) {
+        bool progress = false;
+        // S of chunk sn reuses TMEM buffer sn & 1 once the softmax of chunk sn - 2 has
+        // released it, i.e. once that chunk's PV has been issued (sn <= pn + 1)
+        if (sn < n && sn <= pn + 1 &&
+            mbar_test_wait(smem_u32(&X.kv_full[sn & 1]), (uint32_t)(sn >> 1) & 1)) {
+          tc_fence_after();
+          const uint32_t kvb = kv0 + (sn & 1) * kBufBytes;
+          const uint32_t d = tmem + kColS + 64 * (sn & 1);
+#pragma unroll
+          for (int db = 0; db < 8; ++db)
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              umma_bf16(d, sdesc_sw128(qb + db * kDimBlock + kk * 32, 16, 1024),
+                        sdesc_sw128(kvb + db * kDimBlock + kk * 32, 16, 1024), id_s,
+                        (db | kk) != 0);
+          umma_commit(smem_u32(&X.s_full[sn & 1]));
+          ++sn;
+          progress = true;
+        }
+        if (pn < sn && mbar_test_wait(smem_u32(&X.p_full[pn & 1]), (uint32_t)(pn >> 1) & 1)) {
+          tc_fence_after();
+          const uint32_t kvb = kv0 + (pn & 1) * kBufBytes;
+          const uint32_t pb = p0 + (pn & 1) * kPBytes;
+#pragma unroll
+          for (int mt = 0; mt < 4; ++mt)
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              umma_bf16(tmem + kColO + 64 * mt,
+                        sdesc_sw128(kvb + 2 * mt * kDimBlock + kk * 2048, kDimBlock, 1024),
+                        sdesc_sw128(pb + kk * 32, 16, 1024), id_o, (pn > 0 || kk > 0) ? 1 : 0);
+          umma_commit(smem_u32(&X.pv_done[pn & 1]));
+          ++pn;
+          progress = true;
+        }
+        if (progress) {
+          t0 = globaltimer_ns();
+        } else if (globaltimer_ns() - t0 > 2000000000ull) {
+          raise_fault(kFaultTimeout);
+          X.abort = 1;
+        }
+      }
+      // no MMA may still be running when the TMEM is released, whatever happened above
+      if (sn > 0) {
+        umma_commit(smem_u32(&X.fin));
+        mbar_wait(smem_u32(&X.fin), 0, 100000000ull);
+      }
+    }
+  } else if (warp < kGatherWarp0) {
+    // ========== softmax (warps 0, 1: thread h = head h) + O^T rescale (warps 0..3) ==========
+    const bool soft = warp < 2;
+    const int h = tid;  // head of a softmax thread (TMEM lane h)
+    const uint32_t lrow = (uint32_t)(warp * 32) << 16;
+    float m = -INFINITY, l = 0.f;
+    if (soft && nsplit == 1 && a.sink) { m = a.sink[h] * kLog2e; l = 1.f; }
+    for (int it = 0; it < n; ++it) {
+      const int bsel = it & 1;
+      const uint32_t ph = (uint32_t)(it >> 1) & 1;
+      const int slot = X.chunks[it];
+      const uint32_t mlo = X.rowmask[slot][0], mhi = X.rowmask[slot][1];
+      const bool full = (mlo & mhi) == 0xFFFFFFFFu;
+      bool need = false;
+      if (soft) {
+        if (!X.abort && !mbar_wait(smem_u32(&X.s_full[bsel]), ph)) X.abort = 1;
         tc_fence_after();
-        const int r = warp * 32 + lane;
-        const uint32_t lrow = (uint32_t)(warp * 32) << 16;
-        float s[64];
-        {
-          uint32_t v0[32], v1[32];
-          tmem_ld32(tmem + lrow + kColS, v0);
-          tmem_ld32(tmem + lrow + kColS + 32, v1);
-          tmem_ld_wait();
-          const bool ok = X.rowsrc[slot][r] >= 0;
-#pragma unroll
-          for (int h = 0; h < 32; ++h) {
-            s[h] = ok ? __uint_as_float(v0[h]) * scale2 : -INFINITY;
-            s[h + 32] = ok ? __uint_as_float(v1[h]) * scale2 : -INFINITY;
-          }
-        }
-        float red[64];
-#pragma unroll
-        for (int h = 0; h < 64; ++h) red[h] = s[h];
-        warp_reduce_heads<true>(red, lane);
-        X.red[warp][2 * lane] = red[0];
-        X.red[warp][2 * lane + 1] = red[1];
-        asm volatile("bar.sync 1, 128;" ::: "memory");
-        if (tid < 64) {
-          const float tm =
-              fmaxf(fmaxf(X.red[0][tid], X.red[1][tid]), fmaxf(X.red[2][tid], X.red[3][tid]));
-          const float mo = X.m_run[tid];
-          const float mn = fmaxf(mo, tm);
-          if (mn > mo + kLazy) {
-            X.fac[tid] = ex2(mo - mn);
-            X.m_run[tid] = mn;
-            X.rescale = 1;
-          } else {
-            X.fac[tid] = 1.f;
-          }
-        }
-        asm volatile("bar.sync 1, 128;" ::: "memory");
-        uint32_t pk[32];
-#pragma unroll
-        for (int h = 0; h < 64; h += 2) {
-          const float p0 = ex2(s[h] - X.m_run[h]);
-          const float p1 = ex2(s[h + 1] - X.m_run[h + 1]);
-          pk[h >> 1] = pack_bf16x2(p0, p1);
-          red[h] = __uint_as_float(pk[h >> 1] << 16);
-          red[h + 1] = __uint_as_float(pk[h >> 1] & 0xFFFF0000u);
-        }
-        const uint32_t pb = smem_u32(p_s);
-#pragma unroll
-        for (int c = 0; c < 8; ++c)
-          st_shared16(pb + sw128_off(r, c),
-                      make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]));
-        warp_reduce_heads<false>(red, lane);
-        X.red[warp][2 * lane] = red[0];
-        X.red[warp][2 * lane + 1] = red[1];
-        asm volatile("bar.sync 1, 128;" ::: "memory");
-        const bool rescale = X.rescale != 0;
-        if (tid < 64)
-          X.l_run[tid] = X.l_run[tid] * X.fac[tid] + (X.red[0][tid] + X.red[1][tid]) +
-                         (X.red[2][tid] + X.red[3][tid]);
-        if (rescale && it > 0) {
-          // O^T columns are heads: scale column h of every O tile by fac[h].  The PV of
-          // the previous tile is complete (its last commit was waited for above).
+        // largest s_j - m over the valid rows (log2 units) decides a rescale
+        float mx = -INFINITY;
 #pragma unroll 1
-          for (int mt = 0; mt < 4; ++mt) {
+        for (int hf = 0; hf < 2; ++hf) {
+          uint32_t v[32];
+          tmem_ld32(tmem + lrow + kColS + 64 * bsel + 32 * hf, v);
+          tmem_ld_wait();
+          const uint32_t mk = full ? 0xFFFFFFFFu : (hf ? mhi : mlo);
 #pragma unroll
-            for (int hb = 0; hb < 64; hb += 32) {
-              uint32_t v[32];
-              const uint32_t ta = tmem + lrow + kColO + 64 * mt + hb;
-              tmem_ld32(ta, v);
-              tmem_ld_wait();
+          for (int j = 0; j < 32; ++j)
+            if ((mk >> j) & 1u) mx = fmaxf(mx, fmaf(__uint_as_float(v[j]), scale2, -m));
+        }
+        need = !(mx <= kLazy);
+        // tcgen05.ld is warp-collective: the whole warp reloads when any lane needs it
+        if (__any_sync(0xFFFFFFFFu, need)) {
+          // new running max: the chunk's largest score (the previous max may be -inf)
+          float sm = -INFINITY;
+#pragma unroll 1
+          for (int hf = 0; hf < 2; ++hf) {
+            uint32_t v[32];
+            tmem_ld32(tmem + lrow + kColS + 64 * bsel + 32 * hf, v);
+            tmem_ld_wait();
+            const uint32_t mk = full ? 0xFFFFFFFFu : (hf ? mhi : mlo);
 #pragma unroll
-              for (int j = 0; j < 32; ++j)
-                v[j] = __float_as_uint(__uint_as_float(v[j]) * X.fac[hb + j]);
-              tmem_st32(ta, v);
-            }
+            for (int j = 0; j < 32; ++j)
+              if ((mk >> j) & 1u) sm = fmaxf(sm, __uint_as_float(v[j]) * scale2);
           }
-          tmem_st_wait();
+          const float fac = need ? ex2(m - sm) : 1.f;  // 0 when m = -inf
+          X.fac[bsel][h] = fac;
+          if (need) {
+            l *= fac;
+            m = sm;
+          }
+        } else {
+          X.fac[bsel][h] = 1.f;
         }
-        asm volatile("bar.sync 1, 128;" ::: "memory");  // all read X.rescale and X.red
-        if (tid == 0) X.rescale = 0;
-        fence_proxy_async_smem();
-        tc_fence_before();
-        mbar_arrive(smem_u32(&X.bar_p));
       }
-    }
-    if (ntile > 0) mbar_wait(smem_u32(&X.bar_pv[3]), (ntile - 1) & 1);
-    tc_fence_after();
-  } else if (lane == 0) {
-    // =================== MMA issuer (warp 8, lane 0) ===================
-    const uint32_t kvb = smem_u32(kv_s);
-    const uint32_t qb = smem_u32(q_s);
-    const uint32_t pb = smem_u32(p_s);
-    const uint32_t id_s = idesc_bf16(128, 64, 0, 0);
-    const uint32_t id_o = idesc_bf16(128, 64, 1, 1);
-    for (int it = 0; it < ntile; ++it) {
-      for (int g = 0; g < 4; ++g) {
-        mbar_wait(smem_u32(&X.bar_g[g]), it & 1);
+      if (group_any(need) && it > 0) {
+        // O^T columns are heads: scale column h of every O tile by fac[h] once the PV of
+        // the previous chunk is complete.  Warp w covers TMEM lanes 32w.. of all tiles.
+        if (!X.abort &&
+            !mbar_wait(smem_u32(&X.pv_done[(it - 1) & 1]), (uint32_t)((it - 1) >> 1) & 1))
+          X.abort = 1;
         tc_fence_after();
+#pragma unroll 1
+        for (int mt = 0; mt < 4; ++mt) {
+#pragma unroll 1
+          for (int hb = 0; hb < 64; hb += 32) {
+            uint32_t v[32];
+            const uint32_t ta = tmem + lrow + kColO + 64 * mt + hb;
+            tmem_ld32(ta, v);
+            tmem_ld_wait();
 #pragma unroll
-        for (int d2 = 0; d2 < 2; ++d2) {
-          const int db = 2 * g + d2;
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            umma_bf16(tmem + kColS, sdesc_sw128(kvb + db * 16384 + kk * 32, 16, 1024),
-                      sdesc_sw128(qb + db * 8192 + kk * 32, 16, 1024), id_s, (db | kk) != 0);
+            for (int j = 0; j < 32; ++j)
+              v[j] = __float_as_uint(__uint_as_float(v[j]) * X.fac[bsel][hb + j]);
+            tmem_st32(ta, v);
+          }
         }
+        tmem_st_wait();
       }
-      umma_commit(smem_u32(&X.bar_s));
-      mbar_wait(smem_u32(&X.bar_p), it & 1);
-      tc_fence_after();
-      for (int mt = 0; mt < 4; ++mt) {
+      if (soft) {
+        // the P buffer was last read by the PV of chunk it - 2
+        if (it >= 2 && !X.abort &&
+            !mbar_wait(smem_u32(&X.pv_done[bsel]), (uint32_t)((it - 2) >> 1) & 1))
+          X.abort = 1;
+        const uint32_t pb = p0 + bsel * kPBytes;
+        float ls = 0.f;
+#pragma unroll 1
+        for (int hf = 0; hf < 2; ++hf) {
+          uint32_t v[32];
+          tmem_ld32(tmem + lrow + kColS + 64 * bsel + 32 * hf, v);
+          tmem_ld_wait();
+          const uint32_t mk = full ? 0xFFFFFFFFu : (hf ? mhi : mlo);
+          uint32_t pk[16];
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          umma_bf16(tmem + kColO + 64 * mt,
-                    sdesc_sw128(kvb + 2 * mt * 16384 + kk * 2048, 16384, 1024),
-                    sdesc_sw128(pb + kk * 2048, 8192, 1024), id_o, (it > 0 || kk > 0) ? 1 : 0);
-        umma_commit(smem_u32(&X.bar_pv[mt]));
+          for (int j = 0; j < 32; j += 2) {
+            const float e0 = ((mk >> j) & 1u) ? ex2(fmaf(__uint_as_float(v[j]), scale2, -m)) : 0.f;
+            const float e1 =
+                ((mk >> (j + 1)) & 1u) ? ex2(fmaf(__uint_as_float(v[j + 1]), scale2, -m)) : 0.f;
+            pk[j >> 1] = pack_bf16x2(e0, e1);
+            ls += __uint_as_float(pk[j >> 1] << 16) + __uint_as_float(pk[j >> 1] & 0xFFFF0000u);
+          }
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+            st_shared16(pb + sw128_off(h, 4 * hf + c),
+                        make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]));
+        }
+        l += ls;
       }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(smem_u32(&X.p_full[bsel]));
     }
+    if (soft) { X.m_run[h] = m; X.l_run[h] = l; }
+    if (n > 0 && !X.abort)
+      mbar_wait(smem_u32(&X.pv_done[(n - 1) & 1]), (uint32_t)((n - 1) >> 1) & 1);
+    tc_fence_after();
   }
 
-  // ---- epilogue ----
+  // ---- epilogue (warps 0..3: warp w reads TMEM lanes 32w.. = dims mt*128 + 32w ..) ----
+  if (tid == 0 && n == 0) mbar_wait(smem_u32(&X.q_full), 0, 100000000ull);  // Q copy landed
   __syncthreads();
   if (nsplit == 1) {
-    // O^T / l -> bf16 [64 heads][512], staged in the KV tile, then coalesced stores
-    if (tid < 64) X.fac[tid] = 1.f / X.l_run[tid];
+    // O^T / l -> bf16 [64 heads][512], staged in the KV buffers, then coalesced stores
+    if (tid < 64) X.fac[0][tid] = 1.f / X.l_run[tid];
     __syncthreads();
     uint16_t* stage = reinterpret_cast<uint16_t*>(kv_s);
-    if (warp < 8) {
-      const int sub = warp & 3;
-      const uint32_t lrow = (uint32_t)(sub * 32) << 16;
+    if (warp < 4) {
+      const uint32_t lrow = (uint32_t)(warp * 32) << 16;
 #pragma unroll 1
-      for (int mi = 0; mi < 2; ++mi) {
-        const int mt = 2 * (warp >> 2) + mi;
-        const int dim = mt * 128 + sub * 32 + lane;
+      for (int mt = 0; mt < 4; ++mt) {
+        const int dim = mt * 128 + warp * 32 + lane;
 #pragma unroll
         for (int hb = 0; hb < 64; hb += 32) {
           uint32_t v[32];
@@ -415,7 +464,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(AttnArgs a) {
           tmem_ld_wait();
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
-            const float o = ntile > 0 ? __uint_as_float(v[j]) * X.fac[hb + j] : 0.f;
+            const float o = n > 0 ? __uint_as_float(v[j]) * X.fac[0][hb + j] : 0.f;
             __nv_bfloat16 bv = __float2bfloat16_rn(o);
             stage[(hb + j) * kDLat + dim] = *reinterpret_cast<uint16_t*>(&bv);
           }
@@ -433,17 +482,15 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(AttnArgs a) {
     // partial O^T (unnormalised fp32) -> workspace [Q][nsplit][64 heads][512], plus the
     // running max (log2 units) and sum per head
     float* po = a.part_o + ((int64_t)q * nsplit + rank) * kHeads * kDLat;
-    if (warp < 8) {
-      const int sub = warp & 3;
-      const uint32_t lrow = (uint32_t)(sub * 32) << 16;
+    if (warp < 4) {
+      const uint32_t lrow = (uint32_t)(warp * 32) << 16;
 #pragma unroll 1
-      for (int mi = 0; mi < 2; ++mi) {
-        const int mt = 2 * (warp >> 2) + mi;
-        const int dim = mt * 128 + sub * 32 + lane;
+      for (int mt = 0; mt < 4; ++mt) {
+        const int dim = mt * 128 + warp * 32 + lane;
 #pragma unroll
         for (int hb = 0; hb < 64; hb += 32) {
           uint32_t v[32];
-          if (ntile > 0) {
+          if (n > 0) {
             tmem_ld32(tmem + lrow + kColO + 64 * mt + hb, v);
             tmem_ld_wait();
           } else {
@@ -463,12 +510,12 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(AttnArgs a) {
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 8) tmem_dealloc(tmem, 512);
+  if (warp == kMmaWarp) tmem_dealloc(tmem, 512);
 }
 
 // Merge of the nsplit partials of each query: grid = Q x 8, each CTA 8 heads.
 __global__ void __launch_bounds__(256) attn_combine_kernel(AttnArgs a, int nsplit) {
-  __shared__ float coef[8][8];  // [split][head within the CTA]
+  __shared__ float coef[kMaxChunks][8];  // [split][head within the CTA]
   __shared__ float lse2[8];
   const int q = blockIdx.x, h0 = blockIdx.y * 8, tid = threadIdx.x;
   griddep_launch_dependents();
@@ -513,24 +560,30 @@ __global__ void __launch_bounds__(256) attn_combine_kernel(AttnArgs a, int nspli
 
 }  // namespace
 
-size_t attn_smem_bytes() { return 1024 + kQBytes + kKVBytes + kPBytes + sizeof(Aux); }
+size_t attn_smem_bytes() {
+  return 1024 + kQBytes + 2 * kBufBytes + 2 * kPBytes + sizeof(Aux);
+}
 
 // CTAs per query: as many as keep every CTA of the launch in one wave (one CTA per SM),
-// at most one tile each.
+// at least one chunk each.
 int attn_num_splits(int Q, int nsel, int num_sms) {
-  const int ntiles = 1 + (nsel + 127) / 128;
+  const int nchunks = 2 + (nsel + kChunk - 1) / kChunk;
   int nsplit = num_sms / (Q > 0 ? Q : 1);
-  return nsplit < 1 ? 1 : (nsplit > ntiles ? ntiles : nsplit);
+  return nsplit < 1 ? 1 : (nsplit > nchunks ? nchunks : nsplit);
 }
 
 cudaError_t launch_attn(const AttnArgs& a, int nsplit, cudaStream_t s) {
   if (a.Q == 0) return cudaSuccess;
+  // Q of each query as eight boxes of 64 heads x 64 dims
+  CUtensorMap qm;
+  if (!encode_rows_bf16(&qm, a.q, (uint64_t)a.Q * kHeads, kDLat, 64, 64))
+    return cudaErrorInvalidValue;
   const size_t smem = attn_smem_bytes();
   cudaError_t e = cudaFuncSetAttribute(sparse_attn_kernel,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   e = launch_pdl(sparse_attn_kernel, dim3((unsigned)nsplit, (unsigned)a.Q), dim3(kThreads), smem,
-                 s, a);
+                 s, a, qm);
   if (e != cudaSuccess || nsplit == 1) return e;
   return launch_pdl(attn_combine_kernel, dim3((unsigned)a.Q, kHeads / 8), dim3(256), 0, s, a,
                     nsplit);

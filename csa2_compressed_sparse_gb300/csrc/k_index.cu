@@ -18,8 +18,6 @@
 //               (tiles of parity e) -> relu * w -> sum -> order-preserving key
 // TMEM holds two 256-column fp32 accumulators, so two tiles are in the epilogue while
 // the MMAs of the next one run.  The scores are written as uint32 keys for the top-k.
-#include <cudaTypedefs.h>
-
 #include "common.cuh"
 
 CSA2_DEFINE_FAULT_FLAG(index)
@@ -446,32 +444,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 1) tmem_dealloc(tmem, 512);
 }
 
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  if (!fn) {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult qr;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                         &qr) == cudaSuccess &&
-        qr == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-  }
-  return fn;
-}
-
-bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint32_t box_rows) {
-  auto fn = encode_fn();
-  if (!fn) return false;
-  cuuint64_t dims[2] = {(cuuint64_t)kDIdx, (cuuint64_t)rows};
-  cuuint64_t strides[1] = {(cuuint64_t)kDIdx * 2};
-  cuuint32_t box[2] = {64, box_rows};
-  cuuint32_t estr[2] = {1, 1};
-  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
-                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS;
-}
-
 }  // namespace
 
 size_t index_smem_bytes() {
@@ -484,9 +456,9 @@ cudaError_t launch_index(const IndexArgs& a, int num_sms, cudaStream_t s) {
   cudaError_t e = launch_pdl(index_prep_kernel, dim3(1), dim3(kPrepThreads), 0, s, a, a.tmp);
   if (e != cudaSuccess) return e;
   CUtensorMap kt, kb, qm;
-  if (!make_map(&kt, a.index_k, (uint64_t)a.index_rows, kTileRows) ||
-      !make_map(&kb, a.index_k, (uint64_t)a.index_rows, 8) ||
-      !make_map(&qm, a.iq, (uint64_t)a.Q * a.H, (uint32_t)a.H))
+  if (!encode_rows_bf16(&kt, a.index_k, (uint64_t)a.index_rows, kDIdx, 64, kTileRows) ||
+      !encode_rows_bf16(&kb, a.index_k, (uint64_t)a.index_rows, kDIdx, 64, 8) ||
+      !encode_rows_bf16(&qm, a.iq, (uint64_t)a.Q * a.H, kDIdx, 64, (uint32_t)a.H))
     return cudaErrorInvalidValue;
   const size_t smem = index_smem_bytes();
   e = cudaFuncSetAttribute(index_score_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,

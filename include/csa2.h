@@ -193,8 +193,10 @@ csa2_status csa2_topk_scores(const float* scores, const int32_t* n, int Q, int64
  *                  lin_base[b] + pos - lin_pos0[b]
  *          BF16 rows are 512 bf16; FP8_S128 rows are 528 bytes: 512 E4M3 codes then
  *          four fp32 scales, value = code * scale[d / 128]
- *          n_rows = rows in data (indices beyond raise CSA2_EBOUNDS and are skipped)
- *   plane  [plane_rows][512] bf16;  row_base int64;  sel [Q][nsel] int32, nsel <= 512
+ *          n_rows = rows in data, < 2^31 (indices beyond raise CSA2_EBOUNDS and are
+ *          skipped)
+ *   plane  [plane_rows][512] bf16, plane_rows < 2^31;  row_base int64;
+ *          sel [Q][nsel] int32, nsel <= 512
  *          (sel may be NULL with nsel == 0: window only)
  *   sink   [64] fp32 or NULL (no sink term);  scale: softmax temperature (1/sqrt(512))
  *   out    [Q][64][512] bf16;  lse [Q][64] fp32 or NULL

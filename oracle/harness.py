@@ -9,6 +9,7 @@ GPU output into the oracle.
 from functools import lru_cache
 
 import numpy as np
+import torch
 
 import synth
 
@@ -110,7 +111,9 @@ def window_rows(wl, q, layer):
     return dict(swa=lin, swa_mode="linear", lin_base=[0], lin_pos0=[lo])
 
 
-def oracle_attn(wl, key, q, sel, layer=0):
+def oracle_attn(wl, key, q, sel, layer=0, head_scale=None):
+    """Oracle output and lse of query q over its window and `sel`.  `head_scale`
+    (optional, 64 powers of two) multiplies the query of each head, exactly in bf16."""
     b = int(wl.q_seq[q])
     hs = host_seq(key, b)
     sel = np.asarray(sel, dtype=np.int32)
@@ -119,6 +122,9 @@ def oracle_attn(wl, key, q, sel, layer=0):
     sel_c = np.full(len(sel), -1, dtype=np.int32)
     sel_c[valid] = np.arange(int(valid.sum()), dtype=np.int32)
     qh = wl.host_q(q, layer).view(1, 64, 512)
+    if head_scale is not None:
+        hsc = torch.as_tensor(np.asarray(head_scale, dtype=np.float64)).view(1, 64, 1)
+        qh = (qh.double() * hsc).to(torch.bfloat16)  # exact for powers of two
     win = window_rows(wl, q, layer)
     sink = synth.normal_f32(64, wl.seed, synth.SINK)
     out, lse = sparse_attn(qh, [0], [int(wl.q_pos[q])], win["swa"],

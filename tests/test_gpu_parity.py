@@ -255,6 +255,32 @@ def test_attention_split_and_unsplit_agree_with_the_oracle():
             assert np.abs(lse[q].cpu().numpy() - ref_lse).max() < 1e-2
 
 
+def test_attention_running_max_rescale_paths():
+    """Queries of heads 0..31 scaled by 2^8 (exact in bf16): their scores spread over
+    hundreds of nats, so later chunks overtake the running max by far more than the
+    lazy threshold and the O^T rescale runs; heads 32..63 keep the plain path."""
+    from csa2_compressed_sparse_gb300 import (csa2_attn_workspace_size, csa2_device_status,
+                                              csa2_sparse_attn)
+    from csa2_compressed_sparse_gb300.step import swa_of
+    wl = W.decode_batch(B=5, lo=300, hi=7000, seed=28)
+    t, spec, buf = run_workload(wl)
+    key = register(wl)
+    hs = np.ones(64)
+    hs[:32] = 256.0
+    qs = (t["q"][0].double() * torch.tensor(hs, device="cuda").view(1, 64, 1)).to(torch.bfloat16)
+    nb = csa2_attn_workspace_size(wl.Q, spec.k)
+    for ws in (None, torch.empty(nb, dtype=torch.uint8, device="cuda")):
+        out = torch.empty_like(buf.out[0])
+        lse = torch.empty((wl.Q, 64), dtype=torch.float32, device="cuda")
+        csa2_sparse_attn(qs, t["q_seq"], t["q_pos"], swa_of(spec, t, 0), t["plane"],
+                         t["row_base"], buf.sel, t["sink"], out, lse=lse, ws=ws)
+        csa2_device_status()
+        for q in range(wl.Q):
+            ref, ref_lse = oracle_attn(wl, key, q, buf.sel[q].cpu().numpy(), head_scale=hs)
+            check_attn(out[q].float().cpu().numpy(), ref)
+            assert np.abs(lse[q].cpu().numpy() - ref_lse).max() < 2e-2
+
+
 def test_bounds_fault_is_reported_and_recoverable():
     from csa2_compressed_sparse_gb300 import (Csa2Error, Swa, csa2_device_status,
                                               csa2_sparse_attn)
