@@ -16,11 +16,12 @@
 //            (bf16 rows by 16-byte cp.async, FP8 rows dequantised to bf16).  Row
 //            gathers reach the HBM rate only with many requests in flight per SM, so
 //            most of the CTA's threads are gatherers
-//   S        = Q[64 x 512] . KV^T[512 x 64] -> TMEM buffer b: lane = head, column =
-//            row.  The MMA is M = 128; its upper 64 rows read the next 8 KiB of shared
-//            memory and land in TMEM lanes 64..127, which nothing reads
-//   softmax  thread h (warps 0, 1) owns head h: its running max m_h and sum l_h stay
-//            in registers and every reduction is over its own 64 columns.  P uses the
+//   S        = Q[64 x 512] . KV^T[512 x 64] -> TMEM buffer b as two M = 64 accumulators
+//            (dims 0..255 and 256..511, issued by two threads): head h in lane
+//            32 (h / 16) + h % 16, column = row
+//   softmax  warps 0..3, four threads per pair of heads (16x256b TMEM loads): running
+//            max and partial sums in registers, reductions over the thread's own
+//            columns plus two shuffles where a head's four threads must agree.  P uses the
 //            running max, which moves only when a score exceeds it by more than 64
 //            (log2 units: P <= 2^64 keeps bf16 P and the fp32 sums finite); then
 //            warps 0..3 rescale O^T in TMEM, decided by one barrier vote
@@ -32,8 +33,8 @@
 // and writes the output.  Otherwise every CTA writes its partial (max, sum, O) to the
 // workspace and attn_combine_kernel merges them, adding the sink's e^{sink_h} once.
 //
-// Warps 0..3 softmax (0, 1) + O^T rescale + output, warps 4..19 gather (teams of eight
-// warps), warp 20 owns the TMEM allocation and its lane 0 issues every tcgen05.mma.
+// Warps 0..3 softmax + O^T rescale + output, warps 4..19 gather (teams of eight
+// warps), warps 20..22 issue the MMAs (lane 0 each; warp 20 also owns the TMEM).
 #include <cuda_fp8.h>
 
 #include "common.cuh"
@@ -43,19 +44,20 @@ CSA2_DEFINE_FAULT_FLAG(attn)
 namespace csa2 {
 namespace {
 
-constexpr int kThreads = 672;             // 21 warps
+constexpr int kThreads = 736;             // 23 warps
 constexpr int kGroupThreads = 128;        // warps 0..3
 constexpr int kTeam = 256;                // threads per gather team
 constexpr int kGatherWarp0 = 4;
-constexpr int kMmaWarp = 20;
+constexpr int kMmaWarp = 20;              // warps 20..22 issue the MMAs
 constexpr int kChunk = 64;                // rows per chunk
 constexpr int kMaxChunks = 10;            // 2 window + 8 selected chunks
 constexpr int kDimBlock = 64 * 128;       // one 64-dim block of 64 rows (8 KiB)
 constexpr int kQBytes = 8 * kDimBlock;    // Q [8 dim blocks][64 heads][128 B]
 constexpr int kBufBytes = 8 * kDimBlock;  // KV [8 dim blocks][64 rows][128 B]
 constexpr int kPBytes = 64 * 128;         // P [64 heads][64 rows] bf16
-constexpr uint32_t kColS = 0;             // TMEM columns of S buffer b: 64 b
-constexpr uint32_t kColO = 128;           // O^T tiles at 128 + 64 * mt
+constexpr uint32_t kColSa = 0;            // TMEM columns of S buffer b, dims 0..255: 64 b
+constexpr uint32_t kColSb = 128;          // the same for dims 256..511: 128 + 64 b
+constexpr uint32_t kColO = 256;           // O^T tiles at 256 + 64 * mt
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLazy = 64.0f;
 
@@ -68,10 +70,10 @@ struct __align__(16) Aux {
   int chunks[kMaxChunks];              // non-empty slots, in order
   uint64_t q_full;      // Q landed (TMA transaction count)
   uint64_t kv_full[2];  // KV buffer filled (one arrival of the team)
-  uint64_t s_full[2];   // S buffer written (commit)
+  uint64_t s_full[2];   // both S halves of the buffer written (two commits)
   uint64_t p_full[2];   // P buffer written and O^T rescaled (128 arrivals)
   uint64_t pv_done[2];  // PV of the buffer's chunk complete (commit)
-  uint64_t fin;         // every MMA of the CTA complete (commit)
+  uint64_t fin[3];      // every MMA of an issuer complete (commit)
   uint32_t tmem_slot;
   int nchunk;
   int abort;
@@ -171,11 +173,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(smem_u32(&X.q_full), 1);
     for (int b = 0; b < 2; ++b) {
       mbar_init(smem_u32(&X.kv_full[b]), 1);
-      mbar_init(smem_u32(&X.s_full[b]), 1);
+      mbar_init(smem_u32(&X.s_full[b]), 2);
       mbar_init(smem_u32(&X.p_full[b]), kGroupThreads);
       mbar_init(smem_u32(&X.pv_done[b]), 1);
     }
-    mbar_init(smem_u32(&X.fin), 1);
+    for (int r = 0; r < 3; ++r) mbar_init(smem_u32(&X.fin[r]), 1);
     X.nchunk = 0;
     X.abort = 0;
     mbar_fence_init();
@@ -273,114 +275,159 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     // no copy may still be landing in shared memory when the CTA exits
     if (t == 0 && last >= 0) mbar_wait(full_bar, (uint32_t)(last >> 1) & 1, 100000000ull);
-  } else if (warp == kMmaWarp) {
-    // =================== MMA issuer (warp 20, lane 0) ===================
-    if (lane == 0 && n > 0 && mbar_wait(smem_u32(&X.q_full), 0)) {
-      const uint32_t id_s = idesc_bf16(128, 64, 0, 0);
-      const uint32_t id_o = idesc_bf16(128, 64, 1, 0);
-      int sn = 0, pn = 0;  // next chunk to score / to accumulate
-      uint64_t t0 = globaltimer_ns();
-      while (pn < n && !X.abort) {
-        bool progress = false;
-        // S of chunk sn reuses TMEM buffer sn & 1 once the softmax of chunk sn - 2 has
-        // released it, i.e. once that chunk's PV has been issued (sn <= pn + 1)
-        if (sn < n && sn <= pn + 1 &&
-            mbar_test_wait(smem_u32(&X.kv_full[sn & 1]), (uint32_t)(sn >> 1) & 1)) {
+  } else if (warp >= kMmaWarp) {
+    // ====== MMA issuers (lane 0): warp 20 S over dims 0..255, warp 21 S over dims
+    // 256..511 (two accumulators, summed by the softmax), warp 22 PV ======
+    // One thread issues a tcgen05.mma about every 28 ns however small it is, so the
+    // chunk's 48 small MMAs are spread over three threads.
+    const int role = warp - kMmaWarp;
+    if (lane == 0 && n > 0) {
+      int issued = 0;
+      if (role < 2) {
+        const uint32_t id_s = idesc_bf16(64, 64, 0, 0);
+        if (!mbar_wait(smem_u32(&X.q_full), 0)) X.abort = 1;
+        for (int c = 0; c < n && !X.abort; ++c) {
+          // kv_full of chunk c also means that the softmax of chunk c - 2 is done with
+          // S buffer c & 1 (the gather of chunk c waited for the PV of chunk c - 2)
+          if (!mbar_wait(smem_u32(&X.kv_full[c & 1]), (uint32_t)(c >> 1) & 1)) {
+            X.abort = 1;
+            break;
+          }
           tc_fence_after();
-          const uint32_t kvb = kv0 + (sn & 1) * kBufBytes;
-          const uint32_t d = tmem + kColS + 64 * (sn & 1);
+          const uint32_t kvb = kv0 + (c & 1) * kBufBytes;
+          const uint32_t d = tmem + (role ? kColSb : kColSa) + 64 * (c & 1);
 #pragma unroll
-          for (int db = 0; db < 8; ++db)
+          for (int i = 0; i < 4; ++i) {
+            const int db = 4 * role + i;
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
               umma_bf16(d, sdesc_sw128(qb + db * kDimBlock + kk * 32, 16, 1024),
                         sdesc_sw128(kvb + db * kDimBlock + kk * 32, 16, 1024), id_s,
-                        (db | kk) != 0);
-          umma_commit(smem_u32(&X.s_full[sn & 1]));
-          ++sn;
-          progress = true;
+                        (i | kk) != 0);
+          }
+          umma_commit(smem_u32(&X.s_full[c & 1]));
+          ++issued;
         }
-        if (pn < sn && mbar_test_wait(smem_u32(&X.p_full[pn & 1]), (uint32_t)(pn >> 1) & 1)) {
+      } else {
+        const uint32_t id_o = idesc_bf16(128, 64, 1, 0);
+        for (int c = 0; c < n && !X.abort; ++c) {
+          if (!mbar_wait(smem_u32(&X.p_full[c & 1]), (uint32_t)(c >> 1) & 1)) {
+            X.abort = 1;
+            break;
+          }
           tc_fence_after();
-          const uint32_t kvb = kv0 + (pn & 1) * kBufBytes;
-          const uint32_t pb = p0 + (pn & 1) * kPBytes;
+          const uint32_t kvb = kv0 + (c & 1) * kBufBytes;
+          const uint32_t pb = p0 + (c & 1) * kPBytes;
 #pragma unroll
           for (int mt = 0; mt < 4; ++mt)
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
               umma_bf16(tmem + kColO + 64 * mt,
                         sdesc_sw128(kvb + 2 * mt * kDimBlock + kk * 2048, kDimBlock, 1024),
-                        sdesc_sw128(pb + kk * 32, 16, 1024), id_o, (pn > 0 || kk > 0) ? 1 : 0);
-          umma_commit(smem_u32(&X.pv_done[pn & 1]));
-          ++pn;
-          progress = true;
-        }
-        if (progress) {
-          t0 = globaltimer_ns();
-        } else if (globaltimer_ns() - t0 > 2000000000ull) {
-          raise_fault(kFaultTimeout);
-          X.abort = 1;
+                        sdesc_sw128(pb + kk * 32, 16, 1024), id_o, (c > 0 || kk > 0) ? 1 : 0);
+          umma_commit(smem_u32(&X.pv_done[c & 1]));
+          ++issued;
         }
       }
       // no MMA may still be running when the TMEM is released, whatever happened above
-      if (sn > 0) {
-        umma_commit(smem_u32(&X.fin));
-        mbar_wait(smem_u32(&X.fin), 0, 100000000ull);
+      if (issued > 0) {
+        umma_commit(smem_u32(&X.fin[role]));
+        mbar_wait(smem_u32(&X.fin[role]), 0, 100000000ull);
       }
     }
-  } else if (warp < kGatherWarp0) {
-    // ========== softmax (warps 0, 1: thread h = head h) + O^T rescale (warps 0..3) ==========
-    const bool soft = warp < 2;
-    const int h = tid;  // head of a softmax thread (TMEM lane h)
+  } else {
+    // ============ softmax + O^T rescale (warps 0..3) ============
+    // S of a chunk is the sum of two M = 64 accumulators; head 16 w + i sits in TMEM lane
+    // 32 w + i.  A 16x256b load of column group g gives thread t of warp w the columns
+    // 8 g + 2 (t % 4) + {0, 1} of heads hA = 16 w + t / 4 and hB = hA + 8, so the four
+    // threads with the same t / 4 share two heads: each keeps the running max of both
+    // (kept equal across the four) and a partial running sum over its own columns.
+    const int r4 = lane & 3;
+    const int hA = 16 * warp + (lane >> 2), hB = hA + 8;
     const uint32_t lrow = (uint32_t)(warp * 32) << 16;
-    float m = -INFINITY, l = 0.f;
-    if (soft && nsplit == 1 && a.sink) { m = a.sink[h] * kLog2e; l = 1.f; }
+    float mA = -INFINITY, mB = -INFINITY, lA = 0.f, lB = 0.f;
+    if (nsplit == 1 && a.sink) {
+      mA = a.sink[hA] * kLog2e;
+      mB = a.sink[hB] * kLog2e;
+      if (r4 == 0) { lA = 1.f; lB = 1.f; }
+    }
     for (int it = 0; it < n; ++it) {
       const int bsel = it & 1;
       const uint32_t ph = (uint32_t)(it >> 1) & 1;
       const int slot = X.chunks[it];
       const uint32_t mlo = X.rowmask[slot][0], mhi = X.rowmask[slot][1];
       const bool full = (mlo & mhi) == 0xFFFFFFFFu;
-      bool need = false;
-      if (soft) {
-        if (!X.abort && !mbar_wait(smem_u32(&X.s_full[bsel]), ph)) X.abort = 1;
-        tc_fence_after();
-        // largest s_j - m over the valid rows (log2 units) decides a rescale
-        float mx = -INFINITY;
+      const uint32_t sa = tmem + lrow + kColSa + 64 * bsel;
+      const uint32_t sb = tmem + lrow + kColSb + 64 * bsel;
+      if (!X.abort && !mbar_wait(smem_u32(&X.s_full[bsel]), ph)) X.abort = 1;
+      tc_fence_after();
+      // largest s - m over this thread's valid columns, per head (log2 units)
+      float mxA = -INFINITY, mxB = -INFINITY;
 #pragma unroll 1
-        for (int hf = 0; hf < 2; ++hf) {
-          uint32_t v[32];
-          tmem_ld32(tmem + lrow + kColS + 64 * bsel + 32 * hf, v);
+      for (int gb = 0; gb < 8; gb += 4) {
+        uint32_t x[4][4], y[4][4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          tmem_ld_16x256b(sa + 8 * (gb + i), x[i]);
+          tmem_ld_16x256b(sb + 8 * (gb + i), y[i]);
+        }
+        tmem_ld_wait();
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int g = gb + i;
+          const uint32_t mk = full ? 3u : ((g < 4 ? mlo : mhi) >> (8 * (g & 3) + 2 * r4)) & 3u;
+          const float s0 = __uint_as_float(x[i][0]) + __uint_as_float(y[i][0]);
+          const float s1 = __uint_as_float(x[i][1]) + __uint_as_float(y[i][1]);
+          const float s2 = __uint_as_float(x[i][2]) + __uint_as_float(y[i][2]);
+          const float s3 = __uint_as_float(x[i][3]) + __uint_as_float(y[i][3]);
+          if (mk & 1u) {
+            mxA = fmaxf(mxA, fmaf(s0, scale2, -mA));
+            mxB = fmaxf(mxB, fmaf(s2, scale2, -mB));
+          }
+          if (mk & 2u) {
+            mxA = fmaxf(mxA, fmaf(s1, scale2, -mA));
+            mxB = fmaxf(mxB, fmaf(s3, scale2, -mB));
+          }
+        }
+      }
+      // a head moves its running max when any of its four threads saw a score above it
+      // by more than the lazy threshold; the four decide together
+      uint32_t nA = !(mxA <= kLazy), nB = !(mxB <= kLazy);
+      nA |= __shfl_xor_sync(0xFFFFFFFFu, nA, 1);
+      nA |= __shfl_xor_sync(0xFFFFFFFFu, nA, 2);
+      nB |= __shfl_xor_sync(0xFFFFFFFFu, nB, 1);
+      nB |= __shfl_xor_sync(0xFFFFFFFFu, nB, 2);
+      const bool need = (nA | nB) != 0u;
+      float facA = 1.f, facB = 1.f;
+      if (__any_sync(0xFFFFFFFFu, need)) {
+        // new running max: the chunk's largest score of the head (the old one may be -inf)
+        float smA = -INFINITY, smB = -INFINITY;
+#pragma unroll 1
+        for (int g = 0; g < 8; ++g) {
+          uint32_t x[4], y[4];
+          tmem_ld_16x256b(sa + 8 * g, x);
+          tmem_ld_16x256b(sb + 8 * g, y);
           tmem_ld_wait();
-          const uint32_t mk = full ? 0xFFFFFFFFu : (hf ? mhi : mlo);
-#pragma unroll
-          for (int j = 0; j < 32; ++j)
-            if ((mk >> j) & 1u) mx = fmaxf(mx, fmaf(__uint_as_float(v[j]), scale2, -m));
-        }
-        need = !(mx <= kLazy);
-        // tcgen05.ld is warp-collective: the whole warp reloads when any lane needs it
-        if (__any_sync(0xFFFFFFFFu, need)) {
-          // new running max: the chunk's largest score (the previous max may be -inf)
-          float sm = -INFINITY;
-#pragma unroll 1
-          for (int hf = 0; hf < 2; ++hf) {
-            uint32_t v[32];
-            tmem_ld32(tmem + lrow + kColS + 64 * bsel + 32 * hf, v);
-            tmem_ld_wait();
-            const uint32_t mk = full ? 0xFFFFFFFFu : (hf ? mhi : mlo);
-#pragma unroll
-            for (int j = 0; j < 32; ++j)
-              if ((mk >> j) & 1u) sm = fmaxf(sm, __uint_as_float(v[j]) * scale2);
+          const uint32_t mk = full ? 3u : ((g < 4 ? mlo : mhi) >> (8 * (g & 3) + 2 * r4)) & 3u;
+          if (mk & 1u) {
+            smA = fmaxf(smA, (__uint_as_float(x[0]) + __uint_as_float(y[0])) * scale2);
+            smB = fmaxf(smB, (__uint_as_float(x[2]) + __uint_as_float(y[2])) * scale2);
           }
-          const float fac = need ? ex2(m - sm) : 1.f;  // 0 when m = -inf
-          X.fac[bsel][h] = fac;
-          if (need) {
-            l *= fac;
-            m = sm;
+          if (mk & 2u) {
+            smA = fmaxf(smA, (__uint_as_float(x[1]) + __uint_as_float(y[1])) * scale2);
+            smB = fmaxf(smB, (__uint_as_float(x[3]) + __uint_as_float(y[3])) * scale2);
           }
-        } else {
-          X.fac[bsel][h] = 1.f;
         }
+        smA = fmaxf(smA, __shfl_xor_sync(0xFFFFFFFFu, smA, 1));
+        smA = fmaxf(smA, __shfl_xor_sync(0xFFFFFFFFu, smA, 2));
+        smB = fmaxf(smB, __shfl_xor_sync(0xFFFFFFFFu, smB, 1));
+        smB = fmaxf(smB, __shfl_xor_sync(0xFFFFFFFFu, smB, 2));
+        if (nA) { facA = ex2(mA - smA); mA = smA; lA *= facA; }  // fac = 0 when m was -inf
+        if (nB) { facB = ex2(mB - smB); mB = smB; lB *= facB; }
+      }
+      if (r4 == 0) {
+        X.fac[bsel][hA] = facA;
+        X.fac[bsel][hB] = facB;
       }
       if (group_any(need) && it > 0) {
         // O^T columns are heads: scale column h of every O tile by fac[h] once the PV of
@@ -405,40 +452,58 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tmem_st_wait();
       }
-      if (soft) {
-        // the P buffer was last read by the PV of chunk it - 2
-        if (it >= 2 && !X.abort &&
-            !mbar_wait(smem_u32(&X.pv_done[bsel]), (uint32_t)((it - 2) >> 1) & 1))
-          X.abort = 1;
-        const uint32_t pb = p0 + bsel * kPBytes;
-        float ls = 0.f;
+      // the P buffer was last read by the PV of chunk it - 2
+      if (it >= 2 && !X.abort &&
+          !mbar_wait(smem_u32(&X.pv_done[bsel]), (uint32_t)((it - 2) >> 1) & 1))
+        X.abort = 1;
+      // P [head][row] bf16, 128-byte swizzled rows: thread t writes 4 bytes (two rows) of
+      // heads hA and hB in each 16-byte chunk g
+      const uint32_t pA = p0 + bsel * kPBytes + hA * 128 + 4 * r4;
+      const uint32_t pB = p0 + bsel * kPBytes + hB * 128 + 4 * r4;
+      const int sw = hA & 7;  // hB & 7 is the same
 #pragma unroll 1
-        for (int hf = 0; hf < 2; ++hf) {
-          uint32_t v[32];
-          tmem_ld32(tmem + lrow + kColS + 64 * bsel + 32 * hf, v);
-          tmem_ld_wait();
-          const uint32_t mk = full ? 0xFFFFFFFFu : (hf ? mhi : mlo);
-          uint32_t pk[16];
+      for (int gb = 0; gb < 8; gb += 4) {
+        uint32_t x[4][4], y[4][4];
 #pragma unroll
-          for (int j = 0; j < 32; j += 2) {
-            const float e0 = ((mk >> j) & 1u) ? ex2(fmaf(__uint_as_float(v[j]), scale2, -m)) : 0.f;
-            const float e1 =
-                ((mk >> (j + 1)) & 1u) ? ex2(fmaf(__uint_as_float(v[j + 1]), scale2, -m)) : 0.f;
-            pk[j >> 1] = pack_bf16x2(e0, e1);
-            ls += __uint_as_float(pk[j >> 1] << 16) + __uint_as_float(pk[j >> 1] & 0xFFFF0000u);
-          }
-#pragma unroll
-          for (int c = 0; c < 4; ++c)
-            st_shared16(pb + sw128_off(h, 4 * hf + c),
-                        make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]));
+        for (int i = 0; i < 4; ++i) {
+          tmem_ld_16x256b(sa + 8 * (gb + i), x[i]);
+          tmem_ld_16x256b(sb + 8 * (gb + i), y[i]);
         }
-        l += ls;
+        tmem_ld_wait();
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int g = gb + i;
+          const uint32_t mk = full ? 3u : ((g < 4 ? mlo : mhi) >> (8 * (g & 3) + 2 * r4)) & 3u;
+          const float s0 = __uint_as_float(x[i][0]) + __uint_as_float(y[i][0]);
+          const float s1 = __uint_as_float(x[i][1]) + __uint_as_float(y[i][1]);
+          const float s2 = __uint_as_float(x[i][2]) + __uint_as_float(y[i][2]);
+          const float s3 = __uint_as_float(x[i][3]) + __uint_as_float(y[i][3]);
+          const float e0 = (mk & 1u) ? ex2(fmaf(s0, scale2, -mA)) : 0.f;
+          const float e1 = (mk & 2u) ? ex2(fmaf(s1, scale2, -mA)) : 0.f;
+          const float e2 = (mk & 1u) ? ex2(fmaf(s2, scale2, -mB)) : 0.f;
+          const float e3 = (mk & 2u) ? ex2(fmaf(s3, scale2, -mB)) : 0.f;
+          const uint32_t qa = pack_bf16x2(e0, e1), qb2 = pack_bf16x2(e2, e3);
+          lA += __uint_as_float(qa << 16) + __uint_as_float(qa & 0xFFFF0000u);
+          lB += __uint_as_float(qb2 << 16) + __uint_as_float(qb2 & 0xFFFF0000u);
+          st_shared32(pA + ((g ^ sw) << 4), qa);
+          st_shared32(pB + ((g ^ sw) << 4), qb2);
+        }
       }
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(smem_u32(&X.p_full[bsel]));
     }
-    if (soft) { X.m_run[h] = m; X.l_run[h] = l; }
+    // running sums of the four threads of each head
+    lA += __shfl_xor_sync(0xFFFFFFFFu, lA, 1);
+    lA += __shfl_xor_sync(0xFFFFFFFFu, lA, 2);
+    lB += __shfl_xor_sync(0xFFFFFFFFu, lB, 1);
+    lB += __shfl_xor_sync(0xFFFFFFFFu, lB, 2);
+    if (r4 == 0) {
+      X.m_run[hA] = mA;
+      X.l_run[hA] = lA;
+      X.m_run[hB] = mB;
+      X.l_run[hB] = lB;
+    }
     if (n > 0 && !X.abort)
       mbar_wait(smem_u32(&X.pv_done[(n - 1) & 1]), (uint32_t)((n - 1) >> 1) & 1);
     tc_fence_after();

@@ -221,6 +221,19 @@ __device__ __forceinline__ void umma_commit(uint32_t bar) {
 
 // 32 lanes x 32 consecutive 32-bit columns: thread t of the warp receives lane
 // (taddr.lane + t), columns taddr.col .. +31.
+// 16 TMEM lanes x 8 columns from (lane, column) = taddr: thread t receives lanes
+// t / 4 and t / 4 + 8, columns 2 (t % 4) and 2 (t % 4) + 1 of each, as
+// {(l, c), (l, c + 1), (l + 8, c), (l + 8, c + 1)}.
+__device__ __forceinline__ void tmem_ld_16x256b(uint32_t taddr, uint32_t (&r)[4]) {
+  asm volatile("tcgen05.ld.sync.aligned.16x256b.x1.b32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(taddr));
+}
+
+__device__ __forceinline__ void st_shared32(uint32_t addr, uint32_t v) {
+  asm volatile("st.shared.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
