@@ -101,6 +101,7 @@ struct AttnArgs {
   float* lse;
   float* part_o;   // [Q][nsplit][64][512] partial outputs (nsplit > 1)
   float* part_ml;  // [Q][nsplit][2][64] partial running max (log2) and sum
+  int cluster;     // nsplit == 2: the two CTAs of a query form a cluster and merge in place
 };
 
 cudaError_t launch_compress(const CompressArgs& a, cudaStream_t s);

@@ -75,9 +75,10 @@ size_t topk_ws_bytes(int Q, int64_t ld, int k) {
 }
 
 // Workspace of the split attention: partial O [nsplit][64][512] fp32 and (max, sum)
-// [nsplit][2][64] fp32 per query.
+// [nsplit][2][64] fp32 per query.  One or two CTAs per query need none (two merge in
+// distributed shared memory).
 size_t attn_ws_bytes(int Q, int nsplit) {
-  if (nsplit <= 1) return 0;
+  if (nsplit <= 2) return 0;
   return up256((size_t)Q * nsplit * 64 * 512 * 4) + up256((size_t)Q * nsplit * 128 * 4);
 }
 
@@ -115,8 +116,8 @@ csa2_status attn_common(const char* name, const csa2_bf16* q, int Q, const int32
   const int sms = num_sms();
   if (sms <= 0) return fail(CSA2_ECUDA, "%s: no CUDA device", name);
   int nsplit = csa2::attn_num_splits(Q, nsel, sms);
-  while (nsplit > 1 && (ws == nullptr || attn_ws_bytes(Q, nsplit) > ws_bytes)) --nsplit;
-  if (nsplit > 1) {
+  while (nsplit > 2 && (ws == nullptr || attn_ws_bytes(Q, nsplit) > ws_bytes)) --nsplit;
+  if (nsplit > 2) {
     a.part_o = static_cast<float*>(ws);
     a.part_ml = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) +
                                          up256((size_t)Q * nsplit * 64 * 512 * 4));

@@ -23,15 +23,18 @@
 //            max and partial sums in registers, reductions over the thread's own
 //            columns plus two shuffles where a head's four threads must agree.  P uses the
 //            running max, which moves only when a score exceeds it by more than 64
-//            (log2 units: P <= 2^64 keeps bf16 P and the fp32 sums finite); then
-//            warps 0..3 rescale O^T in TMEM, decided by one barrier vote
+//            (log2 units: P <= 2^64 keeps bf16 P and the fp32 sums finite).  P is
+//            written in one pass with the current max; when a head's max moved the
+//            chunk's pass is redone and warps 0..3 rescale O^T in TMEM (a barrier vote)
 //   O^T     += V^T[512 x 64] . P^T[64 x 64] -> TMEM, four M = 128 tiles; the KV buffer
 //            is the A operand again, read MN-major, and P [head][row] is the B operand
 // S of the next chunk runs while the softmax of this one does, and the gather of
 // chunk c + 2 starts as soon as the PV of chunk c has released its buffer.
 // With nsplit = 1 the CTA starts from the sink (running max = sink, running sum = 1)
-// and writes the output.  Otherwise every CTA writes its partial (max, sum, O) to the
-// workspace and attn_combine_kernel merges them, adding the sink's e^{sink_h} once.
+// and writes the output.  With nsplit = 2 the two CTAs of a query run as a cluster and
+// merge through distributed shared memory, each finishing half of the dims.  Otherwise
+// every CTA writes its partial (max, sum, O) to the workspace and attn_combine_kernel
+// merges them; the merges add the sink's e^{sink_h} once.
 //
 // Warps 0..3 softmax + O^T rescale + output, warps 4..19 gather (teams of eight
 // warps), warps 20..22 issue the MMAs (lane 0 each; warp 20 also owns the TMEM).
@@ -64,7 +67,9 @@ constexpr float kLazy = 64.0f;
 struct __align__(16) Aux {
   float m_run[64];
   float l_run[64];
-  float fac[2][64];  // rescale factor per head, by chunk parity (1 / l in the epilogue)
+  float fac[2][64];  // rescale factor per head, by chunk parity (merge weights at the end)
+  float peer_m[64];  // cluster merge: the other CTA's running max and sum (filled by a
+  float peer_l[64];  // bulk copy of its m_run, l_run: the pairs must stay adjacent)
   int32_t rowidx[kMaxChunks][kChunk];  // source row per slot (chunk = rank + slot * nsplit)
   uint32_t rowmask[kMaxChunks][2];     // valid rows of each slot
   int chunks[kMaxChunks];              // non-empty slots, in order
@@ -74,6 +79,7 @@ struct __align__(16) Aux {
   uint64_t p_full[2];   // P buffer written and O^T rescaled (128 arrivals)
   uint64_t pv_done[2];  // PV of the buffer's chunk complete (commit)
   uint64_t fin[3];      // every MMA of an issuer complete (commit)
+  uint64_t merge_full;  // cluster merge: the peer's pieces and (max, sum) landed
   uint32_t tmem_slot;
   int nchunk;
   int abort;
@@ -105,6 +111,69 @@ __device__ __forceinline__ bool group_any(bool pred) {
       : "r"((uint32_t)pred)
       : "memory");
   return r != 0;
+}
+
+// Valid-row bits of columns 8 g + 2 r4 and 8 g + 2 r4 + 1 of a chunk (bit 0, bit 1).
+__device__ __forceinline__ uint32_t col_mask(bool full, uint32_t mlo, uint32_t mhi, int g,
+                                             int r4) {
+  return full ? 3u : ((g < 4 ? mlo : mhi) >> (8 * (g & 3) + 2 * r4)) & 3u;
+}
+
+// One pass of a softmax thread over its 16 columns of heads hA and hB of a chunk's S
+// (the sum of the accumulators at sa and sb): P = 2^(s scale2 - m), zero for invalid
+// rows, stored as bf16 pairs into the P rows at pA / pB (swizzle sw); returns the sum
+// of the stored (rounded) values and the largest s scale2 - m over the valid columns.
+__device__ __forceinline__ void p_pass(uint32_t sa, uint32_t sb, bool full, uint32_t mlo,
+                                       uint32_t mhi, int r4, float scale2, float mA, float mB,
+                                       uint32_t pA, uint32_t pB, int sw, float& mxA, float& mxB,
+                                       float& lsA, float& lsB) {
+  mxA = -INFINITY; mxB = -INFINITY; lsA = 0.f; lsB = 0.f;
+#pragma unroll 1
+  for (int gb = 0; gb < 8; gb += 4) {
+    uint32_t x[4][4], y[4][4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      tmem_ld_16x256b(sa + 8 * (gb + i), x[i]);
+      tmem_ld_16x256b(sb + 8 * (gb + i), y[i]);
+    }
+    tmem_ld_wait();
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int g = gb + i;
+      const uint32_t mk = col_mask(full, mlo, mhi, g, r4);
+      const float t0 = fmaf(__uint_as_float(x[i][0]) + __uint_as_float(y[i][0]), scale2, -mA);
+      const float t1 = fmaf(__uint_as_float(x[i][1]) + __uint_as_float(y[i][1]), scale2, -mA);
+      const float t2 = fmaf(__uint_as_float(x[i][2]) + __uint_as_float(y[i][2]), scale2, -mB);
+      const float t3 = fmaf(__uint_as_float(x[i][3]) + __uint_as_float(y[i][3]), scale2, -mB);
+      if (mk & 1u) { mxA = fmaxf(mxA, t0); mxB = fmaxf(mxB, t2); }
+      if (mk & 2u) { mxA = fmaxf(mxA, t1); mxB = fmaxf(mxB, t3); }
+      const uint32_t qa = pack_bf16x2((mk & 1u) ? ex2(t0) : 0.f, (mk & 2u) ? ex2(t1) : 0.f);
+      const uint32_t qb = pack_bf16x2((mk & 1u) ? ex2(t2) : 0.f, (mk & 2u) ? ex2(t3) : 0.f);
+      lsA += __uint_as_float(qa << 16) + __uint_as_float(qa & 0xFFFF0000u);
+      lsB += __uint_as_float(qb << 16) + __uint_as_float(qb & 0xFFFF0000u);
+      st_shared32(pA + ((g ^ sw) << 4), qa);
+      st_shared32(pB + ((g ^ sw) << 4), qb);
+    }
+  }
+}
+
+// Output of O^T: lane l of a warp holds dim d (consecutive over the warp) and o[j] of
+// heads h0 + j.  Adjacent lanes swap one value per pair of heads so that each stores one
+// bf16 pair (dims d & ~1 and d | 1) of one head: even lanes head h0 + j, odd lanes head
+// h0 + j + 1.  out_q is out[q] = [64 heads][512] bf16.
+// (o holds fp32 bit patterns.)
+__device__ __forceinline__ void store_pairs(uint16_t* out_q, int d, int h0,
+                                            const uint32_t (&o)[32], int lane) {
+  const bool odd = (lane & 1) != 0;
+  uint32_t* base = reinterpret_cast<uint32_t*>(out_q);
+#pragma unroll
+  for (int j = 0; j < 32; j += 2) {
+    const float e = __uint_as_float(o[j]), f = __uint_as_float(o[j + 1]);
+    const float recv = __shfl_xor_sync(0xFFFFFFFFu, odd ? e : f, 1);
+    const uint32_t w = odd ? pack_bf16x2(recv, f) : pack_bf16x2(e, recv);
+    const int h = h0 + j + (odd ? 1 : 0);
+    base[(h * kDLat + (d & ~1)) >> 1] = w;
+  }
 }
 
 // Rows of one chunk into the KV buffer at `kvb` by the threads of a team (t = 0..255);
@@ -178,6 +247,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(smem_u32(&X.pv_done[b]), 1);
     }
     for (int r = 0; r < 3; ++r) mbar_init(smem_u32(&X.fin[r]), 1);
+    mbar_init(smem_u32(&X.merge_full), 1);
     X.nchunk = 0;
     X.abort = 0;
     mbar_fence_init();
@@ -361,46 +431,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t sb = tmem + lrow + kColSb + 64 * bsel;
       if (!X.abort && !mbar_wait(smem_u32(&X.s_full[bsel]), ph)) X.abort = 1;
       tc_fence_after();
-      // largest s - m over this thread's valid columns, per head (log2 units)
-      float mxA = -INFINITY, mxB = -INFINITY;
-#pragma unroll 1
-      for (int gb = 0; gb < 8; gb += 4) {
-        uint32_t x[4][4], y[4][4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          tmem_ld_16x256b(sa + 8 * (gb + i), x[i]);
-          tmem_ld_16x256b(sb + 8 * (gb + i), y[i]);
-        }
-        tmem_ld_wait();
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int g = gb + i;
-          const uint32_t mk = full ? 3u : ((g < 4 ? mlo : mhi) >> (8 * (g & 3) + 2 * r4)) & 3u;
-          const float s0 = __uint_as_float(x[i][0]) + __uint_as_float(y[i][0]);
-          const float s1 = __uint_as_float(x[i][1]) + __uint_as_float(y[i][1]);
-          const float s2 = __uint_as_float(x[i][2]) + __uint_as_float(y[i][2]);
-          const float s3 = __uint_as_float(x[i][3]) + __uint_as_float(y[i][3]);
-          if (mk & 1u) {
-            mxA = fmaxf(mxA, fmaf(s0, scale2, -mA));
-            mxB = fmaxf(mxB, fmaf(s2, scale2, -mB));
-          }
-          if (mk & 2u) {
-            mxA = fmaxf(mxA, fmaf(s1, scale2, -mA));
-            mxB = fmaxf(mxB, fmaf(s3, scale2, -mB));
-          }
-        }
-      }
-      // a head moves its running max when any of its four threads saw a score above it
-      // by more than the lazy threshold; the four decide together
-      uint32_t nA = !(mxA <= kLazy), nB = !(mxB <= kLazy);
-      nA |= __shfl_xor_sync(0xFFFFFFFFu, nA, 1);
-      nA |= __shfl_xor_sync(0xFFFFFFFFu, nA, 2);
-      nB |= __shfl_xor_sync(0xFFFFFFFFu, nB, 1);
-      nB |= __shfl_xor_sync(0xFFFFFFFFu, nB, 2);
-      const bool need = (nA | nB) != 0u;
-      float facA = 1.f, facB = 1.f;
-      if (__any_sync(0xFFFFFFFFu, need)) {
-        // new running max: the chunk's largest score of the head (the old one may be -inf)
+      // the P buffer was last read by the PV of chunk it - 2
+      if (it >= 2 && !X.abort &&
+          !mbar_wait(smem_u32(&X.pv_done[bsel]), (uint32_t)((it - 2) >> 1) & 1))
+        X.abort = 1;
+      // P [head][row] bf16, 128-byte swizzled rows: thread t writes 4 bytes (two rows) of
+      // heads hA and hB in each 16-byte chunk g
+      const uint32_t pA = p0 + bsel * kPBytes + hA * 128 + 4 * r4;
+      const uint32_t pB = p0 + bsel * kPBytes + hB * 128 + 4 * r4;
+      const int sw = hA & 7;  // hB & 7 is the same
+      float mxA, mxB, lsA, lsB, facA = 1.f, facB = 1.f;
+      bool need;
+      if (mA == -INFINITY) {
+        // no running max yet (first chunk, no sink; the same for every head): the chunk's
+        // largest score of each head first
         float smA = -INFINITY, smB = -INFINITY;
 #pragma unroll 1
         for (int g = 0; g < 8; ++g) {
@@ -408,7 +452,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_ld_16x256b(sa + 8 * g, x);
           tmem_ld_16x256b(sb + 8 * g, y);
           tmem_ld_wait();
-          const uint32_t mk = full ? 3u : ((g < 4 ? mlo : mhi) >> (8 * (g & 3) + 2 * r4)) & 3u;
+          const uint32_t mk = col_mask(full, mlo, mhi, g, r4);
           if (mk & 1u) {
             smA = fmaxf(smA, (__uint_as_float(x[0]) + __uint_as_float(y[0])) * scale2);
             smB = fmaxf(smB, (__uint_as_float(x[2]) + __uint_as_float(y[2])) * scale2);
@@ -422,9 +466,30 @@ __global__ void __launch_bounds__(kThreads, 1)
         smA = fmaxf(smA, __shfl_xor_sync(0xFFFFFFFFu, smA, 2));
         smB = fmaxf(smB, __shfl_xor_sync(0xFFFFFFFFu, smB, 1));
         smB = fmaxf(smB, __shfl_xor_sync(0xFFFFFFFFu, smB, 2));
-        if (nA) { facA = ex2(mA - smA); mA = smA; lA *= facA; }  // fac = 0 when m was -inf
-        if (nB) { facB = ex2(mB - smB); mB = smB; lB *= facB; }
+        mA = smA;
+        mB = smB;
+        facA = 0.f;
+        facB = 0.f;
+        need = true;
+        p_pass(sa, sb, full, mlo, mhi, r4, scale2, mA, mB, pA, pB, sw, mxA, mxB, lsA, lsB);
+      } else {
+        // P with the current running max; redone only if a head's four threads saw a
+        // score above it by more than the lazy threshold
+        p_pass(sa, sb, full, mlo, mhi, r4, scale2, mA, mB, pA, pB, sw, mxA, mxB, lsA, lsB);
+        mxA = fmaxf(mxA, __shfl_xor_sync(0xFFFFFFFFu, mxA, 1));
+        mxA = fmaxf(mxA, __shfl_xor_sync(0xFFFFFFFFu, mxA, 2));
+        mxB = fmaxf(mxB, __shfl_xor_sync(0xFFFFFFFFu, mxB, 1));
+        mxB = fmaxf(mxB, __shfl_xor_sync(0xFFFFFFFFu, mxB, 2));
+        const bool nA = !(mxA <= kLazy), nB = !(mxB <= kLazy);
+        need = nA || nB;
+        if (__any_sync(0xFFFFFFFFu, need)) {
+          if (nA) { facA = ex2(-mxA); mA += mxA; }
+          if (nB) { facB = ex2(-mxB); mB += mxB; }
+          p_pass(sa, sb, full, mlo, mhi, r4, scale2, mA, mB, pA, pB, sw, mxA, mxB, lsA, lsB);
+        }
       }
+      lA = lA * facA + lsA;
+      lB = lB * facB + lsB;
       if (r4 == 0) {
         X.fac[bsel][hA] = facA;
         X.fac[bsel][hB] = facB;
@@ -452,43 +517,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tmem_st_wait();
       }
-      // the P buffer was last read by the PV of chunk it - 2
-      if (it >= 2 && !X.abort &&
-          !mbar_wait(smem_u32(&X.pv_done[bsel]), (uint32_t)((it - 2) >> 1) & 1))
-        X.abort = 1;
-      // P [head][row] bf16, 128-byte swizzled rows: thread t writes 4 bytes (two rows) of
-      // heads hA and hB in each 16-byte chunk g
-      const uint32_t pA = p0 + bsel * kPBytes + hA * 128 + 4 * r4;
-      const uint32_t pB = p0 + bsel * kPBytes + hB * 128 + 4 * r4;
-      const int sw = hA & 7;  // hB & 7 is the same
-#pragma unroll 1
-      for (int gb = 0; gb < 8; gb += 4) {
-        uint32_t x[4][4], y[4][4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          tmem_ld_16x256b(sa + 8 * (gb + i), x[i]);
-          tmem_ld_16x256b(sb + 8 * (gb + i), y[i]);
-        }
-        tmem_ld_wait();
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int g = gb + i;
-          const uint32_t mk = full ? 3u : ((g < 4 ? mlo : mhi) >> (8 * (g & 3) + 2 * r4)) & 3u;
-          const float s0 = __uint_as_float(x[i][0]) + __uint_as_float(y[i][0]);
-          const float s1 = __uint_as_float(x[i][1]) + __uint_as_float(y[i][1]);
-          const float s2 = __uint_as_float(x[i][2]) + __uint_as_float(y[i][2]);
-          const float s3 = __uint_as_float(x[i][3]) + __uint_as_float(y[i][3]);
-          const float e0 = (mk & 1u) ? ex2(fmaf(s0, scale2, -mA)) : 0.f;
-          const float e1 = (mk & 2u) ? ex2(fmaf(s1, scale2, -mA)) : 0.f;
-          const float e2 = (mk & 1u) ? ex2(fmaf(s2, scale2, -mB)) : 0.f;
-          const float e3 = (mk & 2u) ? ex2(fmaf(s3, scale2, -mB)) : 0.f;
-          const uint32_t qa = pack_bf16x2(e0, e1), qb2 = pack_bf16x2(e2, e3);
-          lA += __uint_as_float(qa << 16) + __uint_as_float(qa & 0xFFFF0000u);
-          lB += __uint_as_float(qb2 << 16) + __uint_as_float(qb2 & 0xFFFF0000u);
-          st_shared32(pA + ((g ^ sw) << 4), qa);
-          st_shared32(pB + ((g ^ sw) << 4), qb2);
-        }
-      }
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(smem_u32(&X.p_full[bsel]));
@@ -513,36 +541,121 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (tid == 0 && n == 0) mbar_wait(smem_u32(&X.q_full), 0, 100000000ull);  // Q copy landed
   __syncthreads();
   if (nsplit == 1) {
-    // O^T / l -> bf16 [64 heads][512], staged in the KV buffers, then coalesced stores
+    // O^T / l -> bf16 out[q][64 heads][512]
     if (tid < 64) X.fac[0][tid] = 1.f / X.l_run[tid];
     __syncthreads();
-    uint16_t* stage = reinterpret_cast<uint16_t*>(kv_s);
     if (warp < 4) {
       const uint32_t lrow = (uint32_t)(warp * 32) << 16;
+      uint16_t* oq = a.out + (int64_t)q * kHeads * kDLat;
 #pragma unroll 1
       for (int mt = 0; mt < 4; ++mt) {
         const int dim = mt * 128 + warp * 32 + lane;
-#pragma unroll
+#pragma unroll 1
         for (int hb = 0; hb < 64; hb += 32) {
           uint32_t v[32];
           tmem_ld32(tmem + lrow + kColO + 64 * mt + hb, v);
           tmem_ld_wait();
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            const float o = n > 0 ? __uint_as_float(v[j]) * X.fac[0][hb + j] : 0.f;
-            __nv_bfloat16 bv = __float2bfloat16_rn(o);
-            stage[(hb + j) * kDLat + dim] = *reinterpret_cast<uint16_t*>(&bv);
-          }
+          for (int j = 0; j < 32; ++j)
+            v[j] = __float_as_uint(n > 0 ? __uint_as_float(v[j]) * X.fac[0][hb + j] : 0.f);
+          store_pairs(oq, dim, hb, v, lane);
         }
       }
     }
-    __syncthreads();
-    const uint4* src = reinterpret_cast<const uint4*>(kv_s);
-    uint4* dst = reinterpret_cast<uint4*>(a.out + (int64_t)q * kHeads * kDLat);
-    for (int i = tid; i < kHeads * kDLat * 2 / 16; i += kThreads) dst[i] = src[i];
     if (a.lse && tid < 64)
       a.lse[(int64_t)q * kHeads + tid] =
           (X.m_run[tid] + __log2f(X.l_run[tid])) * 0.6931471805599453f;
+  } else if (a.cluster) {
+    // Two CTAs per query as a cluster: CTA r finishes dims 256 r .. 256 r + 255.  Each
+    // stages its partial O^T of the other's dims (fp32 [256 dims][64 heads], 16-byte
+    // pieces swizzled by dim) in its second KV buffer and ships it, with its running max
+    // and sum, by bulk copy into the other's first KV buffer; then it merges
+    //   o = (2^(m_own - M) O_own + 2^(m_peer - M) O_peer) / Z,
+    //   M = max(m_own, m_peer, sink),  Z = 2^(sink - M) + sum 2^(m - M) l.
+    const uint32_t peer = (uint32_t)rank ^ 1u;
+    const uint32_t stage_in = smem_u32(kv_s);               // filled by the peer
+    const uint32_t stage_send = smem_u32(kv_s + kBufBytes);  // our pieces for the peer
+    cluster_sync();  // both CTAs are past their main loops: the buffers are free
+    if (warp < 4) {
+      const uint32_t lrow = (uint32_t)(warp * 32) << 16;
+#pragma unroll 1
+      for (int mi = 0; mi < 2; ++mi) {
+        const int mt = 2 * (int)peer + mi;
+        const int d = mi * 128 + warp * 32 + lane;  // dim within the peer's half
+        const uint32_t row = stage_send + d * 256;
+#pragma unroll 1
+        for (int hb = 0; hb < 64; hb += 32) {
+          uint32_t v[32];
+          if (n > 0) {
+            tmem_ld32(tmem + lrow + kColO + 64 * mt + hb, v);
+            tmem_ld_wait();
+          } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) v[j] = 0u;
+          }
+#pragma unroll
+          for (int j4 = 0; j4 < 8; ++j4) {
+            const int c = (hb >> 2) + j4;  // 16-byte piece of the row (heads 4c .. 4c + 3)
+            st_shared16(row + ((c ^ (d & 15)) << 4),
+                        make_uint4(v[4 * j4], v[4 * j4 + 1], v[4 * j4 + 2], v[4 * j4 + 3]));
+          }
+        }
+      }
+      fence_proxy_async_smem();
+      asm volatile("bar.sync 1, 128;" ::: "memory");
+      if (tid == 0) {
+        const uint32_t inbar = smem_u32(&X.merge_full);
+        mbar_arrive_expect_tx(inbar, kBufBytes + 512);
+        const uint32_t pbar = dsmem_addr(inbar, peer);
+        bulk_copy_to_cluster(dsmem_addr(stage_in, peer), stage_send, kBufBytes, pbar);
+        // m_run, l_run -> the peer's peer_m, peer_l (512 contiguous bytes each side)
+        bulk_copy_to_cluster(dsmem_addr(smem_u32(X.peer_m), peer), smem_u32(X.m_run), 512, pbar);
+      }
+      if (!mbar_wait(smem_u32(&X.merge_full), 0)) X.abort = 1;
+      if (tid < 64) {
+        const float mo = X.m_run[tid], mp = X.peer_m[tid];
+        const float sk = a.sink ? a.sink[tid] * kLog2e : -INFINITY;
+        const float M = fmaxf(fmaxf(mo, mp), sk);
+        const float wo = mo == -INFINITY ? 0.f : ex2(mo - M);
+        const float wp = mp == -INFINITY ? 0.f : ex2(mp - M);
+        const float Z = wo * X.l_run[tid] + wp * X.peer_l[tid] + (a.sink ? ex2(sk - M) : 0.f);
+        const float inv = Z > 0.f ? 1.f / Z : 0.f;
+        X.fac[0][tid] = wo * inv;
+        X.fac[1][tid] = wp * inv;
+        if (a.lse && rank == 0)
+          a.lse[(int64_t)q * kHeads + tid] = (M + __log2f(Z)) * 0.6931471805599453f;
+      }
+      asm volatile("bar.sync 1, 128;" ::: "memory");
+      uint16_t* oq = a.out + (int64_t)q * kHeads * kDLat;
+      const float* pin = reinterpret_cast<const float*>(kv_s);
+#pragma unroll 1
+      for (int mi = 0; mi < 2; ++mi) {
+        const int mt = 2 * rank + mi;
+        const int d = mi * 128 + warp * 32 + lane;  // dim within this CTA's half
+        const float* prow = pin + d * 64;
+#pragma unroll 1
+        for (int hb = 0; hb < 64; hb += 32) {
+          uint32_t v[32];
+          if (n > 0) {
+            tmem_ld32(tmem + lrow + kColO + 64 * mt + hb, v);
+            tmem_ld_wait();
+          } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) v[j] = 0u;
+          }
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const int h = hb + j, c = h >> 2;
+            v[j] = __float_as_uint(__uint_as_float(v[j]) * X.fac[0][h] +
+                                   prow[((c ^ (d & 15)) << 2) + (h & 3)] * X.fac[1][h]);
+          }
+          store_pairs(oq, 256 * rank + d, hb, v, lane);
+        }
+      }
+    }
+    // both CTAs have received their pieces, so no copy touches either one's shared
+    // memory any more when they exit
+    cluster_sync();
   } else {
     // partial O^T (unnormalised fp32) -> workspace [Q][nsplit][64 heads][512], plus the
     // running max (log2 units) and sum per head
@@ -647,6 +760,12 @@ cudaError_t launch_attn(const AttnArgs& a, int nsplit, cudaStream_t s) {
   cudaError_t e = cudaFuncSetAttribute(sparse_attn_kernel,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
+  if (nsplit == 2) {  // the two CTAs of a query merge through distributed shared memory
+    AttnArgs b = a;
+    b.cluster = 1;
+    return launch_pdl_cluster(sparse_attn_kernel, dim3(2u, (unsigned)a.Q), dim3(kThreads), smem, s,
+                              2u, b, qm);
+  }
   e = launch_pdl(sparse_attn_kernel, dim3((unsigned)nsplit, (unsigned)a.Q), dim3(kThreads), smem,
                  s, a, qm);
   if (e != cudaSuccess || nsplit == 1) return e;

@@ -202,9 +202,10 @@ csa2_status csa2_topk_scores(const float* scores, const int32_t* n, int Q, int64
  *   out    [Q][64][512] bf16;  lse [Q][64] fp32 or NULL
  *   ws     optional workspace (256-byte aligned) of csa2_attn_workspace_size(Q, nsel)
  *          bytes.  With few queries the entries of one query are spread over several
- *          CTAs whose partial results are merged through it; with ws == NULL (or a
- *          smaller one) fewer CTAs per query are used.  The result does not depend on
- *          it beyond rounding. */
+ *          CTAs; two of them merge in distributed shared memory, more merge through
+ *          this workspace, so with ws == NULL (or a smaller one) at most two CTAs per
+ *          query are used.  The size is 0 when no more are worth it.  The result does
+ *          not depend on it beyond rounding. */
 typedef enum { CSA2_SWA_RING = 0, CSA2_SWA_LINEAR = 1 } csa2_swa_mode;
 typedef enum { CSA2_SWA_BF16 = 0, CSA2_SWA_FP8_S128 = 1 } csa2_swa_dtype;
 typedef struct {
