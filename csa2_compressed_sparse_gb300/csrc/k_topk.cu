@@ -5,12 +5,14 @@
 // Scores are handled as order-preserving uint32 keys (score_key); key 0 marks a
 // position that was not scored.  One CTA selects from a row segment of up to 32768
 // positions:
-//   1. sample: a histogram of the top 11 key bits over an even sample of the segment
-//      gives a threshold bin expected to hold about 2k + 64 of its keys above it;
-//   2. filter: one streaming pass keeps the (key, position) pairs at or above the
-//      threshold (a few times k of them) and counts the scored positions;
+//   1. sample: the segment is staged in shared memory by one bulk copy (a TMA copy has
+//      the whole row in flight at once); a histogram of the top 11 key bits over an
+//      even sample of 2048 keys gives a threshold bin expected to hold about 2k + 64;
+//   2. filter: one pass keeps the (key, position) pairs at or above the threshold (a
+//      few times k of them) and counts the scored positions;
 //   3. select: three histogram passes (key bits 31..21, 20..10, 9..0) over the kept
-//      pairs give the k-th largest key T and how many keys equal to T are needed;
+//      pairs give the k-th largest key T and how many keys equal to T are needed (the
+//      histogram updates are aggregated per warp: most kept keys share a few bins);
 //   4. output: winners are marked in a position bitmap (keys > T; the lowest
 //      positions among keys == T), which is scanned in order, so ties go to the lower
 //      position and the output is ascending.
@@ -39,7 +41,9 @@ constexpr int kWords = kChunkLen / 32;
 namespace {
 
 struct SelectSmem {
+  uint32_t row[kChunkLen + 4];  // the segment's keys (shifted so its aligned part is)
   uint32_t hist[2048];
+  uint32_t hist_kept[2048];  // top 11 key bits of the kept pairs (filled by the filter)
   uint32_t ckey[kCandCap];
   uint32_t cidx[kCandCap];
   uint32_t selmap[kWords];  // positions with key > T
@@ -53,16 +57,17 @@ struct SelectSmem {
   int found_bin;
   int found_above;
   int last;
+  uint64_t bar;  // bulk copy of the segment
 };
 
-// Block-wide: among bins (descending), find the bin where the running count from the
-// top crosses `need`.  Writes found_bin and found_above (= count strictly above).
-// If the total is below `need`, found_bin is 0 and found_above the total.
-__device__ void find_crossing(SelectSmem& S, int nbins, int need) {
+// Block-wide: among bins of `hist` (descending), find the bin where the running count
+// from the top crosses `need`.  Writes found_bin and found_above (= count strictly
+// above).  If the total is below `need`, found_bin is 0 and found_above the total.
+__device__ void find_crossing(SelectSmem& S, const uint32_t* hist, int nbins, int need) {
   const int tid = threadIdx.x;
   const int per = nbins / kTopkThreads;  // 2 or 1
   int local = 0;
-  for (int j = 0; j < per; ++j) local += (int)S.hist[nbins - 1 - per * tid - j];
+  for (int j = 0; j < per; ++j) local += (int)hist[nbins - 1 - per * tid - j];
   const int lane = tid & 31, warp = tid >> 5;
   int incl = local;
 #pragma unroll
@@ -73,15 +78,20 @@ __device__ void find_crossing(SelectSmem& S, int nbins, int need) {
   if (tid == 0) { S.found_bin = 0; S.found_above = 0; }
   if (lane == 31) S.warp_a[warp] = incl;
   __syncthreads();
-  int wbase = 0, total = 0;
-  for (int w = 0; w < kTopkWarps; ++w) {
-    if (w < warp) wbase += S.warp_a[w];
-    total += S.warp_a[w];
+  // every warp scans the 32 warp totals itself
+  const int wt = S.warp_a[lane];
+  int wi = wt;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    int v = __shfl_up_sync(0xFFFFFFFFu, wi, o);
+    if (lane >= o) wi += v;
   }
+  const int wbase = __shfl_sync(0xFFFFFFFFu, wi - wt, warp);
+  const int total = __shfl_sync(0xFFFFFFFFu, wi, 31);
   int above = wbase + incl - local;
   for (int j = 0; j < per; ++j) {
     int bin = nbins - 1 - per * tid - j;
-    int c = (int)S.hist[bin];
+    int c = (int)hist[bin];
     if (above < need && need <= above + c) {
       S.found_bin = bin;
       S.found_above = above;
@@ -92,19 +102,28 @@ __device__ void find_crossing(SelectSmem& S, int nbins, int need) {
   __syncthreads();
 }
 
+// Warp-aggregated histogram increment: lanes with the same bin add once.  Called by
+// all 32 lanes of a warp together; lanes with valid == false add nothing.
+__device__ __forceinline__ void hist_add(uint32_t* hist, uint32_t bin, bool valid) {
+  const uint32_t m = __match_any_sync(0xFFFFFFFFu, valid ? bin : 0xFFFFFFFFu);
+  const int lane = threadIdx.x & 31;
+  if (valid && lane == __ffs(m) - 1) atomicAdd(&hist[bin], (uint32_t)__popc(m));
+}
+
 __device__ __forceinline__ void clear_hist(SelectSmem& S, int nbins) {
   for (int i = threadIdx.x; i < nbins; i += kTopkThreads) S.hist[i] = 0;
 }
 
-// Keys of a row segment: workspace keys, raw fp32 scores, or the merge's (key << 32 |
-// position) pairs.
-enum SrcKind { kSrcKeys = 0, kSrcScores = 1, kSrcPairs = 2 };
+// Keys of a row segment: workspace keys or raw fp32 scores (both staged in shared memory
+// as keys), or the merge's (key << 32 | position) pairs in global memory.
+enum SrcKind { kSrcKeys = 0, kSrcScores = 1, kSrcPairs = 2, kSrcSmem = 3 };
 
 template <int kKind>
 struct RowSrc {
   const void* base;
   bool aligned;  // 16-byte aligned base
   __device__ __forceinline__ uint32_t operator()(int i) const {
+    if (kKind == kSrcSmem) return static_cast<const uint32_t*>(base)[i];
     if (kKind == kSrcPairs) return (uint32_t)(__ldcg(static_cast<const uint64_t*>(base) + i) >> 32);
     if (kKind == kSrcScores) return score_key(__ldcg(static_cast<const float*>(base) + i));
     return __ldcg(static_cast<const uint32_t*>(base) + i);
@@ -115,6 +134,8 @@ struct RowSrc {
     uint4 r = make_uint4(0u, 0u, 0u, 0u);
     if (i >= n) return r;
     if (aligned && i + 4 <= n) {
+      if (kKind == kSrcSmem)
+        return *reinterpret_cast<const uint4*>(static_cast<const uint32_t*>(base) + i);
       if (kKind == kSrcPairs) {
         const uint4* p = reinterpret_cast<const uint4*>(static_cast<const uint64_t*>(base) + i);
         const uint4 a = __ldcg(p), b = __ldcg(p + 1);
@@ -140,47 +161,45 @@ template <int kKind>
 __device__ int select_topk(const RowSrc<kKind>& src, int n, int k, SelectSmem& S) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int nw = (n + 31) >> 5;
-  // ---- 1. threshold from a sample ----
-  const int ns = n < 2 * kTopkThreads ? n : 2 * kTopkThreads;
+  // ---- 1. clear ----
+  // thread (warp w, lane l) handles the 4-key groups w * 32 + l + u * kTopkThreads,
+  // u < kU (n <= kChunkLen)
+  constexpr int kU = kChunkLen / (4 * kTopkThreads);
   clear_hist(S, 2048);
+  for (int i = tid; i < 2048; i += kTopkThreads) S.hist_kept[i] = 0;
   if (tid == 0) { S.ncand = 0; S.nvalid = 0; }
   if (tid < kTopkWarps) S.wcnt[tid] = 0;
   for (int w = tid; w < nw; w += kTopkThreads) { S.selmap[w] = 0; S.eqmap[w] = 0; }
   __syncthreads();
-  for (int s = tid; s < ns; s += kTopkThreads) {
-    const int i = (int)(((int64_t)(2 * s + 1) * n) / (2 * ns));
-    const uint32_t key = src(i);
+  // ---- 2. threshold from an even sample of 2048 keys ----
+  const int ns = n < 2 * kTopkThreads ? n : 2 * kTopkThreads;
+  for (int s2 = tid; s2 < ns; s2 += kTopkThreads) {
+    const uint32_t key = src((int)(((int64_t)(2 * s2 + 1) * n) / (2 * ns)));
     if (key) atomicAdd(&S.hist[key >> 21], 1u);
   }
   __syncthreads();
   // sample keys wanted above the threshold: about (2k + 64) / n of the sample
   const int want = (int)(((int64_t)(2 * k + 64) * ns + n - 1) / (n > 0 ? n : 1));
-  find_crossing(S, 2048, want);
+  find_crossing(S, S.hist, 2048, want);
   const uint32_t thr = want >= ns ? 1u : max((uint32_t)S.found_bin << 21, 1u);
-  // ---- 2. filter: keep keys >= thr, count scored positions ----
-  // groups of 4 keys; each thread holds 8 groups in flight per round (warp-uniform).
+  // ---- 3. filter: keep keys >= thr, count scored positions ----
   // Warp w appends to its own region [w * kWarpCap, ...) through its shared counter.
   int nval = 0;
   uint32_t* wkey = S.ckey + warp * kWarpCap;
   uint32_t* widx = S.cidx + warp * kWarpCap;
-  const int ng = (n + 3) >> 2;
-  constexpr int kU = 8;
-  for (int r0 = warp * 32; r0 < ng; r0 += kU * kTopkThreads) {
-    uint4 v[kU];
+#pragma unroll 2
+  for (int u = 0; u < kU; ++u) {
+    const int g = warp * 32 + u * kTopkThreads + lane;
+    const uint4 vv = src.load4(g, n);
+    const uint32_t kk[4] = {vv.x, vv.y, vv.z, vv.w};
 #pragma unroll
-    for (int u = 0; u < kU; ++u) v[u] = src.load4(r0 + u * kTopkThreads + lane, n);
-#pragma unroll
-    for (int u = 0; u < kU; ++u) {
-      const int g = r0 + u * kTopkThreads + lane;
-      const uint32_t kk[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const uint32_t key = kk[j];
-        nval += key != 0u;
-        if (key >= thr) {  // thr >= 1: unscored keys are never kept
-          const int slot = atomicAdd(&S.wcnt[warp], 1);
-          if (slot < kWarpCap) { wkey[slot] = key; widx[slot] = (uint32_t)(4 * g + j); }
-        }
+    for (int jj = 0; jj < 4; ++jj) {
+      const uint32_t key = kk[jj];
+      nval += key != 0u;
+      if (key >= thr) {  // thr >= 1: unscored keys are never kept
+        const int slot = atomicAdd(&S.wcnt[warp], 1);
+        if (slot < kWarpCap) { wkey[slot] = key; widx[slot] = (uint32_t)(4 * g + jj); }
+        atomicAdd(&S.hist_kept[key >> 21], 1u);
       }
     }
   }
@@ -197,42 +216,54 @@ __device__ int select_topk(const RowSrc<kKind>& src, int n, int k, SelectSmem& S
   if (keff <= 0) return 0;
   const int nc = S.ncand;
   const bool fast = nc >= keff && nc <= kCandCap;  // the kept pairs hold the top-k
-  // ---- 3. radix select over the kept pairs (or the whole segment) ----
+  // ---- 4. radix select over the kept pairs (or the whole segment) ----
+  // fn(key, valid) is called by the 32 lanes of a warp together (warp-uniform loops).
   const int my_cnt = S.wcnt[warp];
   auto for_keys = [&](auto&& fn) {
     if (fast) {  // each warp walks its own region
-      for (int j = lane; j < my_cnt; j += 32) fn(wkey[j]);
+      for (int j0 = 0; j0 < my_cnt; j0 += 32) {
+        const int jx = j0 + lane;
+        const bool ok = jx < my_cnt;
+        fn(ok ? wkey[jx] : 0u, ok);
+      }
     } else {
-      for (int i = tid; i < n; i += kTopkThreads) fn(src(i));
+      for (int i0 = warp * 32; i0 < n; i0 += kTopkThreads) {
+        const int ix = i0 + lane;
+        const bool ok = ix < n;
+        fn(ok ? src(ix) : 0u, ok);
+      }
     }
   };
-  clear_hist(S, 2048);
-  __syncthreads();
-  for_keys([&](uint32_t key) { if (key) atomicAdd(&S.hist[key >> 21], 1u); });
-  __syncthreads();
-  find_crossing(S, 2048, keff);
+  // first pass (key bits 31..21): the filter counted the kept pairs already
+  if (!fast) {
+    clear_hist(S, 2048);
+    __syncthreads();
+    for_keys([&](uint32_t key, bool ok) { hist_add(S.hist, key >> 21, ok && key != 0u); });
+    __syncthreads();
+  }
+  find_crossing(S, fast ? S.hist_kept : S.hist, 2048, keff);
   const uint32_t b1 = (uint32_t)S.found_bin;
   int above = S.found_above;
   clear_hist(S, 2048);
   __syncthreads();
-  for_keys([&](uint32_t key) {
-    if (key && (key >> 21) == b1) atomicAdd(&S.hist[(key >> 10) & 2047u], 1u);
+  for_keys([&](uint32_t key, bool ok) {
+    hist_add(S.hist, (key >> 10) & 2047u, ok && key != 0u && (key >> 21) == b1);
   });
   __syncthreads();
-  find_crossing(S, 2048, keff - above);
+  find_crossing(S, S.hist, 2048, keff - above);
   const uint32_t pre = (b1 << 11) | (uint32_t)S.found_bin;
   above += S.found_above;
   clear_hist(S, 1024);
   __syncthreads();
-  for_keys([&](uint32_t key) {
-    if (key && (key >> 10) == pre) atomicAdd(&S.hist[key & 1023u], 1u);
+  for_keys([&](uint32_t key, bool ok) {
+    hist_add(S.hist, key & 1023u, ok && key != 0u && (key >> 10) == pre);
   });
   __syncthreads();
-  find_crossing(S, 1024, keff - above);
+  find_crossing(S, S.hist, 1024, keff - above);
   const uint32_t T = (pre << 10) | (uint32_t)S.found_bin;
   above += S.found_above;
   const int need_eq = keff - above;  // >= 1
-  // ---- 4. mark winners by position, then scan the bitmaps in order ----
+  // ---- 5. mark winners by position, then scan the bitmaps in order ----
   if (fast) {
     for (int j = lane; j < my_cnt; j += 32) {
       const uint32_t key = wkey[j], idx = widx[j];
@@ -332,9 +363,35 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(TopkArgs a) {
   const int begin = c * a.chunk;
   const int len = max(0, min(a.chunk, n - begin));
   const int64_t rowoff = (int64_t)q * a.ld + begin;
-  const void* base = kKind == kSrcScores ? static_cast<const void*>(a.scores + rowoff)
-                                          : static_cast<const void*>(a.keys + rowoff);
-  RowSrc<kKind> src{base, (reinterpret_cast<uintptr_t>(base) & 15u) == 0};
+  // The segment into shared memory: one bulk copy of its 16-byte aligned interior (a
+  // TMA copy has the whole row in flight at once), the ragged ends (at most 3 keys
+  // each) by plain loads; scores become keys in place.
+  const uint32_t* g = kKind == kSrcScores ? reinterpret_cast<const uint32_t*>(a.scores + rowoff)
+                                          : a.keys + rowoff;
+  const int tid = threadIdx.x;
+  int head = (int)(((16u - (uint32_t)(reinterpret_cast<uintptr_t>(g) & 15u)) & 15u) >> 2);
+  head = min(head, len);
+  const int body = ((len - head) >> 2) << 2;
+  const int pad = (4 - head) & 3;  // row[pad + head] is 16-byte aligned
+  uint32_t* rowbuf = S.row + pad;
+  if (tid == 0) {
+    mbar_init(smem_u32(&S.bar), 1);
+    mbar_fence_init();
+  }
+  __syncthreads();
+  if (tid == 0 && body > 0) {
+    mbar_arrive_expect_tx(smem_u32(&S.bar), (uint32_t)body * 4u);
+    bulk_copy_g2s(smem_u32(rowbuf + head), g + head, (uint32_t)body * 4u, smem_u32(&S.bar));
+  }
+  if (tid < head) rowbuf[tid] = __ldcg(g + tid);
+  if (head + body + tid < len) rowbuf[head + body + tid] = __ldcg(g + head + body + tid);
+  if (body > 0) mbar_wait(smem_u32(&S.bar), 0);
+  if (kKind == kSrcScores) {
+    __syncthreads();
+    for (int i = tid; i < len; i += kTopkThreads) rowbuf[i] = score_key(__uint_as_float(rowbuf[i]));
+  }
+  __syncthreads();
+  RowSrc<kSrcSmem> src{rowbuf, pad == 0};
   int keff = select_topk(src, len, a.k, S);
   if (a.nchunk == 1) {
     write_row(a, q, keff, S.out, [&](int i) { return (uint32_t)(begin + i); },

@@ -283,6 +283,17 @@ __device__ __forceinline__ uint32_t dsmem_addr(uint32_t local, uint32_t rank) {
   return r;
 }
 
+// Bulk copy of `bytes` (a multiple of 16) from global to this CTA's shared memory, both
+// 16-byte aligned; completion is counted as transaction bytes on the mbarrier.
+__device__ __forceinline__ void bulk_copy_g2s(uint32_t dst, const void* src, uint32_t bytes,
+                                              uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+          "r"(dst),
+      "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
 // Bulk copy of `bytes` (a multiple of 16) from this CTA's shared memory to shared memory
 // of a CTA of the cluster; completion is counted as transaction bytes on that CTA's
 // mbarrier.  Addresses 16-byte aligned; dst and bar are cluster addresses (dsmem_addr).

@@ -108,13 +108,16 @@ def test_topk_scores_bit_exact(ld, k):
     from csa2_compressed_sparse_gb300 import (csa2_device_status, csa2_topk_scores,
                                               csa2_topk_workspace_size)
     g = np.random.default_rng(ld + k)
-    Q = 6
+    Q = 7
     s = (g.integers(-40, 40, (Q, ld)) / 8.0).astype(np.float32)  # heavy ties
     s[1] = g.standard_normal(ld).astype(np.float32)
     s[2, ::7] = np.nan
     s[3, ::5] = -0.0
     s[4, ::3] = -np.inf
-    n = np.array([ld, ld, max(ld - 3, 0), ld // 2, min(ld, 511), 0], dtype=np.int32)
+    # one value everywhere: past 8192 positions a chunk keeps more pairs than its buffer
+    # holds and selects over the whole chunk instead; below, ties decide every place
+    s[6] = 1.5
+    n = np.array([ld, ld, max(ld - 3, 0), ld // 2, min(ld, 511), 0, ld], dtype=np.int32)
     st = torch.from_numpy(s).cuda()
     nt = torch.from_numpy(n).cuda()
     sel = torch.empty((Q, k), dtype=torch.int32, device="cuda")
