@@ -50,6 +50,21 @@ def dist_env():
     return rank, world, local
 
 
+def max_over_ranks(x, world, device):
+    """The largest value of x over the ranks (x itself on one rank)."""
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    if world > 1:
+        import torch.distributed as dist
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def weak_value(units_per_rank, world, steps, ms_max):
+    """Whole-job throughput of a weak-scaling run: the units every rank processed in
+    `steps` steps over the slowest rank's time (ms)."""
+    return units_per_rank * world * steps / (ms_max / 1e3)
+
+
 def hbm_peak():
     try:
         with open(PEAKS) as f:
@@ -258,13 +273,9 @@ def run_ours(args):
     ms = ev0.elapsed_time(ev1)
     idx_ms = sum(a.elapsed_time(b) for a, b in sample_ev) / n_samples
     csa2.csa2_device_status()
-    tmax = torch.tensor([ms], dtype=torch.float64, device="cuda")
-    if world > 1:
-        dist.all_reduce(tmax, op=dist.ReduceOp.MAX)
-    ms = float(tmax.item())
+    ms = max_over_ranks(ms, world, "cuda")
     ms_step = ms / args.steps
-    q_total = wl.Q * world * args.steps
-    value = q_total / (ms / 1e3)
+    value = weak_value(wl.Q, world, args.steps, ms)
     total_bytes, index_bytes, attn_bytes = algorithmic_bytes(wl)
     peak, peak_kind = hbm_peak()
     achieved_index = index_bytes / (idx_ms / 1e3) / 1e9
@@ -365,9 +376,9 @@ def run_e2e(args, wl, spec, t, buf, world):
         one()
     e1.record(stream)
     torch.cuda.synchronize()
-    wall = time.perf_counter() - w0
+    wall = max_over_ranks(time.perf_counter() - w0, world, "cuda")
     csa2.csa2_device_status()
-    return {"value": wl.Q * world * steps / wall, "unit": "queries/s",
+    return {"value": weak_value(wl.Q, world, steps, wall * 1e3), "unit": "queries/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "device_ms_per_step": e0.elapsed_time(e1) / steps, "steps": steps}
 
