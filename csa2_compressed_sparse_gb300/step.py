@@ -85,17 +85,30 @@ def kernel_launches(spec: StepSpec, t) -> int:
     return n
 
 
-def run_step(spec: StepSpec, t, buf: StepBuffers, stream=None, compress=True):
-    if compress and t["kv"].shape[0]:
+def run_step(spec: StepSpec, t, buf: StepBuffers, stream=None, compress=True, side=None):
+    """One step on `stream` (default: the current stream).  The compressor writes only the
+    main plane, which the indexer does not read, so with a `side` stream the compressor
+    runs there, concurrently with index + top-k, and the attention waits for both."""
+    main = stream if stream is not None else torch.cuda.current_stream()
+    fork = side is not None and compress and t["kv"].shape[0] > 0
+    if fork:
+        side.wait_stream(main)
+        with torch.cuda.stream(side):
+            csa2_compress(t["kv"], t["score"], t["cu_seqlens"], t["start_pos"], spec.ratio,
+                          t["kv_state"], t["score_state"], t["plane"], t["row_base"],
+                          t["inv_freq"], eps=spec.eps, stream=side)
+    elif compress and t["kv"].shape[0]:
         csa2_compress(t["kv"], t["score"], t["cu_seqlens"], t["start_pos"], spec.ratio,
                       t["kv_state"], t["score_state"], t["plane"], t["row_base"], t["inv_freq"],
-                      eps=spec.eps, stream=stream)
+                      eps=spec.eps, stream=main)
     csa2_index_topk(t["iq"], t["w"], t["index_k"], t["row_base"], t["q_seq"], t["q_pos"],
                     spec.ratio, spec.k, spec.max_scored, buf.sel, buf.ws,
                     sel_scores=buf.sel_scores, cand=t.get("cand"), relu=spec.relu,
-                    scores_out=buf.scores_out, stream=stream)
+                    scores_out=buf.scores_out, stream=main)
+    if fork:
+        main.wait_stream(side)
     for layer in range(len(t["q"])):
         fn = csa2_sparse_attn if layer == 0 else csa2_reuse_attn
         fn(t["q"][layer], t["q_seq"], t["q_pos"], swa_of(spec, t, layer), t["plane"],
            t["row_base"], buf.sel, t["sink"], buf.out[layer], lse=buf.lse[layer],
-           scale=spec.scale, ws=buf.attn_ws, stream=stream)
+           scale=spec.scale, ws=buf.attn_ws, stream=main)

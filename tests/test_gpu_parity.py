@@ -235,6 +235,25 @@ def test_step_h32_and_no_relu():
             check_sel(buf.sel[q].cpu().numpy(), sel_ref, sc, rows, wl.k)
 
 
+def test_step_with_the_compressor_on_a_second_stream_is_identical():
+    """The compressor does not feed the indexer, so a step may run it on a second stream
+    next to index + top-k; the results are the same bits (a decode step is idempotent:
+    the tail state it writes is the one it reads)."""
+    from csa2_compressed_sparse_gb300 import csa2_device_status
+    from csa2_compressed_sparse_gb300.step import run_step
+    wl = W.decode_batch(B=12, lo=300, hi=9000, seed=29)
+    t, spec, buf = run_workload(wl)
+    ref = [buf.sel.clone(), buf.out[0].clone(), buf.lse[0].clone(), t["plane"].clone()]
+    side = torch.cuda.Stream()
+    for b in (buf.sel, buf.out[0], buf.lse[0]):
+        b.zero_()
+    run_step(spec, t, buf, side=side)
+    torch.cuda.synchronize()
+    csa2_device_status()
+    for a, b in zip(ref, [buf.sel, buf.out[0], buf.lse[0], t["plane"]]):
+        assert torch.equal(a, b)
+
+
 def test_attention_split_and_unsplit_agree_with_the_oracle():
     """The same queries with and without the attention workspace (several CTAs per
     query merged through it, or one CTA per query)."""
