@@ -157,22 +157,60 @@ __device__ __forceinline__ void p_pass(uint32_t sa, uint32_t sb, bool full, uint
   }
 }
 
-// Output of O^T: lane l of a warp holds dim d (consecutive over the warp) and o[j] of
-// heads h0 + j.  Adjacent lanes swap one value per pair of heads so that each stores one
-// bf16 pair (dims d & ~1 and d | 1) of one head: even lanes head h0 + j, odd lanes head
-// h0 + j + 1.  out_q is out[q] = [64 heads][512] bf16.
-// (o holds fp32 bit patterns.)
-__device__ __forceinline__ void store_pairs(uint16_t* out_q, int d, int h0,
-                                            const uint32_t (&o)[32], int lane) {
-  const bool odd = (lane & 1) != 0;
-  uint32_t* base = reinterpret_cast<uint32_t*>(out_q);
+// O^T tiles mt0 .. mt0 + ntile - 1 from TMEM into shared memory as fp32 rows of 64 heads
+// (256 B per dim), 16-byte pieces swizzled by the dim (piece c of row d at c ^ (d & 15));
+// row = dim - 128 mt0.  Warps 0..3 (TMEM lanes 32 w ..); with n == 0 the tiles are zero.
+__device__ __forceinline__ void stage_ot(uint32_t tmem_o, int warp, int lane, int mt0, int ntile,
+                                         uint32_t stage, bool have) {
+  const uint32_t lrow = (uint32_t)(warp * 32) << 16;
+#pragma unroll 1
+  for (int mi = 0; mi < ntile; ++mi) {
+    const int d = mi * 128 + warp * 32 + lane;
+    const uint32_t row = stage + d * 256;
+#pragma unroll 1
+    for (int hb = 0; hb < 64; hb += 32) {
+      uint32_t v[32];
+      if (have) {
+        tmem_ld32(tmem_o + lrow + 64 * (mt0 + mi) + hb, v);
+        tmem_ld_wait();
+      } else {
 #pragma unroll
-  for (int j = 0; j < 32; j += 2) {
-    const float e = __uint_as_float(o[j]), f = __uint_as_float(o[j + 1]);
-    const float recv = __shfl_xor_sync(0xFFFFFFFFu, odd ? e : f, 1);
-    const uint32_t w = odd ? pack_bf16x2(recv, f) : pack_bf16x2(e, recv);
-    const int h = h0 + j + (odd ? 1 : 0);
-    base[(h * kDLat + (d & ~1)) >> 1] = w;
+        for (int j = 0; j < 32; ++j) v[j] = 0u;
+      }
+#pragma unroll
+      for (int j4 = 0; j4 < 8; ++j4) {
+        const int c = (hb >> 2) + j4;  // heads 4c .. 4c + 3
+        st_shared16(row + ((c ^ (d & 15)) << 4),
+                    make_uint4(v[4 * j4], v[4 * j4 + 1], v[4 * j4 + 2], v[4 * j4 + 3]));
+      }
+    }
+  }
+}
+
+// out[q][h][dbase + d] = bf16(own[d][h] w0[h] + peer[d][h] w1[h]) for nd dims, from rows
+// staged by stage_ot (peer may be null); all threads of the CTA, 16-byte stores of eight
+// dims of one head, a warp covering 32 heads of one group of eight dims.
+__device__ __forceinline__ void out_pass(const float* own, const float* peer, const float* w0,
+                                         const float* w1, uint16_t* out_q, int nd, int dbase,
+                                         int warp, int lane, int nwarps) {
+  const int items = 2 * (nd >> 3);  // (head half, group of 8 dims)
+  for (int it = warp; it < items; it += nwarps) {
+    const int h = 32 * (it & 1) + lane, dg = it >> 1;
+    const float a = w0[h], b = peer ? w1[h] : 0.f;
+    uint32_t pk[4];
+#pragma unroll
+    for (int k = 0; k < 8; k += 2) {
+      float o[2];
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int d = dg * 8 + k + e;
+        const int idx = d * 64 + ((((h >> 2) ^ (d & 15))) << 2) + (h & 3);
+        o[e] = own[idx] * a + (peer ? peer[idx] * b : 0.f);
+      }
+      pk[k >> 1] = pack_bf16x2(o[0], o[1]);
+    }
+    *reinterpret_cast<uint4*>(out_q + h * kDLat + dbase + dg * 8) =
+        make_uint4(pk[0], pk[1], pk[2], pk[3]);
   }
 }
 
@@ -541,66 +579,29 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (tid == 0 && n == 0) mbar_wait(smem_u32(&X.q_full), 0, 100000000ull);  // Q copy landed
   __syncthreads();
   if (nsplit == 1) {
-    // O^T / l -> bf16 out[q][64 heads][512]
+    // O^T / l -> bf16 out[q][64 heads][512]: O^T staged in the KV buffers (all 512 dims),
+    // then every thread writes
     if (tid < 64) X.fac[0][tid] = 1.f / X.l_run[tid];
+    if (warp < 4) stage_ot(tmem + kColO, warp, lane, 0, 4, smem_u32(kv_s), n > 0);
     __syncthreads();
-    if (warp < 4) {
-      const uint32_t lrow = (uint32_t)(warp * 32) << 16;
-      uint16_t* oq = a.out + (int64_t)q * kHeads * kDLat;
-#pragma unroll 1
-      for (int mt = 0; mt < 4; ++mt) {
-        const int dim = mt * 128 + warp * 32 + lane;
-#pragma unroll 1
-        for (int hb = 0; hb < 64; hb += 32) {
-          uint32_t v[32];
-          tmem_ld32(tmem + lrow + kColO + 64 * mt + hb, v);
-          tmem_ld_wait();
-#pragma unroll
-          for (int j = 0; j < 32; ++j)
-            v[j] = __float_as_uint(n > 0 ? __uint_as_float(v[j]) * X.fac[0][hb + j] : 0.f);
-          store_pairs(oq, dim, hb, v, lane);
-        }
-      }
-    }
+    out_pass(reinterpret_cast<const float*>(kv_s), nullptr, X.fac[0], nullptr,
+             a.out + (int64_t)q * kHeads * kDLat, kDLat, 0, warp, lane, kThreads / 32);
     if (a.lse && tid < 64)
       a.lse[(int64_t)q * kHeads + tid] =
           (X.m_run[tid] + __log2f(X.l_run[tid])) * 0.6931471805599453f;
   } else if (a.cluster) {
     // Two CTAs per query as a cluster: CTA r finishes dims 256 r .. 256 r + 255.  Each
-    // stages its partial O^T of the other's dims (fp32 [256 dims][64 heads], 16-byte
-    // pieces swizzled by dim) in its second KV buffer and ships it, with its running max
-    // and sum, by bulk copy into the other's first KV buffer; then it merges
+    // stages its partial O^T (fp32 rows of 64 heads per dim): the other's dims in its
+    // second KV buffer, which it ships with its running max and sum by bulk copy into the
+    // other's first KV buffer, and its own dims in the Q buffer; then every thread merges
     //   o = (2^(m_own - M) O_own + 2^(m_peer - M) O_peer) / Z,
     //   M = max(m_own, m_peer, sink),  Z = 2^(sink - M) + sum 2^(m - M) l.
     const uint32_t peer = (uint32_t)rank ^ 1u;
     const uint32_t stage_in = smem_u32(kv_s);               // filled by the peer
-    const uint32_t stage_send = smem_u32(kv_s + kBufBytes);  // our pieces for the peer
+    const uint32_t stage_send = smem_u32(kv_s + kBufBytes);  // our rows for the peer
     cluster_sync();  // both CTAs are past their main loops: the buffers are free
     if (warp < 4) {
-      const uint32_t lrow = (uint32_t)(warp * 32) << 16;
-#pragma unroll 1
-      for (int mi = 0; mi < 2; ++mi) {
-        const int mt = 2 * (int)peer + mi;
-        const int d = mi * 128 + warp * 32 + lane;  // dim within the peer's half
-        const uint32_t row = stage_send + d * 256;
-#pragma unroll 1
-        for (int hb = 0; hb < 64; hb += 32) {
-          uint32_t v[32];
-          if (n > 0) {
-            tmem_ld32(tmem + lrow + kColO + 64 * mt + hb, v);
-            tmem_ld_wait();
-          } else {
-#pragma unroll
-            for (int j = 0; j < 32; ++j) v[j] = 0u;
-          }
-#pragma unroll
-          for (int j4 = 0; j4 < 8; ++j4) {
-            const int c = (hb >> 2) + j4;  // 16-byte piece of the row (heads 4c .. 4c + 3)
-            st_shared16(row + ((c ^ (d & 15)) << 4),
-                        make_uint4(v[4 * j4], v[4 * j4 + 1], v[4 * j4 + 2], v[4 * j4 + 3]));
-          }
-        }
-      }
+      stage_ot(tmem + kColO, warp, lane, 2 * (int)peer, 2, stage_send, n > 0);
       fence_proxy_async_smem();
       asm volatile("bar.sync 1, 128;" ::: "memory");
       if (tid == 0) {
@@ -611,6 +612,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // m_run, l_run -> the peer's peer_m, peer_l (512 contiguous bytes each side)
         bulk_copy_to_cluster(dsmem_addr(smem_u32(X.peer_m), peer), smem_u32(X.m_run), 512, pbar);
       }
+      stage_ot(tmem + kColO, warp, lane, 2 * rank, 2, smem_u32(q_s), n > 0);
       if (!mbar_wait(smem_u32(&X.merge_full), 0)) X.abort = 1;
       if (tid < 64) {
         const float mo = X.m_run[tid], mp = X.peer_m[tid];
@@ -625,36 +627,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (a.lse && rank == 0)
           a.lse[(int64_t)q * kHeads + tid] = (M + __log2f(Z)) * 0.6931471805599453f;
       }
-      asm volatile("bar.sync 1, 128;" ::: "memory");
-      uint16_t* oq = a.out + (int64_t)q * kHeads * kDLat;
-      const float* pin = reinterpret_cast<const float*>(kv_s);
-#pragma unroll 1
-      for (int mi = 0; mi < 2; ++mi) {
-        const int mt = 2 * rank + mi;
-        const int d = mi * 128 + warp * 32 + lane;  // dim within this CTA's half
-        const float* prow = pin + d * 64;
-#pragma unroll 1
-        for (int hb = 0; hb < 64; hb += 32) {
-          uint32_t v[32];
-          if (n > 0) {
-            tmem_ld32(tmem + lrow + kColO + 64 * mt + hb, v);
-            tmem_ld_wait();
-          } else {
-#pragma unroll
-            for (int j = 0; j < 32; ++j) v[j] = 0u;
-          }
-#pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            const int h = hb + j, c = h >> 2;
-            v[j] = __float_as_uint(__uint_as_float(v[j]) * X.fac[0][h] +
-                                   prow[((c ^ (d & 15)) << 2) + (h & 3)] * X.fac[1][h]);
-          }
-          store_pairs(oq, 256 * rank + d, hb, v, lane);
-        }
-      }
     }
-    // both CTAs have received their pieces, so no copy touches either one's shared
-    // memory any more when they exit
+    __syncthreads();
+    out_pass(reinterpret_cast<const float*>(q_s), reinterpret_cast<const float*>(kv_s), X.fac[0],
+             X.fac[1], a.out + (int64_t)q * kHeads * kDLat, 256, 256 * rank, warp, lane,
+             kThreads / 32);
+    // both CTAs have received their rows, so no copy touches either one's shared memory
+    // any more when they exit
     cluster_sync();
   } else {
     // partial O^T (unnormalised fp32) -> workspace [Q][nsplit][64 heads][512], plus the
