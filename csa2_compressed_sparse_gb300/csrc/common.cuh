@@ -58,7 +58,6 @@ struct IndexArgs {
   int32_t* grp_nq;      // [Q]  queries in group g
   int64_t* grp_tile0;   // [Q+1] first work tile of group g (prefix)
   int32_t* n_groups;    // [1]
-  int32_t* tmp;         // [Q]  scratch of the grouping pass
   int32_t* topk_count;  // [Q]  zeroed by the prep kernel for the top-k merge
   int group_max;        // queries per group (FULL: 256 / H; REINDEX: 1)
 };

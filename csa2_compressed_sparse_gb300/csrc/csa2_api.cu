@@ -46,7 +46,7 @@ size_t up256(size_t x) { return (x + 255) & ~size_t(255); }
 
 // Workspace of csa2_index_topk.
 struct IndexWs {
-  size_t keys, n_scored, grp_q0, grp_nq, tmp, grp_tile0, n_groups, count, part, total;
+  size_t keys, n_scored, grp_q0, grp_nq, grp_tile0, n_groups, count, part, total;
   int nchunk;
 };
 
@@ -57,7 +57,6 @@ IndexWs index_ws_layout(int Q, int64_t ld, int k) {
   w.n_scored = o; o = up256(o + (size_t)Q * 4);
   w.grp_q0 = o; o = up256(o + (size_t)Q * 4);
   w.grp_nq = o; o = up256(o + (size_t)Q * 4);
-  w.tmp = o; o = up256(o + (size_t)Q * 4);
   w.grp_tile0 = o; o = up256(o + (size_t)(Q + 1) * 8);
   w.n_groups = o; o = up256(o + 4);
   w.count = o; o = up256(o + (size_t)Q * 4);
@@ -223,7 +222,6 @@ csa2_status csa2_index_topk(const csa2_bf16* iq, const float* w, int Q, int H,
   a.n_scored = reinterpret_cast<int32_t*>(base + L.n_scored);
   a.grp_q0 = reinterpret_cast<int32_t*>(base + L.grp_q0);
   a.grp_nq = reinterpret_cast<int32_t*>(base + L.grp_nq);
-  a.tmp = reinterpret_cast<int32_t*>(base + L.tmp);
   a.grp_tile0 = reinterpret_cast<int64_t*>(base + L.grp_tile0);
   a.n_groups = reinterpret_cast<int32_t*>(base + L.n_groups);
   a.topk_count = reinterpret_cast<int32_t*>(base + L.count);

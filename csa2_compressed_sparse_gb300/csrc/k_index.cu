@@ -50,111 +50,135 @@ struct GroupInfo {
 __device__ __forceinline__ int64_t n_visible(int64_t pos, int ratio) { return (pos + 1) / ratio; }
 
 // ---- prep: scored counts, query groups, tile prefix ---------------------------------
+// One pass over blocks of 1024 queries.  A query group is a run of at most group_max
+// consecutive queries of one sequence: query q starts a group when (q - run start) is
+// a multiple of group_max, and the group ends at group_max members or at the end of
+// the run.  The block's sequence ids and visible counts (plus a halo of kMaxGroup) sit
+// in shared memory, so a leader finds its members without global round trips; group
+// ids and tile offsets come from one block-wide exclusive scan of (leader, tiles).
 constexpr int kPrepThreads = 1024;
 
-__device__ int block_excl_sum(int v, int* red, int& total) {
+// Exclusive block sums of (x, y) over threads in index order, with the block totals.
+__device__ __forceinline__ void block_excl_sum2(int x, long long y, int* redx, long long* redy,
+                                                int& ex, long long& ey, int& tx, long long& ty) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  int incl = v;
+  int ix = x;
+  long long iy = y;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
-    int t = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-    if (lane >= o) incl += t;
+    const int tx1 = __shfl_up_sync(0xFFFFFFFFu, ix, o);
+    const long long ty1 = __shfl_up_sync(0xFFFFFFFFu, iy, o);
+    if (lane >= o) { ix += tx1; iy += ty1; }
   }
-  if (lane == 31) red[warp] = incl;
+  if (lane == 31) { redx[warp] = ix; redy[warp] = iy; }
   __syncthreads();
-  int base = 0, tot = 0;
-  for (int w = 0; w < kPrepThreads / 32; ++w) {
-    if (w < warp) base += red[w];
-    tot += red[w];
+  // every warp scans the 32 warp totals itself
+  const int wx = redx[lane];
+  const long long wy = redy[lane];
+  int sx = wx;
+  long long sy = wy;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int tx1 = __shfl_up_sync(0xFFFFFFFFu, sx, o);
+    const long long ty1 = __shfl_up_sync(0xFFFFFFFFu, sy, o);
+    if (lane >= o) { sx += tx1; sy += ty1; }
   }
-  __syncthreads();
-  total = tot;
-  return base + incl - v;
+  ex = __shfl_sync(0xFFFFFFFFu, sx - wx, warp) + ix - x;
+  ey = __shfl_sync(0xFFFFFFFFu, sy - wy, warp) + iy - y;
+  tx = __shfl_sync(0xFFFFFFFFu, sx, 31);
+  ty = __shfl_sync(0xFFFFFFFFu, sy, 31);
+  __syncthreads();  // redx / redy may be rewritten by the next call
 }
 
-__global__ void __launch_bounds__(kPrepThreads) index_prep_kernel(IndexArgs a, int32_t* tmp) {
-  __shared__ int red[kPrepThreads / 32];
-  __shared__ int carry_run;
-  __shared__ int carry_groups;
-  __shared__ long long carry_tiles;
-  const int tid = threadIdx.x;
+__global__ void __launch_bounds__(kPrepThreads) index_prep_kernel(IndexArgs a) {
+  __shared__ int s_seq[kPrepThreads + kMaxGroup];
+  __shared__ int s_ns[kPrepThreads + kMaxGroup];
+  __shared__ int redx[kPrepThreads / 32];
+  __shared__ long long redy[kPrepThreads / 32];
+  __shared__ int red_run[kPrepThreads / 32];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   griddep_launch_dependents();
   griddep_wait();
-  if (tid == 0) { carry_run = 0; carry_groups = 0; carry_tiles = 0; }
-  __syncthreads();
-  // pass 1: scored positions per query and group-start flags
+  int carry_run = 0, carry_groups = 0, prev_seq = -1;
+  long long carry_tiles = 0;
   for (int base = 0; base < a.Q; base += kPrepThreads) {
-    const int q = base + tid;
-    int start = 0;
-    if (q < a.Q) {
-      int64_t ns;
-      if (a.cand) ns = (int64_t)a.ncb * 8;
-      else {
-        ns = n_visible(a.q_pos[q], a.ratio);
-        if (ns > a.ld) { raise_fault(kFaultBounds); ns = a.ld; }
+    for (int i = tid; i < kPrepThreads + kMaxGroup; i += kPrepThreads) {
+      const int q = base + i;
+      if (q < a.Q) {
+        int64_t ns;
+        if (a.cand) {
+          ns = (int64_t)a.ncb * 8;
+        } else {
+          ns = n_visible(a.q_pos[q], a.ratio);
+          if (ns > a.ld) { if (i < kPrepThreads) raise_fault(kFaultBounds); ns = a.ld; }
+        }
+        s_seq[i] = a.q_seq[q];
+        s_ns[i] = (int)ns;
+        if (i < kPrepThreads) {
+          a.n_scored[q] = (int32_t)ns;
+          a.topk_count[q] = 0;
+        }
       }
-      a.n_scored[q] = (int32_t)ns;
-      a.topk_count[q] = 0;
-      start = (q == 0 || a.q_seq[q] != a.q_seq[q - 1]) ? q : -1;
-    } else {
-      start = -1;
     }
-    // inclusive max-scan of run starts
-    int v = start;
-    const int lane = tid & 31, warp = tid >> 5;
+    __syncthreads();
+    const int q = base + tid;
+    const bool in = q < a.Q;
+    // run start of q: inclusive max-scan of the positions where the sequence changes
+    int v = -1;
+    if (in) {
+      const int before = tid > 0 ? s_seq[tid - 1] : prev_seq;
+      v = (q == 0 || s_seq[tid] != before) ? q : -1;
+    }
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-      int t = __shfl_up_sync(0xFFFFFFFFu, v, o);
+      const int t = __shfl_up_sync(0xFFFFFFFFu, v, o);
       if (lane >= o) v = max(v, t);
     }
-    if (lane == 31) red[warp] = v;
+    if (lane == 31) red_run[warp] = v;
     __syncthreads();
-    int pre = carry_run;
-    for (int w = 0; w < warp; ++w) pre = max(pre, red[w]);
-    const int rs = max(pre, v);
-    __syncthreads();
-    if (tid == kPrepThreads - 1) carry_run = rs;
-    if (q < a.Q) tmp[q] = ((q - rs) % a.group_max) == 0 ? 1 : 0;
-    __syncthreads();
-  }
-  // pass 2: group ids, members and tile counts
-  for (int base = 0; base < a.Q; base += kPrepThreads) {
-    const int q = base + tid;
-    const int f = q < a.Q ? tmp[q] : 0;
-    int total;
-    const int g = carry_groups + block_excl_sum(f, red, total);
-    if (f) {
-      int nq = 1;
-      int64_t mx = a.n_scored[q];
-      while (nq < a.group_max && q + nq < a.Q && a.q_seq[q + nq] == a.q_seq[q] &&
-             tmp[q + nq] == 0) {
-        mx = max(mx, (int64_t)a.n_scored[q + nq]);
+    int rs = max(carry_run, v);
+    {
+      const int wv = red_run[lane];
+      int sv = lane < warp ? wv : -1;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) sv = max(sv, __shfl_xor_sync(0xFFFFFFFFu, sv, o));
+      rs = max(rs, sv);
+    }
+    // leaders: members and the group's largest visible count
+    const bool lead = in && ((q - rs) % a.group_max) == 0;
+    int nq = 0;
+    long long tiles = 0;
+    if (lead) {
+      nq = 1;
+      int mx = s_ns[tid];
+      while (nq < a.group_max && q + nq < a.Q && s_seq[tid + nq] == s_seq[tid]) {
+        mx = max(mx, s_ns[tid + nq]);
         ++nq;
       }
+      tiles = (mx + kTileRows - 1) / kTileRows;
+    }
+    int ex, tx;
+    long long ey, ty;
+    block_excl_sum2(lead ? 1 : 0, tiles, redx, redy, ex, ey, tx, ty);
+    if (lead) {
+      const int g = carry_groups + ex;
       a.grp_q0[g] = q;
       a.grp_nq[g] = nq;
-      a.grp_tile0[g] = (mx + kTileRows - 1) / kTileRows;  // count for now
+      a.grp_tile0[g] = carry_tiles + ey;
     }
+    // carries into the next block (every thread keeps its own copy); block_excl_sum2
+    // ended with a barrier, so red_run is free
+    if (tid == kPrepThreads - 1) red_run[0] = rs;
     __syncthreads();
-    if (tid == 0) carry_groups += total;
-    __syncthreads();
-  }
-  const int ng = carry_groups;
-  // pass 3: exclusive prefix of tile counts (in place), total at [ng]
-  for (int base = 0; base < ng; base += kPrepThreads) {
-    const int g = base + tid;
-    const int64_t c = g < ng ? a.grp_tile0[g] : 0;
-    // 64-bit scan through two 32-bit halves is unnecessary: counts fit in int
-    int total;
-    const int ex = block_excl_sum((int)c, red, total);
-    if (g < ng) a.grp_tile0[g] = carry_tiles + ex;
-    __syncthreads();
-    if (tid == 0) carry_tiles += total;
-    __syncthreads();
+    carry_run = red_run[0];
+    prev_seq = s_seq[kPrepThreads - 1];
+    carry_groups += tx;
+    carry_tiles += ty;
+    __syncthreads();  // s_seq / s_ns / red_run are rewritten by the next block
   }
   if (tid == 0) {
-    a.grp_tile0[ng] = carry_tiles;
-    *a.n_groups = ng;
+    a.grp_tile0[carry_groups] = carry_tiles;
+    *a.n_groups = carry_groups;
   }
 }
 
@@ -453,7 +477,7 @@ size_t index_smem_bytes() {
 
 cudaError_t launch_index(const IndexArgs& a, int num_sms, cudaStream_t s) {
   if (a.Q == 0) return cudaSuccess;
-  cudaError_t e = launch_pdl(index_prep_kernel, dim3(1), dim3(kPrepThreads), 0, s, a, a.tmp);
+  cudaError_t e = launch_pdl(index_prep_kernel, dim3(1), dim3(kPrepThreads), 0, s, a);
   if (e != cudaSuccess) return e;
   CUtensorMap kt, kb, qm;
   if (!encode_rows_bf16(&kt, a.index_k, (uint64_t)a.index_rows, kDIdx, 64, kTileRows) ||

@@ -205,14 +205,24 @@ SMALL = {
     "reindex_ragged": lambda: W.reindex_decode(B=3, ctx=9000, ncb=100, seed=26),
     "prefill_small": lambda: W.prefill_reuse(n_new=128, ctx=4224, layers=3, seed=23),
     "long_small": lambda: W.long_decode(B=2, ctx=40000, seed=24),
+    # three prefilling sequences, 2100 queries: query runs cross the 1024-query blocks of
+    # the grouping pass (groups of four queries restart at every sequence)
+    "prefill_multi": lambda: W.Workload(
+        "prefill_multi", 27, 2, ctx=[2000, 1601, 2300], chunk=[700, 501, 900],
+        nq=[700, 501, 900], swa="linear", layers=1,
+        description="three prefill chunks, 2101 queries"),
 }
+
+# queries checked per small workload (all of them when there are few)
+SMALL_QUERIES = {"prefill_multi": [0, 3, 699, 700, 701, 1020, 1023, 1024, 1027, 1200, 1201,
+                                   1202, 2047, 2048, 2100]}
 
 
 @pytest.mark.parametrize("name", list(SMALL))
 def test_step_small(name):
     wl = SMALL[name]()
     t, spec, buf = run_workload(wl)
-    qs = list(range(wl.Q)) if wl.Q <= 12 else [0, 1, 31, 64, 65, wl.Q - 1]
+    qs = SMALL_QUERIES.get(name, list(range(wl.Q)) if wl.Q <= 12 else [0, 1, 31, 64, 65, wl.Q - 1])
     check_queries(wl, t, buf, qs)
 
 
