@@ -26,8 +26,9 @@
 //            (log2 units: P <= 2^64 keeps bf16 P and the fp32 sums finite).  P is
 //            written in one pass with the current max; when a head's max moved the
 //            chunk's pass is redone and warps 0..3 rescale O^T in TMEM (a barrier vote)
-//   O^T     += V^T[512 x 64] . P^T[64 x 64] -> TMEM, four M = 128 tiles; the KV buffer
-//            is the A operand again, read MN-major, and P [head][row] is the B operand
+//   O^T     += V^T[512 x 64] . P^T[64 x 64] -> TMEM, four M = 128 tiles issued by two
+//            threads; the KV buffer is the A operand again, read MN-major, and P
+//            [head][row] is the B operand
 // S of the next chunk runs while the softmax of this one does, and the gather of
 // chunk c + 2 starts as soon as the PV of chunk c has released its buffer.
 // With nsplit = 1 the CTA starts from the sink (running max = sink, running sum = 1)
@@ -37,7 +38,7 @@
 // merges them; the merges add the sink's e^{sink_h} once.
 //
 // Warps 0..3 softmax + O^T rescale + output, warps 4..19 gather (teams of eight
-// warps), warps 20..22 issue the MMAs (lane 0 each; warp 20 also owns the TMEM).
+// warps), warps 20..23 issue the MMAs (lane 0 each; warp 20 also owns the TMEM).
 #include <cuda_fp8.h>
 
 #include "common.cuh"
@@ -47,11 +48,11 @@ CSA2_DEFINE_FAULT_FLAG(attn)
 namespace csa2 {
 namespace {
 
-constexpr int kThreads = 736;             // 23 warps
+constexpr int kThreads = 768;             // 24 warps
 constexpr int kGroupThreads = 128;        // warps 0..3
 constexpr int kTeam = 256;                // threads per gather team
 constexpr int kGatherWarp0 = 4;
-constexpr int kMmaWarp = 20;              // warps 20..22 issue the MMAs
+constexpr int kMmaWarp = 20;              // warps 20..23 issue the MMAs
 constexpr int kChunk = 64;                // rows per chunk
 constexpr int kMaxChunks = 10;            // 2 window + 8 selected chunks
 constexpr int kDimBlock = 64 * 128;       // one 64-dim block of 64 rows (8 KiB)
@@ -77,8 +78,8 @@ struct __align__(16) Aux {
   uint64_t kv_full[2];  // KV buffer filled (one arrival of the team)
   uint64_t s_full[2];   // both S halves of the buffer written (two commits)
   uint64_t p_full[2];   // P buffer written and O^T rescaled (128 arrivals)
-  uint64_t pv_done[2];  // PV of the buffer's chunk complete (commit)
-  uint64_t fin[3];      // every MMA of an issuer complete (commit)
+  uint64_t pv_done[2];  // PV of the buffer's chunk complete (two commits)
+  uint64_t fin[4];      // every MMA of an issuer complete (commit)
   uint64_t merge_full;  // cluster merge: the peer's pieces and (max, sum) landed
   uint32_t tmem_slot;
   int nchunk;
@@ -261,7 +262,8 @@ __device__ __forceinline__ void gather_chunk(const int32_t* rows, bool fp8, cons
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
-    sparse_attn_kernel(AttnArgs a, const __grid_constant__ CUtensorMap qmap) {
+    sparse_attn_kernel(AttnArgs a, const __grid_constant__ CUtensorMap qmap,
+                       const __grid_constant__ CUtensorMap wmap) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -277,14 +279,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   griddep_launch_dependents();
   if (tid == 0) {
     prefetch_tensormap(&qmap);
+    prefetch_tensormap(&wmap);
     mbar_init(smem_u32(&X.q_full), 1);
     for (int b = 0; b < 2; ++b) {
       mbar_init(smem_u32(&X.kv_full[b]), 1);
       mbar_init(smem_u32(&X.s_full[b]), 2);
       mbar_init(smem_u32(&X.p_full[b]), kGroupThreads);
-      mbar_init(smem_u32(&X.pv_done[b]), 1);
+      mbar_init(smem_u32(&X.pv_done[b]), 2);
     }
-    for (int r = 0; r < 3; ++r) mbar_init(smem_u32(&X.fin[r]), 1);
+    for (int r = 0; r < 4; ++r) mbar_init(smem_u32(&X.fin[r]), 1);
     mbar_init(smem_u32(&X.merge_full), 1);
     X.nchunk = 0;
     X.abort = 0;
@@ -338,7 +341,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       X.rowidx[slot][r] = idx32;
-      // the 32 lanes of a warp cover one half of a slot (672 threads = 21 warps)
+      // the 32 lanes of a warp cover one half of a slot (768 threads = 24 warps)
       const uint32_t vm = __ballot_sync(0xFFFFFFFFu, idx32 >= 0);
       if (lane == 0) X.rowmask[slot][r >> 5] = vm;
     }
@@ -371,6 +374,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int slot = X.chunks[it];
       const int c = rank + slot * nsplit;
       const bool fp8 = c < 2 && a.swa_dtype == 1;
+      // a full window chunk of a LINEAR bf16 window is 64 consecutive rows: one TMA box
+      // of 64 x 64 per dim block
+      if (c < 2 && a.swa_mode == 1 && a.swa_dtype == 0 &&
+          (X.rowmask[slot][0] & X.rowmask[slot][1]) == 0xFFFFFFFFu) {
+        if (t == 0) {
+          mbar_arrive_expect_tx(full_bar, kBufBytes);
+          const int32_t y0 = X.rowidx[slot][0];
+          const uint64_t pol = policy_evict_first();
+#pragma unroll
+          for (int db = 0; db < 8; ++db)
+            tma_load_2d(kvb + db * kDimBlock, &wmap, 64 * db, y0, full_bar, pol);
+        }
+        continue;
+      }
       const uint8_t* base = c < 2 ? a.swa : reinterpret_cast<const uint8_t*>(a.plane);
       gather_chunk(X.rowidx[slot], fp8, base, kvb, t);
       cp_async_commit();
@@ -385,9 +402,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (t == 0 && last >= 0) mbar_wait(full_bar, (uint32_t)(last >> 1) & 1, 100000000ull);
   } else if (warp >= kMmaWarp) {
     // ====== MMA issuers (lane 0): warp 20 S over dims 0..255, warp 21 S over dims
-    // 256..511 (two accumulators, summed by the softmax), warp 22 PV ======
+    // 256..511 (two accumulators, summed by the softmax), warps 22 and 23 PV into O^T
+    // tiles 0, 1 and 2, 3 ======
     // One thread issues a tcgen05.mma about every 28 ns however small it is, so the
-    // chunk's 48 small MMAs are spread over three threads.
+    // chunk's 48 small MMAs are spread over four threads.
     const int role = warp - kMmaWarp;
     if (lane == 0 && n > 0) {
       int issued = 0;
@@ -427,7 +445,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t kvb = kv0 + (c & 1) * kBufBytes;
           const uint32_t pb = p0 + (c & 1) * kPBytes;
 #pragma unroll
-          for (int mt = 0; mt < 4; ++mt)
+          for (int mt = 2 * (role - 2); mt < 2 * (role - 2) + 2; ++mt)
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
               umma_bf16(tmem + kColO + 64 * mt,
@@ -731,9 +749,14 @@ int attn_num_splits(int Q, int nsel, int num_sms) {
 
 cudaError_t launch_attn(const AttnArgs& a, int nsplit, cudaStream_t s) {
   if (a.Q == 0) return cudaSuccess;
-  // Q of each query as eight boxes of 64 heads x 64 dims
-  CUtensorMap qm;
+  // Q of each query as eight boxes of 64 heads x 64 dims; a LINEAR bf16 window as boxes of
+  // 64 rows x 64 dims (the Q map stands in when there is none)
+  CUtensorMap qm, wm;
   if (!encode_rows_bf16(&qm, a.q, (uint64_t)a.Q * kHeads, kDLat, 64, 64))
+    return cudaErrorInvalidValue;
+  wm = qm;
+  if (a.swa_mode == 1 && a.swa_dtype == 0 && a.swa_rows > 0 &&
+      !encode_rows_bf16(&wm, a.swa, (uint64_t)a.swa_rows, kDLat, 64, 64))
     return cudaErrorInvalidValue;
   const size_t smem = attn_smem_bytes();
   cudaError_t e = cudaFuncSetAttribute(sparse_attn_kernel,
@@ -743,10 +766,10 @@ cudaError_t launch_attn(const AttnArgs& a, int nsplit, cudaStream_t s) {
     AttnArgs b = a;
     b.cluster = 1;
     return launch_pdl_cluster(sparse_attn_kernel, dim3(2u, (unsigned)a.Q), dim3(kThreads), smem, s,
-                              2u, b, qm);
+                              2u, b, qm, wm);
   }
   e = launch_pdl(sparse_attn_kernel, dim3((unsigned)nsplit, (unsigned)a.Q), dim3(kThreads), smem,
-                 s, a, qm);
+                 s, a, qm, wm);
   if (e != cudaSuccess || nsplit == 1) return e;
   return launch_pdl(attn_combine_kernel, dim3((unsigned)a.Q, kHeads / 8), dim3(256), 0, s, a,
                     nsplit);
