@@ -37,6 +37,7 @@ constexpr int kMaxChunks = 48;     // the merge holds kMaxChunks * 512 <= kChunk
 constexpr int kCandCap = 8192;     // kept (key, index) pairs
 constexpr int kWarpCap = kCandCap / (kTopkThreads / 32);  // per-warp region
 constexpr int kWords = kChunkLen / 32;
+constexpr int kSample = 2048;      // keys sampled for the threshold
 
 namespace {
 
@@ -78,8 +79,8 @@ __device__ void find_crossing(SelectSmem& S, const uint32_t* hist, int nbins, in
   if (tid == 0) { S.found_bin = 0; S.found_above = 0; }
   if (lane == 31) S.warp_a[warp] = incl;
   __syncthreads();
-  // every warp scans the 32 warp totals itself
-  const int wt = S.warp_a[lane];
+  // every warp scans the warp totals itself
+  const int wt = lane < kTopkWarps ? S.warp_a[lane] : 0;
   int wi = wt;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
@@ -172,7 +173,7 @@ __device__ int select_topk(const RowSrc<kKind>& src, int n, int k, SelectSmem& S
   for (int w = tid; w < nw; w += kTopkThreads) { S.selmap[w] = 0; S.eqmap[w] = 0; }
   __syncthreads();
   // ---- 2. threshold from an even sample of 2048 keys ----
-  const int ns = n < 2 * kTopkThreads ? n : 2 * kTopkThreads;
+  const int ns = n < kSample ? n : kSample;
   for (int s2 = tid; s2 < ns; s2 += kTopkThreads) {
     const uint32_t key = src((int)(((int64_t)(2 * s2 + 1) * n) / (2 * ns)));
     if (key) atomicAdd(&S.hist[key >> 21], 1u);

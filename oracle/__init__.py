@@ -42,6 +42,8 @@ def lib():
         L.orc_sparse_attn.argtypes = [_vp, _i32, _vp, _vp, _i32, _i32, _vp, _vp, _vp, _vp, _vp,
                                       _vp, _i32, _vp, _dbl, _vp, _vp]
         L.orc_sparse_attn.restype = None
+        L.orc_inverse_rope.argtypes = [_vp, _i32, _vp, _vp]
+        L.orc_inverse_rope.restype = None
         _LIB = L
     return _LIB
 
@@ -135,7 +137,7 @@ def topk(scores, rows, k):
 
 
 def sparse_attn(q, q_seq, q_pos, swa, plane, row_base, sel, sink, scale=512 ** -0.5,
-                swa_mode="ring", lin_base=None, lin_pos0=None):
+                swa_mode="ring", lin_base=None, lin_pos0=None, inv_freq=None):
     """q [Q,64,512] bf16, swa ring [B,128,512] bf16 / [B,128,528] uint8 or linear rows,
     plane [rows,512] bf16, sel [Q,nsel] int32.  Returns (out [Q,64,512], lse [Q,64])
     in float64."""
@@ -162,4 +164,16 @@ def sparse_attn(q, q_seq, q_pos, swa, plane, row_base, sel, sink, scale=512 ** -
     lse = np.zeros((Q, 64), dtype=np.float64)
     lib().orc_sparse_attn(_p(qb), Q, _p(qs), _p(qp), mode, dt, _p(swa_arr), _p(lb), _p(lp),
                           _p(pb), _p(rb), _p(sl), nsel, _p(sk), scale, _p(out), _p(lse))
+    if inv_freq is not None:
+        inverse_rope(out, qp, inv_freq)
     return out, lse
+
+
+def inverse_rope(out, q_pos, inv_freq):
+    """Rotate dims 448..511 of out [Q,64,512] (float64, in place) back by each query's
+    position: pair i times e^{-i p inv_freq[i]}."""
+    assert out.dtype == np.float64 and out.flags["C_CONTIGUOUS"]
+    qp = np.ascontiguousarray(q_pos, dtype=np.int64)
+    f = np.ascontiguousarray(inv_freq, dtype=np.float32)
+    lib().orc_inverse_rope(_p(out), out.shape[0], _p(qp), _p(f))
+    return out

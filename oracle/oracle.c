@@ -305,3 +305,29 @@ void orc_sparse_attn(const uint16_t* q, int Q, const int32_t* q_seq, const int64
     free(x);
   }
 }
+
+/* ---- inverse RoPE of the attention output [A] "出来之后" (out -> inverse RoPE at the
+ *      query's own position, because K = V carries the rotation); [B] §6.1 (the output's
+ *      last 64 dims times the conjugate phase); [C] A.12.1 -----------------------------
+ *
+ * For query q at position p and every head, pair i of dims 448 + 2i, 449 + 2i, read as
+ * a complex number, is multiplied by e^{-i p theta_i} with theta_i = inv_freq[i]:
+ *   a0' = a0 cos(p theta_i) + a1 sin(p theta_i)
+ *   a1' = a1 cos(p theta_i) - a0 sin(p theta_i)
+ * The other 448 dims are unchanged.  out is [Q][64][512] double, rotated in place. */
+void orc_inverse_rope(double* out, int Q, const int64_t* q_pos, const float* inv_freq) {
+#pragma omp parallel for schedule(static)
+  for (int qi = 0; qi < Q; qi++) {
+    const double p = (double)q_pos[qi];
+    for (int i = 0; i < 32; i++) {
+      const double ang = p * (double)inv_freq[i];
+      const double c = cos(ang), s = sin(ang);
+      for (int h = 0; h < N_HEADS; h++) {
+        double* o = out + ((int64_t)qi * N_HEADS + h) * D_LAT + ROPE_DIM0 + 2 * i;
+        const double a0 = o[0], a1 = o[1];
+        o[0] = a0 * c + a1 * s;
+        o[1] = a1 * c - a0 * s;
+      }
+    }
+  }
+}

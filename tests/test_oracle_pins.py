@@ -165,6 +165,49 @@ def test_rope_unit_vector_phase_and_sign():
             np.testing.assert_allclose(y[448:450], [-r * math.sin(a), r * math.cos(a)], atol=1e-12)
 
 
+def test_inverse_rope_undoes_the_compressor_rotation_at_the_same_position():
+    # [A] "出来之后" / [B] §6.1: the attention output's last 64 dims are rotated back at the
+    # query's own position.  A row the compressor rotated at position t (ratio 1), read
+    # back by a query at position t, must come out as the unrotated RMSNorm row; rows read
+    # at another position keep the difference of the two phases.
+    S = 9
+    kv = RNG.standard_normal((S, 512))
+    n, _, pf, *_ = run_compress(kv, kv, 1, [S])
+    kvr = bf16(kv).double().numpy()  # the compressor sees bf16 inputs
+    plain = kvr / np.sqrt(np.mean(kvr ** 2, axis=1, keepdims=True) + 1e-6)
+    out = np.repeat(pf[:, None, :], 64, axis=1).copy()  # every head sees its row
+    oracle.inverse_rope(out, np.arange(S), INV_FREQ)
+    for t in range(S):
+        np.testing.assert_allclose(out[t], np.broadcast_to(plain[t], (64, 512)), atol=1e-12)
+    out = np.repeat(pf[:, None, :], 64, axis=1).copy()
+    oracle.inverse_rope(out, np.arange(S) + 3, INV_FREQ)  # three positions later
+    for t in range(S):
+        for i in (0, 5, 31):
+            a = -3.0 * float(INV_FREQ[i])
+            c, s_ = math.cos(a), math.sin(a)
+            x0, x1 = plain[t, 448 + 2 * i], plain[t, 449 + 2 * i]
+            np.testing.assert_allclose(out[t, 7, 448 + 2 * i:450 + 2 * i],
+                                       [x0 * c - x1 * s_, x0 * s_ + x1 * c], atol=1e-12)
+
+
+def test_inverse_rope_unit_vector_and_invariants():
+    # (1, 0) in pair i at position p maps to (cos p theta_i, -sin p theta_i) (the
+    # conjugate phase); the 448 content dims and every pair's norm are unchanged.
+    out = np.zeros((3, 64, 512))
+    out[:, :, 448::2] = 1.0
+    out[:, :, :448] = RNG.standard_normal((3, 64, 448))
+    before = out.copy()
+    pos = np.array([0, 7, 1048575])
+    oracle.inverse_rope(out, pos, INV_FREQ)
+    for qi, p in enumerate(pos):
+        ang = p * INV_FREQ.astype(np.float64)
+        np.testing.assert_allclose(out[qi, 11, 448::2], np.cos(ang), atol=1e-12)
+        np.testing.assert_allclose(out[qi, 11, 449::2], -np.sin(ang), atol=1e-12)
+    assert np.array_equal(out[:, :, :448], before[:, :, :448])
+    norms = out[:, :, 448::2] ** 2 + out[:, :, 449::2] ** 2
+    np.testing.assert_allclose(norms, 1.0, atol=1e-12)
+
+
 def test_ratio2_group_head_position_and_equal_scores_mean():
     # Two identical tokens with equal gates pool to that token; the row must then equal
     # the ratio-1 row at the group's FIRST position j*m (not j*m+1).
