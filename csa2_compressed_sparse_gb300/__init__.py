@@ -20,6 +20,7 @@ __all__ = [
     "csa2_index_topk_workspace_size", "csa2_index_topk", "csa2_index_topk_noalloc",
     "csa2_topk_workspace_size",
     "csa2_topk_scores", "csa2_attn_workspace_size", "csa2_sparse_attn", "csa2_reuse_attn",
+    "csa2_sparse_attn_rope", "csa2_reuse_attn_rope",
 ]
 
 STATUS = {0: "CSA2_OK", 1: "CSA2_EINVAL", 2: "CSA2_ECUDA", 3: "CSA2_ETIMEOUT", 4: "CSA2_EBOUNDS",
@@ -60,6 +61,10 @@ _SIGS = {
                           _vp, _f32, _vp, _vp, _vp, _sz, _vp], _i32),
     "csa2_reuse_attn": ([_vp, _i32, _vp, _vp, ctypes.POINTER(_SwaC), _vp, _i64, _vp, _vp, _i32,
                          _vp, _f32, _vp, _vp, _vp, _sz, _vp], _i32),
+    "csa2_sparse_attn_rope": ([_vp, _i32, _vp, _vp, ctypes.POINTER(_SwaC), _vp, _i64, _vp, _vp,
+                               _i32, _vp, _f32, _vp, _vp, _vp, _sz, _vp, _vp], _i32),
+    "csa2_reuse_attn_rope": ([_vp, _i32, _vp, _vp, ctypes.POINTER(_SwaC), _vp, _i64, _vp, _vp,
+                              _i32, _vp, _f32, _vp, _vp, _vp, _sz, _vp, _vp], _i32),
 }
 
 _LIB = None
@@ -175,14 +180,15 @@ def csa2_attn_workspace_size(Q, nsel):
     return int(lib().csa2_attn_workspace_size(Q, nsel))
 
 
-def _attn(fn, q, q_seq, q_pos, swa, plane, row_base, sel, sink, out, lse, scale, ws, stream):
+def _attn(fn, q, q_seq, q_pos, swa, plane, row_base, sel, sink, out, lse, scale, ws, stream,
+          *extra):
     sw = swa.c()
     nsel = 0 if sel is None else sel.shape[1]
     plane_rows = 0 if plane is None else plane.shape[0]
     nbytes = 0 if ws is None else ws.numel() * ws.element_size()
     _check(fn(_p(q), q.shape[0], _p(q_seq), _p(q_pos), ctypes.byref(sw), _p(plane), plane_rows,
               _p(row_base), _p(sel), nsel, _p(sink), float(scale), _p(out), _p(lse), _p(ws),
-              nbytes, _stream(stream)))
+              nbytes, *[_p(x) for x in extra], _stream(stream)))
 
 
 def csa2_sparse_attn(q, q_seq, q_pos, swa: Swa, plane, row_base, sel, sink, out, lse=None,
@@ -195,3 +201,17 @@ def csa2_reuse_attn(q, q_seq, q_pos, swa: Swa, plane, row_base, sel, sink, out, 
                     scale=512 ** -0.5, ws=None, stream=None):
     _attn(lib().csa2_reuse_attn, q, q_seq, q_pos, swa, plane, row_base, sel, sink, out, lse,
           scale, ws, stream)
+
+
+def csa2_sparse_attn_rope(q, q_seq, q_pos, swa: Swa, plane, row_base, sel, sink, out, inv_freq,
+                          lse=None, scale=512 ** -0.5, ws=None, stream=None):
+    """csa2_sparse_attn with the output's dims 448..511 rotated back by q_pos."""
+    _attn(lib().csa2_sparse_attn_rope, q, q_seq, q_pos, swa, plane, row_base, sel, sink, out,
+          lse, scale, ws, stream, inv_freq)
+
+
+def csa2_reuse_attn_rope(q, q_seq, q_pos, swa: Swa, plane, row_base, sel, sink, out, inv_freq,
+                         lse=None, scale=512 ** -0.5, ws=None, stream=None):
+    """csa2_reuse_attn with the output's dims 448..511 rotated back by q_pos."""
+    _attn(lib().csa2_reuse_attn_rope, q, q_seq, q_pos, swa, plane, row_base, sel, sink, out,
+          lse, scale, ws, stream, inv_freq)

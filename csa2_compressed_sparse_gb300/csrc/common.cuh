@@ -101,6 +101,7 @@ struct AttnArgs {
   float* part_o;   // [Q][nsplit][64][512] partial outputs (nsplit > 1)
   float* part_ml;  // [Q][nsplit][2][64] partial running max (log2) and sum
   int cluster;     // nsplit == 2: the two CTAs of a query form a cluster and merge in place
+  const float* inv_freq;  // [32] or null: rotate the output's dims 448..511 back by q_pos
 };
 
 cudaError_t launch_compress(const CompressArgs& a, cudaStream_t s);
@@ -129,6 +130,19 @@ int take_fault_attn();
 
 // Order-preserving map of fp32 scores to uint32 keys: NaN ranks as -inf, -0 as +0,
 // and every key of a real score is >= 1 so that 0 can mark "not scored".
+// RoPE phase of position p for frequency theta: theta / (2 pi) is kept as a 64-bit binary
+// fraction of a turn (its fractional part only), so (p * turn) mod 2^64 is the phase of
+// p exactly in integer arithmetic; read as a signed fraction it is an angle in [-pi, pi).
+__device__ __forceinline__ uint64_t rope_turn(float theta) {
+  double tr = (double)theta * 0.15915494309189535;
+  tr -= floor(tr);
+  const double sc = tr * 18446744073709551616.0;  // 2^64
+  return sc >= 18446744073709551615.0 ? ~0ull : (uint64_t)sc;
+}
+__device__ __forceinline__ float rope_angle(uint64_t turn, uint64_t p) {
+  return (float)(int64_t)(p * turn) * 3.4061215800865545e-19f;  // 2 pi / 2^64
+}
+
 __host__ __device__ __forceinline__ uint32_t score_key(float f) {
   uint32_t u;
 #ifdef __CUDA_ARCH__

@@ -85,7 +85,7 @@ csa2_status attn_common(const char* name, const csa2_bf16* q, int Q, const int32
                         const int64_t* q_pos, const csa2_swa* swa, const csa2_bf16* plane,
                         int64_t plane_rows, const int64_t* row_base, const int32_t* sel, int nsel,
                         const float* sink, float scale, csa2_bf16* out, float* lse, void* ws,
-                        size_t ws_bytes, csa2_stream stream) {
+                        size_t ws_bytes, const float* inv_freq, csa2_stream stream) {
   REQUIRE(Q >= 0 && Q <= 65535, "%s: Q must be in [0, 65535] (got %d)", name, Q);
   if (Q == 0) return CSA2_OK;
   REQUIRE(q && q_seq && q_pos && swa && out, "%s: q, q_seq, q_pos, swa and out are required", name);
@@ -110,6 +110,7 @@ csa2_status attn_common(const char* name, const csa2_bf16* q, int Q, const int32
   a.lin_base = swa->lin_base; a.lin_pos0 = swa->lin_pos0;
   a.plane = plane; a.plane_rows = plane_rows; a.row_base = row_base;
   a.sel = sel; a.nsel = nsel; a.sink = sink; a.scale = scale; a.out = out; a.lse = lse;
+  a.inv_freq = inv_freq;
   REQUIRE(ws == nullptr || (reinterpret_cast<uintptr_t>(ws) & 255u) == 0,
           "%s: ws must be 256-byte aligned", name);
   const int sms = num_sms();
@@ -294,7 +295,7 @@ csa2_status csa2_sparse_attn(const csa2_bf16* q, int Q, const int32_t* q_seq,
                              int nsel, const float* sink, float scale, csa2_bf16* out, float* lse,
                              void* ws, size_t ws_bytes, csa2_stream stream) {
   return attn_common("csa2_sparse_attn", q, Q, q_seq, q_pos, swa, plane, plane_rows, row_base,
-                     sel, nsel, sink, scale, out, lse, ws, ws_bytes, stream);
+                     sel, nsel, sink, scale, out, lse, ws, ws_bytes, nullptr, stream);
 }
 
 csa2_status csa2_reuse_attn(const csa2_bf16* q, int Q, const int32_t* q_seq,
@@ -303,7 +304,31 @@ csa2_status csa2_reuse_attn(const csa2_bf16* q, int Q, const int32_t* q_seq,
                             int nsel, const float* sink, float scale, csa2_bf16* out, float* lse,
                             void* ws, size_t ws_bytes, csa2_stream stream) {
   return attn_common("csa2_reuse_attn", q, Q, q_seq, q_pos, swa, plane, plane_rows, row_base,
-                     sel, nsel, sink, scale, out, lse, ws, ws_bytes, stream);
+                     sel, nsel, sink, scale, out, lse, ws, ws_bytes, nullptr, stream);
+}
+
+csa2_status csa2_sparse_attn_rope(const csa2_bf16* q, int Q, const int32_t* q_seq,
+                                  const int64_t* q_pos, const csa2_swa* swa,
+                                  const csa2_bf16* plane, int64_t plane_rows,
+                                  const int64_t* row_base, const int32_t* sel, int nsel,
+                                  const float* sink, float scale, csa2_bf16* out, float* lse,
+                                  void* ws, size_t ws_bytes, const float* inv_freq,
+                                  csa2_stream stream) {
+  REQUIRE(inv_freq != nullptr, "csa2_sparse_attn_rope: inv_freq is required");
+  return attn_common("csa2_sparse_attn_rope", q, Q, q_seq, q_pos, swa, plane, plane_rows,
+                     row_base, sel, nsel, sink, scale, out, lse, ws, ws_bytes, inv_freq, stream);
+}
+
+csa2_status csa2_reuse_attn_rope(const csa2_bf16* q, int Q, const int32_t* q_seq,
+                                 const int64_t* q_pos, const csa2_swa* swa,
+                                 const csa2_bf16* plane, int64_t plane_rows,
+                                 const int64_t* row_base, const int32_t* sel, int nsel,
+                                 const float* sink, float scale, csa2_bf16* out, float* lse,
+                                 void* ws, size_t ws_bytes, const float* inv_freq,
+                                 csa2_stream stream) {
+  REQUIRE(inv_freq != nullptr, "csa2_reuse_attn_rope: inv_freq is required");
+  return attn_common("csa2_reuse_attn_rope", q, Q, q_seq, q_pos, swa, plane, plane_rows,
+                     row_base, sel, nsel, sink, scale, out, lse, ws, ws_bytes, inv_freq, stream);
 }
 
 }  // extern "C"

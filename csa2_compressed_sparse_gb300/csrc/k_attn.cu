@@ -64,11 +64,14 @@ constexpr uint32_t kColSb = 128;          // the same for dims 256..511: 128 + 6
 constexpr uint32_t kColO = 256;           // O^T tiles at 256 + 64 * mt
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLazy = 64.0f;
+constexpr int kRopeDim0 = 448;            // dims 448..511 carry the RoPE phase
 
 struct __align__(16) Aux {
   float m_run[64];
   float l_run[64];
   float fac[2][64];  // rescale factor per head, by chunk parity (merge weights at the end)
+  float rope_c[32];  // inverse RoPE of the output at the query position: cos, sin of
+  float rope_s[32];  // p theta_i for pair i (dims 448 + 2i, 449 + 2i)
   float peer_m[64];  // cluster merge: the other CTA's running max and sum (filled by a
   float peer_l[64];  // bulk copy of its m_run, l_run: the pairs must stay adjacent)
   int32_t rowidx[kMaxChunks][kChunk];  // source row per slot (chunk = rank + slot * nsplit)
@@ -158,6 +161,16 @@ __device__ __forceinline__ void p_pass(uint32_t sa, uint32_t sb, bool full, uint
   }
 }
 
+// cos, sin of p theta_i for the 32 RoPE pairs (one warp: lane i), for the output's inverse
+// rotation at the query position p.
+__device__ __forceinline__ void rope_table(const float* inv_freq, int64_t p, int lane, float* rc,
+                                           float* rs) {
+  float s, c;
+  sincosf(rope_angle(rope_turn(inv_freq[lane]), (uint64_t)p), &s, &c);
+  rc[lane] = c;
+  rs[lane] = s;
+}
+
 // O^T tiles mt0 .. mt0 + ntile - 1 from TMEM into shared memory as fp32 rows of 64 heads
 // (256 B per dim), 16-byte pieces swizzled by the dim (piece c of row d at c ^ (d & 15));
 // row = dim - 128 mt0.  Warps 0..3 (TMEM lanes 32 w ..); with n == 0 the tiles are zero.
@@ -190,14 +203,17 @@ __device__ __forceinline__ void stage_ot(uint32_t tmem_o, int warp, int lane, in
 
 // out[q][h][dbase + d] = bf16(own[d][h] w0[h] + peer[d][h] w1[h]) for nd dims, from rows
 // staged by stage_ot (peer may be null); all threads of the CTA, 16-byte stores of eight
-// dims of one head, a warp covering 32 heads of one group of eight dims.
+// dims of one head, a warp covering 32 heads of one group of eight dims.  With rc / rs
+// (cos, sin of p theta_i), pair i of dims 448.. is rotated back: times e^{-i p theta_i}.
 __device__ __forceinline__ void out_pass(const float* own, const float* peer, const float* w0,
-                                         const float* w1, uint16_t* out_q, int nd, int dbase,
-                                         int warp, int lane, int nwarps) {
+                                         const float* w1, const float* rc, const float* rs,
+                                         uint16_t* out_q, int nd, int dbase, int warp, int lane,
+                                         int nwarps) {
   const int items = 2 * (nd >> 3);  // (head half, group of 8 dims)
   for (int it = warp; it < items; it += nwarps) {
     const int h = 32 * (it & 1) + lane, dg = it >> 1;
     const float a = w0[h], b = peer ? w1[h] : 0.f;
+    const int gd = dbase + dg * 8;  // first output dim of the group
     uint32_t pk[4];
 #pragma unroll
     for (int k = 0; k < 8; k += 2) {
@@ -207,6 +223,13 @@ __device__ __forceinline__ void out_pass(const float* own, const float* peer, co
         const int d = dg * 8 + k + e;
         const int idx = d * 64 + ((((h >> 2) ^ (d & 15))) << 2) + (h & 3);
         o[e] = own[idx] * a + (peer ? peer[idx] * b : 0.f);
+      }
+      if (rc && gd >= kRopeDim0) {
+        const int i = (gd + k - kRopeDim0) >> 1;
+        const float c = rc[i], s = rs[i];
+        const float o0 = o[0] * c + o[1] * s, o1 = o[1] * c - o[0] * s;
+        o[0] = o0;
+        o[1] = o1;
       }
       pk[k >> 1] = pack_bf16x2(o[0], o[1]);
     }
@@ -600,10 +623,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     // O^T / l -> bf16 out[q][64 heads][512]: O^T staged in the KV buffers (all 512 dims),
     // then every thread writes
     if (tid < 64) X.fac[0][tid] = 1.f / X.l_run[tid];
+    if (a.inv_freq && warp == 4) rope_table(a.inv_freq, p, lane, X.rope_c, X.rope_s);
     if (warp < 4) stage_ot(tmem + kColO, warp, lane, 0, 4, smem_u32(kv_s), n > 0);
     __syncthreads();
     out_pass(reinterpret_cast<const float*>(kv_s), nullptr, X.fac[0], nullptr,
-             a.out + (int64_t)q * kHeads * kDLat, kDLat, 0, warp, lane, kThreads / 32);
+             a.inv_freq ? X.rope_c : nullptr, X.rope_s, a.out + (int64_t)q * kHeads * kDLat,
+             kDLat, 0, warp, lane, kThreads / 32);
     if (a.lse && tid < 64)
       a.lse[(int64_t)q * kHeads + tid] =
           (X.m_run[tid] + __log2f(X.l_run[tid])) * 0.6931471805599453f;
@@ -646,10 +671,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           a.lse[(int64_t)q * kHeads + tid] = (M + __log2f(Z)) * 0.6931471805599453f;
       }
     }
+    if (a.inv_freq && warp == 4) rope_table(a.inv_freq, p, lane, X.rope_c, X.rope_s);
     __syncthreads();
     out_pass(reinterpret_cast<const float*>(q_s), reinterpret_cast<const float*>(kv_s), X.fac[0],
-             X.fac[1], a.out + (int64_t)q * kHeads * kDLat, 256, 256 * rank, warp, lane,
-             kThreads / 32);
+             X.fac[1], a.inv_freq ? X.rope_c : nullptr, X.rope_s,
+             a.out + (int64_t)q * kHeads * kDLat, 256, 256 * rank, warp, lane, kThreads / 32);
     // both CTAs have received their rows, so no copy touches either one's shared memory
     // any more when they exit
     cluster_sync();
@@ -692,9 +718,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 __global__ void __launch_bounds__(256) attn_combine_kernel(AttnArgs a, int nsplit) {
   __shared__ float coef[kMaxChunks][8];  // [split][head within the CTA]
   __shared__ float lse2[8];
+  __shared__ float rc[32], rs[32];
   const int q = blockIdx.x, h0 = blockIdx.y * 8, tid = threadIdx.x;
   griddep_launch_dependents();
   griddep_wait();
+  if (a.inv_freq && tid >= 32 && tid < 64) rope_table(a.inv_freq, a.q_pos[q], tid - 32, rc, rs);
   if (tid < 8) {
     const int h = h0 + tid;
     const float* ml = a.part_ml + (int64_t)q * nsplit * 128;
@@ -725,6 +753,16 @@ __global__ void __launch_bounds__(256) attn_combine_kernel(AttnArgs a, int nspli
       const float4 x0 = src[0], x1 = src[1];
       acc[0] += w * x0.x; acc[1] += w * x0.y; acc[2] += w * x0.z; acc[3] += w * x0.w;
       acc[4] += w * x1.x; acc[5] += w * x1.y; acc[6] += w * x1.z; acc[7] += w * x1.w;
+    }
+    if (a.inv_freq && d >= kRopeDim0) {  // pairs (d - 448) / 2 .. +3 rotated back
+#pragma unroll
+      for (int e = 0; e < 8; e += 2) {
+        const int i = (d + e - kRopeDim0) >> 1;
+        const float o0 = acc[e] * rc[i] + acc[e + 1] * rs[i];
+        const float o1 = acc[e + 1] * rc[i] - acc[e] * rs[i];
+        acc[e] = o0;
+        acc[e + 1] = o1;
+      }
     }
     uint4* dst = reinterpret_cast<uint4*>(a.out + ((int64_t)q * kHeads + h0 + hl) * kDLat + d);
     *dst = make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]),

@@ -80,14 +80,7 @@ __global__ void __launch_bounds__(kWarps * 32) compress_kernel(CompressArgs a) {
   griddep_launch_dependents();
   griddep_wait();
   for (int i = threadIdx.x; i <= a.B; i += blockDim.x) cu_s[i] = a.cu_seqlens[i];
-  if (threadIdx.x < 32) {
-    // inv_freq[i] / (2 pi) as a 64-bit binary fraction of a turn (fractional part only):
-    // the phase of position p is then (p * turn) mod 2^64, exact in integer arithmetic.
-    double tr = (double)a.inv_freq[threadIdx.x] * 0.15915494309189535;
-    tr -= floor(tr);
-    const double sc = tr * 18446744073709551616.0;  // 2^64
-    turn_s[threadIdx.x] = sc >= 18446744073709551615.0 ? ~0ull : (uint64_t)sc;
-  }
+  if (threadIdx.x < 32) turn_s[threadIdx.x] = rope_turn(a.inv_freq[threadIdx.x]);
   const int lane = threadIdx.x & 31;
   const int64_t t = (int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5);
   // this token's own kv / score do not depend on its sequence: start them now
@@ -162,9 +155,7 @@ __global__ void __launch_bounds__(kWarps * 32) compress_kernel(CompressArgs a) {
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
         const int pair = 4 * (lane - 24) + k;
-        // phase in turns as a signed 64-bit fraction, then the angle in [-pi, pi)
-        const int64_t ph = (int64_t)(p0 * turn_s[pair]);
-        const float ang = (float)ph * 3.4061215800865545e-19f;  // 2 pi / 2^64
+        const float ang = rope_angle(turn_s[pair], p0);
         float fs, fc;
         sincosf(ang, &fs, &fc);
         const float x0 = r[1][2 * k], x1 = r[1][2 * k + 1];

@@ -235,6 +235,33 @@ csa2_status csa2_reuse_attn(const csa2_bf16* q, int Q, const int32_t* q_seq,
                             int nsel, const float* sink, float scale, csa2_bf16* out, float* lse,
                             void* ws, size_t ws_bytes, csa2_stream stream);
 
+/* ---------------------------------------------------------------------------------
+ * csa2_sparse_attn_rope, csa2_reuse_attn_rope -- the same calls with the output's
+ * inverse RoPE fused in: [A] "出来之后" (out -> inverse RoPE at the query's own
+ * position, because K = V carries the rotation); [B] §6.1 (the output's last 64 dims
+ * times the conjugate phase, apply_rotary_emb(o, freqs, inverse=True)); [C] A.12.1.
+ * After the softmax-weighted sum, pair i of dims 448 + 2i, 449 + 2i of every head,
+ * read as a complex number, is multiplied by e^{-i p theta_i}, p = q_pos[q],
+ * theta_i = inv_freq[i] (the same 32-entry table as csa2_compress); the other 448 dims
+ * are unchanged.  Arguments as csa2_sparse_attn / csa2_reuse_attn, plus
+ *   inv_freq  [32] fp32 device, required (NULL is CSA2_EINVAL).
+ * The rotation angle is computed from an exact 64-bit phase of p, so it holds for any
+ * position the int64 q_pos can hold. */
+csa2_status csa2_sparse_attn_rope(const csa2_bf16* q, int Q, const int32_t* q_seq,
+                                  const int64_t* q_pos, const csa2_swa* swa,
+                                  const csa2_bf16* plane, int64_t plane_rows,
+                                  const int64_t* row_base, const int32_t* sel, int nsel,
+                                  const float* sink, float scale, csa2_bf16* out, float* lse,
+                                  void* ws, size_t ws_bytes, const float* inv_freq,
+                                  csa2_stream stream);
+csa2_status csa2_reuse_attn_rope(const csa2_bf16* q, int Q, const int32_t* q_seq,
+                                 const int64_t* q_pos, const csa2_swa* swa,
+                                 const csa2_bf16* plane, int64_t plane_rows,
+                                 const int64_t* row_base, const int32_t* sel, int nsel,
+                                 const float* sink, float scale, csa2_bf16* out, float* lse,
+                                 void* ws, size_t ws_bytes, const float* inv_freq,
+                                 csa2_stream stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -111,7 +111,7 @@ def window_rows(wl, q, layer):
     return dict(swa=lin, swa_mode="linear", lin_base=[0], lin_pos0=[lo])
 
 
-def oracle_attn(wl, key, q, sel, layer=0, head_scale=None):
+def oracle_attn(wl, key, q, sel, layer=0, head_scale=None, inv_freq=None):
     """Oracle output and lse of query q over its window and `sel`.  `head_scale`
     (optional, 64 powers of two) multiplies the query of each head, exactly in bf16."""
     b = int(wl.q_seq[q])
@@ -130,7 +130,7 @@ def oracle_attn(wl, key, q, sel, layer=0, head_scale=None):
     out, lse = sparse_attn(qh, [0], [int(wl.q_pos[q])], win["swa"],
                                   bf16_from_bits(plane), [0], sel_c.reshape(1, -1), sink,
                                   swa_mode=win["swa_mode"], lin_base=win["lin_base"],
-                                  lin_pos0=win["lin_pos0"])
+                                  lin_pos0=win["lin_pos0"], inv_freq=inv_freq)
     return out[0], lse[0]
 
 

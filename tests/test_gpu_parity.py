@@ -287,6 +287,52 @@ def test_attention_split_and_unsplit_agree_with_the_oracle():
             assert np.abs(lse[q].cpu().numpy() - ref_lse).max() < 1e-2
 
 
+@pytest.mark.parametrize("use_ws", [False, True])
+def test_attention_with_the_inverse_rope_epilogue(use_ws):
+    """csa2_sparse_attn_rope: the output's dims 448..511 rotated back by the query position
+    ([A] "出来之后"), through the two-CTA cluster merge (no workspace) and through the
+    global combine (workspace: ten CTAs per query).  The other dims are the plain call's."""
+    from csa2_compressed_sparse_gb300 import (csa2_attn_workspace_size, csa2_device_status,
+                                              csa2_sparse_attn, csa2_sparse_attn_rope)
+    from csa2_compressed_sparse_gb300.step import swa_of
+    wl = W.decode_batch(B=9, lo=300, hi=700000, seed=31)
+    t, spec, buf = run_workload(wl)
+    key = register(wl)
+    ws = None
+    if use_ws:
+        ws = torch.empty(csa2_attn_workspace_size(wl.Q, spec.k), dtype=torch.uint8, device="cuda")
+    args = (t["q"][0], t["q_seq"], t["q_pos"], swa_of(spec, t, 0), t["plane"], t["row_base"],
+            buf.sel, t["sink"])
+    plain = torch.empty_like(buf.out[0])
+    rot = torch.empty_like(buf.out[0])
+    csa2_sparse_attn(*args, plain, ws=ws)
+    csa2_sparse_attn_rope(*args, rot, t["inv_freq"], ws=ws)
+    csa2_device_status()
+    assert torch.equal(plain[:, :, :448], rot[:, :, :448])
+    invf = t["inv_freq"].cpu().numpy()
+    for q in range(wl.Q):
+        ref, _ = oracle_attn(wl, key, q, buf.sel[q].cpu().numpy(), inv_freq=invf)
+        check_attn(rot[q].float().cpu().numpy(), ref)
+
+
+def test_reuse_attention_with_the_inverse_rope_epilogue_one_cta_per_query():
+    """csa2_reuse_attn_rope on a prefill chunk (128 queries: one CTA each), LINEAR window."""
+    from csa2_compressed_sparse_gb300 import csa2_device_status, csa2_reuse_attn_rope
+    from csa2_compressed_sparse_gb300.step import swa_of
+    wl = SMALL["prefill_small"]()
+    t, spec, buf = run_workload(wl)
+    key = register(wl)
+    layer = 2
+    rot = torch.empty_like(buf.out[layer])
+    csa2_reuse_attn_rope(t["q"][layer], t["q_seq"], t["q_pos"], swa_of(spec, t, layer), t["plane"],
+                         t["row_base"], buf.sel, t["sink"], rot, t["inv_freq"])
+    csa2_device_status()
+    invf = t["inv_freq"].cpu().numpy()
+    for q in (0, 1, 63, 127):
+        ref, _ = oracle_attn(wl, key, q, buf.sel[q].cpu().numpy(), layer, inv_freq=invf)
+        check_attn(rot[q].float().cpu().numpy(), ref)
+
+
 def test_attention_running_max_rescale_paths():
     """Queries of heads 0..31 scaled by 2^8 (exact in bf16): their scores spread over
     hundreds of nats, so later chunks overtake the running max by far more than the
