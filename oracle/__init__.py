@@ -44,6 +44,8 @@ def lib():
         L.orc_sparse_attn.restype = None
         L.orc_inverse_rope.argtypes = [_vp, _i32, _vp, _vp]
         L.orc_inverse_rope.restype = None
+        L.orc_candidate_pool.argtypes = [_vp, _vp, _i64, _i32, _vp]
+        L.orc_candidate_pool.restype = _i32
         _LIB = L
     return _LIB
 
@@ -176,4 +178,15 @@ def inverse_rope(out, q_pos, inv_freq):
     qp = np.ascontiguousarray(q_pos, dtype=np.int64)
     f = np.ascontiguousarray(inv_freq, dtype=np.float32)
     lib().orc_inverse_rope(_p(out), out.shape[0], _p(qp), _p(f))
+    return out
+
+
+def candidate_pool(scores, rows, nbk=2048):
+    """One query's FULL logits (float64 [ld]) and row ids ([ld], -1 = not scored) ->
+    candidate block ids [nbk] int32: block maxima, newest block pinned, top nbk blocks,
+    ascending, -1 padded."""
+    sc = np.ascontiguousarray(scores, dtype=np.float64)
+    rw = np.ascontiguousarray(rows, dtype=np.int64)
+    out = np.empty(nbk, dtype=np.int32)
+    lib().orc_candidate_pool(_p(sc), _p(rw), len(sc), nbk, _p(out))
     return out

@@ -13,6 +13,7 @@
  *   [C] "万字长文解析DeekSeekV4.1flash" (yuyanqi.com)
  *   [E] "DeepSeek-V4-Pro 架构解剖" (perryzhang01.github.io, v4_pro_anatomy)
  */
+#include <float.h>
 #include <math.h>
 #include <stdint.h>
 #include <stdlib.h>
@@ -330,4 +331,39 @@ void orc_inverse_rope(double* out, int Q, const int64_t* q_pos, const float* inv
       }
     }
   }
+}
+
+/* ---- candidate pool of the FULL layer [A] Fig. 3b (second stage: block maxima, newest
+ *      block pinned to +inf, top-2048 blocks, ascending, -1 padded); [B] §5.2 (block
+ *      score = the block's largest indexer score, the partial newest block is kept);
+ *      [C] A.11 (2048 blocks of 8 positions) ----------------------------------------
+ *
+ * scores [ld] are one query's FULL logits, rows [ld] their row ids (-1 = not scored;
+ * the scored rows are 0 .. n_vis - 1).  Block b holds rows 8b .. 8b + 7; its score is
+ * the largest score of its scored rows, NaN counting as -inf and +inf clamped to the
+ * largest finite value.  The newest block (the one holding row n_vis - 1) gets +inf.
+ * Then the top nbk blocks by (score desc, block id asc), written ascending to cand
+ * [nbk], -1 padded.  Returns the number of blocks selected. */
+int orc_candidate_pool(const double* scores, const int64_t* rows, int64_t ld, int nbk,
+                       int32_t* cand) {
+  int64_t nvis = 0;
+  for (int64_t i = 0; i < ld; i++)
+    if (rows[i] >= 0 && rows[i] + 1 > nvis) nvis = rows[i] + 1;
+  const int64_t nb = (nvis + 7) / 8;
+  double* bs = (double*)malloc(sizeof(double) * (nb > 0 ? nb : 1));
+  int64_t* ids = (int64_t*)malloc(sizeof(int64_t) * (nb > 0 ? nb : 1));
+  for (int64_t b = 0; b < nb; b++) { bs[b] = -INFINITY; ids[b] = b; }
+  for (int64_t i = 0; i < ld; i++) {
+    if (rows[i] < 0) continue;
+    double s = scores[i];
+    if (isnan(s)) s = -INFINITY;
+    if (s == INFINITY) s = DBL_MAX;
+    const int64_t b = rows[i] / 8;
+    if (s > bs[b]) bs[b] = s;
+  }
+  if (nb > 0) bs[nb - 1] = INFINITY;
+  const int keff = orc_topk(bs, ids, nb, nbk, cand);
+  free(bs);
+  free(ids);
+  return keff;
 }

@@ -506,3 +506,59 @@ def test_synth_e4m3_encode_matches_torch():
     assert torch.equal(codes, ref)
     sc = r[:, 512:].contiguous().view(torch.float32)
     assert float(sc.min()) >= 0.75 / 64 and float(sc.max()) < 1.25 / 64
+
+
+# ---- candidate pool (second stage of the FULL layer) ---------------------------------------
+
+def _pool_brute(scores, nvis, nbk):
+    """Every block's score by a scan, then all blocks ranked by sorting tuples."""
+    nb = (nvis + 7) // 8
+    best = []
+    for b in range(nb):
+        m = -math.inf
+        for r in range(8 * b, min(8 * b + 8, nvis)):
+            v = scores[r]
+            v = -math.inf if math.isnan(v) else (np.finfo(np.float64).max if v == math.inf else v)
+            m = max(m, v)
+        best.append(math.inf if b == nb - 1 else m)
+    order = sorted(range(nb), key=lambda b: (-best[b], b))[:nbk]
+    return sorted(order) + [-1] * (nbk - min(nbk, nb))
+
+
+def test_candidate_pool_brute_force_with_partial_block_ties_nan_and_inf():
+    g = np.random.default_rng(7)
+    for trial in range(60):
+        nvis = int(g.integers(1, 90))
+        nbk = int(g.integers(1, 14))
+        sc = g.integers(-3, 4, nvis).astype(np.float64)  # heavy ties
+        sc[g.random(nvis) < 0.1] = np.nan
+        sc[g.random(nvis) < 0.05] = np.inf
+        sc[g.random(nvis) < 0.05] = -np.inf
+        ld = nvis + int(g.integers(0, 9))  # unscored tail
+        scores = np.zeros(ld)
+        scores[:nvis] = sc
+        rows = np.full(ld, -1, dtype=np.int64)
+        rows[:nvis] = np.arange(nvis)
+        got = oracle.candidate_pool(scores, rows, nbk)
+        assert list(got) == _pool_brute(list(sc), nvis, nbk), trial
+
+
+def test_candidate_pool_keeps_the_newest_block_and_covers_the_row_top_k():
+    g = np.random.default_rng(8)
+    nvis, k, nbk = 3001, 64, 72  # the newest block holds 1 row
+    sc = g.standard_normal(nvis)
+    sc[-1] = -np.inf  # the newest row scores lowest: its block is kept all the same
+    rows = np.arange(nvis, dtype=np.int64)
+    pool = oracle.candidate_pool(sc, rows, nbk)
+    assert (nvis - 1) // 8 in pool
+    # every row of the FULL layer's own top-k lies in a selected block
+    top = oracle.topk(sc, rows, k)
+    assert set(int(r) // 8 for r in top if r >= 0) <= set(int(b) for b in pool if b >= 0)
+    # the order of rows inside a block does not matter
+    perm = np.arange(nvis)
+    for b in range(0, nvis // 8):
+        perm[8 * b:8 * b + 8] = g.permutation(perm[8 * b:8 * b + 8])
+    assert np.array_equal(oracle.candidate_pool(sc[perm], rows, nbk), pool)
+    # fewer blocks than places: every block, then -1
+    small = oracle.candidate_pool(sc[:40], rows[:40], nbk)
+    assert list(small[:5]) == [0, 1, 2, 3, 4] and (small[5:] == -1).all()
