@@ -49,7 +49,6 @@ struct SelectSmem {
   uint32_t cidx[kCandCap];
   uint32_t selmap[kWords];  // positions with key > T
   uint32_t eqmap[kWords];   // positions with key == T
-  int out[kMaxK];
   int wcnt[kTopkThreads / 32];  // kept pairs per warp region
   int ncand;
   int nvalid;
@@ -156,10 +155,11 @@ struct RowSrc {
   }
 };
 
-// Exact top-k of src[0..n) (n <= kChunkLen): selected indices, ascending, in S.out.
-// Returns keff = min(k, #scored).
-template <int kKind>
-__device__ int select_topk(const RowSrc<kKind>& src, int n, int k, SelectSmem& S) {
+// Exact top-k of src[0..n) (n <= kChunkLen): emit(o, i) is called once for each selected
+// index i, with o = its place in ascending order (0 .. keff - 1), by some thread of the
+// CTA.  Returns keff = min(k, #scored).
+template <int kKind, typename Emit>
+__device__ int select_topk(const RowSrc<kKind>& src, int n, int k, SelectSmem& S, Emit emit) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int nw = (n + 31) >> 5;
   // ---- 1. clear ----
@@ -321,7 +321,7 @@ __device__ int select_topk(const RowSrc<kKind>& src, int n, int k, SelectSmem& S
     }
     while (bits) {
       const int b = __ffs(bits) - 1;
-      S.out[o++] = w * 32 + b;
+      emit(o++, w * 32 + b);
       bits &= bits - 1u;
     }
   }
@@ -335,25 +335,16 @@ __device__ __forceinline__ int32_t pos_to_row(const TopkArgs& a, int q, uint32_t
   return blk * 8 + (int32_t)(pos & 7u);
 }
 
-// Final write of one row: positions pos_of(i) for i < keff, then -1.
-template <typename PosFn, typename KeyFn>
-__device__ void write_row(const TopkArgs& a, int q, int keff, const int* idx, PosFn pos_of,
-                          KeyFn key_of) {
-  for (int i = threadIdx.x; i < a.k; i += kTopkThreads) {
-    int32_t r = -1;
-    float s = 0.f;
-    if (i < keff) {
-      uint32_t p = pos_of(idx[i]);
-      r = pos_to_row(a, q, p);
-      s = key_score(key_of(idx[i]));
-    }
-    a.sel[(int64_t)q * a.k + i] = r;
-    if (a.sel_scores) a.sel_scores[(int64_t)q * a.k + i] = s;
+// Entries keff .. k - 1 of row q: -1 (score 0).
+__device__ void pad_row(const TopkArgs& a, int q, int keff) {
+  for (int i = keff + (int)threadIdx.x; i < a.k; i += kTopkThreads) {
+    a.sel[(int64_t)q * a.k + i] = -1;
+    if (a.sel_scores) a.sel_scores[(int64_t)q * a.k + i] = 0.f;
   }
 }
 
 template <int kKind>
-__global__ void __launch_bounds__(kTopkThreads) topk_kernel(TopkArgs a) {
+__global__ void __launch_bounds__(kTopkThreads, 1) topk_kernel(TopkArgs a) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
   SelectSmem& S = *reinterpret_cast<SelectSmem*>(smem_raw);
   const int q = blockIdx.y, c = blockIdx.x;
@@ -393,19 +384,22 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(TopkArgs a) {
   }
   __syncthreads();
   RowSrc<kSrcSmem> src{rowbuf, pad == 0};
-  int keff = select_topk(src, len, a.k, S);
+  int32_t* sel_q = a.sel + (int64_t)q * a.k;
+  float* sc_q = a.sel_scores ? a.sel_scores + (int64_t)q * a.k : nullptr;
   if (a.nchunk == 1) {
-    write_row(a, q, keff, S.out, [&](int i) { return (uint32_t)(begin + i); },
-              [&](int i) { return src(i); });
+    const int keff = select_topk(src, len, a.k, S, [&](int o, int i) {
+      sel_q[o] = pos_to_row(a, q, (uint32_t)(begin + i));
+      if (sc_q) sc_q[o] = key_score(src(i));
+    });
+    pad_row(a, q, keff);
     return;
   }
   // partial list of this chunk, then the last chunk CTA of the row merges
   uint64_t* part = a.part + ((int64_t)q * a.nchunk + c) * a.k;
-  for (int i = threadIdx.x; i < a.k; i += kTopkThreads) {
-    uint64_t v = 0;
-    if (i < keff) v = ((uint64_t)src(S.out[i]) << 32) | (uint32_t)(begin + S.out[i]);
-    part[i] = v;
-  }
+  const int keff = select_topk(src, len, a.k, S, [&](int o, int i) {
+    part[o] = ((uint64_t)src(i) << 32) | (uint32_t)(begin + i);
+  });
+  for (int i = keff + (int)threadIdx.x; i < a.k; i += kTopkThreads) part[i] = 0;
   __threadfence();
   __syncthreads();
   if (threadIdx.x == 0) S.last = atomicAdd(&a.count[q], 1) == a.nchunk - 1;
@@ -417,9 +411,11 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(TopkArgs a) {
   const int ncand = a.nchunk * a.k;
   const uint64_t* row = a.part + (int64_t)q * ncand;
   RowSrc<kSrcPairs> msrc{row, (reinterpret_cast<uintptr_t>(row) & 15u) == 0};
-  keff = select_topk(msrc, ncand, a.k, S);
-  write_row(a, q, keff, S.out, [&](int i) { return (uint32_t)(__ldcg(row + i) & 0xFFFFFFFFu); },
-            [&](int i) { return msrc(i); });
+  const int keff2 = select_topk(msrc, ncand, a.k, S, [&](int o, int i) {
+    sel_q[o] = pos_to_row(a, q, (uint32_t)(__ldcg(row + i) & 0xFFFFFFFFu));
+    if (sc_q) sc_q[o] = key_score(msrc(i));
+  });
+  pad_row(a, q, keff2);
   if (threadIdx.x == 0) a.count[q] = 0;  // ready for the next call
 }
 
