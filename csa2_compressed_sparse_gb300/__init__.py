@@ -18,7 +18,7 @@ from . import build as _build
 __all__ = [
     "Csa2Error", "Swa", "lib", "csa2_version", "csa2_device_status", "csa2_compress",
     "csa2_index_topk_workspace_size", "csa2_index_topk", "csa2_index_topk_noalloc",
-    "csa2_topk_workspace_size",
+    "csa2_index_topk_pool_workspace_size", "csa2_index_topk_pool", "csa2_topk_workspace_size",
     "csa2_topk_scores", "csa2_attn_workspace_size", "csa2_sparse_attn", "csa2_reuse_attn",
     "csa2_sparse_attn_rope", "csa2_reuse_attn_rope",
 ]
@@ -54,6 +54,9 @@ _SIGS = {
                          _i32, _i64, _vp, _vp, _vp, _vp, _sz, _vp], _i32),
     "csa2_index_topk_noalloc": ([_vp, _vp, _i32, _i32, _vp, _i64, _vp, _vp, _vp, _i32, _vp,
                                  _i32, _i32, _i32, _i64, _vp, _vp, _vp, _vp], _i32),
+    "csa2_index_topk_pool_workspace_size": ([_i32, _i32, _i64, _i32, _i32], _sz),
+    "csa2_index_topk_pool": ([_vp, _vp, _i32, _i32, _vp, _i64, _vp, _vp, _vp, _i32, _i32, _i32,
+                              _i64, _vp, _vp, _vp, _i32, _vp, _vp, _sz, _vp], _i32),
     "csa2_topk_workspace_size": ([_i32, _i64, _i32], _sz),
     "csa2_topk_scores": ([_vp, _vp, _i32, _i64, _i32, _vp, _vp, _vp, _sz, _vp], _i32),
     "csa2_attn_workspace_size": ([_i32, _i32], _sz),
@@ -163,6 +166,21 @@ def csa2_index_topk_noalloc(iq, w, index_k, row_base, q_seq, q_pos, ratio, k, ma
                                          _p(row_base), _p(q_seq), _p(q_pos), ratio, _p(cand),
                                          ncb, k, 1 if relu else 0, max_scored, _p(sel),
                                          _p(sel_scores), _p(scores_out), _stream(stream)))
+
+
+def csa2_index_topk_pool_workspace_size(Q, H, max_scored, k, nbk):
+    return int(lib().csa2_index_topk_pool_workspace_size(Q, H, max_scored, k, nbk))
+
+
+def csa2_index_topk_pool(iq, w, index_k, row_base, q_seq, q_pos, ratio, k, max_scored, sel,
+                         pool, ws, sel_scores=None, relu=True, scores_out=None, stream=None):
+    """FULL-mode csa2_index_topk plus the candidate pool [Q][nbk] (nbk = pool.shape[1])."""
+    Q, H = iq.shape[0], iq.shape[1]
+    _check(lib().csa2_index_topk_pool(_p(iq), _p(w), Q, H, _p(index_k), index_k.shape[0],
+                                      _p(row_base), _p(q_seq), _p(q_pos), ratio, k,
+                                      1 if relu else 0, max_scored, _p(sel), _p(sel_scores),
+                                      _p(scores_out), pool.shape[1], _p(pool), _p(ws),
+                                      ws.numel() * ws.element_size(), _stream(stream)))
 
 
 def csa2_topk_workspace_size(Q, ld, k):

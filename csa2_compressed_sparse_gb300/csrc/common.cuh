@@ -60,6 +60,11 @@ struct IndexArgs {
   int32_t* n_groups;    // [1]
   int32_t* topk_count;  // [Q]  zeroed by the prep kernel for the top-k merge
   int group_max;        // queries per group (FULL: 256 / H; REINDEX: 1)
+  // candidate pool (FULL only; bkeys == null: none)
+  uint32_t* bkeys;      // [Q][ldb] block keys: max over the block's 8 keys, newest = ~0
+  int64_t ldb;          // row stride of bkeys (blocks per row rounded up to 4)
+  int32_t* nblk;        // [Q]  blocks per row = ceil(n_scored / 8)
+  int32_t* pool_count;  // [Q]  zeroed by the prep kernel for the pool's top-k merge
 };
 
 struct TopkArgs {
@@ -118,6 +123,9 @@ cudaError_t launch_attn(const AttnArgs& a, int nsplit, cudaStream_t s);
 int topk_chunk_len(int64_t ld);
 int topk_num_chunks(int64_t ld);
 int64_t topk_max_len();
+// Can one call select the top-k of rows of ld positions?  (the chunk merge holds
+// chunks * k pairs)
+bool topk_fits(int64_t ld, int k);
 
 // Replace the calling thread's csa2_last_error() text.
 void set_last_error(const char* msg);

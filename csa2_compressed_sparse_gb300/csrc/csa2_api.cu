@@ -48,9 +48,16 @@ size_t up256(size_t x) { return (x + 255) & ~size_t(255); }
 struct IndexWs {
   size_t keys, n_scored, grp_q0, grp_nq, grp_tile0, n_groups, count, part, total;
   int nchunk;
+  // candidate pool (nbk > 0): block keys, blocks per row, merge counters, partial lists
+  size_t bkeys, nblk, pcount, ppart;
+  int64_t nb_max, ldb;
+  int pnchunk;
 };
 
-IndexWs index_ws_layout(int Q, int64_t ld, int k) {
+// Blocks of 8 positions in a row of ld positions.
+int64_t pool_blocks(int64_t ld) { return (ld + 7) / 8; }
+
+IndexWs index_ws_layout(int Q, int64_t ld, int k, int nbk = 0) {
   IndexWs w{};
   size_t o = 0;
   w.keys = o; o = up256(o + (size_t)Q * (size_t)((ld + 3) & ~int64_t(3)) * 4);
@@ -63,6 +70,16 @@ IndexWs index_ws_layout(int Q, int64_t ld, int k) {
   w.nchunk = csa2::topk_num_chunks(ld);
   w.part = o;
   if (w.nchunk > 1) o = up256(o + (size_t)Q * w.nchunk * k * 8);
+  if (nbk > 0) {
+    w.nb_max = pool_blocks(ld);
+    w.ldb = (w.nb_max + 3) & ~int64_t(3);
+    w.pnchunk = csa2::topk_num_chunks(w.nb_max);
+    w.bkeys = o; o = up256(o + (size_t)Q * (size_t)w.ldb * 4);
+    w.nblk = o; o = up256(o + (size_t)Q * 4);
+    w.pcount = o; o = up256(o + (size_t)Q * 4);
+    w.ppart = o;
+    if (w.pnchunk > 1) o = up256(o + (size_t)Q * w.pnchunk * nbk * 8);
+  }
   w.total = o;
   return w;
 }
@@ -183,12 +200,15 @@ size_t csa2_index_topk_workspace_size(int Q, int H, int64_t max_scored, int k) {
   return index_ws_layout(Q, max_scored, k).total;
 }
 
-csa2_status csa2_index_topk(const csa2_bf16* iq, const float* w, int Q, int H,
+namespace {
+
+csa2_status index_topk_impl(const csa2_bf16* iq, const float* w, int Q, int H,
                             const csa2_bf16* index_k, int64_t index_rows,
                             const int64_t* row_base, const int32_t* q_seq, const int64_t* q_pos,
                             int ratio, const int32_t* cand, int ncb, int k, int relu,
                             int64_t max_scored, int32_t* sel, float* sel_scores,
-                            float* scores_out, void* ws, size_t ws_bytes, csa2_stream stream) {
+                            float* scores_out, int nbk, int32_t* pool, void* ws, size_t ws_bytes,
+                            csa2_stream stream) {
   REQUIRE(Q >= 0, "csa2_index_topk: Q must be >= 0 (got %d)", Q);
   REQUIRE(H == 32 || H == 64, "csa2_index_topk: H must be 32 or 64 (got %d)", H);
   REQUIRE(ratio == 1 || ratio == 2, "csa2_index_topk: ratio must be 1 or 2 (got %d)", ratio);
@@ -210,7 +230,7 @@ csa2_status csa2_index_topk(const csa2_bf16* iq, const float* w, int Q, int H,
   REQUIRE(index_rows >= 1 && index_rows < (int64_t)1 << 31, "csa2_index_topk: index_rows out of range");
   REQUIRE((int64_t)Q * H < (int64_t)1 << 31, "csa2_index_topk: Q * H out of range");
   REQUIRE((reinterpret_cast<uintptr_t>(ws) & 255u) == 0, "csa2_index_topk: ws must be 256-byte aligned");
-  const IndexWs L = index_ws_layout(Q, max_scored, k);
+  const IndexWs L = index_ws_layout(Q, max_scored, k, nbk);
   if (ws_bytes < L.total)
     return fail(CSA2_ENOSPACE, "csa2_index_topk: workspace %zu bytes < required %zu", ws_bytes, L.total);
   uint8_t* base = static_cast<uint8_t*>(ws);
@@ -227,6 +247,12 @@ csa2_status csa2_index_topk(const csa2_bf16* iq, const float* w, int Q, int H,
   a.n_groups = reinterpret_cast<int32_t*>(base + L.n_groups);
   a.topk_count = reinterpret_cast<int32_t*>(base + L.count);
   a.group_max = cand ? 1 : 256 / H;
+  if (nbk > 0) {
+    a.bkeys = reinterpret_cast<uint32_t*>(base + L.bkeys);
+    a.ldb = L.ldb;
+    a.nblk = reinterpret_cast<int32_t*>(base + L.nblk);
+    a.pool_count = reinterpret_cast<int32_t*>(base + L.pcount);
+  }
   const int sms = num_sms();
   if (sms <= 0) return fail(CSA2_ECUDA, "csa2_index_topk: no CUDA device");
   cudaError_t e = csa2::launch_index(a, sms, stream);
@@ -240,11 +266,56 @@ csa2_status csa2_index_topk(const csa2_bf16* iq, const float* w, int Q, int H,
   // n_scored <= max_scored <= ldk: the chunking of max_scored covers every row
   e = csa2::launch_topk(t, stream);
   if (e != cudaSuccess) return cuda_fail(e, "csa2_index_topk (top-k)");
+  if (nbk > 0) {
+    csa2::TopkArgs p{};
+    p.keys = a.bkeys; p.n = a.nblk; p.Q = Q; p.ld = L.ldb; p.k = nbk;
+    p.sel = pool; p.part = reinterpret_cast<uint64_t*>(base + L.ppart); p.nchunk = L.pnchunk;
+    p.count = a.pool_count;
+    p.chunk = csa2::topk_chunk_len(L.nb_max);
+    e = csa2::launch_topk(p, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "csa2_index_topk_pool (block top-k)");
+  }
   return CSA2_OK;
 }
 
+}  // namespace
+
+csa2_status csa2_index_topk(const csa2_bf16* iq, const float* w, int Q, int H,
+                            const csa2_bf16* index_k, int64_t index_rows,
+                            const int64_t* row_base, const int32_t* q_seq, const int64_t* q_pos,
+                            int ratio, const int32_t* cand, int ncb, int k, int relu,
+                            int64_t max_scored, int32_t* sel, float* sel_scores,
+                            float* scores_out, void* ws, size_t ws_bytes, csa2_stream stream) {
+  return index_topk_impl(iq, w, Q, H, index_k, index_rows, row_base, q_seq, q_pos, ratio, cand,
+                         ncb, k, relu, max_scored, sel, sel_scores, scores_out, 0, nullptr, ws,
+                         ws_bytes, stream);
+}
+
+size_t csa2_index_topk_pool_workspace_size(int Q, int H, int64_t max_scored, int k, int nbk) {
+  (void)H;
+  if (Q < 0 || max_scored < 1 || k < 1 || k > 512 || nbk < 1 || nbk > 2048) return 0;
+  return index_ws_layout(Q, max_scored, k, nbk).total;
+}
+
+csa2_status csa2_index_topk_pool(const csa2_bf16* iq, const float* w, int Q, int H,
+                                 const csa2_bf16* index_k, int64_t index_rows,
+                                 const int64_t* row_base, const int32_t* q_seq,
+                                 const int64_t* q_pos, int ratio, int k, int relu,
+                                 int64_t max_scored, int32_t* sel, float* sel_scores,
+                                 float* scores_out, int nbk, int32_t* pool, void* ws,
+                                 size_t ws_bytes, csa2_stream stream) {
+  REQUIRE(nbk >= 1 && nbk <= 2048, "csa2_index_topk_pool: nbk must be in [1, 2048] (got %d)", nbk);
+  REQUIRE(max_scored >= 1 && csa2::topk_fits(pool_blocks(max_scored), nbk),
+          "csa2_index_topk_pool: %lld blocks per row with nbk = %d exceed the block selection",
+          (long long)pool_blocks(max_scored), nbk);
+  REQUIRE(Q == 0 || pool, "csa2_index_topk_pool: pool is required");
+  return index_topk_impl(iq, w, Q, H, index_k, index_rows, row_base, q_seq, q_pos, ratio,
+                         nullptr, 0, k, relu, max_scored, sel, sel_scores, scores_out, nbk, pool,
+                         ws, ws_bytes, stream);
+}
+
 size_t csa2_topk_workspace_size(int Q, int64_t ld, int k) {
-  if (Q < 0 || ld < 1 || k < 1 || k > 512) return 0;
+  if (Q < 0 || ld < 1 || k < 1 || k > 2048 || !csa2::topk_fits(ld, k)) return 0;
   return topk_ws_bytes(Q, ld, k);
 }
 
@@ -252,11 +323,14 @@ csa2_status csa2_topk_scores(const float* scores, const int32_t* n, int Q, int64
                              int32_t* sel, float* sel_scores, void* ws, size_t ws_bytes,
                              csa2_stream stream) {
   REQUIRE(Q >= 0, "csa2_topk_scores: Q must be >= 0");
-  REQUIRE(k >= 1 && k <= 512, "csa2_topk_scores: k must be in [1, 512] (got %d)", k);
+  REQUIRE(k >= 1 && k <= 2048, "csa2_topk_scores: k must be in [1, 2048] (got %d)", k);
   REQUIRE(ld >= 1, "csa2_topk_scores: ld must be >= 1");
   REQUIRE(ld <= csa2::topk_max_len(),
           "csa2_topk_scores: ld %lld exceeds the supported %lld positions", (long long)ld,
           (long long)csa2::topk_max_len());
+  REQUIRE(csa2::topk_fits(ld, k),
+          "csa2_topk_scores: rows of %lld positions with k = %d exceed the chunk merge "
+          "(chunks of 32768 positions x k must be <= 32768)", (long long)ld, k);
   if (Q == 0) return CSA2_OK;
   REQUIRE(scores && n && sel, "csa2_topk_scores: scores, n and sel are required");
   const size_t need = topk_ws_bytes(Q, ld, k);

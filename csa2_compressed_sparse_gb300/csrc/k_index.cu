@@ -117,6 +117,10 @@ __global__ void __launch_bounds__(kPrepThreads) index_prep_kernel(IndexArgs a) {
         if (i < kPrepThreads) {
           a.n_scored[q] = (int32_t)ns;
           a.topk_count[q] = 0;
+          if (a.bkeys) {
+            a.nblk[q] = (int32_t)((ns + 7) >> 3);
+            a.pool_count[q] = 0;
+          }
         }
       }
     }
@@ -202,11 +206,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                                              ~uintptr_t(1023));
   uint8_t* a_smem = smem;                              // kStages x 32 KiB
   uint8_t* b_smem = smem + kStages * kStageBytes;      // 64 KiB
-  float* w_all = reinterpret_cast<float*>(b_smem + kBBytes);  // [2][256], per epilogue group
-  Bars* bars = reinterpret_cast<Bars*>(w_all + 512);
+  float* w_all = reinterpret_cast<float*>(b_smem + kBBytes);  // [8][256], per epilogue warp
+  Bars* bars = reinterpret_cast<Bars*>(w_all + 8 * 256);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  int64_t* gq_all = reinterpret_cast<int64_t*>(tmem_slot + 4);  // [2][kMaxGroup] row limit
+  int64_t* gq_all = reinterpret_cast<int64_t*>(tmem_slot + 4);  // [8][kMaxGroup] row limit
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   griddep_launch_dependents();
@@ -367,30 +371,31 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     // ============ epilogue: warps 2..5 (tiles k even), warps 6..9 (k odd) ============
     const int eg = (warp - 2) >> 2;       // epilogue group = TMEM accumulator it reads
-    const int et = threadIdx.x - 64 - 128 * eg;  // thread index within the group
     const int sub = warp & 3;             // TMEM sub-partition of this warp
     const int r = sub * 32 + lane;        // tile row = TMEM lane
-    float* w_s = w_all + 256 * eg;
-    int64_t* gq = gq_all + kMaxGroup * eg;
+    // every warp keeps its own copy of the group's weights and row limits, so a new
+    // group needs no barrier across warps (an abort cannot strand one at a barrier)
+    float* w_s = w_all + 256 * (warp - 2);
+    int64_t* gq = gq_all + kMaxGroup * (warp - 2);
     GroupInfo gi;
     int g = g_first - 1;
     gi.tile1 = -1;
     int loaded = -1;  // query group whose weights sit in w_s
     for (int64_t it = it_lo + eg; it < it_hi; it += 2) {
-      if (*abort_flag) break;
+      // warp-uniform exits: the loop body holds warp-collective TMEM loads and shuffles
+      if (__any_sync(0xFFFFFFFFu, *abort_flag != 0)) break;
       while (it >= gi.tile1) {
         ++g;
         load_group(a, g, gi);
       }
       if (g != loaded) {
-        if (eg == 0) asm volatile("bar.sync 1, 128;" ::: "memory");
-        else asm volatile("bar.sync 2, 128;" ::: "memory");
+        __syncwarp();
         const int nw = gi.nq * a.H;
-        for (int i = et; i < nw; i += 128) w_s[i] = a.w[(int64_t)gi.q0 * a.H + i] * alpha;
-        if (et < gi.nq)
-          gq[et] = a.cand ? n_visible(a.q_pos[gi.q0 + et], a.ratio) : (int64_t)a.n_scored[gi.q0 + et];
-        if (eg == 0) asm volatile("bar.sync 1, 128;" ::: "memory");
-        else asm volatile("bar.sync 2, 128;" ::: "memory");
+        for (int i = lane; i < nw; i += 32) w_s[i] = a.w[(int64_t)gi.q0 * a.H + i] * alpha;
+        if (lane < gi.nq)
+          gq[lane] = a.cand ? n_visible(a.q_pos[gi.q0 + lane], a.ratio)
+                            : (int64_t)a.n_scored[gi.q0 + lane];
+        __syncwarp();
         loaded = g;
       }
       const int64_t k = it - it_lo;
@@ -400,7 +405,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       // REINDEX groups hold one query: fetch its candidate block id before the wait
       const int32_t cblk = a.cand && (pos >> 3) < a.ncb
                                ? __ldg(a.cand + (int64_t)gi.q0 * a.ncb + (pos >> 3)) : -1;
-      if (!mbar_wait(smem_u32(&bars->acc_full[eg]), use & 1)) { *abort_flag = 1; break; }
+      if (!__all_sync(0xFFFFFFFFu, mbar_wait(smem_u32(&bars->acc_full[eg]), use & 1))) {
+        *abort_flag = 1;
+        break;
+      }
       tc_fence_after();
       const uint32_t tbase = tmem + ((uint32_t)(sub * 32) << 16) + (uint32_t)(eg * 256);
       for (int i = 0; i < gi.nq; ++i) {
@@ -451,9 +459,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         } else {
           valid = cblk >= 0 && (int64_t)cblk * 8 + (pos & 7) < gq[i];
         }
+        const uint32_t key = valid ? score_key(score) : 0u;
         if (pos < a.ld) {
-          a.keys[(int64_t)q * a.ldk + pos] = valid ? score_key(score) : 0u;
+          a.keys[(int64_t)q * a.ldk + pos] = key;
           if (valid && a.scores_out) a.scores_out[(int64_t)q * a.ld + pos] = score;
+        }
+        if (a.bkeys) {
+          // candidate block pos / 8 = lanes 8j .. 8j+7 of this warp: its largest key
+          // (NaN already ranks as -inf, +inf stays below the pinned key ~0), the newest
+          // visible block pinned to ~0, blocks past the visible rows 0
+          uint32_t m = key;
+          m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
+          m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));
+          m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 4));
+          const int64_t blk = pos >> 3;
+          if ((lane & 7) == 0 && blk < a.ldb) {
+            const bool newest = gq[i] > 0 && blk == ((gq[i] - 1) >> 3);
+            a.bkeys[(int64_t)q * a.ldb + blk] = newest ? 0xFFFFFFFFu : m;
+          }
         }
       }
       tc_fence_before();
@@ -471,8 +494,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 }  // namespace
 
 size_t index_smem_bytes() {
-  return 1024 + kStages * kStageBytes + kBBytes + 512 * 4 + sizeof(Bars) + 16 +
-         2 * 8 * kMaxGroup;
+  return 1024 + kStages * kStageBytes + kBBytes + 8 * 256 * 4 + sizeof(Bars) + 16 +
+         8 * 8 * kMaxGroup;
 }
 
 cudaError_t launch_index(const IndexArgs& a, int num_sms, cudaStream_t s) {

@@ -33,7 +33,7 @@ namespace csa2 {
 constexpr int kTopkThreads = 1024;
 constexpr int kTopkWarps = kTopkThreads / 32;
 constexpr int kChunkLen = 32768;   // positions per CTA
-constexpr int kMaxChunks = 48;     // the merge holds kMaxChunks * 512 <= kChunkLen pairs
+constexpr int kMaxChunks = 48;     // chunks per row; the merge holds chunks * k <= kChunkLen pairs
 constexpr int kCandCap = 8192;     // kept (key, index) pairs
 constexpr int kWarpCap = kCandCap / (kTopkThreads / 32);  // per-warp region
 constexpr int kWords = kChunkLen / 32;
@@ -429,6 +429,10 @@ int topk_num_chunks(int64_t ld) {
   return (int)((ld + c - 1) / c);
 }
 int64_t topk_max_len() { return (int64_t)kChunkLen * kMaxChunks; }
+bool topk_fits(int64_t ld, int k) {
+  return ld >= 1 && ld <= topk_max_len() && k >= 1 &&
+         (topk_num_chunks(ld) == 1 || (int64_t)topk_num_chunks(ld) * k <= kChunkLen);
+}
 
 cudaError_t launch_topk(const TopkArgs& a, cudaStream_t s) {
   if (a.Q == 0) return cudaSuccess;

@@ -133,6 +133,35 @@ csa2_status csa2_index_topk(const csa2_bf16* iq, const float* w, int Q, int H,
                             float* scores_out, void* ws, size_t ws_bytes, csa2_stream stream);
 
 /* ---------------------------------------------------------------------------------
+ * csa2_index_topk_pool -- csa2_index_topk in FULL mode plus the candidate pool that a
+ * FULL layer hands to the REINDEX layers after it.  [A] Fig. 3b (second stage of the
+ * indexer: block maxima, newest block pinned to +inf, top-2048 blocks, ascending, -1
+ * padded); [B] §5.2 (a block scores as its best row; the partial newest block is
+ * always kept); [C] A.11 (2048 candidate blocks of 8 rows).
+ *
+ * sel / sel_scores / scores_out are those of csa2_index_topk with cand == NULL.  In
+ * addition, for query q with n_vis visible rows, block j (rows 8j .. 8j+7, j <
+ * ceil(n_vis / 8)) scores as the largest s(c) of its visible rows (NaN ranks as -inf;
+ * +inf ranks below the pinned block), the newest block ceil(n_vis / 8) - 1 is pinned
+ * above every score, and the min(nbk, ceil(n_vis / 8)) best blocks (ties: lower block
+ * id) are written as ascending block ids to pool[q][0..), the rest of pool[q][0..nbk)
+ * set to -1.  pool rows feed csa2_index_topk's `cand` (ncb = nbk) directly.
+ *   nbk        1..2048, with ceil(max_scored / 8) blocks per row selectable
+ *              (csa2_index_topk_pool_workspace_size returns 0 otherwise)
+ *   pool       [Q][nbk] int32
+ *   ws         workspace of csa2_index_topk_pool_workspace_size(Q, H, max_scored, k,
+ *              nbk) bytes, 256-byte aligned; contents are scratch.
+ * Other arguments and errors as csa2_index_topk (cand = NULL). */
+size_t csa2_index_topk_pool_workspace_size(int Q, int H, int64_t max_scored, int k, int nbk);
+csa2_status csa2_index_topk_pool(const csa2_bf16* iq, const float* w, int Q, int H,
+                                 const csa2_bf16* index_k, int64_t index_rows,
+                                 const int64_t* row_base, const int32_t* q_seq,
+                                 const int64_t* q_pos, int ratio, int k, int relu,
+                                 int64_t max_scored, int32_t* sel, float* sel_scores,
+                                 float* scores_out, int nbk, int32_t* pool, void* ws,
+                                 size_t ws_bytes, csa2_stream stream);
+
+/* ---------------------------------------------------------------------------------
  * csa2_index_topk_noalloc -- the paper has no counterpart: this is a library service.
  *
  * Same arguments and results as csa2_index_topk, minus the workspace.  It is for
@@ -164,7 +193,9 @@ csa2_status csa2_index_topk_noalloc(const csa2_bf16* iq, const float* w, int Q, 
  * For row q of scores [Q][ld] fp32, the k_eff = min(k, n[q]) highest of
  * scores[q][0..n[q]) (ties: lower index; NaN ranks as -inf; -0 equals +0) are
  * written as ascending indices to sel[q][0..k_eff), -1 after.  sel_scores optional.
- *   n  [Q] int32, 0 <= n[q] <= ld;  k 1..512
+ *   n  [Q] int32, 0 <= n[q] <= ld;  k 1..2048, where rows longer than 32768 are
+ *      cut into ceil(ld / 32768) chunks whose top-k lists are merged: chunks * k must
+ *      be <= 32768 (csa2_topk_workspace_size returns 0 otherwise)
  *   ws workspace of csa2_topk_workspace_size(Q, ld, k) bytes, 256-byte aligned. */
 size_t csa2_topk_workspace_size(int Q, int64_t ld, int k);
 csa2_status csa2_topk_scores(const float* scores, const int32_t* n, int Q, int64_t ld, int k,

@@ -110,3 +110,49 @@ def test_attn_rejects_bad_arguments():
     st = L.csa2_sparse_attn(p, 2, p, p, ctypes.byref(sw), p, 100, p, p, 512, None,
                             float("nan"), p, None, None, 0, None)
     assert st == 1 and b"scale" in L.csa2_last_error()
+
+
+def test_index_topk_pool_rejects_bad_arguments():
+    L = _raw()
+    p = ctypes.c_void_p(256)
+    args = dict(iq=p, w=p, Q=4, H=64, index_k=p, index_rows=1000, row_base=p, q_seq=p, q_pos=p,
+                ratio=2, k=512, relu=1, max_scored=20000, sel=p, sel_scores=None,
+                scores_out=None, nbk=2048, pool=p, ws=p, ws_bytes=1 << 30, stream=None)
+
+    def call(**kw):
+        a = dict(args)
+        a.update(kw)
+        return L.csa2_index_topk_pool(*a.values()), L.csa2_last_error()
+
+    for nbk in (0, 2049):
+        st, msg = call(nbk=nbk)
+        assert st == 1 and b"nbk" in msg
+    st, msg = call(pool=None)
+    assert st == 1 and b"pool" in msg
+    st, msg = call(k=513)
+    assert st == 1 and b"k must" in msg
+    need = csa2.csa2_index_topk_pool_workspace_size(4, 64, 20000, 512, 2048)
+    st, msg = call(ws_bytes=need - 1)
+    assert st == 5 and b"workspace" in msg
+
+
+def test_pool_workspace_holds_the_block_keys():
+    base = csa2.csa2_index_topk_workspace_size(64, 64, 16384, 512)
+    pool = csa2.csa2_index_topk_pool_workspace_size(64, 64, 16384, 512, 2048)
+    assert pool >= base + 64 * 2048 * 4  # one key per block of 8 rows
+    # 2^20 rows: 131072 blocks in 4 chunks, whose 2048-block lists are merged
+    big = csa2.csa2_index_topk_pool_workspace_size(8, 64, 1 << 20, 512, 2048)
+    assert big >= csa2.csa2_index_topk_workspace_size(8, 64, 1 << 20, 512) + 8 * 4 * 2048 * 8
+    assert csa2.csa2_index_topk_pool_workspace_size(8, 64, 1 << 20, 512, 2049) == 0
+
+
+def test_topk_scores_k_limits():
+    L = _raw()
+    p = ctypes.c_void_p(256)
+    st = L.csa2_topk_scores(p, p, 4, 1000, 2049, p, None, None, 0, None)
+    assert st == 1 and b"k must" in L.csa2_last_error()
+    # 32 chunks x 2048 pairs do not fit the merge
+    st = L.csa2_topk_scores(p, p, 4, 1 << 20, 2048, p, None, p, 1 << 30, None)
+    assert st == 1 and b"merge" in L.csa2_last_error()
+    assert csa2.csa2_topk_workspace_size(4, 1 << 20, 2048) == 0
+    assert csa2.csa2_topk_workspace_size(4, 1 << 17, 2048) >= 4 * 4 * 2048 * 8
