@@ -60,11 +60,8 @@ struct IndexArgs {
   int32_t* n_groups;    // [1]
   int32_t* topk_count;  // [Q]  zeroed by the prep kernel for the top-k merge
   int group_max;        // queries per group (FULL: 256 / H; REINDEX: 1)
-  // candidate pool (FULL only; bkeys == null: none)
-  uint32_t* bkeys;      // [Q][ldb] block keys: max over the block's 8 keys, newest = ~0
-  int64_t ldb;          // row stride of bkeys (blocks per row rounded up to 4)
-  int32_t* nblk;        // [Q]  blocks per row = ceil(n_scored / 8)
-  int32_t* pool_count;  // [Q]  zeroed by the prep kernel for the pool's top-k merge
+  int32_t* pool_count;  // [Q]  or null: zeroed by the prep kernel for the candidate
+                        //      pool's top-k merge
 };
 
 struct TopkArgs {
@@ -81,7 +78,11 @@ struct TopkArgs {
   uint64_t* part;         // [Q][nchunk][k] (key << 32 | position) partial results
   int32_t* count;         // [Q] chunk arrivals (zero before the call; reset by the merge)
   int nchunk;             // chunks per row (1 = single pass)
-  int chunk;              // positions per chunk
+  int chunk;              // positions (blocks) per chunk
+  int blocks;             // 1: select blocks of 8 positions of `keys` instead (candidate
+                          //    pool): a block's key is the largest key of its positions
+                          //    < n[q], the newest block ceil(n[q] / 8) - 1 is pinned to
+                          //    ~0, and the output holds block ids
 };
 
 struct AttnArgs {
@@ -111,7 +112,9 @@ struct AttnArgs {
 
 cudaError_t launch_compress(const CompressArgs& a, cudaStream_t s);
 cudaError_t launch_index(const IndexArgs& a, int num_sms, cudaStream_t s);
-cudaError_t launch_topk(const TopkArgs& a, cudaStream_t s);
+// One launch for selection `a` and, when b != null, a second selection over the same
+// queries that runs beside it.
+cudaError_t launch_topk(const TopkArgs& a, cudaStream_t s, const TopkArgs* b = nullptr);
 int attn_num_splits(int Q, int nsel, int num_sms);
 
 // 2-D tensor map over `rows` bf16 rows of `cols` elements (row stride cols * 2 bytes),

@@ -48,14 +48,28 @@ size_t up256(size_t x) { return (x + 255) & ~size_t(255); }
 struct IndexWs {
   size_t keys, n_scored, grp_q0, grp_nq, grp_tile0, n_groups, count, part, total;
   int nchunk;
-  // candidate pool (nbk > 0): block keys, blocks per row, merge counters, partial lists
-  size_t bkeys, nblk, pcount, ppart;
-  int64_t nb_max, ldb;
+  // candidate pool (nbk > 0): merge counters and partial lists of the block selection
+  size_t pcount, ppart;
+  int64_t nb_max;
   int pnchunk;
 };
 
 // Blocks of 8 positions in a row of ld positions.
 int64_t pool_blocks(int64_t ld) { return (ld + 7) / 8; }
+
+// Chunks of the candidate-block selection.  A chunk CTA reads 8 position keys per block;
+// when few queries have long rows (a long-context decode batch) most SMs would idle
+// while a handful of CTAs each stream 1 MiB, so the rows are cut into chunks of 8192
+// blocks (256 KiB of keys) as long as the merge holds their lists and the chunks fit
+// twice over on the SMs; otherwise chunks of up to 32768 blocks.  sms == 0 gives the
+// most chunks any call can use (for the workspace size).
+int pool_chunks(int64_t nb, int nbk, int Q, int sms) {
+  const int big = csa2::topk_num_chunks(nb);
+  const int64_t small = (nb + 8191) / 8192;
+  if (small > big && small * nbk <= 32768 && (sms == 0 || (int64_t)Q * small <= 2 * sms))
+    return (int)small;
+  return big;
+}
 
 IndexWs index_ws_layout(int Q, int64_t ld, int k, int nbk = 0) {
   IndexWs w{};
@@ -72,10 +86,7 @@ IndexWs index_ws_layout(int Q, int64_t ld, int k, int nbk = 0) {
   if (w.nchunk > 1) o = up256(o + (size_t)Q * w.nchunk * k * 8);
   if (nbk > 0) {
     w.nb_max = pool_blocks(ld);
-    w.ldb = (w.nb_max + 3) & ~int64_t(3);
-    w.pnchunk = csa2::topk_num_chunks(w.nb_max);
-    w.bkeys = o; o = up256(o + (size_t)Q * (size_t)w.ldb * 4);
-    w.nblk = o; o = up256(o + (size_t)Q * 4);
+    w.pnchunk = pool_chunks(w.nb_max, nbk, Q, 0);
     w.pcount = o; o = up256(o + (size_t)Q * 4);
     w.ppart = o;
     if (w.pnchunk > 1) o = up256(o + (size_t)Q * w.pnchunk * nbk * 8);
@@ -247,12 +258,7 @@ csa2_status index_topk_impl(const csa2_bf16* iq, const float* w, int Q, int H,
   a.n_groups = reinterpret_cast<int32_t*>(base + L.n_groups);
   a.topk_count = reinterpret_cast<int32_t*>(base + L.count);
   a.group_max = cand ? 1 : 256 / H;
-  if (nbk > 0) {
-    a.bkeys = reinterpret_cast<uint32_t*>(base + L.bkeys);
-    a.ldb = L.ldb;
-    a.nblk = reinterpret_cast<int32_t*>(base + L.nblk);
-    a.pool_count = reinterpret_cast<int32_t*>(base + L.pcount);
-  }
+  if (nbk > 0) a.pool_count = reinterpret_cast<int32_t*>(base + L.pcount);
   const int sms = num_sms();
   if (sms <= 0) return fail(CSA2_ECUDA, "csa2_index_topk: no CUDA device");
   cudaError_t e = csa2::launch_index(a, sms, stream);
@@ -264,17 +270,19 @@ csa2_status index_topk_impl(const csa2_bf16* iq, const float* w, int Q, int H,
   t.count = a.topk_count;
   t.chunk = csa2::topk_chunk_len(max_scored);
   // n_scored <= max_scored <= ldk: the chunking of max_scored covers every row
-  e = csa2::launch_topk(t, stream);
-  if (e != cudaSuccess) return cuda_fail(e, "csa2_index_topk (top-k)");
-  if (nbk > 0) {
-    csa2::TopkArgs p{};
-    p.keys = a.bkeys; p.n = a.nblk; p.Q = Q; p.ld = L.ldb; p.k = nbk;
-    p.sel = pool; p.part = reinterpret_cast<uint64_t*>(base + L.ppart); p.nchunk = L.pnchunk;
+  csa2::TopkArgs p{};
+  if (nbk > 0) {  // the candidate blocks, from the same keys, in the same launch
+    p = t;
+    p.sel_scores = nullptr;
+    p.k = nbk; p.sel = pool; p.blocks = 1;
+    p.part = reinterpret_cast<uint64_t*>(base + L.ppart);
+    p.nchunk = pool_chunks(L.nb_max, nbk, Q, sms);
     p.count = a.pool_count;
-    p.chunk = csa2::topk_chunk_len(L.nb_max);
-    e = csa2::launch_topk(p, stream);
-    if (e != cudaSuccess) return cuda_fail(e, "csa2_index_topk_pool (block top-k)");
+    p.chunk = (int)((L.nb_max + p.nchunk - 1) / p.nchunk);
   }
+  // the block selection's CTAs (the longer ones) first
+  e = nbk > 0 ? csa2::launch_topk(p, stream, &t) : csa2::launch_topk(t, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "csa2_index_topk (top-k)");
   return CSA2_OK;
 }
 

@@ -117,10 +117,7 @@ __global__ void __launch_bounds__(kPrepThreads) index_prep_kernel(IndexArgs a) {
         if (i < kPrepThreads) {
           a.n_scored[q] = (int32_t)ns;
           a.topk_count[q] = 0;
-          if (a.bkeys) {
-            a.nblk[q] = (int32_t)((ns + 7) >> 3);
-            a.pool_count[q] = 0;
-          }
+          if (a.pool_count) a.pool_count[q] = 0;
         }
       }
     }
@@ -389,12 +386,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         load_group(a, g, gi);
       }
       if (g != loaded) {
-        __syncwarp();
+        // all loads in flight at once (nq * H <= 256: eight per lane), then the stores
         const int nw = gi.nq * a.H;
-        for (int i = lane; i < nw; i += 32) w_s[i] = a.w[(int64_t)gi.q0 * a.H + i] * alpha;
+        const float* wg = a.w + (int64_t)gi.q0 * a.H;
+        float wv[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) wv[u] = lane + 32 * u < nw ? __ldg(wg + lane + 32 * u) : 0.f;
+        int64_t lim = 0;
         if (lane < gi.nq)
-          gq[lane] = a.cand ? n_visible(a.q_pos[gi.q0 + lane], a.ratio)
-                            : (int64_t)a.n_scored[gi.q0 + lane];
+          lim = a.cand ? n_visible(a.q_pos[gi.q0 + lane], a.ratio)
+                       : (int64_t)a.n_scored[gi.q0 + lane];
+        __syncwarp();
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+          if (lane + 32 * u < nw) w_s[lane + 32 * u] = wv[u] * alpha;
+        if (lane < gi.nq) gq[lane] = lim;
         __syncwarp();
         loaded = g;
       }
@@ -459,24 +465,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         } else {
           valid = cblk >= 0 && (int64_t)cblk * 8 + (pos & 7) < gq[i];
         }
-        const uint32_t key = valid ? score_key(score) : 0u;
         if (pos < a.ld) {
-          a.keys[(int64_t)q * a.ldk + pos] = key;
+          a.keys[(int64_t)q * a.ldk + pos] = valid ? score_key(score) : 0u;
           if (valid && a.scores_out) a.scores_out[(int64_t)q * a.ld + pos] = score;
-        }
-        if (a.bkeys) {
-          // candidate block pos / 8 = lanes 8j .. 8j+7 of this warp: its largest key
-          // (NaN already ranks as -inf, +inf stays below the pinned key ~0), the newest
-          // visible block pinned to ~0, blocks past the visible rows 0
-          uint32_t m = key;
-          m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
-          m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));
-          m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 4));
-          const int64_t blk = pos >> 3;
-          if ((lane & 7) == 0 && blk < a.ldb) {
-            const bool newest = gq[i] > 0 && blk == ((gq[i] - 1) >> 3);
-            a.bkeys[(int64_t)q * a.ldb + blk] = newest ? 0xFFFFFFFFu : m;
-          }
         }
       }
       tc_fence_before();

@@ -7,7 +7,8 @@
 // positions:
 //   1. sample: the segment is staged in shared memory by one bulk copy (a TMA copy has
 //      the whole row in flight at once); a histogram of the top 11 key bits over an
-//      even sample of 2048 keys gives a threshold bin expected to hold about 2k + 64;
+//      even sample of 2048 keys gives a threshold bin expected to hold about 2k + 64
+//      (refined by the next 11 bits when the sample crowds into that bin);
 //   2. filter: one pass keeps the (key, position) pairs at or above the threshold (a
 //      few times k of them) and counts the scored positions;
 //   3. select: three histogram passes (key bits 31..21, 20..10, 9..0) over the kept
@@ -24,6 +25,13 @@
 // counter) selects the top-k of the concatenated lists.  The true top-k is a subset of
 // the union of the per-chunk top-k sets under the same total order (key desc,
 // position asc), so the merge is exact.
+//
+// Block mode (the candidate pool of a FULL layer, [A] Fig. 3b second stage): the items
+// are blocks of 8 positions.  Each chunk CTA builds its blocks' keys from the row's
+// position keys (the largest key of the block; the newest block pinned to ~0, above
+// every score key, +inf included) in shared memory and selects among them in the same
+// way; the output holds block ids.  It runs in the same launch as the row selection, on
+// CTAs of its own.
 #include "common.cuh"
 
 CSA2_DEFINE_FAULT_FLAG(topk)
@@ -114,9 +122,9 @@ __device__ __forceinline__ void clear_hist(SelectSmem& S, int nbins) {
   for (int i = threadIdx.x; i < nbins; i += kTopkThreads) S.hist[i] = 0;
 }
 
-// Keys of a row segment: workspace keys or raw fp32 scores (both staged in shared memory
-// as keys), or the merge's (key << 32 | position) pairs in global memory.
-enum SrcKind { kSrcKeys = 0, kSrcScores = 1, kSrcPairs = 2, kSrcSmem = 3 };
+// Keys of a row segment: workspace keys or raw fp32 scores in global memory, or keys
+// staged in shared memory (the select always runs on the staged copy).
+enum SrcKind { kSrcKeys = 0, kSrcScores = 1, kSrcSmem = 3 };
 
 template <int kKind>
 struct RowSrc {
@@ -124,7 +132,6 @@ struct RowSrc {
   bool aligned;  // 16-byte aligned base
   __device__ __forceinline__ uint32_t operator()(int i) const {
     if (kKind == kSrcSmem) return static_cast<const uint32_t*>(base)[i];
-    if (kKind == kSrcPairs) return (uint32_t)(__ldcg(static_cast<const uint64_t*>(base) + i) >> 32);
     if (kKind == kSrcScores) return score_key(__ldcg(static_cast<const float*>(base) + i));
     return __ldcg(static_cast<const uint32_t*>(base) + i);
   }
@@ -136,11 +143,6 @@ struct RowSrc {
     if (aligned && i + 4 <= n) {
       if (kKind == kSrcSmem)
         return *reinterpret_cast<const uint4*>(static_cast<const uint32_t*>(base) + i);
-      if (kKind == kSrcPairs) {
-        const uint4* p = reinterpret_cast<const uint4*>(static_cast<const uint64_t*>(base) + i);
-        const uint4 a = __ldcg(p), b = __ldcg(p + 1);
-        return make_uint4(a.y, a.w, b.y, b.w);
-      }
       r = __ldcg(reinterpret_cast<const uint4*>(static_cast<const uint32_t*>(base) + i));
       if (kKind == kSrcScores)
         r = make_uint4(score_key(__uint_as_float(r.x)), score_key(__uint_as_float(r.y)),
@@ -182,7 +184,26 @@ __device__ int select_topk(const RowSrc<kKind>& src, int n, int k, SelectSmem& S
   // sample keys wanted above the threshold: about (2k + 64) / n of the sample
   const int want = (int)(((int64_t)(2 * k + 64) * ns + n - 1) / (n > 0 ? n : 1));
   find_crossing(S, S.hist, 2048, want);
-  const uint32_t thr = want >= ns ? 1u : max((uint32_t)S.found_bin << 21, 1u);
+  uint32_t thr = want >= ns ? 1u : max((uint32_t)S.found_bin << 21, 1u);
+  if (want < ns) {
+    // A crowded threshold bin (keys bunched in one quarter octave, as block maxima
+    // are) would keep far more than the buffer holds: refine it by the sample's next
+    // 11 key bits.
+    const uint32_t bin = (uint32_t)S.found_bin;
+    const int above = S.found_above;
+    if (above + (int)S.hist[bin] > 2 * want + 64) {
+      __syncthreads();  // every thread has read hist[bin]
+      clear_hist(S, 2048);
+      __syncthreads();
+      for (int s2 = tid; s2 < ns; s2 += kTopkThreads) {
+        const uint32_t key = src((int)(((int64_t)(2 * s2 + 1) * n) / (2 * ns)));
+        if (key && (key >> 21) == bin) atomicAdd(&S.hist[(key >> 10) & 2047u], 1u);
+      }
+      __syncthreads();
+      find_crossing(S, S.hist, 2048, want - above);
+      thr = max((bin << 21) | ((uint32_t)S.found_bin << 10), 1u);
+    }
+  }
   // ---- 3. filter: keep keys >= thr, count scored positions ----
   // Warp w appends to its own region [w * kWarpCap, ...) through its shared counter.
   int nval = 0;
@@ -343,44 +364,81 @@ __device__ void pad_row(const TopkArgs& a, int q, int keff) {
   }
 }
 
+// Chunk blockIdx.x of row blockIdx.y of the selection described by `a`.
 template <int kKind>
-__global__ void __launch_bounds__(kTopkThreads, 1) topk_kernel(TopkArgs a) {
+__device__ __forceinline__ void topk_row(const TopkArgs& a, int c) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
   SelectSmem& S = *reinterpret_cast<SelectSmem*>(smem_raw);
-  const int q = blockIdx.y, c = blockIdx.x;
-  griddep_launch_dependents();
+  const int q = blockIdx.y;
   griddep_wait();
   int n = a.n[q];
   if (n > a.ld) { if (threadIdx.x == 0) raise_fault(kFaultBounds); n = (int)a.ld; }
+  const int items = a.blocks ? (n + 7) >> 3 : n;  // positions, or blocks of 8 positions
   const int begin = c * a.chunk;
-  const int len = max(0, min(a.chunk, n - begin));
-  const int64_t rowoff = (int64_t)q * a.ld + begin;
-  // The segment into shared memory: one bulk copy of its 16-byte aligned interior (a
-  // TMA copy has the whole row in flight at once), the ragged ends (at most 3 keys
-  // each) by plain loads; scores become keys in place.
-  const uint32_t* g = kKind == kSrcScores ? reinterpret_cast<const uint32_t*>(a.scores + rowoff)
-                                          : a.keys + rowoff;
+  const int len = max(0, min(a.chunk, items - begin));
   const int tid = threadIdx.x;
-  int head = (int)(((16u - (uint32_t)(reinterpret_cast<uintptr_t>(g) & 15u)) & 15u) >> 2);
-  head = min(head, len);
-  const int body = ((len - head) >> 2) << 2;
-  const int pad = (4 - head) & 3;  // row[pad + head] is 16-byte aligned
-  uint32_t* rowbuf = S.row + pad;
-  if (tid == 0) {
-    mbar_init(smem_u32(&S.bar), 1);
-    mbar_fence_init();
-  }
-  __syncthreads();
-  if (tid == 0 && body > 0) {
-    mbar_arrive_expect_tx(smem_u32(&S.bar), (uint32_t)body * 4u);
-    bulk_copy_g2s(smem_u32(rowbuf + head), g + head, (uint32_t)body * 4u, smem_u32(&S.bar));
-  }
-  if (tid < head) rowbuf[tid] = __ldcg(g + tid);
-  if (head + body + tid < len) rowbuf[head + body + tid] = __ldcg(g + head + body + tid);
-  if (body > 0) mbar_wait(smem_u32(&S.bar), 0);
-  if (kKind == kSrcScores) {
+  uint32_t* rowbuf = S.row;
+  int pad = 0;
+  if (a.blocks) {
+    // Block keys of this chunk straight from the row's position keys (8 keys = two
+    // 16-byte loads per block; rows start 16-byte aligned): the largest key of the
+    // block's positions < n, the newest block pinned above every key.
+    // Four blocks per thread and step, all loads in flight before the first use.
+    const uint32_t* g = a.keys + (int64_t)q * a.ld;
+    constexpr int kU = 4;
+    for (int j0 = tid; j0 < len; j0 += kU * kTopkThreads) {
+      uint4 x[kU], y[kU];
+#pragma unroll
+      for (int u = 0; u < kU; ++u) {
+        const int j = j0 + u * kTopkThreads;
+        const int p0 = 8 * (begin + j);
+        x[u] = y[u] = make_uint4(0u, 0u, 0u, 0u);
+        if (j < len && p0 + 8 <= n) {
+          x[u] = __ldcg(reinterpret_cast<const uint4*>(g + p0));
+          y[u] = __ldcg(reinterpret_cast<const uint4*>(g + p0 + 4));
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < kU; ++u) {
+        const int j = j0 + u * kTopkThreads;
+        if (j >= len) break;
+        const int b = begin + j;
+        // only the newest block can be partial, and it is pinned
+        const uint32_t m = max(max(max(x[u].x, x[u].y), max(x[u].z, x[u].w)),
+                               max(max(y[u].x, y[u].y), max(y[u].z, y[u].w)));
+        rowbuf[j] = b == items - 1 ? 0xFFFFFFFFu : m;
+      }
+    }
+  } else {
+    // The segment into shared memory: one bulk copy of its 16-byte aligned interior (a
+    // TMA copy has the whole row in flight at once), the ragged ends (at most 3 keys
+    // each) by plain loads; scores become keys in place.
+    const int64_t rowoff = (int64_t)q * a.ld + begin;
+    const uint32_t* g = kKind == kSrcScores
+                            ? reinterpret_cast<const uint32_t*>(a.scores + rowoff)
+                            : a.keys + rowoff;
+    int head = (int)(((16u - (uint32_t)(reinterpret_cast<uintptr_t>(g) & 15u)) & 15u) >> 2);
+    head = min(head, len);
+    const int body = ((len - head) >> 2) << 2;
+    pad = (4 - head) & 3;  // row[pad + head] is 16-byte aligned
+    rowbuf = S.row + pad;
+    if (tid == 0) {
+      mbar_init(smem_u32(&S.bar), 1);
+      mbar_fence_init();
+    }
     __syncthreads();
-    for (int i = tid; i < len; i += kTopkThreads) rowbuf[i] = score_key(__uint_as_float(rowbuf[i]));
+    if (tid == 0 && body > 0) {
+      mbar_arrive_expect_tx(smem_u32(&S.bar), (uint32_t)body * 4u);
+      bulk_copy_g2s(smem_u32(rowbuf + head), g + head, (uint32_t)body * 4u, smem_u32(&S.bar));
+    }
+    if (tid < head) rowbuf[tid] = __ldcg(g + tid);
+    if (head + body + tid < len) rowbuf[head + body + tid] = __ldcg(g + head + body + tid);
+    if (body > 0) mbar_wait(smem_u32(&S.bar), 0);
+    if (kKind == kSrcScores) {
+      __syncthreads();
+      for (int i = tid; i < len; i += kTopkThreads)
+        rowbuf[i] = score_key(__uint_as_float(rowbuf[i]));
+    }
   }
   __syncthreads();
   RowSrc<kSrcSmem> src{rowbuf, pad == 0};
@@ -408,15 +466,51 @@ __global__ void __launch_bounds__(kTopkThreads, 1) topk_kernel(TopkArgs a) {
   __threadfence();
   // candidates are in chunk order and ascending within a chunk: index order is
   // position order, so the select's tie rule stays "lower position".
-  const int ncand = a.nchunk * a.k;
+  // The lists' keys go to shared memory (the segment's buffer is free again: the
+  // select reads them several times); positions are fetched for the winners only.
+  const int ncand = a.nchunk * a.k;  // <= kChunkLen
   const uint64_t* row = a.part + (int64_t)q * ncand;
-  RowSrc<kSrcPairs> msrc{row, (reinterpret_cast<uintptr_t>(row) & 15u) == 0};
+  uint32_t* mk = S.row;
+  if ((reinterpret_cast<uintptr_t>(row) & 15u) == 0) {
+    const uint4* r4 = reinterpret_cast<const uint4*>(row);
+    const int npair2 = ncand >> 1;
+    constexpr int kU = 4;
+    for (int i0 = tid; i0 < npair2; i0 += kU * kTopkThreads) {
+      uint4 v[kU];
+#pragma unroll
+      for (int u = 0; u < kU; ++u) {
+        const int i = i0 + u * kTopkThreads;
+        v[u] = i < npair2 ? __ldcg(r4 + i) : make_uint4(0u, 0u, 0u, 0u);
+      }
+#pragma unroll
+      for (int u = 0; u < kU; ++u) {
+        const int i = i0 + u * kTopkThreads;
+        if (i < npair2) { mk[2 * i] = v[u].y; mk[2 * i + 1] = v[u].w; }
+      }
+    }
+    if ((ncand & 1) && tid == 0) mk[ncand - 1] = (uint32_t)(__ldcg(row + ncand - 1) >> 32);
+  } else {
+    for (int i = tid; i < ncand; i += kTopkThreads) mk[i] = (uint32_t)(__ldcg(row + i) >> 32);
+  }
+  __syncthreads();
+  RowSrc<kSrcSmem> msrc{mk, true};
   const int keff2 = select_topk(msrc, ncand, a.k, S, [&](int o, int i) {
     sel_q[o] = pos_to_row(a, q, (uint32_t)(__ldcg(row + i) & 0xFFFFFFFFu));
-    if (sc_q) sc_q[o] = key_score(msrc(i));
+    if (sc_q) sc_q[o] = key_score(mk[i]);
   });
   pad_row(a, q, keff2);
   if (threadIdx.x == 0) a.count[q] = 0;  // ready for the next call
+}
+
+// One launch runs one or two independent selections over the same queries, e.g. the
+// top rows and the top candidate blocks of a FULL layer side by side: blockIdx.x below
+// a0.nchunk is a chunk of a0, the rest are chunks of a1.
+template <int kKind>
+__global__ void __launch_bounds__(kTopkThreads, 1) topk_kernel(TopkArgs a0, TopkArgs a1) {
+  griddep_launch_dependents();
+  const int c = blockIdx.x;
+  if (c < a0.nchunk) topk_row<kKind>(a0, c);
+  else topk_row<kKind>(a1, c - a0.nchunk);
 }
 
 }  // namespace
@@ -434,14 +528,17 @@ bool topk_fits(int64_t ld, int k) {
          (topk_num_chunks(ld) == 1 || (int64_t)topk_num_chunks(ld) * k <= kChunkLen);
 }
 
-cudaError_t launch_topk(const TopkArgs& a, cudaStream_t s) {
+cudaError_t launch_topk(const TopkArgs& a, cudaStream_t s, const TopkArgs* b) {
   if (a.Q == 0) return cudaSuccess;
+  if (b && (b->Q != a.Q || (b->scores != nullptr) != (a.scores != nullptr)))
+    return cudaErrorInvalidValue;
   const size_t smem = sizeof(SelectSmem);
   auto kern = a.scores ? topk_kernel<kSrcScores> : topk_kernel<kSrcKeys>;
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  return launch_pdl(kern, dim3(a.nchunk, a.Q), dim3(kTopkThreads), smem, s, a);
+  const int nx = a.nchunk + (b ? b->nchunk : 0);
+  return launch_pdl(kern, dim3(nx, a.Q), dim3(kTopkThreads), smem, s, a, b ? *b : a);
 }
 
 }  // namespace csa2

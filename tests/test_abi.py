@@ -136,10 +136,10 @@ def test_index_topk_pool_rejects_bad_arguments():
     assert st == 5 and b"workspace" in msg
 
 
-def test_pool_workspace_holds_the_block_keys():
+def test_pool_workspace_holds_the_block_merge():
     base = csa2.csa2_index_topk_workspace_size(64, 64, 16384, 512)
     pool = csa2.csa2_index_topk_pool_workspace_size(64, 64, 16384, 512, 2048)
-    assert pool >= base + 64 * 2048 * 4  # one key per block of 8 rows
+    assert pool >= base + 64 * 4  # the block selection's arrival counters
     # 2^20 rows: 131072 blocks in 4 chunks, whose 2048-block lists are merged
     big = csa2.csa2_index_topk_pool_workspace_size(8, 64, 1 << 20, 512, 2048)
     assert big >= csa2.csa2_index_topk_workspace_size(8, 64, 1 << 20, 512) + 8 * 4 * 2048 * 8

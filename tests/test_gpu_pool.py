@@ -98,17 +98,19 @@ def check_pool(pool_gpu, pool_ref, sc, rows, nbk):
     return len(diff)
 
 
-def test_topk_scores_k2048_bit_exact():
+@pytest.mark.parametrize("k", [2048, 512])
+def test_topk_scores_large_k_bit_exact(k):
     from csa2_compressed_sparse_gb300 import (csa2_device_status, csa2_topk_scores,
                                               csa2_topk_workspace_size)
-    k = 2048
     for ld in (1500, 2048, 5000, 32768, 100000):
         g = np.random.default_rng(ld)
-        Q = 4
+        Q = 5
         s = g.standard_normal((Q, ld)).astype(np.float32)
         s[1] = (g.integers(-30, 30, ld) / 4.0).astype(np.float32)  # heavy ties
         s[2, ::3] = np.nan
-        n = np.array([ld, ld, ld - 1, ld // 3], dtype=np.int32)
+        # all keys within one quarter octave: the sampled threshold bin is refined
+        s[4] = (1.0 + 1e-3 * g.standard_normal(ld)).astype(np.float32)
+        n = np.array([ld, ld, ld - 1, ld // 3, ld], dtype=np.int32)
         sel = torch.empty((Q, k), dtype=torch.int32, device="cuda")
         ws = torch.empty(max(csa2_topk_workspace_size(Q, ld, k), 256), dtype=torch.uint8,
                          device="cuda")
