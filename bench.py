@@ -40,6 +40,9 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--cpu-queries", type=int, default=64)
+    ap.add_argument("--stages", action="store_true",
+                    help="time every entry point of the step (and the candidate-pool and "
+                         "inverse-RoPE variants) on its own instead; prints one JSON line")
     return ap.parse_args()
 
 
@@ -482,10 +485,79 @@ def run_reference(args):
     }), flush=True)
 
 
+def run_stages(args):
+    """Mean device time of each entry point on the chosen workload: 20 calls captured in
+    one CUDA graph, replayed `reps` times between CUDA events on the launching stream."""
+    import csa2_compressed_sparse_gb300 as csa2
+    from csa2_compressed_sparse_gb300.step import allocate, run_step, swa_of
+    torch.cuda.set_device(0)
+    wl = make_workload(args.config, 0)
+    spec = spec_for(wl)
+    t = wl.materialize("cuda")
+    buf = allocate(spec, t)
+    for _ in range(3):
+        run_step(spec, t, buf)
+    torch.cuda.synchronize()
+    csa2.csa2_device_status()
+
+    def timed(fn, inner=20, reps=20):
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            fn()
+        torch.cuda.current_stream().wait_stream(side)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for _ in range(inner):
+                fn()
+        for _ in range(3):
+            g.replay()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        stream = torch.cuda.current_stream()
+        e0.record(stream)
+        for _ in range(reps):
+            g.replay()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) * 1e3 / (inner * reps)
+
+    cand = t.get("cand")
+    swa0 = swa_of(spec, t, 0)
+    res = {}
+    res["compress"] = timed(lambda: csa2.csa2_compress(
+        t["kv"], t["score"], t["cu_seqlens"], t["start_pos"], spec.ratio, t["kv_state"],
+        t["score_state"], t["plane"], t["row_base"], t["inv_freq"], eps=spec.eps))
+    res["index_topk"] = timed(lambda: csa2.csa2_index_topk(
+        t["iq"], t["w"], t["index_k"], t["row_base"], t["q_seq"], t["q_pos"], spec.ratio, spec.k,
+        spec.max_scored, buf.sel, buf.ws, sel_scores=buf.sel_scores, cand=cand))
+    if cand is None:
+        nbk = 2048
+        pws = torch.empty(csa2.csa2_index_topk_pool_workspace_size(
+            wl.Q, spec.H, spec.max_scored, spec.k, nbk), dtype=torch.uint8, device="cuda")
+        pool = torch.empty((wl.Q, nbk), dtype=torch.int32, device="cuda")
+        res["index_topk_pool"] = timed(lambda: csa2.csa2_index_topk_pool(
+            t["iq"], t["w"], t["index_k"], t["row_base"], t["q_seq"], t["q_pos"], spec.ratio,
+            spec.k, spec.max_scored, buf.sel, pool, pws, sel_scores=buf.sel_scores))
+    res["sparse_attn"] = timed(lambda: csa2.csa2_sparse_attn(
+        t["q"][0], t["q_seq"], t["q_pos"], swa0, t["plane"], t["row_base"], buf.sel, t["sink"],
+        buf.out[0], scale=spec.scale, ws=buf.attn_ws))
+    res["sparse_attn_rope"] = timed(lambda: csa2.csa2_sparse_attn_rope(
+        t["q"][0], t["q_seq"], t["q_pos"], swa0, t["plane"], t["row_base"], buf.sel, t["sink"],
+        buf.out[0], t["inv_freq"], scale=spec.scale, ws=buf.attn_ws))
+    res["step"] = timed(lambda: run_step(spec, t, buf))
+    csa2.csa2_device_status()
+    print(json.dumps({"stages_us": {k: round(v, 2) for k, v in res.items()},
+                      "workload": wl.name, "description": wl.description,
+                      "queries": wl.Q}), flush=True)
+
+
 def main():
     args = parse()
     if args.impl == "reference":
         run_reference(args)
+    elif args.stages:
+        run_stages(args)
     else:
         run_ours(args)
 
