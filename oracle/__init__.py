@@ -37,6 +37,15 @@ def lib():
         L.orc_index_scores.argtypes = [_vp, _vp, _i32, _i32, _vp, _vp, _vp, _vp, _i32, _vp, _i32,
                                        _i32, _vp, _vp, _i64]
         L.orc_index_scores.restype = None
+        L.orc_e4m3_code.argtypes = [_dbl]
+        L.orc_e4m3_code.restype = ctypes.c_uint8
+        L.orc_ue8m0_scale.argtypes = [_dbl]
+        L.orc_ue8m0_scale.restype = _dbl
+        L.orc_index_plane_fp8.argtypes = [_vp, _i64, _vp]
+        L.orc_index_plane_fp8.restype = None
+        L.orc_index_scores_fp8.argtypes = [_vp, _vp, _i32, _i32, _vp, _vp, _vp, _vp, _i32, _vp,
+                                           _i32, _i32, _vp, _vp, _i64]
+        L.orc_index_scores_fp8.restype = None
         L.orc_topk.argtypes = [_vp, _vp, _i64, _i32, _vp]
         L.orc_topk.restype = _i32
         L.orc_sparse_attn.argtypes = [_vp, _i32, _vp, _vp, _i32, _i32, _vp, _vp, _vp, _vp, _vp,
@@ -122,6 +131,52 @@ def index_scores(iq, w, index_k, row_base, q_seq, q_pos, ratio, cand=None, relu=
     rows = np.zeros((Q, ld), dtype=np.int64)
     lib().orc_index_scores(_p(iqb), _p(wf), Q, H, _p(kb), _p(rb), _p(qs), _p(qp), ratio, _p(cd),
                            ncb, 1 if relu else 0, _p(sc), _p(rows), ld)
+    return sc, rows
+
+
+def e4m3_code(x):
+    """E4M3 code of a double: nearest, ties to even, saturating at 448."""
+    return int(lib().orc_e4m3_code(float(x)))
+
+
+def ue8m0_scale(amax):
+    """Smallest power of two s with amax / s <= 448 (1 for amax == 0)."""
+    return float(lib().orc_ue8m0_scale(float(amax)))
+
+
+FP8_BLOCK_BYTES = 1056  # 8 rows x (128 E4M3 codes) then 8 fp32 scales
+
+
+def index_plane_fp8(index_k):
+    """bf16 [n, 128] index rows -> FP8 plane bytes [ceil(n / 8) * 1056] (uint8)."""
+    kb = bf16_bits(index_k)
+    n = kb.shape[0]
+    out = np.zeros(((n + 7) // 8) * FP8_BLOCK_BYTES, dtype=np.uint8)
+    lib().orc_index_plane_fp8(_p(kb), n, _p(out))
+    return out
+
+
+def index_scores_fp8(iq, w, plane, row_base, q_seq, q_pos, ratio, cand=None, relu=True, ld=None):
+    """index_scores on an FP8 plane (row_base multiples of 8); the query is quantised
+    per (token, head) inside, as the FP8 indexer does."""
+    iqb = bf16_bits(iq)
+    Q, H = iqb.shape[0], iqb.shape[1]
+    wf = np.ascontiguousarray(w.detach().cpu().numpy() if isinstance(w, torch.Tensor) else w,
+                              dtype=np.float32)
+    pl = np.ascontiguousarray(plane, dtype=np.uint8)
+    rb = np.ascontiguousarray(row_base, dtype=np.int64)
+    assert np.all(rb % 8 == 0)
+    qs = np.ascontiguousarray(q_seq, dtype=np.int32)
+    qp = np.ascontiguousarray(q_pos, dtype=np.int64)
+    cd = None if cand is None else np.ascontiguousarray(cand, dtype=np.int32)
+    ncb = 0 if cand is None else cd.shape[1]
+    if ld is None:
+        ld = ncb * 8 if cand is not None else int(max(n_visible(p, ratio) for p in qp))
+    ld = max(int(ld), 1)
+    sc = np.zeros((Q, ld), dtype=np.float64)
+    rows = np.zeros((Q, ld), dtype=np.int64)
+    lib().orc_index_scores_fp8(_p(iqb), _p(wf), Q, H, _p(pl), _p(rb), _p(qs), _p(qp), ratio,
+                               _p(cd), ncb, 1 if relu else 0, _p(sc), _p(rows), ld)
     return sc, rows
 
 

@@ -65,6 +65,39 @@ double orc_e4m3_val(uint8_t c) {
   return sgn ? -v : v;
 }
 
+/* OCP FP8 E4M3 encode from the same definition: round to nearest, ties to the even
+ * mantissa, finite values beyond the largest (448 = 1.75 * 2^8) saturate to it (the
+ * format has no infinity).  Subnormals step by 2^-9 below 2^-6. */
+uint8_t orc_e4m3_code(double x) {
+  if (isnan(x)) return 0x7F;
+  uint8_t sign = signbit(x) ? 0x80 : 0;
+  double a = fabs(x);
+  if (a < ldexp(1.0, -6)) {                       /* subnormal range (or zero) */
+    double qv = nearbyint(ldexp(a, 9));            /* 0 .. 8; 8 is the smallest normal */
+    return sign | (uint8_t)qv;
+  }
+  int e;
+  double m = frexp(a, &e);                         /* a = m * 2^e, 0.5 <= m < 1 */
+  int E = e - 1;                                   /* a = (2m) * 2^E, 1 <= 2m < 2 */
+  double q = nearbyint((2.0 * m - 1.0) * 8.0);     /* mantissa steps of 1/8 */
+  if (q == 8.0) { q = 0.0; E += 1; }
+  if (E > 8 || (E == 8 && q > 6.0)) return sign | 0x7E;  /* saturate to 448 */
+  return sign | (uint8_t)(((E + 7) << 3) | (int)q);
+}
+
+/* Power-of-two (E8M0) scale of a group with largest magnitude amax: the smallest
+ * 2^e with amax / 2^e <= 448, so the group's codes use the top of the E4M3 range
+ * without saturating.  amax == 0 gives 1.  [E] indexer compressor ("row amax ->
+ * ue8m0 -> e4m3"). */
+double orc_ue8m0_scale(double amax) {
+  if (!(amax > 0.0)) return 1.0;
+  int e;
+  frexp(amax, &e);
+  e -= 9;                                          /* below the answer */
+  while (amax > 448.0 * ldexp(1.0, e)) e++;
+  return ldexp(1.0, e);
+}
+
 /* ---- visibility [A] "visible 是每行自己的前缀长度"; [B] §4.1 -------------------- */
 
 /* Compressed row j covers positions j*m .. j*m+m-1 and becomes visible to the
@@ -178,6 +211,88 @@ void orc_index_scores(const uint16_t* iq, const float* w, int Q, int H, const ui
       for (int h = 0; h < H; h++) {
         double dot = 0.0;
         for (int d = 0; d < D_IDX; d++) dot += qv[h * D_IDX + d] * kr[d];
+        if (relu && dot < 0.0) dot = 0.0;
+        s += (double)w[(int64_t)q * H + h] * dot;
+      }
+      scores[(int64_t)q * ld + pos] = alpha * s;
+    }
+  }
+}
+
+/* ---- FP8 index plane [A] indexer figure (FP8: 132 B per row, blocks of 8 rows with
+ *      the values first and the fp32 scales at the block tail; the query quantised per
+ *      (token, head) with its fp32 scale folded into w); [E] indexer compressor
+ *      ("row amax -> ue8m0 -> e4m3") -----------------------------------------------
+ *
+ * One row (128 bf16 values) -> scale = orc_ue8m0_scale(max |x|), codes = E4M3(x / scale).
+ * Block b of the plane holds rows 8b .. 8b+7: 8 x 128 code bytes, then 8 fp32 scales
+ * (1056 bytes).  n rows are written to ceil(n / 8) blocks; the rows of a partial last
+ * block past n are zero with scale 1. */
+void orc_index_plane_fp8(const uint16_t* k, int64_t n, uint8_t* plane) {
+  int64_t nb = (n + 7) / 8;
+  memset(plane, 0, (size_t)nb * 1056);
+  for (int64_t r = 0; r < nb * 8; r++) {
+    uint8_t* blk = plane + (r / 8) * 1056;
+    float* sc = (float*)(blk + 1024);
+    if (r >= n) { sc[r % 8] = 1.0f; continue; }
+    double amax = 0.0;
+    for (int d = 0; d < D_IDX; d++) {
+      double v = fabs(bf16_val(k[r * D_IDX + d]));
+      if (v > amax) amax = v;
+    }
+    double s = orc_ue8m0_scale(amax);
+    for (int d = 0; d < D_IDX; d++)
+      blk[(r % 8) * D_IDX + d] = orc_e4m3_code(bf16_val(k[r * D_IDX + d]) / s);
+    sc[r % 8] = (float)s; /* a power of two: exact in fp32 */
+  }
+}
+
+/* Index scores on the FP8 plane: the query of (q, h) is quantised like a plane row
+ * (scale sq), the row c of sequence b is block (row_base[b] + c) / 8, slot
+ * (row_base[b] + c) % 8 (row_base[b] is a multiple of 8), and
+ *     s(c) = alpha * sum_h w[q][h] * relu(sq_h * sk_c * sum_d e4m3(qc_h,d) * e4m3(kc_c,d))
+ * with the rest (visibility, REINDEX positions, alpha) as orc_index_scores. */
+void orc_index_scores_fp8(const uint16_t* iq, const float* w, int Q, int H, const uint8_t* plane,
+                          const int64_t* row_base, const int32_t* q_seq, const int64_t* q_pos,
+                          int m, const int32_t* cand, int ncb, int relu, double* scores,
+                          int64_t* rows, int64_t ld) {
+  double alpha = 1.0 / sqrt((double)D_IDX) / sqrt((double)H);
+  for (int q = 0; q < Q; q++) {
+    int64_t nvis = orc_n_visible(q_pos[q], m);
+    int64_t rb = row_base[q_seq[q]];
+    double qv[64 * D_IDX], qs[64];
+    for (int h = 0; h < H; h++) {
+      const uint16_t* x = iq + ((int64_t)q * H + h) * D_IDX;
+      double amax = 0.0;
+      for (int d = 0; d < D_IDX; d++) if (fabs(bf16_val(x[d])) > amax) amax = fabs(bf16_val(x[d]));
+      qs[h] = orc_ue8m0_scale(amax);
+      for (int d = 0; d < D_IDX; d++) qv[h * D_IDX + d] = orc_e4m3_val(orc_e4m3_code(bf16_val(x[d]) / qs[h]));
+    }
+    int64_t npos = cand ? (int64_t)ncb * 8 : nvis;
+#pragma omp parallel for schedule(static)
+    for (int64_t pos = 0; pos < ld; pos++) {
+      int64_t row = -1;
+      if (pos < npos) {
+        if (!cand) row = pos;
+        else {
+          int32_t blk = cand[(int64_t)q * ncb + pos / 8];
+          if (blk >= 0 && (int64_t)blk * 8 + pos % 8 < nvis) row = (int64_t)blk * 8 + pos % 8;
+        }
+      }
+      rows[(int64_t)q * ld + pos] = row;
+      if (row < 0) { scores[(int64_t)q * ld + pos] = 0.0; continue; }
+      const uint8_t* blk = plane + ((rb + row) / 8) * 1056;
+      int slot = (int)((rb + row) % 8);
+      float skf;
+      memcpy(&skf, blk + 1024 + 4 * slot, 4);
+      double sk = (double)skf;
+      double kr[D_IDX];
+      for (int d = 0; d < D_IDX; d++) kr[d] = orc_e4m3_val(blk[slot * D_IDX + d]);
+      double s = 0.0;
+      for (int h = 0; h < H; h++) {
+        double dot = 0.0;
+        for (int d = 0; d < D_IDX; d++) dot += qv[h * D_IDX + d] * kr[d];
+        dot *= qs[h] * sk;
         if (relu && dot < 0.0) dot = 0.0;
         s += (double)w[(int64_t)q * H + h] * dot;
       }

@@ -331,6 +331,115 @@ def test_index_reindex_rows_and_masks():
             assert sc[0, i] == full[0, r]
 
 
+# ---- FP8 index plane (NEXT-3) --------------------------------------------------------
+
+def _e4m3_values():
+    return np.array([oracle.e4m3_value(c) for c in range(0x7F)])  # +0 .. 448
+
+
+def test_e4m3_encode_matches_torch_float8_and_ties_to_even():
+    vals = _e4m3_values()
+    mids = (vals[:-1] + vals[1:]) / 2  # exact in fp32: at most 5 significant bits
+    rnd = RNG.uniform(-448, 448, 20000) * np.exp2(RNG.integers(-12, 1, 20000))
+    x = np.concatenate([vals, -vals, mids, -mids, rnd]).astype(np.float32)
+    ref = torch.from_numpy(x).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    got = np.array([oracle.e4m3_code(float(v)) for v in x], dtype=np.uint8)
+    assert np.array_equal(got, ref)
+    # every finite code round-trips; beyond 448 saturates (no infinity in the format)
+    assert all(oracle.e4m3_code(oracle.e4m3_value(c)) == c for c in range(0x7F))
+    assert oracle.e4m3_code(470.0) == 0x7E and oracle.e4m3_code(-1e6) == 0xFE
+    # a tie between 1.0 (mantissa 0) and 1.125 (mantissa 1) goes to the even mantissa
+    assert oracle.e4m3_code(1.0625) == 0x38 and oracle.e4m3_code(1.1875) == 0x3A
+
+
+def test_ue8m0_scale_is_the_smallest_power_of_two_that_fits():
+    for amax in np.concatenate([RNG.uniform(0, 1, 200) * np.exp2(RNG.integers(-40, 40, 200)),
+                                [448.0, 449.0, 1.0, 2.0 ** -30, 448 * 2.0 ** -5]]):
+        s = oracle.ue8m0_scale(amax)
+        m, e = math.frexp(s)
+        assert m == 0.5  # a power of two
+        assert amax / s <= 448.0 < amax / (s / 2)
+    assert oracle.ue8m0_scale(448.0) == 1.0 and oracle.ue8m0_scale(448.0 * 2 ** -7) == 2 ** -7
+    assert oracle.ue8m0_scale(0.0) == 1.0
+
+
+def test_fp8_plane_layout_and_quantisation_error():
+    n = 21  # two full blocks and a partial third
+    x = RNG.standard_normal((n, 128)) * np.exp2(RNG.integers(-6, 6, (n, 1)))
+    K = bf16(x)
+    Kd = bf16_np(K)
+    plane = oracle.index_plane_fp8(K)
+    assert plane.size == 3 * oracle.FP8_BLOCK_BYTES
+    blocks = plane.reshape(3, oracle.FP8_BLOCK_BYTES)
+    codes = blocks[:, :1024].reshape(24, 128)
+    scales = blocks[:, 1024:].copy().view(np.float32).reshape(24).astype(np.float64)
+    # rows past n: zero codes, scale 1
+    assert np.all(codes[n:] == 0) and np.all(scales[n:] == 1.0)
+    vals = _e4m3_values()
+    for r in range(n):
+        amax = np.abs(Kd[r]).max()
+        assert 224.0 < amax / scales[r] <= 448.0  # the row's largest value uses the top octave
+        deq = np.array([oracle.e4m3_value(c) for c in codes[r]]) * scales[r]
+        # nearest E4M3 value: relative error <= 2^-4 in the normal range, absolute
+        # <= 2^-10 * scale in the subnormal one
+        err = np.abs(deq - Kd[r])
+        bound = np.maximum(np.abs(Kd[r]) * 2.0 ** -4, 2.0 ** -10 * scales[r])
+        assert np.all(err <= bound * (1 + 1e-12))
+        # and it is the nearest one: no other code is closer
+        cand = np.abs(vals[None, :] * scales[r] - np.abs(Kd[r])[:, None]).min(1)
+        np.testing.assert_allclose(err, cand, rtol=0, atol=1e-300)
+
+
+def _lossless_fp8_rows(rows, H=None):
+    """bf16 rows that the FP8 quantiser represents exactly: every value is an E4M3
+    normal value times 2^k, and each row holds 448 * 2^k, which fixes its scale."""
+    vals = _e4m3_values()
+    normal = vals[(vals >= 2.0 ** -6)]
+    shape = (rows, 128) if H is None else (rows, H, 128)
+    v = RNG.choice(normal, size=shape) * RNG.choice([-1.0, 1.0], size=shape)
+    k = RNG.integers(-8, 4, size=shape[:-1] + (1,))
+    v[..., 5] = 448.0
+    return bf16(v * np.exp2(k))
+
+
+def test_fp8_scores_equal_bf16_scores_when_quantisation_is_lossless():
+    # two sequences (row_base 0 and 64), FULL and REINDEX: the FP8 path (its own loops,
+    # codes and scales) must give the bf16 path's scores when nothing is lost
+    K = _lossless_fp8_rows(128)
+    iq = _lossless_fp8_rows(3, H=64)
+    w = RNG.standard_normal((3, 64)).astype(np.float32)
+    rb = np.array([0, 64], dtype=np.int64)
+    plane = oracle.index_plane_fp8(K)
+    pos = [120, 63, 37]
+    seqs = [0, 1, 1]
+    for ratio in (1, 2):
+        a, ra = oracle.index_scores(iq, w, K, rb, seqs, pos, ratio)
+        b, rb8 = oracle.index_scores_fp8(iq, w, plane, rb, seqs, pos, ratio)
+        assert np.array_equal(ra, rb8)
+        np.testing.assert_allclose(b, a, rtol=1e-12, atol=1e-12)
+    cand = np.array([[0, 5, 14, -1], [7, 2, -1, -1], [1, 3, 4, 0]], dtype=np.int32)
+    a, ra = oracle.index_scores(iq, w, K, rb, seqs, pos, 1, cand=cand)
+    b, rb8 = oracle.index_scores_fp8(iq, w, plane, rb, seqs, pos, 1, cand=cand)
+    assert np.array_equal(ra, rb8)
+    np.testing.assert_allclose(b, a, rtol=1e-12, atol=1e-12)
+
+
+def test_fp8_scores_stay_within_the_quantisation_error_of_bf16():
+    iq, K, w, rb = make_index_case(Q=2, H=64, rows=160, seq=1)
+    plane = oracle.index_plane_fp8(K)
+    a, _ = oracle.index_scores(iq, w, K, rb, [0, 0], [159, 100], 1, relu=False)
+    b, _ = oracle.index_scores_fp8(iq, w, plane, rb, [0, 0], [159, 100], 1, relu=False)
+    # each factor is within 2^-4 relative (plus subnormal flushes): the sum of |terms|
+    # bounds the error
+    Kd, qd = bf16_np(K), bf16_np(iq)
+    alpha = 1.0 / math.sqrt(128 * 64)
+    for q, nv in ((0, 160), (1, 101)):
+        mag = alpha * (np.abs(w[q]).astype(np.float64)[:, None, None]
+                       * np.abs(qd[q])[:, None, :] * np.abs(Kd[:nv])[None, :, :]).sum((0, 2))
+        assert np.all(np.abs(b[q, :nv] - a[q, :nv]) <= 0.14 * mag + 1e-9)
+        assert np.corrcoef(a[q, :nv], b[q, :nv])[0, 1] > 0.99
+
+
 # ---- top-k --------------------------------------------------------------------------
 
 def brute_topk(scores, rows, k):
