@@ -19,6 +19,8 @@ __all__ = [
     "Csa2Error", "Swa", "lib", "csa2_version", "csa2_device_status", "csa2_compress",
     "csa2_index_topk_workspace_size", "csa2_index_topk", "csa2_index_topk_noalloc",
     "csa2_index_topk_pool_workspace_size", "csa2_index_topk_pool", "csa2_topk_workspace_size",
+    "csa2_index_plane_fp8_bytes", "csa2_index_plane_fp8", "csa2_index_topk_fp8_workspace_size",
+    "csa2_index_topk_fp8",
     "csa2_topk_scores", "csa2_attn_workspace_size", "csa2_sparse_attn", "csa2_reuse_attn",
     "csa2_sparse_attn_rope", "csa2_reuse_attn_rope",
 ]
@@ -57,6 +59,11 @@ _SIGS = {
     "csa2_index_topk_pool_workspace_size": ([_i32, _i32, _i64, _i32, _i32], _sz),
     "csa2_index_topk_pool": ([_vp, _vp, _i32, _i32, _vp, _i64, _vp, _vp, _vp, _i32, _i32, _i32,
                               _i64, _vp, _vp, _vp, _i32, _vp, _vp, _sz, _vp], _i32),
+    "csa2_index_plane_fp8_bytes": ([_i64], _sz),
+    "csa2_index_plane_fp8": ([_vp, _i64, _vp, _vp], _i32),
+    "csa2_index_topk_fp8_workspace_size": ([_i32, _i32, _i64, _i32], _sz),
+    "csa2_index_topk_fp8": ([_vp, _vp, _i32, _i32, _vp, _i64, _vp, _vp, _vp, _i32, _vp, _i32,
+                             _i32, _i32, _i64, _vp, _vp, _vp, _vp, _sz, _vp], _i32),
     "csa2_topk_workspace_size": ([_i32, _i64, _i32], _sz),
     "csa2_topk_scores": ([_vp, _vp, _i32, _i64, _i32, _vp, _vp, _vp, _sz, _vp], _i32),
     "csa2_attn_workspace_size": ([_i32, _i32], _sz),
@@ -181,6 +188,32 @@ def csa2_index_topk_pool(iq, w, index_k, row_base, q_seq, q_pos, ratio, k, max_s
                                       1 if relu else 0, max_scored, _p(sel), _p(sel_scores),
                                       _p(scores_out), pool.shape[1], _p(pool), _p(ws),
                                       ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def csa2_index_plane_fp8_bytes(rows):
+    return int(lib().csa2_index_plane_fp8_bytes(rows))
+
+
+def csa2_index_plane_fp8(index_k, plane, stream=None):
+    """bf16 index rows [rows, 128] -> FP8 plane bytes (blocks of 8 rows, 1056 B each)."""
+    _check(lib().csa2_index_plane_fp8(_p(index_k), index_k.shape[0], _p(plane), _stream(stream)))
+
+
+def csa2_index_topk_fp8_workspace_size(Q, H, max_scored, k):
+    return int(lib().csa2_index_topk_fp8_workspace_size(Q, H, max_scored, k))
+
+
+def csa2_index_topk_fp8(iq, w, plane, index_rows, row_base, q_seq, q_pos, ratio, k, max_scored,
+                        sel, ws, sel_scores=None, cand=None, relu=True, scores_out=None,
+                        stream=None):
+    """csa2_index_topk on an FP8 index plane of index_rows rows."""
+    Q, H = iq.shape[0], iq.shape[1]
+    ncb = 0 if cand is None else cand.shape[1]
+    _check(lib().csa2_index_topk_fp8(_p(iq), _p(w), Q, H, _p(plane), index_rows, _p(row_base),
+                                     _p(q_seq), _p(q_pos), ratio, _p(cand), ncb, k,
+                                     1 if relu else 0, max_scored, _p(sel), _p(sel_scores),
+                                     _p(scores_out), _p(ws), ws.numel() * ws.element_size(),
+                                     _stream(stream)))
 
 
 def csa2_topk_workspace_size(Q, ld, k):

@@ -62,6 +62,11 @@ struct IndexArgs {
   int group_max;        // queries per group (FULL: 256 / H; REINDEX: 1)
   int32_t* pool_count;  // [Q]  or null: zeroed by the prep kernel for the candidate
                         //      pool's top-k merge
+  // FP8 index plane (null: index_k is bf16): blocks of 8 rows, 8 x 128 E4M3 codes then
+  // 8 fp32 scales (1056 bytes); row_base values are multiples of 8
+  const uint8_t* plane8;
+  uint8_t* q8;          // [Q*H][128] E4M3 codes of the quantised queries (workspace)
+  float* qscale;        // [Q*H] their power-of-two scales (workspace)
 };
 
 struct TopkArgs {
@@ -112,6 +117,8 @@ struct AttnArgs {
 
 cudaError_t launch_compress(const CompressArgs& a, cudaStream_t s);
 cudaError_t launch_index(const IndexArgs& a, int num_sms, cudaStream_t s);
+// bf16 index rows [n][128] -> FP8 plane (ceil(n / 8) blocks of 1056 bytes).
+cudaError_t launch_plane_fp8(const uint16_t* k, int64_t n, uint8_t* plane, cudaStream_t s);
 // One launch for selection `a` and, when b != null, a second selection over the same
 // queries that runs beside it.
 cudaError_t launch_topk(const TopkArgs& a, cudaStream_t s, const TopkArgs* b = nullptr);
@@ -119,6 +126,10 @@ int attn_num_splits(int Q, int nsel, int num_sms);
 
 // 2-D tensor map over `rows` bf16 rows of `cols` elements (row stride cols * 2 bytes),
 // boxes of box_cols x box_rows, 128-byte swizzle, out-of-range elements read as zero.
+// A tensor map over bytes: rank 2 or 3, dims[0] contiguous, strides[i] = byte stride of
+// dims[i + 1]; 128-byte swizzle (box[0] must be 128).
+bool encode_bytes(CUtensorMap* m, const void* base, int rank, const uint64_t* dims,
+                  const uint64_t* strides, const uint32_t* box);
 bool encode_rows_bf16(CUtensorMap* m, const void* base, uint64_t rows, uint32_t cols,
                       uint32_t box_cols, uint32_t box_rows);
 cudaError_t launch_attn(const AttnArgs& a, int nsplit, cudaStream_t s);

@@ -50,6 +50,8 @@ struct IndexWs {
   int nchunk;
   // candidate pool (nbk > 0): merge counters and partial lists of the block selection
   size_t pcount, ppart;
+  // FP8 plane (qrows > 0): the quantised queries and their scales
+  size_t q8, qscale;
   int64_t nb_max;
   int pnchunk;
 };
@@ -71,7 +73,7 @@ int pool_chunks(int64_t nb, int nbk, int Q, int sms) {
   return big;
 }
 
-IndexWs index_ws_layout(int Q, int64_t ld, int k, int nbk = 0) {
+IndexWs index_ws_layout(int Q, int64_t ld, int k, int nbk = 0, int64_t qrows = 0) {
   IndexWs w{};
   size_t o = 0;
   w.keys = o; o = up256(o + (size_t)Q * (size_t)((ld + 3) & ~int64_t(3)) * 4);
@@ -90,6 +92,10 @@ IndexWs index_ws_layout(int Q, int64_t ld, int k, int nbk = 0) {
     w.pcount = o; o = up256(o + (size_t)Q * 4);
     w.ppart = o;
     if (w.pnchunk > 1) o = up256(o + (size_t)Q * w.pnchunk * nbk * 8);
+  }
+  if (qrows > 0) {
+    w.q8 = o; o = up256(o + (size_t)qrows * 128);
+    w.qscale = o; o = up256(o + (size_t)qrows * 4);
   }
   w.total = o;
   return w;
@@ -214,7 +220,7 @@ size_t csa2_index_topk_workspace_size(int Q, int H, int64_t max_scored, int k) {
 namespace {
 
 csa2_status index_topk_impl(const csa2_bf16* iq, const float* w, int Q, int H,
-                            const csa2_bf16* index_k, int64_t index_rows,
+                            const csa2_bf16* index_k, const uint8_t* plane8, int64_t index_rows,
                             const int64_t* row_base, const int32_t* q_seq, const int64_t* q_pos,
                             int ratio, const int32_t* cand, int ncb, int k, int relu,
                             int64_t max_scored, int32_t* sel, float* sel_scores,
@@ -235,13 +241,14 @@ csa2_status index_topk_impl(const csa2_bf16* iq, const float* w, int Q, int H,
           "csa2_index_topk: max_scored %lld exceeds the supported %lld positions",
           (long long)max_scored, (long long)csa2::topk_max_len());
   if (Q == 0) return CSA2_OK;
-  REQUIRE(iq && w && index_k && row_base && q_seq && q_pos && sel && ws,
-          "csa2_index_topk: iq, w, index_k, row_base, q_seq, q_pos, sel and ws are required");
-  REQUIRE(aligned16(iq) && aligned16(index_k), "csa2_index_topk: iq and index_k must be 16-byte aligned");
+  REQUIRE(iq && w && (index_k || plane8) && row_base && q_seq && q_pos && sel && ws,
+          "csa2_index_topk: iq, w, the index plane, row_base, q_seq, q_pos, sel and ws are required");
+  REQUIRE(aligned16(iq) && aligned16(index_k ? (const void*)index_k : (const void*)plane8),
+          "csa2_index_topk: iq and the index plane must be 16-byte aligned");
   REQUIRE(index_rows >= 1 && index_rows < (int64_t)1 << 31, "csa2_index_topk: index_rows out of range");
   REQUIRE((int64_t)Q * H < (int64_t)1 << 31, "csa2_index_topk: Q * H out of range");
   REQUIRE((reinterpret_cast<uintptr_t>(ws) & 255u) == 0, "csa2_index_topk: ws must be 256-byte aligned");
-  const IndexWs L = index_ws_layout(Q, max_scored, k, nbk);
+  const IndexWs L = index_ws_layout(Q, max_scored, k, nbk, plane8 ? (int64_t)Q * H : 0);
   if (ws_bytes < L.total)
     return fail(CSA2_ENOSPACE, "csa2_index_topk: workspace %zu bytes < required %zu", ws_bytes, L.total);
   uint8_t* base = static_cast<uint8_t*>(ws);
@@ -259,6 +266,12 @@ csa2_status index_topk_impl(const csa2_bf16* iq, const float* w, int Q, int H,
   a.topk_count = reinterpret_cast<int32_t*>(base + L.count);
   a.group_max = cand ? 1 : 256 / H;
   if (nbk > 0) a.pool_count = reinterpret_cast<int32_t*>(base + L.pcount);
+  if (plane8) {
+    a.index_k = nullptr;
+    a.plane8 = plane8;
+    a.q8 = base + L.q8;
+    a.qscale = reinterpret_cast<float*>(base + L.qscale);
+  }
   const int sms = num_sms();
   if (sms <= 0) return fail(CSA2_ECUDA, "csa2_index_topk: no CUDA device");
   cudaError_t e = csa2::launch_index(a, sms, stream);
@@ -294,9 +307,9 @@ csa2_status csa2_index_topk(const csa2_bf16* iq, const float* w, int Q, int H,
                             int ratio, const int32_t* cand, int ncb, int k, int relu,
                             int64_t max_scored, int32_t* sel, float* sel_scores,
                             float* scores_out, void* ws, size_t ws_bytes, csa2_stream stream) {
-  return index_topk_impl(iq, w, Q, H, index_k, index_rows, row_base, q_seq, q_pos, ratio, cand,
-                         ncb, k, relu, max_scored, sel, sel_scores, scores_out, 0, nullptr, ws,
-                         ws_bytes, stream);
+  return index_topk_impl(iq, w, Q, H, index_k, nullptr, index_rows, row_base, q_seq, q_pos,
+                         ratio, cand, ncb, k, relu, max_scored, sel, sel_scores, scores_out, 0,
+                         nullptr, ws, ws_bytes, stream);
 }
 
 size_t csa2_index_topk_pool_workspace_size(int Q, int H, int64_t max_scored, int k, int nbk) {
@@ -317,9 +330,44 @@ csa2_status csa2_index_topk_pool(const csa2_bf16* iq, const float* w, int Q, int
           "csa2_index_topk_pool: %lld blocks per row with nbk = %d exceed the block selection",
           (long long)pool_blocks(max_scored), nbk);
   REQUIRE(Q == 0 || pool, "csa2_index_topk_pool: pool is required");
-  return index_topk_impl(iq, w, Q, H, index_k, index_rows, row_base, q_seq, q_pos, ratio,
-                         nullptr, 0, k, relu, max_scored, sel, sel_scores, scores_out, nbk, pool,
+  return index_topk_impl(iq, w, Q, H, index_k, nullptr, index_rows, row_base, q_seq, q_pos,
+                         ratio, nullptr, 0, k, relu, max_scored, sel, sel_scores, scores_out,
+                         nbk, pool, ws, ws_bytes, stream);
+}
+
+size_t csa2_index_topk_fp8_workspace_size(int Q, int H, int64_t max_scored, int k) {
+  if (Q < 0 || (H != 32 && H != 64) || max_scored < 1 || k < 1 || k > 512) return 0;
+  return index_ws_layout(Q, max_scored, k, 0, (int64_t)Q * H).total;
+}
+
+csa2_status csa2_index_topk_fp8(const csa2_bf16* iq, const float* w, int Q, int H,
+                                const uint8_t* plane, int64_t index_rows,
+                                const int64_t* row_base, const int32_t* q_seq,
+                                const int64_t* q_pos, int ratio, const int32_t* cand, int ncb,
+                                int k, int relu, int64_t max_scored, int32_t* sel,
+                                float* sel_scores, float* scores_out, void* ws, size_t ws_bytes,
+                                csa2_stream stream) {
+  REQUIRE(Q == 0 || plane, "csa2_index_topk_fp8: plane is required");
+  return index_topk_impl(iq, w, Q, H, nullptr, plane, index_rows, row_base, q_seq, q_pos, ratio,
+                         cand, ncb, k, relu, max_scored, sel, sel_scores, scores_out, 0, nullptr,
                          ws, ws_bytes, stream);
+}
+
+size_t csa2_index_plane_fp8_bytes(int64_t rows) {
+  return rows <= 0 ? 0 : (size_t)((rows + 7) / 8) * 1056;
+}
+
+csa2_status csa2_index_plane_fp8(const csa2_bf16* index_k, int64_t rows, uint8_t* plane,
+                                 csa2_stream stream) {
+  REQUIRE(rows >= 0 && rows < (int64_t)1 << 34, "csa2_index_plane_fp8: rows out of range");
+  if (rows == 0) return CSA2_OK;
+  REQUIRE(index_k && plane, "csa2_index_plane_fp8: index_k and plane are required");
+  REQUIRE(aligned16(index_k) && aligned16(plane),
+          "csa2_index_plane_fp8: index_k and plane must be 16-byte aligned");
+  cudaError_t e = csa2::launch_plane_fp8(reinterpret_cast<const uint16_t*>(index_k), rows, plane,
+                                         stream);
+  if (e != cudaSuccess) return cuda_fail(e, "csa2_index_plane_fp8");
+  return CSA2_OK;
 }
 
 size_t csa2_topk_workspace_size(int Q, int64_t ld, int k) {
@@ -428,6 +476,24 @@ static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
       fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
   }
   return fn;
+}
+
+bool encode_bytes(CUtensorMap* m, const void* base, int rank, const uint64_t* dims,
+                  const uint64_t* strides, const uint32_t* box) {
+  auto fn = tensor_map_encoder();
+  if (!fn || !base || rank < 2 || rank > 3) return false;
+  cuuint64_t d[3], st[2];
+  cuuint32_t bx[3], es[3] = {1, 1, 1};
+  for (int i = 0; i < rank; ++i) {
+    d[i] = dims[i];
+    bx[i] = box[i];
+    if (dims[i] == 0) return false;
+  }
+  for (int i = 0; i + 1 < rank; ++i) st[i] = strides[i];
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, (cuuint32_t)rank, const_cast<void*>(base), d,
+                  st, bx, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
 }
 
 bool encode_rows_bf16(CUtensorMap* m, const void* base, uint64_t rows, uint32_t cols,

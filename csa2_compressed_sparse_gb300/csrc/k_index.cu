@@ -25,16 +25,21 @@ CSA2_DEFINE_FAULT_FLAG(index)
 namespace csa2 {
 namespace {
 
-constexpr int kStages = 4;
 constexpr int kTileRows = 128;
 constexpr int kThreads = 320;
-constexpr int kStageBytes = kTileRows * kDIdx * 2;  // 32 KiB: two 64-dim blocks
+// K-tile ring: bf16 tiles are 32 KiB (two 64-dim blocks of 128-byte rows), FP8 tiles
+// 16 KiB (one block); both rings hold 128 KiB.
+constexpr int kRingBytes = 4 * kTileRows * kDIdx * 2;
+__host__ __device__ constexpr int stage_bytes(bool fp8) { return fp8 ? kTileRows * kDIdx : kTileRows * kDIdx * 2; }
+__host__ __device__ constexpr int num_stages(bool fp8) { return kRingBytes / stage_bytes(fp8); }
+constexpr int kMaxStages = num_stages(true);
 constexpr int kBBytes = 2 * 256 * 128;              // 64 KiB: two 64-dim blocks x 256 rows
 constexpr int kMaxGroup = 8;
+constexpr int kFp8BlockBytes = 8 * kDIdx + 8 * 4;   // 1056: 8 rows of codes, 8 scales
 
 struct __align__(8) Bars {
-  uint64_t full[kStages];
-  uint64_t empty[kStages];
+  uint64_t full[kMaxStages];
+  uint64_t empty[kMaxStages];
   uint64_t acc_full[2];
   uint64_t acc_empty[2];
   uint64_t b_full;
@@ -114,6 +119,8 @@ __global__ void __launch_bounds__(kPrepThreads) index_prep_kernel(IndexArgs a) {
         }
         s_seq[i] = a.q_seq[q];
         s_ns[i] = (int)ns;
+        if (a.plane8 && i < kPrepThreads && (a.row_base[s_seq[i]] & 7) != 0)
+          raise_fault(kFaultBounds);  // FP8 planes start every sequence on a block
         if (i < kPrepThreads) {
           a.n_scored[q] = (int32_t)ns;
           a.topk_count[q] = 0;
@@ -194,6 +201,85 @@ __device__ __forceinline__ void load_group(const IndexArgs& a, int g, GroupInfo&
   gi.rb = a.row_base[gi.seq];
 }
 
+// ---- FP8 quantisation: [A] indexer figure (FP8 rows of 128 E4M3 codes with one fp32
+//      scale; the query quantised per (token, head)); [E] indexer compressor ("row amax
+//      -> ue8m0 -> e4m3") ----------------------------------------------------------------
+
+// Exponent of the power-of-two scale of a group whose largest magnitude is amax: the
+// smallest e with amax <= 448 * 2^e (448 = 1.75 * 2^8, the largest E4M3 value), read off
+// the bits of amax; 0 for amax == 0.
+__device__ __forceinline__ int ue8m0_exp(float amax) {
+  const uint32_t u = __float_as_uint(amax);
+  if (u == 0u) return 0;
+  int E;
+  uint32_t m;
+  if ((u >> 23) != 0u) {
+    E = (int)(u >> 23) - 127;
+    m = u & 0x7FFFFFu;
+  } else {  // subnormal: normalise the fraction
+    const int p = 31 - __clz((int)u);
+    E = p - 149;
+    m = (u << (23 - p)) & 0x7FFFFFu;
+  }
+  return E - 8 + (m > 0x600000u ? 1 : 0);
+}
+
+// One warp quantises one row of 128 bf16 values (live == false: a row of zeros); lane l
+// returns the codes of values 4l .. 4l+3 as one word.  Returns the row's scale 2^e.
+// Dividing by 2^e is exact (two power-of-two factors keep each one a normal float).
+__device__ __forceinline__ float quant_row_e4m3(const uint16_t* src, bool live, uint32_t& codes) {
+  const int lane = threadIdx.x & 31;
+  float v[4] = {0.f, 0.f, 0.f, 0.f};
+  if (live) {
+    const uint2 r = __ldg(reinterpret_cast<const uint2*>(src) + lane);
+    v[0] = __uint_as_float(r.x << 16); v[1] = __uint_as_float(r.x & 0xFFFF0000u);
+    v[2] = __uint_as_float(r.y << 16); v[3] = __uint_as_float(r.y & 0xFFFF0000u);
+  }
+  float amax = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
+  const int e = ue8m0_exp(amax);
+  int ne = -e;
+  float f1 = 1.f;
+  if (ne > 100) { f1 = __uint_as_float((100u + 127u) << 23); ne -= 100; }
+  const float f2 = __uint_as_float((uint32_t)(ne + 127) << 23);
+  const uint32_t c01 = cvt_e4m3x2(v[0] * f1 * f2, v[1] * f1 * f2);
+  const uint32_t c23 = cvt_e4m3x2(v[2] * f1 * f2, v[3] * f1 * f2);
+  codes = c01 | (c23 << 16);
+  return e >= -126 ? __uint_as_float((uint32_t)(e + 127) << 23)
+                   : __uint_as_float(1u << (e + 149));
+}
+
+// One CTA per block of the FP8 plane: warp w quantises row 8 * blockIdx.x + w.
+__global__ void __launch_bounds__(256) plane_fp8_kernel(const uint16_t* k, int64_t n,
+                                                        uint8_t* plane) {
+  griddep_launch_dependents();
+  griddep_wait();
+  const int lane = threadIdx.x & 31;
+  const int64_t r = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+  uint32_t codes;
+  const float sc = quant_row_e4m3(k + (r < n ? r : 0) * kDIdx, r < n, codes);
+  uint8_t* blk = plane + (int64_t)blockIdx.x * kFp8BlockBytes;
+  reinterpret_cast<uint32_t*>(blk + (r & 7) * kDIdx)[lane] = codes;
+  if (lane == 0) reinterpret_cast<float*>(blk + 8 * kDIdx)[r & 7] = sc;
+}
+
+// The queries of an FP8 index call: row q * H + h -> codes [128] and a scale.
+__global__ void __launch_bounds__(256) quant_q_kernel(IndexArgs a) {
+  griddep_launch_dependents();
+  griddep_wait();
+  const int lane = threadIdx.x & 31;
+  const int64_t r = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (r >= (int64_t)a.Q * a.H) return;
+  uint32_t codes;
+  const float sc = quant_row_e4m3(a.iq + r * kDIdx, true, codes);
+  reinterpret_cast<uint32_t*>(a.q8 + r * kDIdx)[lane] = codes;
+  if (lane == 0) a.qscale[r] = sc;
+}
+
+// kFp8: K tiles and queries are E4M3 codes (tcgen05 kind::f8f6f4, K = 32 per MMA); the
+// row scale of K and the query scales multiply the head sum in the epilogue.
+template <bool kFp8>
 __global__ void __launch_bounds__(kThreads, 1)
     index_score_kernel(IndexArgs a, const __grid_constant__ CUtensorMap kmap_tile,
                        const __grid_constant__ CUtensorMap kmap_blk,
@@ -201,8 +287,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
-  uint8_t* a_smem = smem;                              // kStages x 32 KiB
-  uint8_t* b_smem = smem + kStages * kStageBytes;      // 64 KiB
+  constexpr int kStages = num_stages(kFp8);
+  constexpr int kStageBytes = stage_bytes(kFp8);
+  uint8_t* a_smem = smem;                              // the K-tile ring, 128 KiB
+  uint8_t* b_smem = smem + kRingBytes;                 // 64 KiB
   float* w_all = reinterpret_cast<float*>(b_smem + kBBytes);  // [8][256], per epilogue warp
   Bars* bars = reinterpret_cast<Bars*>(w_all + 8 * 256);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 1);
@@ -282,11 +370,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (it == it_lo || it == gi.tile0) {  // new group: load its Q block
           if (u > 0 && !mbar_wait(smem_u32(&bars->b_empty), (u - 1) & 1)) { *abort_flag = 1; break; }
           const uint32_t bb = smem_u32(&bars->b_full);
-          mbar_arrive_expect_tx(bb, (uint32_t)(gi.nq * a.H * kDIdx * 2));
-          for (int i = 0; i < gi.nq; ++i)
-            for (int db = 0; db < 2; ++db)
-              tma_load_2d(smem_u32(b_smem + db * 32768 + i * a.H * 128), &qmap, db * 64,
-                          (gi.q0 + i) * a.H, bb, pol_q);
+          mbar_arrive_expect_tx(bb, (uint32_t)(gi.nq * a.H * kDIdx * (kFp8 ? 1 : 2)));
+          for (int i = 0; i < gi.nq; ++i) {
+            if (kFp8) {
+              tma_load_2d(smem_u32(b_smem + i * a.H * 128), &qmap, 0, (gi.q0 + i) * a.H, bb,
+                          pol_q);
+            } else {
+              for (int db = 0; db < 2; ++db)
+                tma_load_2d(smem_u32(b_smem + db * 32768 + i * a.H * 128), &qmap, db * 64,
+                            (gi.q0 + i) * a.H, bb, pol_q);
+            }
+          }
           ++u;
         }
         const int64_t k = it - it_lo;
@@ -298,7 +392,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         issued[s] = round;
         const int64_t tile = it - gi.tile0;
         uint8_t* dst = a_smem + s * kStageBytes;
-        if (!a.cand) {
+        if (kFp8) {
+          // block (row_base + 128 * tile) / 8 .. + 15, as [16][8 rows][128 B]; REINDEX:
+          // one box per candidate block
+          const int64_t b0 = gi.rb >> 3;
+          if (!a.cand) {
+            tma_load_3d(smem_u32(dst), &kmap_tile, 0, 0, (int32_t)(b0 + tile * 16), fb, pol_k);
+          } else {
+            const int32_t* cb = a.cand + (int64_t)gi.q0 * a.ncb + tile * 16;
+            int32_t blk[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) blk[i] = tile * 16 + i < a.ncb ? __ldg(cb + i) : -1;
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+              tma_load_3d(smem_u32(dst + i * 1024), &kmap_blk, 0, 0,
+                          (int32_t)(b0 + (blk[i] >= 0 ? blk[i] : 0)), fb, pol_k);
+          }
+        } else if (!a.cand) {
           const int32_t y = (int32_t)(gi.rb + tile * kTileRows);
           for (int db = 0; db < 2; ++db)
             tma_load_2d(smem_u32(dst + db * 16384), &kmap_tile, db * 64, y, fb, pol_k);
@@ -339,7 +449,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (it == it_lo || it == gi.tile0) {
           if (!mbar_wait(smem_u32(&bars->b_full), u & 1)) { *abort_flag = 1; break; }
           ++u;
-          idesc = idesc_bf16(128, gi.nq * a.H, 0, 0);
+          idesc = kFp8 ? idesc_e4m3(128, gi.nq * a.H) : idesc_bf16(128, gi.nq * a.H, 0, 0);
         }
         const int64_t k = it - it_lo;
         const int s = (int)(k % kStages);
@@ -352,14 +462,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t a_base = smem_u32(a_smem + s * kStageBytes);
         const uint32_t b_base = smem_u32(b_smem);
         const uint32_t d = tmem + (uint32_t)(ab * 256);
+        if (kFp8) {
 #pragma unroll
-        for (int db = 0; db < 2; ++db)
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            const uint64_t ad = sdesc_sw128(a_base + db * 16384 + kk * 32, 16, 1024);
-            const uint64_t bd = sdesc_sw128(b_base + db * 32768 + kk * 32, 16, 1024);
-            umma_bf16(d, ad, bd, idesc, (db | kk) != 0);
+          for (int kk = 0; kk < 4; ++kk) {  // 4 x K = 32 codes, 32 bytes apart
+            const uint64_t ad = sdesc_sw128(a_base + kk * 32, 16, 1024);
+            const uint64_t bd = sdesc_sw128(b_base + kk * 32, 16, 1024);
+            umma_f8(d, ad, bd, idesc, kk != 0);
           }
+        } else {
+#pragma unroll
+          for (int db = 0; db < 2; ++db)
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+              const uint64_t ad = sdesc_sw128(a_base + db * 16384 + kk * 32, 16, 1024);
+              const uint64_t bd = sdesc_sw128(b_base + db * 32768 + kk * 32, 16, 1024);
+              umma_bf16(d, ad, bd, idesc, (db | kk) != 0);
+            }
+        }
         umma_commit(smem_u32(&bars->empty[s]));
         umma_commit(smem_u32(&bars->acc_full[ab]));
         if (it + 1 == it_hi || it + 1 == gi.tile1) umma_commit(smem_u32(&bars->b_empty));
@@ -392,6 +511,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         float wv[8];
 #pragma unroll
         for (int u = 0; u < 8; ++u) wv[u] = lane + 32 * u < nw ? __ldg(wg + lane + 32 * u) : 0.f;
+        if (kFp8) {  // the queries' power-of-two scales fold into the weights exactly
+          const float* qs = a.qscale + (int64_t)gi.q0 * a.H;
+#pragma unroll
+          for (int u = 0; u < 8; ++u)
+            if (lane + 32 * u < nw) wv[u] *= __ldg(qs + lane + 32 * u);
+        }
         int64_t lim = 0;
         if (lane < gi.nq)
           lim = a.cand ? n_visible(a.q_pos[gi.q0 + lane], a.ratio)
@@ -411,6 +536,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       // REINDEX groups hold one query: fetch its candidate block id before the wait
       const int32_t cblk = a.cand && (pos >> 3) < a.ncb
                                ? __ldg(a.cand + (int64_t)gi.q0 * a.ncb + (pos >> 3)) : -1;
+      // FP8: this row's scale, from its block's tail (rows of a group share it)
+      float sk = 1.f;
+      if (kFp8) {
+        const int64_t row = !a.cand ? gi.rb + pos
+                                    : (cblk >= 0 ? gi.rb + (int64_t)cblk * 8 + (pos & 7) : -1);
+        if (row >= 0 && row < a.index_rows)
+          sk = __ldg(reinterpret_cast<const float*>(a.plane8 + (row >> 3) * kFp8BlockBytes +
+                                                    8 * kDIdx) + (row & 7));
+      }
       if (!__all_sync(0xFFFFFFFFu, mbar_wait(smem_u32(&bars->acc_full[eg]), use & 1))) {
         *abort_flag = 1;
         break;
@@ -457,7 +591,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             acc[2] = fmaf(wa.z, x2, acc[2]); acc[3] = fmaf(wa.w, x3, acc[3]);
           }
         }
-        const float score = (acc[0] + acc[1]) + (acc[2] + acc[3]);
+        const float score = ((acc[0] + acc[1]) + (acc[2] + acc[3])) * sk;
         const int q = gi.q0 + i;
         bool valid;
         if (!a.cand) {
@@ -485,8 +619,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 }  // namespace
 
 size_t index_smem_bytes() {
-  return 1024 + kStages * kStageBytes + kBBytes + 8 * 256 * 4 + sizeof(Bars) + 16 +
-         8 * 8 * kMaxGroup;
+  return 1024 + kRingBytes + kBBytes + 8 * 256 * 4 + sizeof(Bars) + 16 + 8 * 8 * kMaxGroup;
 }
 
 cudaError_t launch_index(const IndexArgs& a, int num_sms, cudaStream_t s) {
@@ -494,15 +627,39 @@ cudaError_t launch_index(const IndexArgs& a, int num_sms, cudaStream_t s) {
   cudaError_t e = launch_pdl(index_prep_kernel, dim3(1), dim3(kPrepThreads), 0, s, a);
   if (e != cudaSuccess) return e;
   CUtensorMap kt, kb, qm;
-  if (!encode_rows_bf16(&kt, a.index_k, (uint64_t)a.index_rows, kDIdx, 64, kTileRows) ||
-      !encode_rows_bf16(&kb, a.index_k, (uint64_t)a.index_rows, kDIdx, 64, 8) ||
-      !encode_rows_bf16(&qm, a.iq, (uint64_t)a.Q * a.H, kDIdx, 64, (uint32_t)a.H))
+  const bool f8 = a.plane8 != nullptr;
+  if (f8) {
+    const int64_t qrows = (int64_t)a.Q * a.H;
+    e = launch_pdl(quant_q_kernel, dim3((unsigned)((qrows + 7) / 8)), dim3(256), 0, s, a);
+    if (e != cudaSuccess) return e;
+    // the plane as [blocks][8 rows][128 B] (scales skipped by the block stride)
+    const uint64_t dims[3] = {(uint64_t)kDIdx, 8, (uint64_t)((a.index_rows + 7) / 8)};
+    const uint64_t strides[2] = {(uint64_t)kDIdx, (uint64_t)kFp8BlockBytes};
+    const uint32_t box_t[3] = {(uint32_t)kDIdx, 8, kTileRows / 8};
+    const uint32_t box_b[3] = {(uint32_t)kDIdx, 8, 1};
+    const uint64_t qd[2] = {(uint64_t)kDIdx, (uint64_t)qrows};
+    const uint64_t qs[1] = {(uint64_t)kDIdx};
+    const uint32_t qbox[2] = {(uint32_t)kDIdx, (uint32_t)a.H};
+    if (!encode_bytes(&kt, a.plane8, 3, dims, strides, box_t) ||
+        !encode_bytes(&kb, a.plane8, 3, dims, strides, box_b) ||
+        !encode_bytes(&qm, a.q8, 2, qd, qs, qbox))
+      return cudaErrorInvalidValue;
+  } else if (!encode_rows_bf16(&kt, a.index_k, (uint64_t)a.index_rows, kDIdx, 64, kTileRows) ||
+             !encode_rows_bf16(&kb, a.index_k, (uint64_t)a.index_rows, kDIdx, 64, 8) ||
+             !encode_rows_bf16(&qm, a.iq, (uint64_t)a.Q * a.H, kDIdx, 64, (uint32_t)a.H)) {
     return cudaErrorInvalidValue;
+  }
   const size_t smem = index_smem_bytes();
-  e = cudaFuncSetAttribute(index_score_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)smem);
+  auto kern = f8 ? index_score_kernel<true> : index_score_kernel<false>;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  return launch_pdl(index_score_kernel, dim3(num_sms), dim3(kThreads), smem, s, a, kt, kb, qm);
+  return launch_pdl(kern, dim3(num_sms), dim3(kThreads), smem, s, a, kt, kb, qm);
+}
+
+cudaError_t launch_plane_fp8(const uint16_t* k, int64_t n, uint8_t* plane, cudaStream_t s) {
+  if (n <= 0) return cudaSuccess;
+  const int64_t nb = (n + 7) / 8;
+  return launch_pdl(plane_fp8_kernel, dim3((unsigned)nb), dim3(256), 0, s, k, n, plane);
 }
 
 }  // namespace csa2

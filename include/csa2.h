@@ -162,6 +162,44 @@ csa2_status csa2_index_topk_pool(const csa2_bf16* iq, const float* w, int Q, int
                                  size_t ws_bytes, csa2_stream stream);
 
 /* ---------------------------------------------------------------------------------
+ * csa2_index_plane_fp8 -- the FP8 index plane.  [A] indexer figure (FP8 index rows of
+ * 132 B: 128 E4M3 codes and one fp32 scale; blocks of 8 rows with the values first and
+ * the scales at the block tail); [E] indexer compressor (row amax -> ue8m0 -> e4m3).
+ *
+ * Row r of index_k [rows][128] bf16 is quantised with the scale s = 2^e, the smallest
+ * power of two with max_d |x_d| / s <= 448 (s = 1 for an all-zero row), into codes
+ * E4M3(x_d / s) (nearest, ties to even).  Block b = r / 8 of the plane holds, at byte
+ * 1056 * b, the codes of rows 8b .. 8b+7 (128 bytes each) and then their 8 scales as
+ * fp32.  Rows of the last block past `rows` are zero with scale 1.
+ *   plane  csa2_index_plane_fp8_bytes(rows) bytes, 16-byte aligned */
+size_t csa2_index_plane_fp8_bytes(int64_t rows);
+csa2_status csa2_index_plane_fp8(const csa2_bf16* index_k, int64_t rows, uint8_t* plane,
+                                 csa2_stream stream);
+
+/* ---------------------------------------------------------------------------------
+ * csa2_index_topk_fp8 -- csa2_index_topk on an FP8 index plane.  [A] indexer figure
+ * (FP8 plane; the query quantised per (token, head), its fp32 scale folded into w).
+ *
+ * Each query row iq[q][h] is quantised like a plane row (scale sq_qh, codes cq); with
+ * plane row c of sequence b = the row row_base[b] + c of the plane (codes ck_c, scale
+ * sk_c),
+ *     s(c) = alpha * sum_h w[q][h] * relu(sq_qh * sk_c * <E4M3(cq_qh), E4M3(ck_c)>)
+ * on the tensor cores (E4M3 x E4M3 products, fp32 sums); everything else (visibility,
+ * REINDEX, selection, outputs, errors) as csa2_index_topk.
+ *   plane      csa2_index_plane_fp8 layout holding index_rows rows; every row_base[b]
+ *              must be a multiple of 8 (each sequence starts on a block; a query of a
+ *              sequence that does not raises CSA2_EBOUNDS)
+ *   ws         csa2_index_topk_fp8_workspace_size(Q, H, max_scored, k) bytes */
+size_t csa2_index_topk_fp8_workspace_size(int Q, int H, int64_t max_scored, int k);
+csa2_status csa2_index_topk_fp8(const csa2_bf16* iq, const float* w, int Q, int H,
+                                const uint8_t* plane, int64_t index_rows,
+                                const int64_t* row_base, const int32_t* q_seq,
+                                const int64_t* q_pos, int ratio, const int32_t* cand, int ncb,
+                                int k, int relu, int64_t max_scored, int32_t* sel,
+                                float* sel_scores, float* scores_out, void* ws, size_t ws_bytes,
+                                csa2_stream stream);
+
+/* ---------------------------------------------------------------------------------
  * csa2_index_topk_noalloc -- the paper has no counterpart: this is a library service.
  *
  * Same arguments and results as csa2_index_topk, minus the workspace.  It is for
