@@ -539,6 +539,16 @@ def run_stages(args):
         res["index_topk_pool"] = timed(lambda: csa2.csa2_index_topk_pool(
             t["iq"], t["w"], t["index_k"], t["row_base"], t["q_seq"], t["q_pos"], spec.ratio,
             spec.k, spec.max_scored, buf.sel, pool, pws, sel_scores=buf.sel_scores))
+    # the FP8 index plane (NEXT-3): sequences re-laid on 8-row blocks, quantised once
+    from csa2_compressed_sparse_gb300.step import fp8_index_plane
+    plane8, rb8, rows8 = fp8_index_plane(t["index_k"], wl.row_base, wl.n_rows)
+    ws8 = torch.empty(csa2.csa2_index_topk_fp8_workspace_size(wl.Q, spec.H, spec.max_scored,
+                                                               spec.k),
+                      dtype=torch.uint8, device="cuda")
+    sel8 = torch.empty_like(buf.sel)
+    res["index_topk_fp8"] = timed(lambda: csa2.csa2_index_topk_fp8(
+        t["iq"], t["w"], plane8, rows8, rb8, t["q_seq"], t["q_pos"], spec.ratio, spec.k,
+        spec.max_scored, sel8, ws8, cand=cand))
     res["sparse_attn"] = timed(lambda: csa2.csa2_sparse_attn(
         t["q"][0], t["q_seq"], t["q_pos"], swa0, t["plane"], t["row_base"], buf.sel, t["sink"],
         buf.out[0], scale=spec.scale, ws=buf.attn_ws))

@@ -112,3 +112,25 @@ def run_step(spec: StepSpec, t, buf: StepBuffers, stream=None, compress=True, si
         fn(t["q"][layer], t["q_seq"], t["q_pos"], swa_of(spec, t, layer), t["plane"],
            t["row_base"], buf.sel, t["sink"], buf.out[layer], lse=buf.lse[layer],
            scale=spec.scale, ws=buf.attn_ws, stream=main)
+
+
+def fp8_index_plane(index_k, row_base, n_rows):
+    """The FP8 index plane of bf16 index rows held per sequence at row_base[b] (host
+    int sequences n_rows / row_base): every sequence is re-laid to start on an 8-row
+    block, then quantised on the device.  Returns (plane, block-aligned row_base on the
+    device, rows in the plane)."""
+    import numpy as np
+    import torch
+    from . import csa2_index_plane_fp8, csa2_index_plane_fp8_bytes
+    n = np.asarray(n_rows, dtype=np.int64)
+    padded = (n + 7) // 8 * 8
+    rb8 = np.concatenate([[0], np.cumsum(padded)[:-1]]).astype(np.int64)
+    total = max(int(padded.sum()), 8)
+    kpad = torch.zeros((total, index_k.shape[1]), dtype=index_k.dtype, device=index_k.device)
+    for b in range(len(n)):
+        r0 = int(row_base[b])
+        kpad[int(rb8[b]):int(rb8[b]) + int(n[b])] = index_k[r0:r0 + int(n[b])]
+    plane = torch.empty(csa2_index_plane_fp8_bytes(total), dtype=torch.uint8,
+                        device=index_k.device)
+    csa2_index_plane_fp8(kpad, plane)
+    return plane, torch.from_numpy(rb8).to(index_k.device), total

@@ -24,21 +24,11 @@ def _gpu():
 def fp8_plane_of(wl, t):
     """The workload's index rows re-laid so that every sequence starts on an 8-row block,
     quantised on the device.  Returns (plane, row_base, rows)."""
-    from csa2_compressed_sparse_gb300 import (csa2_device_status, csa2_index_plane_fp8,
-                                              csa2_index_plane_fp8_bytes)
-    n = wl.n_rows.astype(np.int64)
-    padded = (n + 7) // 8 * 8
-    rb8 = np.concatenate([[0], np.cumsum(padded)[:-1]]).astype(np.int64)
-    total = int(padded.sum())
-    kpad = torch.zeros((max(total, 8), 128), dtype=torch.bfloat16, device="cuda")
-    for b in range(wl.B):
-        r0 = int(wl.row_base[b])
-        kpad[rb8[b]:rb8[b] + n[b]] = t["index_k"][r0:r0 + n[b]]
-    plane = torch.empty(csa2_index_plane_fp8_bytes(kpad.shape[0]), dtype=torch.uint8,
-                        device="cuda")
-    csa2_index_plane_fp8(kpad, plane)
+    from csa2_compressed_sparse_gb300 import csa2_device_status
+    from csa2_compressed_sparse_gb300.step import fp8_index_plane
+    out = fp8_index_plane(t["index_k"], wl.row_base, wl.n_rows)
     csa2_device_status()
-    return plane, torch.from_numpy(rb8).cuda(), kpad.shape[0]
+    return out
 
 
 def run_fp8(wl, t, plane, rb8, rows, cand=None):
