@@ -171,9 +171,14 @@ __device__ __forceinline__ void rope_table(const float* inv_freq, int64_t p, int
   rs[lane] = s;
 }
 
-// O^T tiles mt0 .. mt0 + ntile - 1 from TMEM into shared memory as fp32 rows of 64 heads
-// (256 B per dim), 16-byte pieces swizzled by the dim (piece c of row d at c ^ (d & 15));
-// row = dim - 128 mt0.  Warps 0..3 (TMEM lanes 32 w ..); with n == 0 the tiles are zero.
+// Staged O^T rows: fp32, 64 heads per dim (256 B), 16-byte pieces of 4 heads; piece c
+// of row d sits at position c ^ ot_swz(d), which keeps both the writer (32 consecutive
+// dims, one piece each) and the reader (eight consecutive dims per thread, threads eight
+// dims apart) free of bank conflicts.
+__device__ __forceinline__ int ot_swz(int d) { return (d ^ (d >> 3)) & 7; }
+
+// O^T tiles mt0 .. mt0 + ntile - 1 from TMEM into shared memory as staged rows; row =
+// dim - 128 mt0.  Warps 0..3 (TMEM lanes 32 w ..); with n == 0 the tiles are zero.
 __device__ __forceinline__ void stage_ot(uint32_t tmem_o, int warp, int lane, int mt0, int ntile,
                                          uint32_t stage, bool have) {
   const uint32_t lrow = (uint32_t)(warp * 32) << 16;
@@ -181,6 +186,7 @@ __device__ __forceinline__ void stage_ot(uint32_t tmem_o, int warp, int lane, in
   for (int mi = 0; mi < ntile; ++mi) {
     const int d = mi * 128 + warp * 32 + lane;
     const uint32_t row = stage + d * 256;
+    const int sw = ot_swz(d);
 #pragma unroll 1
     for (int hb = 0; hb < 64; hb += 32) {
       uint32_t v[32];
@@ -194,7 +200,7 @@ __device__ __forceinline__ void stage_ot(uint32_t tmem_o, int warp, int lane, in
 #pragma unroll
       for (int j4 = 0; j4 < 8; ++j4) {
         const int c = (hb >> 2) + j4;  // heads 4c .. 4c + 3
-        st_shared16(row + ((c ^ (d & 15)) << 4),
+        st_shared16(row + ((c ^ sw) << 4),
                     make_uint4(v[4 * j4], v[4 * j4 + 1], v[4 * j4 + 2], v[4 * j4 + 3]));
       }
     }
@@ -202,39 +208,57 @@ __device__ __forceinline__ void stage_ot(uint32_t tmem_o, int warp, int lane, in
 }
 
 // out[q][h][dbase + d] = bf16(own[d][h] w0[h] + peer[d][h] w1[h]) for nd dims, from rows
-// staged by stage_ot (peer may be null); all threads of the CTA, 16-byte stores of eight
-// dims of one head, a warp covering 32 heads of one group of eight dims.  With rc / rs
-// (cos, sin of p theta_i), pair i of dims 448.. is rotated back: times e^{-i p theta_i}.
+// staged by stage_ot (peer may be null), by threads tid of nthreads.  A thread takes four
+// heads x eight dims (eight 16-byte loads from each source) and stores four 16-byte runs;
+// a warp covers consecutive dim groups of the same four heads, so each store is one
+// contiguous 512-byte run per head.  With rc / rs (cos, sin of p theta_i), pair i of
+// dims 448.. is rotated back: times e^{-i p theta_i}.
 __device__ __forceinline__ void out_pass(const float* own, const float* peer, const float* w0,
                                          const float* w1, const float* rc, const float* rs,
-                                         uint16_t* out_q, int nd, int dbase, int warp, int lane,
-                                         int nwarps) {
-  const int items = 2 * (nd >> 3);  // (head half, group of 8 dims)
-  for (int it = warp; it < items; it += nwarps) {
-    const int h = 32 * (it & 1) + lane, dg = it >> 1;
-    const float a = w0[h], b = peer ? w1[h] : 0.f;
-    const int gd = dbase + dg * 8;  // first output dim of the group
-    uint32_t pk[4];
+                                         uint16_t* out_q, int nd, int dbase, int tid,
+                                         int nthreads) {
+  const int ng = nd >> 3;  // groups of eight dims
+  for (int it = tid; it < 16 * ng; it += nthreads) {
+    const int c = it / ng, g = it - c * ng;
+    float wa[4], wb[4];
 #pragma unroll
-    for (int k = 0; k < 8; k += 2) {
-      float o[2];
-#pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        const int d = dg * 8 + k + e;
-        const int idx = d * 64 + ((((h >> 2) ^ (d & 15))) << 2) + (h & 3);
-        o[e] = own[idx] * a + (peer ? peer[idx] * b : 0.f);
-      }
-      if (rc && gd >= kRopeDim0) {
-        const int i = (gd + k - kRopeDim0) >> 1;
-        const float c = rc[i], s = rs[i];
-        const float o0 = o[0] * c + o[1] * s, o1 = o[1] * c - o[0] * s;
-        o[0] = o0;
-        o[1] = o1;
-      }
-      pk[k >> 1] = pack_bf16x2(o[0], o[1]);
+    for (int hh = 0; hh < 4; ++hh) {
+      wa[hh] = w0[4 * c + hh];
+      wb[hh] = peer ? w1[4 * c + hh] : 0.f;
     }
-    *reinterpret_cast<uint4*>(out_q + h * kDLat + dbase + dg * 8) =
-        make_uint4(pk[0], pk[1], pk[2], pk[3]);
+    float o[4][8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int d = 8 * g + j;
+      const int off = d * 64 + ((c ^ ot_swz(d)) << 2);
+      const float4 x = *reinterpret_cast<const float4*>(own + off);
+      float4 y = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (peer) y = *reinterpret_cast<const float4*>(peer + off);
+      o[0][j] = x.x * wa[0] + y.x * wb[0];
+      o[1][j] = x.y * wa[1] + y.y * wb[1];
+      o[2][j] = x.z * wa[2] + y.z * wb[2];
+      o[3][j] = x.w * wa[3] + y.w * wb[3];
+    }
+    const int gd = dbase + 8 * g;  // first output dim of the group
+    if (rc && gd >= kRopeDim0) {
+#pragma unroll
+      for (int j = 0; j < 8; j += 2) {
+        const int i = (gd + j - kRopeDim0) >> 1;
+        const float cs = rc[i], sn = rs[i];
+#pragma unroll
+        for (int hh = 0; hh < 4; ++hh) {
+          const float o0 = o[hh][j] * cs + o[hh][j + 1] * sn;
+          const float o1 = o[hh][j + 1] * cs - o[hh][j] * sn;
+          o[hh][j] = o0;
+          o[hh][j + 1] = o1;
+        }
+      }
+    }
+#pragma unroll
+    for (int hh = 0; hh < 4; ++hh)
+      *reinterpret_cast<uint4*>(out_q + (4 * c + hh) * kDLat + gd) =
+          make_uint4(pack_bf16x2(o[hh][0], o[hh][1]), pack_bf16x2(o[hh][2], o[hh][3]),
+                     pack_bf16x2(o[hh][4], o[hh][5]), pack_bf16x2(o[hh][6], o[hh][7]));
   }
 }
 
@@ -628,7 +652,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     out_pass(reinterpret_cast<const float*>(kv_s), nullptr, X.fac[0], nullptr,
              a.inv_freq ? X.rope_c : nullptr, X.rope_s, a.out + (int64_t)q * kHeads * kDLat,
-             kDLat, 0, warp, lane, kThreads / 32);
+             kDLat, 0, tid, kThreads);
     if (a.lse && tid < 64)
       a.lse[(int64_t)q * kHeads + tid] =
           (X.m_run[tid] + __log2f(X.l_run[tid])) * 0.6931471805599453f;
@@ -675,7 +699,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     out_pass(reinterpret_cast<const float*>(q_s), reinterpret_cast<const float*>(kv_s), X.fac[0],
              X.fac[1], a.inv_freq ? X.rope_c : nullptr, X.rope_s,
-             a.out + (int64_t)q * kHeads * kDLat, 256, 256 * rank, warp, lane, kThreads / 32);
+             a.out + (int64_t)q * kHeads * kDLat, 256, 256 * rank, tid, kThreads);
     // both CTAs have received their rows, so no copy touches either one's shared memory
     // any more when they exit
     cluster_sync();

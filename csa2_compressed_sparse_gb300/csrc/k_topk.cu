@@ -159,9 +159,10 @@ struct RowSrc {
 
 // Exact top-k of src[0..n) (n <= kChunkLen): emit(o, i) is called once for each selected
 // index i, with o = its place in ascending order (0 .. keff - 1), by some thread of the
-// CTA.  Returns keff = min(k, #scored).
+// CTA.  Returns keff = min(k, #scored).  dense: every key of src[0..n) is nonzero.
 template <int kKind, typename Emit>
-__device__ int select_topk(const RowSrc<kKind>& src, int n, int k, SelectSmem& S, Emit emit) {
+__device__ int select_topk(const RowSrc<kKind>& src, int n, int k, bool dense, SelectSmem& S,
+                           Emit emit) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int nw = (n + 31) >> 5;
   // ---- 1. clear ----
@@ -205,7 +206,10 @@ __device__ int select_topk(const RowSrc<kKind>& src, int n, int k, SelectSmem& S
     }
   }
   // ---- 3. filter: keep keys >= thr, count scored positions ----
-  // Warp w appends to its own region [w * kWarpCap, ...) through its shared counter.
+  // A lane tests its four keys at once (their maximum); only the lanes holding a kept
+  // key take a run of slots in the warp's region [w * kWarpCap, ...) with one shared
+  // atomic and add their keys' top bits to the histogram.  A dense segment (every
+  // position scored) needs no count.
   int nval = 0;
   uint32_t* wkey = S.ckey + warp * kWarpCap;
   uint32_t* widx = S.cidx + warp * kWarpCap;
@@ -213,26 +217,31 @@ __device__ int select_topk(const RowSrc<kKind>& src, int n, int k, SelectSmem& S
   for (int u = 0; u < kU; ++u) {
     const int g = warp * 32 + u * kTopkThreads + lane;
     const uint4 vv = src.load4(g, n);
-    const uint32_t kk[4] = {vv.x, vv.y, vv.z, vv.w};
+    if (!dense) nval += (vv.x != 0u) + (vv.y != 0u) + (vv.z != 0u) + (vv.w != 0u);
+    if (max(max(vv.x, vv.y), max(vv.z, vv.w)) >= thr) {  // thr >= 1: never an unscored key
+      const uint32_t kk[4] = {vv.x, vv.y, vv.z, vv.w};
+      const int cnt = (kk[0] >= thr) + (kk[1] >= thr) + (kk[2] >= thr) + (kk[3] >= thr);
+      int slot = atomicAdd(&S.wcnt[warp], cnt);
 #pragma unroll
-    for (int jj = 0; jj < 4; ++jj) {
-      const uint32_t key = kk[jj];
-      nval += key != 0u;
-      if (key >= thr) {  // thr >= 1: unscored keys are never kept
-        const int slot = atomicAdd(&S.wcnt[warp], 1);
-        if (slot < kWarpCap) { wkey[slot] = key; widx[slot] = (uint32_t)(4 * g + jj); }
-        atomicAdd(&S.hist_kept[key >> 21], 1u);
+      for (int jj = 0; jj < 4; ++jj) {
+        if (kk[jj] >= thr) {
+          if (slot < kWarpCap) { wkey[slot] = kk[jj]; widx[slot] = (uint32_t)(4 * g + jj); }
+          ++slot;
+          atomicAdd(&S.hist_kept[kk[jj] >> 21], 1u);
+        }
       }
     }
   }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) nval += __shfl_xor_sync(0xFFFFFFFFu, nval, o);
-  if (lane == 0) atomicAdd(&S.nvalid, nval);
   __syncwarp();
-  if (lane == 0) {
-    const int wc = S.wcnt[warp];
-    atomicAdd(&S.ncand, wc > kWarpCap ? kCandCap + 1 : wc);  // a full region: no fast path
+  const int wc = S.wcnt[warp];
+  if (!dense) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) nval += __shfl_xor_sync(0xFFFFFFFFu, nval, o);
+    if (lane == 0) atomicAdd(&S.nvalid, nval);
+  } else if (tid == 0) {
+    S.nvalid = n;
   }
+  if (lane == 0) atomicAdd(&S.ncand, wc > kWarpCap ? kCandCap + 1 : wc);  // full: no fast path
   __syncthreads();
   const int keff = S.nvalid < k ? S.nvalid : k;
   if (keff <= 0) return 0;
@@ -307,30 +316,30 @@ __device__ int select_topk(const RowSrc<kKind>& src, int n, int k, SelectSmem& S
   const int w0 = tid * wpt, w1 = min(nw, w0 + wpt);
   int c_eq = 0, c_gt = 0;
   for (int w = w0; w < w1; ++w) { c_eq += __popc(S.eqmap[w]); c_gt += __popc(S.selmap[w]); }
-  int eq_incl = c_eq;
+  // one block-wide scan of both counts: winners before this thread's words are the
+  // keys > T before them plus the first need_eq keys == T, min(need_eq, eq_before)
+  int eq_incl = c_eq, gt_incl = c_gt;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
-    int v = __shfl_up_sync(0xFFFFFFFFu, eq_incl, o);
-    if (lane >= o) eq_incl += v;
+    const int ve = __shfl_up_sync(0xFFFFFFFFu, eq_incl, o);
+    const int vg = __shfl_up_sync(0xFFFFFFFFu, gt_incl, o);
+    if (lane >= o) { eq_incl += ve; gt_incl += vg; }
   }
-  if (lane == 31) S.warp_a[warp] = eq_incl;
+  if (lane == 31) { S.warp_a[warp] = eq_incl; S.warp_b[warp] = gt_incl; }
   __syncthreads();
-  int eq_base = 0;
-  for (int w = 0; w < warp; ++w) eq_base += S.warp_a[w];
-  const int eq_before = eq_base + eq_incl - c_eq;
+  const int we = lane < kTopkWarps ? S.warp_a[lane] : 0;
+  const int wg = lane < kTopkWarps ? S.warp_b[lane] : 0;
+  int we_incl = we, wg_incl = wg;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int ve = __shfl_up_sync(0xFFFFFFFFu, we_incl, o);
+    const int vg = __shfl_up_sync(0xFFFFFFFFu, wg_incl, o);
+    if (lane >= o) { we_incl += ve; wg_incl += vg; }
+  }
+  const int eq_before = __shfl_sync(0xFFFFFFFFu, we_incl - we, warp) + eq_incl - c_eq;
+  const int gt_before = __shfl_sync(0xFFFFFFFFu, wg_incl - wg, warp) + gt_incl - c_gt;
   int take_eq = min(max(need_eq - eq_before, 0), c_eq);
-  const int c_sel = c_gt + take_eq;
-  int sel_incl = c_sel;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    int v = __shfl_up_sync(0xFFFFFFFFu, sel_incl, o);
-    if (lane >= o) sel_incl += v;
-  }
-  if (lane == 31) S.warp_b[warp] = sel_incl;
-  __syncthreads();
-  int sel_base = 0;
-  for (int w = 0; w < warp; ++w) sel_base += S.warp_b[w];
-  int o = sel_base + sel_incl - c_sel;
+  int o = gt_before + min(need_eq, eq_before);
   for (int w = w0; w < w1; ++w) {
     uint32_t bits = S.selmap[w];
     uint32_t eqb = S.eqmap[w];
@@ -442,10 +451,13 @@ __device__ __forceinline__ void topk_row(const TopkArgs& a, int c) {
   }
   __syncthreads();
   RowSrc<kSrcSmem> src{rowbuf, pad == 0};
+  // every position below n is scored unless the row maps candidate blocks (REINDEX);
+  // every block below the row's count has a key
+  const bool dense = a.blocks || a.cand == nullptr;
   int32_t* sel_q = a.sel + (int64_t)q * a.k;
   float* sc_q = a.sel_scores ? a.sel_scores + (int64_t)q * a.k : nullptr;
   if (a.nchunk == 1) {
-    const int keff = select_topk(src, len, a.k, S, [&](int o, int i) {
+    const int keff = select_topk(src, len, a.k, dense, S, [&](int o, int i) {
       sel_q[o] = pos_to_row(a, q, (uint32_t)(begin + i));
       if (sc_q) sc_q[o] = key_score(src(i));
     });
@@ -454,7 +466,7 @@ __device__ __forceinline__ void topk_row(const TopkArgs& a, int c) {
   }
   // partial list of this chunk, then the last chunk CTA of the row merges
   uint64_t* part = a.part + ((int64_t)q * a.nchunk + c) * a.k;
-  const int keff = select_topk(src, len, a.k, S, [&](int o, int i) {
+  const int keff = select_topk(src, len, a.k, dense, S, [&](int o, int i) {
     part[o] = ((uint64_t)src(i) << 32) | (uint32_t)(begin + i);
   });
   for (int i = keff + (int)threadIdx.x; i < a.k; i += kTopkThreads) part[i] = 0;
@@ -494,7 +506,7 @@ __device__ __forceinline__ void topk_row(const TopkArgs& a, int c) {
   }
   __syncthreads();
   RowSrc<kSrcSmem> msrc{mk, true};
-  const int keff2 = select_topk(msrc, ncand, a.k, S, [&](int o, int i) {
+  const int keff2 = select_topk(msrc, ncand, a.k, false, S, [&](int o, int i) {
     sel_q[o] = pos_to_row(a, q, (uint32_t)(__ldcg(row + i) & 0xFFFFFFFFu));
     if (sc_q) sc_q[o] = key_score(mk[i]);
   });
