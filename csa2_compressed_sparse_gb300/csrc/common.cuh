@@ -35,6 +35,20 @@ struct CompressArgs {
   const float* inv_freq;
 };
 
+// A query group of the indexer: queries q0 .. q0 + nq - 1 of sequence seq (row_base rb)
+// own the work tiles tile0 .. tile1 - 1.
+struct __align__(16) GroupRec {
+  int32_t q0, nq, seq, pad0;
+  int64_t tile0, tile1;
+  int64_t rb, pad1;
+};
+// A score CTA's work: tiles it_lo .. it_hi - 1, starting in group g_first.
+struct __align__(16) CtaRec {
+  int32_t g_first, pad0;
+  int64_t it_lo, it_hi, pad1;
+};
+constexpr int kMaxIndexCtas = 1024;
+
 struct IndexArgs {
   const uint16_t* iq;   // [Q][H][128]
   const float* w;       // [Q][H]
@@ -54,10 +68,10 @@ struct IndexArgs {
   // workspace views
   uint32_t* keys;       // [Q][ldk]
   int32_t* n_scored;    // [Q]
-  int32_t* grp_q0;      // [Q]  first query of group g
-  int32_t* grp_nq;      // [Q]  queries in group g
-  int64_t* grp_tile0;   // [Q+1] first work tile of group g (prefix)
-  int32_t* n_groups;    // [1]
+  struct GroupRec* grp;  // [Q]  query groups (written by the prep kernel)
+  struct CtaRec* cta;    // [nctas] each score CTA's tile range and first group
+  int nctas;             // score kernel CTAs (<= kMaxIndexCtas)
+  int32_t* n_groups;     // [2]  groups, largest group size
   int32_t* topk_count;  // [Q]  zeroed by the prep kernel for the top-k merge
   int group_max;        // queries per group (FULL: 256 / H; REINDEX: 1)
   int32_t* pool_count;  // [Q]  or null: zeroed by the prep kernel for the candidate

@@ -46,7 +46,7 @@ size_t up256(size_t x) { return (x + 255) & ~size_t(255); }
 
 // Workspace of csa2_index_topk.
 struct IndexWs {
-  size_t keys, n_scored, grp_q0, grp_nq, grp_tile0, n_groups, count, part, total;
+  size_t keys, n_scored, grp, cta, n_groups, count, part, total;
   int nchunk;
   // candidate pool (nbk > 0): merge counters and partial lists of the block selection
   size_t pcount, ppart;
@@ -78,10 +78,9 @@ IndexWs index_ws_layout(int Q, int64_t ld, int k, int nbk = 0, int64_t qrows = 0
   size_t o = 0;
   w.keys = o; o = up256(o + (size_t)Q * (size_t)((ld + 3) & ~int64_t(3)) * 4);
   w.n_scored = o; o = up256(o + (size_t)Q * 4);
-  w.grp_q0 = o; o = up256(o + (size_t)Q * 4);
-  w.grp_nq = o; o = up256(o + (size_t)Q * 4);
-  w.grp_tile0 = o; o = up256(o + (size_t)(Q + 1) * 8);
-  w.n_groups = o; o = up256(o + 4);
+  w.grp = o; o = up256(o + (size_t)Q * sizeof(csa2::GroupRec));
+  w.cta = o; o = up256(o + (size_t)csa2::kMaxIndexCtas * sizeof(csa2::CtaRec));
+  w.n_groups = o; o = up256(o + 8);
   w.count = o; o = up256(o + (size_t)Q * 4);
   w.nchunk = csa2::topk_num_chunks(ld);
   w.part = o;
@@ -259,9 +258,8 @@ csa2_status index_topk_impl(const csa2_bf16* iq, const float* w, int Q, int H,
   a.ldk = (max_scored + 3) & ~int64_t(3);
   a.keys = reinterpret_cast<uint32_t*>(base + L.keys);
   a.n_scored = reinterpret_cast<int32_t*>(base + L.n_scored);
-  a.grp_q0 = reinterpret_cast<int32_t*>(base + L.grp_q0);
-  a.grp_nq = reinterpret_cast<int32_t*>(base + L.grp_nq);
-  a.grp_tile0 = reinterpret_cast<int64_t*>(base + L.grp_tile0);
+  a.grp = reinterpret_cast<csa2::GroupRec*>(base + L.grp);
+  a.cta = reinterpret_cast<csa2::CtaRec*>(base + L.cta);
   a.n_groups = reinterpret_cast<int32_t*>(base + L.n_groups);
   a.topk_count = reinterpret_cast<int32_t*>(base + L.count);
   a.group_max = cand ? 1 : 256 / H;

@@ -169,10 +169,16 @@ __global__ void __launch_bounds__(kPrepThreads) index_prep_kernel(IndexArgs a) {
     long long ey, ty;
     block_excl_sum2(lead ? 1 : 0, tiles, redx, redy, ex, ey, tx, ty);
     if (lead) {
-      const int g = carry_groups + ex;
-      a.grp_q0[g] = q;
-      a.grp_nq[g] = nq;
-      a.grp_tile0[g] = carry_tiles + ey;
+      GroupRec r;
+      r.q0 = q;
+      r.nq = nq;
+      r.seq = s_seq[tid];
+      r.pad0 = 0;
+      r.tile0 = carry_tiles + ey;
+      r.tile1 = r.tile0 + tiles;
+      r.rb = a.row_base[r.seq];
+      r.pad1 = 0;
+      a.grp[carry_groups + ex] = r;
     }
     // carries into the next block (every thread keeps its own copy); block_excl_sum2
     // ended with a barrier, so red_run is free
@@ -184,21 +190,41 @@ __global__ void __launch_bounds__(kPrepThreads) index_prep_kernel(IndexArgs a) {
     carry_tiles += ty;
     __syncthreads();  // s_seq / s_ns / red_run are rewritten by the next block
   }
-  if (tid == 0) {
-    a.grp_tile0[carry_groups] = carry_tiles;
-    *a.n_groups = carry_groups;
+  if (tid == 0) a.n_groups[0] = carry_groups;
+  // the score CTAs' ranges (ceil(total / nctas) tiles each) and the group each starts in,
+  // so that a score CTA starts after two loads instead of a search
+  const int64_t total = carry_tiles;
+  const int64_t per = (total + a.nctas - 1) / a.nctas;
+  for (int c = tid; c < a.nctas; c += kPrepThreads) {
+    CtaRec r;
+    r.g_first = 0;
+    r.pad0 = 0;
+    r.it_lo = min(total, (int64_t)c * per);
+    r.it_hi = min(total, r.it_lo + per);
+    r.pad1 = 0;
+    a.cta[c] = r;
+  }
+  __syncthreads();  // the records above and the group records are visible to all threads
+  if (per > 0) {
+    for (int g = tid; g < carry_groups; g += kPrepThreads) {
+      const int64_t t0 = a.grp[g].tile0, t1 = a.grp[g].tile1;
+      // CTAs whose first tile c * per lies in [t0, t1)
+      for (int64_t c = (t0 + per - 1) / per; c * per < t1 && c < a.nctas; ++c)
+        a.cta[c].g_first = g;
+    }
   }
 }
 
 // ---- main kernel -----------------------------------------------------------------------
 
 __device__ __forceinline__ void load_group(const IndexArgs& a, int g, GroupInfo& gi) {
-  gi.q0 = a.grp_q0[g];
-  gi.nq = a.grp_nq[g];
-  gi.seq = a.q_seq[gi.q0];
-  gi.tile0 = a.grp_tile0[g];
-  gi.tile1 = a.grp_tile0[g + 1];
-  gi.rb = a.row_base[gi.seq];
+  const GroupRec r = a.grp[g];
+  gi.q0 = r.q0;
+  gi.nq = r.nq;
+  gi.seq = r.seq;
+  gi.tile0 = r.tile0;
+  gi.tile1 = r.tile1;
+  gi.rb = r.rb;
 }
 
 // ---- FP8 quantisation: [A] indexer figure (FP8 rows of 128 E4M3 codes with one fp32
@@ -305,11 +331,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     prefetch_tensormap(&qmap);
   }
   griddep_wait();
-  const int ng = *a.n_groups;
-  const int64_t total = a.grp_tile0[ng];
-  const int64_t per = (total + gridDim.x - 1) / gridDim.x;
-  const int64_t it_lo = (int64_t)blockIdx.x * per;
-  const int64_t it_hi = min(total, it_lo + per);
+  // this CTA's tile range and first group, from the prep kernel
+  const CtaRec cr = a.cta[blockIdx.x];
+  const int64_t it_lo = cr.it_lo, it_hi = cr.it_hi;
+  const int g_first = cr.g_first;
   if (it_lo >= it_hi) return;
 
   if (threadIdx.x == 0) {
@@ -335,16 +360,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  // first group of this CTA's range: last g with grp_tile0[g] <= it_lo
-  int g_first;
-  {
-    int lo = 0, hi = ng - 1;
-    while (lo < hi) {
-      int mid = (lo + hi + 1) >> 1;
-      if (a.grp_tile0[mid] <= it_lo) lo = mid; else hi = mid - 1;
-    }
-    g_first = lo;
-  }
   const float alpha = rsqrtf((float)kDIdx) * rsqrtf((float)a.H);
 
   if (warp == 0) {
@@ -622,8 +637,10 @@ size_t index_smem_bytes() {
   return 1024 + kRingBytes + kBBytes + 8 * 256 * 4 + sizeof(Bars) + 16 + 8 * 8 * kMaxGroup;
 }
 
-cudaError_t launch_index(const IndexArgs& a, int num_sms, cudaStream_t s) {
-  if (a.Q == 0) return cudaSuccess;
+cudaError_t launch_index(const IndexArgs& args, int num_sms, cudaStream_t s) {
+  if (args.Q == 0) return cudaSuccess;
+  IndexArgs a = args;
+  a.nctas = num_sms < kMaxIndexCtas ? num_sms : kMaxIndexCtas;  // one score CTA per SM
   cudaError_t e = launch_pdl(index_prep_kernel, dim3(1), dim3(kPrepThreads), 0, s, a);
   if (e != cudaSuccess) return e;
   CUtensorMap kt, kb, qm;
@@ -653,7 +670,7 @@ cudaError_t launch_index(const IndexArgs& a, int num_sms, cudaStream_t s) {
   auto kern = f8 ? index_score_kernel<true> : index_score_kernel<false>;
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  return launch_pdl(kern, dim3(num_sms), dim3(kThreads), smem, s, a, kt, kb, qm);
+  return launch_pdl(kern, dim3(a.nctas), dim3(kThreads), smem, s, a, kt, kb, qm);
 }
 
 cudaError_t launch_plane_fp8(const uint16_t* k, int64_t n, uint8_t* plane, cudaStream_t s) {
