@@ -34,6 +34,9 @@ def lib():
         L.orc_compress.argtypes = [_vp, _vp, _vp, _i32, _vp, _i32, _vp, _vp, _vp, _vp, _vp, _vp,
                                    _dbl, _vp]
         L.orc_compress.restype = _i64
+        L.orc_compress_index.argtypes = [_vp, _vp, _vp, _i32, _vp, _i32, _vp, _vp, _vp, _vp,
+                                         _vp, _vp, _dbl, _vp, _vp, _vp, _vp, _vp]
+        L.orc_compress_index.restype = _i64
         L.orc_index_scores.argtypes = [_vp, _vp, _i32, _i32, _vp, _vp, _vp, _vp, _i32, _vp, _i32,
                                        _i32, _vp, _vp, _i64]
         L.orc_index_scores.restype = None
@@ -110,6 +113,30 @@ def compress(kv, score, cu_seqlens, start_pos, ratio, kv_state, score_state, pla
     n = lib().orc_compress(_p(kv), _p(score), _p(cu), len(cu) - 1, _p(sp), ratio, _p(kv_state),
                            _p(score_state), _p(plane), _p(pf), _p(rb), _p(nw), eps, _p(invf))
     return n, pf
+
+
+def compress_index(kv, score, cu_seqlens, start_pos, ratio, kv_state, score_state, plane,
+                   index_plane, row_base, inv_freq, wk, knorm_w=None, norm_w=None, eps=1e-6):
+    """compress() plus the index K of every emitted row (index_plane uint16 [rows,128], in
+    place).  Returns (rows emitted, plane_f64 [rows,512], index_f64 [rows,128])."""
+    kv = bf16_bits(kv) if isinstance(kv, torch.Tensor) else kv
+    score = None if score is None else (bf16_bits(score) if isinstance(score, torch.Tensor)
+                                        else score)
+    cu = np.ascontiguousarray(cu_seqlens, dtype=np.int32)
+    sp = np.ascontiguousarray(start_pos, dtype=np.int64)
+    rb = np.ascontiguousarray(row_base, dtype=np.int64)
+    invf = np.ascontiguousarray(inv_freq, dtype=np.float32)
+    nw = None if norm_w is None else np.ascontiguousarray(norm_w, dtype=np.float32)
+    kw = None if knorm_w is None else np.ascontiguousarray(knorm_w, dtype=np.float32)
+    wkb = bf16_bits(wk) if isinstance(wk, torch.Tensor) else np.ascontiguousarray(wk, np.uint16)
+    assert wkb.shape == (128, 512)
+    assert index_plane.dtype == np.uint16 and index_plane.shape[1] == 128
+    pf = np.zeros(plane.shape, dtype=np.float64)
+    kf = np.zeros(index_plane.shape, dtype=np.float64)
+    n = lib().orc_compress_index(_p(kv), _p(score), _p(cu), len(cu) - 1, _p(sp), ratio,
+                                 _p(kv_state), _p(score_state), _p(plane), _p(pf), _p(rb),
+                                 _p(nw), eps, _p(invf), _p(wkb), _p(kw), _p(index_plane), _p(kf))
+    return n, pf, kf
 
 
 def index_scores(iq, w, index_k, row_base, q_seq, q_pos, ratio, cand=None, relu=True, ld=None):

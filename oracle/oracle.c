@@ -120,10 +120,65 @@ int64_t orc_n_visible(int64_t p, int m) {
  * and y is stored to plane row row_base[b] + j as bf16.
  * State arrays are [B][m][512]; slot s holds the last token with t % m == s.
  * Returns the number of rows emitted in total. */
+/* ---- index K of a compressed row [A] indexer figure, key side ("the compressed,
+ *      pre-RoPE latent [512] BF16 -> indexer.wk [128, 512] -> k_norm -> RoPE -> the
+ *      index plane"); [A] compressor figure (the two branches part after RMSNorm);
+ *      [C] A.6.2 (index K projected from the main latent) -----------------------------
+ *
+ * x = bf16(y) is the row's normalized latent before RoPE, rounded to bf16 once;
+ *   k[o] = sum_d wk[o][d] x[d]                     (o < 128)
+ *   k    = k / sqrt(mean(k^2) + eps) * knorm_w     (RMSNorm over the 128 dims)
+ *   k[64+2i], k[65+2i] rotated by angle p0 * inv_freq[i], i < 32 (the last 64 dims)
+ * at the row's group-head position p0; stored as bf16 (and as double in k_f64). */
+static void index_k_row(const double* y, double p0, const uint16_t* wk, const float* knorm_w,
+                        double eps, const float* inv_freq, uint16_t* out, double* out_f64) {
+  double x[D_LAT], k[D_IDX];
+  for (int d = 0; d < D_LAT; d++) x[d] = bf16_val(orc_f64_to_bf16(y[d]));
+  for (int o = 0; o < D_IDX; o++) {
+    double acc = 0.0;
+    for (int d = 0; d < D_LAT; d++) acc += bf16_val(wk[o * D_LAT + d]) * x[d];
+    k[o] = acc;
+  }
+  double ms = 0.0;
+  for (int o = 0; o < D_IDX; o++) ms += k[o] * k[o];
+  double inv = 1.0 / sqrt(ms / D_IDX + eps);
+  for (int o = 0; o < D_IDX; o++) k[o] = k[o] * inv * (knorm_w ? (double)knorm_w[o] : 1.0);
+  for (int i = 0; i < 32; i++) {
+    double ang = p0 * (double)inv_freq[i];
+    double c = cos(ang), s = sin(ang);
+    double a0 = k[64 + 2 * i], a1 = k[64 + 2 * i + 1];
+    k[64 + 2 * i] = a0 * c - a1 * s;
+    k[64 + 2 * i + 1] = a0 * s + a1 * c;
+  }
+  for (int o = 0; o < D_IDX; o++) {
+    out[o] = orc_f64_to_bf16(k[o]);
+    if (out_f64) out_f64[o] = k[o];
+  }
+}
+
+/* orc_compress with, when wk != NULL, the row's index K written to index_plane (and
+ * index_f64) at the same row. */
+int64_t orc_compress_index(const uint16_t* kv, const uint16_t* score, const int32_t* cu_seqlens,
+                           int B, const int64_t* start_pos, int m, double* kv_state,
+                           double* score_state, uint16_t* plane, double* plane_f64,
+                           const int64_t* row_base, const float* norm_w, double eps,
+                           const float* inv_freq, const uint16_t* wk, const float* knorm_w,
+                           uint16_t* index_plane, double* index_f64);
+
 int64_t orc_compress(const uint16_t* kv, const uint16_t* score, const int32_t* cu_seqlens, int B,
                      const int64_t* start_pos, int m, double* kv_state, double* score_state,
                      uint16_t* plane, double* plane_f64, const int64_t* row_base,
                      const float* norm_w, double eps, const float* inv_freq) {
+  return orc_compress_index(kv, score, cu_seqlens, B, start_pos, m, kv_state, score_state, plane,
+                            plane_f64, row_base, norm_w, eps, inv_freq, NULL, NULL, NULL, NULL);
+}
+
+int64_t orc_compress_index(const uint16_t* kv, const uint16_t* score, const int32_t* cu_seqlens,
+                           int B, const int64_t* start_pos, int m, double* kv_state,
+                           double* score_state, uint16_t* plane, double* plane_f64,
+                           const int64_t* row_base, const float* norm_w, double eps,
+                           const float* inv_freq, const uint16_t* wk, const float* knorm_w,
+                           uint16_t* index_plane, double* index_f64) {
   int64_t emitted = 0;
   for (int b = 0; b < B; b++) {
     double* ks = kv_state + (int64_t)b * m * D_LAT;
@@ -154,6 +209,9 @@ int64_t orc_compress(const uint16_t* kv, const uint16_t* score, const int32_t* c
       double inv = 1.0 / sqrt(ms / D_LAT + eps);
       for (int d = 0; d < D_LAT; d++) y[d] = y[d] * inv * (norm_w ? (double)norm_w[d] : 1.0);
       double p0 = (double)(j * m); /* group-head position */
+      if (wk) /* the indexer's branch leaves before the main RoPE */
+        index_k_row(y, p0, wk, knorm_w, eps, inv_freq, index_plane + (row_base[b] + j) * D_IDX,
+                    index_f64 ? index_f64 + (row_base[b] + j) * D_IDX : NULL);
       for (int i = 0; i < 32; i++) {
         double ang = p0 * (double)inv_freq[i];
         double c = cos(ang), s = sin(ang);

@@ -331,6 +331,107 @@ def test_index_reindex_rows_and_masks():
             assert sc[0, i] == full[0, r]
 
 
+# ---- index K production (NEXT-4) ---------------------------------------------------
+
+def run_compress_index(kv, ratio, wk, knorm_w=None, start=0, eps=1e-6):
+    """One sequence [S,512] (kv used as score too) in one call: plane, index rows, f64s."""
+    S = kv.shape[0]
+    nrows = max((start + S) // ratio, 1)
+    plane = np.zeros((nrows, 512), dtype=np.uint16)
+    ip = np.zeros((nrows, 128), dtype=np.uint16)
+    ks = np.zeros((1, ratio, 512))
+    ss = np.zeros((1, ratio, 512))
+    kvb = oracle.bf16_bits(bf16(kv))
+    n, pf, kf = oracle.compress_index(kvb, kvb, [0, S], [start], ratio, ks, ss, plane, ip, [0],
+                                      INV_FREQ, wk, knorm_w=knorm_w, eps=eps)
+    return n, plane, pf, ip, kf
+
+
+def _onehot_wk(pairs):
+    wk = np.zeros((128, 512), dtype=np.float32)
+    for o, d, v in pairs:
+        wk[o, d] = v
+    return oracle.bf16_bits(bf16(wk))
+
+
+def test_index_k_single_weight_closed_form():
+    # one nonzero weight wk[o][d] = v: k = v x[d] at output o only; the RMSNorm over the
+    # 128 outputs turns it into sign(v x[d]) * sqrt(128) (eps negligible), rotated by the
+    # row's RoPE phase when o is in the last 64 dims
+    S = 12
+    kv = bf16_np(bf16(RNG.standard_normal((S, 512)) * 2.0))
+    for o, d, v in ((5, 77, 0.75), (64, 300, -1.5), (97, 449, 2.0), (127, 0, 1.0)):
+        n, plane, pf, ip, kf = run_compress_index(kv, 1, _onehot_wk([(o, d, v)]), eps=0.0)
+        assert n == S
+        for t in range(S):
+            xd = bf16_np(bf16(pf[t]))  # the latent before RoPE equals pf on NoPE dims
+            # the pre-RoPE latent of dim d: undo the main rotation where d is a RoPE dim
+            if d >= 448:
+                i = (d - 448) // 2
+                z = (pf[t, 448 + 2 * i] + 1j * pf[t, 449 + 2 * i]) * np.exp(-1j * rope_angles(t)[i])
+                pre = z.real if d % 2 == 0 else z.imag
+            else:
+                pre = pf[t, d]
+            sgn = math.copysign(1.0, v * float(bf16_np(bf16(np.array([pre])))[0]))
+            expect = np.zeros(128)
+            expect[o] = sgn * math.sqrt(128)
+            if o >= 64:
+                i = (o - 64) // 2
+                ang = rope_angles(t)[i]
+                a0, a1 = expect[64 + 2 * i], expect[65 + 2 * i]
+                expect[64 + 2 * i] = a0 * math.cos(ang) - a1 * math.sin(ang)
+                expect[65 + 2 * i] = a0 * math.sin(ang) + a1 * math.cos(ang)
+            np.testing.assert_allclose(kf[t], expect, atol=1e-9)
+            assert all(ip[t, c] == oracle.f64_to_bf16(kf[t, c]) for c in range(128))
+
+
+def test_index_k_projects_the_bf16_latent_before_rope():
+    # two outputs below 64 (no rotation): their ratio is the ratio of the two dot products
+    # of wk rows with the bf16-rounded latent before RoPE, the main plane is unchanged
+    S = 9
+    kv = bf16_np(bf16(RNG.standard_normal((S, 512))))
+    wrow = RNG.standard_normal((2, 512)).astype(np.float32)
+    wk = np.zeros((128, 512), dtype=np.float32)
+    wk[3], wk[40] = wrow[0], wrow[1]
+    wkb = oracle.bf16_bits(bf16(wk))
+    wkd = bf16_np(bf16(wk))
+    n, plane, pf, ip, kf = run_compress_index(kv, 1, wkb)
+    n0, plane0, pf0, *_ = run_compress(kv, kv, 1, [S])
+    assert np.array_equal(plane, plane0)
+    for t in range(S):
+        pre = pf[t].copy()
+        z = (pf[t, 448::2] + 1j * pf[t, 449::2]) * np.exp(-1j * rope_angles(t))
+        pre[448::2], pre[449::2] = z.real, z.imag
+        x = bf16_np(bf16(pre))
+        d3, d40 = wkd[3] @ x, wkd[40] @ x
+        np.testing.assert_allclose(kf[t, 3] / kf[t, 40], d3 / d40, rtol=1e-9)
+        # and the RMSNorm over the 128 outputs (weight 1, eps 1e-6) sets their sum of
+        # squares to 128 ms / (ms + eps)
+        ms = (d3 * d3 + d40 * d40) / 128.0
+        np.testing.assert_allclose(np.sum(kf[t] ** 2), 128.0 * ms / (ms + 1e-6), rtol=1e-9)
+
+
+def test_index_k_norm_weight_rope_phase_and_group_position():
+    # ratio 2: row j rotates at its group-head position 2j; k_norm's weight scales each
+    # output; the rotation keeps each pair's norm and is undone by the conjugate phase
+    S = 20
+    kv = bf16_np(bf16(RNG.standard_normal((S, 512))))
+    wk = oracle.bf16_bits(bf16(RNG.standard_normal((128, 512)) * 0.05))
+    kw = (1.0 + RNG.integers(0, 4, 128) * 0.25).astype(np.float32)
+    n1, _, _, _, k1 = run_compress_index(kv, 2, wk)
+    n2, _, _, _, k2 = run_compress_index(kv, 2, wk, knorm_w=kw)
+    assert n1 == n2 == S // 2
+    for j in range(S // 2):
+        ang = rope_angles(2 * j)
+        u1 = (k1[j, 64::2] + 1j * k1[j, 65::2]) * np.exp(-1j * ang)
+        u2 = (k2[j, 64::2] + 1j * k2[j, 65::2]) * np.exp(-1j * ang)
+        np.testing.assert_allclose(k2[j, :64], k1[j, :64] * kw[:64], rtol=1e-12)
+        np.testing.assert_allclose(u2.real, u1.real * kw[64::2], rtol=1e-9, atol=1e-12)
+        np.testing.assert_allclose(u2.imag, u1.imag * kw[65::2], rtol=1e-9, atol=1e-12)
+        np.testing.assert_allclose(np.abs(u1) ** 2, k1[j, 64::2] ** 2 + k1[j, 65::2] ** 2,
+                                   rtol=1e-12)
+
+
 # ---- FP8 index plane (NEXT-3) --------------------------------------------------------
 
 def _e4m3_values():
