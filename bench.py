@@ -528,6 +528,16 @@ def run_stages(args):
     res["compress"] = timed(lambda: csa2.csa2_compress(
         t["kv"], t["score"], t["cu_seqlens"], t["start_pos"], spec.ratio, t["kv_state"],
         t["score_state"], t["plane"], t["row_base"], t["inv_freq"], eps=spec.eps))
+    # index K production in the compressor (NEXT-4): seeded weights of the pages' shapes
+    g = np.random.default_rng(5)
+    wk = torch.from_numpy((g.standard_normal((128, 512)) / np.sqrt(512)).astype(np.float32))
+    wk = wk.bfloat16().cuda()
+    kw = torch.ones(128, dtype=torch.float32, device="cuda")
+    iplane = torch.empty((t["plane"].shape[0], 128), dtype=torch.bfloat16, device="cuda")
+    res["compress_index"] = timed(lambda: csa2.csa2_compress_index(
+        t["kv"], t["score"], t["cu_seqlens"], t["start_pos"], spec.ratio, t["kv_state"],
+        t["score_state"], t["plane"], t["row_base"], t["inv_freq"], wk, iplane, knorm_w=kw,
+        eps=spec.eps))
     res["index_topk"] = timed(lambda: csa2.csa2_index_topk(
         t["iq"], t["w"], t["index_k"], t["row_base"], t["q_seq"], t["q_pos"], spec.ratio, spec.k,
         spec.max_scored, buf.sel, buf.ws, sel_scores=buf.sel_scores, cand=cand))

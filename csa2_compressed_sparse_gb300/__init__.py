@@ -17,6 +17,7 @@ from . import build as _build
 
 __all__ = [
     "Csa2Error", "Swa", "lib", "csa2_version", "csa2_device_status", "csa2_compress",
+    "csa2_compress_index",
     "csa2_index_topk_workspace_size", "csa2_index_topk", "csa2_index_topk_noalloc",
     "csa2_index_topk_pool_workspace_size", "csa2_index_topk_pool", "csa2_topk_workspace_size",
     "csa2_index_plane_fp8_bytes", "csa2_index_plane_fp8", "csa2_index_topk_fp8_workspace_size",
@@ -51,6 +52,8 @@ _SIGS = {
     "csa2_device_status": ([_vp], _i32),
     "csa2_compress": ([_vp, _vp, _i32, _vp, _i32, _vp, _i32, _vp, _vp, _vp, _i64, _vp, _vp, _f32,
                        _vp, _vp], _i32),
+    "csa2_compress_index": ([_vp, _vp, _i32, _vp, _i32, _vp, _i32, _vp, _vp, _vp, _i64, _vp,
+                             _vp, _f32, _vp, _vp, _vp, _vp, _vp], _i32),
     "csa2_index_topk_workspace_size": ([_i32, _i32, _i64, _i32], _sz),
     "csa2_index_topk": ([_vp, _vp, _i32, _i32, _vp, _i64, _vp, _vp, _vp, _i32, _vp, _i32, _i32,
                          _i32, _i64, _vp, _vp, _vp, _vp, _sz, _vp], _i32),
@@ -146,6 +149,19 @@ def csa2_compress(kv, score, cu_seqlens, start_pos, ratio, kv_state, score_state
                                _p(kv_state), _p(score_state), _p(plane), plane.shape[0],
                                _p(row_base), _p(norm_w), float(eps), _p(inv_freq),
                                _stream(stream)))
+
+
+def csa2_compress_index(kv, score, cu_seqlens, start_pos, ratio, kv_state, score_state, plane,
+                        row_base, inv_freq, wk, index_plane, knorm_w=None, norm_w=None, eps=1e-6,
+                        stream=None):
+    """csa2_compress plus each written row's index K (wk [128, 512] bf16) in index_plane."""
+    T = kv.shape[0]
+    B = cu_seqlens.numel() - 1
+    _check(lib().csa2_compress_index(_p(kv), _p(score), T, _p(cu_seqlens), B, _p(start_pos),
+                                     ratio, _p(kv_state), _p(score_state), _p(plane),
+                                     plane.shape[0], _p(row_base), _p(norm_w), float(eps),
+                                     _p(inv_freq), _p(wk), _p(knorm_w), _p(index_plane),
+                                     _stream(stream)))
 
 
 def csa2_index_topk_workspace_size(Q, H, max_scored, k):

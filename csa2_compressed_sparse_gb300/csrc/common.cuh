@@ -33,6 +33,11 @@ struct CompressArgs {
   const float* norm_w;
   float eps;
   const float* inv_freq;
+  // index K of each row (null wk: none): wk [128][512] bf16, knorm_w [128] (null: ones),
+  // index_plane [plane_rows][128] bf16
+  const uint16_t* wk;
+  const float* knorm_w;
+  uint16_t* index_plane;
 };
 
 // A query group of the indexer: queries q0 .. q0 + nq - 1 of sequence seq (row_base rb)

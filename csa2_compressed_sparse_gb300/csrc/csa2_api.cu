@@ -204,9 +204,44 @@ csa2_status csa2_compress(const csa2_bf16* kv, const csa2_bf16* score, int T,
   REQUIRE(eps >= 0.f && std::isfinite(eps), "csa2_compress: eps must be finite and >= 0");
   REQUIRE(plane_rows >= 0, "csa2_compress: plane_rows must be >= 0");
   csa2::CompressArgs a{kv, score, T, cu_seqlens, B, start_pos, ratio, kv_state, score_state,
-                       plane, plane_rows, row_base, norm_w, eps, inv_freq};
+                       plane, plane_rows, row_base, norm_w, eps, inv_freq,
+                       nullptr, nullptr, nullptr};
   cudaError_t e = csa2::launch_compress(a, stream);
   if (e != cudaSuccess) return cuda_fail(e, "csa2_compress");
+  return CSA2_OK;
+}
+
+csa2_status csa2_compress_index(const csa2_bf16* kv, const csa2_bf16* score, int T,
+                                const int32_t* cu_seqlens, int B, const int64_t* start_pos,
+                                int ratio, float* kv_state, float* score_state, csa2_bf16* plane,
+                                int64_t plane_rows, const int64_t* row_base, const float* norm_w,
+                                float eps, const float* inv_freq, const csa2_bf16* wk,
+                                const float* knorm_w, csa2_bf16* index_plane,
+                                csa2_stream stream) {
+  REQUIRE(T <= 0 || (wk && index_plane), "csa2_compress_index: wk and index_plane are required");
+  REQUIRE(!wk || (aligned16(wk) && aligned16(index_plane)),
+          "csa2_compress_index: wk and index_plane must be 16-byte aligned");
+  // the plain compressor's checks first
+  REQUIRE(ratio == 1 || ratio == 2, "csa2_compress: ratio must be 1 or 2 (got %d)", ratio);
+  REQUIRE(B >= 1 && B <= 8192, "csa2_compress: B must be in [1, 8192] (got %d)", B);
+  REQUIRE(T >= 0, "csa2_compress: T must be >= 0 (got %d)", T);
+  if (T == 0) return CSA2_OK;
+  REQUIRE(kv && cu_seqlens && start_pos && plane && row_base && inv_freq,
+          "csa2_compress: kv, cu_seqlens, start_pos, plane, row_base and inv_freq are required");
+  REQUIRE(ratio == 1 || (score && kv_state && score_state),
+          "csa2_compress: ratio 2 needs score, kv_state and score_state");
+  REQUIRE(aligned16(kv) && aligned16(plane) && (!score || aligned16(score)) &&
+              (!kv_state || aligned16(kv_state)) && (!score_state || aligned16(score_state)) &&
+              (!norm_w || aligned16(norm_w)),
+          "csa2_compress: kv, score, plane, states and norm_w must be 16-byte aligned");
+  REQUIRE(eps >= 0.f && std::isfinite(eps), "csa2_compress: eps must be finite and >= 0");
+  REQUIRE(plane_rows >= 0, "csa2_compress: plane_rows must be >= 0");
+  csa2::CompressArgs a{kv, score, T, cu_seqlens, B, start_pos, ratio, kv_state, score_state,
+                       plane, plane_rows, row_base, norm_w, eps, inv_freq,
+                       reinterpret_cast<const uint16_t*>(wk), knorm_w,
+                       reinterpret_cast<uint16_t*>(index_plane)};
+  cudaError_t e = csa2::launch_compress(a, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "csa2_compress_index");
   return CSA2_OK;
 }
 

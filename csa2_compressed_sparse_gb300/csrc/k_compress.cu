@@ -1,6 +1,8 @@
 // k_compress.cu -- the CSA2 compressor: softmax-gated pooling of m (1 or 2) tokens
 // per row, RMSNorm over the 512 dims, partial RoPE on dims 448..511 at the group's
 // first position, bf16 store; the odd tail is kept in the per-sequence fp32 state.
+// Optionally each row's index K (wk projection of the latent before RoPE, k_norm, RoPE
+// on its last 64 dims) goes to the index plane.
 // [A] "特殊模块 · compressor" and "CSA2 的池化比 V4 简单一截"; [B] §4.1, §6.1-6.2;
 // [C] §6.2 (tail state), §6.4 (ratio 1 degenerates to projection + norm).
 //
@@ -70,6 +72,70 @@ __device__ __forceinline__ void fetch(const CompressArgs& a, int b, int64_t pos,
     load8_f32(a.kv_state + ((int64_t)b * 2 + slot) * kDLat + c0, kv);
     load8_f32(a.score_state + ((int64_t)b * 2 + slot) * kDLat + c0, sc);
   }
+}
+
+// Index K of one row, by the warp that emits it: [A] indexer figure, key side (the bf16
+// latent before RoPE -> wk [128, 512] -> k_norm -> RoPE on the last 64 dims -> the index
+// plane).  r holds the lane's 16 normalized channels before RoPE.  Each lane multiplies
+// its channels into all 128 outputs (one 16-byte load of each wk row per half), and a
+// butterfly over the lanes sums every block of 32 outputs so that lane l ends with
+// outputs l, 32 + l, 64 + l, 96 + l; then the RMSNorm over the 128 and the rotation of
+// pairs (64 + 2i, 65 + 2i), whose halves sit in lanes 2i and 2i + 1.
+__device__ __forceinline__ void emit_index_k(const CompressArgs& a, const float (&r)[2][8],
+                                             const int (&c)[2], int lane, uint64_t p0,
+                                             int64_t row, const uint64_t* turn_s) {
+  float x[2][8];
+#pragma unroll
+  for (int h = 0; h < 2; ++h)
+#pragma unroll
+    for (int i = 0; i < 8; ++i) x[h][i] = __bfloat162float(__float2bfloat16_rn(r[h][i]));
+  float k[4];
+#pragma unroll 1
+  for (int blk = 0; blk < 4; ++blk) {
+    float v[32];
+#pragma unroll
+    for (int oo = 0; oo < 32; ++oo) {
+      const uint16_t* wr = a.wk + (int64_t)(32 * blk + oo) * kDLat;
+      float w0[8], w1[8];
+      load8_bf16(wr + c[0], w0);
+      load8_bf16(wr + c[1], w1);
+      float acc = 0.f;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) acc = fmaf(w0[i], x[0][i], acc);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) acc = fmaf(w1[i], x[1][i], acc);
+      v[oo] = acc;
+    }
+#pragma unroll
+    for (int off = 16, n = 16; off >= 1; off >>= 1, n >>= 1) {
+      const bool upper = (lane & off) != 0;
+#pragma unroll
+      for (int i = 0; i < n; ++i) {
+        const float send = upper ? v[i] : v[i + n];
+        const float keep = upper ? v[i + n] : v[i];
+        v[i] = keep + __shfl_xor_sync(0xFFFFFFFFu, send, off);
+      }
+    }
+    k[blk] = v[0];
+  }
+  float ss = k[0] * k[0] + k[1] * k[1] + k[2] * k[2] + k[3] * k[3];
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xFFFFFFFFu, ss, o);
+  const float rstd = 1.0f / sqrtf(ss / (float)kDIdx + a.eps);
+#pragma unroll
+  for (int blk = 0; blk < 4; ++blk)
+    k[blk] *= rstd * (a.knorm_w ? a.knorm_w[32 * blk + lane] : 1.f);
+#pragma unroll
+  for (int blk = 2; blk < 4; ++blk) {
+    const int pair = 16 * (blk - 2) + (lane >> 1);
+    float fs, fc;
+    sincosf(rope_angle(turn_s[pair], p0), &fs, &fc);
+    const float other = __shfl_xor_sync(0xFFFFFFFFu, k[blk], 1);
+    k[blk] = (lane & 1) ? other * fs + k[blk] * fc : k[blk] * fc - other * fs;
+  }
+  uint16_t* dst = a.index_plane + row * kDIdx;
+#pragma unroll
+  for (int blk = 0; blk < 4; ++blk) dst[32 * blk + lane] = __bfloat16_as_ushort(__float2bfloat16_rn(k[blk]));
 }
 
 __global__ void __launch_bounds__(kWarps * 32) compress_kernel(CompressArgs a) {
@@ -150,6 +216,10 @@ __global__ void __launch_bounds__(kWarps * 32) compress_kernel(CompressArgs a) {
 #pragma unroll
       for (int i = 0; i < 8; ++i) r[h][i] = r[h][i] * rstd * wv[i];
     }
+    const int64_t row = a.row_base[b] + j;
+    const bool row_ok = row >= 0 && row < a.plane_rows;
+    // the indexer's branch leaves before the main RoPE
+    if (a.wk && row_ok) emit_index_k(a, r, c, lane, (uint64_t)(j * m), row, turn_s);
     if (lane >= 24) {  // dims 448 + 8(lane-24) .. +7: four rotation pairs
       const uint64_t p0 = (uint64_t)(j * m);
 #pragma unroll
@@ -163,8 +233,7 @@ __global__ void __launch_bounds__(kWarps * 32) compress_kernel(CompressArgs a) {
         r[1][2 * k + 1] = x0 * fs + x1 * fc;
       }
     }
-    const int64_t row = a.row_base[b] + j;
-    if (row < 0 || row >= a.plane_rows) {
+    if (!row_ok) {
       if (lane == 0) raise_fault(kFaultBounds);
     } else {
       store8_bf16(a.plane + row * kDLat + c[0], r[0]);

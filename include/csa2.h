@@ -99,6 +99,31 @@ csa2_status csa2_compress(const csa2_bf16* kv, const csa2_bf16* score, int T,
                           float eps, const float* inv_freq, csa2_stream stream);
 
 /* ---------------------------------------------------------------------------------
+ * csa2_compress_index -- csa2_compress plus the index K of every row it writes, as a
+ * FULL layer produces it.  [A] indexer figure, key side (the compressed latent before
+ * RoPE, as bf16, through indexer.wk [128, 512], then k_norm, then RoPE, into the index
+ * plane); [A] compressor figure (the two branches part after the RMSNorm); [C] A.6.2
+ * (index K projected from the main latent).
+ *
+ * For each row written, with y its normalized latent before the main RoPE and p0 = j *
+ * ratio its group-head position:
+ *     x    = bf16(y)
+ *     k[o] = sum_d wk[o][d] x[d]                         (o < 128, fp32 sums)
+ *     k    = k * rsqrt(mean(k^2) + eps) * knorm_w        (RMSNorm over the 128 dims)
+ *     k[64+2i], k[65+2i] rotated by angle p0 * inv_freq[i], i = 0..31
+ * stored as bf16 to index_plane row row_base[b] + j (the same row as the main plane).
+ *   wk           [128][512] bf16, 16-byte aligned
+ *   knorm_w      [128] fp32, NULL = all ones
+ *   index_plane  [plane_rows][128] bf16, 16-byte aligned
+ * Everything else (arguments, main plane, states, limits, errors) as csa2_compress. */
+csa2_status csa2_compress_index(const csa2_bf16* kv, const csa2_bf16* score, int T,
+                                const int32_t* cu_seqlens, int B, const int64_t* start_pos,
+                                int ratio, float* kv_state, float* score_state, csa2_bf16* plane,
+                                int64_t plane_rows, const int64_t* row_base, const float* norm_w,
+                                float eps, const float* inv_freq, const csa2_bf16* wk,
+                                const float* knorm_w, csa2_bf16* index_plane, csa2_stream stream);
+
+/* ---------------------------------------------------------------------------------
  * csa2_index_topk -- [A] "特殊模块 · indexer" Fig. 3b and "visible 是每行自己的前缀长度";
  * [A] Fig. 2c (candidate blocks); [C] A.15.2.
  *
