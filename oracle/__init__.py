@@ -51,8 +51,14 @@ def lib():
         L.orc_index_scores_fp8.restype = None
         L.orc_topk.argtypes = [_vp, _vp, _i64, _i32, _vp]
         L.orc_topk.restype = _i32
-        L.orc_sparse_attn.argtypes = [_vp, _i32, _vp, _vp, _i32, _i32, _vp, _vp, _vp, _vp, _vp,
-                                      _vp, _i32, _vp, _dbl, _vp, _vp]
+        L.orc_sparse_attn.argtypes = [_vp, _i32, _vp, _vp, _i32, _i32, _vp, _vp, _vp, _i32, _vp,
+                                      _vp, _vp, _i32, _vp, _dbl, _vp, _vp]
+        L.orc_e2m1_val.argtypes = [ctypes.c_uint8]
+        L.orc_e2m1_val.restype = _dbl
+        L.orc_e2m1_code.argtypes = [_dbl]
+        L.orc_e2m1_code.restype = ctypes.c_uint8
+        L.orc_plane_fp4.argtypes = [_vp, _i64, _vp]
+        L.orc_plane_fp4.restype = None
         L.orc_sparse_attn.restype = None
         L.orc_inverse_rope.argtypes = [_vp, _i32, _vp, _vp]
         L.orc_inverse_rope.restype = None
@@ -161,6 +167,26 @@ def index_scores(iq, w, index_k, row_base, q_seq, q_pos, ratio, cand=None, relu=
     return sc, rows
 
 
+def e2m1_value(code):
+    return float(lib().orc_e2m1_val(int(code)))
+
+
+def e2m1_code(x):
+    """E2M1 code of a double: nearest, ties to the even code, saturating at 6."""
+    return int(lib().orc_e2m1_code(float(x)))
+
+
+FP4_ROW_BYTES = 288  # 256 bytes of codes (two per byte, low nibble first), 32 E4M3 scales
+
+
+def plane_fp4(rows):
+    """bf16 [n, 512] plane rows -> FP4 rows [n, 288] uint8."""
+    rb = bf16_bits(rows)
+    out = np.zeros((rb.shape[0], FP4_ROW_BYTES), dtype=np.uint8)
+    lib().orc_plane_fp4(_p(rb), rb.shape[0], _p(out))
+    return out
+
+
 def e4m3_code(x):
     """E4M3 code of a double: nearest, ties to even, saturating at 448."""
     return int(lib().orc_e4m3_code(float(x)))
@@ -231,7 +257,12 @@ def sparse_attn(q, q_seq, q_pos, swa, plane, row_base, sel, sink, scale=512 ** -
         swa_arr, dt = np.ascontiguousarray(swa.cpu().numpy()), 1
     else:
         swa_arr, dt = bf16_bits(swa), 0
-    pb = bf16_bits(plane)
+    if isinstance(plane, np.ndarray) and plane.dtype == np.uint8:
+        pb, pdt = np.ascontiguousarray(plane), 1  # FP4 rows of 288 bytes
+    elif isinstance(plane, torch.Tensor) and plane.dtype == torch.uint8:
+        pb, pdt = np.ascontiguousarray(plane.cpu().numpy()), 1
+    else:
+        pb, pdt = bf16_bits(plane), 0
     sl = np.ascontiguousarray(sel, dtype=np.int32)
     if sl.ndim == 1:
         sl = sl.reshape(Q, -1)
@@ -247,7 +278,7 @@ def sparse_attn(q, q_seq, q_pos, swa, plane, row_base, sel, sink, scale=512 ** -
     out = np.zeros((Q, 64, 512), dtype=np.float64)
     lse = np.zeros((Q, 64), dtype=np.float64)
     lib().orc_sparse_attn(_p(qb), Q, _p(qs), _p(qp), mode, dt, _p(swa_arr), _p(lb), _p(lp),
-                          _p(pb), _p(rb), _p(sl), nsel, _p(sk), scale, _p(out), _p(lse))
+                          pdt, _p(pb), _p(rb), _p(sl), nsel, _p(sk), scale, _p(out), _p(lse))
     if inv_freq is not None:
         inverse_rope(out, qp, inv_freq)
     return out, lse

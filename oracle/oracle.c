@@ -98,6 +98,25 @@ double orc_ue8m0_scale(double amax) {
   return ldexp(1.0, e);
 }
 
+/* OCP FP4 E2M1 from its definition: sign, 2 exponent bits (bias 1), 1 mantissa bit;
+ * magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6 for codes 0..7. */
+double orc_e2m1_val(uint8_t c) {
+  static const double mag[8] = {0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0};
+  return (c & 8) ? -mag[c & 7] : mag[c & 7];
+}
+
+/* Nearest E2M1 code, ties to the even code (mantissa bit 0), beyond 6 saturating to 6. */
+uint8_t orc_e2m1_code(double x) {
+  uint8_t sign = signbit(x) ? 8 : 0;
+  double a = fabs(x);
+  int best = 0;
+  for (int c = 1; c < 8; c++) {
+    double dc = fabs(orc_e2m1_val((uint8_t)c) - a), db = fabs(orc_e2m1_val((uint8_t)best) - a);
+    if (dc < db || (dc == db && (c & 1) == 0)) best = c;
+  }
+  return sign | (uint8_t)best;
+}
+
 /* ---- visibility [A] "visible 是每行自己的前缀长度"; [B] §4.1 -------------------- */
 
 /* Compressed row j covers positions j*m .. j*m+m-1 and becomes visible to the
@@ -359,6 +378,45 @@ void orc_index_scores_fp8(const uint16_t* iq, const float* w, int Q, int H, cons
   }
 }
 
+/* ---- FP4 main plane [A] pool switch ("nvfp4": main plane rows of 288 B, the 512 dims
+ *      as E2M1 with one E4M3 scale per group of 16) ---------------------------------
+ *
+ * Row layout: bytes 0..255 hold the 512 codes, element 2i in the low nibble of byte i
+ * and element 2i + 1 in its high nibble; bytes 256..287 the 32 scales, scale g for
+ * elements 16g .. 16g + 15.  A group's scale is the smallest E4M3 value s with 6 s >=
+ * max |x| (0 for an all-zero group; the largest, 448, beyond), its codes E2M1(x / s)
+ * (0 when s == 0); the value of element d is E2M1(code) * E4M3(scale). */
+void orc_plane_fp4(const uint16_t* rows, int64_t n, uint8_t* out) {
+  for (int64_t r = 0; r < n; r++) {
+    uint8_t* o = out + r * 288;
+    memset(o, 0, 288);
+    for (int g = 0; g < 32; g++) {
+      double amax = 0.0;
+      for (int i = 0; i < 16; i++) {
+        double v = fabs(bf16_val(rows[r * D_LAT + 16 * g + i]));
+        if (v > amax) amax = v;
+      }
+      uint8_t sc = 0x7E;
+      if (amax == 0.0) sc = 0;
+      else
+        for (int c = 0; c <= 0x7E; c++)
+          if (6.0 * orc_e4m3_val((uint8_t)c) >= amax) { sc = (uint8_t)c; break; }
+      o[256 + g] = sc;
+      double s = orc_e4m3_val(sc);
+      for (int i = 0; i < 16; i++) {
+        int d = 16 * g + i;
+        uint8_t code = s == 0.0 ? 0 : orc_e2m1_code(bf16_val(rows[r * D_LAT + d]) / s);
+        o[d / 2] |= (uint8_t)(code << (4 * (d & 1)));
+      }
+    }
+  }
+}
+
+static double fp4_plane_val(const uint8_t* row, int d) {
+  uint8_t code = (row[d / 2] >> (4 * (d & 1))) & 15;
+  return orc_e2m1_val(code) * orc_e4m3_val(row[256 + d / 16]);
+}
+
 /* ---- top-k [A] Fig. 3b ("selected [rows, 512] 升序，-1 填充"), "visible 是每行
  *      自己的前缀长度" (-1 means the history is shorter than 512) ----------------------
  *
@@ -412,12 +470,13 @@ int orc_topk(const double* scores, const int64_t* rows, int64_t n, int k, int32_
  *   lse_h = log(e^{sink_h} + sum_j e^{s_j})
  * sink == NULL drops the sink term.  swa_mode 0 = ring [B][128][512],
  * 1 = linear rows lin_base[b] + (pos - lin_pos0[b]).  swa_dtype 0 = bf16,
- * 1 = 528-byte FP8 rows (512 E4M3 codes then 4 fp32 scales, one per 128 codes). */
+ * 1 = 528-byte FP8 rows (512 E4M3 codes then 4 fp32 scales, one per 128 codes).
+ * plane_dtype 0 = bf16 rows [.][512], 1 = FP4 rows of 288 B (orc_plane_fp4 layout). */
 void orc_sparse_attn(const uint16_t* q, int Q, const int32_t* q_seq, const int64_t* q_pos,
                      int swa_mode, int swa_dtype, const void* swa, const int64_t* lin_base,
-                     const int64_t* lin_pos0, const uint16_t* plane, const int64_t* row_base,
-                     const int32_t* sel, int nsel, const float* sink, double scale, double* out,
-                     double* lse) {
+                     const int64_t* lin_pos0, int plane_dtype, const void* plane,
+                     const int64_t* row_base, const int32_t* sel, int nsel, const float* sink,
+                     double scale, double* out, double* lse) {
 #pragma omp parallel for schedule(dynamic)
   for (int qi = 0; qi < Q; qi++) {
     int b = q_seq[qi];
@@ -448,8 +507,13 @@ void orc_sparse_attn(const uint16_t* q, int Q, const int32_t* q_seq, const int64
     for (int i = 0; i < nsel; i++) {
       int32_t r = sel[(int64_t)qi * nsel + i];
       if (r < 0) continue;
-      const uint16_t* src = plane + (row_base[b] + r) * D_LAT;
-      for (int d = 0; d < D_LAT; d++) x[(int64_t)e * D_LAT + d] = bf16_val(src[d]);
+      if (plane_dtype == 0) {
+        const uint16_t* src = (const uint16_t*)plane + (row_base[b] + r) * D_LAT;
+        for (int d = 0; d < D_LAT; d++) x[(int64_t)e * D_LAT + d] = bf16_val(src[d]);
+      } else {
+        const uint8_t* src = (const uint8_t*)plane + (row_base[b] + r) * 288;
+        for (int d = 0; d < D_LAT; d++) x[(int64_t)e * D_LAT + d] = fp4_plane_val(src, d);
+      }
       e++;
     }
     double* s = (double*)malloc(sizeof(double) * (size_t)nent);

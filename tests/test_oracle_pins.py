@@ -432,6 +432,81 @@ def test_index_k_norm_weight_rope_phase_and_group_position():
                                    rtol=1e-12)
 
 
+# ---- FP4 main plane (NEXT-3) ----------------------------------------------------------
+
+E2M1 = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]
+
+
+def _e2m1_nearest_even(x):
+    """Brute force over the 8 magnitudes; ties go to the code with mantissa bit 0."""
+    a = min(abs(x), 6.0)
+    d = [abs(v - a) for v in E2M1]
+    best = min(range(8), key=lambda c: (d[c], c & 1))
+    return best | (8 if math.copysign(1.0, x) < 0 else 0)
+
+
+def test_e2m1_codes_by_brute_force_and_ties():
+    vals = E2M1 + [(E2M1[i] + E2M1[i + 1]) / 2 for i in range(7)] + list(RNG.uniform(-7, 7, 3000))
+    for x in vals + [-v for v in vals]:
+        assert oracle.e2m1_code(x) == _e2m1_nearest_even(x), x
+    assert [oracle.e2m1_value(c) for c in range(8)] == E2M1
+    assert oracle.e2m1_code(0.25) == 0 and oracle.e2m1_code(0.75) == 2 and oracle.e2m1_code(5.0) == 6
+    assert oracle.e2m1_code(100.0) == 7 and oracle.e2m1_code(-100.0) == 15
+
+
+def test_fp4_plane_layout_scales_and_error():
+    n = 6
+    x = RNG.standard_normal((n, 512)) * np.exp2(RNG.integers(-4, 4, (n, 32)).repeat(16, axis=1))
+    x[2, 16:32] = 0.0  # an all-zero group: scale 0, codes 0
+    rows = bf16(x)
+    xd = bf16_np(rows)
+    out = oracle.plane_fp4(rows)
+    assert out.shape == (n, 288)
+    e4 = np.array([oracle.e4m3_value(c) for c in range(0x7F)])
+    for r in range(n):
+        codes = np.empty(512, dtype=np.int64)
+        codes[0::2] = out[r, :256] & 15
+        codes[1::2] = out[r, :256] >> 4
+        for g in range(32):
+            amax = np.abs(xd[r, 16 * g:16 * g + 16]).max()
+            sc = int(out[r, 256 + g])
+            if amax == 0:
+                assert sc == 0 and np.all(codes[16 * g:16 * g + 16] == 0)
+                continue
+            s = e4[sc]
+            assert 6 * s >= amax and (sc == 0 or 6 * e4[sc - 1] < amax)  # the smallest that fits
+            for i in range(16):
+                d = 16 * g + i
+                assert codes[d] == _e2m1_nearest_even(xd[r, d] / s)
+    # row 2, group 1 decodes to zeros; the rest within half a code step of the input
+    deq = np.array([[oracle.e2m1_value((out[r, d // 2] >> (4 * (d & 1))) & 15) *
+                     e4[out[r, 256 + d // 16]] for d in range(512)] for r in range(n)])
+    assert np.all(deq[2, 16:32] == 0)
+    rel = np.abs(deq - xd) / np.repeat(np.abs(xd).reshape(n, 32, 16).max(2), 16, axis=1).clip(1e-30)
+    # half the widest E2M1 step (2, between 4 and 6) times the scale, and the scale is at
+    # most 9/8 of amax / 6 (the smallest E4M3 value above it)
+    assert rel.max() <= 1.0 * (9 / 8) / 6 + 1e-12
+
+
+def test_attention_on_an_fp4_plane_equals_the_dequantised_bf16_plane():
+    # E2M1 times E4M3 has at most six significant bits, so the dequantised plane is exact
+    # in bf16: the FP4 path must give the bf16 path's result on that plane, bit for bit
+    rows = bf16(RNG.standard_normal((40, 512)))
+    p4 = oracle.plane_fp4(rows)
+    e4 = np.array([oracle.e4m3_value(c) for c in range(256)])
+    deq = np.array([[oracle.e2m1_value((p4[r, d // 2] >> (4 * (d & 1))) & 15) *
+                     e4[p4[r, 256 + d // 16]] for d in range(512)] for r in range(40)])
+    plane_bf = bf16(deq)
+    assert np.array_equal(bf16_np(plane_bf), deq)
+    q = bf16(RNG.standard_normal((2, 64, 512)))
+    ring = bf16(RNG.standard_normal((1, 128, 512)))
+    sel = np.array([[3, 0, 39, -1, 17, 8], [5, 5, -1, 22, 1, 30]], dtype=np.int32)
+    sink = RNG.standard_normal(64).astype(np.float32)
+    a, la = oracle.sparse_attn(q, [0, 0], [300, 77], ring, plane_bf, [0], sel, sink)
+    b, lb = oracle.sparse_attn(q, [0, 0], [300, 77], ring, p4, [0], sel, sink)
+    assert np.array_equal(a, b) and np.array_equal(la, lb)
+
+
 # ---- FP8 index plane (NEXT-3) --------------------------------------------------------
 
 def _e4m3_values():
