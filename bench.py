@@ -565,6 +565,13 @@ def run_stages(args):
     res["sparse_attn_rope"] = timed(lambda: csa2.csa2_sparse_attn_rope(
         t["q"][0], t["q_seq"], t["q_pos"], swa0, t["plane"], t["row_base"], buf.sel, t["sink"],
         buf.out[0], t["inv_freq"], scale=spec.scale, ws=buf.attn_ws))
+    # the FP4 main plane (NEXT-3): the same rows quantised once
+    rows = t["plane"].shape[0]
+    p4 = torch.empty(csa2.csa2_plane_fp4_bytes(rows), dtype=torch.uint8, device="cuda")
+    csa2.csa2_plane_fp4(t["plane"], p4)
+    res["sparse_attn_fp4"] = timed(lambda: csa2.csa2_sparse_attn_fp4(
+        t["q"][0], t["q_seq"], t["q_pos"], swa0, p4, rows, t["row_base"], buf.sel, t["sink"],
+        buf.out[0], scale=spec.scale, ws=buf.attn_ws))
     res["step"] = timed(lambda: run_step(spec, t, buf))
     csa2.csa2_device_status()
     print(json.dumps({"stages_us": {k: round(v, 2) for k, v in res.items()},

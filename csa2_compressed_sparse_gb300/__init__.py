@@ -23,7 +23,8 @@ __all__ = [
     "csa2_index_plane_fp8_bytes", "csa2_index_plane_fp8", "csa2_index_topk_fp8_workspace_size",
     "csa2_index_topk_fp8",
     "csa2_topk_scores", "csa2_attn_workspace_size", "csa2_sparse_attn", "csa2_reuse_attn",
-    "csa2_sparse_attn_rope", "csa2_reuse_attn_rope",
+    "csa2_sparse_attn_rope", "csa2_reuse_attn_rope", "csa2_plane_fp4_bytes", "csa2_plane_fp4",
+    "csa2_sparse_attn_fp4",
 ]
 
 STATUS = {0: "CSA2_OK", 1: "CSA2_EINVAL", 2: "CSA2_ECUDA", 3: "CSA2_ETIMEOUT", 4: "CSA2_EBOUNDS",
@@ -76,6 +77,10 @@ _SIGS = {
                          _vp, _f32, _vp, _vp, _vp, _sz, _vp], _i32),
     "csa2_sparse_attn_rope": ([_vp, _i32, _vp, _vp, ctypes.POINTER(_SwaC), _vp, _i64, _vp, _vp,
                                _i32, _vp, _f32, _vp, _vp, _vp, _sz, _vp, _vp], _i32),
+    "csa2_plane_fp4_bytes": ([_i64], _sz),
+    "csa2_plane_fp4": ([_vp, _i64, _vp, _vp], _i32),
+    "csa2_sparse_attn_fp4": ([_vp, _i32, _vp, _vp, ctypes.POINTER(_SwaC), _vp, _i64, _vp, _vp,
+                              _i32, _vp, _f32, _vp, _vp, _vp, _sz, _vp, _vp], _i32),
     "csa2_reuse_attn_rope": ([_vp, _i32, _vp, _vp, ctypes.POINTER(_SwaC), _vp, _i64, _vp, _vp,
                               _i32, _vp, _f32, _vp, _vp, _vp, _sz, _vp, _vp], _i32),
 }
@@ -282,3 +287,25 @@ def csa2_reuse_attn_rope(q, q_seq, q_pos, swa: Swa, plane, row_base, sel, sink, 
     """csa2_reuse_attn with the output's dims 448..511 rotated back by q_pos."""
     _attn(lib().csa2_reuse_attn_rope, q, q_seq, q_pos, swa, plane, row_base, sel, sink, out,
           lse, scale, ws, stream, inv_freq)
+
+
+def csa2_plane_fp4_bytes(rows):
+    return int(lib().csa2_plane_fp4_bytes(rows))
+
+
+def csa2_plane_fp4(plane, out, stream=None):
+    """bf16 plane rows [rows, 512] -> FP4 rows (288 bytes each) in out."""
+    _check(lib().csa2_plane_fp4(_p(plane), plane.shape[0], _p(out), _stream(stream)))
+
+
+def csa2_sparse_attn_fp4(q, q_seq, q_pos, swa, plane4, plane_rows, row_base, sel, sink, out,
+                         inv_freq=None, lse=None, scale=512 ** -0.5, ws=None, stream=None):
+    """csa2_sparse_attn with the selected rows read from an FP4 plane of plane_rows rows."""
+    Q = q.shape[0]
+    nsel = 0 if sel is None else sel.shape[1]
+    sw = swa.c()
+    nbytes = 0 if ws is None else ws.numel() * ws.element_size()
+    _check(lib().csa2_sparse_attn_fp4(_p(q), Q, _p(q_seq), _p(q_pos), ctypes.byref(sw),
+                                      _p(plane4), plane_rows, _p(row_base), _p(sel), nsel,
+                                      _p(sink), float(scale), _p(out), _p(lse), _p(ws), nbytes,
+                                      _p(inv_freq), _stream(stream)))

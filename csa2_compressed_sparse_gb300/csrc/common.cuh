@@ -132,10 +132,14 @@ struct AttnArgs {
   float* part_ml;  // [Q][nsplit][2][64] partial running max (log2) and sum
   int cluster;     // nsplit == 2: the two CTAs of a query form a cluster and merge in place
   const float* inv_freq;  // [32] or null: rotate the output's dims 448..511 back by q_pos
+  int plane_dtype;        // 0: bf16 plane rows [512]; 1: FP4 rows of 288 bytes (E2M1 codes,
+                          //    low nibble first, then 32 E4M3 scales, one per 16 dims)
 };
 
 cudaError_t launch_compress(const CompressArgs& a, cudaStream_t s);
 cudaError_t launch_index(const IndexArgs& a, int num_sms, cudaStream_t s);
+// bf16 plane rows [n][512] -> FP4 rows [n][288].
+cudaError_t launch_plane_fp4(const uint16_t* rows, int64_t n, uint8_t* out, cudaStream_t s);
 // bf16 index rows [n][128] -> FP8 plane (ceil(n / 8) blocks of 1056 bytes).
 cudaError_t launch_plane_fp8(const uint16_t* k, int64_t n, uint8_t* plane, cudaStream_t s);
 // One launch for selection `a` and, when b != null, a second selection over the same

@@ -115,10 +115,10 @@ size_t attn_ws_bytes(int Q, int nsplit) {
 }
 
 csa2_status attn_common(const char* name, const csa2_bf16* q, int Q, const int32_t* q_seq,
-                        const int64_t* q_pos, const csa2_swa* swa, const csa2_bf16* plane,
+                        const int64_t* q_pos, const csa2_swa* swa, const void* plane,
                         int64_t plane_rows, const int64_t* row_base, const int32_t* sel, int nsel,
                         const float* sink, float scale, csa2_bf16* out, float* lse, void* ws,
-                        size_t ws_bytes, const float* inv_freq, csa2_stream stream) {
+                        size_t ws_bytes, const float* inv_freq, int plane_dtype, csa2_stream stream) {
   REQUIRE(Q >= 0 && Q <= 65535, "%s: Q must be in [0, 65535] (got %d)", name, Q);
   if (Q == 0) return CSA2_OK;
   REQUIRE(q && q_seq && q_pos && swa && out, "%s: q, q_seq, q_pos, swa and out are required", name);
@@ -141,7 +141,8 @@ csa2_status attn_common(const char* name, const csa2_bf16* q, int Q, const int32
   a.swa_mode = swa->mode; a.swa_dtype = swa->dtype;
   a.swa = static_cast<const uint8_t*>(swa->data); a.swa_rows = swa->n_rows;
   a.lin_base = swa->lin_base; a.lin_pos0 = swa->lin_pos0;
-  a.plane = plane; a.plane_rows = plane_rows; a.row_base = row_base;
+  a.plane = static_cast<const uint16_t*>(plane); a.plane_rows = plane_rows; a.row_base = row_base;
+  a.plane_dtype = plane_dtype;
   a.sel = sel; a.nsel = nsel; a.sink = sink; a.scale = scale; a.out = out; a.lse = lse;
   a.inv_freq = inv_freq;
   REQUIRE(ws == nullptr || (reinterpret_cast<uintptr_t>(ws) & 255u) == 0,
@@ -458,7 +459,7 @@ csa2_status csa2_sparse_attn(const csa2_bf16* q, int Q, const int32_t* q_seq,
                              int nsel, const float* sink, float scale, csa2_bf16* out, float* lse,
                              void* ws, size_t ws_bytes, csa2_stream stream) {
   return attn_common("csa2_sparse_attn", q, Q, q_seq, q_pos, swa, plane, plane_rows, row_base,
-                     sel, nsel, sink, scale, out, lse, ws, ws_bytes, nullptr, stream);
+                     sel, nsel, sink, scale, out, lse, ws, ws_bytes, nullptr, 0, stream);
 }
 
 csa2_status csa2_reuse_attn(const csa2_bf16* q, int Q, const int32_t* q_seq,
@@ -467,7 +468,7 @@ csa2_status csa2_reuse_attn(const csa2_bf16* q, int Q, const int32_t* q_seq,
                             int nsel, const float* sink, float scale, csa2_bf16* out, float* lse,
                             void* ws, size_t ws_bytes, csa2_stream stream) {
   return attn_common("csa2_reuse_attn", q, Q, q_seq, q_pos, swa, plane, plane_rows, row_base,
-                     sel, nsel, sink, scale, out, lse, ws, ws_bytes, nullptr, stream);
+                     sel, nsel, sink, scale, out, lse, ws, ws_bytes, nullptr, 0, stream);
 }
 
 csa2_status csa2_sparse_attn_rope(const csa2_bf16* q, int Q, const int32_t* q_seq,
@@ -479,7 +480,8 @@ csa2_status csa2_sparse_attn_rope(const csa2_bf16* q, int Q, const int32_t* q_se
                                   csa2_stream stream) {
   REQUIRE(inv_freq != nullptr, "csa2_sparse_attn_rope: inv_freq is required");
   return attn_common("csa2_sparse_attn_rope", q, Q, q_seq, q_pos, swa, plane, plane_rows,
-                     row_base, sel, nsel, sink, scale, out, lse, ws, ws_bytes, inv_freq, stream);
+                     row_base, sel, nsel, sink, scale, out, lse, ws, ws_bytes, inv_freq, 0,
+                     stream);
 }
 
 csa2_status csa2_reuse_attn_rope(const csa2_bf16* q, int Q, const int32_t* q_seq,
@@ -491,7 +493,33 @@ csa2_status csa2_reuse_attn_rope(const csa2_bf16* q, int Q, const int32_t* q_seq
                                  csa2_stream stream) {
   REQUIRE(inv_freq != nullptr, "csa2_reuse_attn_rope: inv_freq is required");
   return attn_common("csa2_reuse_attn_rope", q, Q, q_seq, q_pos, swa, plane, plane_rows,
-                     row_base, sel, nsel, sink, scale, out, lse, ws, ws_bytes, inv_freq, stream);
+                     row_base, sel, nsel, sink, scale, out, lse, ws, ws_bytes, inv_freq, 0,
+                     stream);
+}
+
+csa2_status csa2_sparse_attn_fp4(const csa2_bf16* q, int Q, const int32_t* q_seq,
+                                 const int64_t* q_pos, const csa2_swa* swa, const uint8_t* plane,
+                                 int64_t plane_rows, const int64_t* row_base, const int32_t* sel,
+                                 int nsel, const float* sink, float scale, csa2_bf16* out,
+                                 float* lse, void* ws, size_t ws_bytes, const float* inv_freq,
+                                 csa2_stream stream) {
+  return attn_common("csa2_sparse_attn_fp4", q, Q, q_seq, q_pos, swa, plane, plane_rows,
+                     row_base, sel, nsel, sink, scale, out, lse, ws, ws_bytes, inv_freq, 1,
+                     stream);
+}
+
+size_t csa2_plane_fp4_bytes(int64_t rows) { return rows <= 0 ? 0 : (size_t)rows * 288; }
+
+csa2_status csa2_plane_fp4(const csa2_bf16* plane, int64_t rows, uint8_t* out,
+                           csa2_stream stream) {
+  REQUIRE(rows >= 0 && rows < (int64_t)1 << 31, "csa2_plane_fp4: rows out of range");
+  if (rows == 0) return CSA2_OK;
+  REQUIRE(plane && out, "csa2_plane_fp4: plane and out are required");
+  REQUIRE(aligned16(plane) && aligned16(out), "csa2_plane_fp4: plane and out must be 16-byte aligned");
+  cudaError_t e =
+      csa2::launch_plane_fp4(reinterpret_cast<const uint16_t*>(plane), rows, out, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "csa2_plane_fp4");
+  return CSA2_OK;
 }
 
 }  // extern "C"

@@ -39,6 +39,7 @@
 //
 // Warps 0..3 softmax + O^T rescale + output, warps 4..19 gather (teams of eight
 // warps), warps 20..23 issue the MMAs (lane 0 each; warp 20 also owns the TMEM).
+#include <cuda_fp4.h>
 #include <cuda_fp8.h>
 
 #include "common.cuh"
@@ -264,9 +265,41 @@ __device__ __forceinline__ void out_pass(const float* own, const float* peer, co
 
 // Rows of one chunk into the KV buffer at `kvb` by the threads of a team (t = 0..255);
 // a row index below zero gives a row of zeros.
-__device__ __forceinline__ void gather_chunk(const int32_t* rows, bool fp8, const uint8_t* base,
-                                             uint32_t kvb, int t) {
-  if (fp8) {
+__device__ __forceinline__ void gather_chunk(const int32_t* rows, bool fp8, bool fp4,
+                                             const uint8_t* base, uint32_t kvb, int t) {
+  if (fp4) {
+    // FP4 plane rows: 64 rows x 32 groups of 16 dims (8 code bytes + 1 scale byte); each
+    // group becomes two 16-byte bf16 chunks.  E2M1 x E4M3 has at most six significant
+    // bits, so the bf16 values are exact.
+#pragma unroll 2
+    for (int i = 0; i < 64 * 32 / kTeam; ++i) {
+      const int flat = i * kTeam + t;
+      const int r = flat >> 5, g = flat & 31;
+      const int64_t off = rows[r] < 0 ? -1 : (int64_t)rows[r] * 288;
+      const uint32_t d0 = kvb + (g >> 2) * kDimBlock + sw128_off(r, (2 * g) & 7);
+      const uint32_t d1 = kvb + (g >> 2) * kDimBlock + sw128_off(r, (2 * g + 1) & 7);
+      if (off < 0) { st_shared_zero16(d0); st_shared_zero16(d1); continue; }
+      const uint8_t* src = base + off;
+      const uint2 codes = *reinterpret_cast<const uint2*>(src + 8 * g);
+      const __half2_raw sr = __nv_cvt_fp8x2_to_halfraw2(
+          (__nv_fp8x2_storage_t)src[256 + g], __NV_E4M3);
+      const float sc = __low2float(*reinterpret_cast<const __half2*>(&sr));
+      const uint32_t w2[2] = {codes.x, codes.y};
+      uint32_t packed[8];
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {  // byte b of word j: dims 8 j + 2 b, + 1
+          const __half2_raw hr = __nv_cvt_fp4x2_to_halfraw2(
+              (__nv_fp4x2_storage_t)((w2[j] >> (8 * b)) & 0xFFu), __NV_E2M1);
+          const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&hr));
+          packed[4 * j + b] = pack_bf16x2(f.x * sc, f.y * sc);
+        }
+      }
+      st_shared16(d0, make_uint4(packed[0], packed[1], packed[2], packed[3]));
+      st_shared16(d1, make_uint4(packed[4], packed[5], packed[6], packed[7]));
+    }
+  } else if (fp8) {
     // 64 rows x 32 pieces of 16 codes; each piece becomes two 16-byte bf16 chunks
 #pragma unroll 2
     for (int i = 0; i < 64 * 32 / kTeam; ++i) {
@@ -436,7 +469,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         continue;
       }
       const uint8_t* base = c < 2 ? a.swa : reinterpret_cast<const uint8_t*>(a.plane);
-      gather_chunk(X.rowidx[slot], fp8, base, kvb, t);
+      gather_chunk(X.rowidx[slot], fp8, c >= 2 && a.plane_dtype == 1, base, kvb, t);
       cp_async_commit();
       cp_async_wait_group<0>();
       fence_proxy_async_smem();

@@ -16,6 +16,9 @@
 // Lane layout: lane l owns channels [8l, 8l+8) and [256+8l, 256+8l+8), i.e. two
 // 16-byte vectors per row (coalesced 1 KiB row accesses).  Lanes 24..31 hold the
 // RoPE dims 448..511 in their second vector, four adjacent pairs each.
+#include <cuda_fp4.h>
+#include <cuda_fp8.h>
+
 #include "common.cuh"
 
 CSA2_DEFINE_FAULT_FLAG(compress)
@@ -265,7 +268,56 @@ __global__ void __launch_bounds__(kWarps * 32) compress_kernel(CompressArgs a) {
   }
 }
 
+// E4M3 value of a code below 0x7F, from the format's fields.
+__device__ __forceinline__ float e4m3_value(uint32_t c) {
+  const uint32_t e = (c >> 3) & 15u, m = c & 7u;
+  return e == 0 ? (float)m * (1.f / 512.f) : __uint_as_float(((e + 120u) << 23) | (m << 20));
+}
+
+// FP4 plane rows ([A] pool switch: nvfp4 rows of 288 B, E2M1 with an E4M3 scale per 16
+// dims): one warp per row, lane l quantises dims 16 l .. 16 l + 15.  The scale is the
+// smallest E4M3 value s with 6 s >= max |x| (0 for an all-zero group; 448 at most),
+// found from the nearest code and one exact comparison; codes are E2M1(x / s).
+__global__ void __launch_bounds__(256) plane_fp4_kernel(const uint16_t* rows, int64_t n,
+                                                        uint8_t* out) {
+  griddep_launch_dependents();
+  griddep_wait();
+  const int lane = threadIdx.x & 31;
+  const int64_t r = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (r >= n) return;
+  float v[16];
+  load8_bf16(rows + r * kDLat + 16 * lane, *reinterpret_cast<float(*)[8]>(v));
+  load8_bf16(rows + r * kDLat + 16 * lane + 8, *reinterpret_cast<float(*)[8]>(v + 8));
+  float amax = 0.f;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(v[i]));
+  uint32_t sc = 0;
+  if (amax > 0.f) {
+    sc = (uint32_t)__nv_cvt_float_to_fp8(amax / 6.f, __NV_SATFINITE, __NV_E4M3);
+    if (6.f * e4m3_value(sc) < amax && sc < 0x7Eu) ++sc;  // 6 * value is exact in fp32
+  }
+  const float s = e4m3_value(sc);
+  uint32_t w[2] = {0u, 0u};
+  if (sc != 0) {
+#pragma unroll
+    for (int i = 0; i < 16; i += 2) {
+      const uint32_t two = (uint32_t)__nv_cvt_float2_to_fp4x2(make_float2(v[i] / s, v[i + 1] / s),
+                                                              __NV_E2M1, cudaRoundNearest);
+      w[i >> 3] |= (two & 0xFFu) << (8 * ((i & 7) >> 1));
+    }
+  }
+  uint8_t* o = out + r * 288;
+  *reinterpret_cast<uint2*>(o + 8 * lane) = make_uint2(w[0], w[1]);
+  o[256 + lane] = (uint8_t)sc;
+}
+
 }  // namespace
+
+cudaError_t launch_plane_fp4(const uint16_t* rows, int64_t n, uint8_t* out, cudaStream_t s) {
+  if (n <= 0) return cudaSuccess;
+  return launch_pdl(plane_fp4_kernel, dim3((unsigned)((n + 7) / 8)), dim3(256), 0, s, rows, n,
+                    out);
+}
 
 cudaError_t launch_compress(const CompressArgs& a, cudaStream_t s) {
   if (a.T == 0) return cudaSuccess;

@@ -356,6 +356,34 @@ csa2_status csa2_reuse_attn_rope(const csa2_bf16* q, int Q, const int32_t* q_seq
                                  void* ws, size_t ws_bytes, const float* inv_freq,
                                  csa2_stream stream);
 
+/* ---------------------------------------------------------------------------------
+ * csa2_plane_fp4 -- the FP4 main plane.  [A] pool switch ("nvfp4": main plane rows of
+ * 288 B, the 512 dims as E2M1 with an E4M3 scale per group of 16).
+ *
+ * Row r of plane [rows][512] bf16 becomes 288 bytes: bytes 0..255 the 512 E2M1 codes,
+ * dim 2i in the low nibble of byte i and dim 2i + 1 in its high nibble; bytes 256..287
+ * the 32 E4M3 scales, scale g for dims 16g .. 16g + 15.  A group's scale is the smallest
+ * E4M3 value s with 6 s >= max |x| (0 for an all-zero group, 448 at most); its codes are
+ * E2M1(x / s), nearest, ties to even, saturating at 6 (0 when s == 0).  The value of dim
+ * d is E2M1(code) * E4M3(scale), which bf16 holds exactly.
+ *   out  csa2_plane_fp4_bytes(rows) bytes, 16-byte aligned; plane 16-byte aligned */
+size_t csa2_plane_fp4_bytes(int64_t rows);
+csa2_status csa2_plane_fp4(const csa2_bf16* plane, int64_t rows, uint8_t* out,
+                           csa2_stream stream);
+
+/* ---------------------------------------------------------------------------------
+ * csa2_sparse_attn_fp4 -- csa2_sparse_attn (or csa2_reuse_attn: the same computation)
+ * reading the selected rows from an FP4 plane (csa2_plane_fp4 layout, plane_rows rows
+ * of 288 bytes); the window is unchanged.  Each selected row is dequantised exactly to
+ * bf16 before the dot products.  inv_freq: NULL, or the table of csa2_sparse_attn_rope
+ * for the output's inverse RoPE.  [A] pool switch; the rest as csa2_sparse_attn. */
+csa2_status csa2_sparse_attn_fp4(const csa2_bf16* q, int Q, const int32_t* q_seq,
+                                 const int64_t* q_pos, const csa2_swa* swa, const uint8_t* plane,
+                                 int64_t plane_rows, const int64_t* row_base, const int32_t* sel,
+                                 int nsel, const float* sink, float scale, csa2_bf16* out,
+                                 float* lse, void* ws, size_t ws_bytes, const float* inv_freq,
+                                 csa2_stream stream);
+
 #ifdef __cplusplus
 }
 #endif

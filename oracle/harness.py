@@ -13,7 +13,7 @@ import torch
 
 import synth
 
-from . import bf16_bits, bf16_from_bits, compress, index_scores, sparse_attn, topk
+from . import bf16_bits, bf16_from_bits, compress, index_scores, plane_fp4, sparse_attn, topk
 
 # ---- host regeneration of one sequence's inputs ------------------------------------------
 
@@ -111,9 +111,10 @@ def window_rows(wl, q, layer):
     return dict(swa=lin, swa_mode="linear", lin_base=[0], lin_pos0=[lo])
 
 
-def oracle_attn(wl, key, q, sel, layer=0, head_scale=None, inv_freq=None):
+def oracle_attn(wl, key, q, sel, layer=0, head_scale=None, inv_freq=None, fp4_plane=False):
     """Oracle output and lse of query q over its window and `sel`.  `head_scale`
-    (optional, 64 powers of two) multiplies the query of each head, exactly in bf16."""
+    (optional, 64 powers of two) multiplies the query of each head, exactly in bf16.
+    fp4_plane: the selected rows are read through the FP4 plane format."""
     b = int(wl.q_seq[q])
     hs = host_seq(key, b)
     sel = np.asarray(sel, dtype=np.int32)
@@ -127,8 +128,9 @@ def oracle_attn(wl, key, q, sel, layer=0, head_scale=None, inv_freq=None):
         qh = (qh.double() * hsc).to(torch.bfloat16)  # exact for powers of two
     win = window_rows(wl, q, layer)
     sink = synth.normal_f32(64, wl.seed, synth.SINK)
+    plane_in = plane_fp4(bf16_from_bits(plane)) if fp4_plane else bf16_from_bits(plane)
     out, lse = sparse_attn(qh, [0], [int(wl.q_pos[q])], win["swa"],
-                                  bf16_from_bits(plane), [0], sel_c.reshape(1, -1), sink,
+                                  plane_in, [0], sel_c.reshape(1, -1), sink,
                                   swa_mode=win["swa_mode"], lin_base=win["lin_base"],
                                   lin_pos0=win["lin_pos0"], inv_freq=inv_freq)
     return out[0], lse[0]

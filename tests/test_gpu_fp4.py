@@ -1,0 +1,94 @@
+"""The FP4 main plane through the C ABI: the quantiser is bit-exact against the oracle's,
+and the attention reading FP4 plane rows matches the oracle's (which decodes the same
+format by definition) within the attention tolerance, on ring, FP8 ring and linear
+windows, one, two (cluster) and several CTAs per query, with and without the inverse
+RoPE.  The selected rows are history rows (bit-identical on host and device), drawn
+without replacement per query with some -1 entries."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from synth import workloads as W
+
+from _harness import check_attn, oracle_attn, register, spec_of
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a GPU")
+
+
+def test_plane_fp4_quantiser_is_bit_exact():
+    from csa2_compressed_sparse_gb300 import (csa2_device_status, csa2_plane_fp4,
+                                              csa2_plane_fp4_bytes)
+    g = np.random.default_rng(9)
+    n = 333
+    x = g.standard_normal((n, 512)) * np.exp2(g.integers(-12, 12, (n, 32)).repeat(16, axis=1))
+    x[4, :16] = 0.0                                   # an all-zero group
+    e4 = np.array([oracle.e4m3_value(c) for c in range(1, 0x7F)])
+    mids = np.array([0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0, 6.0])
+    for r in range(8, 40):                            # E2M1 ties at exact E4M3 scales
+        s = e4[g.integers(20, 110)]
+        x[r, :16] = g.choice(mids, 16) * s * g.choice([-1.0, 1.0], 16)
+        x[r, 0] = 6.0 * s                             # pins the scale to s
+    x[41, :16] = 1e-30                                # tiny: the smallest scales
+    k = torch.from_numpy(x.astype(np.float32)).bfloat16()
+    out = torch.full((csa2_plane_fp4_bytes(n),), 0xA5, dtype=torch.uint8, device="cuda")
+    csa2_plane_fp4(k.cuda(), out)
+    csa2_device_status()
+    ref = oracle.plane_fp4(k).reshape(-1)
+    got = out.cpu().numpy()
+    bad = np.nonzero(got != ref)[0]
+    assert bad.size == 0, f"{bad.size} bytes differ, first row {bad[0] // 288} byte {bad[0] % 288}"
+
+
+def _sel_history(wl, nsel, seed):
+    g = np.random.default_rng(seed)
+    sel = np.full((wl.Q, nsel), -1, dtype=np.int32)
+    for q in range(wl.Q):
+        nh = int(wl.n_hist[wl.q_seq[q]])
+        take = min(nsel - nsel // 8, nh)
+        sel[q, :take] = np.sort(g.choice(nh, take, replace=False))
+    return sel
+
+
+@pytest.mark.parametrize("name", ["ring", "fp8ring", "linear", "many"])
+def test_attention_on_an_fp4_plane_matches_the_oracle(name):
+    from csa2_compressed_sparse_gb300 import (csa2_attn_workspace_size, csa2_device_status,
+                                              csa2_plane_fp4, csa2_plane_fp4_bytes,
+                                              csa2_sparse_attn_fp4)
+    from csa2_compressed_sparse_gb300.step import swa_of
+    if name == "ring":
+        wl = W.decode_batch(B=6, lo=3000, hi=9000, seed=81)
+    elif name == "fp8ring":
+        wl = W.Workload("fp4_fp8ring", 82, 1, ctx=[20000, 5001], chunk=[1, 1], nq=[1, 1],
+                        swa_dtype="fp8")
+    elif name == "linear":
+        wl = W.prefill_reuse(n_new=96, ctx=8192, layers=1, seed=83)
+    else:  # many queries: one CTA per query
+        wl = W.decode_batch(B=160, lo=2000, hi=4000, seed=84)
+    key = register(wl)
+    t = wl.materialize("cuda")
+    spec = spec_of(wl)
+    sel = _sel_history(wl, 512, seed=85)
+    rows = t["plane"].shape[0]
+    p4 = torch.empty(csa2_plane_fp4_bytes(rows), dtype=torch.uint8, device="cuda")
+    csa2_plane_fp4(t["plane"], p4)
+    out = torch.empty((wl.Q, 64, 512), dtype=torch.bfloat16, device="cuda")
+    ws = torch.empty(max(csa2_attn_workspace_size(wl.Q, 512), 256), dtype=torch.uint8,
+                     device="cuda")
+    for rope in (False, True):
+        invf = t["inv_freq"] if rope else None
+        csa2_sparse_attn_fp4(t["q"][0], t["q_seq"], t["q_pos"], swa_of(spec, t, 0), p4, rows,
+                             t["row_base"], torch.from_numpy(sel).cuda(), t["sink"], out,
+                             inv_freq=invf, ws=ws)
+        csa2_device_status()
+        got = out.float().cpu().numpy()
+        for q in sorted({0, wl.Q // 2, wl.Q - 1}):
+            ref, _ = oracle_attn(wl, key, q, sel[q], inv_freq=wl.inv_freq if rope else None,
+                                 fp4_plane=True)
+            check_attn(got[q], ref)
