@@ -270,21 +270,33 @@ __device__ __forceinline__ void gather_chunk(const int32_t* rows, bool fp8, bool
   if (fp4) {
     // FP4 plane rows: 64 rows x 32 groups of 16 dims (8 code bytes + 1 scale byte); each
     // group becomes two 16-byte bf16 chunks.  E2M1 x E4M3 has at most six significant
-    // bits, so the bf16 values are exact.
-#pragma unroll 2
-    for (int i = 0; i < 64 * 32 / kTeam; ++i) {
+    // bits, so the bf16 values are exact.  All of a thread's loads are issued before the
+    // first conversion.
+    constexpr int kItems = 64 * 32 / kTeam;
+    uint2 codes[kItems];
+    uint32_t scb[kItems];
+#pragma unroll
+    for (int i = 0; i < kItems; ++i) {
       const int flat = i * kTeam + t;
       const int r = flat >> 5, g = flat & 31;
-      const int64_t off = rows[r] < 0 ? -1 : (int64_t)rows[r] * 288;
+      codes[i] = make_uint2(0u, 0u);
+      scb[i] = 0u;
+      if (rows[r] >= 0) {
+        const uint8_t* src = base + (int64_t)rows[r] * 288;
+        codes[i] = __ldg(reinterpret_cast<const uint2*>(src + 8 * g));
+        scb[i] = __ldg(src + 256 + g);
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < kItems; ++i) {
+      const int flat = i * kTeam + t;
+      const int r = flat >> 5, g = flat & 31;
       const uint32_t d0 = kvb + (g >> 2) * kDimBlock + sw128_off(r, (2 * g) & 7);
       const uint32_t d1 = kvb + (g >> 2) * kDimBlock + sw128_off(r, (2 * g + 1) & 7);
-      if (off < 0) { st_shared_zero16(d0); st_shared_zero16(d1); continue; }
-      const uint8_t* src = base + off;
-      const uint2 codes = *reinterpret_cast<const uint2*>(src + 8 * g);
-      const __half2_raw sr = __nv_cvt_fp8x2_to_halfraw2(
-          (__nv_fp8x2_storage_t)src[256 + g], __NV_E4M3);
+      // a missing row has zero codes and scale code 0: its values are zero
+      const __half2_raw sr = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)scb[i], __NV_E4M3);
       const float sc = __low2float(*reinterpret_cast<const __half2*>(&sr));
-      const uint32_t w2[2] = {codes.x, codes.y};
+      const uint32_t w2[2] = {codes[i].x, codes[i].y};
       uint32_t packed[8];
 #pragma unroll
       for (int j = 0; j < 2; ++j) {
