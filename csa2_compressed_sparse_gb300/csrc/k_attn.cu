@@ -389,7 +389,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_alloc(smem_u32(&X.tmem_slot), 512);
     tmem_relinquish();
   }
-  griddep_wait();
+  // ---- before the dependency wait: only this call's inputs (q, positions, the window),
+  // never the selection a preceding kernel may still be writing ----
   const uint32_t qb = smem_u32(q_s), kv0 = smem_u32(kv_s), p0 = smem_u32(p_s);
   if (tid == 0) {
     // Q [64 heads][512] of this query: eight 64 x 64 boxes, one per dim block
@@ -403,40 +404,86 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int64_t p = a.q_pos[q];
   const float scale2 = a.scale * kLog2e;
   const int nchunks_total = 2 + (a.nsel + kChunk - 1) / kChunk;
-
-  // ---- row sources of this CTA's chunks (chunk = rank + slot * nsplit), one pass ----
-  {
-    const int nslot = (nchunks_total - rank + nsplit - 1) / nsplit;
-    const int64_t rb = a.row_base[b];
-    for (int e = tid; e < nslot * kChunk; e += kThreads) {
-      const int slot = e >> 6, r = e & 63;
-      const int c = rank + slot * nsplit;
-      int32_t idx32 = -1;
-      if (c < 2) {
-        const int64_t pos = p - (kRing - 1) + kChunk * c + r;
-        if (pos >= 0) {
-          int64_t idx;
-          if (a.swa_mode == 0) idx = (int64_t)b * kRing + (pos & (kRing - 1));
-          else idx = a.lin_base[b] + (pos - a.lin_pos0[b]);
-          if (idx >= 0 && idx < a.swa_rows) idx32 = (int32_t)idx;
+  // row sources of this CTA's chunks (chunk = rank + slot * nsplit): the window slots
+  // (chunks 0, 1) now, the selected ones after the wait
+  const int nslot = (nchunks_total - rank + nsplit - 1) / nsplit;
+  int nwin = 0;  // window slots come first
+  while (nwin < nslot && rank + nwin * nsplit < 2) ++nwin;
+  const int64_t rb = a.row_base[b];
+  auto row_source = [&](int e) {
+    const int slot = e >> 6, r = e & 63;
+    const int c = rank + slot * nsplit;
+    int32_t idx32 = -1;
+    if (c < 2) {
+      const int64_t pos = p - (kRing - 1) + kChunk * c + r;
+      if (pos >= 0) {
+        int64_t idx;
+        if (a.swa_mode == 0) idx = (int64_t)b * kRing + (pos & (kRing - 1));
+        else idx = a.lin_base[b] + (pos - a.lin_pos0[b]);
+        if (idx >= 0 && idx < a.swa_rows) idx32 = (int32_t)idx;
+        else raise_fault(kFaultBounds);
+      }
+    } else {
+      const int i = (c - 2) * kChunk + r;
+      if (i < a.nsel) {
+        const int32_t rr = a.sel[(int64_t)q * a.nsel + i];
+        if (rr >= 0) {
+          const int64_t idx = rb + rr;
+          if (idx >= 0 && idx < a.plane_rows) idx32 = (int32_t)idx;
           else raise_fault(kFaultBounds);
         }
-      } else {
-        const int i = (c - 2) * kChunk + r;
-        if (i < a.nsel) {
-          const int32_t rr = a.sel[(int64_t)q * a.nsel + i];
-          if (rr >= 0) {
-            const int64_t idx = rb + rr;
-            if (idx >= 0 && idx < a.plane_rows) idx32 = (int32_t)idx;
-            else raise_fault(kFaultBounds);
-          }
-        }
       }
-      X.rowidx[slot][r] = idx32;
-      // the 32 lanes of a warp cover one half of a slot (768 threads = 24 warps)
-      const uint32_t vm = __ballot_sync(0xFFFFFFFFu, idx32 >= 0);
-      if (lane == 0) X.rowmask[slot][r >> 5] = vm;
     }
+    X.rowidx[slot][r] = idx32;
+    // the 32 lanes of a warp cover one half of a slot (768 threads = 24 warps)
+    const uint32_t vm = __ballot_sync(0xFFFFFFFFu, idx32 >= 0);
+    if (lane == 0) X.rowmask[slot][r >> 5] = vm;
+  };
+  for (int e = tid; e < nwin * kChunk; e += kThreads) row_source(e);
+  __syncthreads();
+  // The non-empty window slots are the CTA's first chunks, so gather team t (t = 0, 1)
+  // owns the t-th of them: it issues that gather now, before the wait.
+  const bool is_gather = warp >= kGatherWarp0 && warp < kMmaWarp;
+  const int team = is_gather ? (warp - kGatherWarp0) / (kTeam / 32) : 0;
+  const int t_in_team = tid - kGatherWarp0 * 32 - kTeam * team;
+  int pre_slot = -1;  // uniform within a team
+  {
+    int k = 0;
+    for (int slot = 0; slot < nwin; ++slot)
+      if (X.rowmask[slot][0] | X.rowmask[slot][1]) {
+        if (k == team) pre_slot = slot;
+        ++k;
+      }
+  }
+  auto issue_gather = [&](int slot) -> bool {  // true: a TMA box load (arrives by itself)
+    const int c = rank + slot * nsplit;
+    const uint32_t kvb = kv0 + team * kBufBytes;
+    const uint32_t full_bar = smem_u32(&X.kv_full[team]);
+    // a full window chunk of a LINEAR bf16 window is 64 consecutive rows: one TMA box
+    // of 64 x 64 per dim block
+    if (c < 2 && a.swa_mode == 1 && a.swa_dtype == 0 &&
+        (X.rowmask[slot][0] & X.rowmask[slot][1]) == 0xFFFFFFFFu) {
+      if (t_in_team == 0) {
+        mbar_arrive_expect_tx(full_bar, kBufBytes);
+        const int32_t y0 = X.rowidx[slot][0];
+        const uint64_t pol = policy_evict_first();
+#pragma unroll
+        for (int db = 0; db < 8; ++db)
+          tma_load_2d(kvb + db * kDimBlock, &wmap, 64 * db, y0, full_bar, pol);
+      }
+      return true;
+    }
+    const bool fp8 = c < 2 && a.swa_dtype == 1;
+    const uint8_t* base = c < 2 ? a.swa : reinterpret_cast<const uint8_t*>(a.plane);
+    gather_chunk(X.rowidx[slot], fp8, c >= 2 && a.plane_dtype == 1, base, kvb, t_in_team);
+    cp_async_commit();
+    return false;
+  };
+  bool pre_tma = false;
+  if (is_gather && pre_slot >= 0) pre_tma = issue_gather(pre_slot);
+  griddep_wait();
+  {
+    for (int e = nwin * kChunk + tid; e < nslot * kChunk; e += kThreads) row_source(e);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -451,11 +498,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int n = X.nchunk;
   const uint32_t tmem = X.tmem_slot;
 
-  if (warp >= kGatherWarp0 && warp < kMmaWarp) {
+  if (is_gather) {
     // =================== gather: team 0 = warps 4..11; team 1 = warps 12..19 ===================
-    const int team = (warp - kGatherWarp0) / (kTeam / 32);
-    const int t = tid - kGatherWarp0 * 32 - kTeam * team;
-    const uint32_t kvb = kv0 + team * kBufBytes;
+    const int t = t_in_team;
     const uint32_t full_bar = smem_u32(&X.kv_full[team]);
     int last = -1;  // last chunk of this team (its kv_full phase ends every copy of the team)
     for (int it = team; it < n; it += 2) {
@@ -464,25 +509,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           !mbar_wait(smem_u32(&X.pv_done[team]), (uint32_t)((it - 2) >> 1) & 1))
         X.abort = 1;
       const int slot = X.chunks[it];
-      const int c = rank + slot * nsplit;
-      const bool fp8 = c < 2 && a.swa_dtype == 1;
-      // a full window chunk of a LINEAR bf16 window is 64 consecutive rows: one TMA box
-      // of 64 x 64 per dim block
-      if (c < 2 && a.swa_mode == 1 && a.swa_dtype == 0 &&
-          (X.rowmask[slot][0] & X.rowmask[slot][1]) == 0xFFFFFFFFu) {
-        if (t == 0) {
-          mbar_arrive_expect_tx(full_bar, kBufBytes);
-          const int32_t y0 = X.rowidx[slot][0];
-          const uint64_t pol = policy_evict_first();
-#pragma unroll
-          for (int db = 0; db < 8; ++db)
-            tma_load_2d(kvb + db * kDimBlock, &wmap, 64 * db, y0, full_bar, pol);
-        }
-        continue;
-      }
-      const uint8_t* base = c < 2 ? a.swa : reinterpret_cast<const uint8_t*>(a.plane);
-      gather_chunk(X.rowidx[slot], fp8, c >= 2 && a.plane_dtype == 1, base, kvb, t);
-      cp_async_commit();
+      // the team's first chunk may have been issued before the wait (a window slot)
+      const bool tma = it == team && pre_slot >= 0 ? pre_tma : issue_gather(slot);
+      if (tma) continue;
       cp_async_wait_group<0>();
       fence_proxy_async_smem();
       // every thread of the team has landed its rows
