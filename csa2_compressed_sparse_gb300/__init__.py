@@ -30,7 +30,7 @@ __all__ = [
 STATUS = {0: "CSA2_OK", 1: "CSA2_EINVAL", 2: "CSA2_ECUDA", 3: "CSA2_ETIMEOUT", 4: "CSA2_EBOUNDS",
           5: "CSA2_ENOSPACE"}
 SWA_RING, SWA_LINEAR = 0, 1
-SWA_BF16, SWA_FP8_S128 = 0, 1
+SWA_BF16, SWA_FP8_S128, SWA_FP8_E8M0 = 0, 1, 2
 
 
 class Csa2Error(RuntimeError):
@@ -138,10 +138,11 @@ class Swa:
     mode: int = SWA_RING
     lin_base: Optional[torch.Tensor] = None
     lin_pos0: Optional[torch.Tensor] = None
+    fp8_dtype: int = SWA_FP8_S128  # the layout of uint8 rows: SWA_FP8_S128 or SWA_FP8_E8M0
 
     def c(self):
-        dtype = SWA_FP8_S128 if self.data.dtype == torch.uint8 else SWA_BF16
-        row = 528 if dtype == SWA_FP8_S128 else 512
+        dtype = self.fp8_dtype if self.data.dtype == torch.uint8 else SWA_BF16
+        row = 512 if dtype == SWA_BF16 else 528
         n_rows = self.data.numel() // row
         return _SwaC(self.mode, dtype, _p(self.data), n_rows, _p(self.lin_base), _p(self.lin_pos0))
 

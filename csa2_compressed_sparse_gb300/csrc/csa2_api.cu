@@ -127,7 +127,9 @@ csa2_status attn_common(const char* name, const csa2_bf16* q, int Q, const int32
   REQUIRE(nsel == 0 || (sel && plane && row_base), "%s: sel, plane and row_base are required when nsel > 0", name);
   REQUIRE(plane == nullptr || aligned16(plane), "%s: plane must be 16-byte aligned", name);
   REQUIRE(swa->mode == CSA2_SWA_RING || swa->mode == CSA2_SWA_LINEAR, "%s: bad swa.mode %d", name, swa->mode);
-  REQUIRE(swa->dtype == CSA2_SWA_BF16 || swa->dtype == CSA2_SWA_FP8_S128, "%s: bad swa.dtype %d", name, swa->dtype);
+  REQUIRE(swa->dtype == CSA2_SWA_BF16 || swa->dtype == CSA2_SWA_FP8_S128 ||
+              swa->dtype == CSA2_SWA_FP8_E8M0,
+          "%s: bad swa.dtype %d", name, swa->dtype);
   REQUIRE(swa->data && aligned16(swa->data), "%s: swa.data must be a 16-byte aligned pointer", name);
   REQUIRE(swa->n_rows >= 0, "%s: swa.n_rows must be >= 0", name);
   REQUIRE(swa->mode == CSA2_SWA_RING || (swa->lin_base && swa->lin_pos0),

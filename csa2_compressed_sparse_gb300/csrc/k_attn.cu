@@ -265,7 +265,7 @@ __device__ __forceinline__ void out_pass(const float* own, const float* peer, co
 
 // Rows of one chunk into the KV buffer at `kvb` by the threads of a team (t = 0..255);
 // a row index below zero gives a row of zeros.
-__device__ __forceinline__ void gather_chunk(const int32_t* rows, bool fp8, bool fp4,
+__device__ __forceinline__ void gather_chunk(const int32_t* rows, int fp8, bool fp4,
                                              const uint8_t* base, uint32_t kvb, int t) {
   if (fp4) {
     // FP4 plane rows: 64 rows x 32 groups of 16 dims (8 code bytes + 1 scale byte); each
@@ -323,7 +323,12 @@ __device__ __forceinline__ void gather_chunk(const int32_t* rows, bool fp8, bool
       if (off < 0) { st_shared_zero16(d0); st_shared_zero16(d1); continue; }
       const uint8_t* src = base + off;
       const uint4 codes = *reinterpret_cast<const uint4*>(src + c16 * 16);
-      const float sc = *reinterpret_cast<const float*>(src + 512 + 4 * (c16 >> 3));
+      // fp8 == 1: one fp32 scale per 128 dims; 2: one E8M0 byte per 32 dims (2^(e - 127))
+      const float sc = fp8 == 1
+                           ? *reinterpret_cast<const float*>(src + 512 + 4 * (c16 >> 3))
+                           : (src[512 + (c16 >> 1)] == 0
+                                  ? __uint_as_float(0x00400000u)  // 2^-127 (subnormal)
+                                  : __uint_as_float((uint32_t)src[512 + (c16 >> 1)] << 23));
       const uint32_t w4[4] = {codes.x, codes.y, codes.z, codes.w};
       uint32_t packed[8];
 #pragma unroll
@@ -473,7 +478,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       return true;
     }
-    const bool fp8 = c < 2 && a.swa_dtype == 1;
+    const int fp8 = c < 2 ? a.swa_dtype : 0;  // 1, 2: the FP8 window layouts
     const uint8_t* base = c < 2 ? a.swa : reinterpret_cast<const uint8_t*>(a.plane);
     gather_chunk(X.rowidx[slot], fp8, c >= 2 && a.plane_dtype == 1, base, kvb, t_in_team);
     cp_async_commit();

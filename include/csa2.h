@@ -291,7 +291,9 @@ csa2_status csa2_topk_scores(const float* scores, const int32_t* n, int Q, int64
  *          LINEAR: data holds rows; position pos of sequence b is row
  *                  lin_base[b] + pos - lin_pos0[b]
  *          BF16 rows are 512 bf16; FP8_S128 rows are 528 bytes: 512 E4M3 codes then
- *          four fp32 scales, value = code * scale[d / 128]
+ *          four fp32 scales, value = code * scale[d / 128]; FP8_E8M0 rows are 528
+ *          bytes: 512 E4M3 codes then 16 E8M0 scales, value = code * 2^(e[d / 32] - 127)
+ *          ([A] pool switch: nvfp4 window rows of 512 FP8 and 16 E8M0)
  *          n_rows = rows in data, < 2^31 (indices beyond raise CSA2_EBOUNDS and are
  *          skipped)
  *   plane  [plane_rows][512] bf16, plane_rows < 2^31;  row_base int64;
@@ -306,7 +308,7 @@ csa2_status csa2_topk_scores(const float* scores, const int32_t* n, int Q, int64
  *          query are used.  The size is 0 when no more are worth it.  The result does
  *          not depend on it beyond rounding. */
 typedef enum { CSA2_SWA_RING = 0, CSA2_SWA_LINEAR = 1 } csa2_swa_mode;
-typedef enum { CSA2_SWA_BF16 = 0, CSA2_SWA_FP8_S128 = 1 } csa2_swa_dtype;
+typedef enum { CSA2_SWA_BF16 = 0, CSA2_SWA_FP8_S128 = 1, CSA2_SWA_FP8_E8M0 = 2 } csa2_swa_dtype;
 typedef struct {
   int32_t mode;            /* csa2_swa_mode */
   int32_t dtype;           /* csa2_swa_dtype */

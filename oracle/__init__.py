@@ -247,14 +247,14 @@ def topk(scores, rows, k):
 
 
 def sparse_attn(q, q_seq, q_pos, swa, plane, row_base, sel, sink, scale=512 ** -0.5,
-                swa_mode="ring", lin_base=None, lin_pos0=None, inv_freq=None):
+                swa_mode="ring", lin_base=None, lin_pos0=None, inv_freq=None, swa_e8m0=False):
     """q [Q,64,512] bf16, swa ring [B,128,512] bf16 / [B,128,528] uint8 or linear rows,
     plane [rows,512] bf16, sel [Q,nsel] int32.  Returns (out [Q,64,512], lse [Q,64])
     in float64."""
     qb = bf16_bits(q)
     Q = qb.shape[0]
     if swa.dtype == torch.uint8:
-        swa_arr, dt = np.ascontiguousarray(swa.cpu().numpy()), 1
+        swa_arr, dt = np.ascontiguousarray(swa.cpu().numpy()), 2 if swa_e8m0 else 1
     else:
         swa_arr, dt = bf16_bits(swa), 0
     if isinstance(plane, np.ndarray) and plane.dtype == np.uint8:

@@ -470,7 +470,8 @@ int orc_topk(const double* scores, const int64_t* rows, int64_t n, int k, int32_
  *   lse_h = log(e^{sink_h} + sum_j e^{s_j})
  * sink == NULL drops the sink term.  swa_mode 0 = ring [B][128][512],
  * 1 = linear rows lin_base[b] + (pos - lin_pos0[b]).  swa_dtype 0 = bf16,
- * 1 = 528-byte FP8 rows (512 E4M3 codes then 4 fp32 scales, one per 128 codes).
+ * 1 = 528-byte FP8 rows (512 E4M3 codes then 4 fp32 scales, one per 128 codes),
+ * 2 = 528-byte FP8 rows with 16 E8M0 scales, one per 32 codes ([A] pool switch).
  * plane_dtype 0 = bf16 rows [.][512], 1 = FP4 rows of 288 B (orc_plane_fp4 layout). */
 void orc_sparse_attn(const uint16_t* q, int Q, const int32_t* q_seq, const int64_t* q_pos,
                      int swa_mode, int swa_dtype, const void* swa, const int64_t* lin_base,
@@ -498,9 +499,16 @@ void orc_sparse_attn(const uint16_t* q, int Q, const int32_t* q_seq, const int64
         if (swa_mode == 0) src = (const uint8_t*)swa + ((int64_t)b * RING + pos % RING) * 528;
         else src = (const uint8_t*)swa + (lin_base[b] + (pos - lin_pos0[b])) * 528;
         for (int d = 0; d < D_LAT; d++) {
-          float sc;
-          memcpy(&sc, src + 512 + 4 * (d / 128), 4);
-          x[(int64_t)e * D_LAT + d] = orc_e4m3_val(src[d]) * (double)sc;
+          double sc;
+          if (swa_dtype == 1) {
+            float f;
+            memcpy(&f, src + 512 + 4 * (d / 128), 4);
+            sc = (double)f;
+          } else { /* E8M0: 2^(e - 127), e = 255 is NaN */
+            int ex = src[512 + d / 32];
+            sc = ex == 255 ? NAN : ldexp(1.0, ex - 127);
+          }
+          x[(int64_t)e * D_LAT + d] = orc_e4m3_val(src[d]) * sc;
         }
       }
     }

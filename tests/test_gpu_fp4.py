@@ -92,3 +92,34 @@ def test_attention_on_an_fp4_plane_matches_the_oracle(name):
             ref, _ = oracle_attn(wl, key, q, sel[q], inv_freq=wl.inv_freq if rope else None,
                                  fp4_plane=True)
             check_attn(got[q], ref)
+
+
+def test_attention_on_an_e8m0_fp8_window_matches_the_oracle():
+    # the pool switch's 528-byte window rows (512 E4M3, 16 E8M0 scales) in a ring
+    from csa2_compressed_sparse_gb300 import (SWA_FP8_E8M0, SWA_RING, Swa, csa2_device_status,
+                                              csa2_sparse_attn)
+    g = np.random.default_rng(77)
+    B, Q = 3, 5
+    ring = np.zeros((B, 128, 528), dtype=np.uint8)
+    ring[..., :512] = (g.integers(0, 0x7F, (B, 128, 512)) |
+                       (g.integers(0, 2, (B, 128, 512)) << 7)).astype(np.uint8)
+    ring[..., 512:] = g.integers(121, 133, (B, 128, 16)).astype(np.uint8)
+    plane = torch.from_numpy(g.standard_normal((300, 512)).astype(np.float32)).bfloat16()
+    q = torch.from_numpy(g.standard_normal((Q, 64, 512)).astype(np.float32)).bfloat16()
+    q_seq = np.array([0, 1, 2, 2, 0], dtype=np.int32)
+    q_pos = np.array([700, 33, 1000, 999, 128], dtype=np.int64)
+    row_base = np.array([0, 100, 200], dtype=np.int64)
+    sel = g.integers(0, 100, (Q, 256)).astype(np.int32)
+    sel[:, 200:] = -1
+    sink = g.standard_normal(64).astype(np.float32)
+    out = torch.empty((Q, 64, 512), dtype=torch.bfloat16, device="cuda")
+    swa = Swa(torch.from_numpy(ring).cuda(), SWA_RING, fp8_dtype=SWA_FP8_E8M0)
+    csa2_sparse_attn(q.cuda(), torch.from_numpy(q_seq).cuda(), torch.from_numpy(q_pos).cuda(),
+                     swa, plane.cuda(), torch.from_numpy(row_base).cuda(),
+                     torch.from_numpy(sel).cuda(), torch.from_numpy(sink).cuda(), out)
+    csa2_device_status()
+    ref, _ = oracle.sparse_attn(q, q_seq, q_pos, torch.from_numpy(ring), plane, row_base, sel,
+                                sink, swa_e8m0=True)
+    got = out.float().cpu().numpy()
+    for i in range(Q):
+        check_attn(got[i], ref[i])

@@ -507,6 +507,34 @@ def test_attention_on_an_fp4_plane_equals_the_dequantised_bf16_plane():
     assert np.array_equal(a, b) and np.array_equal(la, lb)
 
 
+def _e8m0_ring(g, B):
+    """[B,128,528] uint8 rows: random finite E4M3 codes, then 16 E8M0 scales in 2^-6..2^5."""
+    ring = np.zeros((B, 128, 528), dtype=np.uint8)
+    codes = g.integers(0, 0x7F, (B, 128, 512)) | (g.integers(0, 2, (B, 128, 512)) << 7)
+    ring[..., :512] = codes.astype(np.uint8)
+    ring[..., 512:] = g.integers(121, 133, (B, 128, 16)).astype(np.uint8)
+    return ring
+
+
+def test_attention_on_an_e8m0_window_equals_the_dequantised_bf16_window():
+    # E4M3 times a power of two is exact in bf16: the E8M0 window path must give the
+    # bf16 path's result on the dequantised window, bit for bit
+    g = np.random.default_rng(31)
+    ring = _e8m0_ring(g, 1)
+    e4 = np.array([oracle.e4m3_value(c) for c in range(256)])
+    deq = e4[ring[..., :512]] * np.exp2(ring[..., 512:].astype(np.float64) - 127).repeat(32, axis=-1)
+    ring_bf = bf16(deq)
+    assert np.array_equal(bf16_np(ring_bf), deq)
+    plane = bf16(RNG.standard_normal((20, 512)))
+    q = bf16(RNG.standard_normal((2, 64, 512)))
+    sel = np.array([[3, 0, 19, -1], [5, -1, 11, 2]], dtype=np.int32)
+    sink = RNG.standard_normal(64).astype(np.float32)
+    a, la = oracle.sparse_attn(q, [0, 0], [300, 40], ring_bf, plane, [0], sel, sink)
+    b, lb = oracle.sparse_attn(q, [0, 0], [300, 40], torch.from_numpy(ring), plane, [0], sel,
+                               sink, swa_e8m0=True)
+    assert np.array_equal(a, b) and np.array_equal(la, lb)
+
+
 # ---- FP8 index plane (NEXT-3) --------------------------------------------------------
 
 def _e4m3_values():
