@@ -57,6 +57,11 @@ def lib():
         L.orc_e2m1_val.restype = _dbl
         L.orc_e2m1_code.argtypes = [_dbl]
         L.orc_e2m1_code.restype = ctypes.c_uint8
+        L.orc_index_plane_fp4.argtypes = [_vp, _i64, _vp]
+        L.orc_index_plane_fp4.restype = None
+        L.orc_index_scores_fp4.argtypes = [_vp, _vp, _i32, _i32, _vp, _vp, _vp, _vp, _i32, _vp,
+                                           _i32, _i32, _vp, _vp, _i64]
+        L.orc_index_scores_fp4.restype = None
         L.orc_plane_fp4.argtypes = [_vp, _i64, _vp]
         L.orc_plane_fp4.restype = None
         L.orc_sparse_attn.restype = None
@@ -229,6 +234,41 @@ def index_scores_fp8(iq, w, plane, row_base, q_seq, q_pos, ratio, cand=None, rel
     sc = np.zeros((Q, ld), dtype=np.float64)
     rows = np.zeros((Q, ld), dtype=np.int64)
     lib().orc_index_scores_fp8(_p(iqb), _p(wf), Q, H, _p(pl), _p(rb), _p(qs), _p(qp), ratio,
+                               _p(cd), ncb, 1 if relu else 0, _p(sc), _p(rows), ld)
+    return sc, rows
+
+
+FP4_INDEX_BLOCK_BYTES = 544  # 8 rows x 64 code bytes, then 8 x 4 E8M0 scales
+
+
+def index_plane_fp4(index_k):
+    """bf16 [n, 128] index rows -> MXFP4 plane bytes [ceil(n / 8) * 544] (uint8)."""
+    kb = bf16_bits(index_k)
+    n = kb.shape[0]
+    out = np.zeros(((n + 7) // 8) * FP4_INDEX_BLOCK_BYTES, dtype=np.uint8)
+    lib().orc_index_plane_fp4(_p(kb), n, _p(out))
+    return out
+
+
+def index_scores_fp4(iq, w, plane, row_base, q_seq, q_pos, ratio, cand=None, relu=True, ld=None):
+    """index_scores on an MXFP4 plane (row_base multiples of 8), bf16 queries."""
+    iqb = bf16_bits(iq)
+    Q, H = iqb.shape[0], iqb.shape[1]
+    wf = np.ascontiguousarray(w.detach().cpu().numpy() if isinstance(w, torch.Tensor) else w,
+                              dtype=np.float32)
+    pl = np.ascontiguousarray(plane, dtype=np.uint8)
+    rb = np.ascontiguousarray(row_base, dtype=np.int64)
+    assert np.all(rb % 8 == 0)
+    qs = np.ascontiguousarray(q_seq, dtype=np.int32)
+    qp = np.ascontiguousarray(q_pos, dtype=np.int64)
+    cd = None if cand is None else np.ascontiguousarray(cand, dtype=np.int32)
+    ncb = 0 if cand is None else cd.shape[1]
+    if ld is None:
+        ld = ncb * 8 if cand is not None else int(max(n_visible(p, ratio) for p in qp))
+    ld = max(int(ld), 1)
+    sc = np.zeros((Q, ld), dtype=np.float64)
+    rows = np.zeros((Q, ld), dtype=np.int64)
+    lib().orc_index_scores_fp4(_p(iqb), _p(wf), Q, H, _p(pl), _p(rb), _p(qs), _p(qp), ratio,
                                _p(cd), ncb, 1 if relu else 0, _p(sc), _p(rows), ld)
     return sc, rows
 

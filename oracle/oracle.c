@@ -417,6 +417,90 @@ static double fp4_plane_val(const uint8_t* row, int d) {
   return orc_e2m1_val(code) * orc_e4m3_val(row[256 + d / 16]);
 }
 
+/* ---- MXFP4 index plane [A] indexer figure (FP4 index rows of 68 B: 64 B of values and
+ *      4 B of scales; planes paged in blocks of 8 rows); [A] indexer K (E2M1 with one
+ *      E8M0 scale per 32 channels, pure powers of two) --------------------------------
+ *
+ * Block b holds rows 8b .. 8b+7: 8 x 64 code bytes (dim 2i in the low nibble of byte i),
+ * then 8 x 4 E8M0 scale bytes (scale j of a row for dims 32j .. 32j+31): 544 bytes.  A
+ * group's scale is the smallest 2^(e-127) with max |x| <= 6 * 2^(e-127) (e = 127 for an
+ * all-zero group), its codes E2M1(x / 2^(e-127)).  Rows of a partial last block past n
+ * are zero with e = 127. */
+void orc_index_plane_fp4(const uint16_t* k, int64_t n, uint8_t* plane) {
+  int64_t nb = (n + 7) / 8;
+  memset(plane, 0, (size_t)nb * 544);
+  for (int64_t r = 0; r < nb * 8; r++) {
+    uint8_t* blk = plane + (r / 8) * 544;
+    uint8_t* codes = blk + (r % 8) * 64;
+    uint8_t* sc = blk + 512 + (r % 8) * 4;
+    for (int j = 0; j < 4; j++) {
+      if (r >= n) { sc[j] = 127; continue; }
+      double amax = 0.0;
+      for (int i = 0; i < 32; i++) {
+        double v = fabs(bf16_val(k[r * D_IDX + 32 * j + i]));
+        if (v > amax) amax = v;
+      }
+      int e = 127;
+      if (amax > 0.0) {
+        e = 0;
+        while (e < 254 && amax > 6.0 * ldexp(1.0, e - 127)) e++;
+      }
+      sc[j] = (uint8_t)e;
+      for (int i = 0; i < 32; i++) {
+        int d = 32 * j + i;
+        uint8_t c = orc_e2m1_code(bf16_val(k[r * D_IDX + d]) / ldexp(1.0, e - 127));
+        codes[d / 2] |= (uint8_t)(c << (4 * (d & 1)));
+      }
+    }
+  }
+}
+
+static double fp4_index_val(const uint8_t* plane, int64_t row, int d) {
+  const uint8_t* blk = plane + (row / 8) * 544;
+  uint8_t c = (blk[(row % 8) * 64 + d / 2] >> (4 * (d & 1))) & 15;
+  int e = blk[512 + (row % 8) * 4 + d / 32];
+  return orc_e2m1_val(c) * ldexp(1.0, e - 127);
+}
+
+/* Index scores on the MXFP4 plane: orc_index_scores with K[c][d] the decoded value of
+ * row row_base[b] + c (row_base a multiple of 8); the query stays bf16. */
+void orc_index_scores_fp4(const uint16_t* iq, const float* w, int Q, int H, const uint8_t* plane,
+                          const int64_t* row_base, const int32_t* q_seq, const int64_t* q_pos,
+                          int m, const int32_t* cand, int ncb, int relu, double* scores,
+                          int64_t* rows, int64_t ld) {
+  double alpha = 1.0 / sqrt((double)D_IDX) / sqrt((double)H);
+  for (int q = 0; q < Q; q++) {
+    int64_t nvis = orc_n_visible(q_pos[q], m);
+    int64_t rb = row_base[q_seq[q]];
+    double qv[64 * D_IDX];
+    for (int i = 0; i < H * D_IDX; i++) qv[i] = bf16_val(iq[(int64_t)q * H * D_IDX + i]);
+    int64_t npos = cand ? (int64_t)ncb * 8 : nvis;
+#pragma omp parallel for schedule(static)
+    for (int64_t pos = 0; pos < ld; pos++) {
+      int64_t row = -1;
+      if (pos < npos) {
+        if (!cand) row = pos;
+        else {
+          int32_t blk = cand[(int64_t)q * ncb + pos / 8];
+          if (blk >= 0 && (int64_t)blk * 8 + pos % 8 < nvis) row = (int64_t)blk * 8 + pos % 8;
+        }
+      }
+      rows[(int64_t)q * ld + pos] = row;
+      if (row < 0) { scores[(int64_t)q * ld + pos] = 0.0; continue; }
+      double kr[D_IDX];
+      for (int d = 0; d < D_IDX; d++) kr[d] = fp4_index_val(plane, rb + row, d);
+      double s = 0.0;
+      for (int h = 0; h < H; h++) {
+        double dot = 0.0;
+        for (int d = 0; d < D_IDX; d++) dot += qv[h * D_IDX + d] * kr[d];
+        if (relu && dot < 0.0) dot = 0.0;
+        s += (double)w[(int64_t)q * H + h] * dot;
+      }
+      scores[(int64_t)q * ld + pos] = alpha * s;
+    }
+  }
+}
+
 /* ---- top-k [A] Fig. 3b ("selected [rows, 512] 升序，-1 填充"), "visible 是每行
  *      自己的前缀长度" (-1 means the history is shorter than 512) ----------------------
  *

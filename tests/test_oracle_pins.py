@@ -535,6 +535,61 @@ def test_attention_on_an_e8m0_window_equals_the_dequantised_bf16_window():
     assert np.array_equal(a, b) and np.array_equal(la, lb)
 
 
+def test_mxfp4_index_plane_layout_scales_and_codes():
+    n = 13  # a partial second block
+    x = RNG.standard_normal((n, 128)) * np.exp2(RNG.integers(-10, 10, (n, 4)).repeat(32, axis=1))
+    x[5, 32:64] = 0.0
+    K = bf16(x)
+    Kd = bf16_np(K)
+    pl = oracle.index_plane_fp4(K)
+    assert pl.size == 2 * oracle.FP4_INDEX_BLOCK_BYTES
+    blocks = pl.reshape(2, 544)
+    for r in range(16):
+        codes_b = blocks[r // 8, (r % 8) * 64:(r % 8) * 64 + 64]
+        sc = blocks[r // 8, 512 + (r % 8) * 4:512 + (r % 8) * 4 + 4]
+        if r >= n:
+            assert np.all(codes_b == 0) and np.all(sc == 127)
+            continue
+        codes = np.empty(128, dtype=np.int64)
+        codes[0::2], codes[1::2] = codes_b & 15, codes_b >> 4
+        for j in range(4):
+            amax = np.abs(Kd[r, 32 * j:32 * j + 32]).max()
+            e = int(sc[j])
+            if amax == 0:
+                assert e == 127 and np.all(codes[32 * j:32 * j + 32] == 0)
+                continue
+            s = 2.0 ** (e - 127)
+            assert amax <= 6 * s and amax > 3 * s  # the smallest power of two that fits
+            for i in range(32):
+                d = 32 * j + i
+                assert codes[d] == _e2m1_nearest_even(Kd[r, d] / s)
+
+
+def test_mxfp4_scores_equal_bf16_scores_when_lossless():
+    # rows whose every group holds E2M1 values times one power of two, with 6 * 2^k in
+    # the group (which fixes the scale), are quantised losslessly: FULL and REINDEX over
+    # two sequences must give the bf16 scorer's scores
+    g = np.random.default_rng(41)
+    mags = np.array(E2M1[1:])
+    v = g.choice(mags, (64, 128)) * g.choice([-1.0, 1.0], (64, 128))
+    v[:, ::32] = 6.0
+    K = bf16(v * np.exp2(g.integers(-6, 6, (64, 4))).repeat(32, axis=1))
+    iq = bf16(g.standard_normal((3, 64, 128)))
+    w = g.standard_normal((3, 64)).astype(np.float32)
+    rb = np.array([0, 32], dtype=np.int64)
+    plane = oracle.index_plane_fp4(K)
+    pos, seqs = [60, 31, 17], [0, 1, 1]
+    a, ra = oracle.index_scores(iq, w, K, rb, seqs, pos, 1)
+    b, rb4 = oracle.index_scores_fp4(iq, w, plane, rb, seqs, pos, 1)
+    assert np.array_equal(ra, rb4)
+    np.testing.assert_allclose(b, a, rtol=1e-12, atol=1e-12)
+    cand = np.array([[0, 3, 7, -1], [1, 2, -1, -1], [0, 2, 3, 1]], dtype=np.int32)
+    a, ra = oracle.index_scores(iq, w, K, rb, seqs, pos, 1, cand=cand)
+    b, rb4 = oracle.index_scores_fp4(iq, w, plane, rb, seqs, pos, 1, cand=cand)
+    assert np.array_equal(ra, rb4)
+    np.testing.assert_allclose(b, a, rtol=1e-12, atol=1e-12)
+
+
 # ---- FP8 index plane (NEXT-3) --------------------------------------------------------
 
 def _e4m3_values():
