@@ -559,6 +559,16 @@ def run_stages(args):
     res["index_topk_fp8"] = timed(lambda: csa2.csa2_index_topk_fp8(
         t["iq"], t["w"], plane8, rows8, rb8, t["q_seq"], t["q_pos"], spec.ratio, spec.k,
         spec.max_scored, sel8, ws8, cand=cand))
+    # the MXFP4 index plane (NEXT-3): the same re-laying, quantised once
+    from csa2_compressed_sparse_gb300.step import block_index_plane
+    plane4i, rb4, rows4 = block_index_plane(t["index_k"], wl.row_base, wl.n_rows, "fp4")
+    ws4 = torch.empty(csa2.csa2_index_topk_fp4_workspace_size(wl.Q, spec.H, spec.max_scored,
+                                                               spec.k),
+                      dtype=torch.uint8, device="cuda")
+    sel4 = torch.empty_like(buf.sel)
+    res["index_topk_fp4"] = timed(lambda: csa2.csa2_index_topk_fp4(
+        t["iq"], t["w"], plane4i, rows4, rb4, t["q_seq"], t["q_pos"], spec.ratio, spec.k,
+        spec.max_scored, sel4, ws4, cand=cand))
     res["sparse_attn"] = timed(lambda: csa2.csa2_sparse_attn(
         t["q"][0], t["q_seq"], t["q_pos"], swa0, t["plane"], t["row_base"], buf.sel, t["sink"],
         buf.out[0], scale=spec.scale, ws=buf.attn_ws))

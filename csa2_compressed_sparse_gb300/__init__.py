@@ -21,7 +21,8 @@ __all__ = [
     "csa2_index_topk_workspace_size", "csa2_index_topk", "csa2_index_topk_noalloc",
     "csa2_index_topk_pool_workspace_size", "csa2_index_topk_pool", "csa2_topk_workspace_size",
     "csa2_index_plane_fp8_bytes", "csa2_index_plane_fp8", "csa2_index_topk_fp8_workspace_size",
-    "csa2_index_topk_fp8",
+    "csa2_index_topk_fp8", "csa2_index_plane_fp4_bytes", "csa2_index_plane_fp4",
+    "csa2_index_topk_fp4_workspace_size", "csa2_index_topk_fp4",
     "csa2_topk_scores", "csa2_attn_workspace_size", "csa2_sparse_attn", "csa2_reuse_attn",
     "csa2_sparse_attn_rope", "csa2_reuse_attn_rope", "csa2_plane_fp4_bytes", "csa2_plane_fp4",
     "csa2_sparse_attn_fp4",
@@ -67,6 +68,11 @@ _SIGS = {
     "csa2_index_plane_fp8": ([_vp, _i64, _vp, _vp], _i32),
     "csa2_index_topk_fp8_workspace_size": ([_i32, _i32, _i64, _i32], _sz),
     "csa2_index_topk_fp8": ([_vp, _vp, _i32, _i32, _vp, _i64, _vp, _vp, _vp, _i32, _vp, _i32,
+                             _i32, _i32, _i64, _vp, _vp, _vp, _vp, _sz, _vp], _i32),
+    "csa2_index_plane_fp4_bytes": ([_i64], _sz),
+    "csa2_index_plane_fp4": ([_vp, _i64, _vp, _vp], _i32),
+    "csa2_index_topk_fp4_workspace_size": ([_i32, _i32, _i64, _i32], _sz),
+    "csa2_index_topk_fp4": ([_vp, _vp, _i32, _i32, _vp, _i64, _vp, _vp, _vp, _i32, _vp, _i32,
                              _i32, _i32, _i64, _vp, _vp, _vp, _vp, _sz, _vp], _i32),
     "csa2_topk_workspace_size": ([_i32, _i64, _i32], _sz),
     "csa2_topk_scores": ([_vp, _vp, _i32, _i64, _i32, _vp, _vp, _vp, _sz, _vp], _i32),
@@ -232,6 +238,32 @@ def csa2_index_topk_fp8(iq, w, plane, index_rows, row_base, q_seq, q_pos, ratio,
     Q, H = iq.shape[0], iq.shape[1]
     ncb = 0 if cand is None else cand.shape[1]
     _check(lib().csa2_index_topk_fp8(_p(iq), _p(w), Q, H, _p(plane), index_rows, _p(row_base),
+                                     _p(q_seq), _p(q_pos), ratio, _p(cand), ncb, k,
+                                     1 if relu else 0, max_scored, _p(sel), _p(sel_scores),
+                                     _p(scores_out), _p(ws), ws.numel() * ws.element_size(),
+                                     _stream(stream)))
+
+
+def csa2_index_plane_fp4_bytes(rows):
+    return int(lib().csa2_index_plane_fp4_bytes(rows))
+
+
+def csa2_index_plane_fp4(index_k, plane, stream=None):
+    """bf16 index rows [rows, 128] -> MXFP4 plane bytes (blocks of 8 rows, 544 B each)."""
+    _check(lib().csa2_index_plane_fp4(_p(index_k), index_k.shape[0], _p(plane), _stream(stream)))
+
+
+def csa2_index_topk_fp4_workspace_size(Q, H, max_scored, k):
+    return int(lib().csa2_index_topk_fp4_workspace_size(Q, H, max_scored, k))
+
+
+def csa2_index_topk_fp4(iq, w, plane, index_rows, row_base, q_seq, q_pos, ratio, k, max_scored,
+                        sel, ws, sel_scores=None, cand=None, relu=True, scores_out=None,
+                        stream=None):
+    """csa2_index_topk on an MXFP4 index plane of index_rows rows."""
+    Q, H = iq.shape[0], iq.shape[1]
+    ncb = 0 if cand is None else cand.shape[1]
+    _check(lib().csa2_index_topk_fp4(_p(iq), _p(w), Q, H, _p(plane), index_rows, _p(row_base),
                                      _p(q_seq), _p(q_pos), ratio, _p(cand), ncb, k,
                                      1 if relu else 0, max_scored, _p(sel), _p(sel_scores),
                                      _p(scores_out), _p(ws), ws.numel() * ws.element_size(),

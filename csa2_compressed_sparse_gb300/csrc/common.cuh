@@ -84,6 +84,7 @@ struct IndexArgs {
   // FP8 index plane (null: index_k is bf16): blocks of 8 rows, 8 x 128 E4M3 codes then
   // 8 fp32 scales (1056 bytes); row_base values are multiples of 8
   const uint8_t* plane8;
+  const uint8_t* plane4;  // MXFP4 index plane (blocks of 8 rows, 544 bytes), or null
   uint8_t* q8;          // [Q*H][128] E4M3 codes of the quantised queries (workspace)
   float* qscale;        // [Q*H] their power-of-two scales (workspace)
 };
@@ -138,6 +139,7 @@ struct AttnArgs {
 
 cudaError_t launch_compress(const CompressArgs& a, cudaStream_t s);
 cudaError_t launch_index(const IndexArgs& a, int num_sms, cudaStream_t s);
+cudaError_t launch_plane_fp4_index(const uint16_t* k, int64_t n, uint8_t* plane, cudaStream_t s);
 // bf16 plane rows [n][512] -> FP4 rows [n][288].
 cudaError_t launch_plane_fp4(const uint16_t* rows, int64_t n, uint8_t* out, cudaStream_t s);
 // bf16 index rows [n][128] -> FP8 plane (ceil(n / 8) blocks of 1056 bytes).

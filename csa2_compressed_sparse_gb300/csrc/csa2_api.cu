@@ -256,8 +256,10 @@ size_t csa2_index_topk_workspace_size(int Q, int H, int64_t max_scored, int k) {
 
 namespace {
 
+// plane_fmt: 1 = FP8 blocks (plane), 2 = MXFP4 blocks (plane); 0 = bf16 rows (index_k)
 csa2_status index_topk_impl(const csa2_bf16* iq, const float* w, int Q, int H,
-                            const csa2_bf16* index_k, const uint8_t* plane8, int64_t index_rows,
+                            const csa2_bf16* index_k, const uint8_t* plane, int plane_fmt,
+                            int64_t index_rows,
                             const int64_t* row_base, const int32_t* q_seq, const int64_t* q_pos,
                             int ratio, const int32_t* cand, int ncb, int k, int relu,
                             int64_t max_scored, int32_t* sel, float* sel_scores,
@@ -278,14 +280,15 @@ csa2_status index_topk_impl(const csa2_bf16* iq, const float* w, int Q, int H,
           "csa2_index_topk: max_scored %lld exceeds the supported %lld positions",
           (long long)max_scored, (long long)csa2::topk_max_len());
   if (Q == 0) return CSA2_OK;
-  REQUIRE(iq && w && (index_k || plane8) && row_base && q_seq && q_pos && sel && ws,
+  REQUIRE(iq && w && (plane_fmt ? plane != nullptr : index_k != nullptr) && row_base && q_seq &&
+              q_pos && sel && ws,
           "csa2_index_topk: iq, w, the index plane, row_base, q_seq, q_pos, sel and ws are required");
-  REQUIRE(aligned16(iq) && aligned16(index_k ? (const void*)index_k : (const void*)plane8),
+  REQUIRE(aligned16(iq) && aligned16(plane_fmt ? (const void*)plane : (const void*)index_k),
           "csa2_index_topk: iq and the index plane must be 16-byte aligned");
   REQUIRE(index_rows >= 1 && index_rows < (int64_t)1 << 31, "csa2_index_topk: index_rows out of range");
   REQUIRE((int64_t)Q * H < (int64_t)1 << 31, "csa2_index_topk: Q * H out of range");
   REQUIRE((reinterpret_cast<uintptr_t>(ws) & 255u) == 0, "csa2_index_topk: ws must be 256-byte aligned");
-  const IndexWs L = index_ws_layout(Q, max_scored, k, nbk, plane8 ? (int64_t)Q * H : 0);
+  const IndexWs L = index_ws_layout(Q, max_scored, k, nbk, plane_fmt == 1 ? (int64_t)Q * H : 0);
   if (ws_bytes < L.total)
     return fail(CSA2_ENOSPACE, "csa2_index_topk: workspace %zu bytes < required %zu", ws_bytes, L.total);
   uint8_t* base = static_cast<uint8_t*>(ws);
@@ -302,11 +305,14 @@ csa2_status index_topk_impl(const csa2_bf16* iq, const float* w, int Q, int H,
   a.topk_count = reinterpret_cast<int32_t*>(base + L.count);
   a.group_max = cand ? 1 : 256 / H;
   if (nbk > 0) a.pool_count = reinterpret_cast<int32_t*>(base + L.pcount);
-  if (plane8) {
+  if (plane_fmt == 1) {
     a.index_k = nullptr;
-    a.plane8 = plane8;
+    a.plane8 = plane;
     a.q8 = base + L.q8;
     a.qscale = reinterpret_cast<float*>(base + L.qscale);
+  } else if (plane_fmt == 2) {
+    a.index_k = nullptr;
+    a.plane4 = plane;
   }
   const int sms = num_sms();
   if (sms <= 0) return fail(CSA2_ECUDA, "csa2_index_topk: no CUDA device");
@@ -343,7 +349,7 @@ csa2_status csa2_index_topk(const csa2_bf16* iq, const float* w, int Q, int H,
                             int ratio, const int32_t* cand, int ncb, int k, int relu,
                             int64_t max_scored, int32_t* sel, float* sel_scores,
                             float* scores_out, void* ws, size_t ws_bytes, csa2_stream stream) {
-  return index_topk_impl(iq, w, Q, H, index_k, nullptr, index_rows, row_base, q_seq, q_pos,
+  return index_topk_impl(iq, w, Q, H, index_k, nullptr, 0, index_rows, row_base, q_seq, q_pos,
                          ratio, cand, ncb, k, relu, max_scored, sel, sel_scores, scores_out, 0,
                          nullptr, ws, ws_bytes, stream);
 }
@@ -366,7 +372,7 @@ csa2_status csa2_index_topk_pool(const csa2_bf16* iq, const float* w, int Q, int
           "csa2_index_topk_pool: %lld blocks per row with nbk = %d exceed the block selection",
           (long long)pool_blocks(max_scored), nbk);
   REQUIRE(Q == 0 || pool, "csa2_index_topk_pool: pool is required");
-  return index_topk_impl(iq, w, Q, H, index_k, nullptr, index_rows, row_base, q_seq, q_pos,
+  return index_topk_impl(iq, w, Q, H, index_k, nullptr, 0, index_rows, row_base, q_seq, q_pos,
                          ratio, nullptr, 0, k, relu, max_scored, sel, sel_scores, scores_out,
                          nbk, pool, ws, ws_bytes, stream);
 }
@@ -384,9 +390,44 @@ csa2_status csa2_index_topk_fp8(const csa2_bf16* iq, const float* w, int Q, int 
                                 float* sel_scores, float* scores_out, void* ws, size_t ws_bytes,
                                 csa2_stream stream) {
   REQUIRE(Q == 0 || plane, "csa2_index_topk_fp8: plane is required");
-  return index_topk_impl(iq, w, Q, H, nullptr, plane, index_rows, row_base, q_seq, q_pos, ratio,
-                         cand, ncb, k, relu, max_scored, sel, sel_scores, scores_out, 0, nullptr,
-                         ws, ws_bytes, stream);
+  return index_topk_impl(iq, w, Q, H, nullptr, plane, 1, index_rows, row_base, q_seq, q_pos,
+                         ratio, cand, ncb, k, relu, max_scored, sel, sel_scores, scores_out, 0,
+                         nullptr, ws, ws_bytes, stream);
+}
+
+size_t csa2_index_topk_fp4_workspace_size(int Q, int H, int64_t max_scored, int k) {
+  if (Q < 0 || (H != 32 && H != 64) || max_scored < 1 || k < 1 || k > 512) return 0;
+  return index_ws_layout(Q, max_scored, k).total;
+}
+
+csa2_status csa2_index_topk_fp4(const csa2_bf16* iq, const float* w, int Q, int H,
+                                const uint8_t* plane, int64_t index_rows,
+                                const int64_t* row_base, const int32_t* q_seq,
+                                const int64_t* q_pos, int ratio, const int32_t* cand, int ncb,
+                                int k, int relu, int64_t max_scored, int32_t* sel,
+                                float* sel_scores, float* scores_out, void* ws, size_t ws_bytes,
+                                csa2_stream stream) {
+  REQUIRE(Q == 0 || plane, "csa2_index_topk_fp4: plane is required");
+  return index_topk_impl(iq, w, Q, H, nullptr, plane, 2, index_rows, row_base, q_seq, q_pos,
+                         ratio, cand, ncb, k, relu, max_scored, sel, sel_scores, scores_out, 0,
+                         nullptr, ws, ws_bytes, stream);
+}
+
+size_t csa2_index_plane_fp4_bytes(int64_t rows) {
+  return rows <= 0 ? 0 : (size_t)((rows + 7) / 8) * 544;
+}
+
+csa2_status csa2_index_plane_fp4(const csa2_bf16* index_k, int64_t rows, uint8_t* plane,
+                                 csa2_stream stream) {
+  REQUIRE(rows >= 0 && rows < (int64_t)1 << 34, "csa2_index_plane_fp4: rows out of range");
+  if (rows == 0) return CSA2_OK;
+  REQUIRE(index_k && plane, "csa2_index_plane_fp4: index_k and plane are required");
+  REQUIRE(aligned16(index_k) && aligned16(plane),
+          "csa2_index_plane_fp4: index_k and plane must be 16-byte aligned");
+  cudaError_t e = csa2::launch_plane_fp4_index(reinterpret_cast<const uint16_t*>(index_k), rows,
+                                               plane, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "csa2_index_plane_fp4");
+  return CSA2_OK;
 }
 
 size_t csa2_index_plane_fp8_bytes(int64_t rows) {

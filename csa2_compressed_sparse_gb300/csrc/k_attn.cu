@@ -100,12 +100,6 @@ __device__ __forceinline__ void st_shared_zero16(uint32_t addr) {
   asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(addr), "r"(0) : "memory");
 }
 
-__device__ __forceinline__ void st_shared16(uint32_t addr, uint4 v) {
-  asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y),
-               "r"(v.z), "r"(v.w)
-               : "memory");
-}
-
 // OR of `pred` over warps 0..3 (a barrier of the group with a reduction)
 __device__ __forceinline__ bool group_any(bool pred) {
   uint32_t r;
@@ -362,8 +356,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     sparse_attn_kernel(AttnArgs a, const __grid_constant__ CUtensorMap qmap,
                        const __grid_constant__ CUtensorMap wmap) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                             ~uintptr_t(1023));
+  // rounded up to 1024 bytes by pointer arithmetic, so that accesses stay shared-space
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint8_t* q_s = smem;
   uint8_t* kv_s = smem + kQBytes;            // two buffers
   uint8_t* p_s = kv_s + 2 * kBufBytes;       // two buffers

@@ -16,8 +16,11 @@
 //   warp 1      TMEM allocation; lane 0 issues the MMAs (8 x K=16 per tile)
 //   warps 2..9  epilogue in two groups of four warps: group e reads TMEM accumulator e
 //               (tiles of parity e) -> relu * w -> sum -> order-preserving key
+//   warps 10..17 (MXFP4 planes only) convert packed E2M1 blocks to bf16 tiles
 // TMEM holds two 256-column fp32 accumulators, so two tiles are in the epilogue while
 // the MMAs of the next one run.  The scores are written as uint32 keys for the top-k.
+#include <cuda_fp4.h>
+
 #include "common.cuh"
 
 CSA2_DEFINE_FAULT_FLAG(index)
@@ -26,20 +29,45 @@ namespace csa2 {
 namespace {
 
 constexpr int kTileRows = 128;
-constexpr int kThreads = 320;
-// K-tile ring: bf16 tiles are 32 KiB (two 64-dim blocks of 128-byte rows), FP8 tiles
-// 16 KiB (one block); both rings hold 128 KiB.
-constexpr int kRingBytes = 4 * kTileRows * kDIdx * 2;
-__host__ __device__ constexpr int stage_bytes(bool fp8) { return fp8 ? kTileRows * kDIdx : kTileRows * kDIdx * 2; }
-__host__ __device__ constexpr int num_stages(bool fp8) { return kRingBytes / stage_bytes(fp8); }
-constexpr int kMaxStages = num_stages(true);
+// Operand formats of the index plane.
+constexpr int kModeBf16 = 0;  // bf16 rows
+constexpr int kModeFp8 = 1;   // blocks of 8 E4M3 rows with fp32 row scales
+constexpr int kModeFp4 = 2;   // blocks of 8 E2M1 rows with E8M0 scales per 32 dims
+constexpr int kFp4ConvWarps = 8;  // FP4: warps 10 .. 17 convert packed blocks to bf16
+__host__ __device__ constexpr int num_threads(int mode) {
+  return mode == kModeFp4 ? 320 + 32 * kFp4ConvWarps : 320;
+}
+// MMA operand ring: bf16 tiles are 32 KiB (two 64-dim blocks of 128-byte rows), FP8 tiles
+// 16 KiB (one block).  bf16 and FP8 rings hold 128 KiB, filled by TMA.  FP4 tiles are
+// converted to bf16 in shared memory: an 8-stage ring of packed blocks (filled by bulk
+// copies) feeds a 2-stage ring of bf16 tiles.
+constexpr int kBf16Tile = kTileRows * kDIdx * 2;
+constexpr int kFp4BlockBytes = 8 * 64 + 8 * 4;      // 544: 8 rows of codes, 8 x 4 scales
+constexpr int kFp4StgBytes = 16 * kFp4BlockBytes;    // 8704: the 16 blocks of a tile
+constexpr int kFp4StgStages = 8;
+constexpr int kFp4CvStages = 2;
+__host__ __device__ constexpr int stage_bytes(int mode) {
+  return mode == kModeFp8 ? kTileRows * kDIdx : kBf16Tile;
+}
+__host__ __device__ constexpr int num_stages(int mode) {
+  return mode == kModeFp4 ? kFp4CvStages : 4 * kBf16Tile / stage_bytes(mode);
+}
+__host__ __device__ constexpr int ring_bytes(int mode) {
+  return mode == kModeFp4 ? kFp4CvStages * kBf16Tile + kFp4StgStages * kFp4StgBytes
+                          : 4 * kBf16Tile;
+}
+constexpr int kMaxStages = 8;
+static_assert(num_stages(kModeFp8) <= kMaxStages && kFp4StgStages <= kMaxStages, "ring");
+static_assert(ring_bytes(kModeFp4) % 1024 == 0, "the Q block must stay 1024-byte aligned");
 constexpr int kBBytes = 2 * 256 * 128;              // 64 KiB: two 64-dim blocks x 256 rows
 constexpr int kMaxGroup = 8;
 constexpr int kFp8BlockBytes = 8 * kDIdx + 8 * 4;   // 1056: 8 rows of codes, 8 scales
 
 struct __align__(8) Bars {
-  uint64_t full[kMaxStages];
+  uint64_t full[kMaxStages];   // the ring the producer fills
   uint64_t empty[kMaxStages];
+  uint64_t cv_full[kFp4CvStages];   // FP4: converted bf16 tiles
+  uint64_t cv_empty[kFp4CvStages];
   uint64_t acc_full[2];
   uint64_t acc_empty[2];
   uint64_t b_full;
@@ -119,8 +147,8 @@ __global__ void __launch_bounds__(kPrepThreads) index_prep_kernel(IndexArgs a) {
         }
         s_seq[i] = a.q_seq[q];
         s_ns[i] = (int)ns;
-        if (a.plane8 && i < kPrepThreads && (a.row_base[s_seq[i]] & 7) != 0)
-          raise_fault(kFaultBounds);  // FP8 planes start every sequence on a block
+        if ((a.plane8 || a.plane4) && i < kPrepThreads && (a.row_base[s_seq[i]] & 7) != 0)
+          raise_fault(kFaultBounds);  // block planes start every sequence on a block
         if (i < kPrepThreads) {
           a.n_scored[q] = (int32_t)ns;
           a.topk_count[q] = 0;
@@ -303,20 +331,135 @@ __global__ void __launch_bounds__(256) quant_q_kernel(IndexArgs a) {
   if (lane == 0) a.qscale[r] = sc;
 }
 
-// kFp8: K tiles and queries are E4M3 codes (tcgen05 kind::f8f6f4, K = 32 per MMA); the
+// ---- MXFP4 quantisation: [A] indexer figure (FP4 index rows of 64 code bytes and 4 scale
+//      bytes, paged in blocks of 8 rows); [A] indexer K (E2M1 values, one E8M0 scale per
+//      32 dims) ----------------------------------------------------------------------------
+
+// E8M0 code of a group whose largest magnitude is amax: the smallest e in [0, 254] with
+// amax <= 6 * 2^(e - 127), and 127 for amax == 0.  With amax = M * 2^E (1 <= M < 2),
+// 6 * 2^(E - 2) = 1.5 * 2^E covers M <= 1.5 and 3 * 2^E covers the rest.
+__device__ __forceinline__ int e8m0_fp4(float amax) {
+  const uint32_t u = __float_as_uint(amax);
+  if (u == 0u) return 127;
+  int E;
+  uint32_t m;
+  if ((u >> 23) != 0u) {
+    E = (int)(u >> 23) - 127;
+    m = u & 0x7FFFFFu;
+  } else {
+    const int p = 31 - __clz((int)u);
+    E = p - 149;
+    m = (u << (23 - p)) & 0x7FFFFFu;
+  }
+  const int e = 127 + E - 2 + (m > 0x400000u ? 1 : 0);
+  return e < 0 ? 0 : (e > 254 ? 254 : e);
+}
+
+// One CTA per block of the plane: warp w quantises row 8 * blockIdx.x + w; lane l holds
+// dims 4l .. 4l+3 of group l / 8.  Rows past n get zero codes and scale code 127.
+__global__ void __launch_bounds__(256) plane_fp4_index_kernel(const uint16_t* k, int64_t n,
+                                                              uint8_t* plane) {
+  griddep_launch_dependents();
+  griddep_wait();
+  const int lane = threadIdx.x & 31, slot = threadIdx.x >> 5;
+  const int64_t r = (int64_t)blockIdx.x * 8 + slot;
+  float v[4] = {0.f, 0.f, 0.f, 0.f};
+  if (r < n) {
+    const uint2 w = __ldg(reinterpret_cast<const uint2*>(k + r * kDIdx) + lane);
+    v[0] = __uint_as_float(w.x << 16); v[1] = __uint_as_float(w.x & 0xFFFF0000u);
+    v[2] = __uint_as_float(w.y << 16); v[3] = __uint_as_float(w.y & 0xFFFF0000u);
+  }
+  float amax = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
+#pragma unroll
+  for (int o = 1; o < 8; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
+  const int e = e8m0_fp4(amax);
+  // x / 2^(e - 127) as two exact power-of-two factors, each a normal float
+  const int ne = 127 - e;  // in [-127, 127]
+  const float f1 = __uint_as_float((uint32_t)((ne >> 1) + 127) << 23);
+  const float f2 = __uint_as_float((uint32_t)((ne - (ne >> 1)) + 127) << 23);
+  const __nv_fp4x2_storage_t c01 =
+      __nv_cvt_float2_to_fp4x2(make_float2(v[0] * f1 * f2, v[1] * f1 * f2), __NV_E2M1,
+                               cudaRoundNearest);
+  const __nv_fp4x2_storage_t c23 =
+      __nv_cvt_float2_to_fp4x2(make_float2(v[2] * f1 * f2, v[3] * f1 * f2), __NV_E2M1,
+                               cudaRoundNearest);
+  uint8_t* blk = plane + (int64_t)blockIdx.x * kFp4BlockBytes;
+  reinterpret_cast<uint16_t*>(blk + slot * 64)[lane] =
+      (uint16_t)((uint32_t)c01 | ((uint32_t)c23 << 8));
+  if ((lane & 7) == 0) blk[512 + slot * 4 + (lane >> 3)] = (uint8_t)e;
+}
+
+// ---- FP4 tile conversion ------------------------------------------------------------------
+// A code byte holds dims 2i (low nibble) and 2i+1.  The hardware conversion gives the
+// E2M1 values as f16 (exact); shifting each f16 magnitude right by 3 gives the bf16 bits
+// of the same value times 2^-112 (bias 15 against 127, 10 mantissa bits against 7, and an
+// E2M1 value uses only the top mantissa bit), and a bf16 multiply by 2^(e - 15) then gives
+// value * 2^(e - 127) exactly while the result is normal (2 <= e <= 142).  Groups with
+// other scale codes take the float path.
+
+// The eight E2M1 codes of a word as four f16 pairs.
+__device__ __forceinline__ void e2m1x8_to_f16x2(uint32_t w, uint32_t (&h)[4]) {
+  asm("{\n\t.reg .b8 c0, c1, c2, c3;\n\t"
+      "mov.b32 {c0, c1, c2, c3}, %4;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %0, c0;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %1, c1;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %2, c2;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %3, c3;\n\t}"
+      : "=r"(h[0]), "=r"(h[1]), "=r"(h[2]), "=r"(h[3])
+      : "r"(w));
+}
+
+__device__ __forceinline__ uint32_t mul_bf16x2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
+// Eight values of a group with scale code e in [2, 142], as one 16-byte bf16 chunk.
+__device__ __forceinline__ uint4 fp4_word_fast(uint32_t w, uint32_t s2) {
+  uint32_t h[4], o[4];
+  e2m1x8_to_f16x2(w, h);
+#pragma unroll
+  for (int b = 0; b < 4; ++b)
+    o[b] = mul_bf16x2(((h[b] & 0x7FFF7FFFu) >> 3) | (h[b] & 0x80008000u), s2);
+  return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+// The float path for any scale code (2^(e - 127), subnormal below -126), one chunk.
+__device__ __noinline__ uint4 fp4_word_slow(uint32_t w, int e) {
+  const int ex = e - 127;
+  const float sf = ex >= -126 ? __uint_as_float((uint32_t)(ex + 127) << 23)
+                              : __uint_as_float(1u << (ex + 149));
+  uint32_t h[4], o[4];
+  e2m1x8_to_f16x2(w, h);
+#pragma unroll
+  for (int b = 0; b < 4; ++b) {
+    const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h[b]));
+    o[b] = pack_bf16x2(f.x * sf, f.y * sf);
+  }
+  return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+// kModeFp8: K tiles and queries are E4M3 codes (tcgen05 kind::f8f6f4, K = 32 per MMA); the
 // row scale of K and the query scales multiply the head sum in the epilogue.
-template <bool kFp8>
-__global__ void __launch_bounds__(kThreads, 1)
+// kModeFp4: the producer bulk-copies the tile's 16 packed blocks, warps 10..17 convert
+// them to a bf16 tile (exact) and the MMAs and epilogue are those of the bf16 mode.
+template <int kMode>
+__global__ void __launch_bounds__(num_threads(kMode), 1)
     index_score_kernel(IndexArgs a, const __grid_constant__ CUtensorMap kmap_tile,
                        const __grid_constant__ CUtensorMap kmap_blk,
                        const __grid_constant__ CUtensorMap qmap) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                             ~uintptr_t(1023));
-  constexpr int kStages = num_stages(kFp8);
-  constexpr int kStageBytes = stage_bytes(kFp8);
-  uint8_t* a_smem = smem;                              // the K-tile ring, 128 KiB
-  uint8_t* b_smem = smem + kRingBytes;                 // 64 KiB
+  // rounded up to 1024 bytes by pointer arithmetic, so that accesses stay shared-space
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  constexpr bool kFp8 = kMode == kModeFp8;
+  constexpr bool kFp4 = kMode == kModeFp4;
+  // the ring the producer fills: operand tiles, or the FP4 mode's packed blocks
+  constexpr int kStages = kFp4 ? kFp4StgStages : num_stages(kMode);
+  constexpr int kStageBytes = kFp4 ? kFp4StgBytes : stage_bytes(kMode);
+  uint8_t* a_smem = smem;                              // MMA operand tiles
+  uint8_t* fill_smem = kFp4 ? smem + kFp4CvStages * kBf16Tile : smem;
+  uint8_t* b_smem = smem + ring_bytes(kMode);          // 64 KiB
   float* w_all = reinterpret_cast<float*>(b_smem + kBBytes);  // [8][256], per epilogue warp
   Bars* bars = reinterpret_cast<Bars*>(w_all + 8 * 256);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 1);
@@ -326,8 +469,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   griddep_launch_dependents();
   if (threadIdx.x == 0) {
-    prefetch_tensormap(&kmap_tile);
-    prefetch_tensormap(&kmap_blk);
+    if (!kFp4) {
+      prefetch_tensormap(&kmap_tile);
+      prefetch_tensormap(&kmap_blk);
+    }
     prefetch_tensormap(&qmap);
   }
   griddep_wait();
@@ -340,7 +485,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(smem_u32(&bars->full[s]), 1);
-      mbar_init(smem_u32(&bars->empty[s]), 1);
+      mbar_init(smem_u32(&bars->empty[s]), kFp4 ? kFp4ConvWarps : 1);  // FP4: the converters
+    }
+    for (int s = 0; s < kFp4CvStages; ++s) {
+      mbar_init(smem_u32(&bars->cv_full[s]), kFp4ConvWarps);
+      mbar_init(smem_u32(&bars->cv_empty[s]), 1);
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(smem_u32(&bars->acc_full[s]), 1);
@@ -365,9 +514,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) {
     // ===================== TMA producer =====================
     if (lane == 0) {
-      prefetch_tensormap(&kmap_tile);
-      prefetch_tensormap(&kmap_blk);
-      prefetch_tensormap(&qmap);
       const uint64_t pol_k = policy_evict_first();
       const uint64_t pol_q = policy_evict_last();
       GroupInfo gi;
@@ -403,11 +549,40 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t round = (uint32_t)(k / kStages);
         if (!mbar_wait(smem_u32(&bars->empty[s]), (round & 1) ^ 1)) { *abort_flag = 1; break; }
         const uint32_t fb = smem_u32(&bars->full[s]);
-        mbar_arrive_expect_tx(fb, kStageBytes);
+        if (!kFp4) mbar_arrive_expect_tx(fb, kStageBytes);  // FP4: per copy below
         issued[s] = round;
         const int64_t tile = it - gi.tile0;
-        uint8_t* dst = a_smem + s * kStageBytes;
-        if (kFp8) {
+        uint8_t* dst = fill_smem + s * kStageBytes;
+        if (kFp4) {
+          // the tile's 16 packed blocks; copies never leave the plane (a block id outside
+          // it is a caller error: flagged, and block 0 is read instead)
+          const int64_t nbt = (a.index_rows + 7) >> 3;
+          const int64_t b0 = gi.rb >> 3;
+          if (!a.cand) {
+            const int64_t first = b0 + tile * 16;
+            const int64_t nblk = first < 0 ? 0 : (nbt - first < 16 ? nbt - first : 16);
+            if (nblk > 0) {
+              mbar_arrive_expect_tx(fb, (uint32_t)(nblk * kFp4BlockBytes));
+              bulk_copy_g2s(smem_u32(dst), a.plane4 + first * kFp4BlockBytes,
+                            (uint32_t)(nblk * kFp4BlockBytes), fb);
+            } else {
+              mbar_arrive(fb);
+            }
+          } else {
+            const int32_t* cb = a.cand + (int64_t)gi.q0 * a.ncb + tile * 16;
+            int32_t blk[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) blk[i] = tile * 16 + i < a.ncb ? __ldg(cb + i) : -1;
+            mbar_arrive_expect_tx(fb, (uint32_t)kFp4StgBytes);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              int64_t src = blk[i] >= 0 ? b0 + blk[i] : 0;
+              if (src >= nbt) { raise_fault(kFaultBounds); src = 0; }
+              bulk_copy_g2s(smem_u32(dst + i * kFp4BlockBytes), a.plane4 + src * kFp4BlockBytes,
+                            (uint32_t)kFp4BlockBytes, fb);
+            }
+          }
+        } else if (kFp8) {
           // block (row_base + 128 * tile) / 8 .. + 15, as [16][8 rows][128 B]; REINDEX:
           // one box per candidate block
           const int64_t b0 = gi.rb >> 3;
@@ -471,10 +646,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t round = (uint32_t)(k / kStages);
         const int ab = (int)(k & 1);
         const uint32_t use = (uint32_t)(k >> 1);
-        if (!mbar_wait(smem_u32(&bars->full[s]), round & 1)) { *abort_flag = 1; break; }
+        // FP4: the converted tile k & 1 (its use k >> 1, the accumulator's)
+        const uint32_t in_bar = kFp4 ? smem_u32(&bars->cv_full[ab]) : smem_u32(&bars->full[s]);
+        if (!mbar_wait(in_bar, kFp4 ? (use & 1) : (round & 1))) { *abort_flag = 1; break; }
         if (!mbar_wait(smem_u32(&bars->acc_empty[ab]), (use & 1) ^ 1)) { *abort_flag = 1; break; }
         tc_fence_after();
-        const uint32_t a_base = smem_u32(a_smem + s * kStageBytes);
+        const uint32_t a_base = kFp4 ? smem_u32(a_smem + ab * kBf16Tile)
+                                     : smem_u32(a_smem + s * kStageBytes);
         const uint32_t b_base = smem_u32(b_smem);
         const uint32_t d = tmem + (uint32_t)(ab * 256);
         if (kFp8) {
@@ -494,12 +672,59 @@ __global__ void __launch_bounds__(kThreads, 1)
               umma_bf16(d, ad, bd, idesc, (db | kk) != 0);
             }
         }
-        umma_commit(smem_u32(&bars->empty[s]));
+        umma_commit(kFp4 ? smem_u32(&bars->cv_empty[ab]) : smem_u32(&bars->empty[s]));
         umma_commit(smem_u32(&bars->acc_full[ab]));
         if (it + 1 == it_hi || it + 1 == gi.tile1) umma_commit(smem_u32(&bars->b_empty));
       }
     }
-  } else {
+  } else if (kFp4 && warp >= 10) {
+    // ============ FP4 converters: warps 10..17 ============
+    // Warp c converts blocks c and c+8 of a tile; lane l takes row l / 4 of the
+    // block and its dims 32 j .. 32 j + 31 (j = l % 4, one scale).  Each quarter-warp
+    // reads 128 contiguous bytes; lanes with j >= 2 write their four 16-byte chunks in the
+    // order 2, 3, 0, 1, so that each quarter-warp's stores fall in eight distinct chunk
+    // positions of the swizzled rows (no bank conflicts).
+    const int cw = warp - 10, j = lane & 3;
+    for (int64_t it = it_lo; it < it_hi; ++it) {
+      if (__any_sync(0xFFFFFFFFu, *abort_flag != 0)) break;
+      const int64_t k = it - it_lo;
+      const int s = (int)(k % kStages);
+      const uint32_t round = (uint32_t)(k / kStages);
+      const int c = (int)(k & 1);
+      const uint32_t use = (uint32_t)(k >> 1);
+      if (!__all_sync(0xFFFFFFFFu, mbar_wait(smem_u32(&bars->full[s]), round & 1)) ||
+          !__all_sync(0xFFFFFFFFu, mbar_wait(smem_u32(&bars->cv_empty[c]), (use & 1) ^ 1))) {
+        *abort_flag = 1;
+        break;
+      }
+      const uint8_t* src = fill_smem + s * kStageBytes;
+      const uint32_t dst = smem_u32(a_smem + c * kBf16Tile) + (uint32_t)(j >> 1) * (kBf16Tile / 2);
+#pragma unroll
+      for (int i = 0; i < 16 / kFp4ConvWarps; ++i) {
+        const int blk = cw + kFp4ConvWarps * i;
+        uint4 cd = *reinterpret_cast<const uint4*>(src + blk * kFp4BlockBytes + lane * 16);
+        const int e = src[blk * kFp4BlockBytes + 512 + lane];
+        if (j & 2) {
+          const uint32_t x = cd.x, y = cd.y;
+          cd.x = cd.z; cd.y = cd.w; cd.z = x; cd.w = y;
+        }
+        const uint32_t row = (uint32_t)(blk * 8 + (lane >> 2));
+        const uint32_t w4[4] = {cd.x, cd.y, cd.z, cd.w};
+        const bool fast = e >= 2 && e <= 142;
+        const uint32_t sb = (uint32_t)(e + 112) << 7, s2 = sb | (sb << 16);  // 2^(e - 15)
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          st_shared16(dst + sw128_off(row, (uint32_t)((j & 1) * 4 + (q ^ (j & 2)))),
+                      fast ? fp4_word_fast(w4[q], s2) : fp4_word_slow(w4[q], e));
+      }
+      fence_proxy_async_smem();  // the bf16 tile is read by the tensor cores
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(smem_u32(&bars->cv_full[c]));
+        mbar_arrive(smem_u32(&bars->empty[s]));
+      }
+    }
+  } else if (warp >= 2 && warp < 10) {
     // ============ epilogue: warps 2..5 (tiles k even), warps 6..9 (k odd) ============
     const int eg = (warp - 2) >> 2;       // epilogue group = TMEM accumulator it reads
     const int sub = warp & 3;             // TMEM sub-partition of this warp
@@ -633,8 +858,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 }  // namespace
 
-size_t index_smem_bytes() {
-  return 1024 + kRingBytes + kBBytes + 8 * 256 * 4 + sizeof(Bars) + 16 + 8 * 8 * kMaxGroup;
+size_t index_smem_bytes(int mode) {
+  return 1024 + ring_bytes(mode) + kBBytes + 8 * 256 * 4 + sizeof(Bars) + 16 + 8 * 8 * kMaxGroup;
 }
 
 cudaError_t launch_index(const IndexArgs& args, int num_sms, cudaStream_t s) {
@@ -644,8 +869,8 @@ cudaError_t launch_index(const IndexArgs& args, int num_sms, cudaStream_t s) {
   cudaError_t e = launch_pdl(index_prep_kernel, dim3(1), dim3(kPrepThreads), 0, s, a);
   if (e != cudaSuccess) return e;
   CUtensorMap kt, kb, qm;
-  const bool f8 = a.plane8 != nullptr;
-  if (f8) {
+  const int mode = a.plane8 ? kModeFp8 : (a.plane4 ? kModeFp4 : kModeBf16);
+  if (mode == kModeFp8) {
     const int64_t qrows = (int64_t)a.Q * a.H;
     e = launch_pdl(quant_q_kernel, dim3((unsigned)((qrows + 7) / 8)), dim3(256), 0, s, a);
     if (e != cudaSuccess) return e;
@@ -661,22 +886,37 @@ cudaError_t launch_index(const IndexArgs& args, int num_sms, cudaStream_t s) {
         !encode_bytes(&kb, a.plane8, 3, dims, strides, box_b) ||
         !encode_bytes(&qm, a.q8, 2, qd, qs, qbox))
       return cudaErrorInvalidValue;
+  } else if (mode == kModeFp4) {
+    // K blocks arrive by bulk copies: only the query map is used (passed three times)
+    if (!encode_rows_bf16(&qm, a.iq, (uint64_t)a.Q * a.H, kDIdx, 64, (uint32_t)a.H))
+      return cudaErrorInvalidValue;
+    kt = qm;
+    kb = qm;
   } else if (!encode_rows_bf16(&kt, a.index_k, (uint64_t)a.index_rows, kDIdx, 64, kTileRows) ||
              !encode_rows_bf16(&kb, a.index_k, (uint64_t)a.index_rows, kDIdx, 64, 8) ||
              !encode_rows_bf16(&qm, a.iq, (uint64_t)a.Q * a.H, kDIdx, 64, (uint32_t)a.H)) {
     return cudaErrorInvalidValue;
   }
-  const size_t smem = index_smem_bytes();
-  auto kern = f8 ? index_score_kernel<true> : index_score_kernel<false>;
+  const size_t smem = index_smem_bytes(mode);
+  auto kern = mode == kModeFp8 ? index_score_kernel<kModeFp8>
+                               : (mode == kModeFp4 ? index_score_kernel<kModeFp4>
+                                                   : index_score_kernel<kModeBf16>);
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  return launch_pdl(kern, dim3(a.nctas), dim3(kThreads), smem, s, a, kt, kb, qm);
+  return launch_pdl(kern, dim3(a.nctas), dim3(num_threads(mode)), smem, s, a, kt, kb, qm);
 }
 
 cudaError_t launch_plane_fp8(const uint16_t* k, int64_t n, uint8_t* plane, cudaStream_t s) {
   if (n <= 0) return cudaSuccess;
   const int64_t nb = (n + 7) / 8;
   return launch_pdl(plane_fp8_kernel, dim3((unsigned)nb), dim3(256), 0, s, k, n, plane);
+}
+
+cudaError_t launch_plane_fp4_index(const uint16_t* k, int64_t n, uint8_t* plane,
+                                   cudaStream_t s) {
+  if (n <= 0) return cudaSuccess;
+  const int64_t nb = (n + 7) / 8;
+  return launch_pdl(plane_fp4_index_kernel, dim3((unsigned)nb), dim3(256), 0, s, k, n, plane);
 }
 
 }  // namespace csa2

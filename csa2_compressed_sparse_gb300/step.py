@@ -114,14 +114,17 @@ def run_step(spec: StepSpec, t, buf: StepBuffers, stream=None, compress=True, si
            scale=spec.scale, ws=buf.attn_ws, stream=main)
 
 
-def fp8_index_plane(index_k, row_base, n_rows):
-    """The FP8 index plane of bf16 index rows held per sequence at row_base[b] (host
-    int sequences n_rows / row_base): every sequence is re-laid to start on an 8-row
-    block, then quantised on the device.  Returns (plane, block-aligned row_base on the
-    device, rows in the plane)."""
+def block_index_plane(index_k, row_base, n_rows, fmt="fp8"):
+    """The FP8 ("fp8") or MXFP4 ("fp4") index plane of bf16 index rows held per sequence
+    at row_base[b] (host int sequences n_rows / row_base): every sequence is re-laid to
+    start on an 8-row block, then quantised on the device.  Returns (plane, block-aligned
+    row_base on the device, rows in the plane)."""
     import numpy as np
     import torch
-    from . import csa2_index_plane_fp8, csa2_index_plane_fp8_bytes
+    from . import (csa2_index_plane_fp4, csa2_index_plane_fp4_bytes, csa2_index_plane_fp8,
+                   csa2_index_plane_fp8_bytes)
+    quant, nbytes = {"fp8": (csa2_index_plane_fp8, csa2_index_plane_fp8_bytes),
+                     "fp4": (csa2_index_plane_fp4, csa2_index_plane_fp4_bytes)}[fmt]
     n = np.asarray(n_rows, dtype=np.int64)
     padded = (n + 7) // 8 * 8
     rb8 = np.concatenate([[0], np.cumsum(padded)[:-1]]).astype(np.int64)
@@ -130,7 +133,11 @@ def fp8_index_plane(index_k, row_base, n_rows):
     for b in range(len(n)):
         r0 = int(row_base[b])
         kpad[int(rb8[b]):int(rb8[b]) + int(n[b])] = index_k[r0:r0 + int(n[b])]
-    plane = torch.empty(csa2_index_plane_fp8_bytes(total), dtype=torch.uint8,
-                        device=index_k.device)
-    csa2_index_plane_fp8(kpad, plane)
+    plane = torch.empty(nbytes(total), dtype=torch.uint8, device=index_k.device)
+    quant(kpad, plane)
     return plane, torch.from_numpy(rb8).to(index_k.device), total
+
+
+def fp8_index_plane(index_k, row_base, n_rows):
+    """block_index_plane in the FP8 format."""
+    return block_index_plane(index_k, row_base, n_rows, "fp8")

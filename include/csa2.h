@@ -230,6 +230,46 @@ csa2_status csa2_index_topk_fp8(const csa2_bf16* iq, const float* w, int Q, int 
                                 csa2_stream stream);
 
 /* ---------------------------------------------------------------------------------
+ * csa2_index_plane_fp4 -- the MXFP4 index plane.  [A] indexer figure (FP4 index rows of
+ * 68 B: 64 B of values and 4 B of scales; planes paged in blocks of 8 rows); [A] indexer
+ * K (E2M1 values with one E8M0 scale per 32 channels, pure powers of two).
+ *
+ * Quantises rows 0 .. rows-1 of a bf16 [rows][128] index plane.  Block b of the output
+ * starts at byte 544 * b: 8 x 64 code bytes for rows 8b .. 8b+7 (byte i of a row holds
+ * dim 2i in its low nibble and dim 2i+1 in its high nibble), then 8 x 4 scale bytes (byte
+ * j of a row scales dims 32j .. 32j+31 by 2^(e - 127)).  A group's e is the smallest in
+ * [0, 254] with max |x| <= 6 * 2^(e - 127), 127 for an all-zero group; its codes are the
+ * E2M1 values nearest x / 2^(e - 127), ties to the even code.  Rows of the last block past
+ * `rows` are zero with e = 127.  The values must stay below 3 * 2^125 in magnitude.
+ *   index_k  device, [rows][128] bf16, 16-byte aligned
+ *   plane    device, csa2_index_plane_fp4_bytes(rows) bytes, 16-byte aligned */
+size_t csa2_index_plane_fp4_bytes(int64_t rows);
+csa2_status csa2_index_plane_fp4(const csa2_bf16* index_k, int64_t rows, uint8_t* plane,
+                                 csa2_stream stream);
+
+/* ---------------------------------------------------------------------------------
+ * csa2_index_topk_fp4 -- csa2_index_topk on an MXFP4 index plane.  [A] indexer figure
+ * (the FP4 plane); [A] Fig. 3b (the scores).
+ *
+ * K[c][d] is the decoded plane value (an E2M1 value times its group's power of two,
+ * which bf16 holds exactly); the queries stay bf16 and the scores are those of
+ * csa2_index_topk on these K rows, computed on the tensor cores in bf16 with fp32 sums.
+ * Everything else (visibility, REINDEX, selection, outputs, errors) as csa2_index_topk.
+ *   plane      csa2_index_plane_fp4 layout holding index_rows rows; every row_base[b]
+ *              must be a multiple of 8 (each sequence starts on a block; a query of a
+ *              sequence that does not raises CSA2_EBOUNDS); a REINDEX candidate block
+ *              outside the plane raises CSA2_EBOUNDS
+ *   ws         csa2_index_topk_fp4_workspace_size(Q, H, max_scored, k) bytes */
+size_t csa2_index_topk_fp4_workspace_size(int Q, int H, int64_t max_scored, int k);
+csa2_status csa2_index_topk_fp4(const csa2_bf16* iq, const float* w, int Q, int H,
+                                const uint8_t* plane, int64_t index_rows,
+                                const int64_t* row_base, const int32_t* q_seq,
+                                const int64_t* q_pos, int ratio, const int32_t* cand, int ncb,
+                                int k, int relu, int64_t max_scored, int32_t* sel,
+                                float* sel_scores, float* scores_out, void* ws, size_t ws_bytes,
+                                csa2_stream stream);
+
+/* ---------------------------------------------------------------------------------
  * csa2_index_topk_noalloc -- the paper has no counterpart: this is a library service.
  *
  * Same arguments and results as csa2_index_topk, minus the workspace.  It is for
