@@ -26,7 +26,9 @@ CSA2_DEFINE_FAULT_FLAG(compress)
 namespace csa2 {
 namespace {
 
-constexpr int kWarps = 8;
+// 4 warps (one token each) per CTA: a compress CTA (128 threads, at most 128 registers)
+// fits beside a score CTA of the indexer, which may run concurrently on another stream.
+constexpr int kWarps = 4;
 
 __device__ __forceinline__ void load8_bf16(const uint16_t* p, float (&v)[8]) {
   uint4 u = *reinterpret_cast<const uint4*>(p);
@@ -141,7 +143,7 @@ __device__ __forceinline__ void emit_index_k(const CompressArgs& a, const float 
   for (int blk = 0; blk < 4; ++blk) dst[32 * blk + lane] = __bfloat16_as_ushort(__float2bfloat16_rn(k[blk]));
 }
 
-__global__ void __launch_bounds__(kWarps * 32) compress_kernel(CompressArgs a) {
+__global__ void __launch_bounds__(kWarps * 32, 4) compress_kernel(CompressArgs a) {
   // cu_seqlens in shared memory (one coalesced read instead of a chain of dependent
   // global loads in the binary search below)
   extern __shared__ int32_t cu_s[];

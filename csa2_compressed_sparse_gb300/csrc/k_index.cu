@@ -89,7 +89,10 @@ __device__ __forceinline__ int64_t n_visible(int64_t pos, int ratio) { return (p
 // the run.  The block's sequence ids and visible counts (plus a halo of kMaxGroup) sit
 // in shared memory, so a leader finds its members without global round trips; group
 // ids and tile offsets come from one block-wide exclusive scan of (leader, tiles).
-constexpr int kPrepThreads = 1024;
+// 256 threads: the prep CTA (8 K registers) fits beside a score CTA on its SM, so that
+// score CTA starts at once instead of after the prep.
+constexpr int kPrepThreads = 256;
+constexpr int kPrepWarps = kPrepThreads / 32;
 
 // Exclusive block sums of (x, y) over threads in index order, with the block totals.
 __device__ __forceinline__ void block_excl_sum2(int x, long long y, int* redx, long long* redy,
@@ -105,9 +108,9 @@ __device__ __forceinline__ void block_excl_sum2(int x, long long y, int* redx, l
   }
   if (lane == 31) { redx[warp] = ix; redy[warp] = iy; }
   __syncthreads();
-  // every warp scans the 32 warp totals itself
-  const int wx = redx[lane];
-  const long long wy = redy[lane];
+  // every warp scans the warp totals itself
+  const int wx = lane < kPrepWarps ? redx[lane] : 0;
+  const long long wy = lane < kPrepWarps ? redy[lane] : 0;
   int sx = wx;
   long long sy = wy;
 #pragma unroll
@@ -126,12 +129,14 @@ __device__ __forceinline__ void block_excl_sum2(int x, long long y, int* redx, l
 __global__ void __launch_bounds__(kPrepThreads) index_prep_kernel(IndexArgs a) {
   __shared__ int s_seq[kPrepThreads + kMaxGroup];
   __shared__ int s_ns[kPrepThreads + kMaxGroup];
-  __shared__ int redx[kPrepThreads / 32];
-  __shared__ long long redy[kPrepThreads / 32];
-  __shared__ int red_run[kPrepThreads / 32];
+  __shared__ int redx[kPrepWarps];
+  __shared__ long long redy[kPrepWarps];
+  __shared__ int red_run[kPrepWarps];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  // The first block's loads read only the call's inputs (positions, sequence ids, row
+  // bases), so they are issued while the preceding kernel drains; nothing is written to
+  // the workspace before the wait (the preceding kernels may still read it).
   griddep_launch_dependents();
-  griddep_wait();
   int carry_run = 0, carry_groups = 0, prev_seq = -1;
   long long carry_tiles = 0;
   for (int base = 0; base < a.Q; base += kPrepThreads) {
@@ -149,16 +154,17 @@ __global__ void __launch_bounds__(kPrepThreads) index_prep_kernel(IndexArgs a) {
         s_ns[i] = (int)ns;
         if ((a.plane8 || a.plane4) && i < kPrepThreads && (a.row_base[s_seq[i]] & 7) != 0)
           raise_fault(kFaultBounds);  // block planes start every sequence on a block
-        if (i < kPrepThreads) {
-          a.n_scored[q] = (int32_t)ns;
-          a.topk_count[q] = 0;
-          if (a.pool_count) a.pool_count[q] = 0;
-        }
       }
     }
-    __syncthreads();
+    if (base == 0) griddep_wait();
     const int q = base + tid;
     const bool in = q < a.Q;
+    if (in) {
+      a.n_scored[q] = (int32_t)s_ns[tid];
+      a.topk_count[q] = 0;
+      if (a.pool_count) a.pool_count[q] = 0;
+    }
+    __syncthreads();
     // run start of q: inclusive max-scan of the positions where the sequence changes
     int v = -1;
     if (in) {
@@ -174,7 +180,7 @@ __global__ void __launch_bounds__(kPrepThreads) index_prep_kernel(IndexArgs a) {
     __syncthreads();
     int rs = max(carry_run, v);
     {
-      const int wv = red_run[lane];
+      const int wv = lane < kPrepWarps ? red_run[lane] : -1;
       int sv = lane < warp ? wv : -1;
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) sv = max(sv, __shfl_xor_sync(0xFFFFFFFFu, sv, o));

@@ -18,8 +18,8 @@
  *     launched as programmatic dependents: a call may start while the preceding kernel
  *     of this library on the stream drains, and reads only its own inputs (queries,
  *     positions, window rows) before that kernel has finished; whatever that kernel
- *     produces (a selection, keys) is read after it.  Inputs written by other kernels
- *     must be complete in stream order, as usual.
+ *     produces (a selection, keys) is read after it, and workspace is written after it.
+ *     Inputs written by other kernels must be complete in stream order, as usual.
  *   - Argument errors are detected on the host before anything is launched and
  *     return CSA2_EINVAL.  CUDA launch failures return CSA2_ECUDA.  The text of the
  *     last failure on the calling thread is available from csa2_last_error().
