@@ -156,3 +156,51 @@ def test_topk_scores_k_limits():
     assert st == 1 and b"merge" in L.csa2_last_error()
     assert csa2.csa2_topk_workspace_size(4, 1 << 20, 2048) == 0
     assert csa2.csa2_topk_workspace_size(4, 1 << 17, 2048) >= 4 * 4 * 2048 * 8
+
+
+def test_block_plane_entry_points_reject_bad_arguments():
+    L = _raw()
+    p = ctypes.c_void_p(256)
+    for name in ("csa2_index_topk_fp8", "csa2_index_topk_fp4"):
+        fn = getattr(L, name)
+        args = dict(iq=p, w=p, Q=4, H=64, plane=p, index_rows=1000, row_base=p, q_seq=p, q_pos=p,
+                    ratio=2, cand=None, ncb=0, k=512, relu=1, max_scored=2048, sel=p,
+                    sel_scores=None, scores_out=None, ws=p, ws_bytes=1 << 30, stream=None)
+
+        def call(**kw):
+            a = dict(args)
+            a.update(kw)
+            return fn(*a.values()), L.csa2_last_error()
+
+        st, msg = call(plane=None)
+        assert st == 1 and b"plane is required" in msg, name
+        st, msg = call(plane=ctypes.c_void_p(264))
+        assert st == 1 and b"aligned" in msg, name
+        st, msg = call(H=16)
+        assert st == 1 and b"H must" in msg, name
+        st, msg = call(ws_bytes=64)
+        assert st == 5 and b"workspace" in msg, name
+        # nothing to do is not an error
+        assert call(Q=0, plane=None)[0] == 0, name
+    for name in ("csa2_index_plane_fp8", "csa2_index_plane_fp4"):
+        fn = getattr(L, name)
+        assert fn(p, 0, p, None) == 0, name  # no rows
+        assert fn(None, 10, p, None) == 1, name
+        assert fn(ctypes.c_void_p(258), 10, p, None) == 1 and b"aligned" in L.csa2_last_error()
+        assert fn(p, -1, p, None) == 1, name
+
+
+def test_block_plane_sizes():
+    assert csa2.csa2_index_plane_fp8_bytes(0) == 0
+    assert csa2.csa2_index_plane_fp8_bytes(1) == 1056
+    assert csa2.csa2_index_plane_fp8_bytes(17) == 3 * 1056
+    assert csa2.csa2_index_plane_fp4_bytes(0) == 0
+    assert csa2.csa2_index_plane_fp4_bytes(8) == 544
+    assert csa2.csa2_index_plane_fp4_bytes(9) == 2 * 544
+    # the FP4 indexer needs no query codes: its workspace is the bf16 indexer's
+    assert (csa2.csa2_index_topk_fp4_workspace_size(64, 64, 32768, 512) ==
+            csa2.csa2_index_topk_workspace_size(64, 64, 32768, 512))
+    assert (csa2.csa2_index_topk_fp8_workspace_size(64, 64, 32768, 512) >
+            csa2.csa2_index_topk_workspace_size(64, 64, 32768, 512))
+    for f in (csa2.csa2_index_topk_fp4_workspace_size, csa2.csa2_index_topk_fp8_workspace_size):
+        assert f(4, 48, 1024, 512) == 0 and f(4, 64, 1024, 513) == 0
