@@ -11,6 +11,7 @@ Under torchrun every rank runs its own batch (weak scaling, no collective on the
 data path); the step time is the maximum over ranks.
 """
 import argparse
+import copy
 import json
 import os
 import statistics
@@ -354,46 +355,104 @@ def run_ours(args):
 
 def run_e2e(args, wl, spec, t, buf, world):
     """Each step copies its inputs from pinned host memory, runs the step through the
-    C ABI and reads the outputs back; timed on the host and on the stream."""
+    C ABI and reads the outputs back; timed on the host and on the stream.
+
+    The step's small inputs (new tokens, queries, positions, weights) live in one
+    contiguous device buffer per slot and are filled by one copy from one pinned host
+    buffer; the outputs (attention output of every layer, the selection) likewise leave
+    in one copy.  Two slots alternate, so the copies of one step run on their own
+    streams while the neighbouring step computes; the steps themselves stay in order on
+    one compute stream (they share the planes and the workspace), each a CUDA graph of
+    the same C-ABI calls."""
     import csa2_compressed_sparse_gb300 as csa2
     from csa2_compressed_sparse_gb300.step import run_step
     names = ["kv", "score", "iq", "w", "q_pos", "q_seq", "cu_seqlens", "start_pos"]
-    host = {n: t[n].cpu().pin_memory() for n in names}
-    hq = [x.cpu().pin_memory() for x in t["q"]]
-    out_h = [torch.empty(x.shape, dtype=x.dtype).pin_memory() for x in buf.out]
-    sel_h = torch.empty(buf.sel.shape, dtype=buf.sel.dtype).pin_memory()
-    h2d = sum(x.numel() * x.element_size() for x in host.values()) + \
-        sum(x.numel() * x.element_size() for x in hq)
-    d2h = sum(x.numel() * x.element_size() for x in out_h) + sel_h.numel() * 4
+    align = 256
+
+    def layout(tensors):
+        offs, o = [], 0
+        for x in tensors:
+            offs.append(o)
+            o += (x.numel() * x.element_size() + align - 1) // align * align
+        return offs, max(o, align)
+
+    def views(flat, tensors, offs):
+        return [flat[o:o + x.numel() * x.element_size()].view(x.dtype).view(x.shape)
+                for x, o in zip(tensors, offs)]
+
+    ins = [t[n] for n in names] + list(t["q"])
+    outs = list(buf.out) + [buf.sel]
+    in_offs, in_bytes = layout(ins)
+    out_offs, out_bytes = layout(outs)
+    h2d = sum(x.numel() * x.element_size() for x in ins)
+    d2h = sum(x.numel() * x.element_size() for x in outs)
+    slots = []
+    for _ in range(2):
+        d_in = torch.empty(in_bytes, dtype=torch.uint8, device="cuda")
+        d_out = torch.empty(out_bytes, dtype=torch.uint8, device="cuda")
+        h_in = torch.empty(in_bytes, dtype=torch.uint8).pin_memory()
+        h_out = torch.empty(out_bytes, dtype=torch.uint8).pin_memory()
+        for v, x in zip(views(h_in, ins, in_offs), ins):
+            v.copy_(x.cpu())
+        iv, ov = views(d_in, ins, in_offs), views(d_out, outs, out_offs)
+        ts = dict(t)
+        ts.update({n: v for n, v in zip(names, iv)})
+        ts["q"] = iv[len(names):]
+        bs = copy.copy(buf)
+        bs.out, bs.sel = ov[:-1], ov[-1]
+        slots.append((d_in, d_out, h_in, h_out, ts, bs))
+    comp, cp_in, cp_out, side = (torch.cuda.Stream() for _ in range(4))
+    graphs = []
+    for d_in, d_out, h_in, h_out, ts, bs in slots:
+        d_in.copy_(h_in)
+        comp.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(comp):
+            run_step(spec, ts, bs, side=side)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=comp):
+            run_step(spec, ts, bs, side=side)
+        graphs.append(g)
+    torch.cuda.synchronize()
+    ev = {k: [torch.cuda.Event() for _ in range(2)] for k in ("in", "comp", "out")}
     steps = max(20, args.steps // 10)
-    stream = torch.cuda.current_stream()
-    side = torch.cuda.Stream()
 
-    def one():
-        for n in names:
-            t[n].copy_(host[n], non_blocking=True)
-        for d, h in zip(t["q"], hq):
-            d.copy_(h, non_blocking=True)
-        run_step(spec, t, buf, side=side)
-        for h, d in zip(out_h, buf.out):
-            h.copy_(d, non_blocking=True)
-        sel_h.copy_(buf.sel, non_blocking=True)
+    def run(n):
+        for i in range(n):
+            s = i & 1
+            d_in, d_out, h_in, h_out, _, _ = slots[s]
+            if i >= 2:
+                cp_in.wait_event(ev["comp"][s])   # step i-2 has read this slot's inputs
+            with torch.cuda.stream(cp_in):
+                d_in.copy_(h_in, non_blocking=True)
+                ev["in"][s].record(cp_in)
+            comp.wait_event(ev["in"][s])
+            if i >= 2:
+                comp.wait_event(ev["out"][s])     # step i-2's outputs have left
+            with torch.cuda.stream(comp):
+                graphs[s].replay()
+                ev["comp"][s].record(comp)
+            cp_out.wait_event(ev["comp"][s])
+            with torch.cuda.stream(cp_out):
+                h_out.copy_(d_out, non_blocking=True)
+                ev["out"][s].record(cp_out)
 
-    for _ in range(3):
-        one()
+    run(4)
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     w0 = time.perf_counter()
-    e0.record(stream)
-    for _ in range(steps):
-        one()
-    e1.record(stream)
+    e0.record(cp_in)
+    run(steps)
+    cp_out.wait_stream(comp)
+    e1.record(cp_out)
     torch.cuda.synchronize()
     wall = max_over_ranks(time.perf_counter() - w0, world, "cuda")
     csa2.csa2_device_status()
     return {"value": weak_value(wl.Q, world, steps, wall * 1e3), "unit": "queries/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-            "device_ms_per_step": e0.elapsed_time(e1) / steps, "steps": steps}
+            "device_ms_per_step": e0.elapsed_time(e1) / steps, "steps": steps,
+            "copies": "one packed H2D and one packed D2H per step, overlapped with the "
+                      "neighbouring step's compute (two slots)"}
 
 
 # ---- CPU oracle legs ------------------------------------------------------------------------
