@@ -126,9 +126,16 @@ __device__ __forceinline__ void block_excl_sum2(int x, long long y, int* redx, l
   __syncthreads();  // redx / redy may be rewritten by the next call
 }
 
+// Groups whose tile ranges the prep keeps in shared memory for the CTA-record pass (more
+// groups are read back from the group records).
+constexpr int kPrepGroupCache = 256;
+
 __global__ void __launch_bounds__(kPrepThreads) index_prep_kernel(IndexArgs a) {
   __shared__ int s_seq[kPrepThreads + kMaxGroup];
   __shared__ int s_ns[kPrepThreads + kMaxGroup];
+  __shared__ long long s_rb[kPrepThreads];       // row base of each query's sequence
+  __shared__ long long s_t0[kPrepGroupCache], s_t1[kPrepGroupCache];
+  __shared__ int s_gfirst[kMaxIndexCtas];
   __shared__ int redx[kPrepWarps];
   __shared__ long long redy[kPrepWarps];
   __shared__ int red_run[kPrepWarps];
@@ -152,8 +159,11 @@ __global__ void __launch_bounds__(kPrepThreads) index_prep_kernel(IndexArgs a) {
         }
         s_seq[i] = a.q_seq[q];
         s_ns[i] = (int)ns;
-        if ((a.plane8 || a.plane4) && i < kPrepThreads && (a.row_base[s_seq[i]] & 7) != 0)
-          raise_fault(kFaultBounds);  // block planes start every sequence on a block
+        if (i < kPrepThreads) {
+          s_rb[i] = a.row_base[s_seq[i]];
+          if ((a.plane8 || a.plane4) && (s_rb[i] & 7) != 0)
+            raise_fault(kFaultBounds);  // block planes start every sequence on a block
+        }
       }
     }
     if (base == 0) griddep_wait();
@@ -210,9 +220,13 @@ __global__ void __launch_bounds__(kPrepThreads) index_prep_kernel(IndexArgs a) {
       r.pad0 = 0;
       r.tile0 = carry_tiles + ey;
       r.tile1 = r.tile0 + tiles;
-      r.rb = a.row_base[r.seq];
+      r.rb = s_rb[tid];
       r.pad1 = 0;
       a.grp[carry_groups + ex] = r;
+      if (carry_groups + ex < kPrepGroupCache) {
+        s_t0[carry_groups + ex] = r.tile0;
+        s_t1[carry_groups + ex] = r.tile1;
+      }
     }
     // carries into the next block (every thread keeps its own copy); block_excl_sum2
     // ended with a barrier, so red_run is free
@@ -229,23 +243,27 @@ __global__ void __launch_bounds__(kPrepThreads) index_prep_kernel(IndexArgs a) {
   // so that a score CTA starts after two loads instead of a search
   const int64_t total = carry_tiles;
   const int64_t per = (total + a.nctas - 1) / a.nctas;
+  for (int c = tid; c < a.nctas; c += kPrepThreads) s_gfirst[c] = 0;
+  __syncthreads();  // the group records (global and cached) are visible to all threads
+  if (per > 0) {
+    const bool cached = carry_groups <= kPrepGroupCache;
+    for (int g = tid; g < carry_groups; g += kPrepThreads) {
+      const int64_t t0 = cached ? s_t0[g] : a.grp[g].tile0;
+      const int64_t t1 = cached ? s_t1[g] : a.grp[g].tile1;
+      // CTAs whose first tile c * per lies in [t0, t1)
+      for (int64_t c = (t0 + per - 1) / per; c * per < t1 && c < a.nctas; ++c)
+        s_gfirst[c] = g;
+    }
+  }
+  __syncthreads();
   for (int c = tid; c < a.nctas; c += kPrepThreads) {
     CtaRec r;
-    r.g_first = 0;
+    r.g_first = s_gfirst[c];
     r.pad0 = 0;
     r.it_lo = min(total, (int64_t)c * per);
     r.it_hi = min(total, r.it_lo + per);
     r.pad1 = 0;
     a.cta[c] = r;
-  }
-  __syncthreads();  // the records above and the group records are visible to all threads
-  if (per > 0) {
-    for (int g = tid; g < carry_groups; g += kPrepThreads) {
-      const int64_t t0 = a.grp[g].tile0, t1 = a.grp[g].tile1;
-      // CTAs whose first tile c * per lies in [t0, t1)
-      for (int64_t c = (t0 + per - 1) / per; c * per < t1 && c < a.nctas; ++c)
-        a.cta[c].g_first = g;
-    }
   }
 }
 
