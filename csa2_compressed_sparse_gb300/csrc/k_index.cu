@@ -723,23 +723,39 @@ __global__ void __launch_bounds__(num_threads(kMode), 1)
       }
       const uint8_t* src = fill_smem + s * kStageBytes;
       const uint32_t dst = smem_u32(a_smem + c * kBf16Tile) + (uint32_t)(j >> 1) * (kBf16Tile / 2);
+      // all of the warp's blocks are loaded, then decoded, then stored, so that their
+      // independent conversions overlap
+      constexpr int kB = 16 / kFp4ConvWarps;
+      uint4 cd[kB];
+      int e[kB];
 #pragma unroll
-      for (int i = 0; i < 16 / kFp4ConvWarps; ++i) {
+      for (int i = 0; i < kB; ++i) {
         const int blk = cw + kFp4ConvWarps * i;
-        uint4 cd = *reinterpret_cast<const uint4*>(src + blk * kFp4BlockBytes + lane * 16);
-        const int e = src[blk * kFp4BlockBytes + 512 + lane];
+        cd[i] = *reinterpret_cast<const uint4*>(src + blk * kFp4BlockBytes + lane * 16);
+        e[i] = src[blk * kFp4BlockBytes + 512 + lane];
+      }
+      uint4 o[kB][4];
+#pragma unroll
+      for (int i = 0; i < kB; ++i) {
         if (j & 2) {
-          const uint32_t x = cd.x, y = cd.y;
-          cd.x = cd.z; cd.y = cd.w; cd.z = x; cd.w = y;
+          const uint32_t x = cd[i].x, y = cd[i].y;
+          cd[i].x = cd[i].z; cd[i].y = cd[i].w; cd[i].z = x; cd[i].w = y;
         }
-        const uint32_t row = (uint32_t)(blk * 8 + (lane >> 2));
-        const uint32_t w4[4] = {cd.x, cd.y, cd.z, cd.w};
-        const bool fast = e >= 2 && e <= 142;
-        const uint32_t sb = (uint32_t)(e + 112) << 7, s2 = sb | (sb << 16);  // 2^(e - 15)
+        const uint32_t w4[4] = {cd[i].x, cd[i].y, cd[i].z, cd[i].w};
+        const uint32_t sb = (uint32_t)(e[i] + 112) << 7, s2 = sb | (sb << 16);  // 2^(e - 15)
+#pragma unroll
+        for (int q = 0; q < 4; ++q) o[i][q] = fp4_word_fast(w4[q], s2);
+        if (!(e[i] >= 2 && e[i] <= 142)) {  // rare: scale codes outside the fast path
+#pragma unroll
+          for (int q = 0; q < 4; ++q) o[i][q] = fp4_word_slow(w4[q], e[i]);
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < kB; ++i) {
+        const uint32_t row = (uint32_t)((cw + kFp4ConvWarps * i) * 8 + (lane >> 2));
 #pragma unroll
         for (int q = 0; q < 4; ++q)
-          st_shared16(dst + sw128_off(row, (uint32_t)((j & 1) * 4 + (q ^ (j & 2)))),
-                      fast ? fp4_word_fast(w4[q], s2) : fp4_word_slow(w4[q], e));
+          st_shared16(dst + sw128_off(row, (uint32_t)((j & 1) * 4 + (q ^ (j & 2)))), o[i][q]);
       }
       fence_proxy_async_smem();  // the bf16 tile is read by the tensor cores
       __syncwarp();
