@@ -16,7 +16,8 @@ import torch
 from . import build as _build
 
 __all__ = [
-    "Csa2Error", "Swa", "lib", "csa2_version", "csa2_device_status", "csa2_compress",
+    "Csa2Error", "Swa", "lib", "csa2_version", "csa2_last_error", "csa2_device_status",
+    "csa2_compress",
     "csa2_compress_index",
     "csa2_index_topk_workspace_size", "csa2_index_topk", "csa2_index_topk_noalloc",
     "csa2_index_topk_pool_workspace_size", "csa2_index_topk_pool", "csa2_topk_workspace_size",
@@ -131,6 +132,11 @@ def _stream(stream):
 
 def csa2_version():
     return lib().csa2_version().decode()
+
+
+def csa2_last_error():
+    """Text of the last failure on the calling thread ('' if none)."""
+    return (lib().csa2_last_error() or b"").decode()
 
 
 def csa2_device_status(stream=None):

@@ -204,3 +204,18 @@ def test_block_plane_sizes():
             csa2.csa2_index_topk_workspace_size(64, 64, 32768, 512))
     for f in (csa2.csa2_index_topk_fp4_workspace_size, csa2.csa2_index_topk_fp8_workspace_size):
         assert f(4, 48, 1024, 512) == 0 and f(4, 64, 1024, 513) == 0
+
+
+def test_binding_has_every_declared_function():
+    # the Python binding mirrors the C ABI name for name
+    missing = [n for n in declared_functions() if not hasattr(csa2, n)]
+    assert not missing, f"declared in csa2.h without a binding: {missing}"
+    assert all(n in csa2.__all__ for n in declared_functions())
+
+
+def test_last_error_text_after_a_rejected_call():
+    L = _raw()
+    one = ctypes.c_void_p(16)
+    assert L.csa2_compress(one, one, 4, one, 1, one, 3, one, one, one, 10, one, None, 1e-6,
+                           one, None) == 1
+    assert "ratio" in csa2.csa2_last_error()
