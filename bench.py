@@ -588,7 +588,7 @@ def run_stages(args):
     res["compress"] = timed(lambda: csa2.csa2_compress(
         t["kv"], t["score"], t["cu_seqlens"], t["start_pos"], spec.ratio, t["kv_state"],
         t["score_state"], t["plane"], t["row_base"], t["inv_freq"], eps=spec.eps))
-    # index K production in the compressor (NEXT-4): seeded weights of the pages' shapes
+    # index K produced inside the compressor (wk, k_norm, RoPE): seeded weights of the pages' shapes
     g = np.random.default_rng(5)
     wk = torch.from_numpy((g.standard_normal((128, 512)) / np.sqrt(512)).astype(np.float32))
     wk = wk.bfloat16().cuda()
@@ -609,7 +609,7 @@ def run_stages(args):
         res["index_topk_pool"] = timed(lambda: csa2.csa2_index_topk_pool(
             t["iq"], t["w"], t["index_k"], t["row_base"], t["q_seq"], t["q_pos"], spec.ratio,
             spec.k, spec.max_scored, buf.sel, pool, pws, sel_scores=buf.sel_scores))
-    # the FP8 index plane (NEXT-3): sequences re-laid on 8-row blocks, quantised once
+    # the FP8 index plane: sequences re-laid on 8-row blocks, quantised once
     from csa2_compressed_sparse_gb300.step import fp8_index_plane
     plane8, rb8, rows8 = fp8_index_plane(t["index_k"], wl.row_base, wl.n_rows)
     ws8 = torch.empty(csa2.csa2_index_topk_fp8_workspace_size(wl.Q, spec.H, spec.max_scored,
@@ -619,7 +619,7 @@ def run_stages(args):
     res["index_topk_fp8"] = timed(lambda: csa2.csa2_index_topk_fp8(
         t["iq"], t["w"], plane8, rows8, rb8, t["q_seq"], t["q_pos"], spec.ratio, spec.k,
         spec.max_scored, sel8, ws8, cand=cand))
-    # the MXFP4 index plane (NEXT-3): the same re-laying, quantised once
+    # the MXFP4 index plane: the same re-laying, quantised once
     from csa2_compressed_sparse_gb300.step import block_index_plane
     plane4i, rb4, rows4 = block_index_plane(t["index_k"], wl.row_base, wl.n_rows, "fp4")
     ws4 = torch.empty(csa2.csa2_index_topk_fp4_workspace_size(wl.Q, spec.H, spec.max_scored,
@@ -635,7 +635,7 @@ def run_stages(args):
     res["sparse_attn_rope"] = timed(lambda: csa2.csa2_sparse_attn_rope(
         t["q"][0], t["q_seq"], t["q_pos"], swa0, t["plane"], t["row_base"], buf.sel, t["sink"],
         buf.out[0], t["inv_freq"], scale=spec.scale, ws=buf.attn_ws))
-    # the FP4 main plane (NEXT-3): the same rows quantised once
+    # the FP4 main plane: the same rows quantised once
     rows = t["plane"].shape[0]
     p4 = torch.empty(csa2.csa2_plane_fp4_bytes(rows), dtype=torch.uint8, device="cuda")
     csa2.csa2_plane_fp4(t["plane"], p4)

@@ -26,7 +26,7 @@ __all__ = [
     "csa2_index_topk_fp4_workspace_size", "csa2_index_topk_fp4",
     "csa2_topk_scores", "csa2_attn_workspace_size", "csa2_sparse_attn", "csa2_reuse_attn",
     "csa2_sparse_attn_rope", "csa2_reuse_attn_rope", "csa2_plane_fp4_bytes", "csa2_plane_fp4",
-    "csa2_sparse_attn_fp4",
+    "csa2_sparse_attn_fp4", "csa2_selftest_wait_timeout",
 ]
 
 STATUS = {0: "CSA2_OK", 1: "CSA2_EINVAL", 2: "CSA2_ECUDA", 3: "CSA2_ETIMEOUT", 4: "CSA2_EBOUNDS",
@@ -53,6 +53,7 @@ _SIGS = {
     "csa2_last_error": ([], ctypes.c_char_p),
     "csa2_version": ([], ctypes.c_char_p),
     "csa2_device_status": ([_vp], _i32),
+    "csa2_selftest_wait_timeout": ([_i64, _vp], _i32),
     "csa2_compress": ([_vp, _vp, _i32, _vp, _i32, _vp, _i32, _vp, _vp, _vp, _i64, _vp, _vp, _f32,
                        _vp, _vp], _i32),
     "csa2_compress_index": ([_vp, _vp, _i32, _vp, _i32, _vp, _i32, _vp, _vp, _vp, _i64, _vp,
@@ -141,6 +142,10 @@ def csa2_last_error():
 
 def csa2_device_status(stream=None):
     _check(lib().csa2_device_status(_stream(stream)))
+
+
+def csa2_selftest_wait_timeout(limit_ns, stream=None):
+    _check(lib().csa2_selftest_wait_timeout(int(limit_ns), _stream(stream)))
 
 
 @dataclass

@@ -138,6 +138,8 @@ struct AttnArgs {
 };
 
 cudaError_t launch_compress(const CompressArgs& a, cudaStream_t s);
+// One CTA whose bounded wait runs out after limit_ns (test of the timeout path).
+cudaError_t launch_wait_timeout(uint64_t limit_ns, cudaStream_t s);
 cudaError_t launch_index(const IndexArgs& a, int num_sms, cudaStream_t s);
 cudaError_t launch_plane_fp4_index(const uint16_t* k, int64_t n, uint8_t* plane, cudaStream_t s);
 // bf16 plane rows [n][512] -> FP4 rows [n][288].

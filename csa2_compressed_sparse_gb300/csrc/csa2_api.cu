@@ -187,6 +187,15 @@ csa2_status csa2_device_status(csa2_stream stream) {
   return CSA2_OK;
 }
 
+csa2_status csa2_selftest_wait_timeout(int64_t limit_ns, csa2_stream stream) {
+  REQUIRE(limit_ns >= 1000 && limit_ns <= 1000000000,
+          "csa2_selftest_wait_timeout: limit_ns must be in [1e3, 1e9] (got %lld)",
+          (long long)limit_ns);
+  cudaError_t e = csa2::launch_wait_timeout((uint64_t)limit_ns, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "csa2_selftest_wait_timeout");
+  return CSA2_OK;
+}
+
 csa2_status csa2_compress(const csa2_bf16* kv, const csa2_bf16* score, int T,
                           const int32_t* cu_seqlens, int B, const int64_t* start_pos, int ratio,
                           float* kv_state, float* score_state, csa2_bf16* plane,

@@ -417,9 +417,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int64_t pos = p - (kRing - 1) + kChunk * c + r;
       if (pos >= 0) {
         int64_t idx;
-        if (a.swa_mode == 0) idx = (int64_t)b * kRing + (pos & (kRing - 1));
-        else idx = a.lin_base[b] + (pos - a.lin_pos0[b]);
-        if (idx >= 0 && idx < a.swa_rows) idx32 = (int32_t)idx;
+        bool ok = true;
+        if (a.swa_mode == 0) {
+          idx = (int64_t)b * kRing + (pos & (kRing - 1));
+        } else {
+          // a position before the sequence's first stored row would index the previous
+          // sequence's rows: a caller error, skipped and flagged
+          const int64_t p0 = a.lin_pos0[b];
+          ok = pos >= p0;
+          idx = a.lin_base[b] + (pos - p0);
+        }
+        if (ok && idx >= 0 && idx < a.swa_rows) idx32 = (int32_t)idx;
         else raise_fault(kFaultBounds);
       }
     } else {

@@ -321,6 +321,23 @@ cudaError_t launch_plane_fp4(const uint16_t* rows, int64_t n, uint8_t* out, cuda
                     out);
 }
 
+// Self-test of the bounded waits: thread 0 waits for the first phase of a fresh
+// mbarrier that nothing arrives on (no copy or MMA is attached to it), so the wait runs
+// out after limit_ns, records the timeout in the fault flag and the kernel returns.
+__global__ void __launch_bounds__(32) wait_timeout_kernel(uint64_t limit_ns) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&bar), 1);
+    mbar_fence_init();
+    mbar_wait(smem_u32(&bar), 0, limit_ns);
+  }
+}
+
+cudaError_t launch_wait_timeout(uint64_t limit_ns, cudaStream_t s) {
+  wait_timeout_kernel<<<1, 32, 0, s>>>(limit_ns);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_compress(const CompressArgs& a, cudaStream_t s) {
   if (a.T == 0) return cudaSuccess;
   const int grid = (a.T + kWarps - 1) / kWarps;

@@ -17,6 +17,8 @@
 #include <cstdio>
 #include <mutex>
 
+#include <cudaTypedefs.h>
+
 #include "../../include/csa2.h"
 #include "common.cuh"
 
@@ -28,23 +30,66 @@ static __device__ __align__(256) uint8_t g_index_scratch[kScratchBytes];
 
 constexpr int kMaxDevices = 64;
 std::mutex g_mu;
+// Per device: the context the address was looked up in, and the address.  A device
+// reset (cudaDeviceReset) or a re-created primary context reloads the library's module,
+// and the array may then sit elsewhere, so the address is looked up again whenever the
+// current context is not the one it came from.
+CUcontext g_scratch_ctx[kMaxDevices] = {};
 void* g_scratch_ptr[kMaxDevices] = {};
 
-// Device address of g_index_scratch on the current device (looked up once per device;
-// the host-side name of the array is only a stand-in and must not reach a kernel).
-csa2_status scratch_on_current_device(void** out, int* dev_out) {
+PFN_cuCtxGetCurrent_v4000 ctx_getter() {
+  static PFN_cuCtxGetCurrent_v4000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult qr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault, &qr) ==
+            cudaSuccess &&
+        qr == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(p);
+  });
+  return fn;
+}
+
+// Device address of g_index_scratch in the current device's current context (the
+// host-side name of the array is only a stand-in and must not reach a kernel).  On
+// failure writes the reason to msg and returns CSA2_ECUDA, leaving no CUDA error pending.
+csa2_status scratch_on_current_device(void** out, char* msg, size_t msg_len) {
   int dev = -1;
   cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess || dev < 0 || dev >= kMaxDevices) return CSA2_ECUDA;
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    snprintf(msg, msg_len, "csa2_index_topk_noalloc: cudaGetDevice failed: %s",
+             cudaGetErrorString(e));
+    return CSA2_ECUDA;
+  }
+  if (dev < 0 || dev >= kMaxDevices) {
+    snprintf(msg, msg_len, "csa2_index_topk_noalloc: device %d is beyond the %d devices this "
+             "entry point serves", dev, kMaxDevices);
+    return CSA2_ECUDA;
+  }
+  // cudaFree(0) is not called: with no context yet, cudaGetSymbolAddress creates the
+  // primary context itself; the context is read after it.
   std::lock_guard<std::mutex> lock(g_mu);
-  if (!g_scratch_ptr[dev]) {
+  CUcontext ctx = nullptr;
+  PFN_cuCtxGetCurrent_v4000 get = ctx_getter();
+  if (get && get(&ctx) != CUDA_SUCCESS) ctx = nullptr;
+  if (!g_scratch_ptr[dev] || ctx == nullptr || ctx != g_scratch_ctx[dev]) {
     void* p = nullptr;
     e = cudaGetSymbolAddress(&p, g_index_scratch);
-    if (e != cudaSuccess || p == nullptr) return CSA2_ECUDA;
+    if (e != cudaSuccess || p == nullptr) {
+      cudaGetLastError();  // a failed lookup must not surface in the caller's next check
+      snprintf(msg, msg_len,
+               "csa2_index_topk_noalloc: no device address for the scratch array on device %d: %s",
+               dev, e != cudaSuccess ? cudaGetErrorString(e) : "null address");
+      g_scratch_ptr[dev] = nullptr;
+      return CSA2_ECUDA;
+    }
+    if (get && get(&ctx) != CUDA_SUCCESS) ctx = nullptr;  // the lookup may have made it
     g_scratch_ptr[dev] = p;
+    g_scratch_ctx[dev] = ctx;
   }
   *out = g_scratch_ptr[dev];
-  *dev_out = dev;
   return CSA2_OK;
 }
 
@@ -70,9 +115,9 @@ csa2_status csa2_index_topk_noalloc(const csa2_bf16* iq, const float* w, int Q, 
     return CSA2_ENOSPACE;
   }
   void* p = nullptr;
-  int dev = 0;
-  if (scratch_on_current_device(&p, &dev) != CSA2_OK) {
-    csa2::set_last_error("csa2_index_topk_noalloc: no device address for the scratch array");
+  char msg[256];
+  if (scratch_on_current_device(&p, msg, sizeof(msg)) != CSA2_OK) {
+    csa2::set_last_error(msg);
     return CSA2_ECUDA;
   }
   return csa2_index_topk(iq, w, Q, H, index_k, index_rows, row_base, q_seq, q_pos, ratio, cand,

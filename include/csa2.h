@@ -71,6 +71,19 @@ const char* csa2_version(void);
 csa2_status csa2_device_status(csa2_stream stream);
 
 /* ---------------------------------------------------------------------------------
+ * csa2_selftest_wait_timeout -- test export; the pages have no counterpart.
+ *
+ * Every wait inside the library's kernels (on an mbarrier: a copy landing, an MMA
+ * completing, a partner warp) is bounded: when it runs out the kernel records
+ * CSA2_ETIMEOUT in the device fault flag and unwinds instead of hanging the GPU.  This
+ * call exercises that path on purpose: it launches one CTA whose thread waits for an
+ * mbarrier phase that nothing completes (no copy or MMA is attached to it), with the
+ * limit limit_ns nanoseconds (1e3 .. 1e9).  The wait runs out, the kernel returns, and
+ * the next csa2_device_status() reports CSA2_ETIMEOUT (and clears the flag).  The
+ * context stays usable. */
+csa2_status csa2_selftest_wait_timeout(int64_t limit_ns, csa2_stream stream);
+
+/* ---------------------------------------------------------------------------------
  * csa2_compress -- [A] "特殊模块 · compressor", "CSA2 的池化比 V4 简单一截";
  * [B] §4.1 (odd tail), §6.1-6.2 (partial RoPE at the group head); [C] §6.2, §6.4.
  *
@@ -282,7 +295,12 @@ csa2_status csa2_index_topk_fp4(const csa2_bf16* iq, const float* w, int Q, int 
  *   - Sizes needing more than 64 MiB (see csa2_index_topk_workspace_size) are refused
  *     with CSA2_ENOSPACE before anything is enqueued.
  *   - The first call on a device looks up the array's device address with a host-side
- *     runtime call; make that first call before any stream capture.
+ *     runtime call; make that first call before any stream capture.  The address is
+ *     kept per device together with the CUDA context it came from; after a device reset
+ *     or a re-created primary context the next call looks it up again (so, after a
+ *     reset, make one call before capturing again).
+ *   - A failed lookup returns CSA2_ECUDA with the CUDA error text in csa2_last_error()
+ *     and leaves no error pending in cudaGetLastError().
  *   - All calls on a device share the array.  Calls whose kernels can overlap on the
  *     GPU (unordered streams) race and give wrong results: order them.
  *   - Nothing in the array needs to start at zero: each call writes every entry it
@@ -329,7 +347,11 @@ csa2_status csa2_topk_scores(const float* scores, const int32_t* n, int Q, int64
  *   swa    window source (HOST struct, device pointers inside):
  *          RING:   data holds [B][128] rows, position pos in slot pos % 128
  *          LINEAR: data holds rows; position pos of sequence b is row
- *                  lin_base[b] + pos - lin_pos0[b]
+ *                  lin_base[b] + pos - lin_pos0[b]; the rows must cover every
+ *                  window position max(0, p-127) .. p of each query, i.e.
+ *                  lin_pos0[b] <= max(0, p-127).  A window position below lin_pos0[b]
+ *                  raises CSA2_EBOUNDS and is skipped (it is never read from another
+ *                  sequence's rows)
  *          BF16 rows are 512 bf16; FP8_S128 rows are 528 bytes: 512 E4M3 codes then
  *          four fp32 scales, value = code * scale[d / 128]; FP8_E8M0 rows are 528
  *          bytes: 512 E4M3 codes then 16 E8M0 scales, value = code * 2^(e[d / 32] - 127)

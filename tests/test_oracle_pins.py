@@ -331,7 +331,7 @@ def test_index_reindex_rows_and_masks():
             assert sc[0, i] == full[0, r]
 
 
-# ---- index K production (NEXT-4) ---------------------------------------------------
+# ---- index K production in the compressor ---------------------------------------------------
 
 def run_compress_index(kv, ratio, wk, knorm_w=None, start=0, eps=1e-6):
     """One sequence [S,512] (kv used as score too) in one call: plane, index rows, f64s."""
@@ -432,7 +432,7 @@ def test_index_k_norm_weight_rope_phase_and_group_position():
                                    rtol=1e-12)
 
 
-# ---- FP4 main plane (NEXT-3) ----------------------------------------------------------
+# ---- FP4 main plane ----------------------------------------------------------
 
 E2M1 = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]
 
@@ -590,7 +590,7 @@ def test_mxfp4_scores_equal_bf16_scores_when_lossless():
     np.testing.assert_allclose(b, a, rtol=1e-12, atol=1e-12)
 
 
-# ---- FP8 index plane (NEXT-3) --------------------------------------------------------
+# ---- FP8 index plane --------------------------------------------------------
 
 def _e4m3_values():
     return np.array([oracle.e4m3_value(c) for c in range(0x7F)])  # +0 .. 448
