@@ -167,6 +167,60 @@ class Clocks:
                 "samples": len(sm)}
 
 
+def steps_per_graph(steps, cap=16):
+    """Steps captured in one CUDA graph: the largest divisor of `steps` up to `cap`."""
+    return max(g for g in range(1, min(cap, max(steps, 1)) + 1) if steps % g == 0)
+
+
+def upload_graphs(graphs, stream):
+    """Upload instantiated graphs to the device (cuGraphUpload), so that their first replay
+    costs no more than any other; where the exec handle is not exposed, replay each once."""
+    import ctypes
+    try:
+        cu = ctypes.CDLL("libcuda.so.1")
+        cu.cuGraphUpload.argtypes = [ctypes.c_void_p, ctypes.c_void_p]
+        for g in graphs:
+            if cu.cuGraphUpload(ctypes.c_void_p(g.raw_cuda_graph_exec()),
+                                ctypes.c_void_p(stream.cuda_stream)) != 0:
+                raise RuntimeError("cuGraphUpload failed")
+    except (AttributeError, OSError, RuntimeError):
+        for g in graphs:
+            g.replay()
+    torch.cuda.synchronize()
+
+
+def step_fn(csa2, spec, t, buf, side_c):
+    """One step on the current stream, returned as a function of an optional pair of
+    events recorded around the index stage.  The compressor writes only the main plane,
+    which the indexer does not read: it runs on `side_c`, concurrently with index + top-k,
+    joined before the attention."""
+    from csa2_compressed_sparse_gb300.step import swa_of
+
+    def one_step(ev=None):
+        cur = torch.cuda.current_stream()
+        side_c.wait_stream(cur)
+        with torch.cuda.stream(side_c):
+            if t["kv"].shape[0]:
+                csa2.csa2_compress(t["kv"], t["score"], t["cu_seqlens"], t["start_pos"],
+                                   spec.ratio, t["kv_state"], t["score_state"], t["plane"],
+                                   t["row_base"], t["inv_freq"], eps=spec.eps)
+        if ev is not None:
+            ev[0].record()
+        csa2.csa2_index_topk(t["iq"], t["w"], t["index_k"], t["row_base"], t["q_seq"],
+                             t["q_pos"], spec.ratio, spec.k, spec.max_scored, buf.sel, buf.ws,
+                             sel_scores=buf.sel_scores, cand=t.get("cand"), relu=spec.relu)
+        if ev is not None:
+            ev[1].record()
+        cur.wait_stream(side_c)
+        for layer in range(len(t["q"])):
+            fn = csa2.csa2_sparse_attn if layer == 0 else csa2.csa2_reuse_attn
+            fn(t["q"][layer], t["q_seq"], t["q_pos"], swa_of(spec, t, layer), t["plane"],
+               t["row_base"], buf.sel, t["sink"], buf.out[layer], scale=spec.scale,
+               ws=buf.attn_ws)
+
+    return one_step
+
+
 def traffic_from_profile(config):
     """DRAM bytes per launch of the index score kernel from the committed ncu summary."""
     p = os.path.join(ROOT, "profiles", f"index_score_kernel.{config}.md")
@@ -198,48 +252,19 @@ def run_ours(args):
     csa2.csa2_device_status()
 
     # ---- device-resident timing of K steps ----
-    # One step (compress || index + top-k, then attention layers) is captured as one CUDA graph
-    # (the C ABI only enqueues kernels, so it captures as is) and replayed K times.  The
-    # index stage is timed on the launching stream by event-record nodes: NS copies of
-    # the step graph carry their own pair of events around the index stage, and they
-    # replace every (K // NS)-th plain replay, so the sampled durations span the timed
-    # region without a host synchronisation inside it.
-    from csa2_compressed_sparse_gb300.step import swa_of
-
-    def st_compress():
-        if t["kv"].shape[0]:
-            csa2.csa2_compress(t["kv"], t["score"], t["cu_seqlens"], t["start_pos"],
-                               spec.ratio, t["kv_state"], t["score_state"], t["plane"],
-                               t["row_base"], t["inv_freq"], eps=spec.eps)
-
-    def st_index():
-        csa2.csa2_index_topk(t["iq"], t["w"], t["index_k"], t["row_base"], t["q_seq"],
-                             t["q_pos"], spec.ratio, spec.k, spec.max_scored, buf.sel, buf.ws,
-                             sel_scores=buf.sel_scores, cand=t.get("cand"), relu=spec.relu)
-
-    def st_attn():
-        for layer in range(len(t["q"])):
-            fn = csa2.csa2_sparse_attn if layer == 0 else csa2.csa2_reuse_attn
-            fn(t["q"][layer], t["q_seq"], t["q_pos"], swa_of(spec, t, layer), t["plane"],
-               t["row_base"], buf.sel, t["sink"], buf.out[layer], scale=spec.scale,
-               ws=buf.attn_ws)
-
-    # The compressor writes only the main plane, which the indexer does not read: it runs
-    # on a second stream, concurrently with index + top-k, joined before the attention.
+    # The K steps run as replays of CUDA graphs that each hold G consecutive steps (G the
+    # largest divisor of K up to 16; the C ABI only enqueues kernels, so it captures as is):
+    # inside a graph the kernels of one step follow those of the previous step with
+    # programmatic dependent launch, as they would in an engine's decode loop, instead of
+    # paying a graph launch per step.  Every step keeps its full order: a step's first
+    # kernels wait for the previous step's last one.  The index stage is timed on the
+    # launching stream by event-record nodes: NS copies of the G-step graph carry a pair of
+    # events around the index stage of their middle step and replace every (K/G // NS)-th
+    # plain replay, so the sampled durations span the timed region without a host
+    # synchronisation inside it.  Every graph is uploaded to the device before the
+    # warm-up, so no replay in the timed region pays for its first launch.
     side_c = torch.cuda.Stream()
-
-    def one_step(ev=None):
-        cur = torch.cuda.current_stream()
-        side_c.wait_stream(cur)
-        with torch.cuda.stream(side_c):
-            st_compress()
-        if ev is not None:
-            ev[0].record()
-        st_index()
-        if ev is not None:
-            ev[1].record()
-        cur.wait_stream(side_c)
-        st_attn()
+    one_step = step_fn(csa2, spec, t, buf, side_c)
 
     side = torch.cuda.Stream()
     side.wait_stream(stream)
@@ -247,20 +272,25 @@ def run_ours(args):
         one_step()
     stream.wait_stream(side)
     torch.cuda.synchronize()
-    n_samples = max(1, min(args.steps, 32))
-    stride = args.steps // n_samples
+    G = steps_per_graph(args.steps)
+    n_chain = args.steps // G
+    n_samples = max(1, min(n_chain, 32))
+    stride = n_chain // n_samples
     sample_ev = [(torch.cuda.Event(enable_timing=True, external=True),
                   torch.cuda.Event(enable_timing=True, external=True))
                  for _ in range(n_samples)]
-    g_plain = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g_plain):
-        one_step()
-    g_sample = []
-    for ev in sample_ev:
+
+    def capture(n, ev=None):
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g):
-            one_step(ev)
-        g_sample.append(g)
+            for i in range(n):
+                one_step(ev if i == n // 2 else None)
+        return g
+
+    g_one = capture(1)                 # warm-up steps
+    g_plain = capture(G)
+    g_sample = [capture(G, ev) for ev in sample_ev]
+    upload_graphs([g_one, g_plain] + g_sample, stream)
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     clocks = Clocks(local)
     clocks.start()
@@ -268,14 +298,14 @@ def run_ours(args):
     # the W warm-up steps run after the clock sampler's start-up pause, so that the GPU
     # enters the timed region from the warm-up, not from idle
     for i in range(max(args.warmup, 3)):
-        (g_sample[i % n_samples] if i < n_samples else g_plain).replay()
+        g_one.replay()
     torch.cuda.synchronize()
     csa2.csa2_device_status()
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
     ev0.record(stream)
-    for i in range(args.steps):
+    for i in range(n_chain):
         j, r = divmod(i, stride)
         (g_sample[j] if r == 0 and j < n_samples else g_plain).replay()
     ev1.record(stream)
@@ -296,7 +326,7 @@ def run_ours(args):
     # ---- end to end through the public API with host buffers ----
     e2e = None
     if not args.no_e2e:
-        e2e = run_e2e(args, wl, spec, t, buf, world)
+        e2e = run_e2e(args, wl, spec, t, buf, world, ms_step)
 
     line = {
         "metric": METRIC,
@@ -325,6 +355,7 @@ def run_ours(args):
             "l2": "inputs larger than L2: the index plane read per step is "
                   f"{index_bytes / 1e6:.0f} MB",
             "parallelism": f"dp{world} (independent sequence batches per GPU)",
+            "steps_per_graph": G,
         },
         "achieved_hbm_gbs": total_bytes / (ms_step / 1e3) / 1e9,
         "algorithmic_bytes_per_step": total_bytes,
@@ -353,7 +384,7 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
-def run_e2e(args, wl, spec, t, buf, world):
+def run_e2e(args, wl, spec, t, buf, world, ms_step):
     """Each step copies its inputs from pinned host memory, runs the step through the
     C ABI and reads the outputs back; timed on the host and on the stream.
 
@@ -415,7 +446,8 @@ def run_e2e(args, wl, spec, t, buf, world):
         graphs.append(g)
     torch.cuda.synchronize()
     ev = {k: [torch.cuda.Event() for _ in range(2)] for k in ("in", "comp", "out")}
-    steps = max(20, args.steps // 10)
+    # at least half a second of steps, whatever --steps is
+    steps = max(20, args.steps // 10, int(0.5e3 / max(ms_step, 1e-3)) + 1)
 
     def run(n):
         for i in range(n):

@@ -31,9 +31,10 @@
 //            [head][row] is the B operand
 // S of the next chunk runs while the softmax of this one does, and the gather of
 // chunk c + 2 starts as soon as the PV of chunk c has released its buffer.
-// With nsplit = 1 the CTA starts from the sink (running max = sink, running sum = 1)
-// and writes the output.  With nsplit = 2 the two CTAs of a query run as a cluster and
-// merge through distributed shared memory, each finishing half of the dims.  Otherwise
+// Every CTA starts its running max at the sink logit.  With nsplit = 1 its running sum
+// starts at the sink's mass (1) and the CTA writes the output.  With nsplit = 2 the two
+// CTAs of a query run as a cluster and merge through distributed shared memory, each
+// finishing half of the dims.  Otherwise
 // every CTA writes its partial (max, sum, O) to the workspace and attn_combine_kernel
 // merges them; the merges add the sink's e^{sink_h} once.
 //
@@ -74,7 +75,8 @@ struct __align__(16) Aux {
   float rope_c[32];  // inverse RoPE of the output at the query position: cos, sin of
   float rope_s[32];  // p theta_i for pair i (dims 448 + 2i, 449 + 2i)
   float peer_m[64];  // cluster merge: the other CTA's running max and sum (filled by a
-  float peer_l[64];  // bulk copy of its m_run, l_run: the pairs must stay adjacent)
+  float peer_l[64];  // store of its m_run, l_run: the pairs must stay adjacent)
+  float sink2[64];   // sink logit per head in log2 units (-inf without a sink)
   int32_t rowidx[kMaxChunks][kChunk];  // source row per slot (chunk = rank + slot * nsplit)
   uint32_t rowmask[kMaxChunks][2];     // valid rows of each slot
   int chunks[kMaxChunks];              // non-empty slots, in order
@@ -84,7 +86,7 @@ struct __align__(16) Aux {
   uint64_t p_full[2];   // P buffer written and O^T rescaled (128 arrivals)
   uint64_t pv_done[2];  // PV of the buffer's chunk complete (two commits)
   uint64_t fin[4];      // every MMA of an issuer complete (commit)
-  uint64_t merge_full;  // cluster merge: the peer's pieces and (max, sum) landed
+  uint64_t merge_full[2];  // cluster merge: the peer's rows of each tile landed
   uint32_t tmem_slot;
   int nchunk;
   int abort;
@@ -379,7 +381,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(smem_u32(&X.pv_done[b]), 2);
     }
     for (int r = 0; r < 4; ++r) mbar_init(smem_u32(&X.fin[r]), 1);
-    mbar_init(smem_u32(&X.merge_full), 1);
+    for (int t = 0; t < 2; ++t) mbar_init(smem_u32(&X.merge_full[t]), 1);
     X.nchunk = 0;
     X.abort = 0;
     mbar_fence_init();
@@ -600,10 +602,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int hA = 16 * warp + (lane >> 2), hB = hA + 8;
     const uint32_t lrow = (uint32_t)(warp * 32) << 16;
     float mA = -INFINITY, mB = -INFINITY, lA = 0.f, lB = 0.f;
-    if (nsplit == 1 && a.sink) {
+    if (a.sink) {
+      // the running max starts at the sink logit, so no chunk needs a separate max pass;
+      // the sink's own mass enters the sum here with one CTA per query, else once in the
+      // merge
       mA = a.sink[hA] * kLog2e;
       mB = a.sink[hB] * kLog2e;
-      if (r4 == 0) { lA = 1.f; lB = 1.f; }
+      if (nsplit == 1 && r4 == 0) { lA = 1.f; lB = 1.f; }
+    }
+    if (r4 == 0) {
+      X.sink2[hA] = mA;
+      X.sink2[hB] = mB;
     }
     for (int it = 0; it < n; ++it) {
       const int bsel = it & 1;
@@ -738,52 +747,134 @@ __global__ void __launch_bounds__(kThreads, 1)
       a.lse[(int64_t)q * kHeads + tid] =
           (X.m_run[tid] + __log2f(X.l_run[tid])) * 0.6931471805599453f;
   } else if (a.cluster) {
-    // Two CTAs per query as a cluster: CTA r finishes dims 256 r .. 256 r + 255.  Each
-    // stages its partial O^T (fp32 rows of 64 heads per dim): the other's dims in its
-    // second KV buffer, which it ships with its running max and sum by bulk copy into the
-    // other's first KV buffer, and its own dims in the Q buffer; then every thread merges
-    //   o = (2^(m_own - M) O_own + 2^(m_peer - M) O_peer) / Z,
-    //   M = max(m_own, m_peer, sink),  Z = 2^(sink - M) + sum 2^(m - M) l.
+    // Two CTAs per query as a cluster: CTA r finishes dims 256 r .. 256 r + 255 (the O^T
+    // tiles 2 r and 2 r + 1).  Warps 0..7 stage the two tiles the peer finishes from TMEM
+    // (warp w: TMEM lanes 32 (w % 4) .., tile w / 4) in the second KV buffer, and the
+    // lanes of warp 16 store (m_run, l_run) into the peer's peer_m, peer_l.  After a
+    // cluster barrier (both CTAs past their main loops, so the peer's Q buffer is free)
+    // one bulk copy per tile ships the staged rows into the peer's Q buffer, each counted
+    // by its own merge barrier, and warps 8 and 9 form the merge weights of the 64 heads,
+    //   M = max(m_own, m_peer, sink),  Z = 2^(sink - M) + sum 2^(m - M) l,
+    //   o = (2^(m_own - M) O_own + 2^(m_peer - M) O_peer) / Z.
+    // Warps 8..11 merge their own first tile as soon as its peer rows land (while the
+    // second tile's copy is in flight), warps 12..15 the second: every thread takes one
+    // dim for all heads and writes it, one shuffle per pair of heads giving each lane a
+    // bf16 pair of neighbouring dims, so a warp's store covers 64 contiguous bytes of two
+    // heads.  A staged row holds one dim's 64 heads as 16 pieces of four, piece c at
+    // c ^ (d % 8), which keeps the 16-byte stores and loads free of bank conflicts.
     const uint32_t peer = (uint32_t)rank ^ 1u;
-    const uint32_t stage_in = smem_u32(kv_s);               // filled by the peer
-    const uint32_t stage_send = smem_u32(kv_s + kBufBytes);  // our rows for the peer
-    cluster_sync();  // both CTAs are past their main loops: the buffers are free
-    if (warp < 4) {
-      stage_ot(tmem + kColO, warp, lane, 2 * (int)peer, 2, stage_send, n > 0);
-      fence_proxy_async_smem();
-      asm volatile("bar.sync 1, 128;" ::: "memory");
-      if (tid == 0) {
-        const uint32_t inbar = smem_u32(&X.merge_full);
-        mbar_arrive_expect_tx(inbar, kBufBytes + 512);
-        const uint32_t pbar = dsmem_addr(inbar, peer);
-        bulk_copy_to_cluster(dsmem_addr(stage_in, peer), stage_send, kBufBytes, pbar);
-        // m_run, l_run -> the peer's peer_m, peer_l (512 contiguous bytes each side)
-        bulk_copy_to_cluster(dsmem_addr(smem_u32(X.peer_m), peer), smem_u32(X.m_run), 512, pbar);
+    constexpr uint32_t kTileBytes = 128 * 256;  // one staged tile: 128 dims x 64 heads fp32
+    if (tid == 0) {
+      mbar_arrive_expect_tx(smem_u32(&X.merge_full[0]), kTileBytes);
+      mbar_arrive_expect_tx(smem_u32(&X.merge_full[1]), kTileBytes);
+    }
+    const int sp = warp & 3, tl = (warp >> 2) & 1;
+    const int d = sp * 32 + lane;  // dim within the tile = TMEM lane
+    const uint32_t rowb = (uint32_t)(tl * 128 + d) * 256;  // this dim's staged row
+    if (warp < 8) {
+      const uint32_t trow =
+          tmem + ((uint32_t)(sp * 32) << 16) + kColO + 64 * (2 * (int)peer + tl);
+      const uint32_t stage = smem_u32(kv_s + kBufBytes) + rowb;
+#pragma unroll 1
+      for (int hb = 0; hb < 64; hb += 32) {
+        uint32_t v[32];
+        if (n > 0) {
+          tmem_ld32(trow + hb, v);
+          tmem_ld_wait();
+        } else {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) v[j] = 0u;
+        }
+#pragma unroll
+        for (int c4 = 0; c4 < 8; ++c4) {
+          const int c = (hb >> 2) + c4;
+          st_shared16(stage + ((c ^ (d & 7)) << 4),
+                      make_uint4(v[4 * c4], v[4 * c4 + 1], v[4 * c4 + 2], v[4 * c4 + 3]));
+        }
       }
-      stage_ot(tmem + kColO, warp, lane, 2 * rank, 2, smem_u32(q_s), n > 0);
-      if (!mbar_wait(smem_u32(&X.merge_full), 0)) X.abort = 1;
-      if (tid < 64) {
-        const float mo = X.m_run[tid], mp = X.peer_m[tid];
-        const float sk = a.sink ? a.sink[tid] * kLog2e : -INFINITY;
+      fence_proxy_async_smem();  // the staged rows are read by the bulk copies
+    } else if (warp == 16) {  // m_run[64], l_run[64]: 512 adjacent bytes -> peer_m, peer_l
+      const uint4 ml = reinterpret_cast<const uint4*>(&X.m_run[0])[lane];
+      st_cluster16(dsmem_addr(smem_u32(&X.peer_m[0]) + 16 * lane, peer), ml);
+    } else if (a.inv_freq && warp == 17) {
+      rope_table(a.inv_freq, p, lane, X.rope_c, X.rope_s);
+    }
+    cluster_sync();  // both main loops are done; the staged rows and (m, l) are visible
+    tc_fence_after();
+    if (tid == 0) {
+#pragma unroll 1
+      for (int t = 0; t < 2; ++t)
+        bulk_copy_to_cluster(dsmem_addr(smem_u32(q_s) + t * kTileBytes, peer),
+                             smem_u32(kv_s + kBufBytes) + t * kTileBytes, kTileBytes,
+                             dsmem_addr(smem_u32(&X.merge_full[t]), peer));
+    }
+    if (warp >= 8 && warp < 16) {
+      if (warp < 10) {  // merge weights of head tid - 256
+        const int h = tid - 256;
+        const float mo = X.m_run[h], mp = X.peer_m[h], sk = X.sink2[h];
         const float M = fmaxf(fmaxf(mo, mp), sk);
         const float wo = mo == -INFINITY ? 0.f : ex2(mo - M);
         const float wp = mp == -INFINITY ? 0.f : ex2(mp - M);
-        const float Z = wo * X.l_run[tid] + wp * X.peer_l[tid] + (a.sink ? ex2(sk - M) : 0.f);
+        const float Z =
+            wo * X.l_run[h] + wp * X.peer_l[h] + (sk == -INFINITY ? 0.f : ex2(sk - M));
         const float inv = Z > 0.f ? 1.f / Z : 0.f;
-        X.fac[0][tid] = wo * inv;
-        X.fac[1][tid] = wp * inv;
+        X.fac[0][h] = wo * inv;
+        X.fac[1][h] = wp * inv;
         if (a.lse && rank == 0)
-          a.lse[(int64_t)q * kHeads + tid] = (M + __log2f(Z)) * 0.6931471805599453f;
+          a.lse[(int64_t)q * kHeads + h] = (M + __log2f(Z)) * 0.6931471805599453f;
+      }
+      asm volatile("bar.sync 5, 256;" ::: "memory");  // warps 8..15: the weights are written
+      const uint32_t trow =
+          tmem + ((uint32_t)(sp * 32) << 16) + kColO + 64 * (2 * rank + tl);
+      const int gd = 256 * rank + 128 * tl + d;  // output dim; a warp's 32 dims share `rot`
+      const bool rot = a.inv_freq && gd >= kRopeDim0;
+      const float cs = rot ? X.rope_c[(gd - kRopeDim0) >> 1] : 1.f;
+      const float sn = rot ? X.rope_s[(gd - kRopeDim0) >> 1] : 0.f;
+      const float* pin = reinterpret_cast<const float*>(q_s + rowb);
+      uint16_t* oq = a.out + (int64_t)q * kHeads * kDLat;
+      if (!mbar_wait(smem_u32(&X.merge_full[tl]), 0)) X.abort = 1;
+#pragma unroll 1
+      for (int hb = 0; hb < 64; hb += 32) {
+        uint32_t v[32];
+        if (n > 0) {
+          tmem_ld32(trow + hb, v);
+          tmem_ld_wait();
+        } else {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) v[j] = 0u;
+        }
+        // merged values replace the own ones in v (as float bits)
+#pragma unroll
+        for (int c4 = 0; c4 < 8; ++c4) {
+          const int c = (hb >> 2) + c4;
+          const float4 y = *reinterpret_cast<const float4*>(pin + ((c ^ (d & 7)) << 2));
+          const float4 f0 = *reinterpret_cast<const float4*>(&X.fac[0][4 * c]);
+          const float4 f1 = *reinterpret_cast<const float4*>(&X.fac[1][4 * c]);
+          v[4 * c4 + 0] = __float_as_uint(__uint_as_float(v[4 * c4 + 0]) * f0.x + y.x * f1.x);
+          v[4 * c4 + 1] = __float_as_uint(__uint_as_float(v[4 * c4 + 1]) * f0.y + y.y * f1.y);
+          v[4 * c4 + 2] = __float_as_uint(__uint_as_float(v[4 * c4 + 2]) * f0.z + y.z * f1.z);
+          v[4 * c4 + 3] = __float_as_uint(__uint_as_float(v[4 * c4 + 3]) * f0.w + y.w * f1.w);
+        }
+        if (rot) {  // pair (2i, 2i + 1) times e^{-i p theta_i}: the partner is lane ^ 1
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const float x = __uint_as_float(v[j]);
+            const float pt = __shfl_xor_sync(0xFFFFFFFFu, x, 1);
+            v[j] = __float_as_uint((lane & 1) ? x * cs - pt * sn : x * cs + pt * sn);
+          }
+        }
+#pragma unroll
+        for (int j = 0; j < 32; j += 2) {
+          const int h = hb + j;
+          const float a0 = __uint_as_float(v[j]), a1 = __uint_as_float(v[j + 1]);
+          const float rcv = __shfl_xor_sync(0xFFFFFFFFu, (lane & 1) ? a0 : a1, 1);
+          if (lane & 1)
+            *reinterpret_cast<uint32_t*>(oq + (h + 1) * kDLat + gd - 1) = pack_bf16x2(rcv, a1);
+          else
+            *reinterpret_cast<uint32_t*>(oq + h * kDLat + gd) = pack_bf16x2(a0, rcv);
+        }
       }
     }
-    if (a.inv_freq && warp == 4) rope_table(a.inv_freq, p, lane, X.rope_c, X.rope_s);
-    __syncthreads();
-    out_pass(reinterpret_cast<const float*>(q_s), reinterpret_cast<const float*>(kv_s), X.fac[0],
-             X.fac[1], a.inv_freq ? X.rope_c : nullptr, X.rope_s,
-             a.out + (int64_t)q * kHeads * kDLat, 256, 256 * rank, tid, kThreads);
-    // both CTAs have received their rows, so no copy touches either one's shared memory
-    // any more when they exit
-    cluster_sync();
   } else {
     // partial O^T (unnormalised fp32) -> workspace [Q][nsplit][64 heads][512], plus the
     // running max (log2 units) and sum per head

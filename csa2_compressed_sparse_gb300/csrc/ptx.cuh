@@ -346,6 +346,15 @@ __device__ __forceinline__ void bulk_copy_to_cluster(uint32_t dst, uint32_t src,
       : "memory");
 }
 
+// 16-byte store into shared memory of a CTA of the cluster (dst: a 16-byte aligned
+// cluster address, dsmem_addr); it becomes visible to that CTA's threads through a
+// cluster barrier (cluster_sync).
+__device__ __forceinline__ void st_cluster16(uint32_t dst, uint4 v) {
+  asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(v.x),
+               "r"(v.y), "r"(v.z), "r"(v.w)
+               : "memory");
+}
+
 template <int N>
 __device__ __forceinline__ void cp_async_wait_group() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
