@@ -19,7 +19,8 @@ __all__ = [
     "Csa2Error", "Swa", "lib", "csa2_version", "csa2_last_error", "csa2_device_status",
     "csa2_compress",
     "csa2_compress_index",
-    "csa2_index_topk_workspace_size", "csa2_index_topk", "csa2_index_topk_noalloc",
+    "csa2_index_topk_workspace_size", "csa2_index_topk", "csa2_compress_index_topk",
+    "csa2_index_topk_noalloc",
     "csa2_index_topk_pool_workspace_size", "csa2_index_topk_pool", "csa2_topk_workspace_size",
     "csa2_index_plane_fp8_bytes", "csa2_index_plane_fp8", "csa2_index_topk_fp8_workspace_size",
     "csa2_index_topk_fp8", "csa2_index_plane_fp4_bytes", "csa2_index_plane_fp4",
@@ -61,6 +62,10 @@ _SIGS = {
     "csa2_index_topk_workspace_size": ([_i32, _i32, _i64, _i32], _sz),
     "csa2_index_topk": ([_vp, _vp, _i32, _i32, _vp, _i64, _vp, _vp, _vp, _i32, _vp, _i32, _i32,
                          _i32, _i64, _vp, _vp, _vp, _vp, _sz, _vp], _i32),
+    "csa2_compress_index_topk": ([_vp, _vp, _i32, _vp, _i32, _vp, _vp, _vp, _vp, _i64, _vp, _f32,
+                                  _vp, _vp, _vp, _i32, _i32, _vp, _i64, _vp, _vp, _vp, _i32,
+                                  _vp, _i32, _i32, _i32, _i64, _vp, _vp, _vp, _vp, _sz, _vp],
+                                 _i32),
     "csa2_index_topk_noalloc": ([_vp, _vp, _i32, _i32, _vp, _i64, _vp, _vp, _vp, _i32, _vp,
                                  _i32, _i32, _i32, _i64, _vp, _vp, _vp, _vp], _i32),
     "csa2_index_topk_pool_workspace_size": ([_i32, _i32, _i64, _i32, _i32], _sz),
@@ -200,6 +205,24 @@ def csa2_index_topk(iq, w, index_k, row_base, q_seq, q_pos, ratio, k, max_scored
                                  1 if relu else 0, max_scored, _p(sel), _p(sel_scores),
                                  _p(scores_out), _p(ws), ws.numel() * ws.element_size(),
                                  _stream(stream)))
+
+
+def csa2_compress_index_topk(kv, score, cu_seqlens, start_pos, kv_state, score_state, plane,
+                             inv_freq, iq, w, index_k, row_base, q_seq, q_pos, ratio, k,
+                             max_scored, sel, ws, sel_scores=None, cand=None, relu=True,
+                             scores_out=None, norm_w=None, eps=1e-6, stream=None):
+    """csa2_compress followed by csa2_index_topk in one call (the compressor's tokens run on
+    extra CTAs of the top-k launch)."""
+    T = kv.shape[0]
+    B = cu_seqlens.numel() - 1
+    Q, H = iq.shape[0], iq.shape[1]
+    ncb = 0 if cand is None else cand.shape[1]
+    _check(lib().csa2_compress_index_topk(
+        _p(kv), _p(score), T, _p(cu_seqlens), B, _p(start_pos), _p(kv_state), _p(score_state),
+        _p(plane), plane.shape[0], _p(norm_w), float(eps), _p(inv_freq), _p(iq), _p(w), Q, H,
+        _p(index_k), index_k.shape[0], _p(row_base), _p(q_seq), _p(q_pos), ratio, _p(cand), ncb,
+        k, 1 if relu else 0, max_scored, _p(sel), _p(sel_scores), _p(scores_out), _p(ws),
+        ws.numel() * ws.element_size(), _stream(stream)))
 
 
 def csa2_index_topk_noalloc(iq, w, index_k, row_base, q_seq, q_pos, ratio, k, max_scored, sel,

@@ -10,7 +10,7 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libcsa2.so")
 SOURCES = ["csa2_api.cu", "k_compress.cu", "k_index.cu", "k_topk.cu", "k_attn.cu", "noalloc.cu"]
-HEADERS = ["common.cuh", "ptx.cuh"]
+HEADERS = ["common.cuh", "ptx.cuh", "compress_dev.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
          "-Xptxas", "-v"] + ARCH

@@ -147,8 +147,10 @@ cudaError_t launch_plane_fp4(const uint16_t* rows, int64_t n, uint8_t* out, cuda
 // bf16 index rows [n][128] -> FP8 plane (ceil(n / 8) blocks of 1056 bytes).
 cudaError_t launch_plane_fp8(const uint16_t* k, int64_t n, uint8_t* plane, cudaStream_t s);
 // One launch for selection `a` and, when b != null, a second selection over the same
-// queries that runs beside it.
-cudaError_t launch_topk(const TopkArgs& a, cudaStream_t s, const TopkArgs* b = nullptr);
+// queries that runs beside it; when comp != null (comp->T > 0) further CTAs of the same
+// launch run the compressor's tokens (csa2_compress_index_topk).
+cudaError_t launch_topk(const TopkArgs& a, cudaStream_t s, const TopkArgs* b = nullptr,
+                        const CompressArgs* comp = nullptr);
 int attn_num_splits(int Q, int nsel, int num_sms);
 
 // 2-D tensor map over `rows` bf16 rows of `cols` elements (row stride cols * 2 bytes),

@@ -196,28 +196,48 @@ csa2_status csa2_selftest_wait_timeout(int64_t limit_ns, csa2_stream stream) {
   return CSA2_OK;
 }
 
+namespace {
+
+// Checks of the compressor's arguments (csa2_compress and the calls that include it);
+// fills *a (a->T == 0: nothing to compress).
+csa2_status compress_args(const char* name, const csa2_bf16* kv, const csa2_bf16* score, int T,
+                          const int32_t* cu_seqlens, int B, const int64_t* start_pos, int ratio,
+                          float* kv_state, float* score_state, csa2_bf16* plane,
+                          int64_t plane_rows, const int64_t* row_base, const float* norm_w,
+                          float eps, const float* inv_freq, csa2::CompressArgs* a) {
+  *a = csa2::CompressArgs{};
+  REQUIRE(ratio == 1 || ratio == 2, "%s: ratio must be 1 or 2 (got %d)", name, ratio);
+  REQUIRE(B >= 1 && B <= 8192, "%s: B must be in [1, 8192] (got %d)", name, B);
+  REQUIRE(T >= 0, "%s: T must be >= 0 (got %d)", name, T);
+  if (T == 0) return CSA2_OK;
+  REQUIRE(kv && cu_seqlens && start_pos && plane && row_base && inv_freq,
+          "%s: kv, cu_seqlens, start_pos, plane, row_base and inv_freq are required", name);
+  REQUIRE(ratio == 1 || (score && kv_state && score_state),
+          "%s: ratio 2 needs score, kv_state and score_state", name);
+  REQUIRE(aligned16(kv) && aligned16(plane) && (!score || aligned16(score)) &&
+              (!kv_state || aligned16(kv_state)) && (!score_state || aligned16(score_state)) &&
+              (!norm_w || aligned16(norm_w)),
+          "%s: kv, score, plane, states and norm_w must be 16-byte aligned", name);
+  REQUIRE(eps >= 0.f && std::isfinite(eps), "%s: eps must be finite and >= 0", name);
+  REQUIRE(plane_rows >= 0, "%s: plane_rows must be >= 0", name);
+  *a = csa2::CompressArgs{kv, score, T, cu_seqlens, B, start_pos, ratio, kv_state, score_state,
+                          plane, plane_rows, row_base, norm_w, eps, inv_freq,
+                          nullptr, nullptr, nullptr};
+  return CSA2_OK;
+}
+
+}  // namespace
+
 csa2_status csa2_compress(const csa2_bf16* kv, const csa2_bf16* score, int T,
                           const int32_t* cu_seqlens, int B, const int64_t* start_pos, int ratio,
                           float* kv_state, float* score_state, csa2_bf16* plane,
                           int64_t plane_rows, const int64_t* row_base, const float* norm_w,
                           float eps, const float* inv_freq, csa2_stream stream) {
-  REQUIRE(ratio == 1 || ratio == 2, "csa2_compress: ratio must be 1 or 2 (got %d)", ratio);
-  REQUIRE(B >= 1 && B <= 8192, "csa2_compress: B must be in [1, 8192] (got %d)", B);
-  REQUIRE(T >= 0, "csa2_compress: T must be >= 0 (got %d)", T);
-  if (T == 0) return CSA2_OK;
-  REQUIRE(kv && cu_seqlens && start_pos && plane && row_base && inv_freq,
-          "csa2_compress: kv, cu_seqlens, start_pos, plane, row_base and inv_freq are required");
-  REQUIRE(ratio == 1 || (score && kv_state && score_state),
-          "csa2_compress: ratio 2 needs score, kv_state and score_state");
-  REQUIRE(aligned16(kv) && aligned16(plane) && (!score || aligned16(score)) &&
-              (!kv_state || aligned16(kv_state)) && (!score_state || aligned16(score_state)) &&
-              (!norm_w || aligned16(norm_w)),
-          "csa2_compress: kv, score, plane, states and norm_w must be 16-byte aligned");
-  REQUIRE(eps >= 0.f && std::isfinite(eps), "csa2_compress: eps must be finite and >= 0");
-  REQUIRE(plane_rows >= 0, "csa2_compress: plane_rows must be >= 0");
-  csa2::CompressArgs a{kv, score, T, cu_seqlens, B, start_pos, ratio, kv_state, score_state,
-                       plane, plane_rows, row_base, norm_w, eps, inv_freq,
-                       nullptr, nullptr, nullptr};
+  csa2::CompressArgs a;
+  const csa2_status st = compress_args("csa2_compress", kv, score, T, cu_seqlens, B, start_pos,
+                                       ratio, kv_state, score_state, plane, plane_rows, row_base,
+                                       norm_w, eps, inv_freq, &a);
+  if (st != CSA2_OK || a.T == 0) return st;
   cudaError_t e = csa2::launch_compress(a, stream);
   if (e != cudaSuccess) return cuda_fail(e, "csa2_compress");
   return CSA2_OK;
@@ -233,25 +253,15 @@ csa2_status csa2_compress_index(const csa2_bf16* kv, const csa2_bf16* score, int
   REQUIRE(T <= 0 || (wk && index_plane), "csa2_compress_index: wk and index_plane are required");
   REQUIRE(!wk || (aligned16(wk) && aligned16(index_plane)),
           "csa2_compress_index: wk and index_plane must be 16-byte aligned");
-  // the plain compressor's checks first
-  REQUIRE(ratio == 1 || ratio == 2, "csa2_compress: ratio must be 1 or 2 (got %d)", ratio);
-  REQUIRE(B >= 1 && B <= 8192, "csa2_compress: B must be in [1, 8192] (got %d)", B);
-  REQUIRE(T >= 0, "csa2_compress: T must be >= 0 (got %d)", T);
-  if (T == 0) return CSA2_OK;
-  REQUIRE(kv && cu_seqlens && start_pos && plane && row_base && inv_freq,
-          "csa2_compress: kv, cu_seqlens, start_pos, plane, row_base and inv_freq are required");
-  REQUIRE(ratio == 1 || (score && kv_state && score_state),
-          "csa2_compress: ratio 2 needs score, kv_state and score_state");
-  REQUIRE(aligned16(kv) && aligned16(plane) && (!score || aligned16(score)) &&
-              (!kv_state || aligned16(kv_state)) && (!score_state || aligned16(score_state)) &&
-              (!norm_w || aligned16(norm_w)),
-          "csa2_compress: kv, score, plane, states and norm_w must be 16-byte aligned");
-  REQUIRE(eps >= 0.f && std::isfinite(eps), "csa2_compress: eps must be finite and >= 0");
-  REQUIRE(plane_rows >= 0, "csa2_compress: plane_rows must be >= 0");
-  csa2::CompressArgs a{kv, score, T, cu_seqlens, B, start_pos, ratio, kv_state, score_state,
-                       plane, plane_rows, row_base, norm_w, eps, inv_freq,
-                       reinterpret_cast<const uint16_t*>(wk), knorm_w,
-                       reinterpret_cast<uint16_t*>(index_plane)};
+  // the plain compressor's checks next
+  csa2::CompressArgs a;
+  const csa2_status st = compress_args("csa2_compress", kv, score, T, cu_seqlens, B, start_pos,
+                                       ratio, kv_state, score_state, plane, plane_rows, row_base,
+                                       norm_w, eps, inv_freq, &a);
+  if (st != CSA2_OK || a.T == 0) return st;
+  a.wk = reinterpret_cast<const uint16_t*>(wk);
+  a.knorm_w = knorm_w;
+  a.index_plane = reinterpret_cast<uint16_t*>(index_plane);
   cudaError_t e = csa2::launch_compress(a, stream);
   if (e != cudaSuccess) return cuda_fail(e, "csa2_compress_index");
   return CSA2_OK;
@@ -273,7 +283,7 @@ csa2_status index_topk_impl(const csa2_bf16* iq, const float* w, int Q, int H,
                             int ratio, const int32_t* cand, int ncb, int k, int relu,
                             int64_t max_scored, int32_t* sel, float* sel_scores,
                             float* scores_out, int nbk, int32_t* pool, void* ws, size_t ws_bytes,
-                            csa2_stream stream) {
+                            csa2_stream stream, const csa2::CompressArgs* comp = nullptr) {
   REQUIRE(Q >= 0, "csa2_index_topk: Q must be >= 0 (got %d)", Q);
   REQUIRE(H == 32 || H == 64, "csa2_index_topk: H must be 32 or 64 (got %d)", H);
   REQUIRE(ratio == 1 || ratio == 2, "csa2_index_topk: ratio must be 1 or 2 (got %d)", ratio);
@@ -288,7 +298,13 @@ csa2_status index_topk_impl(const csa2_bf16* iq, const float* w, int Q, int H,
   REQUIRE(max_scored <= csa2::topk_max_len(),
           "csa2_index_topk: max_scored %lld exceeds the supported %lld positions",
           (long long)max_scored, (long long)csa2::topk_max_len());
-  if (Q == 0) return CSA2_OK;
+  if (Q == 0) {  // nothing to score: the compressor's tokens (if any) run on their own
+    if (comp && comp->T > 0) {
+      cudaError_t e = csa2::launch_compress(*comp, stream);
+      if (e != cudaSuccess) return cuda_fail(e, "csa2_compress_index_topk (compress)");
+    }
+    return CSA2_OK;
+  }
   REQUIRE(iq && w && (plane_fmt ? plane != nullptr : index_k != nullptr) && row_base && q_seq &&
               q_pos && sel && ws,
           "csa2_index_topk: iq, w, the index plane, row_base, q_seq, q_pos, sel and ws are required");
@@ -345,7 +361,7 @@ csa2_status index_topk_impl(const csa2_bf16* iq, const float* w, int Q, int H,
     p.chunk = (int)((L.nb_max + p.nchunk - 1) / p.nchunk);
   }
   // the block selection's CTAs (the longer ones) first
-  e = nbk > 0 ? csa2::launch_topk(p, stream, &t) : csa2::launch_topk(t, stream);
+  e = nbk > 0 ? csa2::launch_topk(p, stream, &t, comp) : csa2::launch_topk(t, stream, nullptr, comp);
   if (e != cudaSuccess) return cuda_fail(e, "csa2_index_topk (top-k)");
   return CSA2_OK;
 }
@@ -361,6 +377,24 @@ csa2_status csa2_index_topk(const csa2_bf16* iq, const float* w, int Q, int H,
   return index_topk_impl(iq, w, Q, H, index_k, nullptr, 0, index_rows, row_base, q_seq, q_pos,
                          ratio, cand, ncb, k, relu, max_scored, sel, sel_scores, scores_out, 0,
                          nullptr, ws, ws_bytes, stream);
+}
+
+csa2_status csa2_compress_index_topk(
+    const csa2_bf16* kv, const csa2_bf16* score, int T, const int32_t* cu_seqlens, int B,
+    const int64_t* start_pos, float* kv_state, float* score_state, csa2_bf16* plane,
+    int64_t plane_rows, const float* norm_w, float eps, const float* inv_freq,
+    const csa2_bf16* iq, const float* w, int Q, int H, const csa2_bf16* index_k,
+    int64_t index_rows, const int64_t* row_base, const int32_t* q_seq, const int64_t* q_pos,
+    int ratio, const int32_t* cand, int ncb, int k, int relu, int64_t max_scored, int32_t* sel,
+    float* sel_scores, float* scores_out, void* ws, size_t ws_bytes, csa2_stream stream) {
+  csa2::CompressArgs c;
+  const csa2_status st = compress_args("csa2_compress_index_topk", kv, score, T, cu_seqlens, B,
+                                       start_pos, ratio, kv_state, score_state, plane,
+                                       plane_rows, row_base, norm_w, eps, inv_freq, &c);
+  if (st != CSA2_OK) return st;
+  return index_topk_impl(iq, w, Q, H, index_k, nullptr, 0, index_rows, row_base, q_seq, q_pos,
+                         ratio, cand, ncb, k, relu, max_scored, sel, sel_scores, scores_out, 0,
+                         nullptr, ws, ws_bytes, stream, c.T > 0 ? &c : nullptr);
 }
 
 size_t csa2_index_topk_pool_workspace_size(int Q, int H, int64_t max_scored, int k, int nbk) {

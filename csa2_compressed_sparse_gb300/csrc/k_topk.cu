@@ -33,6 +33,7 @@
 // way; the output holds block ids.  It runs in the same launch as the row selection, on
 // CTAs of its own.
 #include "common.cuh"
+#include "compress_dev.cuh"
 
 CSA2_DEFINE_FAULT_FLAG(topk)
 
@@ -514,13 +515,43 @@ __device__ __forceinline__ void topk_row(const TopkArgs& a, int c) {
   if (threadIdx.x == 0) a.count[q] = 0;  // ready for the next call
 }
 
+// The compressor's tokens on CTA `cta` of the compressor rows of a top-k launch
+// (csa2_compress_index_topk): warp w takes token cta * 32 + w, with the same per-token
+// work as the compressor kernel (compress_dev.cuh).  The compressor writes only the main
+// plane and its states, which no selection reads, so these CTAs run beside the selection
+// CTAs on SMs the selection leaves idle.  Kept out of line, apart from the selection's
+// code.
+__device__ __noinline__ void compress_cta(const CompressArgs& c, int64_t cta) {
+  extern __shared__ __align__(16) uint8_t smem_raw[];
+  uint64_t* turn_s = reinterpret_cast<uint64_t*>(smem_raw);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x < 32) turn_s[threadIdx.x] = rope_turn(c.inv_freq[threadIdx.x]);
+  __syncthreads();
+  const int64_t t = cta * kTopkWarps + warp;
+  if (t >= c.T) return;
+  float own_kv[2][8], own_sc[2][8];
+  cdev::load_own(c, t, lane, own_kv, own_sc);
+  const int b = cdev::warp_find_seq(c.cu_seqlens, c.B, t, lane);
+  cdev::token<false>(c, t, b, __ldg(c.cu_seqlens + b), __ldg(c.cu_seqlens + b + 1), own_kv,
+                     own_sc, lane, turn_s);
+}
+
 // One launch runs one or two independent selections over the same queries, e.g. the
 // top rows and the top candidate blocks of a FULL layer side by side: blockIdx.x below
-// a0.nchunk is a chunk of a0, the rest are chunks of a1.
+// a0.nchunk is a chunk of a0, the rest are chunks of a1 (blockIdx.y = query).  Rows
+// blockIdx.y >= Q (if any) run the compressor's tokens, just as many CTAs as they need.
 template <int kKind>
-__global__ void __launch_bounds__(kTopkThreads, 1) topk_kernel(TopkArgs a0, TopkArgs a1) {
+__global__ void __launch_bounds__(kTopkThreads, 1)
+    topk_kernel(TopkArgs a0, TopkArgs a1, CompressArgs comp) {
   griddep_launch_dependents();
   const int c = blockIdx.x;
+  if ((int)blockIdx.y >= a0.Q) {
+    const int64_t cta = (int64_t)(blockIdx.y - a0.Q) * gridDim.x + c;
+    if (cta * kTopkWarps >= comp.T) return;
+    griddep_wait();  // the previous step's readers of the plane and states are done
+    compress_cta(comp, cta);
+    return;
+  }
   if (c < a0.nchunk) topk_row<kKind>(a0, c);
   else topk_row<kKind>(a1, c - a0.nchunk);
 }
@@ -540,7 +571,8 @@ bool topk_fits(int64_t ld, int k) {
          (topk_num_chunks(ld) == 1 || (int64_t)topk_num_chunks(ld) * k <= kChunkLen);
 }
 
-cudaError_t launch_topk(const TopkArgs& a, cudaStream_t s, const TopkArgs* b) {
+cudaError_t launch_topk(const TopkArgs& a, cudaStream_t s, const TopkArgs* b,
+                        const CompressArgs* comp) {
   if (a.Q == 0) return cudaSuccess;
   if (b && (b->Q != a.Q || (b->scores != nullptr) != (a.scores != nullptr)))
     return cudaErrorInvalidValue;
@@ -550,7 +582,11 @@ cudaError_t launch_topk(const TopkArgs& a, cudaStream_t s, const TopkArgs* b) {
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   const int nx = a.nchunk + (b ? b->nchunk : 0);
-  return launch_pdl(kern, dim3(nx, a.Q), dim3(kTopkThreads), smem, s, a, b ? *b : a);
+  // compressor rows: 32 tokens (one per warp) per CTA, nx CTAs per row
+  const int64_t per_row = (int64_t)kTopkWarps * nx;
+  const int ncomp = comp && comp->T > 0 ? (int)((comp->T + per_row - 1) / per_row) : 0;
+  const CompressArgs c = ncomp ? *comp : CompressArgs{};
+  return launch_pdl(kern, dim3(nx, a.Q + ncomp), dim3(kTopkThreads), smem, s, a, b ? *b : a, c);
 }
 
 }  // namespace csa2

@@ -2,7 +2,8 @@
 
 A step is: compress the new tokens -> index + top-k (FULL or REINDEX) -> sparse
 attention for the scoring layer -> REUSE attention for the following layers of the
-index group (same selection, each layer with its own q and window).
+index group (same selection, each layer with its own q and window).  By default the
+first two parts are one call (csa2_compress_index_topk).
 """
 from dataclasses import dataclass, field
 from typing import List, Optional
@@ -10,8 +11,8 @@ from typing import List, Optional
 import torch
 
 from . import (Swa, SWA_LINEAR, SWA_RING, csa2_attn_workspace_size, csa2_compress,
-               csa2_index_topk, csa2_index_topk_workspace_size, csa2_reuse_attn,
-               csa2_sparse_attn)
+               csa2_compress_index_topk, csa2_index_topk, csa2_index_topk_workspace_size,
+               csa2_reuse_attn, csa2_sparse_attn)
 
 
 @dataclass
@@ -71,42 +72,56 @@ def topk_chunks(ld: int) -> int:
     return (ld + 32767) // 32768
 
 
-def kernel_launches(spec: StepSpec, t) -> int:
-    """Kernels one step launches (compress, index prep + scores, top-k, attention)."""
+def kernel_launches(spec: StepSpec, t, fused=True) -> int:
+    """Kernels one step launches: the index prep, the score kernel and the top-k (it
+    merges in its last CTA; fused, its launch also runs the compressor's tokens), a
+    separate compressor when not fused, and the attention layers."""
     from . import lib  # noqa: F401  (library must be loaded)
     n = 0
-    if t["kv"].shape[0]:
-        n += 1
     Q = t["iq"].shape[0]
+    if t["kv"].shape[0] and (not fused or Q == 0):
+        n += 1
     if Q:
-        n += 3  # prep, score and top-k kernels (the top-k merges in its last CTA)
+        n += 3
         split = csa2_attn_workspace_size(Q, spec.k) > 0
         n += len(t["q"]) * (2 if split else 1)
     return n
 
 
-def run_step(spec: StepSpec, t, buf: StepBuffers, stream=None, compress=True, side=None):
-    """One step on `stream` (default: the current stream).  The compressor writes only the
-    main plane, which the indexer does not read, so with a `side` stream the compressor
-    runs there, concurrently with index + top-k, and the attention waits for both."""
+def run_step(spec: StepSpec, t, buf: StepBuffers, stream=None, compress=True, side=None,
+             fused=True):
+    """One step on `stream` (default: the current stream).  With `fused` the compressor
+    runs inside the indexer's call (csa2_compress_index_topk: its tokens on extra CTAs of
+    the top-k launch), so the step is one chain of kernels on one stream.  Otherwise csa2_compress is a call of its own; it writes only
+    the main plane, which the indexer does not read, so with a `side` stream it runs there,
+    concurrently with index + top-k, and the attention waits for both."""
     main = stream if stream is not None else torch.cuda.current_stream()
-    fork = side is not None and compress and t["kv"].shape[0] > 0
-    if fork:
-        side.wait_stream(main)
-        with torch.cuda.stream(side):
+    comp = compress and t["kv"].shape[0] > 0
+    if fused and comp:
+        csa2_compress_index_topk(t["kv"], t["score"], t["cu_seqlens"], t["start_pos"],
+                                 t["kv_state"], t["score_state"], t["plane"], t["inv_freq"],
+                                 t["iq"], t["w"], t["index_k"], t["row_base"], t["q_seq"],
+                                 t["q_pos"], spec.ratio, spec.k, spec.max_scored, buf.sel, buf.ws,
+                                 sel_scores=buf.sel_scores, cand=t.get("cand"), relu=spec.relu,
+                                 scores_out=buf.scores_out, eps=spec.eps, stream=main)
+    else:
+        fork = side is not None and comp
+        if fork:
+            side.wait_stream(main)
+            with torch.cuda.stream(side):
+                csa2_compress(t["kv"], t["score"], t["cu_seqlens"], t["start_pos"], spec.ratio,
+                              t["kv_state"], t["score_state"], t["plane"], t["row_base"],
+                              t["inv_freq"], eps=spec.eps, stream=side)
+        elif comp:
             csa2_compress(t["kv"], t["score"], t["cu_seqlens"], t["start_pos"], spec.ratio,
                           t["kv_state"], t["score_state"], t["plane"], t["row_base"],
-                          t["inv_freq"], eps=spec.eps, stream=side)
-    elif compress and t["kv"].shape[0]:
-        csa2_compress(t["kv"], t["score"], t["cu_seqlens"], t["start_pos"], spec.ratio,
-                      t["kv_state"], t["score_state"], t["plane"], t["row_base"], t["inv_freq"],
-                      eps=spec.eps, stream=main)
-    csa2_index_topk(t["iq"], t["w"], t["index_k"], t["row_base"], t["q_seq"], t["q_pos"],
-                    spec.ratio, spec.k, spec.max_scored, buf.sel, buf.ws,
-                    sel_scores=buf.sel_scores, cand=t.get("cand"), relu=spec.relu,
-                    scores_out=buf.scores_out, stream=main)
-    if fork:
-        main.wait_stream(side)
+                          t["inv_freq"], eps=spec.eps, stream=main)
+        csa2_index_topk(t["iq"], t["w"], t["index_k"], t["row_base"], t["q_seq"], t["q_pos"],
+                        spec.ratio, spec.k, spec.max_scored, buf.sel, buf.ws,
+                        sel_scores=buf.sel_scores, cand=t.get("cand"), relu=spec.relu,
+                        scores_out=buf.scores_out, stream=main)
+        if fork:
+            main.wait_stream(side)
     for layer in range(len(t["q"])):
         fn = csa2_sparse_attn if layer == 0 else csa2_reuse_attn
         fn(t["q"][layer], t["q_seq"], t["q_pos"], swa_of(spec, t, layer), t["plane"],

@@ -176,6 +176,32 @@ csa2_status csa2_index_topk(const csa2_bf16* iq, const float* w, int Q, int H,
                             float* scores_out, void* ws, size_t ws_bytes, csa2_stream stream);
 
 /* ---------------------------------------------------------------------------------
+ * csa2_compress_index_topk -- csa2_compress and csa2_index_topk as one call: the first
+ * two parts of the step ([A] "特殊模块 · compressor" and "特殊模块 · indexer" Fig. 3b,
+ * as for the two calls).  The compressor writes only the main plane and its states,
+ * which the indexer does not read (the index plane is an input), so the library runs
+ * the compressor's tokens on extra CTAs of the top-k launch, beside the selection (on
+ * SMs it leaves idle), instead of as a kernel of its own; the step is then one chain of
+ * kernels on one stream.  The results are exactly those of
+ * csa2_compress followed by csa2_index_topk with the same arguments (bit for bit: the
+ * same per-token and per-row arithmetic), and a following csa2_sparse_attn on the
+ * same stream sees the compressed rows.
+ *   kv, score, T, cu_seqlens, B, start_pos, kv_state, score_state, plane, plane_rows,
+ *   norm_w, eps, inv_freq   as csa2_compress (ratio and row_base are shared with the
+ *                           indexer); T == 0 compresses nothing
+ *   the remaining arguments as csa2_index_topk (bf16 index plane)
+ * Errors: the compressor's argument checks first, then the indexer's; nothing is
+ * enqueued when either fails.  With Q == 0 only the compressor runs. */
+csa2_status csa2_compress_index_topk(
+    const csa2_bf16* kv, const csa2_bf16* score, int T, const int32_t* cu_seqlens, int B,
+    const int64_t* start_pos, float* kv_state, float* score_state, csa2_bf16* plane,
+    int64_t plane_rows, const float* norm_w, float eps, const float* inv_freq,
+    const csa2_bf16* iq, const float* w, int Q, int H, const csa2_bf16* index_k,
+    int64_t index_rows, const int64_t* row_base, const int32_t* q_seq, const int64_t* q_pos,
+    int ratio, const int32_t* cand, int ncb, int k, int relu, int64_t max_scored, int32_t* sel,
+    float* sel_scores, float* scores_out, void* ws, size_t ws_bytes, csa2_stream stream);
+
+/* ---------------------------------------------------------------------------------
  * csa2_index_topk_pool -- csa2_index_topk in FULL mode plus the candidate pool that a
  * FULL layer hands to the REINDEX layers after it.  [A] Fig. 3b (second stage of the
  * indexer: block maxima, newest block pinned to +inf, top-2048 blocks, ascending, -1

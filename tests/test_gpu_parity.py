@@ -249,23 +249,39 @@ def test_step_h32_and_no_relu():
             check_sel(buf.sel[q].cpu().numpy(), sel_ref, sc, rows, wl.k)
 
 
-def test_step_with_the_compressor_on_a_second_stream_is_identical():
-    """The compressor does not feed the indexer, so a step may run it on a second stream
-    next to index + top-k; the results are the same bits (a decode step is idempotent:
-    the tail state it writes is the one it reads)."""
+@pytest.mark.parametrize("make", [
+    lambda: W.decode_batch(B=12, lo=300, hi=9000, seed=29),            # in-CTA prep path
+    lambda: W.prefill_reuse(n_new=300, ctx=8192, layers=2, seed=31),   # 300 queries: prep kernel
+    lambda: W.reindex_decode(B=3, ctx=40000, ncb=96, seed=33),
+])
+def test_fused_compress_index_topk_equals_the_separate_calls(make):
+    """csa2_compress_index_topk (the compressor's tokens on a warp of the score kernel, one
+    stream) against csa2_compress on a second stream next to csa2_index_topk, from the same
+    starting plane and tail state: the plane, the states, the selection, the scores and the
+    attention output are the same bits."""
     from csa2_compressed_sparse_gb300 import csa2_device_status
-    from csa2_compressed_sparse_gb300.step import run_step
-    wl = W.decode_batch(B=12, lo=300, hi=9000, seed=29)
-    t, spec, buf = run_workload(wl)
-    ref = [buf.sel.clone(), buf.out[0].clone(), buf.lse[0].clone(), t["plane"].clone()]
-    side = torch.cuda.Stream()
-    for b in (buf.sel, buf.out[0], buf.lse[0]):
-        b.zero_()
-    run_step(spec, t, buf, side=side)
-    torch.cuda.synchronize()
-    csa2_device_status()
-    for a, b in zip(ref, [buf.sel, buf.out[0], buf.lse[0], t["plane"]]):
-        assert torch.equal(a, b)
+    from csa2_compressed_sparse_gb300.step import allocate, run_step
+    wl = make()
+    t = wl.materialize("cuda")
+    spec = spec_of(wl)
+    start = {k: t[k].clone() for k in ("plane", "kv_state", "score_state")}
+    runs = []
+    for fused in (True, False):
+        for k, v in start.items():
+            t[k].copy_(v)
+        buf = allocate(spec, t, want_scores=True, want_lse=True)
+        side = torch.cuda.Stream()
+        run_step(spec, t, buf, side=side, fused=fused)
+        torch.cuda.synchronize()
+        csa2_device_status()
+        runs.append([t["plane"].clone(), t["kv_state"].clone(), t["score_state"].clone(),
+                     buf.sel.clone(), buf.scores_out.clone(), buf.out[-1].clone(),
+                     buf.lse[-1].clone()])
+    assert not torch.equal(runs[0][0], start["plane"]) or wl.T == 0  # the step wrote rows
+    for x, y in zip(*runs):
+        assert torch.equal(x.view(torch.uint8) if x.dtype == torch.bfloat16 else x,
+                           y.view(torch.uint8) if y.dtype == torch.bfloat16 else y) or \
+            torch.equal(torch.nan_to_num(x.float(), nan=7.0), torch.nan_to_num(y.float(), nan=7.0))
 
 
 def test_attention_split_and_unsplit_agree_with_the_oracle():
