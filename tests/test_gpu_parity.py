@@ -250,13 +250,13 @@ def test_step_h32_and_no_relu():
 
 
 @pytest.mark.parametrize("make", [
-    lambda: W.decode_batch(B=12, lo=300, hi=9000, seed=29),            # in-CTA prep path
-    lambda: W.prefill_reuse(n_new=300, ctx=8192, layers=2, seed=31),   # 300 queries: prep kernel
-    lambda: W.reindex_decode(B=3, ctx=40000, ncb=96, seed=33),
+    lambda: W.decode_batch(B=12, lo=300, hi=9000, seed=29),            # one compressor CTA
+    lambda: W.prefill_reuse(n_new=300, ctx=8192, layers=2, seed=31),   # 300 tokens: 10 CTAs
+    lambda: W.reindex_decode(B=3, ctx=40000, ncb=96, seed=33),         # ratio 1
 ])
 def test_fused_compress_index_topk_equals_the_separate_calls(make):
-    """csa2_compress_index_topk (the compressor's tokens on a warp of the score kernel, one
-    stream) against csa2_compress on a second stream next to csa2_index_topk, from the same
+    """csa2_compress_index_topk (the compressor's tokens on extra CTAs of the top-k launch,
+    one stream) against csa2_compress on a second stream next to csa2_index_topk, from the same
     starting plane and tail state: the plane, the states, the selection, the scores and the
     attention output are the same bits."""
     from csa2_compressed_sparse_gb300 import csa2_device_status
