@@ -41,6 +41,8 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--cpu-queries", type=int, default=64)
+    ap.add_argument("--no-extra", action="store_true",
+                    help="skip the REINDEX / prefill / long figures of the default line")
     ap.add_argument("--stages", action="store_true",
                     help="time every entry point of the step (and the candidate-pool and "
                          "inverse-RoPE variants) on its own instead; prints one JSON line")
@@ -395,10 +397,114 @@ def run_ours(args):
     }
     if rank == 0 and not args.no_cpu:
         line["cpu_baseline"] = cpu_baseline(wl, args.cpu_queries)
+    if world == 1 and args.config == "decode" and not args.no_extra:
+        line["other_configs"] = other_configs()
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
+
+
+def bf16_peaks():
+    """Measured dense bf16 tensor peaks (burst, sustained) in TFLOP/s, else the fallback."""
+    try:
+        with open(PEAKS) as f:
+            d = json.load(f)
+        return float(d["bf16_tflops"]), float(d.get("bf16_tflops_sustained", d["bf16_tflops"])), \
+            "measured"
+    except Exception:
+        return 1900.0, 1700.0, "fallback"
+
+
+def index_flops(wl):
+    """Tensor FLOPs of the index scores: 2 * H * 128 per scored (row, query) pair, counting
+    only the visible rows (FULL) or the candidate rows (REINDEX) each query scores."""
+    nvis = np.array([(int(p) + 1) // wl.ratio for p in wl.q_pos], dtype=np.int64)
+    scored = np.full_like(nvis, wl.ncb * 8) if wl.reindex else nvis
+    return float(scored.sum()) * 2 * wl.H * 128
+
+
+def attn_flops(wl):
+    """Tensor FLOPs of one attention layer: S = Q K^T and O = P V over each query's window
+    (min(p + 1, 128) rows) and its selected rows, 64 heads x 512 dims."""
+    nvis = np.array([(int(p) + 1) // wl.ratio for p in wl.q_pos], dtype=np.int64)
+    scored = np.full_like(nvis, wl.ncb * 8) if wl.reindex else nvis
+    rows = np.minimum(scored, wl.k) + np.minimum(np.asarray(wl.q_pos) + 1, 128)
+    return float(rows.sum()) * 2 * 2 * 64 * 512
+
+
+def other_configs():
+    """The REINDEX, prefill and long configurations, each timed on this GPU: the device
+    time of csa2_compress_index_topk (the index stage), of each attention layer and of the
+    whole step (CUDA graphs of several calls, CUDA events), with the index stage's HBM
+    fraction (decode-shaped configurations) or tensor fractions (prefill)."""
+    import csa2_compressed_sparse_gb300 as csa2
+    from csa2_compressed_sparse_gb300.step import allocate, run_step, swa_of
+    peak_hbm, hbm_kind = hbm_peak()
+    tf_burst, tf_sus, tf_kind = bf16_peaks()
+    res = {}
+    for name, inner, reps in (("reindex", 10, 20), ("long", 4, 10), ("prefill", 1, 4)):
+        wl = make_workload(name, 0)
+        spec = spec_for(wl)
+        t = wl.materialize("cuda")
+        buf = allocate(spec, t)
+        run_step(spec, t, buf)
+        torch.cuda.synchronize()
+        csa2.csa2_device_status()
+        cand = t.get("cand")
+
+        def index_call():
+            csa2.csa2_compress_index_topk(
+                t["kv"], t["score"], t["cu_seqlens"], t["start_pos"], t["kv_state"],
+                t["score_state"], t["plane"], t["inv_freq"], t["iq"], t["w"], t["index_k"],
+                t["row_base"], t["q_seq"], t["q_pos"], spec.ratio, spec.k, spec.max_scored,
+                buf.sel, buf.ws, sel_scores=buf.sel_scores, cand=cand, relu=spec.relu,
+                eps=spec.eps)
+
+        def attn_call(layer):
+            fn = csa2.csa2_sparse_attn if layer == 0 else csa2.csa2_reuse_attn
+            return lambda: fn(t["q"][layer], t["q_seq"], t["q_pos"], swa_of(spec, t, layer),
+                              t["plane"], t["row_base"], buf.sel, t["sink"], buf.out[layer],
+                              scale=spec.scale, ws=buf.attn_ws)
+
+        idx_us = graph_time_us(index_call, inner, reps)
+        att_us = [graph_time_us(attn_call(layer), inner, reps) for layer in range(wl.layers)]
+        step_us = graph_time_us(lambda: run_step(spec, t, buf), inner, reps)
+        csa2.csa2_device_status()
+        total, index_b, attn_b = algorithmic_bytes(wl)
+        index_b += total - index_b - attn_b * wl.layers  # the compressor's bytes
+        r = {"workload": wl.name, "description": wl.description, "queries": wl.Q,
+             "attention_layers": wl.layers,
+             "stages_us": {"compress_index_topk": round(idx_us, 2),
+                           "attention_per_layer": [round(x, 2) for x in att_us],
+                           "step": round(step_us, 2)},
+             "queries_per_s": wl.Q / (step_us * 1e-6)}
+        if name == "prefill":
+            fi, fa = index_flops(wl), attn_flops(wl)
+            att_mean = sum(att_us) / len(att_us)
+            r["index_tflops"] = fi / (idx_us * 1e-6) / 1e12
+            r["attn_tflops"] = fa / (att_mean * 1e-6) / 1e12
+            r["index_frac_of_bf16"] = {"burst": r["index_tflops"] / tf_burst,
+                                       "sustained": r["index_tflops"] / tf_sus}
+            r["attn_frac_of_bf16"] = {"burst": r["attn_tflops"] / tf_burst,
+                                      "sustained": r["attn_tflops"] / tf_sus}
+            r["formula"] = ("tflops = tensor FLOPs / device time; index FLOPs = 2 H 128 per "
+                            "scored (row, query); attention FLOPs = 2 x 2 x 64 x 512 per "
+                            "(row, query), rows = window + selected; peaks: " + tf_kind +
+                            f" bf16 {tf_burst:.0f} (burst) / {tf_sus:.0f} (sustained) TFLOP/s")
+        else:
+            r["index_gbs"] = index_b / (idx_us * 1e-6) / 1e9
+            r["index_hbm_frac"] = r["index_gbs"] / peak_hbm
+            r["step_gbs"] = total / (step_us * 1e-6) / 1e9
+            r["step_hbm_frac"] = r["step_gbs"] / peak_hbm
+            r["formula"] = ("GB/s = algorithmic bytes / device time (index: 256 B per scored "
+                            "row + queries, weights, selection, candidate ids, compressor "
+                            "tokens; step: every stage's bytes); peak: " + hbm_kind +
+                            f" copy {peak_hbm:.0f} GB/s")
+        res[name] = r
+        del t, buf
+        torch.cuda.empty_cache()
+    return res
 
 
 def run_e2e(args, wl, spec, t, buf, world, ms_step):
@@ -594,6 +700,32 @@ def run_reference(args):
     }), flush=True)
 
 
+def graph_time_us(fn, inner=20, reps=20):
+    """Mean device time (us) of one fn() call: `inner` calls captured in one CUDA graph,
+    replayed `reps` times between CUDA events on the launching stream (3 untimed replays
+    first)."""
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        fn()
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for _ in range(inner):
+            fn()
+    for _ in range(3):
+        g.replay()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    stream = torch.cuda.current_stream()
+    e0.record(stream)
+    for _ in range(reps):
+        g.replay()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) * 1e3 / (inner * reps)
+
+
 def run_stages(args):
     """Mean device time of each entry point on the chosen workload: 20 calls captured in
     one CUDA graph, replayed `reps` times between CUDA events on the launching stream."""
@@ -609,27 +741,7 @@ def run_stages(args):
     torch.cuda.synchronize()
     csa2.csa2_device_status()
 
-    def timed(fn, inner=20, reps=20):
-        side = torch.cuda.Stream()
-        side.wait_stream(torch.cuda.current_stream())
-        with torch.cuda.stream(side):
-            fn()
-        torch.cuda.current_stream().wait_stream(side)
-        torch.cuda.synchronize()
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g):
-            for _ in range(inner):
-                fn()
-        for _ in range(3):
-            g.replay()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        stream = torch.cuda.current_stream()
-        e0.record(stream)
-        for _ in range(reps):
-            g.replay()
-        e1.record(stream)
-        torch.cuda.synchronize()
-        return e0.elapsed_time(e1) * 1e3 / (inner * reps)
+    timed = graph_time_us
 
     cand = t.get("cand")
     swa0 = swa_of(spec, t, 0)
