@@ -87,6 +87,7 @@ struct IndexArgs {
   const uint8_t* plane4;  // MXFP4 index plane (blocks of 8 rows, 544 bytes), or null
   uint8_t* q8;          // [Q*H][128] E4M3 codes of the quantised queries (workspace)
   float* qscale;        // [Q*H] their power-of-two scales (workspace)
+  int blk3d;            // bf16 REINDEX: kmap_blk copies a whole candidate block per box
 };
 
 struct TopkArgs {
@@ -108,6 +109,8 @@ struct TopkArgs {
                           //    pool): a block's key is the largest key of its positions
                           //    < n[q], the newest block ceil(n[q] / 8) - 1 is pinned to
                           //    ~0, and the output holds block ids
+  const int64_t* q_pos;   // or null: n[q] = min(ld, cand ? ncb * 8 : (q_pos[q] + 1) / ratio),
+  int ratio;              //    the index call's scored count, known before its prep ends
 };
 
 struct AttnArgs {

@@ -349,6 +349,8 @@ csa2_status index_topk_impl(const csa2_bf16* iq, const float* w, int Q, int H,
   t.part = reinterpret_cast<uint64_t*>(base + L.part); t.nchunk = L.nchunk;
   t.count = a.topk_count;
   t.chunk = csa2::topk_chunk_len(max_scored);
+  t.q_pos = q_pos;
+  t.ratio = ratio;
   // n_scored <= max_scored <= ldk: the chunking of max_scored covers every row
   csa2::TopkArgs p{};
   if (nbk > 0) {  // the candidate blocks, from the same keys, in the same launch

@@ -627,7 +627,9 @@ __global__ void __launch_bounds__(num_threads(kMode), 1)
           for (int db = 0; db < 2; ++db)
             tma_load_2d(smem_u32(dst + db * 16384), &kmap_tile, db * 64, y, fb, pol_k);
         } else {
-          // all 16 block ids first (one round trip), then the 32 copies
+          // all 16 block ids first (one round trip), then the copies: with the block map
+          // one 2 KiB box per block ([2 dim halves][8 rows][128 B], so block i sits at
+          // 2048 i), else two 1 KiB boxes per block, one in each dim half of the tile
           const int32_t* cb = a.cand + (int64_t)gi.q0 * a.ncb + tile * 16;
           int32_t blk[16];
 #pragma unroll
@@ -635,8 +637,13 @@ __global__ void __launch_bounds__(num_threads(kMode), 1)
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
             const int32_t y = (int32_t)(gi.rb + (blk[i] >= 0 ? (int64_t)blk[i] * 8 : 0));
-            for (int db = 0; db < 2; ++db)
-              tma_load_2d(smem_u32(dst + db * 16384 + i * 1024), &kmap_blk, db * 64, y, fb, pol_k);
+            if (a.blk3d) {
+              tma_load_3d(smem_u32(dst + i * 2048), &kmap_blk, 0, y, 0, fb, pol_k);
+            } else {
+              for (int db = 0; db < 2; ++db)
+                tma_load_2d(smem_u32(dst + db * 16384 + i * 1024), &kmap_blk, db * 64, y, fb,
+                            pol_k);
+            }
           }
         }
       }
@@ -687,11 +694,14 @@ __global__ void __launch_bounds__(num_threads(kMode), 1)
             umma_f8(d, ad, bd, idesc, kk != 0);
           }
         } else {
+          // tile rows in 8-row atoms: 1 KiB apart in each 16 KiB dim half, or (candidate
+          // blocks by the block map) the two halves of an atom side by side, atoms 2 KiB apart
+          const uint32_t half = a.blk3d ? 1024u : 16384u, sbo = a.blk3d ? 2048u : 1024u;
 #pragma unroll
           for (int db = 0; db < 2; ++db)
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk) {
-              const uint64_t ad = sdesc_sw128(a_base + db * 16384 + kk * 32, 16, 1024);
+              const uint64_t ad = sdesc_sw128(a_base + db * half + kk * 32, 16, sbo);
               const uint64_t bd = sdesc_sw128(b_base + db * 32768 + kk * 32, 16, 1024);
               umma_bf16(d, ad, bd, idesc, (db | kk) != 0);
             }
@@ -932,10 +942,22 @@ cudaError_t launch_index(const IndexArgs& args, int num_sms, cudaStream_t s) {
       return cudaErrorInvalidValue;
     kt = qm;
     kb = qm;
-  } else if (!encode_rows_bf16(&kt, a.index_k, (uint64_t)a.index_rows, kDIdx, 64, kTileRows) ||
-             !encode_rows_bf16(&kb, a.index_k, (uint64_t)a.index_rows, kDIdx, 64, 8) ||
-             !encode_rows_bf16(&qm, a.iq, (uint64_t)a.Q * a.H, kDIdx, 64, (uint32_t)a.H)) {
-    return cudaErrorInvalidValue;
+  } else {
+    if (!encode_rows_bf16(&kt, a.index_k, (uint64_t)a.index_rows, kDIdx, 64, kTileRows) ||
+        !encode_rows_bf16(&qm, a.iq, (uint64_t)a.Q * a.H, kDIdx, 64, (uint32_t)a.H))
+      return cudaErrorInvalidValue;
+    // candidate blocks: the plane viewed as [2 dim halves][rows][128 B], so that one box of
+    // 8 rows x both halves copies a whole block (2 KiB) as two 128-byte-swizzled atoms;
+    // where that view is refused, two boxes of 8 rows x 64 dims per block
+    a.blk3d = 0;
+    if (a.cand) {
+      const uint64_t dims[3] = {128, (uint64_t)a.index_rows, 2};
+      const uint64_t strides[2] = {(uint64_t)kDIdx * 2, 128};
+      const uint32_t box[3] = {128, 8, 2};
+      a.blk3d = encode_bytes(&kb, a.index_k, 3, dims, strides, box) ? 1 : 0;
+    }
+    if (!a.blk3d && !encode_rows_bf16(&kb, a.index_k, (uint64_t)a.index_rows, kDIdx, 64, 8))
+      return cudaErrorInvalidValue;
   }
   const size_t smem = index_smem_bytes(mode);
   auto kern = mode == kModeFp8 ? index_score_kernel<kModeFp8>

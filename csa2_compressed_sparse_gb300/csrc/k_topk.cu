@@ -158,28 +158,53 @@ struct RowSrc {
   }
 };
 
-// Exact top-k of src[0..n) (n <= kChunkLen): emit(o, i) is called once for each selected
-// index i, with o = its place in ascending order (0 .. keff - 1), by some thread of the
-// CTA.  Returns keff = min(k, #scored).  dense: every key of src[0..n) is nonzero.
-template <int kKind, typename Emit>
-__device__ int select_topk(const RowSrc<kKind>& src, int n, int k, bool dense, SelectSmem& S,
-                           Emit emit) {
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int nw = (n + 31) >> 5;
-  // ---- 1. clear ----
-  // thread (warp w, lane l) handles the 4-key groups w * 32 + l + u * kTopkThreads,
-  // u < kU (n <= kChunkLen)
-  constexpr int kU = kChunkLen / (4 * kTopkThreads);
+// The select's counters, histograms and position bitmaps (nw words) set to zero; the
+// caller makes them visible with a barrier.
+__device__ __forceinline__ void clear_select(SelectSmem& S, int nw) {
+  const int tid = threadIdx.x;
   clear_hist(S, 2048);
   for (int i = tid; i < 2048; i += kTopkThreads) S.hist_kept[i] = 0;
   if (tid == 0) { S.ncand = 0; S.nvalid = 0; }
   if (tid < kTopkWarps) S.wcnt[tid] = 0;
   for (int w = tid; w < nw; w += kTopkThreads) { S.selmap[w] = 0; S.eqmap[w] = 0; }
-  __syncthreads();
+}
+
+// Where the threshold's sample is read: the staged keys, or the row in global memory
+// (keys, or raw scores converted on load) while its staged copy lands.
+struct SampleSrc {
+  const uint32_t* s;
+  const uint32_t* gk;
+  const float* gs;
+  __device__ __forceinline__ uint32_t operator()(int i) const {
+    if (s) return s[i];
+    if (gs) return score_key(__ldcg(gs + i));
+    return __ldcg(gk + i);
+  }
+};
+
+// Exact top-k of src[0..n) (n <= kChunkLen): emit(o, i) is called once for each selected
+// index i, with o = its place in ascending order (0 .. keff - 1), by some thread of the
+// CTA.  Returns keff = min(k, #scored).  dense: every key of src[0..n) is nonzero.
+// The threshold's sample is read from ssrc (the same keys: the staged copy, or the row
+// in global memory while its copy lands); ready() is called by every thread, followed by
+// a barrier, before src is first read (it waits for the staged copy).
+template <typename Ready, typename Emit>
+__device__ int select_topk(const RowSrc<kSrcSmem>& src, const SampleSrc& ssrc, int n, int k,
+                           bool dense, SelectSmem& S, bool precleared, Ready ready, Emit emit) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int nw = (n + 31) >> 5;
+  // ---- 1. clear (done by the caller, before its dependency wait, when precleared) ----
+  // thread (warp w, lane l) handles the 4-key groups w * 32 + l + u * kTopkThreads,
+  // u < kU (n <= kChunkLen)
+  constexpr int kU = kChunkLen / (4 * kTopkThreads);
+  if (!precleared) {
+    clear_select(S, nw);
+    __syncthreads();
+  }
   // ---- 2. threshold from an even sample of 2048 keys ----
   const int ns = n < kSample ? n : kSample;
   for (int s2 = tid; s2 < ns; s2 += kTopkThreads) {
-    const uint32_t key = src((int)(((int64_t)(2 * s2 + 1) * n) / (2 * ns)));
+    const uint32_t key = ssrc((int)(((int64_t)(2 * s2 + 1) * n) / (2 * ns)));
     if (key) atomicAdd(&S.hist[key >> 21], 1u);
   }
   __syncthreads();
@@ -198,7 +223,7 @@ __device__ int select_topk(const RowSrc<kKind>& src, int n, int k, bool dense, S
       clear_hist(S, 2048);
       __syncthreads();
       for (int s2 = tid; s2 < ns; s2 += kTopkThreads) {
-        const uint32_t key = src((int)(((int64_t)(2 * s2 + 1) * n) / (2 * ns)));
+        const uint32_t key = ssrc((int)(((int64_t)(2 * s2 + 1) * n) / (2 * ns)));
         if (key && (key >> 21) == bin) atomicAdd(&S.hist[(key >> 10) & 2047u], 1u);
       }
       __syncthreads();
@@ -206,35 +231,57 @@ __device__ int select_topk(const RowSrc<kKind>& src, int n, int k, bool dense, S
       thr = max((bin << 21) | ((uint32_t)S.found_bin << 10), 1u);
     }
   }
+  ready();          // the staged copy of the segment has landed
+  __syncthreads();  // ... for every thread; and every thread has read the sample's histogram
   // ---- 3. filter: keep keys >= thr, count scored positions ----
-  // A lane tests its four keys at once (their maximum); only the lanes holding a kept
-  // key take a run of slots in the warp's region [w * kWarpCap, ...) with one shared
-  // atomic and add their keys' top bits to the histogram.  A dense segment (every
-  // position scored) needs no count.
+  // Warp w's lanes take the 4-key groups w * 32 + lane + u * kTopkThreads.  First pass:
+  // each lane counts its kept keys (and which of its groups hold one); one warp-wide
+  // exclusive sum gives each lane its first slot in the warp's region [w * kWarpCap, ...),
+  // so no atomic is needed for the slots; the second pass re-reads only the groups that
+  // hold kept keys, stores them and adds their top bits to the histogram of the kept
+  // pairs (first radix pass).  A dense segment (every position scored) needs no count.
+  // The sample's histogram is cleared here for the second radix pass.
+  clear_hist(S, 2048);
   int nval = 0;
   uint32_t* wkey = S.ckey + warp * kWarpCap;
   uint32_t* widx = S.cidx + warp * kWarpCap;
-#pragma unroll 2
+  const int nu = (n + 4 * kTopkThreads - 1) / (4 * kTopkThreads);  // <= kU, CTA-uniform
+  int mine = 0;
+  uint32_t hit = 0;  // bit u: group u holds a kept key (thr >= 1: never an unscored one)
+#pragma unroll
   for (int u = 0; u < kU; ++u) {
+    if (u < nu) {
+      const uint4 vv = src.load4(warp * 32 + u * kTopkThreads + lane, n);
+      if (!dense) nval += (vv.x != 0u) + (vv.y != 0u) + (vv.z != 0u) + (vv.w != 0u);
+      const int cnt = (vv.x >= thr) + (vv.y >= thr) + (vv.z >= thr) + (vv.w >= thr);
+      mine += cnt;
+      hit |= (cnt ? 1u : 0u) << u;
+    }
+  }
+  int incl = mine;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int t = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+    if (lane >= o) incl += t;
+  }
+  const int wpos = __shfl_sync(0xFFFFFFFFu, incl, 31);
+  int slot = incl - mine;
+  while (hit) {
+    const int u = __ffs(hit) - 1;
+    hit &= hit - 1u;
     const int g = warp * 32 + u * kTopkThreads + lane;
     const uint4 vv = src.load4(g, n);
-    if (!dense) nval += (vv.x != 0u) + (vv.y != 0u) + (vv.z != 0u) + (vv.w != 0u);
-    if (max(max(vv.x, vv.y), max(vv.z, vv.w)) >= thr) {  // thr >= 1: never an unscored key
-      const uint32_t kk[4] = {vv.x, vv.y, vv.z, vv.w};
-      const int cnt = (kk[0] >= thr) + (kk[1] >= thr) + (kk[2] >= thr) + (kk[3] >= thr);
-      int slot = atomicAdd(&S.wcnt[warp], cnt);
+    const uint32_t kk[4] = {vv.x, vv.y, vv.z, vv.w};
 #pragma unroll
-      for (int jj = 0; jj < 4; ++jj) {
-        if (kk[jj] >= thr) {
-          if (slot < kWarpCap) { wkey[slot] = kk[jj]; widx[slot] = (uint32_t)(4 * g + jj); }
-          ++slot;
-          atomicAdd(&S.hist_kept[kk[jj] >> 21], 1u);
-        }
+    for (int jj = 0; jj < 4; ++jj) {
+      if (kk[jj] >= thr) {
+        if (slot < kWarpCap) { wkey[slot] = kk[jj]; widx[slot] = (uint32_t)(4 * g + jj); }
+        ++slot;
+        atomicAdd(&S.hist_kept[kk[jj] >> 21], 1u);
       }
     }
   }
-  __syncwarp();
-  const int wc = S.wcnt[warp];
+  if (lane == 0) S.wcnt[warp] = wpos;
   if (!dense) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) nval += __shfl_xor_sync(0xFFFFFFFFu, nval, o);
@@ -242,7 +289,7 @@ __device__ int select_topk(const RowSrc<kKind>& src, int n, int k, bool dense, S
   } else if (tid == 0) {
     S.nvalid = n;
   }
-  if (lane == 0) atomicAdd(&S.ncand, wc > kWarpCap ? kCandCap + 1 : wc);  // full: no fast path
+  if (lane == 0) atomicAdd(&S.ncand, wpos > kWarpCap ? kCandCap + 1 : wpos);  // full: no fast path
   __syncthreads();
   const int keff = S.nvalid < k ? S.nvalid : k;
   if (keff <= 0) return 0;
@@ -266,32 +313,36 @@ __device__ int select_topk(const RowSrc<kKind>& src, int n, int k, bool dense, S
       }
     }
   };
-  // first pass (key bits 31..21): the filter counted the kept pairs already
-  if (!fast) {
-    clear_hist(S, 2048);
-    __syncthreads();
-    for_keys([&](uint32_t key, bool ok) { hist_add(S.hist, key >> 21, ok && key != 0u); });
+  // Pass 1 (key bits 31..21): the filter counted the kept pairs into hist_kept; over the
+  // whole segment it counts into hist (cleared by the filter) instead.  Pass 2 counts into
+  // the other histogram (clear: hist since the filter, hist_kept since the start), pass 3
+  // into pass 1's again, cleared while pass 2 runs (its crossing has been read:
+  // find_crossing ends with a barrier).  Passes 2 and 3 count only the few keys of the
+  // crossing bin, with plain atomics.
+  uint32_t* h1 = fast ? S.hist_kept : S.hist;
+  uint32_t* h2 = fast ? S.hist : S.hist_kept;
+  if (!fast) {  // the kept counts are of no use here: hist_kept is cleared for pass 2
+    for (int i = threadIdx.x; i < 2048; i += kTopkThreads) h2[i] = 0;
+    for_keys([&](uint32_t key, bool ok) { hist_add(h1, key >> 21, ok && key != 0u); });
     __syncthreads();
   }
-  find_crossing(S, fast ? S.hist_kept : S.hist, 2048, keff);
+  find_crossing(S, h1, 2048, keff);
   const uint32_t b1 = (uint32_t)S.found_bin;
   int above = S.found_above;
-  clear_hist(S, 2048);
-  __syncthreads();
+  uint32_t* h3 = h1;
+  for (int i = threadIdx.x; i < 1024; i += kTopkThreads) h3[i] = 0;
   for_keys([&](uint32_t key, bool ok) {
-    hist_add(S.hist, (key >> 10) & 2047u, ok && key != 0u && (key >> 21) == b1);
+    if (ok && key != 0u && (key >> 21) == b1) atomicAdd(&h2[(key >> 10) & 2047u], 1u);
   });
   __syncthreads();
-  find_crossing(S, S.hist, 2048, keff - above);
+  find_crossing(S, h2, 2048, keff - above);
   const uint32_t pre = (b1 << 11) | (uint32_t)S.found_bin;
   above += S.found_above;
-  clear_hist(S, 1024);
-  __syncthreads();
   for_keys([&](uint32_t key, bool ok) {
-    hist_add(S.hist, key & 1023u, ok && key != 0u && (key >> 10) == pre);
+    if (ok && key != 0u && (key >> 10) == pre) atomicAdd(&h3[key & 1023u], 1u);
   });
   __syncthreads();
-  find_crossing(S, S.hist, 1024, keff - above);
+  find_crossing(S, h3, 1024, keff - above);
   const uint32_t T = (pre << 10) | (uint32_t)S.found_bin;
   above += S.found_above;
   const int need_eq = keff - above;  // >= 1
@@ -380,15 +431,32 @@ __device__ __forceinline__ void topk_row(const TopkArgs& a, int c) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
   SelectSmem& S = *reinterpret_cast<SelectSmem*>(smem_raw);
   const int q = blockIdx.y;
-  griddep_wait();
-  int n = a.n[q];
+  if (!a.blocks && threadIdx.x == 0) {  // the staging copy's barrier (shared memory only)
+    mbar_init(smem_u32(&S.bar), 1);
+    mbar_fence_init();
+  }
+  // the select's state, for a segment of up to kChunkLen items (shared memory only, so
+  // before the wait; a barrier below makes it visible)
+  clear_select(S, kWords);
+  // positions of this row: from the query's position when the call gives it (a call
+  // input, read before the dependency wait), else from the count array
+  int n;
+  if (a.q_pos) {
+    const int64_t v = a.cand ? (int64_t)a.ncb * 8 : (a.q_pos[q] + 1) / a.ratio;
+    n = (int)(v < a.ld ? v : a.ld);
+    griddep_wait();
+  } else {
+    griddep_wait();
+    n = a.n[q];
+  }
   if (n > a.ld) { if (threadIdx.x == 0) raise_fault(kFaultBounds); n = (int)a.ld; }
   const int items = a.blocks ? (n + 7) >> 3 : n;  // positions, or blocks of 8 positions
   const int begin = c * a.chunk;
   const int len = max(0, min(a.chunk, items - begin));
   const int tid = threadIdx.x;
   uint32_t* rowbuf = S.row;
-  int pad = 0;
+  int pad = 0, head = 0, body = 0;
+  SampleSrc ssrc{nullptr, nullptr, nullptr};
   if (a.blocks) {
     // Block keys of this chunk straight from the row's position keys (8 keys = two
     // 16-byte loads per block; rows start 16-byte aligned): the largest key of the
@@ -427,20 +495,30 @@ __device__ __forceinline__ void topk_row(const TopkArgs& a, int c) {
     const uint32_t* g = kKind == kSrcScores
                             ? reinterpret_cast<const uint32_t*>(a.scores + rowoff)
                             : a.keys + rowoff;
-    int head = (int)(((16u - (uint32_t)(reinterpret_cast<uintptr_t>(g) & 15u)) & 15u) >> 2);
+    head = (int)(((16u - (uint32_t)(reinterpret_cast<uintptr_t>(g) & 15u)) & 15u) >> 2);
     head = min(head, len);
-    const int body = ((len - head) >> 2) << 2;
+    body = ((len - head) >> 2) << 2;
+    if (kKind == kSrcScores) ssrc.gs = a.scores + rowoff;
+    else ssrc.gk = g;
     pad = (4 - head) & 3;  // row[pad + head] is 16-byte aligned
     rowbuf = S.row + pad;
-    if (tid == 0) {
-      mbar_init(smem_u32(&S.bar), 1);
-      mbar_fence_init();
-    }
-    __syncthreads();
+    __syncthreads();  // the barrier's initialisation is visible
     if (tid == 0 && body > 0) {
       mbar_arrive_expect_tx(smem_u32(&S.bar), (uint32_t)body * 4u);
       bulk_copy_g2s(smem_u32(rowbuf + head), g + head, (uint32_t)body * 4u, smem_u32(&S.bar));
     }
+    // the copy (and the ragged ends, in ready()) are waited for inside the select, after
+    // the threshold's sample, which reads the row from global memory meanwhile
+  }
+  __syncthreads();
+  RowSrc<kSrcSmem> src{rowbuf, pad == 0};
+  if (a.blocks) ssrc.s = rowbuf;  // block keys exist only in shared memory
+  auto ready = [&]() {
+    if (a.blocks) return;
+    const int64_t rowoff = (int64_t)q * a.ld + begin;
+    const uint32_t* g = kKind == kSrcScores
+                            ? reinterpret_cast<const uint32_t*>(a.scores + rowoff)
+                            : a.keys + rowoff;
     if (tid < head) rowbuf[tid] = __ldcg(g + tid);
     if (head + body + tid < len) rowbuf[head + body + tid] = __ldcg(g + head + body + tid);
     if (body > 0) mbar_wait(smem_u32(&S.bar), 0);
@@ -449,16 +527,14 @@ __device__ __forceinline__ void topk_row(const TopkArgs& a, int c) {
       for (int i = tid; i < len; i += kTopkThreads)
         rowbuf[i] = score_key(__uint_as_float(rowbuf[i]));
     }
-  }
-  __syncthreads();
-  RowSrc<kSrcSmem> src{rowbuf, pad == 0};
+  };
   // every position below n is scored unless the row maps candidate blocks (REINDEX);
   // every block below the row's count has a key
   const bool dense = a.blocks || a.cand == nullptr;
   int32_t* sel_q = a.sel + (int64_t)q * a.k;
   float* sc_q = a.sel_scores ? a.sel_scores + (int64_t)q * a.k : nullptr;
   if (a.nchunk == 1) {
-    const int keff = select_topk(src, len, a.k, dense, S, [&](int o, int i) {
+    const int keff = select_topk(src, ssrc, len, a.k, dense, S, true, ready, [&](int o, int i) {
       sel_q[o] = pos_to_row(a, q, (uint32_t)(begin + i));
       if (sc_q) sc_q[o] = key_score(src(i));
     });
@@ -467,7 +543,7 @@ __device__ __forceinline__ void topk_row(const TopkArgs& a, int c) {
   }
   // partial list of this chunk, then the last chunk CTA of the row merges
   uint64_t* part = a.part + ((int64_t)q * a.nchunk + c) * a.k;
-  const int keff = select_topk(src, len, a.k, dense, S, [&](int o, int i) {
+  const int keff = select_topk(src, ssrc, len, a.k, dense, S, true, ready, [&](int o, int i) {
     part[o] = ((uint64_t)src(i) << 32) | (uint32_t)(begin + i);
   });
   for (int i = keff + (int)threadIdx.x; i < a.k; i += kTopkThreads) part[i] = 0;
@@ -507,7 +583,8 @@ __device__ __forceinline__ void topk_row(const TopkArgs& a, int c) {
   }
   __syncthreads();
   RowSrc<kSrcSmem> msrc{mk, true};
-  const int keff2 = select_topk(msrc, ncand, a.k, false, S, [&](int o, int i) {
+  const SampleSrc mss{mk, nullptr, nullptr};
+  const int keff2 = select_topk(msrc, mss, ncand, a.k, false, S, false, [] {}, [&](int o, int i) {
     sel_q[o] = pos_to_row(a, q, (uint32_t)(__ldcg(row + i) & 0xFFFFFFFFu));
     if (sc_q) sc_q[o] = key_score(mk[i]);
   });
@@ -520,7 +597,8 @@ __device__ __forceinline__ void topk_row(const TopkArgs& a, int c) {
 // work as the compressor kernel (compress_dev.cuh).  The compressor writes only the main
 // plane and its states, which no selection reads, so these CTAs run beside the selection
 // CTAs on SMs the selection leaves idle.  Kept out of line, apart from the selection's
-// code.
+// code.  The token's own channels and its sequence come from the call's inputs, so they
+// are read before the dependency wait; the states and the plane after it.
 __device__ __noinline__ void compress_cta(const CompressArgs& c, int64_t cta) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
   uint64_t* turn_s = reinterpret_cast<uint64_t*>(smem_raw);
@@ -528,12 +606,13 @@ __device__ __noinline__ void compress_cta(const CompressArgs& c, int64_t cta) {
   if (threadIdx.x < 32) turn_s[threadIdx.x] = rope_turn(c.inv_freq[threadIdx.x]);
   __syncthreads();
   const int64_t t = cta * kTopkWarps + warp;
-  if (t >= c.T) return;
+  if (t >= c.T) return;  // nothing to read or write
   float own_kv[2][8], own_sc[2][8];
   cdev::load_own(c, t, lane, own_kv, own_sc);
   const int b = cdev::warp_find_seq(c.cu_seqlens, c.B, t, lane);
-  cdev::token<false>(c, t, b, __ldg(c.cu_seqlens + b), __ldg(c.cu_seqlens + b + 1), own_kv,
-                     own_sc, lane, turn_s);
+  const int64_t t0 = __ldg(c.cu_seqlens + b), t1 = __ldg(c.cu_seqlens + b + 1);
+  griddep_wait();  // the previous step's readers of the plane and states are done
+  cdev::token<false>(c, t, b, t0, t1, own_kv, own_sc, lane, turn_s);
 }
 
 // One launch runs one or two independent selections over the same queries, e.g. the
@@ -548,8 +627,7 @@ __global__ void __launch_bounds__(kTopkThreads, 1)
   if ((int)blockIdx.y >= a0.Q) {
     const int64_t cta = (int64_t)(blockIdx.y - a0.Q) * gridDim.x + c;
     if (cta * kTopkWarps >= comp.T) return;
-    griddep_wait();  // the previous step's readers of the plane and states are done
-    compress_cta(comp, cta);
+    compress_cta(comp, cta);  // waits for the preceding kernel after reading its inputs
     return;
   }
   if (c < a0.nchunk) topk_row<kKind>(a0, c);
