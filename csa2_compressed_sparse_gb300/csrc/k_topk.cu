@@ -231,7 +231,14 @@ __device__ int select_topk(const RowSrc<kSrcSmem>& src, const SampleSrc& ssrc, i
       thr = max((bin << 21) | ((uint32_t)S.found_bin << 10), 1u);
     }
   }
-  ready();          // the staged copy of the segment has landed
+  ready();  // the staged copy of the segment has landed
+  // keys past n up to whole 4096-key steps of the filter read as unscored (0), so the
+  // filter's loads need no bounds (nu * 4096 <= kChunkLen: inside the staging buffer)
+  const int nu = (n + 4 * kTopkThreads - 1) / (4 * kTopkThreads);  // <= kU, CTA-uniform
+  {
+    uint32_t* rb = const_cast<uint32_t*>(static_cast<const uint32_t*>(src.base));
+    for (int i = n + tid; i < nu * 4 * kTopkThreads; i += kTopkThreads) rb[i] = 0u;
+  }
   __syncthreads();  // ... for every thread; and every thread has read the sample's histogram
   // ---- 3. filter: keep keys >= thr, count scored positions ----
   // Warp w's lanes take the 4-key groups w * 32 + lane + u * kTopkThreads.  First pass:
@@ -245,18 +252,32 @@ __device__ int select_topk(const RowSrc<kSrcSmem>& src, const SampleSrc& ssrc, i
   int nval = 0;
   uint32_t* wkey = S.ckey + warp * kWarpCap;
   uint32_t* widx = S.cidx + warp * kWarpCap;
-  const int nu = (n + 4 * kTopkThreads - 1) / (4 * kTopkThreads);  // <= kU, CTA-uniform
   int mine = 0;
   uint32_t hit = 0;  // bit u: group u holds a kept key (thr >= 1: never an unscored one)
+  const uint32_t gaddr = smem_u32(src.base) + 16u * (uint32_t)(warp * 32 + lane);
+  auto count = [&](const uint4& vv, int u) {
+    if (!dense) nval += (vv.x != 0u) + (vv.y != 0u) + (vv.z != 0u) + (vv.w != 0u);
+    const int cnt = (vv.x >= thr) + (vv.y >= thr) + (vv.z >= thr) + (vv.w >= thr);
+    mine += cnt;
+    hit |= (cnt ? 1u : 0u) << u;
+  };
+  if (src.aligned) {  // plain 16-byte shared loads, four in flight
 #pragma unroll
-  for (int u = 0; u < kU; ++u) {
-    if (u < nu) {
-      const uint4 vv = src.load4(warp * 32 + u * kTopkThreads + lane, n);
-      if (!dense) nval += (vv.x != 0u) + (vv.y != 0u) + (vv.z != 0u) + (vv.w != 0u);
-      const int cnt = (vv.x >= thr) + (vv.y >= thr) + (vv.z >= thr) + (vv.w >= thr);
-      mine += cnt;
-      hit |= (cnt ? 1u : 0u) << u;
+    for (int u0 = 0; u0 < kU; u0 += 4) {
+      if (u0 < nu) {
+        uint4 vv[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          vv[j] = u0 + j < nu ? ld_shared16(gaddr + 16u * kTopkThreads * (uint32_t)(u0 + j))
+                              : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) count(vv[j], u0 + j);
+      }
     }
+  } else {
+#pragma unroll
+    for (int u = 0; u < kU; ++u)
+      if (u < nu) count(src.load4(warp * 32 + u * kTopkThreads + lane, n), u);
   }
   int incl = mine;
 #pragma unroll

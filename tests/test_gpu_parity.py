@@ -142,6 +142,34 @@ def test_topk_scores_bit_exact(ld, k):
         assert np.array_equal(ss[q, m], exp)
 
 
+@pytest.mark.parametrize("ld", [16384, 40000])
+def test_topk_scores_far_above_the_threshold(ld):
+    """Rows whose best keys lie many octaves above the sampled threshold, so that the
+    k-th key falls in the kept keys' shared top bin (and the exact recount path runs): a
+    block of huge distinct scores, a block of +inf, and huge scores with ties among them."""
+    from csa2_compressed_sparse_gb300 import (csa2_device_status, csa2_topk_scores,
+                                              csa2_topk_workspace_size)
+    g = np.random.default_rng(ld)
+    Q, k = 3, 512
+    s = g.standard_normal((Q, ld)).astype(np.float32)
+    big = g.choice(ld, 700, replace=False)
+    s[0, big] = (1e30 * (1.0 + np.arange(700) * 2.0 ** -20)).astype(np.float32)
+    s[1, big[:600]] = np.inf
+    s[2, big] = (1e25 * (1.0 + (np.arange(700) % 50) * 2.0 ** -16)).astype(np.float32)
+    n = np.full(Q, ld, dtype=np.int32)
+    st, nt = torch.from_numpy(s).cuda(), torch.from_numpy(n).cuda()
+    sel = torch.empty((Q, k), dtype=torch.int32, device="cuda")
+    ss = torch.empty((Q, k), dtype=torch.float32, device="cuda")
+    ws = torch.empty(max(csa2_topk_workspace_size(Q, ld, k), 256), dtype=torch.uint8,
+                     device="cuda")
+    csa2_topk_scores(st, nt, k, sel, ss, ws)
+    csa2_device_status()
+    sel = sel.cpu().numpy()
+    for q in range(Q):
+        ref = oracle.topk(s[q].astype(np.float64), np.arange(ld), k)
+        assert np.array_equal(sel[q], ref), f"row {q}"
+
+
 # ---- compressor ---------------------------------------------------------------------------
 
 def _compress_case(ratio, lens_a, lens_b, seed=11):
