@@ -37,7 +37,9 @@ def parse():
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--config", default="decode",
-                    choices=["tiny", "decode", "reindex", "prefill", "long"])
+                    choices=["tiny", "decode", "reindex", "prefill", "long", "prefill_small",
+                             "reindex_small", "long_small"],
+                    help="workload; the *_small ones are reduced cases for profiler captures")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--cpu-queries", type=int, default=64)
@@ -90,6 +92,13 @@ def make_workload(name, rank):
         return W.reindex_decode(seed=2 + seed_off)
     if name == "prefill":
         return W.prefill_reuse(seed=3 + seed_off)
+    # reduced cases of the same shapes (inputs still larger than L2) for profiler captures
+    if name == "prefill_small":
+        return W.prefill_reuse(n_new=512, layers=1, seed=3 + seed_off)
+    if name == "reindex_small":
+        return W.reindex_decode(ctx=32768, seed=2 + seed_off)
+    if name == "long_small":
+        return W.long_decode(ctx=131072, seed=4 + seed_off)
     return W.long_decode(seed=4 + seed_off)
 
 

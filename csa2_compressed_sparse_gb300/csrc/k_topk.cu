@@ -6,14 +6,14 @@
 // position that was not scored.  One CTA selects from a row segment of up to 32768
 // positions:
 //   1. sample: the segment is staged in shared memory by one bulk copy (a TMA copy has
-//      the whole row in flight at once); a histogram of the top 11 key bits over an
-//      even sample of 2048 keys gives a threshold bin expected to hold about 2k + 64
-//      (refined by the next 11 bits when the sample crowds into that bin);
+//      the whole row in flight at once); meanwhile a histogram of the top 11 key bits
+//      over an even sample of 2048 keys, read from global memory, gives a threshold bin
+//      expected to hold about 2k + 64 (refined by the next 11 bits when the sample
+//      crowds into that bin);
 //   2. filter: one pass keeps the (key, position) pairs at or above the threshold (a
 //      few times k of them) and counts the scored positions;
 //   3. select: three histogram passes (key bits 31..21, 20..10, 9..0) over the kept
-//      pairs give the k-th largest key T and how many keys equal to T are needed (the
-//      histogram updates are aggregated per warp: most kept keys share a few bins);
+//      pairs give the k-th largest key T and how many keys equal to T are needed;
 //   4. output: winners are marked in a position bitmap (keys > T; the lowest
 //      positions among keys == T), which is scanned in order, so ties go to the lower
 //      position and the output is ascending.
@@ -203,13 +203,20 @@ __device__ int select_topk(const RowSrc<kSrcSmem>& src, const SampleSrc& ssrc, i
   }
   // ---- 2. threshold from an even sample of 2048 keys ----
   const int ns = n < kSample ? n : kSample;
+  // sample s2 reads key (2 s2 + 1) n / (2 ns): s2 itself when the segment is no longer
+  // than the sample, else a shift (2 ns = 4096; (2 s2 + 1) n < 2^32 for n <= kChunkLen)
+  static_assert(2 * kSample == 4096 && (uint64_t)(2 * kSample) * kChunkLen < (1ull << 32),
+                "sample index");
+  auto sample_at = [&](int s2) {
+    return ns == n ? s2 : (int)(((uint32_t)(2 * s2 + 1) * (uint32_t)n) >> 12);
+  };
   for (int s2 = tid; s2 < ns; s2 += kTopkThreads) {
-    const uint32_t key = ssrc((int)(((int64_t)(2 * s2 + 1) * n) / (2 * ns)));
+    const uint32_t key = ssrc(sample_at(s2));
     if (key) atomicAdd(&S.hist[key >> 21], 1u);
   }
   __syncthreads();
   // sample keys wanted above the threshold: about (2k + 64) / n of the sample
-  const int want = (int)(((int64_t)(2 * k + 64) * ns + n - 1) / (n > 0 ? n : 1));
+  const int want = (int)(((uint32_t)(2 * k + 64) * (uint32_t)ns + n - 1) / (uint32_t)(n > 0 ? n : 1));
   find_crossing(S, S.hist, 2048, want);
   uint32_t thr = want >= ns ? 1u : max((uint32_t)S.found_bin << 21, 1u);
   if (want < ns) {
@@ -223,7 +230,7 @@ __device__ int select_topk(const RowSrc<kSrcSmem>& src, const SampleSrc& ssrc, i
       clear_hist(S, 2048);
       __syncthreads();
       for (int s2 = tid; s2 < ns; s2 += kTopkThreads) {
-        const uint32_t key = ssrc((int)(((int64_t)(2 * s2 + 1) * n) / (2 * ns)));
+        const uint32_t key = ssrc(sample_at(s2));
         if (key && (key >> 21) == bin) atomicAdd(&S.hist[(key >> 10) & 2047u], 1u);
       }
       __syncthreads();
@@ -245,9 +252,8 @@ __device__ int select_topk(const RowSrc<kSrcSmem>& src, const SampleSrc& ssrc, i
   // each lane counts its kept keys (and which of its groups hold one); one warp-wide
   // exclusive sum gives each lane its first slot in the warp's region [w * kWarpCap, ...),
   // so no atomic is needed for the slots; the second pass re-reads only the groups that
-  // hold kept keys, stores them and adds their top bits to the histogram of the kept
-  // pairs (first radix pass).  A dense segment (every position scored) needs no count.
-  // The sample's histogram is cleared here for the second radix pass.
+  // hold kept keys and stores them.  A dense segment (every position scored) needs no
+  // count.  The sample's histogram is cleared here for the radix passes.
   clear_hist(S, 2048);
   int nval = 0;
   uint32_t* wkey = S.ckey + warp * kWarpCap;
@@ -298,7 +304,6 @@ __device__ int select_topk(const RowSrc<kSrcSmem>& src, const SampleSrc& ssrc, i
       if (kk[jj] >= thr) {
         if (slot < kWarpCap) { wkey[slot] = kk[jj]; widx[slot] = (uint32_t)(4 * g + jj); }
         ++slot;
-        atomicAdd(&S.hist_kept[kk[jj] >> 21], 1u);
       }
     }
   }
@@ -334,19 +339,21 @@ __device__ int select_topk(const RowSrc<kSrcSmem>& src, const SampleSrc& ssrc, i
       }
     }
   };
-  // Pass 1 (key bits 31..21): the filter counted the kept pairs into hist_kept; over the
-  // whole segment it counts into hist (cleared by the filter) instead.  Pass 2 counts into
-  // the other histogram (clear: hist since the filter, hist_kept since the start), pass 3
-  // into pass 1's again, cleared while pass 2 runs (its crossing has been read:
-  // find_crossing ends with a barrier).  Passes 2 and 3 count only the few keys of the
-  // crossing bin, with plain atomics.
+  // Pass 1 (key bits 31..21) counts the kept pairs into hist_kept (clear since the start),
+  // or the whole segment's keys into hist (cleared by the filter).  Pass 2 counts into the
+  // other histogram, pass 3 into pass 1's again, cleared while pass 2 runs (its crossing
+  // has been read: find_crossing ends with a barrier).  Passes 1 and 2 over the kept pairs
+  // and pass 3 count with plain atomics (few keys per bin).
   uint32_t* h1 = fast ? S.hist_kept : S.hist;
   uint32_t* h2 = fast ? S.hist : S.hist_kept;
-  if (!fast) {  // the kept counts are of no use here: hist_kept is cleared for pass 2
-    for (int i = threadIdx.x; i < 2048; i += kTopkThreads) h2[i] = 0;
+  if (fast) {
+    for_keys([&](uint32_t key, bool ok) {
+      if (ok && key != 0u) atomicAdd(&h1[key >> 21], 1u);
+    });
+  } else {  // hist_kept (clear since the start) is pass 2's
     for_keys([&](uint32_t key, bool ok) { hist_add(h1, key >> 21, ok && key != 0u); });
-    __syncthreads();
   }
+  __syncthreads();
   find_crossing(S, h1, 2048, keff);
   const uint32_t b1 = (uint32_t)S.found_bin;
   int above = S.found_above;
@@ -463,7 +470,8 @@ __device__ __forceinline__ void topk_row(const TopkArgs& a, int c) {
   // input, read before the dependency wait), else from the count array
   int n;
   if (a.q_pos) {
-    const int64_t v = a.cand ? (int64_t)a.ncb * 8 : (a.q_pos[q] + 1) / a.ratio;
+    const int64_t p1 = a.q_pos[q] + 1;  // ratio 1 or 2
+    const int64_t v = a.cand ? (int64_t)a.ncb * 8 : (a.ratio == 2 ? p1 >> 1 : p1);
     n = (int)(v < a.ld ? v : a.ld);
     griddep_wait();
   } else {
