@@ -140,8 +140,8 @@ __global__ void __launch_bounds__(kPrepThreads) index_prep_kernel(IndexArgs a) {
   __shared__ long long redy[kPrepWarps];
   __shared__ int red_run[kPrepWarps];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  // The first block's loads read only the call's inputs (positions, sequence ids, row
-  // bases), so they are issued while the preceding kernel drains; nothing is written to
+  // The first block reads only the call's inputs (positions, sequence ids, row bases),
+  // so its loads and scans run while the preceding kernel drains; nothing is written to
   // the workspace before the wait (the preceding kernels may still read it).
   griddep_launch_dependents();
   int carry_run = 0, carry_groups = 0, prev_seq = -1;
@@ -166,14 +166,8 @@ __global__ void __launch_bounds__(kPrepThreads) index_prep_kernel(IndexArgs a) {
         }
       }
     }
-    if (base == 0) griddep_wait();
     const int q = base + tid;
     const bool in = q < a.Q;
-    if (in) {
-      a.n_scored[q] = (int32_t)s_ns[tid];
-      a.topk_count[q] = 0;
-      if (a.pool_count) a.pool_count[q] = 0;
-    }
     __syncthreads();
     // run start of q: inclusive max-scan of the positions where the sequence changes
     int v = -1;
@@ -212,6 +206,12 @@ __global__ void __launch_bounds__(kPrepThreads) index_prep_kernel(IndexArgs a) {
     int ex, tx;
     long long ey, ty;
     block_excl_sum2(lead ? 1 : 0, tiles, redx, redy, ex, ey, tx, ty);
+    if (base == 0) griddep_wait();  // the workspace writes of this call start here
+    if (in) {
+      a.n_scored[q] = (int32_t)s_ns[tid];
+      a.topk_count[q] = 0;
+      if (a.pool_count) a.pool_count[q] = 0;
+    }
     if (lead) {
       GroupRec r;
       r.q0 = q;
