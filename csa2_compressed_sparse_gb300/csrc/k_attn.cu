@@ -356,7 +356,8 @@ __device__ __forceinline__ void gather_chunk(const int32_t* rows, int fp8, bool 
 
 __global__ void __launch_bounds__(kThreads, 1)
     sparse_attn_kernel(AttnArgs a, const __grid_constant__ CUtensorMap qmap,
-                       const __grid_constant__ CUtensorMap wmap) {
+                       const __grid_constant__ CUtensorMap wmap,
+                       const __grid_constant__ CUtensorMap omap) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   // rounded up to 1024 bytes by pointer arithmetic, so that accesses stay shared-space
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -756,12 +757,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     // by its own merge barrier, and warps 8 and 9 form the merge weights of the 64 heads,
     //   M = max(m_own, m_peer, sink),  Z = 2^(sink - M) + sum 2^(m - M) l,
     //   o = (2^(m_own - M) O_own + 2^(m_peer - M) O_peer) / Z.
-    // Warps 8..11 merge their own first tile as soon as its peer rows land (while the
-    // second tile's copy is in flight), warps 12..15 the second: every thread takes one
-    // dim for all heads and writes it, one shuffle per pair of heads giving each lane a
-    // bf16 pair of neighbouring dims, so a warp's store covers 64 contiguous bytes of two
-    // heads.  A staged row holds one dim's 64 heads as 16 pieces of four, piece c at
-    // c ^ (d % 8), which keeps the 16-byte stores and loads free of bank conflicts.
+    // Warps 8..11 and 16..19 merge their own first tile as soon as its peer rows land
+    // (while the second tile's copy is in flight), warps 12..15 and 20..23 the second:
+    // every thread takes one dim and 32 heads, one shuffle per pair of heads giving each
+    // lane a bf16 pair of neighbouring dims, which go to a 128-byte-swizzled staging box
+    // in shared memory; each tile leaves by two tensor stores.  A staged fp32 row holds
+    // one dim's 64 heads as 16 pieces of four, piece c at c ^ (d % 8), which keeps the
+    // 16-byte stores and loads free of bank conflicts.
     const uint32_t peer = (uint32_t)rank ^ 1u;
     constexpr uint32_t kTileBytes = 128 * 256;  // one staged tile: 128 dims x 64 heads fp32
     if (tid == 0) {
@@ -808,7 +810,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                              smem_u32(kv_s + kBufBytes) + t * kTileBytes, kTileBytes,
                              dsmem_addr(smem_u32(&X.merge_full[t]), peer));
     }
-    if (warp >= 8 && warp < 16) {
+    if (warp >= 8) {
+      // merge warps: warp 8 + 4 t + i (t = tile) and 16 + 4 t + i take TMEM lanes 32 i..
+      // of their own tile t, for heads 0..31 and 32..63 respectively
       if (warp < 10) {  // merge weights of head tid - 256
         const int h = tid - 256;
         const float mo = X.m_run[h], mp = X.peer_m[h], sk = X.sink2[h];
@@ -823,7 +827,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (a.lse && rank == 0)
           a.lse[(int64_t)q * kHeads + h] = (M + __log2f(Z)) * 0.6931471805599453f;
       }
-      asm volatile("bar.sync 5, 256;" ::: "memory");  // warps 8..15: the weights are written
+      asm volatile("bar.sync 5, 512;" ::: "memory");  // warps 8..23: the weights are written
       const uint32_t trow =
           tmem + ((uint32_t)(sp * 32) << 16) + kColO + 64 * (2 * rank + tl);
       const int gd = 256 * rank + 128 * tl + d;  // output dim; a warp's 32 dims share `rot`
@@ -831,10 +835,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float cs = rot ? X.rope_c[(gd - kRopeDim0) >> 1] : 1.f;
       const float sn = rot ? X.rope_s[(gd - kRopeDim0) >> 1] : 0.f;
       const float* pin = reinterpret_cast<const float*>(q_s + rowb);
-      uint16_t* oq = a.out + (int64_t)q * kHeads * kDLat;
+      // bf16 output of this tile staged in the first KV buffer as two 128-byte-swizzled
+      // boxes of 64 heads x 64 dims (box sp / 2 holds this warp's dims), written out by
+      // two tensor stores
+      const int dd = (sp * 32 + lane) & 63;  // dim within the box
+      const uint32_t obox = smem_u32(kv_s) + (uint32_t)tl * 16384u + (uint32_t)(sp >> 1) * 8192u;
       if (!mbar_wait(smem_u32(&X.merge_full[tl]), 0)) X.abort = 1;
-#pragma unroll 1
-      for (int hb = 0; hb < 64; hb += 32) {
+      {
+        const int hb = warp >= 16 ? 32 : 0;
         uint32_t v[32];
         if (n > 0) {
           tmem_ld32(trow + hb, v);
@@ -868,11 +876,28 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int h = hb + j;
           const float a0 = __uint_as_float(v[j]), a1 = __uint_as_float(v[j + 1]);
           const float rcv = __shfl_xor_sync(0xFFFFFFFFu, (lane & 1) ? a0 : a1, 1);
-          if (lane & 1)
-            *reinterpret_cast<uint32_t*>(oq + (h + 1) * kDLat + gd - 1) = pack_bf16x2(rcv, a1);
-          else
-            *reinterpret_cast<uint32_t*>(oq + h * kDLat + gd) = pack_bf16x2(a0, rcv);
+          // the even lane writes head h at dims (d, d + 1), the odd one head h + 1 at
+          // (d - 1, d): row hr, 4 bytes at the pair's even dim de
+          const int hr = (lane & 1) ? h + 1 : h;
+          const int de = dd & ~1;
+          const uint32_t w = (lane & 1) ? pack_bf16x2(rcv, a1) : pack_bf16x2(a0, rcv);
+          asm volatile("st.shared.b32 [%0], %1;" ::"r"(obox + (uint32_t)hr * 128u +
+                                                          ((uint32_t)((de >> 3) ^ (hr & 7)) << 4) +
+                                                          (uint32_t)(de & 7) * 2u),
+                       "r"(w)
+                       : "memory");
         }
+      }
+      fence_proxy_async_smem();  // the staged boxes are read by the tensor stores
+      if (tl == 0) asm volatile("bar.sync 6, 256;" ::: "memory");  // warps 8..11, 16..19
+      else asm volatile("bar.sync 7, 256;" ::: "memory");          // warps 12..15, 20..23
+      if (warp < 16 && sp == 0 && lane == 0) {
+        const uint32_t tb = smem_u32(kv_s) + (uint32_t)tl * 16384u;
+        const int x0 = 256 * rank + 128 * tl;
+        tma_store_2d(&omap, x0, q * kHeads, tb);
+        tma_store_2d(&omap, x0 + 64, q * kHeads, tb + 8192u);
+        bulk_commit_group();
+        bulk_wait_group_read0();  // the CTA may exit once the boxes have been read
       }
     }
   } else {
@@ -984,9 +1009,11 @@ int attn_num_splits(int Q, int nsel, int num_sms) {
 cudaError_t launch_attn(const AttnArgs& a, int nsplit, cudaStream_t s) {
   if (a.Q == 0) return cudaSuccess;
   // Q of each query as eight boxes of 64 heads x 64 dims; a LINEAR bf16 window as boxes of
-  // 64 rows x 64 dims (the Q map stands in when there is none)
-  CUtensorMap qm, wm;
-  if (!encode_rows_bf16(&qm, a.q, (uint64_t)a.Q * kHeads, kDLat, 64, 64))
+  // 64 rows x 64 dims (the Q map stands in when there is none); the output likewise (the
+  // cluster merge writes it by tensor stores)
+  CUtensorMap qm, wm, om;
+  if (!encode_rows_bf16(&qm, a.q, (uint64_t)a.Q * kHeads, kDLat, 64, 64) ||
+      !encode_rows_bf16(&om, a.out, (uint64_t)a.Q * kHeads, kDLat, 64, 64))
     return cudaErrorInvalidValue;
   wm = qm;
   if (a.swa_mode == 1 && a.swa_dtype == 0 && a.swa_rows > 0 &&
@@ -1000,10 +1027,10 @@ cudaError_t launch_attn(const AttnArgs& a, int nsplit, cudaStream_t s) {
     AttnArgs b = a;
     b.cluster = 1;
     return launch_pdl_cluster(sparse_attn_kernel, dim3(2u, (unsigned)a.Q), dim3(kThreads), smem, s,
-                              2u, b, qm, wm);
+                              2u, b, qm, wm, om);
   }
   e = launch_pdl(sparse_attn_kernel, dim3((unsigned)nsplit, (unsigned)a.Q), dim3(kThreads), smem,
-                 s, a, qm, wm);
+                 s, a, qm, wm, om);
   if (e != cudaSuccess || nsplit == 1) return e;
   return launch_pdl(attn_combine_kernel, dim3((unsigned)a.Q, kHeads / 8), dim3(256), 0, s, a,
                     nsplit);
