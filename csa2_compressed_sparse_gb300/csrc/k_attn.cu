@@ -79,7 +79,6 @@ struct __align__(16) Aux {
   float sink2[64];   // sink logit per head in log2 units (-inf without a sink)
   int32_t rowidx[kMaxChunks][kChunk];  // source row per slot (chunk = rank + slot * nsplit)
   uint32_t rowmask[kMaxChunks][2];     // valid rows of each slot
-  int chunks[kMaxChunks];              // non-empty slots, in order
   uint64_t q_full;      // Q landed (TMA transaction count)
   uint64_t kv_full[2];  // KV buffer filled (one arrival of the team)
   uint64_t s_full[2];   // both S halves of the buffer written (two commits)
@@ -88,7 +87,6 @@ struct __align__(16) Aux {
   uint64_t fin[4];      // every MMA of an issuer complete (commit)
   uint64_t merge_full[2];  // cluster merge: the peer's rows of each tile landed
   uint32_t tmem_slot;
-  int nchunk;
   int abort;
 };
 
@@ -112,6 +110,43 @@ __device__ __forceinline__ bool group_any(bool pred) {
       : "r"((uint32_t)pred)
       : "memory");
   return r != 0;
+}
+
+// Source row of entry r of chunk c of query q (sequence b, position p, compressed rows
+// from rb): chunks 0 and 1 are window slots, chunk c >= 2 holds sel[64 (c - 2) + r]; -1
+// for none.  A row outside its buffer raises the bounds fault and gives -1.
+__device__ __forceinline__ int32_t chunk_row(const AttnArgs& a, int q, int b, int64_t p,
+                                             int64_t rb, int c, int r) {
+  int32_t idx32 = -1;
+  if (c < 2) {
+    const int64_t pos = p - (kRing - 1) + kChunk * c + r;
+    if (pos >= 0) {
+      int64_t idx;
+      bool ok = true;
+      if (a.swa_mode == 0) {
+        idx = (int64_t)b * kRing + (pos & (kRing - 1));
+      } else {
+        // a position before the sequence's first stored row would index the previous
+        // sequence's rows: a caller error, skipped and flagged
+        const int64_t p0 = a.lin_pos0[b];
+        ok = pos >= p0;
+        idx = a.lin_base[b] + (pos - p0);
+      }
+      if (ok && idx >= 0 && idx < a.swa_rows) idx32 = (int32_t)idx;
+      else raise_fault(kFaultBounds);
+    }
+  } else {
+    const int i = (c - 2) * kChunk + r;
+    if (i < a.nsel) {
+      const int32_t rr = a.sel[(int64_t)q * a.nsel + i];
+      if (rr >= 0) {
+        const int64_t idx = rb + rr;
+        if (idx >= 0 && idx < a.plane_rows) idx32 = (int32_t)idx;
+        else raise_fault(kFaultBounds);
+      }
+    }
+  }
+  return idx32;
 }
 
 // Valid-row bits of columns 8 g + 2 r4 and 8 g + 2 r4 + 1 of a chunk (bit 0, bit 1).
@@ -383,7 +418,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int r = 0; r < 4; ++r) mbar_init(smem_u32(&X.fin[r]), 1);
     for (int t = 0; t < 2; ++t) mbar_init(smem_u32(&X.merge_full[t]), 1);
-    X.nchunk = 0;
     X.abort = 0;
     mbar_fence_init();
   }
@@ -414,57 +448,24 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int64_t rb = a.row_base[b];
   auto row_source = [&](int e) {
     const int slot = e >> 6, r = e & 63;
-    const int c = rank + slot * nsplit;
-    int32_t idx32 = -1;
-    if (c < 2) {
-      const int64_t pos = p - (kRing - 1) + kChunk * c + r;
-      if (pos >= 0) {
-        int64_t idx;
-        bool ok = true;
-        if (a.swa_mode == 0) {
-          idx = (int64_t)b * kRing + (pos & (kRing - 1));
-        } else {
-          // a position before the sequence's first stored row would index the previous
-          // sequence's rows: a caller error, skipped and flagged
-          const int64_t p0 = a.lin_pos0[b];
-          ok = pos >= p0;
-          idx = a.lin_base[b] + (pos - p0);
-        }
-        if (ok && idx >= 0 && idx < a.swa_rows) idx32 = (int32_t)idx;
-        else raise_fault(kFaultBounds);
-      }
-    } else {
-      const int i = (c - 2) * kChunk + r;
-      if (i < a.nsel) {
-        const int32_t rr = a.sel[(int64_t)q * a.nsel + i];
-        if (rr >= 0) {
-          const int64_t idx = rb + rr;
-          if (idx >= 0 && idx < a.plane_rows) idx32 = (int32_t)idx;
-          else raise_fault(kFaultBounds);
-        }
-      }
-    }
+    const int32_t idx32 = chunk_row(a, q, b, p, rb, rank + slot * nsplit, r);
     X.rowidx[slot][r] = idx32;
     // the 32 lanes of a warp cover one half of a slot (768 threads = 24 warps)
     const uint32_t vm = __ballot_sync(0xFFFFFFFFu, idx32 >= 0);
     if (lane == 0) X.rowmask[slot][r >> 5] = vm;
   };
   for (int e = tid; e < nwin * kChunk; e += kThreads) row_source(e);
+  tc_fence_before();
   __syncthreads();
-  // The non-empty window slots are the CTA's first chunks, so gather team t (t = 0, 1)
-  // owns the t-th of them: it issues that gather now, before the wait.
+  tc_fence_after();
+  // Every slot of the CTA is a chunk (an empty one runs as a fully masked chunk), the
+  // window slots first; gather team t owns slots t, t + 2, ..  The window slots run before
+  // the wait: team t (t < nwin) lands window slot t now.
   const bool is_gather = warp >= kGatherWarp0 && warp < kMmaWarp;
   const int team = is_gather ? (warp - kGatherWarp0) / (kTeam / 32) : 0;
   const int t_in_team = tid - kGatherWarp0 * 32 - kTeam * team;
-  int pre_slot = -1;  // uniform within a team
-  {
-    int k = 0;
-    for (int slot = 0; slot < nwin; ++slot)
-      if (X.rowmask[slot][0] | X.rowmask[slot][1]) {
-        if (k == team) pre_slot = slot;
-        ++k;
-      }
-  }
+  const int n = nslot;
+  const uint32_t tmem = X.tmem_slot;
   auto issue_gather = [&](int slot) -> bool {  // true: a TMA box load (arrives by itself)
     const int c = rank + slot * nsplit;
     const uint32_t kvb = kv0 + team * kBufBytes;
@@ -489,39 +490,39 @@ __global__ void __launch_bounds__(kThreads, 1)
     cp_async_commit();
     return false;
   };
-  bool pre_tma = false;
-  if (is_gather && pre_slot >= 0) pre_tma = issue_gather(pre_slot);
-  griddep_wait();
-  {
-    for (int e = nwin * kChunk + tid; e < nslot * kChunk; e += kThreads) row_source(e);
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    if (tid == 0) {
-      int n = 0;
-      for (int slot = 0; slot < nslot; ++slot)
-        if (X.rowmask[slot][0] | X.rowmask[slot][1]) X.chunks[n++] = slot;
-      X.nchunk = n;
-    }
-    __syncthreads();
+  if (is_gather && team < nwin && !issue_gather(team)) {
+    cp_async_wait_group<0>();
+    fence_proxy_async_smem();
+    if (team == 0) asm volatile("bar.sync 2, 256;" ::: "memory");
+    else asm volatile("bar.sync 3, 256;" ::: "memory");
+    if (t_in_team == 0) mbar_arrive(smem_u32(&X.kv_full[team]));
   }
-  const int n = X.nchunk;
-  const uint32_t tmem = X.tmem_slot;
 
   if (is_gather) {
     // =================== gather: team 0 = warps 4..11; team 1 = warps 12..19 ===================
+    // Only the gathers read what the preceding kernels write (the selection, the
+    // compressed plane), so only they wait for them.  Each team then reads the row
+    // sources of its own selected slots (at most four, one entry per thread, the loads in
+    // flight together) and starts gathering.
     const int t = t_in_team;
     const uint32_t full_bar = smem_u32(&X.kv_full[team]);
+    griddep_wait();
+    {
+      int s0 = team;  // the team's first selected slot
+      while (s0 < nwin) s0 += 2;
+      const int slot = s0 + 2 * (t >> 6);
+      if (slot < nslot) row_source(slot * kChunk + (t & 63));  // uniform within a warp
+      if (team == 0) asm volatile("bar.sync 2, 256;" ::: "memory");
+      else asm volatile("bar.sync 3, 256;" ::: "memory");
+    }
     int last = -1;  // last chunk of this team (its kv_full phase ends every copy of the team)
     for (int it = team; it < n; it += 2) {
       last = it;
+      if (it < nwin) continue;  // a window slot: landed before the wait
       if (it >= 2 && !X.abort &&
           !mbar_wait(smem_u32(&X.pv_done[team]), (uint32_t)((it - 2) >> 1) & 1))
         X.abort = 1;
-      const int slot = X.chunks[it];
-      // the team's first chunk may have been issued before the wait (a window slot)
-      const bool tma = it == team && pre_slot >= 0 ? pre_tma : issue_gather(slot);
-      if (tma) continue;
+      if (issue_gather(it)) continue;
       cp_async_wait_group<0>();
       fence_proxy_async_smem();
       // every thread of the team has landed its rows
@@ -538,12 +539,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     // One thread issues a tcgen05.mma about every 28 ns however small it is, so the
     // chunk's 48 small MMAs are spread over four threads.
     const int role = warp - kMmaWarp;
-    if (lane == 0 && n > 0) {
+    if (lane == 0) {
       int issued = 0;
       if (role < 2) {
         const uint32_t id_s = idesc_bf16(64, 64, 0, 0);
         if (!mbar_wait(smem_u32(&X.q_full), 0)) X.abort = 1;
-        for (int c = 0; c < n && !X.abort; ++c) {
+        for (int c = 0; !X.abort && c < n; ++c) {
           // kv_full of chunk c also means that the softmax of chunk c - 2 is done with
           // S buffer c & 1 (the gather of chunk c waited for the PV of chunk c - 2)
           if (!mbar_wait(smem_u32(&X.kv_full[c & 1]), (uint32_t)(c >> 1) & 1)) {
@@ -567,7 +568,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       } else {
         const uint32_t id_o = idesc_bf16(128, 64, 1, 0);
-        for (int c = 0; c < n && !X.abort; ++c) {
+        for (int c = 0; !X.abort && c < n; ++c) {
           if (!mbar_wait(smem_u32(&X.p_full[c & 1]), (uint32_t)(c >> 1) & 1)) {
             X.abort = 1;
             break;
@@ -618,13 +619,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int it = 0; it < n; ++it) {
       const int bsel = it & 1;
       const uint32_t ph = (uint32_t)(it >> 1) & 1;
-      const int slot = X.chunks[it];
-      const uint32_t mlo = X.rowmask[slot][0], mhi = X.rowmask[slot][1];
-      const bool full = (mlo & mhi) == 0xFFFFFFFFu;
       const uint32_t sa = tmem + lrow + kColSa + 64 * bsel;
       const uint32_t sb = tmem + lrow + kColSb + 64 * bsel;
       if (!X.abort && !mbar_wait(smem_u32(&X.s_full[bsel]), ph)) X.abort = 1;
       tc_fence_after();
+      // the chunk's valid rows: written by its gather team before its rows landed (a
+      // selected slot's only after the dependency wait), so read after S
+      const uint32_t mlo = X.rowmask[it][0], mhi = X.rowmask[it][1];
+      const bool full = (mlo & mhi) == 0xFFFFFFFFu;
       // the P buffer was last read by the PV of chunk it - 2
       if (it >= 2 && !X.abort &&
           !mbar_wait(smem_u32(&X.pv_done[bsel]), (uint32_t)((it - 2) >> 1) & 1))

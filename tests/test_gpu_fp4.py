@@ -81,7 +81,10 @@ def test_attention_on_an_fp4_plane_matches_the_oracle(name):
     out = torch.empty((wl.Q, 64, 512), dtype=torch.bfloat16, device="cuda")
     ws = torch.empty(max(csa2_attn_workspace_size(wl.Q, 512), 256), dtype=torch.uint8,
                      device="cuda")
-    for rope in (False, True):
+    # few queries: through the workspace combine (up to ten CTAs per query), then without
+    # a workspace (two CTAs per query, merged in distributed shared memory)
+    runs = [(False, ws), (True, ws)] + ([(False, None), (True, None)] if wl.Q <= 76 else [])
+    for rope, ws in runs:
         invf = t["inv_freq"] if rope else None
         csa2_sparse_attn_fp4(t["q"][0], t["q_seq"], t["q_pos"], swa_of(spec, t, 0), p4, rows,
                              t["row_base"], torch.from_numpy(sel).cuda(), t["sink"], out,
@@ -123,3 +126,49 @@ def test_attention_on_an_e8m0_fp8_window_matches_the_oracle():
     got = out.float().cpu().numpy()
     for i in range(Q):
         check_attn(got[i], ref[i])
+
+
+def test_attention_without_a_sink_through_every_path():
+    """sink = NULL (no sink term): the running max starts at the first chunk's own
+    largest score.  Heads 0..15 carry queries scaled by 2^8, so their later chunks also
+    overtake the running max.  Two CTAs per query (the cluster merge: no workspace), the
+    workspace combine, and one CTA per query (the queries repeated to fill the GPU)."""
+    from csa2_compressed_sparse_gb300 import (SWA_RING, Swa, csa2_attn_workspace_size,
+                                              csa2_device_status, csa2_sparse_attn)
+    g = np.random.default_rng(91)
+    B, Q = 3, 6
+    ring = torch.from_numpy(g.standard_normal((B, 128, 512)).astype(np.float32)).bfloat16()
+    plane = torch.from_numpy(g.standard_normal((900, 512)).astype(np.float32)).bfloat16()
+    qf = g.standard_normal((Q, 64, 512))
+    qf[:, :16] *= 256.0
+    q = torch.from_numpy(qf.astype(np.float32)).bfloat16()
+    q_seq = np.array([0, 1, 2, 2, 0, 1], dtype=np.int32)
+    q_pos = np.array([700, 5, 1000, 999, 128, 64], dtype=np.int64)
+    row_base = np.array([0, 300, 600], dtype=np.int64)
+    sel = g.integers(0, 300, (Q, 512)).astype(np.int32)
+    sel[1, 100:] = -1
+    sel[5, :] = -1
+    ref, ref_lse = oracle.sparse_attn(q, q_seq, q_pos, ring, plane, row_base, sel, None)
+    dev = dict(q_seq=torch.from_numpy(q_seq).cuda(), q_pos=torch.from_numpy(q_pos).cuda(),
+               row_base=torch.from_numpy(row_base).cuda(), sel=torch.from_numpy(sel).cuda())
+    swa = Swa(ring.cuda(), SWA_RING)
+    ws = torch.empty(csa2_attn_workspace_size(Q, 512), dtype=torch.uint8, device="cuda")
+    for w in (None, ws):
+        out = torch.empty((Q, 64, 512), dtype=torch.bfloat16, device="cuda")
+        lse = torch.empty((Q, 64), dtype=torch.float32, device="cuda")
+        csa2_sparse_attn(q.cuda(), dev["q_seq"], dev["q_pos"], swa, plane.cuda(),
+                         dev["row_base"], dev["sel"], None, out, lse=lse, ws=w)
+        csa2_device_status()
+        got = out.float().cpu().numpy()
+        for i in range(Q):
+            check_attn(got[i], ref[i])
+            assert np.abs(lse[i].cpu().numpy() - ref_lse[i]).max() < 2e-2
+    idx = torch.arange(Q, device="cuda").repeat(14)
+    out = torch.empty((len(idx), 64, 512), dtype=torch.bfloat16, device="cuda")
+    csa2_sparse_attn(q.cuda()[idx].contiguous(), dev["q_seq"][idx].contiguous(),
+                     dev["q_pos"][idx].contiguous(), swa, plane.cuda(), dev["row_base"],
+                     dev["sel"][idx].contiguous(), None, out)
+    csa2_device_status()
+    got = out.float().cpu().numpy()
+    for i in range(len(idx)):
+        check_attn(got[i], ref[i % Q])
