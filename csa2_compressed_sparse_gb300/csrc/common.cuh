@@ -87,7 +87,6 @@ struct IndexArgs {
   const uint8_t* plane4;  // MXFP4 index plane (blocks of 8 rows, 544 bytes), or null
   uint8_t* q8;          // [Q*H][128] E4M3 codes of the quantised queries (workspace)
   float* qscale;        // [Q*H] their power-of-two scales (workspace)
-  int blk3d;            // bf16 REINDEX: kmap_blk copies a whole candidate block per box
 };
 
 struct TopkArgs {

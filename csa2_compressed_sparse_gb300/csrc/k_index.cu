@@ -33,9 +33,12 @@ constexpr int kTileRows = 128;
 constexpr int kModeBf16 = 0;  // bf16 rows
 constexpr int kModeFp8 = 1;   // blocks of 8 E4M3 rows with fp32 row scales
 constexpr int kModeFp4 = 2;   // blocks of 8 E2M1 rows with E8M0 scales per 32 dims
+constexpr int kModeGather = 3;  // bf16 rows of candidate blocks, gathered by eight warps
 constexpr int kFp4ConvWarps = 8;  // FP4: warps 10 .. 17 convert packed blocks to bf16
+constexpr int kGatherWarps = 8;   // gather mode: warps 10 .. 17 copy the candidate blocks
 __host__ __device__ constexpr int num_threads(int mode) {
-  return mode == kModeFp4 ? 320 + 32 * kFp4ConvWarps : 320;
+  return mode == kModeFp4 ? 320 + 32 * kFp4ConvWarps
+                          : (mode == kModeGather ? 320 + 32 * kGatherWarps : 320);
 }
 // MMA operand ring: bf16 tiles are 32 KiB (two 64-dim blocks of 128-byte rows), FP8 tiles
 // 16 KiB (one block).  bf16 and FP8 rings hold 128 KiB, filled by TMA.  FP4 tiles are
@@ -468,6 +471,10 @@ __device__ __noinline__ uint4 fp4_word_slow(uint32_t w, int e) {
 // row scale of K and the query scales multiply the head sum in the epilogue.
 // kModeFp4: the producer bulk-copies the tile's 16 packed blocks, warps 10..17 convert
 // them to a bf16 tile (exact) and the MMAs and epilogue are those of the bf16 mode.
+// kModeGather (REINDEX on the bf16 plane): the tile's 16 candidate blocks are 2 KiB each at
+// random places, which a TMA copy per block fetches at about 20 GB/s per SM; instead warps
+// 10..17 gather them by 16-byte asynchronous copies into the swizzled tile (each warp two
+// blocks, up to four tiles in flight), and the producer only loads the Q blocks.
 template <int kMode>
 __global__ void __launch_bounds__(num_threads(kMode), 1)
     index_score_kernel(IndexArgs a, const __grid_constant__ CUtensorMap kmap_tile,
@@ -478,6 +485,7 @@ __global__ void __launch_bounds__(num_threads(kMode), 1)
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   constexpr bool kFp8 = kMode == kModeFp8;
   constexpr bool kFp4 = kMode == kModeFp4;
+  constexpr bool kGat = kMode == kModeGather;
   // the ring the producer fills: operand tiles, or the FP4 mode's packed blocks
   constexpr int kStages = kFp4 ? kFp4StgStages : num_stages(kMode);
   constexpr int kStageBytes = kFp4 ? kFp4StgBytes : stage_bytes(kMode);
@@ -508,7 +516,7 @@ __global__ void __launch_bounds__(num_threads(kMode), 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(smem_u32(&bars->full[s]), 1);
+      mbar_init(smem_u32(&bars->full[s]), kGat ? 32 * kGatherWarps : 1);  // gather: its threads
       mbar_init(smem_u32(&bars->empty[s]), kFp4 ? kFp4ConvWarps : 1);  // FP4: the converters
     }
     for (int s = 0; s < kFp4CvStages; ++s) {
@@ -568,6 +576,7 @@ __global__ void __launch_bounds__(num_threads(kMode), 1)
           }
           ++u;
         }
+        if (kGat) continue;  // the gather warps fill the ring
         const int64_t k = it - it_lo;
         const int s = (int)(k % kStages);
         const uint32_t round = (uint32_t)(k / kStages);
@@ -622,29 +631,10 @@ __global__ void __launch_bounds__(num_threads(kMode), 1)
               tma_load_3d(smem_u32(dst + i * 1024), &kmap_blk, 0, 0,
                           (int32_t)(b0 + (blk[i] >= 0 ? blk[i] : 0)), fb, pol_k);
           }
-        } else if (!a.cand) {
+        } else {  // bf16 FULL (candidate blocks are gathered, kModeGather)
           const int32_t y = (int32_t)(gi.rb + tile * kTileRows);
           for (int db = 0; db < 2; ++db)
             tma_load_2d(smem_u32(dst + db * 16384), &kmap_tile, db * 64, y, fb, pol_k);
-        } else {
-          // all 16 block ids first (one round trip), then the copies: with the block map
-          // one 2 KiB box per block ([2 dim halves][8 rows][128 B], so block i sits at
-          // 2048 i), else two 1 KiB boxes per block, one in each dim half of the tile
-          const int32_t* cb = a.cand + (int64_t)gi.q0 * a.ncb + tile * 16;
-          int32_t blk[16];
-#pragma unroll
-          for (int i = 0; i < 16; ++i) blk[i] = tile * 16 + i < a.ncb ? __ldg(cb + i) : -1;
-#pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const int32_t y = (int32_t)(gi.rb + (blk[i] >= 0 ? (int64_t)blk[i] * 8 : 0));
-            if (a.blk3d) {
-              tma_load_3d(smem_u32(dst + i * 2048), &kmap_blk, 0, y, 0, fb, pol_k);
-            } else {
-              for (int db = 0; db < 2; ++db)
-                tma_load_2d(smem_u32(dst + db * 16384 + i * 1024), &kmap_blk, db * 64, y, fb,
-                            pol_k);
-            }
-          }
         }
       }
       // do not leave the CTA with copies still landing in shared memory
@@ -681,6 +671,7 @@ __global__ void __launch_bounds__(num_threads(kMode), 1)
         const uint32_t in_bar = kFp4 ? smem_u32(&bars->cv_full[ab]) : smem_u32(&bars->full[s]);
         if (!mbar_wait(in_bar, kFp4 ? (use & 1) : (round & 1))) { *abort_flag = 1; break; }
         if (!mbar_wait(smem_u32(&bars->acc_empty[ab]), (use & 1) ^ 1)) { *abort_flag = 1; break; }
+        if (kGat) fence_proxy_async_smem();  // the gathered tile was written by cp.async
         tc_fence_after();
         const uint32_t a_base = kFp4 ? smem_u32(a_smem + ab * kBf16Tile)
                                      : smem_u32(a_smem + s * kStageBytes);
@@ -694,9 +685,8 @@ __global__ void __launch_bounds__(num_threads(kMode), 1)
             umma_f8(d, ad, bd, idesc, kk != 0);
           }
         } else {
-          // tile rows in 8-row atoms: 1 KiB apart in each 16 KiB dim half, or (candidate
-          // blocks by the block map) the two halves of an atom side by side, atoms 2 KiB apart
-          const uint32_t half = a.blk3d ? 1024u : 16384u, sbo = a.blk3d ? 2048u : 1024u;
+          // tile rows in 8-row atoms, 1 KiB apart in each 16 KiB dim half
+          const uint32_t half = 16384u, sbo = 1024u;
 #pragma unroll
           for (int db = 0; db < 2; ++db)
 #pragma unroll
@@ -711,6 +701,62 @@ __global__ void __launch_bounds__(num_threads(kMode), 1)
         if (it + 1 == it_hi || it + 1 == gi.tile1) umma_commit(smem_u32(&bars->b_empty));
       }
     }
+  } else if (kGat && warp >= 10) {
+    // ============ candidate-block gathers: warps 10..17 ============
+    // Warp w copies blocks 2w and 2w + 1 of each tile: lane l, step j takes 16-byte piece
+    // 32 j + l of the pair (a block is 8 rows x 16 pieces; a step covers two rows of one
+    // block, 512 contiguous bytes) into row 8 (2w + j / 4) + r8 of the tile, dim half c / 8,
+    // swizzled as a TMA tile.  A missing block (-1), or rows past the plane's end (those of
+    // a partial newest block), are not copied: such rows are invalid in the epilogue and
+    // an MMA row depends only on its own tile row.  Every thread's part of a tile arrives
+    // on the tile's barrier when it lands (the MMA warp fences before reading it), so up to
+    // four tiles are in flight; the next tile's block ids are fetched meanwhile.
+    const int gw = warp - 10;
+    GroupInfo gi;
+    int g = g_first - 1;
+    gi.tile1 = -1;
+    const int64_t ntile = it_hi - it_lo;
+    int32_t nb0 = -1, nb1 = -1;
+    int64_t nrb = 0;
+    auto fetch_ids = [&](int64_t it) {  // block ids of this warp's pair in tile it
+      while (it >= gi.tile1) {
+        ++g;
+        load_group(a, g, gi);
+      }
+      const int64_t c0 = (it - gi.tile0) * 16 + 2 * gw;
+      const int32_t* cb = a.cand + (int64_t)gi.q0 * a.ncb;
+      nb0 = c0 < a.ncb ? __ldg(cb + c0) : -1;
+      nb1 = c0 + 1 < a.ncb ? __ldg(cb + c0 + 1) : -1;
+      nrb = gi.rb;
+    };
+    if (ntile > 0) fetch_ids(it_lo);
+    int64_t k = 0;
+    for (; k < ntile; ++k) {
+      if (__any_sync(0xFFFFFFFFu, *abort_flag != 0)) break;
+      const int s = (int)(k % kStages);
+      const uint32_t round = (uint32_t)(k / kStages);
+      if (!__all_sync(0xFFFFFFFFu, mbar_wait(smem_u32(&bars->empty[s]), (round & 1) ^ 1))) {
+        *abort_flag = 1;
+        break;
+      }
+      const int32_t b0 = nb0, b1 = nb1;
+      const int64_t rb = nrb;
+      const uint32_t stg = smem_u32(a_smem + s * kStageBytes);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int pc = j * 32 + lane;
+        const int32_t blk = j < 4 ? b0 : b1;
+        const int r8 = (pc & 127) >> 4, c = pc & 15;
+        const uint32_t row = (uint32_t)((2 * gw + (j >> 2)) * 8 + r8);
+        const int64_t grow = rb + (int64_t)blk * 8 + r8;
+        if (blk >= 0 && grow < a.index_rows)
+          cp_async16(stg + (uint32_t)(c >> 3) * 16384u + sw128_off(row, (uint32_t)(c & 7)),
+                     a.index_k + grow * kDIdx + c * 8);
+      }
+      cp_async_arrive_noinc(smem_u32(&bars->full[s]));
+      if (k + 1 < ntile) fetch_ids(it_lo + k + 1);
+    }
+    cp_async_wait_all();  // nothing may still be landing when the CTA exits
   } else if (kFp4 && warp >= 10) {
     // ============ FP4 converters: warps 10..17 ============
     // Warp c converts blocks c and c+8 of a tile; lane l takes row l / 4 of the
@@ -919,7 +965,8 @@ cudaError_t launch_index(const IndexArgs& args, int num_sms, cudaStream_t s) {
   cudaError_t e = launch_pdl(index_prep_kernel, dim3(1), dim3(kPrepThreads), 0, s, a);
   if (e != cudaSuccess) return e;
   CUtensorMap kt, kb, qm;
-  const int mode = a.plane8 ? kModeFp8 : (a.plane4 ? kModeFp4 : kModeBf16);
+  const int mode = a.plane8 ? kModeFp8
+                            : (a.plane4 ? kModeFp4 : (a.cand ? kModeGather : kModeBf16));
   if (mode == kModeFp8) {
     const int64_t qrows = (int64_t)a.Q * a.H;
     e = launch_pdl(quant_q_kernel, dim3((unsigned)((qrows + 7) / 8)), dim3(256), 0, s, a);
@@ -936,8 +983,9 @@ cudaError_t launch_index(const IndexArgs& args, int num_sms, cudaStream_t s) {
         !encode_bytes(&kb, a.plane8, 3, dims, strides, box_b) ||
         !encode_bytes(&qm, a.q8, 2, qd, qs, qbox))
       return cudaErrorInvalidValue;
-  } else if (mode == kModeFp4) {
-    // K blocks arrive by bulk copies: only the query map is used (passed three times)
+  } else if (mode == kModeFp4 || mode == kModeGather) {
+    // K blocks arrive by bulk copies or gathers: only the query map is used (passed three
+    // times)
     if (!encode_rows_bf16(&qm, a.iq, (uint64_t)a.Q * a.H, kDIdx, 64, (uint32_t)a.H))
       return cudaErrorInvalidValue;
     kt = qm;
@@ -946,23 +994,13 @@ cudaError_t launch_index(const IndexArgs& args, int num_sms, cudaStream_t s) {
     if (!encode_rows_bf16(&kt, a.index_k, (uint64_t)a.index_rows, kDIdx, 64, kTileRows) ||
         !encode_rows_bf16(&qm, a.iq, (uint64_t)a.Q * a.H, kDIdx, 64, (uint32_t)a.H))
       return cudaErrorInvalidValue;
-    // candidate blocks: the plane viewed as [2 dim halves][rows][128 B], so that one box of
-    // 8 rows x both halves copies a whole block (2 KiB) as two 128-byte-swizzled atoms;
-    // where that view is refused, two boxes of 8 rows x 64 dims per block
-    a.blk3d = 0;
-    if (a.cand) {
-      const uint64_t dims[3] = {128, (uint64_t)a.index_rows, 2};
-      const uint64_t strides[2] = {(uint64_t)kDIdx * 2, 128};
-      const uint32_t box[3] = {128, 8, 2};
-      a.blk3d = encode_bytes(&kb, a.index_k, 3, dims, strides, box) ? 1 : 0;
-    }
-    if (!a.blk3d && !encode_rows_bf16(&kb, a.index_k, (uint64_t)a.index_rows, kDIdx, 64, 8))
-      return cudaErrorInvalidValue;
+    kb = kt;  // FULL tiles only (candidate blocks are gathered)
   }
   const size_t smem = index_smem_bytes(mode);
-  auto kern = mode == kModeFp8 ? index_score_kernel<kModeFp8>
-                               : (mode == kModeFp4 ? index_score_kernel<kModeFp4>
-                                                   : index_score_kernel<kModeBf16>);
+  auto kern = mode == kModeFp8    ? index_score_kernel<kModeFp8>
+              : mode == kModeFp4  ? index_score_kernel<kModeFp4>
+              : mode == kModeGather ? index_score_kernel<kModeGather>
+                                    : index_score_kernel<kModeBf16>;
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   return launch_pdl(kern, dim3(a.nctas), dim3(num_threads(mode)), smem, s, a, kt, kb, qm);
