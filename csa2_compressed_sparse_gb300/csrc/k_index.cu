@@ -38,7 +38,8 @@ constexpr int kFp4ConvWarps = 8;  // FP4: warps 10 .. 17 convert packed blocks t
 constexpr int kGatherWarps = 8;   // gather mode: warps 10 .. 17 copy the candidate blocks
 __host__ __device__ constexpr int num_threads(int mode) {
   return mode == kModeFp4 ? 320 + 32 * kFp4ConvWarps
-                          : (mode == kModeGather ? 320 + 32 * kGatherWarps : 320);
+                          : (mode == kModeGather || mode == kModeFp8 ? 320 + 32 * kGatherWarps
+                                                                     : 320);
 }
 // MMA operand ring: bf16 tiles are 32 KiB (two 64-dim blocks of 128-byte rows), FP8 tiles
 // 16 KiB (one block).  bf16 and FP8 rings hold 128 KiB, filled by TMA.  FP4 tiles are
@@ -468,7 +469,10 @@ __device__ __noinline__ uint4 fp4_word_slow(uint32_t w, int e) {
 }
 
 // kModeFp8: K tiles and queries are E4M3 codes (tcgen05 kind::f8f6f4, K = 32 per MMA); the
-// row scale of K and the query scales multiply the head sum in the epilogue.
+// row scale of K and the query scales multiply the head sum in the epilogue.  FULL tiles
+// come by one TMA box over the block layout ([16 blocks][8 rows][128 B], the scales skipped
+// by the block stride); REINDEX tiles are gathered by warps 10..17 as in the gather mode
+// (one box per 1 KiB candidate block is as slow as the bf16 plane's).
 // kModeFp4: the producer bulk-copies the tile's 16 packed blocks, warps 10..17 convert
 // them to a bf16 tile (exact) and the MMAs and epilogue are those of the bf16 mode.
 // kModeGather (REINDEX on the bf16 plane): the tile's 16 candidate blocks are 2 KiB each at
@@ -486,6 +490,8 @@ __global__ void __launch_bounds__(num_threads(kMode), 1)
   constexpr bool kFp8 = kMode == kModeFp8;
   constexpr bool kFp4 = kMode == kModeFp4;
   constexpr bool kGat = kMode == kModeGather;
+  // warps 10..17 fill the operand ring (candidate blocks on the bf16 or FP8 plane)
+  const bool fill = kGat || (kFp8 && a.cand != nullptr);
   // the ring the producer fills: operand tiles, or the FP4 mode's packed blocks
   constexpr int kStages = kFp4 ? kFp4StgStages : num_stages(kMode);
   constexpr int kStageBytes = kFp4 ? kFp4StgBytes : stage_bytes(kMode);
@@ -516,7 +522,7 @@ __global__ void __launch_bounds__(num_threads(kMode), 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(smem_u32(&bars->full[s]), kGat ? 32 * kGatherWarps : 1);  // gather: its threads
+      mbar_init(smem_u32(&bars->full[s]), fill ? 32 * kGatherWarps : 1);  // gathers: their threads
       mbar_init(smem_u32(&bars->empty[s]), kFp4 ? kFp4ConvWarps : 1);  // FP4: the converters
     }
     for (int s = 0; s < kFp4CvStages; ++s) {
@@ -576,7 +582,7 @@ __global__ void __launch_bounds__(num_threads(kMode), 1)
           }
           ++u;
         }
-        if (kGat) continue;  // the gather warps fill the ring
+        if (fill) continue;  // the gather warps fill the ring
         const int64_t k = it - it_lo;
         const int s = (int)(k % kStages);
         const uint32_t round = (uint32_t)(k / kStages);
@@ -616,21 +622,9 @@ __global__ void __launch_bounds__(num_threads(kMode), 1)
             }
           }
         } else if (kFp8) {
-          // block (row_base + 128 * tile) / 8 .. + 15, as [16][8 rows][128 B]; REINDEX:
-          // one box per candidate block
-          const int64_t b0 = gi.rb >> 3;
-          if (!a.cand) {
-            tma_load_3d(smem_u32(dst), &kmap_tile, 0, 0, (int32_t)(b0 + tile * 16), fb, pol_k);
-          } else {
-            const int32_t* cb = a.cand + (int64_t)gi.q0 * a.ncb + tile * 16;
-            int32_t blk[16];
-#pragma unroll
-            for (int i = 0; i < 16; ++i) blk[i] = tile * 16 + i < a.ncb ? __ldg(cb + i) : -1;
-#pragma unroll
-            for (int i = 0; i < 16; ++i)
-              tma_load_3d(smem_u32(dst + i * 1024), &kmap_blk, 0, 0,
-                          (int32_t)(b0 + (blk[i] >= 0 ? blk[i] : 0)), fb, pol_k);
-          }
+          // FULL: blocks (row_base + 128 tile) / 8 .. + 15 as [16][8 rows][128 B]
+          tma_load_3d(smem_u32(dst), &kmap_tile, 0, 0, (int32_t)((gi.rb >> 3) + tile * 16), fb,
+                      pol_k);
         } else {  // bf16 FULL (candidate blocks are gathered, kModeGather)
           const int32_t y = (int32_t)(gi.rb + tile * kTileRows);
           for (int db = 0; db < 2; ++db)
@@ -671,7 +665,7 @@ __global__ void __launch_bounds__(num_threads(kMode), 1)
         const uint32_t in_bar = kFp4 ? smem_u32(&bars->cv_full[ab]) : smem_u32(&bars->full[s]);
         if (!mbar_wait(in_bar, kFp4 ? (use & 1) : (round & 1))) { *abort_flag = 1; break; }
         if (!mbar_wait(smem_u32(&bars->acc_empty[ab]), (use & 1) ^ 1)) { *abort_flag = 1; break; }
-        if (kGat) fence_proxy_async_smem();  // the gathered tile was written by cp.async
+        if (fill) fence_proxy_async_smem();  // the gathered tile was written by cp.async
         tc_fence_after();
         const uint32_t a_base = kFp4 ? smem_u32(a_smem + ab * kBf16Tile)
                                      : smem_u32(a_smem + s * kStageBytes);
@@ -701,16 +695,19 @@ __global__ void __launch_bounds__(num_threads(kMode), 1)
         if (it + 1 == it_hi || it + 1 == gi.tile1) umma_commit(smem_u32(&bars->b_empty));
       }
     }
-  } else if (kGat && warp >= 10) {
-    // ============ candidate-block gathers: warps 10..17 ============
+  } else if (fill && warp >= 10) {
+    // ============ tile gathers: warps 10..17 ============
     // Warp w copies blocks 2w and 2w + 1 of each tile: lane l, step j takes 16-byte piece
     // 32 j + l of the pair (a block is 8 rows x 16 pieces; a step covers two rows of one
     // block, 512 contiguous bytes) into row 8 (2w + j / 4) + r8 of the tile, dim half c / 8,
     // swizzled as a TMA tile.  A missing block (-1), or rows past the plane's end (those of
     // a partial newest block), are not copied: such rows are invalid in the epilogue and
     // an MMA row depends only on its own tile row.  Every thread's part of a tile arrives
-    // on the tile's barrier when it lands (the MMA warp fences before reading it), so up to
-    // four tiles are in flight; the next tile's block ids are fetched meanwhile.
+    // on the tile's barrier when it lands (the MMA warp fences before reading it), so the
+    // whole ring is in flight; the next tile's block ids are fetched meanwhile.
+    // FP8 (FULL: the 16 consecutive blocks of the tile; REINDEX: 16 candidate blocks): a
+    // block is 8 rows x 8 pieces of codes (its 32 scale bytes are read by the epilogue), a
+    // step of the warp is four rows of one block; the tile is [128 rows][128 B].
     const int gw = warp - 10;
     GroupInfo gi;
     int g = g_first - 1;
@@ -724,9 +721,14 @@ __global__ void __launch_bounds__(num_threads(kMode), 1)
         load_group(a, g, gi);
       }
       const int64_t c0 = (it - gi.tile0) * 16 + 2 * gw;
-      const int32_t* cb = a.cand + (int64_t)gi.q0 * a.ncb;
-      nb0 = c0 < a.ncb ? __ldg(cb + c0) : -1;
-      nb1 = c0 + 1 < a.ncb ? __ldg(cb + c0 + 1) : -1;
+      if (a.cand) {
+        const int32_t* cb = a.cand + (int64_t)gi.q0 * a.ncb;
+        nb0 = c0 < a.ncb ? __ldg(cb + c0) : -1;
+        nb1 = c0 + 1 < a.ncb ? __ldg(cb + c0 + 1) : -1;
+      } else {  // FULL (FP8): the tile's own blocks, from the sequence's first row
+        nb0 = (int32_t)c0;
+        nb1 = (int32_t)c0 + 1;
+      }
       nrb = gi.rb;
     };
     if (ntile > 0) fetch_ids(it_lo);
@@ -742,8 +744,21 @@ __global__ void __launch_bounds__(num_threads(kMode), 1)
       const int32_t b0 = nb0, b1 = nb1;
       const int64_t rb = nrb;
       const uint32_t stg = smem_u32(a_smem + s * kStageBytes);
+      if (kFp8) {
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
+        for (int j = 0; j < 4; ++j) {
+          const int pc = j * 32 + lane;
+          const int32_t blk = j < 2 ? b0 : b1;
+          const int r8 = (pc & 63) >> 3, c = pc & 7;
+          const uint32_t row = (uint32_t)((2 * gw + (j >> 1)) * 8 + r8);
+          const int64_t grow = rb + (int64_t)blk * 8 + r8;  // rb is a multiple of 8
+          if (blk >= 0 && grow < a.index_rows)
+            cp_async16(stg + sw128_off(row, (uint32_t)c),
+                       a.plane8 + (grow >> 3) * kFp8BlockBytes + r8 * kDIdx + c * 16);
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < 8 && !kFp8; ++j) {
         const int pc = j * 32 + lane;
         const int32_t blk = j < 4 ? b0 : b1;
         const int r8 = (pc & 127) >> 4, c = pc & 15;
@@ -971,18 +986,18 @@ cudaError_t launch_index(const IndexArgs& args, int num_sms, cudaStream_t s) {
     const int64_t qrows = (int64_t)a.Q * a.H;
     e = launch_pdl(quant_q_kernel, dim3((unsigned)((qrows + 7) / 8)), dim3(256), 0, s, a);
     if (e != cudaSuccess) return e;
-    // the plane as [blocks][8 rows][128 B] (scales skipped by the block stride)
+    // FULL tiles: the plane as [blocks][8 rows][128 B] (scales skipped by the block stride);
+    // candidate blocks are gathered
     const uint64_t dims[3] = {(uint64_t)kDIdx, 8, (uint64_t)((a.index_rows + 7) / 8)};
     const uint64_t strides[2] = {(uint64_t)kDIdx, (uint64_t)kFp8BlockBytes};
     const uint32_t box_t[3] = {(uint32_t)kDIdx, 8, kTileRows / 8};
-    const uint32_t box_b[3] = {(uint32_t)kDIdx, 8, 1};
     const uint64_t qd[2] = {(uint64_t)kDIdx, (uint64_t)qrows};
     const uint64_t qs[1] = {(uint64_t)kDIdx};
     const uint32_t qbox[2] = {(uint32_t)kDIdx, (uint32_t)a.H};
     if (!encode_bytes(&kt, a.plane8, 3, dims, strides, box_t) ||
-        !encode_bytes(&kb, a.plane8, 3, dims, strides, box_b) ||
         !encode_bytes(&qm, a.q8, 2, qd, qs, qbox))
       return cudaErrorInvalidValue;
+    kb = kt;
   } else if (mode == kModeFp4 || mode == kModeGather) {
     // K blocks arrive by bulk copies or gathers: only the query map is used (passed three
     // times)
