@@ -178,7 +178,7 @@ class Clocks:
                 "samples": len(sm)}
 
 
-def steps_per_graph(steps, cap=16):
+def steps_per_graph(steps, cap=32):
     """Steps captured in one CUDA graph: the largest divisor of `steps` up to `cap`."""
     return max(g for g in range(1, min(cap, max(steps, 1)) + 1) if steps % g == 0)
 
@@ -278,7 +278,7 @@ def run_ours(args):
 
     # ---- device-resident timing of K steps ----
     # The K steps run as replays of CUDA graphs that each hold G consecutive steps (G the
-    # largest divisor of K up to 16; the C ABI only enqueues kernels, so it captures as is):
+    # largest divisor of K up to 32; the C ABI only enqueues kernels, so it captures as is):
     # inside a graph the kernels of one step follow those of the previous step with
     # programmatic dependent launch, as they would in an engine's decode loop, instead of
     # paying a graph launch per step.  Every step keeps its full order: a step's first
