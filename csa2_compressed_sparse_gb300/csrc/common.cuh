@@ -137,6 +137,8 @@ struct AttnArgs {
   const float* inv_freq;  // [32] or null: rotate the output's dims 448..511 back by q_pos
   int plane_dtype;        // 0: bf16 plane rows [512]; 1: FP4 rows of 288 bytes (E2M1 codes,
                           //    low nibble first, then 32 E4M3 scales, one per 16 dims)
+  int stream_rows;        // 1: the call reads fewer rows than the plane holds, so a row is
+                          //    read about once: gathered bf16 rows are evicted from L2 first
 };
 
 cudaError_t launch_compress(const CompressArgs& a, cudaStream_t s);

@@ -147,6 +147,9 @@ csa2_status attn_common(const char* name, const csa2_bf16* q, int Q, const int32
   a.plane_dtype = plane_dtype;
   a.sel = sel; a.nsel = nsel; a.sink = sink; a.scale = scale; a.out = out; a.lse = lse;
   a.inv_freq = inv_freq;
+  // rows read about once (a decode batch) are streamed through L2; a prefill chunk's
+  // queries share the plane's rows, which stay
+  a.stream_rows = (int64_t)Q * (128 + nsel) <= plane_rows ? 1 : 0;
   REQUIRE(ws == nullptr || (reinterpret_cast<uintptr_t>(ws) & 255u) == 0,
           "%s: ws must be 256-byte aligned", name);
   const int sms = num_sms();

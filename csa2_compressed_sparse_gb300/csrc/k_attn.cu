@@ -286,18 +286,22 @@ __device__ __forceinline__ void out_pass(const float* own, const float* peer, co
         }
       }
     }
+    // streaming stores: the output is not read again here and should not push the
+    // plane's rows out of L2
 #pragma unroll
     for (int hh = 0; hh < 4; ++hh)
-      *reinterpret_cast<uint4*>(out_q + (4 * c + hh) * kDLat + gd) =
-          make_uint4(pack_bf16x2(o[hh][0], o[hh][1]), pack_bf16x2(o[hh][2], o[hh][3]),
-                     pack_bf16x2(o[hh][4], o[hh][5]), pack_bf16x2(o[hh][6], o[hh][7]));
+      __stcs(reinterpret_cast<uint4*>(out_q + (4 * c + hh) * kDLat + gd),
+             make_uint4(pack_bf16x2(o[hh][0], o[hh][1]), pack_bf16x2(o[hh][2], o[hh][3]),
+                        pack_bf16x2(o[hh][4], o[hh][5]), pack_bf16x2(o[hh][6], o[hh][7])));
   }
 }
 
 // Rows of one chunk into the KV buffer at `kvb` by the threads of a team (t = 0..255);
-// a row index below zero gives a row of zeros.
+// a row index below zero gives a row of zeros.  stream: bf16 rows are evicted from L2 first
+// (a call that reads each row about once).
 __device__ __forceinline__ void gather_chunk(const int32_t* rows, int fp8, bool fp4,
-                                             const uint8_t* base, uint32_t kvb, int t) {
+                                             const uint8_t* base, uint32_t kvb, int t,
+                                             bool stream) {
   if (fp4) {
     // FP4 plane rows: 64 rows x 32 groups of 16 dims (8 code bytes + 1 scale byte); each
     // group becomes two 16-byte bf16 chunks.  E2M1 x E4M3 has at most six significant
@@ -377,6 +381,7 @@ __device__ __forceinline__ void gather_chunk(const int32_t* rows, int fp8, bool 
     }
   } else {
     // four 1 KiB rows per iteration of the team
+    const uint64_t pol = stream ? policy_evict_first() : policy_evict_normal();
 #pragma unroll
     for (int i = 0; i < 64 * 64 / kTeam; ++i) {
       const int flat = i * kTeam + t;
@@ -384,7 +389,7 @@ __device__ __forceinline__ void gather_chunk(const int32_t* rows, int fp8, bool 
       const int64_t off = rows[r] < 0 ? -1 : (int64_t)rows[r] * 1024;
       const uint32_t dst = kvb + (c >> 3) * kDimBlock + sw128_off(r, c & 7);
       if (off < 0) st_shared_zero16(dst);
-      else cp_async16(dst, base + off + c * 16);
+      else cp_async16_hint(dst, base + off + c * 16, pol);
     }
   }
 }
@@ -486,7 +491,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     const int fp8 = c < 2 ? a.swa_dtype : 0;  // 1, 2: the FP8 window layouts
     const uint8_t* base = c < 2 ? a.swa : reinterpret_cast<const uint8_t*>(a.plane);
-    gather_chunk(X.rowidx[slot], fp8, c >= 2 && a.plane_dtype == 1, base, kvb, t_in_team);
+    gather_chunk(X.rowidx[slot], fp8, c >= 2 && a.plane_dtype == 1, base, kvb, t_in_team,
+                 a.stream_rows != 0);
     cp_async_commit();
     return false;
   };
