@@ -34,11 +34,12 @@ constexpr int kModeBf16 = 0;  // bf16 rows
 constexpr int kModeFp8 = 1;   // blocks of 8 E4M3 rows with fp32 row scales
 constexpr int kModeFp4 = 2;   // blocks of 8 E2M1 rows with E8M0 scales per 32 dims
 constexpr int kModeGather = 3;  // bf16 rows of candidate blocks, gathered by eight warps
+constexpr int kModeFp8Gat = 4;  // FP8 candidate blocks, gathered by eight warps
 constexpr int kFp4ConvWarps = 8;  // FP4: warps 10 .. 17 convert packed blocks to bf16
 constexpr int kGatherWarps = 8;   // gather mode: warps 10 .. 17 copy the candidate blocks
 __host__ __device__ constexpr int num_threads(int mode) {
   return mode == kModeFp4 ? 320 + 32 * kFp4ConvWarps
-                          : (mode == kModeGather || mode == kModeFp8 ? 320 + 32 * kGatherWarps
+                          : (mode == kModeGather || mode == kModeFp8Gat ? 320 + 32 * kGatherWarps
                                                                      : 320);
 }
 // MMA operand ring: bf16 tiles are 32 KiB (two 64-dim blocks of 128-byte rows), FP8 tiles
@@ -51,7 +52,7 @@ constexpr int kFp4StgBytes = 16 * kFp4BlockBytes;    // 8704: the 16 blocks of a
 constexpr int kFp4StgStages = 8;
 constexpr int kFp4CvStages = 2;
 __host__ __device__ constexpr int stage_bytes(int mode) {
-  return mode == kModeFp8 ? kTileRows * kDIdx : kBf16Tile;
+  return mode == kModeFp8 || mode == kModeFp8Gat ? kTileRows * kDIdx : kBf16Tile;
 }
 __host__ __device__ constexpr int num_stages(int mode) {
   return mode == kModeFp4 ? kFp4CvStages : 4 * kBf16Tile / stage_bytes(mode);
@@ -61,7 +62,8 @@ __host__ __device__ constexpr int ring_bytes(int mode) {
                           : 4 * kBf16Tile;
 }
 constexpr int kMaxStages = 8;
-static_assert(num_stages(kModeFp8) <= kMaxStages && kFp4StgStages <= kMaxStages, "ring");
+static_assert(num_stages(kModeFp8) <= kMaxStages && num_stages(kModeFp8Gat) <= kMaxStages &&
+                  kFp4StgStages <= kMaxStages, "ring");
 static_assert(ring_bytes(kModeFp4) % 1024 == 0, "the Q block must stay 1024-byte aligned");
 constexpr int kBBytes = 2 * 256 * 128;              // 64 KiB: two 64-dim blocks x 256 rows
 constexpr int kMaxGroup = 8;
@@ -468,11 +470,13 @@ __device__ __noinline__ uint4 fp4_word_slow(uint32_t w, int e) {
   return make_uint4(o[0], o[1], o[2], o[3]);
 }
 
-// kModeFp8: K tiles and queries are E4M3 codes (tcgen05 kind::f8f6f4, K = 32 per MMA); the
-// row scale of K and the query scales multiply the head sum in the epilogue.  FULL tiles
-// come by one TMA box over the block layout ([16 blocks][8 rows][128 B], the scales skipped
-// by the block stride); REINDEX tiles are gathered by warps 10..17 as in the gather mode
-// (one box per 1 KiB candidate block is as slow as the bf16 plane's).
+// kModeFp8 / kModeFp8Gat: K tiles and queries are E4M3 codes (tcgen05 kind::f8f6f4, K = 32
+// per MMA); the row scale of K and the query scales multiply the head sum in the epilogue.
+// FULL tiles (kModeFp8, 320 threads) come by one TMA box over the block layout ([16 blocks]
+// [8 rows][128 B], the scales skipped by the block stride); REINDEX tiles (kModeFp8Gat) are
+// gathered by warps 10..17 as in the gather mode (one box per 1 KiB candidate block is as
+// slow as the bf16 plane's).  Two instances, because the gather warps' threads leave the
+// epilogue fewer registers, which costs the FULL instance's wide query groups (prefill).
 // kModeFp4: the producer bulk-copies the tile's 16 packed blocks, warps 10..17 convert
 // them to a bf16 tile (exact) and the MMAs and epilogue are those of the bf16 mode.
 // kModeGather (REINDEX on the bf16 plane): the tile's 16 candidate blocks are 2 KiB each at
@@ -487,11 +491,11 @@ __global__ void __launch_bounds__(num_threads(kMode), 1)
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   // rounded up to 1024 bytes by pointer arithmetic, so that accesses stay shared-space
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-  constexpr bool kFp8 = kMode == kModeFp8;
+  constexpr bool kFp8 = kMode == kModeFp8 || kMode == kModeFp8Gat;
   constexpr bool kFp4 = kMode == kModeFp4;
   constexpr bool kGat = kMode == kModeGather;
   // warps 10..17 fill the operand ring (candidate blocks on the bf16 or FP8 plane)
-  const bool fill = kGat || (kFp8 && a.cand != nullptr);
+  constexpr bool fill = kGat || kMode == kModeFp8Gat;
   // the ring the producer fills: operand tiles, or the FP4 mode's packed blocks
   constexpr int kStages = kFp4 ? kFp4StgStages : num_stages(kMode);
   constexpr int kStageBytes = kFp4 ? kFp4StgBytes : stage_bytes(kMode);
@@ -980,9 +984,9 @@ cudaError_t launch_index(const IndexArgs& args, int num_sms, cudaStream_t s) {
   cudaError_t e = launch_pdl(index_prep_kernel, dim3(1), dim3(kPrepThreads), 0, s, a);
   if (e != cudaSuccess) return e;
   CUtensorMap kt, kb, qm;
-  const int mode = a.plane8 ? kModeFp8
+  const int mode = a.plane8 ? (a.cand ? kModeFp8Gat : kModeFp8)
                             : (a.plane4 ? kModeFp4 : (a.cand ? kModeGather : kModeBf16));
-  if (mode == kModeFp8) {
+  if (mode == kModeFp8 || mode == kModeFp8Gat) {
     const int64_t qrows = (int64_t)a.Q * a.H;
     e = launch_pdl(quant_q_kernel, dim3((unsigned)((qrows + 7) / 8)), dim3(256), 0, s, a);
     if (e != cudaSuccess) return e;
@@ -1013,6 +1017,7 @@ cudaError_t launch_index(const IndexArgs& args, int num_sms, cudaStream_t s) {
   }
   const size_t smem = index_smem_bytes(mode);
   auto kern = mode == kModeFp8    ? index_score_kernel<kModeFp8>
+              : mode == kModeFp8Gat ? index_score_kernel<kModeFp8Gat>
               : mode == kModeFp4  ? index_score_kernel<kModeFp4>
               : mode == kModeGather ? index_score_kernel<kModeGather>
                                     : index_score_kernel<kModeBf16>;
