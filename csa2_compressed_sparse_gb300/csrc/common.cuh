@@ -131,8 +131,6 @@ struct AttnArgs {
   float scale;
   uint16_t* out;
   float* lse;
-  float* part_o;   // [Q][nsplit][64][512] partial outputs (nsplit > 1)
-  float* part_ml;  // [Q][nsplit][2][64] partial running max (log2) and sum
   int cluster;     // nsplit == 2: the two CTAs of a query form a cluster and merge in place
   const float* inv_freq;  // [32] or null: rotate the output's dims 448..511 back by q_pos
   int plane_dtype;        // 0: bf16 plane rows [512]; 1: FP4 rows of 288 bytes (E2M1 codes,

@@ -106,13 +106,6 @@ size_t topk_ws_bytes(int Q, int64_t ld, int k) {
   return nchunk > 1 ? up256((size_t)Q * 4) + up256((size_t)Q * nchunk * k * 8) : 0;
 }
 
-// Workspace of the split attention: partial O [nsplit][64][512] fp32 and (max, sum)
-// [nsplit][2][64] fp32 per query.  One or two CTAs per query need none (two merge in
-// distributed shared memory).
-size_t attn_ws_bytes(int Q, int nsplit) {
-  if (nsplit <= 2) return 0;
-  return up256((size_t)Q * nsplit * 64 * 512 * 4) + up256((size_t)Q * nsplit * 128 * 4);
-}
 
 csa2_status attn_common(const char* name, const csa2_bf16* q, int Q, const int32_t* q_seq,
                         const int64_t* q_pos, const csa2_swa* swa, const void* plane,
@@ -154,13 +147,8 @@ csa2_status attn_common(const char* name, const csa2_bf16* q, int Q, const int32
           "%s: ws must be 256-byte aligned", name);
   const int sms = num_sms();
   if (sms <= 0) return fail(CSA2_ECUDA, "%s: no CUDA device", name);
-  int nsplit = csa2::attn_num_splits(Q, nsel, sms);
-  while (nsplit > 2 && (ws == nullptr || attn_ws_bytes(Q, nsplit) > ws_bytes)) --nsplit;
-  if (nsplit > 2) {
-    a.part_o = static_cast<float*>(ws);
-    a.part_ml = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) +
-                                         up256((size_t)Q * nsplit * 64 * 512 * 4));
-  }
+  (void)ws_bytes;  // the attention needs no workspace (see csa2_attn_workspace_size)
+  const int nsplit = csa2::attn_num_splits(Q, nsel, sms);
   cudaError_t e = csa2::launch_attn(a, nsplit, stream);
   if (e != cudaSuccess) return cuda_fail(e, name);
   return CSA2_OK;
@@ -538,10 +526,9 @@ csa2_status csa2_topk_scores(const float* scores, const int32_t* n, int Q, int64
 }
 
 size_t csa2_attn_workspace_size(int Q, int nsel) {
-  if (Q <= 0 || nsel < 0 || nsel > 512) return 0;
-  const int sms = num_sms();
-  if (sms <= 0) return 0;
-  return attn_ws_bytes(Q, csa2::attn_num_splits(Q, nsel, sms));
+  (void)Q;
+  (void)nsel;
+  return 0;  // one or two CTAs per query, merging in distributed shared memory
 }
 
 csa2_status csa2_sparse_attn(const csa2_bf16* q, int Q, const int32_t* q_seq,

@@ -34,9 +34,7 @@
 // Every CTA starts its running max at the sink logit.  With nsplit = 1 its running sum
 // starts at the sink's mass (1) and the CTA writes the output.  With nsplit = 2 the two
 // CTAs of a query run as a cluster and merge through distributed shared memory, each
-// finishing half of the dims.  Otherwise
-// every CTA writes its partial (max, sum, O) to the workspace and attn_combine_kernel
-// merges them; the merges add the sink's e^{sink_h} once.
+// finishing half of the dims; the merge adds the sink's e^{sink_h} once.
 //
 // Warps 0..3 softmax + O^T rescale + output, warps 4..19 gather (teams of eight
 // warps), warps 20..23 issue the MMAs (lane 0 each; warp 20 also owns the TMEM).
@@ -755,7 +753,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (a.lse && tid < 64)
       a.lse[(int64_t)q * kHeads + tid] =
           (X.m_run[tid] + __log2f(X.l_run[tid])) * 0.6931471805599453f;
-  } else if (a.cluster) {
+  } else {
     // Two CTAs per query as a cluster: CTA r finishes dims 256 r .. 256 r + 255 (the O^T
     // tiles 2 r and 2 r + 1).  Warps 0..7 stage the two tiles the peer finishes from TMEM
     // (warp w: TMEM lanes 32 (w % 4) .., tile w / 4) in the second KV buffer, and the
@@ -908,96 +906,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         bulk_wait_group_read0();  // the CTA may exit once the boxes have been read
       }
     }
-  } else {
-    // partial O^T (unnormalised fp32) -> workspace [Q][nsplit][64 heads][512], plus the
-    // running max (log2 units) and sum per head
-    float* po = a.part_o + ((int64_t)q * nsplit + rank) * kHeads * kDLat;
-    if (warp < 4) {
-      const uint32_t lrow = (uint32_t)(warp * 32) << 16;
-#pragma unroll 1
-      for (int mt = 0; mt < 4; ++mt) {
-        const int dim = mt * 128 + warp * 32 + lane;
-#pragma unroll
-        for (int hb = 0; hb < 64; hb += 32) {
-          uint32_t v[32];
-          if (n > 0) {
-            tmem_ld32(tmem + lrow + kColO + 64 * mt + hb, v);
-            tmem_ld_wait();
-          } else {
-#pragma unroll
-            for (int j = 0; j < 32; ++j) v[j] = 0u;
-          }
-#pragma unroll
-          for (int j = 0; j < 32; ++j) po[(hb + j) * kDLat + dim] = __uint_as_float(v[j]);
-        }
-      }
-    }
-    if (tid < 64) {
-      a.part_ml[((int64_t)q * nsplit + rank) * 128 + tid] = X.m_run[tid];
-      a.part_ml[((int64_t)q * nsplit + rank) * 128 + 64 + tid] = X.l_run[tid];
-    }
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   if (warp == kMmaWarp) tmem_dealloc(tmem, 512);
-}
-
-// Merge of the nsplit partials of each query: grid = Q x 8, each CTA 8 heads.
-__global__ void __launch_bounds__(256) attn_combine_kernel(AttnArgs a, int nsplit) {
-  __shared__ float coef[kMaxChunks][8];  // [split][head within the CTA]
-  __shared__ float lse2[8];
-  __shared__ float rc[32], rs[32];
-  const int q = blockIdx.x, h0 = blockIdx.y * 8, tid = threadIdx.x;
-  griddep_launch_dependents();
-  griddep_wait();
-  if (a.inv_freq && tid >= 32 && tid < 64) rope_table(a.inv_freq, a.q_pos[q], tid - 32, rc, rs);
-  if (tid < 8) {
-    const int h = h0 + tid;
-    const float* ml = a.part_ml + (int64_t)q * nsplit * 128;
-    float M = a.sink ? a.sink[h] * kLog2e : -INFINITY;
-    for (int j = 0; j < nsplit; ++j) M = fmaxf(M, ml[j * 128 + h]);
-    float Z = a.sink ? ex2(a.sink[h] * kLog2e - M) : 0.f;
-    for (int j = 0; j < nsplit; ++j) {
-      const float mj = ml[j * 128 + h];
-      if (mj != -INFINITY) Z += ex2(mj - M) * ml[j * 128 + 64 + h];
-    }
-    const float inv = 1.f / Z;
-    for (int j = 0; j < nsplit; ++j) {
-      const float mj = ml[j * 128 + h];
-      coef[j][tid] = mj == -INFINITY ? 0.f : ex2(mj - M) * inv;
-    }
-    lse2[tid] = M + __log2f(Z);
-  }
-  __syncthreads();
-  // 8 heads x 512 dims = 512 groups of 8 elements; 2 per thread
-  for (int gidx = tid; gidx < 512; gidx += 256) {
-    const int hl = gidx >> 6, d = (gidx & 63) * 8;
-    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-    for (int j = 0; j < nsplit; ++j) {
-      const float w = coef[j][hl];
-      if (w == 0.f) continue;
-      const float4* src = reinterpret_cast<const float4*>(
-          a.part_o + (((int64_t)q * nsplit + j) * kHeads + h0 + hl) * kDLat + d);
-      const float4 x0 = src[0], x1 = src[1];
-      acc[0] += w * x0.x; acc[1] += w * x0.y; acc[2] += w * x0.z; acc[3] += w * x0.w;
-      acc[4] += w * x1.x; acc[5] += w * x1.y; acc[6] += w * x1.z; acc[7] += w * x1.w;
-    }
-    if (a.inv_freq && d >= kRopeDim0) {  // pairs (d - 448) / 2 .. +3 rotated back
-#pragma unroll
-      for (int e = 0; e < 8; e += 2) {
-        const int i = (d + e - kRopeDim0) >> 1;
-        const float o0 = acc[e] * rc[i] + acc[e + 1] * rs[i];
-        const float o1 = acc[e + 1] * rc[i] - acc[e] * rs[i];
-        acc[e] = o0;
-        acc[e + 1] = o1;
-      }
-    }
-    uint4* dst = reinterpret_cast<uint4*>(a.out + ((int64_t)q * kHeads + h0 + hl) * kDLat + d);
-    *dst = make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]),
-                      pack_bf16x2(acc[4], acc[5]), pack_bf16x2(acc[6], acc[7]));
-  }
-  if (a.lse && tid < 8) a.lse[(int64_t)q * kHeads + h0 + tid] = lse2[tid] * 0.6931471805599453f;
 }
 
 }  // namespace
@@ -1006,12 +919,14 @@ size_t attn_smem_bytes() {
   return 1024 + kQBytes + 2 * kBufBytes + 2 * kPBytes + sizeof(Aux);
 }
 
-// CTAs per query: as many as keep every CTA of the launch in one wave (one CTA per SM),
-// at least one chunk each.
+// CTAs per query: two (a cluster that merges in distributed shared memory) when both fit
+// in one wave of one CTA per SM, else one.  More CTAs per query, each writing a partial
+// that a second kernel merged, measured slower at every batch tried (4, 8 and 32 queries:
+// 4, 8 and 6 us per step), the extra launch and the partials' round trip through
+// memory costing more than the shorter chains of chunks save.
 int attn_num_splits(int Q, int nsel, int num_sms) {
-  const int nchunks = 2 + (nsel + kChunk - 1) / kChunk;
-  int nsplit = num_sms / (Q > 0 ? Q : 1);
-  return nsplit < 1 ? 1 : (nsplit > nchunks ? nchunks : nsplit);
+  (void)nsel;
+  return Q > 0 && 2 * Q <= num_sms ? 2 : 1;
 }
 
 cudaError_t launch_attn(const AttnArgs& a, int nsplit, cudaStream_t s) {
@@ -1037,11 +952,8 @@ cudaError_t launch_attn(const AttnArgs& a, int nsplit, cudaStream_t s) {
     return launch_pdl_cluster(sparse_attn_kernel, dim3(2u, (unsigned)a.Q), dim3(kThreads), smem, s,
                               2u, b, qm, wm, om);
   }
-  e = launch_pdl(sparse_attn_kernel, dim3((unsigned)nsplit, (unsigned)a.Q), dim3(kThreads), smem,
-                 s, a, qm, wm, om);
-  if (e != cudaSuccess || nsplit == 1) return e;
-  return launch_pdl(attn_combine_kernel, dim3((unsigned)a.Q, kHeads / 8), dim3(256), 0, s, a,
-                    nsplit);
+  return launch_pdl(sparse_attn_kernel, dim3(1u, (unsigned)a.Q), dim3(kThreads), smem, s, a, qm,
+                    wm, om);
 }
 
 }  // namespace csa2

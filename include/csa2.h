@@ -389,12 +389,11 @@ csa2_status csa2_topk_scores(const float* scores, const int32_t* n, int Q, int64
  *          (sel may be NULL with nsel == 0: window only)
  *   sink   [64] fp32 or NULL (no sink term);  scale: softmax temperature (1/sqrt(512))
  *   out    [Q][64][512] bf16;  lse [Q][64] fp32 or NULL
- *   ws     optional workspace (256-byte aligned) of csa2_attn_workspace_size(Q, nsel)
- *          bytes.  With few queries the entries of one query are spread over several
- *          CTAs; two of them merge in distributed shared memory, more merge through
- *          this workspace, so with ws == NULL (or a smaller one) at most two CTAs per
- *          query are used.  The size is 0 when no more are worth it.  The result does
- *          not depend on it beyond rounding. */
+ *   ws     optional workspace (256-byte aligned, NULL allowed) of
+ *          csa2_attn_workspace_size(Q, nsel) bytes, which is 0: a query's entries run on
+ *          one CTA, or on two that merge in distributed shared memory when 2 Q CTAs fit
+ *          on the GPU at once.  The argument is kept so that callers that size and pass
+ *          a workspace need no change. */
 typedef enum { CSA2_SWA_RING = 0, CSA2_SWA_LINEAR = 1 } csa2_swa_mode;
 typedef enum { CSA2_SWA_BF16 = 0, CSA2_SWA_FP8_S128 = 1, CSA2_SWA_FP8_E8M0 = 2 } csa2_swa_dtype;
 typedef struct {

@@ -5,8 +5,8 @@ query below 127 has a window of p + 1 < 128 rows and its first window chunk
 (positions p - 127 .. p - 64) is partly or wholly empty.  [A] "visible 是每行自己的前缀
 长度": a query with n_vis < 512 visible compressed rows selects all of them and pads
 with -1; a ratio-2 query at p = 0 has none (k_eff = 0) and attends to its window alone.
-These cases run through the three ways the attention merges a query's CTAs (one CTA,
-a two-CTA cluster, the workspace combine).  The LINEAR window's lower bound and the
+These cases run through both ways the attention lays out a query (one CTA, or a
+two-CTA cluster that merges in distributed shared memory).  The LINEAR window's lower bound and the
 bounded waits' timeout path are checked too.
 """
 import numpy as np
@@ -52,19 +52,20 @@ def _short_history(ratio):
 @pytest.mark.parametrize("ratio", [1, 2])
 def test_short_history_decode_through_every_merge_path(ratio):
     """Decode queries at p in {0, 1, 63, 64, 126, 127, 128} on a RING window: the step
-    itself (workspace combine: up to ten CTAs per query, most of them with no rows),
-    then the same selection through the two-CTA cluster (no workspace) and through one
-    CTA per query (the seven queries repeated twelve times)."""
+    itself (two CTAs per query, the cluster merge; several of the CTAs have no rows),
+    then the same selection once more on its own and through one CTA per query (the
+    seven queries repeated twelve times)."""
     from csa2_compressed_sparse_gb300 import csa2_device_status, csa2_sparse_attn
     from csa2_compressed_sparse_gb300.step import swa_of
     wl = _short_history(ratio)
     t, spec, buf = run_workload(wl)
-    assert buf.attn_ws is not None  # the step ran the workspace combine
+    assert buf.attn_ws is None  # the attention needs no workspace
     check_queries(wl, t, buf, list(range(wl.Q)))
     key = register(wl)
     sel = buf.sel
     refs = [oracle_attn(wl, key, q, sel[q].cpu().numpy())[0] for q in range(wl.Q)]
-    # two CTAs per query, merged in distributed shared memory
+    # the same selection on its own (two CTAs per query, merged in distributed shared
+    # memory)
     out = torch.empty_like(buf.out[0])
     csa2_sparse_attn(t["q"][0], t["q_seq"], t["q_pos"], swa_of(spec, t, 0), t["plane"],
                      t["row_base"], sel, t["sink"], out)

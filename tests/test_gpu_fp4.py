@@ -79,10 +79,11 @@ def test_attention_on_an_fp4_plane_matches_the_oracle(name):
     p4 = torch.empty(csa2_plane_fp4_bytes(rows), dtype=torch.uint8, device="cuda")
     csa2_plane_fp4(t["plane"], p4)
     out = torch.empty((wl.Q, 64, 512), dtype=torch.bfloat16, device="cuda")
+    # a workspace is accepted and unused (its size is 0): the runs with and without one
+    # take the same path (two CTAs per query for few queries, merged in distributed
+    # shared memory)
     ws = torch.empty(max(csa2_attn_workspace_size(wl.Q, 512), 256), dtype=torch.uint8,
                      device="cuda")
-    # few queries: through the workspace combine (up to ten CTAs per query), then without
-    # a workspace (two CTAs per query, merged in distributed shared memory)
     runs = [(False, ws), (True, ws)] + ([(False, None), (True, None)] if wl.Q <= 76 else [])
     for rope, ws in runs:
         invf = t["inv_freq"] if rope else None
@@ -131,8 +132,9 @@ def test_attention_on_an_e8m0_fp8_window_matches_the_oracle():
 def test_attention_without_a_sink_through_every_path():
     """sink = NULL (no sink term): the running max starts at the first chunk's own
     largest score.  Heads 0..15 carry queries scaled by 2^8, so their later chunks also
-    overtake the running max.  Two CTAs per query (the cluster merge: no workspace), the
-    workspace combine, and one CTA per query (the queries repeated to fill the GPU)."""
+    overtake the running max.  Two CTAs per query (the cluster merge), with and without
+    the (unused) workspace argument, and one CTA per query (the queries repeated to fill
+    the GPU)."""
     from csa2_compressed_sparse_gb300 import (SWA_RING, Swa, csa2_attn_workspace_size,
                                               csa2_device_status, csa2_sparse_attn)
     g = np.random.default_rng(91)

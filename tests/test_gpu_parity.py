@@ -313,54 +313,59 @@ def test_fused_compress_index_topk_equals_the_separate_calls(make):
 
 
 def test_attention_split_and_unsplit_agree_with_the_oracle():
-    """The same queries with and without the attention workspace (several CTAs per
-    query merged through it, or one CTA per query)."""
+    """The same queries through two CTAs per query (a cluster: nine queries) and through
+    one CTA per query (the nine repeated nine times fill the GPU); the workspace
+    argument is accepted and unused."""
     from csa2_compressed_sparse_gb300 import (csa2_attn_workspace_size, csa2_device_status,
                                               csa2_sparse_attn)
     from csa2_compressed_sparse_gb300.step import swa_of
     wl = W.decode_batch(B=9, lo=300, hi=7000, seed=26)
     t, spec, buf = run_workload(wl)
     key = register(wl)
-    nb = csa2_attn_workspace_size(wl.Q, spec.k)
-    assert nb > 0
-    for ws in (None, torch.empty(nb, dtype=torch.uint8, device="cuda")):
-        out = torch.empty_like(buf.out[0])
-        lse = torch.empty((wl.Q, 64), dtype=torch.float32, device="cuda")
-        csa2_sparse_attn(t["q"][0], t["q_seq"], t["q_pos"], swa_of(spec, t, 0), t["plane"],
-                         t["row_base"], buf.sel, t["sink"], out, lse=lse, ws=ws)
+    assert csa2_attn_workspace_size(wl.Q, spec.k) == 0
+    refs = [oracle_attn(wl, key, q, buf.sel[q].cpu().numpy()) for q in range(wl.Q)]
+    ws = torch.empty(256, dtype=torch.uint8, device="cuda")
+    for rep, w in ((1, None), (1, ws), (9, None)):
+        idx = torch.arange(wl.Q, device="cuda").repeat(rep)
+        out = torch.empty((len(idx), 64, 512), dtype=torch.bfloat16, device="cuda")
+        lse = torch.empty((len(idx), 64), dtype=torch.float32, device="cuda")
+        csa2_sparse_attn(t["q"][0][idx].contiguous(), t["q_seq"][idx].contiguous(),
+                         t["q_pos"][idx].contiguous(), swa_of(spec, t, 0), t["plane"],
+                         t["row_base"], buf.sel[idx].contiguous(), t["sink"], out, lse=lse,
+                         ws=w)
         csa2_device_status()
-        for q in range(wl.Q):
-            ref, ref_lse = oracle_attn(wl, key, q, buf.sel[q].cpu().numpy())
-            check_attn(out[q].float().cpu().numpy(), ref)
-            assert np.abs(lse[q].cpu().numpy() - ref_lse).max() < 1e-2
+        for i in range(len(idx)):
+            ref, ref_lse = refs[i % wl.Q]
+            check_attn(out[i].float().cpu().numpy(), ref)
+            assert np.abs(lse[i].cpu().numpy() - ref_lse).max() < 1e-2
 
 
-@pytest.mark.parametrize("use_ws", [False, True])
-def test_attention_with_the_inverse_rope_epilogue(use_ws):
+@pytest.mark.parametrize("rep", [1, 9])
+def test_attention_with_the_inverse_rope_epilogue(rep):
     """csa2_sparse_attn_rope: the output's dims 448..511 rotated back by the query position
-    ([A] "出来之后"), through the two-CTA cluster merge (no workspace) and through the
-    global combine (workspace: ten CTAs per query).  The other dims are the plain call's."""
-    from csa2_compressed_sparse_gb300 import (csa2_attn_workspace_size, csa2_device_status,
-                                              csa2_sparse_attn, csa2_sparse_attn_rope)
+    ([A] "出来之后"), through the two-CTA cluster merge (nine queries) and through one CTA
+    per query (the nine repeated nine times).  The other dims are the plain call's."""
+    from csa2_compressed_sparse_gb300 import (csa2_device_status, csa2_sparse_attn,
+                                              csa2_sparse_attn_rope)
     from csa2_compressed_sparse_gb300.step import swa_of
     wl = W.decode_batch(B=9, lo=300, hi=700000, seed=31)
     t, spec, buf = run_workload(wl)
     key = register(wl)
-    ws = None
-    if use_ws:
-        ws = torch.empty(csa2_attn_workspace_size(wl.Q, spec.k), dtype=torch.uint8, device="cuda")
-    args = (t["q"][0], t["q_seq"], t["q_pos"], swa_of(spec, t, 0), t["plane"], t["row_base"],
-            buf.sel, t["sink"])
-    plain = torch.empty_like(buf.out[0])
-    rot = torch.empty_like(buf.out[0])
-    csa2_sparse_attn(*args, plain, ws=ws)
-    csa2_sparse_attn_rope(*args, rot, t["inv_freq"], ws=ws)
+    idx = torch.arange(wl.Q, device="cuda").repeat(rep)
+    args = (t["q"][0][idx].contiguous(), t["q_seq"][idx].contiguous(),
+            t["q_pos"][idx].contiguous(), swa_of(spec, t, 0), t["plane"], t["row_base"],
+            buf.sel[idx].contiguous(), t["sink"])
+    plain = torch.empty((len(idx), 64, 512), dtype=torch.bfloat16, device="cuda")
+    rot = torch.empty_like(plain)
+    csa2_sparse_attn(*args, plain)
+    csa2_sparse_attn_rope(*args, rot, t["inv_freq"])
     csa2_device_status()
     assert torch.equal(plain[:, :, :448], rot[:, :, :448])
     invf = t["inv_freq"].cpu().numpy()
     for q in range(wl.Q):
         ref, _ = oracle_attn(wl, key, q, buf.sel[q].cpu().numpy(), inv_freq=invf)
-        check_attn(rot[q].float().cpu().numpy(), ref)
+        for i in range(q, len(idx), wl.Q):
+            check_attn(rot[i].float().cpu().numpy(), ref)
 
 
 def test_reuse_attention_with_the_inverse_rope_epilogue_one_cta_per_query():
