@@ -255,14 +255,12 @@ __device__ int select_topk(const RowSrc<kSrcSmem>& src, const SampleSrc& ssrc, i
   // hold kept keys and stores them.  A dense segment (every position scored) needs no
   // count.  The sample's histogram is cleared here for the radix passes.
   clear_hist(S, 2048);
-  int nval = 0;
   uint32_t* wkey = S.ckey + warp * kWarpCap;
   uint32_t* widx = S.cidx + warp * kWarpCap;
   int mine = 0;
   uint32_t hit = 0;  // bit u: group u holds a kept key (thr >= 1: never an unscored one)
   const uint32_t gaddr = smem_u32(src.base) + 16u * (uint32_t)(warp * 32 + lane);
   auto count = [&](const uint4& vv, int u) {
-    if (!dense) nval += (vv.x != 0u) + (vv.y != 0u) + (vv.z != 0u) + (vv.w != 0u);
     const int cnt = (vv.x >= thr) + (vv.y >= thr) + (vv.z >= thr) + (vv.w >= thr);
     mine += cnt;
     hit |= (cnt ? 1u : 0u) << u;
@@ -308,18 +306,24 @@ __device__ int select_topk(const RowSrc<kSrcSmem>& src, const SampleSrc& ssrc, i
     }
   }
   if (lane == 0) S.wcnt[warp] = wpos;
-  if (!dense) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) nval += __shfl_xor_sync(0xFFFFFFFFu, nval, o);
-    if (lane == 0) atomicAdd(&S.nvalid, nval);
-  } else if (tid == 0) {
-    S.nvalid = n;
-  }
   if (lane == 0) atomicAdd(&S.ncand, wpos > kWarpCap ? kCandCap + 1 : wpos);  // full: no fast path
   __syncthreads();
-  const int keff = S.nvalid < k ? S.nvalid : k;
-  if (keff <= 0) return 0;
   const int nc = S.ncand;
+  // keff = min(k, #scored): a dense segment has n scored positions; otherwise, with at
+  // least k kept keys (all scored), keff = k, and only a segment that kept fewer needs
+  // its scored positions counted
+  int nvalid = dense ? n : nc;
+  if (!dense && nc < k) {
+    int nv = 0;
+    for (int i = tid; i < n; i += kTopkThreads) nv += src(i) != 0u;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) nv += __shfl_xor_sync(0xFFFFFFFFu, nv, o);
+    if (lane == 0) atomicAdd(&S.nvalid, nv);
+    __syncthreads();
+    nvalid = S.nvalid;
+  }
+  const int keff = nvalid < k ? nvalid : k;
+  if (keff <= 0) return 0;
   const bool fast = nc >= keff && nc <= kCandCap;  // the kept pairs hold the top-k
   // ---- 4. radix select over the kept pairs (or the whole segment) ----
   // fn(key, valid) is called by the 32 lanes of a warp together (warp-uniform loops).
@@ -439,9 +443,11 @@ __device__ int select_topk(const RowSrc<kSrcSmem>& src, const SampleSrc& ssrc, i
   return keff;
 }
 
-__device__ __forceinline__ int32_t pos_to_row(const TopkArgs& a, int q, uint32_t pos) {
+// ccache: the row's candidate block ids in shared memory, or null (read from global).
+__device__ __forceinline__ int32_t pos_to_row(const TopkArgs& a, int q, uint32_t pos,
+                                              const int32_t* ccache = nullptr) {
   if (!a.cand) return (int32_t)pos;
-  int32_t blk = a.cand[(int64_t)q * a.ncb + (pos >> 3)];
+  int32_t blk = ccache ? ccache[pos >> 3] : a.cand[(int64_t)q * a.ncb + (pos >> 3)];
   return blk * 8 + (int32_t)(pos & 7u);
 }
 
@@ -563,8 +569,30 @@ __device__ __forceinline__ void topk_row(const TopkArgs& a, int c) {
   int32_t* sel_q = a.sel + (int64_t)q * a.k;
   float* sc_q = a.sel_scores ? a.sel_scores + (int64_t)q * a.k : nullptr;
   if (a.nchunk == 1) {
-    const int keff = select_topk(src, ssrc, len, a.k, dense, S, true, ready, [&](int o, int i) {
-      sel_q[o] = pos_to_row(a, q, (uint32_t)(begin + i));
+    // REINDEX: the row's candidate block ids (up to two per thread) are loaded now (after
+    // the wait: a preceding call may have written them) and stored, once the threshold is
+    // known, at the free end of the staging buffer, so the ordered output maps positions
+    // to rows from shared memory
+    const int nu_end = pad + ((len + 4 * kTopkThreads - 1) / (4 * kTopkThreads)) * 4 * kTopkThreads;
+    const bool cache = a.cand && !a.blocks && a.ncb <= 2 * kTopkThreads &&
+                       nu_end + a.ncb <= kChunkLen + 4;
+    int32_t* cc = reinterpret_cast<int32_t*>(S.row + (kChunkLen + 4 - a.ncb));
+    int32_t cv0 = 0, cv1 = 0;
+    if (cache) {
+      const int32_t* cg = a.cand + (int64_t)q * a.ncb;
+      if (tid < a.ncb) cv0 = __ldg(cg + tid);
+      if (tid + kTopkThreads < a.ncb) cv1 = __ldg(cg + tid + kTopkThreads);
+    }
+    auto ready_c = [&]() {
+      ready();
+      if (cache) {
+        if (tid < a.ncb) cc[tid] = cv0;
+        if (tid + kTopkThreads < a.ncb) cc[tid + kTopkThreads] = cv1;
+      }
+    };
+    const int32_t* ccache = cache ? cc : nullptr;  // read after the select's barriers
+    const int keff = select_topk(src, ssrc, len, a.k, dense, S, true, ready_c, [&](int o, int i) {
+      sel_q[o] = pos_to_row(a, q, (uint32_t)(begin + i), ccache);
       if (sc_q) sc_q[o] = key_score(src(i));
     });
     pad_row(a, q, keff);
