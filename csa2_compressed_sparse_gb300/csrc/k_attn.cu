@@ -208,7 +208,8 @@ __device__ __forceinline__ void rope_table(const float* inv_freq, int64_t p, int
 __device__ __forceinline__ int ot_swz(int d) { return (d ^ (d >> 3)) & 7; }
 
 // O^T tiles mt0 .. mt0 + ntile - 1 from TMEM into shared memory as staged rows; row =
-// dim - 128 mt0.  Warps 0..3 (TMEM lanes 32 w ..); with n == 0 the tiles are zero.
+// dim - 128 mt0.  `warp` is the caller's lane quarter (warp index % 4: TMEM lanes
+// 32 warp ..); with n == 0 the tiles are zero.
 __device__ __forceinline__ void stage_ot(uint32_t tmem_o, int warp, int lane, int mt0, int ntile,
                                          uint32_t stage, bool have) {
   const uint32_t lrow = (uint32_t)(warp * 32) << 16;
@@ -737,15 +738,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
   }
 
-  // ---- epilogue (warps 0..3: warp w reads TMEM lanes 32w.. = dims mt*128 + 32w ..) ----
+  // ---- epilogue (warp w reads TMEM lanes 32 (w % 4) .. = dims mt*128 + 32 (w % 4) ..) ----
   if (tid == 0 && n == 0) mbar_wait(smem_u32(&X.q_full), 0, 100000000ull);  // Q copy landed
   __syncthreads();
+  tc_fence_after();  // every MMA is complete (the softmax warps waited for the last PV)
   if (nsplit == 1) {
-    // O^T / l -> bf16 out[q][64 heads][512]: O^T staged in the KV buffers (all 512 dims),
-    // then every thread writes
+    // O^T / l -> bf16 out[q][64 heads][512]: O^T staged in the KV buffers (all 512 dims;
+    // warp w < 16 stages tile w / 4 from its lane quarter w % 4), then every thread writes
     if (tid < 64) X.fac[0][tid] = 1.f / X.l_run[tid];
     if (a.inv_freq && warp == 4) rope_table(a.inv_freq, p, lane, X.rope_c, X.rope_s);
-    if (warp < 4) stage_ot(tmem + kColO, warp, lane, 0, 4, smem_u32(kv_s), n > 0);
+    if (warp < 16)
+      stage_ot(tmem + kColO, warp & 3, lane, warp >> 2, 1,
+               smem_u32(kv_s) + (uint32_t)(warp >> 2) * 128u * 256u, n > 0);
     __syncthreads();
     out_pass(reinterpret_cast<const float*>(kv_s), nullptr, X.fac[0], nullptr,
              a.inv_freq ? X.rope_c : nullptr, X.rope_s, a.out + (int64_t)q * kHeads * kDLat,

@@ -11,7 +11,8 @@
 //      expected to hold about 2k + 64 (refined by the next 11 bits when the sample
 //      crowds into that bin);
 //   2. filter: one pass keeps the (key, position) pairs at or above the threshold (a
-//      few times k of them) and counts the scored positions;
+//      few times k of them); only a segment that kept fewer than k counts its scored
+//      positions;
 //   3. select: three histogram passes (key bits 31..21, 20..10, 9..0) over the kept
 //      pairs give the k-th largest key T and how many keys equal to T are needed;
 //   4. output: winners are marked in a position bitmap (keys > T; the lowest
@@ -53,7 +54,7 @@ namespace {
 struct SelectSmem {
   uint32_t row[kChunkLen + 4];  // the segment's keys (shifted so its aligned part is)
   uint32_t hist[2048];
-  uint32_t hist_kept[2048];  // top 11 key bits of the kept pairs (filled by the filter)
+  uint32_t hist_kept[2048];  // top 11 key bits of the kept pairs (the first radix pass)
   uint32_t ckey[kCandCap];
   uint32_t cidx[kCandCap];
   uint32_t selmap[kWords];  // positions with key > T
@@ -210,10 +211,19 @@ __device__ int select_topk(const RowSrc<kSrcSmem>& src, const SampleSrc& ssrc, i
   auto sample_at = [&](int s2) {
     return ns == n ? s2 : (int)(((uint32_t)(2 * s2 + 1) * (uint32_t)n) >> 12);
   };
-  for (int s2 = tid; s2 < ns; s2 += kTopkThreads) {
-    const uint32_t key = ssrc(sample_at(s2));
-    if (key) atomicAdd(&S.hist[key >> 21], 1u);
+  // each thread's samples tid + j * kTopkThreads: all loads in flight before the first
+  // use, and kept in registers for the refinement below (no second read of the row)
+  static_assert(kSample % kTopkThreads == 0, "samples per thread");
+  constexpr int kSampPer = kSample / kTopkThreads;
+  uint32_t skey[kSampPer];
+#pragma unroll
+  for (int j = 0; j < kSampPer; ++j) {
+    const int s2 = tid + j * kTopkThreads;
+    skey[j] = s2 < ns ? ssrc(sample_at(s2)) : 0u;
   }
+#pragma unroll
+  for (int j = 0; j < kSampPer; ++j)
+    if (skey[j]) atomicAdd(&S.hist[skey[j] >> 21], 1u);
   __syncthreads();
   // sample keys wanted above the threshold: about (2k + 64) / n of the sample
   const int want = (int)(((uint32_t)(2 * k + 64) * (uint32_t)ns + n - 1) / (uint32_t)(n > 0 ? n : 1));
@@ -229,10 +239,9 @@ __device__ int select_topk(const RowSrc<kSrcSmem>& src, const SampleSrc& ssrc, i
       __syncthreads();  // every thread has read hist[bin]
       clear_hist(S, 2048);
       __syncthreads();
-      for (int s2 = tid; s2 < ns; s2 += kTopkThreads) {
-        const uint32_t key = ssrc(sample_at(s2));
-        if (key && (key >> 21) == bin) atomicAdd(&S.hist[(key >> 10) & 2047u], 1u);
-      }
+#pragma unroll
+      for (int j = 0; j < kSampPer; ++j)
+        if (skey[j] && (skey[j] >> 21) == bin) atomicAdd(&S.hist[(skey[j] >> 10) & 2047u], 1u);
       __syncthreads();
       find_crossing(S, S.hist, 2048, want - above);
       thr = max((bin << 21) | ((uint32_t)S.found_bin << 10), 1u);
