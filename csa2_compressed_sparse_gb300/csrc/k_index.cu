@@ -517,13 +517,9 @@ __global__ void __launch_bounds__(num_threads(kMode), 1)
     }
     prefetch_tensormap(&qmap);
   }
-  griddep_wait();
-  // this CTA's tile range and first group, from the prep kernel
-  const CtaRec cr = a.cta[blockIdx.x];
-  const int64_t it_lo = cr.it_lo, it_hi = cr.it_hi;
-  const int g_first = cr.g_first;
-  if (it_lo >= it_hi) return;
-
+  // the barriers and the accumulators (shared memory and TMEM only) are set up while the
+  // preceding kernel drains: the allocation never waits on another kernel, as no other
+  // kernel that holds TMEM fits beside this one in shared memory
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(smem_u32(&bars->full[s]), fill ? 32 * kGatherWarps : 1);  // gathers: their threads
@@ -550,6 +546,15 @@ __global__ void __launch_bounds__(num_threads(kMode), 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  griddep_wait();
+  // this CTA's tile range and first group, from the prep kernel
+  const CtaRec cr = a.cta[blockIdx.x];
+  const int64_t it_lo = cr.it_lo, it_hi = cr.it_hi;
+  const int g_first = cr.g_first;
+  if (it_lo >= it_hi) {
+    if (warp == 1) tmem_dealloc(tmem, 512);
+    return;
+  }
 
   const float alpha = rsqrtf((float)kDIdx) * rsqrtf((float)a.H);
 
