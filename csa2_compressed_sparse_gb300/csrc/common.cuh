@@ -137,6 +137,8 @@ struct AttnArgs {
                           //    low nibble first, then 32 E4M3 scales, one per 16 dims)
   int stream_rows;        // 1: the call reads fewer rows than the plane holds, so a row is
                           //    read about once: gathered bf16 rows are evicted from L2 first
+  int persist;            // > 0 (one CTA per query, more queries than SMs): that many CTAs,
+                          //    each carrying on from query to query
 };
 
 cudaError_t launch_compress(const CompressArgs& a, cudaStream_t s);

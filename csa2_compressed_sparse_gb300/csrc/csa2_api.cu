@@ -149,6 +149,9 @@ csa2_status attn_common(const char* name, const csa2_bf16* q, int Q, const int32
   if (sms <= 0) return fail(CSA2_ECUDA, "%s: no CUDA device", name);
   (void)ws_bytes;  // the attention needs no workspace (see csa2_attn_workspace_size)
   const int nsplit = csa2::attn_num_splits(Q, nsel, sms);
+  // more queries than SMs: one CTA per SM walks its queries, overlapping a query's output
+  // and the next query's set-up with the gathers
+  a.persist = nsplit == 1 && Q > sms ? sms : 0;
   cudaError_t e = csa2::launch_attn(a, nsplit, stream);
   if (e != cudaSuccess) return cuda_fail(e, name);
   return CSA2_OK;

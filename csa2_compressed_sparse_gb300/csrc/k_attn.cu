@@ -449,7 +449,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int nslot = (nchunks_total - rank + nsplit - 1) / nsplit;
   int nwin = 0;  // window slots come first
   while (nwin < nslot && rank + nwin * nsplit < 2) ++nwin;
-  const int64_t rb = a.row_base[b];
+  const int64_t rb = a.row_base ? a.row_base[b] : 0;  // no row_base: no selected rows
   auto row_source = [&](int e) {
     const int slot = e >> 6, r = e & 63;
     const int32_t idx32 = chunk_row(a, q, b, p, rb, rank + slot * nsplit, r);
@@ -917,10 +917,411 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == kMmaWarp) tmem_dealloc(tmem, 512);
 }
 
+// ---- one CTA per SM carrying on from query to query (nsplit = 1, more queries than SMs) --
+// CTA i takes queries i, i + G, i + 2G, .. (G = gridDim.x) with the same roles and
+// per-chunk pipeline as above, but the barriers' phases run on a chunk count that goes on
+// across queries, so the two KV buffers keep cycling: a gather team resolves its next
+// query's row sources (into the other half of the row tables, by query parity) and starts
+// that query's gathers as soon as its buffer's last PV is done, while the softmax warps
+// finish the query.  The softmax warps then write the output themselves: O^T / l from
+// TMEM, bf16 pairs into the Q buffer laid out as the Q boxes (128-byte swizzle; every S of
+// the query has completed), eight tensor stores, and once those have read the buffer the
+// next query's Q is loaded into it.
+
+struct __align__(16) PAux {
+  float inv_l[64];   // 1 / running sum per head of the query being written
+  float fac[2][64];  // rescale factor per head, by chunk parity
+  float rope_c[32];  // inverse RoPE of the output at the query position
+  float rope_s[32];
+  int32_t rowidx[2][kMaxChunks][kChunk];  // source rows, by query parity
+  uint32_t rowmask[2][kMaxChunks][2];     // valid rows of each chunk, by query parity
+  uint64_t q_full;      // Q of the CTA's current query landed (one load per query)
+  uint64_t kv_full[2];
+  uint64_t s_full[2];
+  uint64_t p_full[2];
+  uint64_t pv_done[2];
+  uint64_t fin[4];
+  uint32_t tmem_slot;
+  int abort;
+};
+
+__global__ void __launch_bounds__(kThreads, 1)
+    sparse_attn_persist_kernel(AttnArgs a, const __grid_constant__ CUtensorMap qmap,
+                               const __grid_constant__ CUtensorMap wmap,
+                               const __grid_constant__ CUtensorMap omap) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  uint8_t* q_s = smem;
+  uint8_t* kv_s = smem + kQBytes;
+  uint8_t* p_s = kv_s + 2 * kBufBytes;
+  PAux& X = *reinterpret_cast<PAux*>(p_s + 2 * kPBytes);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int G = gridDim.x, q0 = blockIdx.x;
+  const int nq = q0 < a.Q ? (a.Q - q0 + G - 1) / G : 0;  // queries of this CTA
+  const int n = 2 + (a.nsel + kChunk - 1) / kChunk;      // chunks per query
+  const uint32_t qb = smem_u32(q_s), kv0 = smem_u32(kv_s), p0 = smem_u32(p_s);
+  griddep_launch_dependents();
+  if (tid == 0) {
+    prefetch_tensormap(&qmap);
+    prefetch_tensormap(&wmap);
+    prefetch_tensormap(&omap);
+    mbar_init(smem_u32(&X.q_full), 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(smem_u32(&X.kv_full[b]), 1);
+      mbar_init(smem_u32(&X.s_full[b]), 2);
+      mbar_init(smem_u32(&X.p_full[b]), kGroupThreads);
+      mbar_init(smem_u32(&X.pv_done[b]), 2);
+    }
+    for (int r = 0; r < 4; ++r) mbar_init(smem_u32(&X.fin[r]), 1);
+    X.abort = 0;
+    mbar_fence_init();
+    if (nq > 0) {  // the first query's Q (a call input: before the dependency wait)
+      const uint32_t qf = smem_u32(&X.q_full);
+      mbar_arrive_expect_tx(qf, kQBytes);
+      const uint64_t pol = policy_evict_first();
+#pragma unroll
+      for (int db = 0; db < 8; ++db)
+        tma_load_2d(qb + db * kDimBlock, &qmap, 64 * db, q0 * kHeads, qf, pol);
+    }
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(smem_u32(&X.tmem_slot), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = X.tmem_slot;
+  const float scale2 = a.scale * kLog2e;
+  const bool is_gather = warp >= kGatherWarp0 && warp < kMmaWarp;
+
+  if (is_gather) {
+    // ======== gather: team b owns KV buffer b and the chunks cg with cg % 2 == b ========
+    const int team = (warp - kGatherWarp0) / (kTeam / 32);
+    const int t = tid - kGatherWarp0 * 32 - kTeam * team;
+    const uint32_t full_bar = smem_u32(&X.kv_full[team]);
+    const uint32_t kvb = kv0 + team * kBufBytes;
+    auto team_sync = [&]() {
+      if (team == 0) asm volatile("bar.sync 2, 256;" ::: "memory");
+      else asm volatile("bar.sync 3, 256;" ::: "memory");
+    };
+    griddep_wait();  // the selection and the plane come from the preceding kernels
+    int last = -1;   // the team's last chunk (its kv_full phase ends every copy)
+    for (int j = 0; j < nq; ++j) {
+      const int q = q0 + j * G, par = j & 1, cg0 = j * n;
+      const int c_first = (team - cg0) & 1;  // the team's chunks of this query: c_first + 2 k
+      const int mine = c_first < n ? (n - c_first + 1) / 2 : 0;
+      const int b = a.q_seq[q];
+      const int64_t p = a.q_pos[q];
+      const int64_t rb = a.row_base ? a.row_base[b] : 0;
+      // row sources of the team's chunks, one entry per thread and step (whole warps)
+      for (int e = t; e < mine * kChunk; e += kTeam) {
+        const int c = c_first + 2 * (e >> 6), r = e & 63;
+        const int32_t idx32 = chunk_row(a, q, b, p, rb, c, r);
+        X.rowidx[par][c][r] = idx32;
+        const uint32_t vm = __ballot_sync(0xFFFFFFFFu, idx32 >= 0);
+        if (lane == 0) X.rowmask[par][c][r >> 5] = vm;
+      }
+      team_sync();
+      for (int k = 0; k < mine; ++k) {
+        const int c = c_first + 2 * k, cg = cg0 + c;
+        last = cg;
+        // the buffer's previous chunk (cg - 2) has been multiplied into O^T
+        if (cg >= 2 && !X.abort &&
+            !mbar_wait(smem_u32(&X.pv_done[team]), (uint32_t)((cg - 2) >> 1) & 1))
+          X.abort = 1;
+        const int32_t* rows = X.rowidx[par][c];
+        // a full window chunk of a LINEAR bf16 window: 64 consecutive rows, one TMA box of
+        // 64 x 64 per dim block (arriving on the barrier by itself)
+        if (c < 2 && a.swa_mode == 1 && a.swa_dtype == 0 &&
+            (X.rowmask[par][c][0] & X.rowmask[par][c][1]) == 0xFFFFFFFFu) {
+          if (t == 0) {
+            mbar_arrive_expect_tx(full_bar, kBufBytes);
+            const uint64_t pol = policy_evict_first();
+#pragma unroll
+            for (int db = 0; db < 8; ++db)
+              tma_load_2d(kvb + db * kDimBlock, &wmap, 64 * db, rows[0], full_bar, pol);
+          }
+          continue;
+        }
+        const int fp8 = c < 2 ? a.swa_dtype : 0;
+        const uint8_t* base = c < 2 ? a.swa : reinterpret_cast<const uint8_t*>(a.plane);
+        gather_chunk(rows, fp8, c >= 2 && a.plane_dtype == 1, base, kvb, t, a.stream_rows != 0);
+        cp_async_commit();
+        cp_async_wait_group<0>();
+        fence_proxy_async_smem();
+        team_sync();  // every thread of the team has landed its rows
+        if (t == 0) mbar_arrive(full_bar);
+      }
+    }
+    // no copy may still be landing in shared memory when the CTA exits
+    if (t == 0 && last >= 0) mbar_wait(full_bar, (uint32_t)(last >> 1) & 1, 100000000ull);
+  } else if (warp >= kMmaWarp) {
+    // ====== MMA issuers (lane 0), as above: warps 20 and 21 S, warps 22 and 23 PV ======
+    const int role = warp - kMmaWarp;
+    if (lane == 0) {
+      int issued = 0;
+      if (role < 2) {
+        const uint32_t id_s = idesc_bf16(64, 64, 0, 0);
+        for (int j = 0; j < nq && !X.abort; ++j) {
+          if (!mbar_wait(smem_u32(&X.q_full), (uint32_t)j & 1)) {
+            X.abort = 1;
+            break;
+          }
+          for (int c = 0; c < n; ++c) {
+            const int cg = j * n + c;
+            // kv_full of chunk cg also means that the softmax of chunk cg - 2 is done with
+            // S buffer cg & 1
+            if (!mbar_wait(smem_u32(&X.kv_full[cg & 1]), (uint32_t)(cg >> 1) & 1)) {
+              X.abort = 1;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t kvb = kv0 + (cg & 1) * kBufBytes;
+            const uint32_t d = tmem + (role ? kColSb : kColSa) + 64 * (cg & 1);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const int db = 4 * role + i;
+#pragma unroll
+              for (int kk = 0; kk < 4; ++kk)
+                umma_bf16(d, sdesc_sw128(qb + db * kDimBlock + kk * 32, 16, 1024),
+                          sdesc_sw128(kvb + db * kDimBlock + kk * 32, 16, 1024), id_s,
+                          (i | kk) != 0);
+            }
+            umma_commit(smem_u32(&X.s_full[cg & 1]));
+            ++issued;
+          }
+        }
+      } else {
+        const uint32_t id_o = idesc_bf16(128, 64, 1, 0);
+        for (int cg = 0; cg < nq * n && !X.abort; ++cg) {
+          const int c = cg % n;  // a query's first chunk starts O^T afresh
+          if (!mbar_wait(smem_u32(&X.p_full[cg & 1]), (uint32_t)(cg >> 1) & 1)) {
+            X.abort = 1;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t kvb = kv0 + (cg & 1) * kBufBytes;
+          const uint32_t pb = p0 + (cg & 1) * kPBytes;
+#pragma unroll
+          for (int mt = 2 * (role - 2); mt < 2 * (role - 2) + 2; ++mt)
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              umma_bf16(tmem + kColO + 64 * mt,
+                        sdesc_sw128(kvb + 2 * mt * kDimBlock + kk * 2048, kDimBlock, 1024),
+                        sdesc_sw128(pb + kk * 32, 16, 1024), id_o, (c > 0 || kk > 0) ? 1 : 0);
+          umma_commit(smem_u32(&X.pv_done[cg & 1]));
+          ++issued;
+        }
+      }
+      // no MMA may still be running when the TMEM is released, whatever happened above
+      if (issued > 0) {
+        umma_commit(smem_u32(&X.fin[role]));
+        mbar_wait(smem_u32(&X.fin[role]), 0, 100000000ull);
+      }
+    }
+  } else {
+    // ============ softmax + O^T rescale + output (warps 0..3) ============
+    const int r4 = lane & 3;
+    const int hA = 16 * warp + (lane >> 2), hB = hA + 8;
+    const uint32_t lrow = (uint32_t)(warp * 32) << 16;
+    const float skA = a.sink ? a.sink[hA] * kLog2e : -INFINITY;
+    const float skB = a.sink ? a.sink[hB] * kLog2e : -INFINITY;
+    auto group_sync = [] { asm volatile("bar.sync 1, 128;" ::: "memory"); };
+    for (int j = 0; j < nq; ++j) {
+      const int q = q0 + j * G, par = j & 1;
+      // the running max starts at the sink logit and the sum at the sink's mass
+      float mA = skA, mB = skB, lA = 0.f, lB = 0.f;
+      if (a.sink && r4 == 0) { lA = 1.f; lB = 1.f; }
+      for (int c = 0; c < n; ++c) {
+        const int cg = j * n + c;
+        const int bsel = cg & 1;
+        const uint32_t ph = (uint32_t)(cg >> 1) & 1;
+        const uint32_t sa = tmem + lrow + kColSa + 64 * bsel;
+        const uint32_t sb = tmem + lrow + kColSb + 64 * bsel;
+        if (!X.abort && !mbar_wait(smem_u32(&X.s_full[bsel]), ph)) X.abort = 1;
+        tc_fence_after();
+        const uint32_t mlo = X.rowmask[par][c][0], mhi = X.rowmask[par][c][1];
+        const bool full = (mlo & mhi) == 0xFFFFFFFFu;
+        // the P buffer was last read by the PV of chunk cg - 2
+        if (cg >= 2 && !X.abort &&
+            !mbar_wait(smem_u32(&X.pv_done[bsel]), (uint32_t)((cg - 2) >> 1) & 1))
+          X.abort = 1;
+        const uint32_t pA = p0 + bsel * kPBytes + hA * 128 + 4 * r4;
+        const uint32_t pB = p0 + bsel * kPBytes + hB * 128 + 4 * r4;
+        const int sw = hA & 7;
+        float mxA, mxB, lsA, lsB, facA = 1.f, facB = 1.f;
+        bool need;
+        if (mA == -INFINITY) {
+          // no running max yet (first chunk, no sink): the chunk's largest score first
+          float smA = -INFINITY, smB = -INFINITY;
+#pragma unroll 1
+          for (int g = 0; g < 8; ++g) {
+            uint32_t x[4], y[4];
+            tmem_ld_16x256b(sa + 8 * g, x);
+            tmem_ld_16x256b(sb + 8 * g, y);
+            tmem_ld_wait();
+            const uint32_t mk = col_mask(full, mlo, mhi, g, r4);
+            if (mk & 1u) {
+              smA = fmaxf(smA, (__uint_as_float(x[0]) + __uint_as_float(y[0])) * scale2);
+              smB = fmaxf(smB, (__uint_as_float(x[2]) + __uint_as_float(y[2])) * scale2);
+            }
+            if (mk & 2u) {
+              smA = fmaxf(smA, (__uint_as_float(x[1]) + __uint_as_float(y[1])) * scale2);
+              smB = fmaxf(smB, (__uint_as_float(x[3]) + __uint_as_float(y[3])) * scale2);
+            }
+          }
+          smA = fmaxf(smA, __shfl_xor_sync(0xFFFFFFFFu, smA, 1));
+          smA = fmaxf(smA, __shfl_xor_sync(0xFFFFFFFFu, smA, 2));
+          smB = fmaxf(smB, __shfl_xor_sync(0xFFFFFFFFu, smB, 1));
+          smB = fmaxf(smB, __shfl_xor_sync(0xFFFFFFFFu, smB, 2));
+          mA = smA;
+          mB = smB;
+          facA = 0.f;
+          facB = 0.f;
+          need = true;
+          p_pass(sa, sb, full, mlo, mhi, r4, scale2, mA, mB, pA, pB, sw, mxA, mxB, lsA, lsB);
+        } else {
+          p_pass(sa, sb, full, mlo, mhi, r4, scale2, mA, mB, pA, pB, sw, mxA, mxB, lsA, lsB);
+          mxA = fmaxf(mxA, __shfl_xor_sync(0xFFFFFFFFu, mxA, 1));
+          mxA = fmaxf(mxA, __shfl_xor_sync(0xFFFFFFFFu, mxA, 2));
+          mxB = fmaxf(mxB, __shfl_xor_sync(0xFFFFFFFFu, mxB, 1));
+          mxB = fmaxf(mxB, __shfl_xor_sync(0xFFFFFFFFu, mxB, 2));
+          const bool nA = !(mxA <= kLazy), nB = !(mxB <= kLazy);
+          need = nA || nB;
+          if (__any_sync(0xFFFFFFFFu, need)) {
+            if (nA) { facA = ex2(-mxA); mA += mxA; }
+            if (nB) { facB = ex2(-mxB); mB += mxB; }
+            p_pass(sa, sb, full, mlo, mhi, r4, scale2, mA, mB, pA, pB, sw, mxA, mxB, lsA, lsB);
+          }
+        }
+        lA = lA * facA + lsA;
+        lB = lB * facB + lsB;
+        if (r4 == 0) {
+          X.fac[bsel][hA] = facA;
+          X.fac[bsel][hB] = facB;
+        }
+        if (group_any(need) && c > 0) {
+          // scale column h of every O tile by fac[h] once the previous chunk's PV is done
+          if (!X.abort && !mbar_wait(smem_u32(&X.pv_done[(cg - 1) & 1]),
+                                     (uint32_t)((cg - 1) >> 1) & 1))
+            X.abort = 1;
+          tc_fence_after();
+#pragma unroll 1
+          for (int mt = 0; mt < 4; ++mt) {
+#pragma unroll 1
+            for (int hb = 0; hb < 64; hb += 32) {
+              uint32_t v[32];
+              const uint32_t ta = tmem + lrow + kColO + 64 * mt + hb;
+              tmem_ld32(ta, v);
+              tmem_ld_wait();
+#pragma unroll
+              for (int jj = 0; jj < 32; ++jj)
+                v[jj] = __float_as_uint(__uint_as_float(v[jj]) * X.fac[bsel][hb + jj]);
+              tmem_st32(ta, v);
+            }
+          }
+          tmem_st_wait();
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        mbar_arrive(smem_u32(&X.p_full[bsel]));
+      }
+      // ---- the query's output: O^T / l, after its last PV ----
+      lA += __shfl_xor_sync(0xFFFFFFFFu, lA, 1);
+      lA += __shfl_xor_sync(0xFFFFFFFFu, lA, 2);
+      lB += __shfl_xor_sync(0xFFFFFFFFu, lB, 1);
+      lB += __shfl_xor_sync(0xFFFFFFFFu, lB, 2);
+      const int cl = j * n + n - 1;
+      if (!X.abort && !mbar_wait(smem_u32(&X.pv_done[cl & 1]), (uint32_t)(cl >> 1) & 1))
+        X.abort = 1;
+      tc_fence_after();
+      if (r4 == 0) {
+        X.inv_l[hA] = 1.f / lA;
+        X.inv_l[hB] = 1.f / lB;
+        if (a.lse) {
+          a.lse[(int64_t)q * kHeads + hA] = (mA + __log2f(lA)) * 0.6931471805599453f;
+          a.lse[(int64_t)q * kHeads + hB] = (mB + __log2f(lB)) * 0.6931471805599453f;
+        }
+      }
+      if (a.inv_freq && warp == 0) rope_table(a.inv_freq, a.q_pos[q], lane, X.rope_c, X.rope_s);
+      group_sync();  // inv_l and the RoPE table are written
+      // warp w holds dims mt * 128 + 32 w + lane of tile mt (TMEM lanes 32 w ..); bf16
+      // pairs of neighbouring dims after one shuffle per pair of heads, into box d / 64
+      // of the Q buffer ([64 heads][64 dims], 128-byte swizzle)
+#pragma unroll 1
+      for (int mt = 0; mt < 4; ++mt) {
+        const int d = mt * 128 + warp * 32 + lane;
+        const bool rot = a.inv_freq && d >= kRopeDim0;  // uniform in a warp
+        const float cs = rot ? X.rope_c[(d - kRopeDim0) >> 1] : 1.f;
+        const float sn = rot ? X.rope_s[(d - kRopeDim0) >> 1] : 0.f;
+        const int dd = d & 63, de = dd & ~1;
+        const uint32_t obox = qb + (uint32_t)(d >> 6) * kDimBlock;
+#pragma unroll 1
+        for (int hb = 0; hb < 64; hb += 32) {
+          uint32_t v[32];
+          tmem_ld32(tmem + lrow + kColO + 64 * mt + hb, v);
+          tmem_ld_wait();
+#pragma unroll
+          for (int jj = 0; jj < 32; ++jj)
+            v[jj] = __float_as_uint(__uint_as_float(v[jj]) * X.inv_l[hb + jj]);
+          if (rot) {  // pair (2i, 2i + 1) times e^{-i p theta_i}: the partner is lane ^ 1
+#pragma unroll
+            for (int jj = 0; jj < 32; ++jj) {
+              const float x = __uint_as_float(v[jj]);
+              const float pt = __shfl_xor_sync(0xFFFFFFFFu, x, 1);
+              v[jj] = __float_as_uint((lane & 1) ? x * cs - pt * sn : x * cs + pt * sn);
+            }
+          }
+#pragma unroll
+          for (int jj = 0; jj < 32; jj += 2) {
+            const int h = hb + jj;
+            const float a0 = __uint_as_float(v[jj]), a1 = __uint_as_float(v[jj + 1]);
+            const float rcv = __shfl_xor_sync(0xFFFFFFFFu, (lane & 1) ? a0 : a1, 1);
+            // the even lane writes head h at dims (d, d + 1), the odd one head h + 1 at
+            // (d - 1, d)
+            const int hr = (lane & 1) ? h + 1 : h;
+            const uint32_t w = (lane & 1) ? pack_bf16x2(rcv, a1) : pack_bf16x2(a0, rcv);
+            asm volatile("st.shared.b32 [%0], %1;" ::"r"(obox + (uint32_t)hr * 128u +
+                                                            ((uint32_t)((de >> 3) ^ (hr & 7)) << 4) +
+                                                            (uint32_t)(de & 7) * 2u),
+                         "r"(w)
+                         : "memory");
+          }
+        }
+      }
+      fence_proxy_async_smem();  // the staged boxes are read by the tensor stores
+      tc_fence_before();
+      group_sync();
+      if (tid == 0 && !X.abort) {
+        for (int db = 0; db < 8; ++db) tma_store_2d(&omap, 64 * db, q * kHeads, qb + db * kDimBlock);
+        bulk_commit_group();
+        bulk_wait_group_read0();  // the Q buffer is free again
+        if (j + 1 < nq) {
+          const uint32_t qf = smem_u32(&X.q_full);
+          mbar_arrive_expect_tx(qf, kQBytes);
+          const uint64_t pol = policy_evict_first();
+#pragma unroll
+          for (int db = 0; db < 8; ++db)
+            tma_load_2d(qb + db * kDimBlock, &qmap, 64 * db, (q + G) * kHeads, qf, pol);
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == kMmaWarp) tmem_dealloc(tmem, 512);
+}
+
 }  // namespace
 
 size_t attn_smem_bytes() {
   return 1024 + kQBytes + 2 * kBufBytes + 2 * kPBytes + sizeof(Aux);
+}
+size_t attn_persist_smem_bytes() {
+  return 1024 + kQBytes + 2 * kBufBytes + 2 * kPBytes + sizeof(PAux);
 }
 
 // CTAs per query: two (a cluster that merges in distributed shared memory) when both fit
@@ -946,6 +1347,14 @@ cudaError_t launch_attn(const AttnArgs& a, int nsplit, cudaStream_t s) {
   if (a.swa_mode == 1 && a.swa_dtype == 0 && a.swa_rows > 0 &&
       !encode_rows_bf16(&wm, a.swa, (uint64_t)a.swa_rows, kDLat, 64, 64))
     return cudaErrorInvalidValue;
+  if (a.persist > 0) {  // one CTA per SM, each carrying on from query to query
+    const size_t psmem = attn_persist_smem_bytes();
+    cudaError_t e = cudaFuncSetAttribute(sparse_attn_persist_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)psmem);
+    if (e != cudaSuccess) return e;
+    return launch_pdl(sparse_attn_persist_kernel, dim3((unsigned)a.persist), dim3(kThreads), psmem,
+                      s, a, qm, wm, om);
+  }
   const size_t smem = attn_smem_bytes();
   cudaError_t e = cudaFuncSetAttribute(sparse_attn_kernel,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);

@@ -312,10 +312,18 @@ def test_fused_compress_index_topk_equals_the_separate_calls(make):
             torch.equal(torch.nan_to_num(x.float(), nan=7.0), torch.nan_to_num(y.float(), nan=7.0))
 
 
+def many_queries(q):
+    """Repeats of q queries that exceed the SM count: one CTA per SM then carries on from
+    query to query (the persistent layout)."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    return -(-(sms + 1) // q) + 1
+
+
 def test_attention_split_and_unsplit_agree_with_the_oracle():
-    """The same queries through two CTAs per query (a cluster: nine queries) and through
-    one CTA per query (the nine repeated nine times fill the GPU); the workspace
-    argument is accepted and unused."""
+    """The same queries through two CTAs per query (a cluster: nine queries), through one
+    CTA per query (the nine repeated nine times fill the GPU) and through one CTA per SM
+    carrying on from query to query (more repeats than SMs); the workspace argument is
+    accepted and unused."""
     from csa2_compressed_sparse_gb300 import (csa2_attn_workspace_size, csa2_device_status,
                                               csa2_sparse_attn)
     from csa2_compressed_sparse_gb300.step import swa_of
@@ -325,7 +333,7 @@ def test_attention_split_and_unsplit_agree_with_the_oracle():
     assert csa2_attn_workspace_size(wl.Q, spec.k) == 0
     refs = [oracle_attn(wl, key, q, buf.sel[q].cpu().numpy()) for q in range(wl.Q)]
     ws = torch.empty(256, dtype=torch.uint8, device="cuda")
-    for rep, w in ((1, None), (1, ws), (9, None)):
+    for rep, w in ((1, None), (1, ws), (9, None), (many_queries(wl.Q), None)):
         idx = torch.arange(wl.Q, device="cuda").repeat(rep)
         out = torch.empty((len(idx), 64, 512), dtype=torch.bfloat16, device="cuda")
         lse = torch.empty((len(idx), 64), dtype=torch.float32, device="cuda")
@@ -340,18 +348,19 @@ def test_attention_split_and_unsplit_agree_with_the_oracle():
             assert np.abs(lse[i].cpu().numpy() - ref_lse).max() < 1e-2
 
 
-@pytest.mark.parametrize("rep", [1, 9])
+@pytest.mark.parametrize("rep", [1, 9, 0])
 def test_attention_with_the_inverse_rope_epilogue(rep):
     """csa2_sparse_attn_rope: the output's dims 448..511 rotated back by the query position
-    ([A] "出来之后"), through the two-CTA cluster merge (nine queries) and through one CTA
-    per query (the nine repeated nine times).  The other dims are the plain call's."""
+    ([A] "出来之后"), through the two-CTA cluster merge (nine queries), through one CTA
+    per query (the nine repeated nine times) and through one CTA per SM carrying on from
+    query to query (rep 0: more repeats than SMs).  The other dims are the plain call's."""
     from csa2_compressed_sparse_gb300 import (csa2_device_status, csa2_sparse_attn,
                                               csa2_sparse_attn_rope)
     from csa2_compressed_sparse_gb300.step import swa_of
     wl = W.decode_batch(B=9, lo=300, hi=700000, seed=31)
     t, spec, buf = run_workload(wl)
     key = register(wl)
-    idx = torch.arange(wl.Q, device="cuda").repeat(rep)
+    idx = torch.arange(wl.Q, device="cuda").repeat(rep or many_queries(wl.Q))
     args = (t["q"][0][idx].contiguous(), t["q_seq"][idx].contiguous(),
             t["q_pos"][idx].contiguous(), swa_of(spec, t, 0), t["plane"], t["row_base"],
             buf.sel[idx].contiguous(), t["sink"])
@@ -400,16 +409,21 @@ def test_attention_running_max_rescale_paths():
     hs[:32] = 256.0
     qs = (t["q"][0].double() * torch.tensor(hs, device="cuda").view(1, 64, 1)).to(torch.bfloat16)
     nb = csa2_attn_workspace_size(wl.Q, spec.k)
-    for ws in (None, torch.empty(nb, dtype=torch.uint8, device="cuda")):
-        out = torch.empty_like(buf.out[0])
-        lse = torch.empty((wl.Q, 64), dtype=torch.float32, device="cuda")
-        csa2_sparse_attn(qs, t["q_seq"], t["q_pos"], swa_of(spec, t, 0), t["plane"],
-                         t["row_base"], buf.sel, t["sink"], out, lse=lse, ws=ws)
+    refs = [oracle_attn(wl, key, q, buf.sel[q].cpu().numpy(), head_scale=hs) for q in range(wl.Q)]
+    # two CTAs per query, and (more repeats than SMs) one CTA per SM walking its queries
+    for rep, ws in ((1, None), (1, torch.empty(nb, dtype=torch.uint8, device="cuda")),
+                    (many_queries(wl.Q), None)):
+        idx = torch.arange(wl.Q, device="cuda").repeat(rep)
+        out = torch.empty((len(idx), 64, 512), dtype=torch.bfloat16, device="cuda")
+        lse = torch.empty((len(idx), 64), dtype=torch.float32, device="cuda")
+        csa2_sparse_attn(qs[idx].contiguous(), t["q_seq"][idx].contiguous(),
+                         t["q_pos"][idx].contiguous(), swa_of(spec, t, 0), t["plane"],
+                         t["row_base"], buf.sel[idx].contiguous(), t["sink"], out, lse=lse, ws=ws)
         csa2_device_status()
-        for q in range(wl.Q):
-            ref, ref_lse = oracle_attn(wl, key, q, buf.sel[q].cpu().numpy(), head_scale=hs)
-            check_attn(out[q].float().cpu().numpy(), ref)
-            assert np.abs(lse[q].cpu().numpy() - ref_lse).max() < 2e-2
+        for i in range(len(idx)):
+            ref, ref_lse = refs[i % wl.Q]
+            check_attn(out[i].float().cpu().numpy(), ref)
+            assert np.abs(lse[i].cpu().numpy() - ref_lse).max() < 2e-2
 
 
 def test_bounds_fault_is_reported_and_recoverable():
