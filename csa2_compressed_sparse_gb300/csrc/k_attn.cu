@@ -923,10 +923,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 // across queries, so the two KV buffers keep cycling: a gather team resolves its next
 // query's row sources (into the other half of the row tables, by query parity) and starts
 // that query's gathers as soon as its buffer's last PV is done, while the softmax warps
-// finish the query.  The softmax warps then write the output themselves: O^T / l from
-// TMEM, bf16 pairs into the Q buffer laid out as the Q boxes (128-byte swizzle; every S of
-// the query has completed), eight tensor stores, and once those have read the buffer the
-// next query's Q is loaded into it.
+// finish the query.  Once the query's last S has completed the next query's Q is loaded
+// into the Q buffer, so the next query's S products run while the softmax warps write this
+// query's output themselves: O^T / l from TMEM, bf16 pairs of neighbouring dims after one
+// shuffle per pair of heads, stored straight to global memory (64 contiguous bytes of two
+// heads per warp store).
 
 struct __align__(16) PAux {
   float inv_l[64];   // 1 / running sum per head of the query being written
@@ -947,8 +948,7 @@ struct __align__(16) PAux {
 
 __global__ void __launch_bounds__(kThreads, 1)
     sparse_attn_persist_kernel(AttnArgs a, const __grid_constant__ CUtensorMap qmap,
-                               const __grid_constant__ CUtensorMap wmap,
-                               const __grid_constant__ CUtensorMap omap) {
+                               const __grid_constant__ CUtensorMap wmap) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint8_t* q_s = smem;
@@ -965,7 +965,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (tid == 0) {
     prefetch_tensormap(&qmap);
     prefetch_tensormap(&wmap);
-    prefetch_tensormap(&omap);
     mbar_init(smem_u32(&X.q_full), 1);
     for (int b = 0; b < 2; ++b) {
       mbar_init(smem_u32(&X.kv_full[b]), 1);
@@ -1142,6 +1141,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t sb = tmem + lrow + kColSb + 64 * bsel;
         if (!X.abort && !mbar_wait(smem_u32(&X.s_full[bsel]), ph)) X.abort = 1;
         tc_fence_after();
+        if (c == n - 1 && tid == 0 && j + 1 < nq && !X.abort) {
+          // every S of this query has completed: the Q buffer takes the next query's Q
+          const uint32_t qf = smem_u32(&X.q_full);
+          mbar_arrive_expect_tx(qf, kQBytes);
+          const uint64_t pol = policy_evict_first();
+#pragma unroll
+          for (int db = 0; db < 8; ++db)
+            tma_load_2d(qb + db * kDimBlock, &qmap, 64 * db, (q + G) * kHeads, qf, pol);
+        }
+        __syncwarp();  // warp-wide TMEM loads follow
         const uint32_t mlo = X.rowmask[par][c][0], mhi = X.rowmask[par][c][1];
         const bool full = (mlo & mhi) == 0xFFFFFFFFu;
         // the P buffer was last read by the PV of chunk cg - 2
@@ -1248,16 +1257,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (a.inv_freq && warp == 0) rope_table(a.inv_freq, a.q_pos[q], lane, X.rope_c, X.rope_s);
       group_sync();  // inv_l and the RoPE table are written
       // warp w holds dims mt * 128 + 32 w + lane of tile mt (TMEM lanes 32 w ..); bf16
-      // pairs of neighbouring dims after one shuffle per pair of heads, into box d / 64
-      // of the Q buffer ([64 heads][64 dims], 128-byte swizzle)
+      // pairs of neighbouring dims after one shuffle per pair of heads, streamed out
+      uint16_t* out_q = a.out + (int64_t)q * kHeads * kDLat;
 #pragma unroll 1
       for (int mt = 0; mt < 4; ++mt) {
         const int d = mt * 128 + warp * 32 + lane;
         const bool rot = a.inv_freq && d >= kRopeDim0;  // uniform in a warp
         const float cs = rot ? X.rope_c[(d - kRopeDim0) >> 1] : 1.f;
         const float sn = rot ? X.rope_s[(d - kRopeDim0) >> 1] : 0.f;
-        const int dd = d & 63, de = dd & ~1;
-        const uint32_t obox = qb + (uint32_t)(d >> 6) * kDimBlock;
+        const int de = d & ~1;  // the pair's even dim
 #pragma unroll 1
         for (int hb = 0; hb < 64; hb += 32) {
           uint32_t v[32];
@@ -1283,30 +1291,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             // (d - 1, d)
             const int hr = (lane & 1) ? h + 1 : h;
             const uint32_t w = (lane & 1) ? pack_bf16x2(rcv, a1) : pack_bf16x2(a0, rcv);
-            asm volatile("st.shared.b32 [%0], %1;" ::"r"(obox + (uint32_t)hr * 128u +
-                                                            ((uint32_t)((de >> 3) ^ (hr & 7)) << 4) +
-                                                            (uint32_t)(de & 7) * 2u),
-                         "r"(w)
-                         : "memory");
+            __stcs(reinterpret_cast<unsigned int*>(out_q + hr * kDLat + de), w);
           }
         }
       }
-      fence_proxy_async_smem();  // the staged boxes are read by the tensor stores
-      tc_fence_before();
-      group_sync();
-      if (tid == 0 && !X.abort) {
-        for (int db = 0; db < 8; ++db) tma_store_2d(&omap, 64 * db, q * kHeads, qb + db * kDimBlock);
-        bulk_commit_group();
-        bulk_wait_group_read0();  // the Q buffer is free again
-        if (j + 1 < nq) {
-          const uint32_t qf = smem_u32(&X.q_full);
-          mbar_arrive_expect_tx(qf, kQBytes);
-          const uint64_t pol = policy_evict_first();
-#pragma unroll
-          for (int db = 0; db < 8; ++db)
-            tma_load_2d(qb + db * kDimBlock, &qmap, 64 * db, (q + G) * kHeads, qf, pol);
-        }
-      }
+      tc_fence_before();  // the TMEM reads precede the next query's first PV
     }
   }
   tc_fence_before();
@@ -1353,7 +1342,7 @@ cudaError_t launch_attn(const AttnArgs& a, int nsplit, cudaStream_t s) {
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)psmem);
     if (e != cudaSuccess) return e;
     return launch_pdl(sparse_attn_persist_kernel, dim3((unsigned)a.persist), dim3(kThreads), psmem,
-                      s, a, qm, wm, om);
+                      s, a, qm, wm);
   }
   const size_t smem = attn_smem_bytes();
   cudaError_t e = cudaFuncSetAttribute(sparse_attn_kernel,
