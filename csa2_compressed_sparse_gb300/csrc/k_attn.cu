@@ -34,7 +34,9 @@
 // Every CTA starts its running max at the sink logit.  With nsplit = 1 its running sum
 // starts at the sink's mass (1) and the CTA writes the output.  With nsplit = 2 the two
 // CTAs of a query run as a cluster and merge through distributed shared memory, each
-// finishing half of the dims; the merge adds the sink's e^{sink_h} once.
+// finishing half of the dims; the merge adds the sink's e^{sink_h} once.  With more
+// queries than SMs (a prefill chunk) a second kernel runs nsplit = 1 on one CTA per SM
+// that carries on from query to query (see sparse_attn_persist_kernel).
 //
 // Warps 0..3 softmax + O^T rescale + output, warps 4..19 gather (teams of eight
 // warps), warps 20..23 issue the MMAs (lane 0 each; warp 20 also owns the TMEM).

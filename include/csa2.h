@@ -392,8 +392,9 @@ csa2_status csa2_topk_scores(const float* scores, const int32_t* n, int Q, int64
  *   ws     optional workspace (256-byte aligned, NULL allowed) of
  *          csa2_attn_workspace_size(Q, nsel) bytes, which is 0: a query's entries run on
  *          one CTA, or on two that merge in distributed shared memory when 2 Q CTAs fit
- *          on the GPU at once.  The argument is kept so that callers that size and pass
- *          a workspace need no change. */
+ *          on the GPU at once; with more queries than SMs one CTA per SM walks its
+ *          queries in turn.  The argument is kept so that callers that size and pass a
+ *          workspace need no change. */
 typedef enum { CSA2_SWA_RING = 0, CSA2_SWA_LINEAR = 1 } csa2_swa_mode;
 typedef enum { CSA2_SWA_BF16 = 0, CSA2_SWA_FP8_S128 = 1, CSA2_SWA_FP8_E8M0 = 2 } csa2_swa_dtype;
 typedef struct {
