@@ -33,7 +33,8 @@ def _gpu():
 
 def test_cold_prefill_from_position_zero():
     """300 new tokens compressed from position 0 (ratio 2, LINEAR windows, two layers):
-    windows of 1 .. 128 rows, n_vis from 0 to 150, one CTA per query."""
+    windows of 1 .. 128 rows, n_vis from 0 to 150; more queries than SMs, so one CTA per
+    SM walks its queries (ragged windows and empty selections inside that layout)."""
     wl = W.Workload("cold_prefill", 41, 2, ctx=[300], chunk=[300], nq=[300], swa="linear",
                     layers=2, description="prefill of 300 tokens from position 0")
     t, spec, buf = run_workload(wl)
