@@ -170,9 +170,14 @@ cudaError_t launch_attn(const AttnArgs& a, int nsplit, cudaStream_t s);
 int topk_chunk_len(int64_t ld);
 int topk_num_chunks(int64_t ld);
 int64_t topk_max_len();
-// Can one call select the top-k of rows of ld positions?  (the chunk merge holds
-// chunks * k pairs)
+// Can one call select the top-k of rows of ld items?  (the chunk merge holds chunks * k
+// pairs)  topk_chunk_len / topk_num_chunks / topk_fits: the staged select of the
+// candidate pool's blocks; topk_row_*: the row selection, whose rows of up to 65536
+// positions run on one CTA.
 bool topk_fits(int64_t ld, int k);
+int topk_row_chunk_len(int64_t ld);
+int topk_row_num_chunks(int64_t ld);
+bool topk_row_fits(int64_t ld, int k);
 
 // Replace the calling thread's csa2_last_error() text.
 void set_last_error(const char* msg);

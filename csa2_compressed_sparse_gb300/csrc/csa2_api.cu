@@ -82,7 +82,7 @@ IndexWs index_ws_layout(int Q, int64_t ld, int k, int nbk = 0, int64_t qrows = 0
   w.cta = o; o = up256(o + (size_t)csa2::kMaxIndexCtas * sizeof(csa2::CtaRec));
   w.n_groups = o; o = up256(o + 8);
   w.count = o; o = up256(o + (size_t)Q * 4);
-  w.nchunk = csa2::topk_num_chunks(ld);
+  w.nchunk = csa2::topk_row_num_chunks(ld);
   w.part = o;
   if (w.nchunk > 1) o = up256(o + (size_t)Q * w.nchunk * k * 8);
   if (nbk > 0) {
@@ -102,7 +102,7 @@ IndexWs index_ws_layout(int Q, int64_t ld, int k, int nbk = 0, int64_t qrows = 0
 
 // csa2_topk_scores: per-row arrival counters, then the partial lists.
 size_t topk_ws_bytes(int Q, int64_t ld, int k) {
-  const int nchunk = csa2::topk_num_chunks(ld);
+  const int nchunk = csa2::topk_row_num_chunks(ld);
   return nchunk > 1 ? up256((size_t)Q * 4) + up256((size_t)Q * nchunk * k * 8) : 0;
 }
 
@@ -342,7 +342,7 @@ csa2_status index_topk_impl(const csa2_bf16* iq, const float* w, int Q, int H,
   t.cand = cand; t.ncb = a.ncb; t.sel = sel; t.sel_scores = sel_scores;
   t.part = reinterpret_cast<uint64_t*>(base + L.part); t.nchunk = L.nchunk;
   t.count = a.topk_count;
-  t.chunk = csa2::topk_chunk_len(max_scored);
+  t.chunk = csa2::topk_row_chunk_len(max_scored);
   t.q_pos = q_pos;
   t.ratio = ratio;
   // n_scored <= max_scored <= ldk: the chunking of max_scored covers every row
@@ -487,7 +487,7 @@ csa2_status csa2_index_plane_fp8(const csa2_bf16* index_k, int64_t rows, uint8_t
 }
 
 size_t csa2_topk_workspace_size(int Q, int64_t ld, int k) {
-  if (Q < 0 || ld < 1 || k < 1 || k > 2048 || !csa2::topk_fits(ld, k)) return 0;
+  if (Q < 0 || ld < 1 || k < 1 || k > 2048 || !csa2::topk_row_fits(ld, k)) return 0;
   return topk_ws_bytes(Q, ld, k);
 }
 
@@ -500,7 +500,7 @@ csa2_status csa2_topk_scores(const float* scores, const int32_t* n, int Q, int64
   REQUIRE(ld <= csa2::topk_max_len(),
           "csa2_topk_scores: ld %lld exceeds the supported %lld positions", (long long)ld,
           (long long)csa2::topk_max_len());
-  REQUIRE(csa2::topk_fits(ld, k),
+  REQUIRE(csa2::topk_row_fits(ld, k),
           "csa2_topk_scores: rows of %lld positions with k = %d exceed the chunk merge "
           "(chunks of 32768 positions x k must be <= 32768)", (long long)ld, k);
   if (Q == 0) return CSA2_OK;
@@ -515,8 +515,8 @@ csa2_status csa2_topk_scores(const float* scores, const int32_t* n, int Q, int64
   csa2::TopkArgs t{};
   t.keys = nullptr; t.scores = scores; t.n = n; t.Q = Q; t.ld = ld; t.k = k; t.cand = nullptr;
   t.ncb = 0; t.sel = sel; t.sel_scores = sel_scores;
-  t.nchunk = csa2::topk_num_chunks(ld);
-  t.chunk = csa2::topk_chunk_len(ld);
+  t.nchunk = csa2::topk_row_num_chunks(ld);
+  t.chunk = csa2::topk_row_chunk_len(ld);
   if (t.nchunk > 1) {
     t.count = static_cast<int32_t*>(ws);
     t.part = reinterpret_cast<uint64_t*>(static_cast<uint8_t*>(ws) + up256((size_t)Q * 4));

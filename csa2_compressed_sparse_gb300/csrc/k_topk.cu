@@ -46,7 +46,9 @@ constexpr int kChunkLen = 32768;   // positions per CTA
 constexpr int kMaxChunks = 48;     // chunks per row; the merge holds chunks * k <= kChunkLen pairs
 constexpr int kCandCap = 8192;     // kept (key, index) pairs
 constexpr int kWarpCap = kCandCap / (kTopkThreads / 32);  // per-warp region
-constexpr int kWords = kChunkLen / 32;
+constexpr int kLongLen = 65536;    // a row of up to this many positions: one CTA reading it
+                                   // straight from global memory (no staging, no merge)
+constexpr int kLongWords = kLongLen / 32;
 constexpr int kSample = 2048;      // keys sampled for the threshold
 
 namespace {
@@ -57,8 +59,8 @@ struct SelectSmem {
   uint32_t hist_kept[2048];  // top 11 key bits of the kept pairs (the first radix pass)
   uint32_t ckey[kCandCap];
   uint32_t cidx[kCandCap];
-  uint32_t selmap[kWords];  // positions with key > T
-  uint32_t eqmap[kWords];   // positions with key == T
+  uint32_t selmap[kLongWords];  // positions with key > T
+  uint32_t eqmap[kLongWords];   // positions with key == T
   int wcnt[kTopkThreads / 32];  // kept pairs per warp region
   int ncand;
   int nvalid;
@@ -183,21 +185,24 @@ struct SampleSrc {
   }
 };
 
-// Exact top-k of src[0..n) (n <= kChunkLen): emit(o, i) is called once for each selected
-// index i, with o = its place in ascending order (0 .. keff - 1), by some thread of the
-// CTA.  Returns keff = min(k, #scored).  dense: every key of src[0..n) is nonzero.
+// Exact top-k of src[0..n): emit(o, i) is called once for each selected index i, with
+// o = its place in ascending order (0 .. keff - 1), by some thread of the CTA.  Returns
+// keff = min(k, #scored).  dense: every key of src[0..n) is nonzero.  src is the staged
+// copy in shared memory (n <= kChunkLen) or the row in global memory (n <= kLongLen).
 // The threshold's sample is read from ssrc (the same keys: the staged copy, or the row
 // in global memory while its copy lands); ready() is called by every thread, followed by
 // a barrier, before src is first read (it waits for the staged copy).
-template <typename Ready, typename Emit>
-__device__ int select_topk(const RowSrc<kSrcSmem>& src, const SampleSrc& ssrc, int n, int k,
+template <int kSrc, typename Ready, typename Emit>
+__device__ int select_topk(const RowSrc<kSrc>& src, const SampleSrc& ssrc, int n, int k,
                            bool dense, SelectSmem& S, bool precleared, Ready ready, Emit emit) {
+  constexpr bool kStaged = kSrc == kSrcSmem;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int nw = (n + 31) >> 5;
   // ---- 1. clear (done by the caller, before its dependency wait, when precleared) ----
   // thread (warp w, lane l) handles the 4-key groups w * 32 + l + u * kTopkThreads,
-  // u < kU (n <= kChunkLen)
-  constexpr int kU = kChunkLen / (4 * kTopkThreads);
+  // u < kU (n <= kChunkLen staged, kLongLen from global memory)
+  constexpr int kU = (kStaged ? kChunkLen : kLongLen) / (4 * kTopkThreads);
+  static_assert(kU <= 32, "one bit per group step");
   if (!precleared) {
     clear_select(S, nw);
     __syncthreads();
@@ -205,8 +210,8 @@ __device__ int select_topk(const RowSrc<kSrcSmem>& src, const SampleSrc& ssrc, i
   // ---- 2. threshold from an even sample of 2048 keys ----
   const int ns = n < kSample ? n : kSample;
   // sample s2 reads key (2 s2 + 1) n / (2 ns): s2 itself when the segment is no longer
-  // than the sample, else a shift (2 ns = 4096; (2 s2 + 1) n < 2^32 for n <= kChunkLen)
-  static_assert(2 * kSample == 4096 && (uint64_t)(2 * kSample) * kChunkLen < (1ull << 32),
+  // than the sample, else a shift (2 ns = 4096; (2 s2 + 1) n < 2^32 for n <= kLongLen)
+  static_assert(2 * kSample == 4096 && (uint64_t)(2 * kSample) * kLongLen < (1ull << 32),
                 "sample index");
   auto sample_at = [&](int s2) {
     return ns == n ? s2 : (int)(((uint32_t)(2 * s2 + 1) * (uint32_t)n) >> 12);
@@ -249,9 +254,10 @@ __device__ int select_topk(const RowSrc<kSrcSmem>& src, const SampleSrc& ssrc, i
   }
   ready();  // the staged copy of the segment has landed
   // keys past n up to whole 4096-key steps of the filter read as unscored (0), so the
-  // filter's loads need no bounds (nu * 4096 <= kChunkLen: inside the staging buffer)
+  // filter's loads need no bounds (nu * 4096 <= kChunkLen: inside the staging buffer);
+  // loads from global memory are bounded at n instead
   const int nu = (n + 4 * kTopkThreads - 1) / (4 * kTopkThreads);  // <= kU, CTA-uniform
-  {
+  if constexpr (kStaged) {
     uint32_t* rb = const_cast<uint32_t*>(static_cast<const uint32_t*>(src.base));
     for (int i = n + tid; i < nu * 4 * kTopkThreads; i += kTopkThreads) rb[i] = 0u;
   }
@@ -268,13 +274,26 @@ __device__ int select_topk(const RowSrc<kSrcSmem>& src, const SampleSrc& ssrc, i
   uint32_t* widx = S.cidx + warp * kWarpCap;
   int mine = 0;
   uint32_t hit = 0;  // bit u: group u holds a kept key (thr >= 1: never an unscored one)
-  const uint32_t gaddr = smem_u32(src.base) + 16u * (uint32_t)(warp * 32 + lane);
   auto count = [&](const uint4& vv, int u) {
     const int cnt = (vv.x >= thr) + (vv.y >= thr) + (vv.z >= thr) + (vv.w >= thr);
     mine += cnt;
     hit |= (cnt ? 1u : 0u) << u;
   };
-  if (src.aligned) {  // plain 16-byte shared loads, four in flight
+  if constexpr (!kStaged) {  // from global memory: four 16-byte loads in flight, bounded
+#pragma unroll
+    for (int u0 = 0; u0 < kU; u0 += 4) {
+      if (u0 < nu) {
+        uint4 vv[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          vv[j] = u0 + j < nu ? src.load4(warp * 32 + (u0 + j) * kTopkThreads + lane, n)
+                              : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) count(vv[j], u0 + j);
+      }
+    }
+  } else if (src.aligned) {  // plain 16-byte shared loads, four in flight
+    const uint32_t gaddr = smem_u32(src.base) + 16u * (uint32_t)(warp * 32 + lane);
 #pragma unroll
     for (int u0 = 0; u0 < kU; u0 += 4) {
       if (u0 < nu) {
@@ -478,9 +497,9 @@ __device__ __forceinline__ void topk_row(const TopkArgs& a, int c) {
     mbar_init(smem_u32(&S.bar), 1);
     mbar_fence_init();
   }
-  // the select's state, for a segment of up to kChunkLen items (shared memory only, so
+  // the select's state, for a segment of up to kLongLen items (shared memory only, so
   // before the wait; a barrier below makes it visible)
-  clear_select(S, kWords);
+  clear_select(S, kLongWords);
   // positions of this row: from the query's position when the call gives it (a call
   // input, read before the dependency wait), else from the count array
   int n;
@@ -498,6 +517,35 @@ __device__ __forceinline__ void topk_row(const TopkArgs& a, int c) {
   const int begin = c * a.chunk;
   const int len = max(0, min(a.chunk, items - begin));
   const int tid = threadIdx.x;
+  int32_t* sel_q = a.sel + (int64_t)q * a.k;
+  float* sc_q = a.sel_scores ? a.sel_scores + (int64_t)q * a.k : nullptr;
+  if (!a.blocks && len > kChunkLen) {
+    // A whole row of up to kLongLen positions (one chunk) on one CTA, read straight from
+    // global memory: no staging copy (it would not fit) and no merge of two chunk lists.
+    const int64_t rowoff = (int64_t)q * a.ld;
+    const bool dense_g = a.cand == nullptr;
+    __syncthreads();  // the cleared select state is visible
+    int keff;
+    if constexpr (kKind == kSrcScores) {
+      const float* g = a.scores + rowoff;
+      const RowSrc<kSrcScores> gsrc{g, (reinterpret_cast<uintptr_t>(g) & 15u) == 0};
+      keff = select_topk(gsrc, SampleSrc{nullptr, nullptr, g}, len, a.k, dense_g, S, true,
+                         [] {}, [&](int o, int i) {
+                           sel_q[o] = pos_to_row(a, q, (uint32_t)i);
+                           if (sc_q) sc_q[o] = key_score(gsrc(i));
+                         });
+    } else {
+      const uint32_t* g = a.keys + rowoff;
+      const RowSrc<kSrcKeys> gsrc{g, (reinterpret_cast<uintptr_t>(g) & 15u) == 0};
+      keff = select_topk(gsrc, SampleSrc{nullptr, g, nullptr}, len, a.k, dense_g, S, true,
+                         [] {}, [&](int o, int i) {
+                           sel_q[o] = pos_to_row(a, q, (uint32_t)i);
+                           if (sc_q) sc_q[o] = key_score(gsrc(i));
+                         });
+    }
+    pad_row(a, q, keff);
+    return;
+  }
   uint32_t* rowbuf = S.row;
   int pad = 0, head = 0, body = 0;
   SampleSrc ssrc{nullptr, nullptr, nullptr};
@@ -575,8 +623,6 @@ __device__ __forceinline__ void topk_row(const TopkArgs& a, int c) {
   // every position below n is scored unless the row maps candidate blocks (REINDEX);
   // every block below the row's count has a key
   const bool dense = a.blocks || a.cand == nullptr;
-  int32_t* sel_q = a.sel + (int64_t)q * a.k;
-  float* sc_q = a.sel_scores ? a.sel_scores + (int64_t)q * a.k : nullptr;
   if (a.nchunk == 1) {
     // REINDEX: the row's candidate block ids (up to two per thread) are loaded now (after
     // the wait: a preceding call may have written them) and stored, once the threshold is
@@ -702,8 +748,8 @@ __global__ void __launch_bounds__(kTopkThreads, 1)
 
 }  // namespace
 
-// Positions per chunk CTA: the whole row up to 32768, else chunks of 32768 (rows up to
-// 48 x 32768 = 1,572,864 positions).
+// Items per chunk CTA of the staged select (the candidate pool's blocks): the whole row
+// up to 32768, else chunks of 32768 (rows up to 48 x 32768 = 1,572,864 items).
 int topk_chunk_len(int64_t ld) { return ld <= kChunkLen ? (int)ld : kChunkLen; }
 int topk_num_chunks(int64_t ld) {
   const int64_t c = topk_chunk_len(ld);
@@ -713,6 +759,17 @@ int64_t topk_max_len() { return (int64_t)kChunkLen * kMaxChunks; }
 bool topk_fits(int64_t ld, int k) {
   return ld >= 1 && ld <= topk_max_len() && k >= 1 &&
          (topk_num_chunks(ld) == 1 || (int64_t)topk_num_chunks(ld) * k <= kChunkLen);
+}
+// Positions per chunk CTA of a row selection: the whole row up to 65536 (one CTA reading
+// it from global memory), else chunks of 32768 merged by the last chunk CTA.
+int topk_row_chunk_len(int64_t ld) { return ld <= kLongLen ? (int)ld : kChunkLen; }
+int topk_row_num_chunks(int64_t ld) {
+  const int64_t c = topk_row_chunk_len(ld);
+  return (int)((ld + c - 1) / c);
+}
+bool topk_row_fits(int64_t ld, int k) {
+  return ld >= 1 && ld <= topk_max_len() && k >= 1 &&
+         (topk_row_num_chunks(ld) == 1 || (int64_t)topk_row_num_chunks(ld) * k <= kChunkLen);
 }
 
 cudaError_t launch_topk(const TopkArgs& a, cudaStream_t s, const TopkArgs* b,
