@@ -96,6 +96,23 @@ def test_workspace_sizes_are_monotone():
     assert csa2.csa2_topk_workspace_size(8, 1 << 20, 512) >= 8 * 32 * 512 * 8
 
 
+def test_row_selection_chunking():
+    """Rows of up to 65536 positions are selected by one CTA each (no merge scratch); longer
+    rows are cut into chunks of 32768 whose k-best lists the last chunk CTA merges."""
+    assert csa2.csa2_topk_workspace_size(8, 40000, 512) == 0
+    assert csa2.csa2_topk_workspace_size(8, 65536, 2048) == 0
+    nb = csa2.csa2_topk_workspace_size(8, 65537, 512)
+    assert nb >= 8 * 3 * 512 * 8  # three chunks of partial (key, position) lists
+    # the merge holds chunks x k <= 32768 pairs, and rows hold at most 48 chunks
+    assert csa2.csa2_topk_workspace_size(8, 48 * 32768, 682) > 0  # 32736 pairs
+    assert csa2.csa2_topk_workspace_size(8, 48 * 32768, 683) == 0  # 32784 pairs
+    assert csa2.csa2_topk_workspace_size(8, 48 * 32768 + 1, 1) == 0
+    # the indexer's workspace holds the keys; a one-CTA row adds no partial lists
+    a = csa2.csa2_index_topk_workspace_size(64, 64, 65536, 512)
+    b = csa2.csa2_index_topk_workspace_size(64, 64, 65537, 512)
+    assert b - a >= 64 * 3 * 512 * 8
+
+
 def test_attn_rejects_bad_arguments():
     L = _raw()
     p = ctypes.c_void_p(256)
