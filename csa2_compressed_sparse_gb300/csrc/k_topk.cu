@@ -21,6 +21,9 @@
 // If the sample misleads (fewer than k kept, or more than the buffer holds), steps 3
 // and 4 run over the whole segment instead; the result is the same.
 //
+// A row of 32769..65536 positions (a prefill chunk's rows) runs on one CTA as well, with
+// the same steps reading the row straight from global memory (the segment would not fit
+// in shared memory; the filter keeps four 16-byte loads in flight per thread).
 // Longer rows are split into chunks of 32768: every chunk CTA writes its exact top-k
 // (key, position) list, and the chunk CTA that finishes last (a per-row arrival
 // counter) selects the top-k of the concatenated lists.  The true top-k is a subset of

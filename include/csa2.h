@@ -345,9 +345,10 @@ csa2_status csa2_index_topk_noalloc(const csa2_bf16* iq, const float* w, int Q, 
  * For row q of scores [Q][ld] fp32, the k_eff = min(k, n[q]) highest of
  * scores[q][0..n[q]) (ties: lower index; NaN ranks as -inf; -0 equals +0) are
  * written as ascending indices to sel[q][0..k_eff), -1 after.  sel_scores optional.
- *   n  [Q] int32, 0 <= n[q] <= ld;  k 1..2048, where rows longer than 32768 are
- *      cut into ceil(ld / 32768) chunks whose top-k lists are merged: chunks * k must
- *      be <= 32768 (csa2_topk_workspace_size returns 0 otherwise)
+ *   n  [Q] int32, 0 <= n[q] <= ld;  k 1..2048.  A row of up to 65536 positions is
+ *      selected by one CTA (no workspace); longer rows are cut into ceil(ld / 32768)
+ *      chunks whose top-k lists are merged: chunks * k must be <= 32768
+ *      (csa2_topk_workspace_size returns 0 otherwise)
  *   ws workspace of csa2_topk_workspace_size(Q, ld, k) bytes, 256-byte aligned. */
 size_t csa2_topk_workspace_size(int Q, int64_t ld, int k);
 csa2_status csa2_topk_scores(const float* scores, const int32_t* n, int Q, int64_t ld, int k,
